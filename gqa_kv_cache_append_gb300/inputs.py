@@ -1,0 +1,220 @@
+"""Seeded synthetic decode-step inputs shaped like the pages' workloads.
+
+This module only draws and lays out data; it holds none of the decode
+arithmetic (no logits, softmax or weighted sums).  The tests feed the same
+tensors to the CUDA path and to the float64 oracle, and the bench times the
+CUDA path on them.
+
+Recipe (per layer l of a workload with seed s):
+  * a torch.Generator on the target device, seeded with s * 1000 + l, draws
+    in this order: the K cache, the V cache, q, k_new, v_new, each N(0, 1)
+    in float32 and then rounded to the storage dtype (bf16 round-to-nearest-
+    even, or kept as fp32);
+  * 'meanpool' workloads first draw an h-head (MHA) K/V cache, k_new and
+    v_new, then average every contiguous block of h/g heads in float32 before
+    the rounding (the MHA -> GQA conversion by group mean, from the GQA
+    lesson "クエリヘッドはそのまま、キー・バリューヘッドだけ減らす", section
+    on merging groups); g = h leaves the MHA data untouched;
+  * 'boost' workloads pick round(0.01 * L_i) positions per sequence without
+    replacement (torch.randperm on a CPU generator seeded s * 1000 + l + 7)
+    and add (boost / scale) * u to their K rows before rounding, where u is
+    the least-norm solution of Q_i u = 1 for the sequence's bf16-rounded
+    query block Q_i [h, d]; every head's logit at those rows then rises by
+    about ``boost`` (exactly, before the bf16 rounding of K);
+  * ragged workloads take lengths numpy.random.default_rng(s).integers(lo,
+    hi, size=b, endpoint=True); the others use L_i = cap for every sequence.
+Rows at or beyond L_i are padding; ``pad_fill`` can fill them with NaN (or a
+large value) to check that nothing reads them into the result.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+__all__ = ["DecodeConfig", "WORKLOADS", "workload", "seq_lens_for",
+           "make_layer", "layer_bytes", "layer_flops"]
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    layers: int
+    b: int
+    h: int
+    g: int
+    d: int
+    cap: int
+    dtype: str                 # 'bf16' or 'f32'
+    scale: float
+    seed: int
+    kind: str = "plain"        # 'plain' | 'meanpool' | 'boost'
+    ragged: Optional[tuple] = None   # (lo, hi) inclusive, or None = full
+    boost: float = 8.0
+    boost_frac: float = 0.01
+
+    @property
+    def r(self) -> int:
+        return self.h // self.g
+
+    @property
+    def elt(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+_S128 = 1.0 / math.sqrt(128.0)
+
+# The five workloads, with the sizes the pages' models give.
+WORKLOADS = {
+    # single-layer MQA step in fp32 (255 cached rows + 1 appended)
+    "mqa_f32_b1_h8_d64_m256": DecodeConfig(
+        "mqa_f32_b1_h8_d64_m256", 1, 1, 8, 1, 64, 256, "f32", 1.0 / 8.0, 1),
+    # g-knob sweep, mean-pooled from one MHA cache (g set per run)
+    "gqa_sweep_b16_h32_d128_m4096": DecodeConfig(
+        "gqa_sweep_b16_h32_d128_m4096", 1, 16, 32, 8, 128, 4096, "bf16",
+        _S128, 2, kind="meanpool"),
+    # Llama-3-70B-shaped step: 80 layers, 64 query / 8 KV heads
+    "llama3_70b_b32_m8192": DecodeConfig(
+        "llama3_70b_b32_m8192", 80, 32, 64, 8, 128, 8192, "bf16", _S128, 3),
+    # Qwen2.5-7B-shaped ragged batch: 28 layers, 28 query / 4 KV heads
+    "qwen25_7b_b64_ragged": DecodeConfig(
+        "qwen25_7b_b64_ragged", 28, 64, 28, 4, 128, 32768, "bf16", _S128, 4,
+        ragged=(512, 32768)),
+    # long-context MQA with a peaked softmax
+    "long_mqa_b8_m131072": DecodeConfig(
+        "long_mqa_b8_m131072", 1, 8, 32, 1, 128, 131072, "bf16", _S128, 5,
+        kind="boost"),
+}
+
+
+def workload(name: str, **overrides) -> DecodeConfig:
+    """The named workload, optionally with fields replaced (e.g. g for the
+    sweep, or smaller b / cap / layers for quick parity runs)."""
+    return dataclasses.replace(WORKLOADS[name], **overrides)
+
+
+def seq_lens_for(cfg: DecodeConfig) -> np.ndarray:
+    """Post-append lengths L_i (int32 [b])."""
+    if cfg.ragged is None:
+        return np.full(cfg.b, cfg.cap, dtype=np.int32)
+    lo, hi = cfg.ragged
+    lens = np.random.default_rng(cfg.seed).integers(lo, hi, size=cfg.b,
+                                                    endpoint=True)
+    return np.minimum(lens, cfg.cap).astype(np.int32)
+
+
+def layer_bytes(cfg: DecodeConfig, lens: np.ndarray) -> int:
+    """Algorithmic bytes of one decode-attention call: the K and V rows below
+    L_i of every KV head, plus q and out (padding and split partials are not
+    counted)."""
+    kv = int(np.sum(lens, dtype=np.int64)) * cfg.g * 2 * cfg.d * cfg.elt
+    return kv + 2 * cfg.b * cfg.h * cfg.d * cfg.elt
+
+
+def layer_flops(cfg: DecodeConfig, lens: np.ndarray) -> int:
+    """Multiply-add flops of one decode-attention call (2 per product, for
+    q.K and for w.V)."""
+    return 4 * cfg.h * cfg.d * int(np.sum(lens, dtype=np.int64))
+
+
+def _randn(shape, gen, device):
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+
+
+def _pool(x: torch.Tensor, g: int) -> torch.Tensor:
+    """Average contiguous blocks of h/g heads on dim 1 (float32)."""
+    b, h = x.shape[:2]
+    if g == h:
+        return x
+    return x.reshape(b, g, h // g, *x.shape[2:]).mean(dim=2)
+
+
+def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
+               lens: Optional[np.ndarray] = None, pad_fill=None) -> dict:
+    """Inputs of one layer: q [b,h,d], k_cache/v_cache [b,g,cap,d],
+    k_new/v_new [b,g,d] in the storage dtype, seq_lens int32 [b] on
+    ``device``, plus the host copy ``lens``."""
+    if cfg.h % cfg.g != 0:
+        raise ValueError("h must be divisible by g")
+    device = torch.device(device)
+    if lens is None:
+        lens = seq_lens_for(cfg)
+    lens = np.asarray(lens, dtype=np.int32)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed * 1000 + layer)
+    b, h, g, d, cap = cfg.b, cfg.h, cfg.g, cfg.d, cfg.cap
+    dt = cfg.torch_dtype
+
+    if cfg.kind == "meanpool":
+        k_cache = _pool(_randn((b, h, cap, d), gen, device), g).to(dt)
+        v_cache = _pool(_randn((b, h, cap, d), gen, device), g).to(dt)
+        q = _randn((b, h, d), gen, device).to(dt)
+        k_new = _pool(_randn((b, h, d), gen, device), g).to(dt)
+        v_new = _pool(_randn((b, h, d), gen, device), g).to(dt)
+    elif cfg.kind in ("plain", "boost"):
+        if cfg.kind == "plain" and dt == torch.bfloat16:
+            # draw and round block by block to bound the float32 temporary
+            k_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
+            v_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
+            for dst in (k_cache, v_cache):
+                for i in range(b):
+                    dst[i].copy_(_randn((g, cap, d), gen, device))
+        else:
+            k_cache = _randn((b, g, cap, d), gen, device)
+            v_cache = _randn((b, g, cap, d), gen, device)
+        q = _randn((b, h, d), gen, device).to(dt)
+        k_new = _randn((b, g, d), gen, device)
+        v_new = _randn((b, g, d), gen, device).to(dt)
+        if cfg.kind == "boost":
+            if g != 1:
+                raise ValueError("the boosted workload is MQA (g = 1)")
+            k_cache, k_new = _boost(cfg, layer, q, k_cache, k_new, lens)
+        k_cache = k_cache.to(dt)
+        v_cache = v_cache.to(dt)
+        k_new = k_new.to(dt)
+    else:
+        raise ValueError(f"unknown workload kind {cfg.kind!r}")
+
+    if pad_fill is not None:
+        for i in range(b):
+            L = int(lens[i])
+            if L < cap:
+                k_cache[i, :, L:, :] = pad_fill
+                v_cache[i, :, L:, :] = pad_fill
+
+    return {
+        "q": q.contiguous(), "k_cache": k_cache.contiguous(),
+        "v_cache": v_cache.contiguous(), "k_new": k_new.contiguous(),
+        "v_new": v_new.contiguous(),
+        "seq_lens": torch.from_numpy(lens.copy()).to(device),
+        "lens": lens,
+    }
+
+
+def _boost(cfg, layer, q, k_cache, k_new, lens):
+    """Raise every head's logit by about cfg.boost at 1 % of the positions."""
+    cpu_gen = torch.Generator(device="cpu")
+    cpu_gen.manual_seed(cfg.seed * 1000 + layer + 7)
+    qd = q.float().cpu().double().numpy()          # bf16-rounded query
+    for i in range(cfg.b):
+        L = int(lens[i])
+        n = int(round(cfg.boost_frac * L))
+        if n == 0:
+            continue
+        pos = torch.randperm(L, generator=cpu_gen)[:n]
+        Q = qd[i]                                   # [h, d]
+        u = Q.T @ np.linalg.solve(Q @ Q.T, np.ones(Q.shape[0]))
+        du = torch.from_numpy((cfg.boost / cfg.scale) * u).float()
+        du = du.to(k_cache.device)
+        rows = pos[pos < L - 1].to(k_cache.device)
+        k_cache[i, 0, rows, :] += du
+        if bool((pos == L - 1).any()):
+            k_new[i, 0, :] += du
+    return k_cache, k_new
