@@ -1,0 +1,448 @@
+"""Decode-step bench for the grouped-KV decode path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = every layer of the workload: gqa_kv_append then gqa_decode_attn
+through the C ABI, on one stream, with all inputs resident in HBM.  Timing:
+W untimed steps, then K steps between a barrier + synchronize on both sides,
+CUDA events on the launching stream, max over ranks.  Prints one JSON line
+(rank 0).  Under torchrun each rank runs an independent replica on its own
+GPU (the units are independent; no data-path collective): weak scaling.
+
+The default workload is the Llama-3-70B-shaped decode step (80 layers,
+b=32, h=64, g=8, d=128, 8192 cached tokens, bf16): 80 GiB of K/V, far
+larger than L2, so no flush is needed between steps.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the
+same workload (the reference arm: there is no other implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("decode-attn KV GB/s and % of GB300 HBM peak; layer-steps/sec at "
+          "Llama-3-70B shape")
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; barrier and max-over-ranks only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own replica of the workload."""
+    return base_seed + 100 * rank
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def smi_id(local_index: int) -> str:
+    """nvidia-smi --id for torch's device index (through CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        items = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_index < len(items):
+            return items[local_index]
+    return str(local_index)
+
+
+# ---------------------------------------------------------------------------
+# byte counts
+# ---------------------------------------------------------------------------
+def step_bytes(cfg, lens) -> dict:
+    from gqa_kv_cache_append_gb300.inputs import layer_bytes
+    attn = layer_bytes(cfg, lens)
+    append = 2 * 2 * cfg.b * cfg.g * cfg.d * cfg.elt   # read + write of k_new, v_new rows
+    return {"attn_per_layer": attn, "append_per_layer": append,
+            "step": cfg.layers * (attn + append)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel_src: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (matched by hash), else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_hash and m_bytes):
+        return None
+    src = open(kernel_src, "rb").read()
+    if hashlib.sha256(src).hexdigest() != m_hash.group(1):
+        return None
+    return int(m_bytes.group(1))
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096):
+    """Time the float64 oracle's decode step on whole units (one sequence, one
+    KV head, its r query heads) of layer 0 of the workload, drawn on the CPU
+    with the same generator recipe, until about target_s seconds of work.
+    Returns (GB/s of algorithmic bytes, seconds, units, bytes)."""
+    import torch
+    import oracle
+    from gqa_kv_cache_append_gb300.inputs import make_layer, seq_lens_for
+    import dataclasses
+
+    lens = seq_lens_for(cfg)
+    one = dataclasses.replace(cfg, b=1, layers=1)
+    done_units, done_bytes, spent = 0, 0, 0.0
+    i = 0
+    while spent < target_s and done_units < max_units:
+        L = int(lens[i % len(lens)])
+        sub = dataclasses.replace(one, seed=cfg.seed * 7919 + i)
+        x = make_layer(sub, 0, "cpu", lens=np.array([L], dtype=np.int32))
+
+        def np_(t):
+            t = t.contiguous()
+            if t.dtype == torch.bfloat16:
+                return t.view(torch.int16).numpy().view(np.uint16), "bf16"
+            return t.numpy(), "f32"
+        tag = np_(x["q"])[1]
+        arrs = [np_(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
+        t0 = time.perf_counter()
+        oracle.decode_step(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
+        spent += time.perf_counter() - t0
+        done_units += cfg.g
+        done_bytes += L * cfg.g * 2 * cfg.d * cfg.elt + 2 * cfg.h * cfg.d * cfg.elt
+        i += 1
+    return done_bytes / spent / 1e9, spent, done_units, done_bytes
+
+
+def blas_threads() -> int:
+    # numpy.einsum without `optimize` runs its own single-threaded loops
+    return 1
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, local_rank, world):
+    import torch
+    from gqa_kv_cache_append_gb300 import binding as B
+    from gqa_kv_cache_append_gb300.inputs import make_layer, seq_lens_for, workload
+    import dataclasses
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    base = workload(args.workload)
+    cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
+    lens = seq_lens_for(cfg)
+    layers = [make_layer(cfg, l, dev) for l in range(cfg.layers)]
+    outs = [torch.empty((cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device=dev)
+            for _ in range(cfg.layers)]
+    stream = torch.cuda.current_stream(dev)
+    sb = step_bytes(cfg, lens)
+
+    def step(ev=None):
+        for l, x in enumerate(layers):
+            B.gqa_kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"],
+                            cfg.b, cfg.g, cfg.d, cfg.d, stream=stream)
+            if ev is not None:
+                ev[l][0].record(stream)
+            B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
+                              cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l], stream=stream)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert B.gqa_device_status(stream) == 0
+
+    # ---- device-resident timing, with per-launch events on the attention ----
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            for _ in range(cfg.layers)] for _ in range(args.steps)]
+    clocks = ClockSampler(smi_id(dev.index))
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(dist, dev)
+    ms_local = t_start.elapsed_time(t_end) / args.steps
+    attn_ms = [e[0].elapsed_time(e[1]) for per in evs for e in per]
+    ms = max_over_ranks(dist, ms_local)
+    attn_avg_ms = max_over_ranks(dist, float(np.mean(attn_ms)))
+    status = B.gqa_device_status(stream)
+
+    # ---- end to end: pinned host inputs in, result out, every step ----
+    hq = [x["q"].cpu().pin_memory() for x in layers]
+    hk = [x["k_new"].cpu().pin_memory() for x in layers]
+    hv = [x["v_new"].cpu().pin_memory() for x in layers]
+    ho = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
+    d2h = sum(t.numel() * t.element_size() for t in ho)
+
+    def e2e_step():
+        for l, x in enumerate(layers):
+            x["q"].copy_(hq[l], non_blocking=True)
+            x["k_new"].copy_(hk[l], non_blocking=True)
+            x["v_new"].copy_(hv[l], non_blocking=True)
+            B.gqa_kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"],
+                            cfg.b, cfg.g, cfg.d, cfg.d, stream=stream)
+            B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
+                              cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l], stream=stream)
+            ho[l].copy_(outs[l], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
+    status |= B.gqa_device_status(stream)
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    achieved = sb["attn_per_layer"] / (attn_avg_ms * 1e-3) / 1e9
+    src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
+    traffic = profiled_traffic(src, args.workload)
+    launches_per_step = 3 * cfg.layers   # append, attention, combine per layer
+    value = world * sb["step"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,1), shapes of the workload)",
+        "config": {
+            "workload": cfg.name, "layers": cfg.layers, "b": cfg.b, "h": cfg.h, "g": cfg.g,
+            "d_head": cfg.d, "seq_len": int(np.max(lens)), "cap": cfg.cap,
+            "sum_seq_lens": int(np.sum(lens)),
+            "l2": "inputs larger than L2: every step streams all layers' K/V "
+                  f"({sb['step'] / 2**30:.1f} GiB)",
+            "parallelism": f"replicas x{world}",
+        },
+        "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
+        "attn_gbs_per_gpu": round(achieved, 2),
+        "pct_of_nominal_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gqa_decode_attn (decode_tc_kernel + combine_kernel)",
+            "achieved": round(achieved, 2),
+            "peak": peaks["hbm_gbs"],
+            "peak_source": peaks["source"],
+            "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": sb["attn_per_layer"],
+            "avg_launch_ms": round(attn_avg_ms, 5),
+        },
+        "e2e": {
+            "value": round(world * sb["step"] / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 4),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_per_step": launches_per_step,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        gbs, spent, units, nbytes = oracle_sample(base, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": round(gbs, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{units} (sequence, KV head) units of {cfg.name} layer-shaped data "
+                      f"({nbytes / 2**20:.0f} MiB, {spent:.1f} s, float64 numpy oracle: "
+                      "append + attention)"}
+    return line
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle on the host cores, timed per
+    step on a bounded sample of the workload; rank 0 only."""
+    from gqa_kv_cache_append_gb300.inputs import seq_lens_for, workload
+    if rank != 0:
+        return None
+    cfg = workload(args.workload)
+    per_step_s = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    total_units = total_bytes = 0
+    for k in range(args.warmup + args.steps):
+        gbs, spent, units, nbytes = oracle_sample(cfg, target_s=per_step_s)
+        if k >= args.warmup:
+            vals.append(gbs)
+            total_units += units
+            total_bytes += nbytes
+    value = float(np.mean(vals))
+    lens = seq_lens_for(cfg)
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), shapes of the workload)",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "b": cfg.b, "h": cfg.h,
+                   "g": cfg.g, "d_head": cfg.d, "seq_len": int(np.max(lens)),
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{total_units} (sequence, KV head) units over {args.steps} "
+                                   f"steps, {total_bytes / 2**20:.0f} MiB"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama3_70b_b32_m8192")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed steps
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, local_rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

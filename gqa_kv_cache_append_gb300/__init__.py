@@ -1,0 +1,18 @@
+"""GB300-native grouped-KV incremental decode attention.
+
+The computation lives in libgqa.so (C ABI in include/gqa.h, CUDA kernels for
+sm_103a under csrc/).  ``binding`` is its ctypes binding, loaded on first use
+of one of the names below; ``inputs`` holds the seeded synthetic workloads.
+"""
+_BINDING = {
+    "gqa_kv_append", "gqa_decode_attn", "gqa_device_status",
+    "gqa_selftest_wait_timeout", "gqa_version", "decode_step", "GqaError",
+    "status_string",
+}
+
+
+def __getattr__(name):
+    if name in _BINDING:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)

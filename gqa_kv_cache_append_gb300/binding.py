@@ -1,0 +1,148 @@
+"""Thin ctypes binding of libgqa.so (include/gqa.h), same names as the C ABI.
+
+Argument marshalling only: tensors become device pointers, torch dtypes
+become GQA_F32 / GQA_BF16, and the current torch CUDA stream is passed when
+no stream is given.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback.  Loading fails loudly when the library
+has not been built (``python -m gqa_kv_cache_append_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+GQA_F32 = 0
+GQA_BF16 = 1
+
+GQA_OK = 0
+GQA_ERR_NULL = -1
+GQA_ERR_SHAPE = -2
+GQA_ERR_DTYPE = -3
+GQA_ERR_ALIGN = -4
+GQA_ERR_UNSUPPORTED = -5
+GQA_ERR_CUDA = -6
+GQA_ERR_DEVICE = -7
+
+GQA_DEV_BAD_SEQ_LEN = 1
+GQA_DEV_WAIT_TIMEOUT = 2
+
+# every function the header declares, with its C signature
+_VP, _I, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+SIGNATURES = {
+    "gqa_kv_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
+    "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I, _VP]),
+    "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
+    "gqa_status_string": (ctypes.c_char_p, [_I]),
+    "gqa_version": (_I, []),
+}
+
+
+class GqaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({status_string(code)})")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB):
+        raise ImportError(
+            f"{LIB} is missing: build it with `python -m gqa_kv_cache_append_gb300.build` "
+            "(or __graft_entry__.build()); there is no fallback implementation")
+    lib = ctypes.CDLL(LIB)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.gqa_status_string(int(code)).decode()
+
+
+def _ptr(x) -> int:
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x) if x is not None else 0
+
+
+def _dtype(x, dtype) -> int:
+    if dtype is not None:
+        return int(dtype)
+    if isinstance(x, torch.Tensor):
+        if x.dtype == torch.bfloat16:
+            return GQA_BF16
+        if x.dtype == torch.float32:
+            return GQA_F32
+        return -99  # the library rejects it with GQA_ERR_DTYPE
+    raise ValueError("dtype must be given when passing raw pointers")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, code: int) -> None:
+    if code != GQA_OK:
+        raise GqaError(fn, code)
+
+
+def gqa_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, b, g, d_k, d_v,
+                  cap=None, dtype=None, stream=None) -> None:
+    """Write row seq_lens[i] - 1 of every (i, j) of the caches (in place)."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_kv_append", lib.gqa_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        int(b), int(g), int(d_k), int(d_v), int(cap), _dtype(k_cache, dtype),
+        _stream(stream)))
+
+
+def gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
+                    out, cap=None, dtype=None, stream=None) -> None:
+    """out[i, a, :] = softmax_p(scale * q[i, a] . K[i, a // (h/g), p]) V[...]."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_decode_attn", lib.gqa_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
+        _dtype(q, dtype), _stream(stream)))
+
+
+def gqa_device_status(stream=None) -> int:
+    """Read and clear the device status word (synchronizes the stream)."""
+    bits = ctypes.c_uint32(0)
+    _check("gqa_device_status", lib.gqa_device_status(_stream(stream), ctypes.byref(bits)))
+    return int(bits.value)
+
+
+def gqa_selftest_wait_timeout(budget_cycles: int, stream=None) -> None:
+    _check("gqa_selftest_wait_timeout",
+           lib.gqa_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
+
+
+def gqa_version() -> int:
+    return int(lib.gqa_version())
+
+
+def decode_step(q, k_cache, v_cache, k_new, v_new, seq_lens, g, scale, out,
+                stream=None) -> None:
+    """One layer's decode step in the order of the decode notes: push the new
+    K/V rows, then attend (two C-ABI calls on the same stream)."""
+    b, h, d = q.shape
+    gqa_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, b, g, d, v_new.shape[-1],
+                  stream=stream)
+    gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d, v_cache.shape[-1],
+                    scale, out, stream=stream)

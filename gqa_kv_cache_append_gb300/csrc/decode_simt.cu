@@ -1,0 +1,357 @@
+// decode_simt.cu - CUDA-core split-KV decode attention (fp32 inputs, and bf16
+// with head dim 64).
+//
+// One persistent CTA per SM streams its share of the (sequence, KV head)
+// tiles (see Walker).  Warp 0 copies each K/V tile of T positions from HBM
+// into a shared-memory ring with one bulk copy per tensor (the rows of a
+// tile are contiguous in the cache), completing on an mbarrier; only the
+// rows below L_i are copied.  Warps 1-4 serve all r = h/g query heads of the
+// KV head from each tile:
+//   A  logits: 16-byte vector loads of K, fp32 dot products against q held
+//      in registers, reduced across the lanes that share a row by xor
+//      shuffles (the "bhk,bhmk->bhm" contraction of the MQA review §2.4);
+//   B  online softmax per head in base 2: warp max, rescale factor, exp2,
+//      warp sum;
+//   C  weighted sum of V rows into fp32 register accumulators ("bhm,bhmv->
+//      bhv"), rescaled by each tile's factor.
+// A segment's end writes the normalised output, or a partial for the
+// combine kernel when the unit is split across CTAs.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gqa_device.cuh"
+#include "gqa_internal.h"
+
+namespace gqa {
+namespace {
+
+template <typename DT>
+struct Elt;
+template <>
+struct Elt<float> {
+  static constexpr int size = 4;
+  __device__ static void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ static void store(float* p, float v) { *p = v; }
+};
+template <>
+struct Elt<__nv_bfloat16> {
+  static constexpr int size = 2;
+  __device__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+template <typename DT, int D, int RMAX>
+struct SimtCfg {
+  static constexpr int ELT = Elt<DT>::size;
+  static constexpr int CH = D * ELT / 16;      // 16-byte chunks per row
+  static constexpr int EPC = 16 / ELT;         // elements per chunk
+  static constexpr int PPW = 32 / CH;          // rows per warp step
+  static constexpr int T = 16384 / (D * ELT);  // positions per tile (32 KiB K+V)
+  static constexpr int PPL = T / 32;           // positions per lane in softmax
+  static constexpr int NPG = 128 / CH;         // position groups in the V pass
+  static constexpr int STAGES = 3;
+  static constexpr int STAGE_BYTES = 2 * T * D * ELT;
+  static constexpr int OFF_P = STAGES * STAGE_BYTES;          // float [RMAX][T]
+  static constexpr int OFF_RED = OFF_P + RMAX * T * 4;        // float [4][RMAX][D]
+  static constexpr int OFF_ML = OFF_RED + 4 * RMAX * D * 4;   // float m,l,alpha [RMAX]
+  static constexpr int OFF_BAR = OFF_ML + 3 * RMAX * 4;
+  static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 128;
+  static_assert(CH <= 32 && 32 % CH == 0, "row must split evenly over lanes");
+  static_assert(T % (4 * PPW) == 0 && T % 32 == 0, "tile shape");
+};
+
+constexpr int kThreads = 160;  // warp 0 copies, warps 1-4 compute
+
+template <typename DT, int D, int RMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_simt_kernel(const DT* __restrict__ q, const DT* __restrict__ kc,
+                       const DT* __restrict__ vc, const int* __restrict__ lens, int b, int h,
+                       int g, int cap, float scale_log2, DT* __restrict__ out,
+                       float* __restrict__ part_o, float* __restrict__ part_ml,
+                       unsigned int* status, long long budget) {
+  using C = SimtCfg<DT, D, RMAX>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~uintptr_t(127));
+  float* sP = reinterpret_cast<float*>(sm + C::OFF_P);
+  float* sRed = reinterpret_cast<float*>(sm + C::OFF_RED);
+  float* sM = reinterpret_cast<float*>(sm + C::OFF_ML);
+  float* sL = sM + RMAX;
+  float* sA = sL + RMAX;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + C::STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = h / g;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x >= 32 && threadIdx.x < 32 + RMAX) {
+    const int t = threadIdx.x - 32;
+    sM[t] = -INFINITY;
+    sL[t] = 0.f;
+    sA[t] = 0.f;
+  }
+  __syncthreads();
+
+  Walker w;
+  w.init(lens, b, g, cap, C::T, blockIdx.x, gridDim.x);
+  Segment seg;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      uint32_t n = 0;
+      int last_n[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) last_n[s] = -1;
+      while (w.next(seg)) {
+        const size_t unit_row = (static_cast<size_t>(seg.i) * g + seg.j) * cap;
+        for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          const int st = n % C::STAGES;
+          const bool ok = mbar_wait(empty0 + 8 * st, ((n / C::STAGES) & 1) ^ 1, abort_flag,
+                                    status, budget);
+          if (!ok) continue;
+          const int p0 = lt * C::T;
+          const int rows = min(C::T, seg.L - p0);
+          const uint32_t bytes = static_cast<uint32_t>(rows) * D * C::ELT;
+          uint8_t* stage = sm + st * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(full0 + 8 * st, 2 * bytes);
+          bulk_load(smem_u32(stage), kc + (unit_row + p0) * D, bytes, full0 + 8 * st);
+          bulk_load(smem_u32(stage + C::T * D * C::ELT), vc + (unit_row + p0) * D, bytes,
+                    full0 + 8 * st);
+          last_n[st] = static_cast<int>(n);
+        }
+      }
+      if (*abort_flag) {  // let copies in flight land before the CTA exits
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (last_n[s] < 0) continue;
+          const uint32_t par = (last_n[s] / C::STAGES) & 1;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(full0 + 8 * s, par) && clock64() - t0 < budget) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- compute (128 threads) ----------------
+    const int ct = threadIdx.x - 32;
+    const int cw = ct >> 5;
+    const int sub = lane / C::CH, ch = lane % C::CH;  // logits mapping
+    const int pg = ct / C::CH;                         // V-pass mapping (chunk = ch)
+    float qreg[RMAX][C::EPC];
+    float acc[RMAX][C::EPC];
+#pragma unroll
+    for (int t = 0; t < RMAX; ++t)
+#pragma unroll
+      for (int e = 0; e < C::EPC; ++e) acc[t][e] = 0.f;
+
+    uint32_t n = 0;
+    while (w.next(seg)) {
+      const int a0 = seg.i * h + seg.j * r;  // first query head of the group
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t) {
+        if (t < r) {
+          const uint4 u =
+              *reinterpret_cast<const uint4*>(q + static_cast<size_t>(a0 + t) * D + ch * C::EPC);
+          Elt<DT>::unpack(u, qreg[t]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < C::EPC; ++e) qreg[t][e] = 0.f;
+        }
+      }
+      for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+        const int st = n % C::STAGES;
+        const int valid = min(C::T, seg.L - lt * C::T);
+        const bool ok = mbar_wait(full0 + 8 * st, (n / C::STAGES) & 1, abort_flag, status,
+                                  budget);
+        const DT* sK = reinterpret_cast<const DT*>(sm + st * C::STAGE_BYTES);
+        const DT* sV = sK + C::T * D;
+        // A: logits
+#pragma unroll 2
+        for (int step = 0; step < C::T / (4 * C::PPW); ++step) {
+          const int p = step * (4 * C::PPW) + cw * C::PPW + sub;
+          float kf[C::EPC];
+          if (ok && p < valid) {
+            const uint4 u = *reinterpret_cast<const uint4*>(sK + p * D + ch * C::EPC);
+            Elt<DT>::unpack(u, kf);
+          } else {
+#pragma unroll
+            for (int e = 0; e < C::EPC; ++e) kf[e] = 0.f;
+          }
+#pragma unroll
+          for (int t = 0; t < RMAX; ++t) {
+            if (t < r) {
+              float part = 0.f;
+#pragma unroll
+              for (int e = 0; e < C::EPC; ++e) part = fmaf(qreg[t][e], kf[e], part);
+#pragma unroll
+              for (int o = C::CH / 2; o > 0; o >>= 1)
+                part += __shfl_xor_sync(0xffffffffu, part, o);
+              if (ch == 0 && p < valid) sP[t * C::T + p] = part * scale_log2;
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+        // B: online softmax, one warp per head
+        for (int t = cw; t < r; t += 4) {
+          float x[C::PPL];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < C::PPL; ++k) {
+            const int p = lane + 32 * k;
+            x[k] = (p < valid) ? sP[t * C::T + p] : -INFINITY;
+            mx = fmaxf(mx, x[k]);
+          }
+          mx = warp_max(mx);
+          const float m_old = sM[t];
+          const float m_new = fmaxf(m_old, mx);
+          const float alpha = ex2(m_old - m_new);
+          float sum = 0.f;
+#pragma unroll
+          for (int k = 0; k < C::PPL; ++k) {
+            const float pv = ex2(x[k] - m_new);
+            sum += pv;
+            sP[t * C::T + lane + 32 * k] = pv;
+          }
+          sum = warp_sum(sum);
+          __syncwarp();
+          if (lane == 0) {
+            sM[t] = m_new;
+            sL[t] = sL[t] * alpha + sum;
+            sA[t] = alpha;
+          }
+        }
+        named_bar_sync(1, 128);
+        // C: weighted sum of V
+#pragma unroll
+        for (int t = 0; t < RMAX; ++t) {
+          if (t < r) {
+            const float al = sA[t];
+#pragma unroll
+            for (int e = 0; e < C::EPC; ++e) acc[t][e] *= al;
+          }
+        }
+        if (ok) {
+          for (int p = pg; p < valid; p += C::NPG) {
+            float vf[C::EPC];
+            const uint4 u = *reinterpret_cast<const uint4*>(sV + p * D + ch * C::EPC);
+            Elt<DT>::unpack(u, vf);
+#pragma unroll
+            for (int t = 0; t < RMAX; ++t) {
+              if (t < r) {
+                const float wgt = sP[t * C::T + p];
+#pragma unroll
+                for (int e = 0; e < C::EPC; ++e) acc[t][e] = fmaf(wgt, vf[e], acc[t][e]);
+              }
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+        if (ct == 0) mbar_arrive(empty0 + 8 * st);
+      }
+
+      // ---- segment end: reduce the position groups, write out ----
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t) {
+        if (t < r) {
+#pragma unroll
+          for (int e = 0; e < C::EPC; ++e) {
+            float v = acc[t][e];
+#pragma unroll
+            for (int o = C::CH; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane < C::CH) sRed[(cw * RMAX + t) * D + ch * C::EPC + e] = v;
+            acc[t][e] = 0.f;
+          }
+        }
+      }
+      named_bar_sync(1, 128);
+      const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
+      const int u = seg.i * g + seg.j;
+      const size_t slot = static_cast<size_t>(u) + blockIdx.x;
+      for (int idx = ct; idx < r * D; idx += 128) {
+        const int t = idx / D, dd = idx % D;
+        const float o = sRed[(0 * RMAX + t) * D + dd] + sRed[(1 * RMAX + t) * D + dd] +
+                        sRed[(2 * RMAX + t) * D + dd] + sRed[(3 * RMAX + t) * D + dd];
+        if (whole) {
+          Elt<DT>::store(out + static_cast<size_t>(a0 + t) * D + dd, o / sL[t]);
+        } else {
+          part_o[(slot * r + t) * D + dd] = o;
+          if (dd == 0) {
+            part_ml[(slot * r + t) * 2 + 0] = sM[t];
+            part_ml[(slot * r + t) * 2 + 1] = sL[t];
+          }
+        }
+      }
+      named_bar_sync(1, 128);
+      if (ct < RMAX) {
+        sM[ct] = -INFINITY;
+        sL[ct] = 0.f;
+        sA[ct] = 0.f;
+      }
+      named_bar_sync(1, 128);
+    }
+  }
+  __syncthreads();
+}
+
+template <typename DT, int D, int RMAX>
+cudaError_t launch_t(const DecodeLaunch& a) {
+  using C = SimtCfg<DT, D, RMAX>;
+  auto kern = decode_simt_kernel<DT, D, RMAX>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<a.nc, kThreads, C::SMEM, a.stream>>>(
+      static_cast<const DT*>(a.q), static_cast<const DT*>(a.k_cache),
+      static_cast<const DT*>(a.v_cache), a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
+      static_cast<DT*>(a.out), a.part_o, a.part_ml, a.status, a.budget);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool simt_supported(int dtype, int d, int r) {
+  if (dtype == GQA_F32) return (d == 64 || d == 128) && r >= 1 && r <= 16;
+  if (dtype == GQA_BF16) return (d == 64 || d == 128) && r >= 1 && r <= 8;
+  return false;
+}
+
+int simt_tile(int dtype, int d) { return 16384 / (d * (dtype == GQA_F32 ? 4 : 2)); }
+
+int simt_ctas_per_sm(int, int, int) { return 1; }
+
+cudaError_t launch_decode_simt(const DecodeLaunch& a) {
+  const int r = a.h / a.g;
+  if (a.dtype == GQA_F32) {
+    if (a.d == 64) return r <= 8 ? launch_t<float, 64, 8>(a) : launch_t<float, 64, 16>(a);
+    return r <= 8 ? launch_t<float, 128, 8>(a) : launch_t<float, 128, 16>(a);
+  }
+  if (a.d == 64) return launch_t<__nv_bfloat16, 64, 8>(a);
+  return launch_t<__nv_bfloat16, 128, 8>(a);
+}
+
+}  // namespace gqa

@@ -1,0 +1,518 @@
+// decode_tc.cu - tensor-core (tcgen05 + TMEM) split-KV decode attention for
+// bf16 caches with head dim 128.
+//
+// The step of the MQA review §2.4 / §3 per (sequence i, KV head j) tile of
+// T = 128 cached positions, with the r = h/g query heads of the group padded
+// to NP columns (16 or 32) and positions on the MMA's M axis:
+//
+//   S^T [T x NP]  = K_tile [T x 128] . Q_g^T          (tcgen05.mma, M=128)
+//   P^T [T x NP]  = exp2(S^T * scale*log2e - m)        (CUDA cores, per head)
+//   O^T [128 x NP] = V_tile^T [128 x T] . P^T          (tcgen05.mma, M=128)
+//
+// Roles (192 threads, one persistent CTA per SM):
+//   warp 0     TMA producer: Q block once per segment, then K and V tiles
+//              (two 64-column boxes each, 128-byte swizzle) into a 3-stage
+//              ring, completing on mbarriers.  Each K/V byte is read from
+//              HBM once and serves all r query heads.
+//   warp 1     allocates tensor memory; one lane issues the MMAs:
+//              S(n) before O(n-1), so the softmax of tile n overlaps the
+//              V product of tile n-1.  S and O are double-buffered in TMEM.
+//   warps 2-5  softmax and correction (128 threads): thread x owns TMEM lane
+//              x, i.e. position x of the tile for S and output column x for
+//              O.  Per tile: load S, mask p >= L_i, per-head max across the
+//              128 positions (redux.sync.max.f32 + one shared-memory
+//              exchange), exp2, write P in the MMA's MN-major swizzled
+//              layout, then fold the previous tile's O into fp32 registers
+//              with its rescale factor.  Segment end: sum the per-thread
+//              softmax denominators and write the output or a partial.
+//
+// Rows >= L_i of the last tile of a unit are masked out of S, and their V
+// rows are zeroed in shared memory before the O product reads them, so
+// whatever the cache holds there never reaches the result.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gqa_device.cuh"
+#include "gqa_internal.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kT = 128;       // positions per tile (MMA M of the S product)
+constexpr int kD = 128;       // head dim (MMA M of the O product)
+constexpr int kStages = 3;    // K/V ring depth
+constexpr int kThreads = 192;
+constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
+
+template <int NP>
+struct TcCfg {
+  static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
+  static constexpr int Q_BYTES = NP * 256;         // two [NP x 64] boxes
+  static constexpr int P_BYTES = kT * NP * 2;      // [T rows x NP] bf16
+  static constexpr int OFF_Q = kStages * KV_BYTES;
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;   // float [2][4][NP]
+  static constexpr int OFF_LRED = OFF_RED + 2 * 4 * NP * 4;  // float [4][NP]
+  static constexpr int OFF_BAR = OFF_LRED + 4 * NP * 4;
+  static constexpr int NBAR = 3 * kStages + 2 * 7 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for 1024-B alignment
+  static constexpr int NCOLS = 4 * NP;               // S0 S1 O0 O1
+  // P rows are NP * 2 bytes: 32 B (NP=16) or 64 B (NP=32) swizzle atoms
+  static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
+  static constexpr uint32_t IDESC = idesc_bf16(128, NP, 0, 0);     // S: K-major A, B
+  static constexpr uint32_t IDESC_O = idesc_bf16(128, NP, 1, 1);   // O: MN-major A, B
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
+};
+
+// barrier slots
+enum {
+  B_FULL_K = 0,
+  B_FULL_V = kStages,
+  B_EMPTY = 2 * kStages,
+  B_Q_FULL = 3 * kStages,
+  B_Q_EMPTY = B_Q_FULL + 2,
+  B_S_FULL = B_Q_EMPTY + 2,
+  B_S_FREE = B_S_FULL + 2,
+  B_P_READY = B_S_FREE + 2,
+  B_O_FULL = B_P_READY + 2,
+  B_O_FREE = B_O_FULL + 2,
+  B_DRAIN = B_O_FREE + 2,
+};
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ lens,
+                     int b, int h, int g, int cap, float scale_log2,
+                     __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
+                     float* __restrict__ part_ml, unsigned int* status, long long budget) {
+  using C = TcCfg<NP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(sm);
+  float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
+  float* lred = reinterpret_cast<float*>(sm + C::OFF_LRED);
+  const uint32_t bar0 = s_base + C::OFF_BAR;
+  auto BAR = [&](int k) -> uint32_t { return bar0 + 8u * k; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = h / g;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < C::NBAR; ++k) {
+      uint32_t cnt = 1;
+      if ((k >= B_S_FREE && k < B_S_FREE + 2) || (k >= B_P_READY && k < B_P_READY + 2) ||
+          (k >= B_O_FREE && k < B_O_FREE + 2))
+        cnt = 4;  // one arrival per softmax warp
+      mbar_init(BAR(k), cnt);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::NCOLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  Walker w;
+  w.init(lens, b, g, cap, kT, blockIdx.x, gridDim.x);
+  Segment seg;
+
+  if (warp == 0) {
+    // =========================== TMA producer ===========================
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      uint32_t n = 0, k = 0;
+      int last_n[kStages] = {-1, -1, -1};
+      int last_q[2] = {-1, -1};
+      while (w.next(seg)) {
+        const uint32_t qs = k & 1;
+        if (mbar_wait(BAR(B_Q_EMPTY + qs), ((k >> 1) & 1) ^ 1, abort_flag, status, budget)) {
+          const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
+          const int qrow = seg.i * h + seg.j * r;
+          mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), C::Q_BYTES);
+          tma_load_2d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, qrow, pol_keep);
+          tma_load_2d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, qrow, pol_keep);
+          last_q[qs] = static_cast<int>(k);
+        }
+        const int unit_row = (seg.i * g + seg.j) * cap;
+        for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          const int st = n % kStages;
+          if (!mbar_wait(BAR(B_EMPTY + st), ((n / kStages) & 1) ^ 1, abort_flag, status,
+                         budget))
+            continue;
+          const int row = unit_row + lt * kT;
+          const uint32_t dst = s_base + st * C::KV_BYTES;
+          mbar_arrive_expect_tx(BAR(B_FULL_K + st), 2 * kBoxBytes);
+          tma_load_2d(dst, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
+          tma_load_2d(dst + kBoxBytes, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
+          mbar_arrive_expect_tx(BAR(B_FULL_V + st), 2 * kBoxBytes);
+          tma_load_2d(dst + 2 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
+          tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
+          last_n[st] = static_cast<int>(n);
+        }
+        ++k;
+      }
+      if (*abort_flag) {  // copies in flight must land before the CTA exits
+        for (int s = 0; s < kStages + 2; ++s) {
+          int idx;
+          uint32_t b0, b1 = 0;
+          bool two = false;
+          if (s < kStages) {
+            idx = last_n[s];
+            if (idx < 0) continue;
+            b0 = BAR(B_FULL_K + s);
+            b1 = BAR(B_FULL_V + s);
+            two = true;
+            idx /= kStages;
+          } else {
+            idx = last_q[s - kStages];
+            if (idx < 0) continue;
+            b0 = BAR(B_Q_FULL + s - kStages);
+            idx >>= 1;
+          }
+          const long long t0 = clock64();
+          while (!mbar_try_wait(b0, idx & 1) && clock64() - t0 < budget) {
+          }
+          while (two && !mbar_try_wait(b1, idx & 1) && clock64() - t0 < budget) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================ MMA issuer ============================
+    if (lane == 0) {
+      const uint32_t tS = tmem, tO = tmem + 2 * NP;
+      auto issue_o = [&](uint32_t m) {
+        const int st = m % kStages;
+        const uint32_t nb = m & 1;
+        bool ok = mbar_wait(BAR(B_P_READY + nb), (m >> 1) & 1, abort_flag, status, budget);
+        ok = ok && mbar_wait(BAR(B_FULL_V + st), (m / kStages) & 1, abort_flag, status, budget);
+        ok = ok &&
+             mbar_wait(BAR(B_O_FREE + nb), ((m >> 1) & 1) ^ 1, abort_flag, status, budget);
+        tc_fence_after();
+        if (ok) {
+          const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
+          const uint32_t pbase = s_base + C::OFF_P + nb * C::P_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk) {
+            // A = V^T: M = 128 head-dim columns (two 64-column boxes, LBO
+            // apart), K = 16 positions (two 8-row groups, SBO apart)
+            const uint64_t a = smem_desc(vbase + kk * 2048, kBoxBytes, 1024, SWZ_128B);
+            // B = P^T: N = NP heads contiguous per row, K = 16 position rows
+            const uint64_t bd =
+                smem_desc(pbase + kk * 16 * NP * 2, C::P_BYTES, 8 * NP * 2, C::P_SWZ);
+            mma_bf16(tO + nb * NP, a, bd, C::IDESC_O, kk > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(BAR(B_O_FULL + nb));
+        mma_commit(BAR(B_EMPTY + st));
+      };
+      uint32_t n = 0, k = 0, prev = 0;
+      bool have_prev = false;
+      while (w.next(seg)) {
+        const uint32_t qs = k & 1;
+        const bool qok = mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget);
+        const uint32_t qbase = s_base + C::OFF_Q + qs * C::Q_BYTES;
+        for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          const int st = n % kStages;
+          const uint32_t nb = n & 1;
+          bool ok = qok && mbar_wait(BAR(B_FULL_K + st), (n / kStages) & 1, abort_flag, status,
+                                     budget);
+          ok = ok &&
+               mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
+          tc_fence_after();
+          if (ok) {
+            const uint32_t kbase = s_base + st * C::KV_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              // A = K tile, K-major: 128 rows, 16 head-dim columns per step;
+              // steps 0-3 in the first 64-column box, 4-7 in the second
+              const uint64_t a =
+                  smem_desc(kbase + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024, SWZ_128B);
+              const uint64_t bq =
+                  smem_desc(qbase + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024, SWZ_128B);
+              mma_bf16(tS + nb * NP, a, bq, C::IDESC, kk > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(BAR(B_S_FULL + nb));
+          if (lt == seg.lt1 - 1) mma_commit(BAR(B_Q_EMPTY + qs));
+          if (have_prev) issue_o(prev);
+          have_prev = true;
+          prev = n;
+        }
+        ++k;
+      }
+      if (have_prev) issue_o(prev);
+      // every MMA must be finished before tensor memory is released
+      mma_commit(BAR(B_DRAIN));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(BAR(B_DRAIN), 0) && clock64() - t0 < budget) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ====================== softmax / correction ========================
+    const int qd = warp & 3;          // TMEM lane quarter this warp may access
+    const int wq = warp - 2;          // index among the four softmax warps
+    const int row = qd * 32 + lane;   // tile position (S) / head-dim column (O)
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tO = tmem + 2 * NP + lane_off;
+
+    float m[NP], l[NP], o[NP], alpha_prev[NP];
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      m[t] = -INFINITY;
+      l[t] = 0.f;
+      o[t] = 0.f;
+      alpha_prev[t] = 0.f;
+    }
+
+    auto correct = [&](uint32_t mt, const float(&al)[NP]) {
+      const uint32_t nb = mt & 1;
+      const bool ok = mbar_wait(BAR(B_O_FULL + nb), (mt >> 1) & 1, abort_flag, status, budget);
+      float ov[NP];
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < NP; c += 16) {
+          float tmp[16];
+          tmem_ld16(tO + nb * NP + c, tmp);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[c + e] = tmp[e];
+        }
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int t = 0; t < NP; ++t) ov[t] = 0.f;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_O_FREE + nb));
+#pragma unroll
+      for (int t = 0; t < NP; ++t) o[t] = fmaf(o[t], al[t], ov[t]);
+    };
+
+    uint32_t n = 0;
+    while (w.next(seg)) {
+      for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+        const uint32_t nb = n & 1;
+        const int st = n % kStages;
+        const int valid = min(kT, seg.L - lt * kT);
+        // ---- logits from TMEM ----
+        const bool ok = mbar_wait(BAR(B_S_FULL + nb), (n >> 1) & 1, abort_flag, status, budget);
+        float x[NP];
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < NP; c += 16) {
+            float tmp[16];
+            tmem_ld16(tS + nb * NP + c, tmp);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[c + e] = tmp[e];
+          }
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int t = 0; t < NP; ++t) x[t] = 0.f;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_S_FREE + nb));
+        const bool live = row < valid;
+#pragma unroll
+        for (int t = 0; t < NP; ++t) x[t] = (live && t < r) ? x[t] * scale_log2 : -INFINITY;
+        // ---- per-head max over the tile's 128 positions ----
+        float mine = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < NP; ++t) {
+          const float wm = warp_max(x[t]);
+          if (lane == t) mine = wm;
+        }
+        float* rb = red + nb * 4 * NP;
+        if (lane < NP) rb[wq * NP + lane] = mine;
+        named_bar_sync(1, 128);
+        float alpha[NP], p[NP];
+#pragma unroll
+        for (int t = 0; t < NP; ++t) {
+          if (t < r) {
+            const float tm =
+                fmaxf(fmaxf(rb[t], rb[NP + t]), fmaxf(rb[2 * NP + t], rb[3 * NP + t]));
+            const float mn = fmaxf(m[t], tm);
+            alpha[t] = ex2(m[t] - mn);
+            m[t] = mn;
+            p[t] = ex2(x[t] - mn);
+            l[t] = fmaf(l[t], alpha[t], p[t]);
+          } else {
+            alpha[t] = 1.f;
+            p[t] = 0.f;
+          }
+        }
+        // ---- P^T row `row` into the MN-major swizzled B operand ----
+        {
+          const uint32_t prow = s_base + C::OFF_P + nb * C::P_BYTES + row * (NP * 2);
+#pragma unroll
+          for (int c = 0; c < NP / 8; ++c) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(p[8 * c + 2 * e], p[8 * c + 2 * e + 1]);
+              wv[e] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            const int phys = (NP == 16) ? (c ^ ((row >> 2) & 1)) : (c ^ ((row >> 1) & 3));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys * 16),
+                         "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                         : "memory");
+          }
+        }
+        // ---- ragged last tile: zero the V rows past L_i ----
+        if (valid < kT) {
+          const bool vok =
+              mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
+          if (vok && !live) {
+            const uint32_t vrow = s_base + st * C::KV_BYTES + 2 * kBoxBytes + row * 128;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                 vrow + hb * kBoxBytes + c * 16),
+                             "r"(0u)
+                             : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_P_READY + nb));
+        // ---- fold the previous tile's O into the registers ----
+        if (lt > seg.lt0) correct(n - 1, alpha_prev);
+#pragma unroll
+        for (int t = 0; t < NP; ++t) alpha_prev[t] = alpha[t];
+        if (lt == seg.lt1 - 1) correct(n, alpha);
+      }
+
+      // ---- segment end: softmax denominators, output or partial ----
+      {
+        float mine = 0.f;
+#pragma unroll
+        for (int t = 0; t < NP; ++t) {
+          const float s = warp_sum(l[t]);
+          if (lane == t) mine = s;
+        }
+        if (lane < NP) lred[wq * NP + lane] = mine;
+        named_bar_sync(1, 128);
+        const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
+        const int a0 = seg.i * h + seg.j * r;
+        const size_t slot = static_cast<size_t>(seg.i * g + seg.j) + blockIdx.x;
+#pragma unroll
+        for (int t = 0; t < NP; ++t) {
+          if (t < r) {
+            const float ltot = lred[t] + lred[NP + t] + lred[2 * NP + t] + lred[3 * NP + t];
+            if (whole) {
+              out[static_cast<size_t>(a0 + t) * kD + row] = __float2bfloat16_rn(o[t] / ltot);
+            } else {
+              part_o[(slot * r + t) * kD + row] = o[t];
+              if (row == 0) {
+                part_ml[(slot * r + t) * 2 + 0] = m[t];
+                part_ml[(slot * r + t) * 2 + 1] = ltot;
+              }
+            }
+          }
+          m[t] = -INFINITY;
+          l[t] = 0.f;
+          o[t] = 0.f;
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::NCOLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D map over a row-major [rows x 128] bf16 tensor, box [box_rows x 64],
+// 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NP>
+cudaError_t launch_np(const DecodeLaunch& a) {
+  using C = TcCfg<NP>;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, static_cast<uint64_t>(a.b) * a.h, NP) ||
+      !make_map(&mk, a.k_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT) ||
+      !make_map(&mv, a.v_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT))
+    return cudaErrorInvalidValue;
+  auto kern = decode_tc_kernel<NP>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<a.nc, kThreads, C::SMEM, a.stream>>>(
+      mq, mk, mv, a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
+      static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.status, a.budget);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, int d, int r) {
+  return dtype == GQA_BF16 && d == kD && r >= 1 && r <= 32;
+}
+
+int tc_tile() { return kT; }
+
+int tc_ctas_per_sm(int) { return 1; }
+
+cudaError_t launch_decode_tc(const DecodeLaunch& a) {
+  const int r = a.h / a.g;
+  return r <= 16 ? launch_np<16>(a) : launch_np<32>(a);
+}
+
+}  // namespace gqa

@@ -1,0 +1,356 @@
+// gqa_device.cuh - device-side helpers shared by the decode kernels:
+// PTX wrappers (mbarrier, bulk/tensor copies, tcgen05), the bounded wait, and
+// the work walker that splits the KV stream of all (sequence, KV head) units
+// evenly across persistent CTAs.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "../../include/gqa.h"
+
+namespace gqa {
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses and mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with the given parity of `bar` has completed, for at
+// most `budget` SM cycles.  Returns false (and raises the CTA's abort flag and
+// the device status bit) when the limit is hit, or at once when the abort
+// flag is already up.  No wait in these kernels is unbounded.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned int* status, long long budget) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > budget) {
+      *abort_flag = 1;
+      atomicOr(status, GQA_DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bulk copies global -> shared, completing on an mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,
+                                            int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap))
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor cores, bulk copies)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// arrive once on `bar` when every tcgen05 op issued so far by this thread is done
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp gets lane
+// (base lane + t), columns [col, col + 16)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+// Shared-memory matrix descriptor of tcgen05.mma: start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, swizzle mode.
+enum : uint32_t { SWZ_NONE = 0, SWZ_128B = 2, SWZ_64B = 4, SWZ_32B = 6 };
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swz) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(swz & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
+// A/B K-major (0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn_major,
+                                                  int b_mn_major) {
+  return (1u << 4)                       // D format: f32
+         | (1u << 7)                     // A format: bf16
+         | (1u << 10)                    // B format: bf16
+         | (static_cast<uint32_t>(a_mn_major) << 15) |
+         (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+  float m;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Work walker.
+//
+// A "unit" is one (sequence i, KV head j); it holds t_i = ceil(L_i / T) tiles
+// of T positions (0 when L_i is outside [1, cap]).  Units are ordered
+// u = i * g + j and their tiles laid end to end, W tiles in all.  CTA c of NC
+// takes the tile range [c * W / NC, (c + 1) * W / NC), so every CTA streams
+// the same number of tiles (to within one) whatever the length mix.  A CTA's
+// range cuts into "segments", one per unit it touches.  A segment that covers
+// a whole unit produces final outputs; any other writes a partial (running
+// max, sum, unnormalised output) to slot u + c, which the combine kernel
+// merges.  u + c is unique per (unit, CTA) pair with a non-empty overlap,
+// so the partial buffer needs b * g + NC slots.
+//
+// Every warp runs its own walker (warp-uniform values, no shared state).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int seq_tiles(int L, int cap, int T) {
+  return (L >= 1 && L <= cap) ? (L + T - 1) / T : 0;
+}
+
+struct Segment {
+  int i, j;      // sequence, KV head
+  int lt0, lt1;  // local tile range within the unit
+  int L;         // post-append length of sequence i
+  int ti;        // tiles of the unit
+};
+
+struct Walker {
+  const int* lens;
+  int b, g, cap, T;
+  long long pos, end;  // global tile cursor and end of this CTA's range
+  int i, j, lt, ti, L;
+
+  // total tiles W (warp-cooperative; all lanes get the result)
+  __device__ static long long total_tiles(const int* lens, int b, int g, int cap, int T) {
+    const int lane = threadIdx.x & 31;
+    long long acc = 0;
+    for (int base = 0; base < b; base += 32) {
+      const int idx = base + lane;
+      int t = 0;
+      if (idx < b) t = seq_tiles(__ldg(lens + idx), cap, T);
+      acc += t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc * g;
+  }
+
+  // Position the walker at CTA `c` of `nc`.  Warp-cooperative.
+  __device__ void init(const int* lens_, int b_, int g_, int cap_, int T_, int c, int nc) {
+    lens = lens_;
+    b = b_;
+    g = g_;
+    cap = cap_;
+    T = T_;
+    const long long W = total_tiles(lens, b, g, cap, T);
+    pos = (W * c) / nc;
+    end = (W * (c + 1)) / nc;
+    i = b;
+    j = 0;
+    lt = 0;
+    ti = 0;
+    L = 0;
+    if (pos >= end) return;
+    // find sequence i with g * P_i <= pos < g * P_{i+1}
+    const int lane = threadIdx.x & 31;
+    long long carry = 0;  // g * (tiles before this chunk)
+    for (int base = 0; base < b; base += 32) {
+      const int idx = base + lane;
+      int Lx = 0, t = 0;
+      if (idx < b) {
+        Lx = __ldg(lens + idx);
+        t = seq_tiles(Lx, cap, T);
+      }
+      long long incl = static_cast<long long>(t) * g;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const long long lo = carry + incl - static_cast<long long>(t) * g;
+      const long long hi = carry + incl;
+      const unsigned hit = __ballot_sync(0xffffffffu, idx < b && t > 0 && lo <= pos && pos < hi);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const long long lo_s = __shfl_sync(0xffffffffu, lo, src);
+        const int t_s = __shfl_sync(0xffffffffu, t, src);
+        i = base + src;
+        ti = t_s;
+        L = __shfl_sync(0xffffffffu, Lx, src);
+        const long long off = pos - lo_s;
+        j = static_cast<int>(off / t_s);
+        lt = static_cast<int>(off % t_s);
+        return;
+      }
+      carry = __shfl_sync(0xffffffffu, hi, 31);
+    }
+    pos = end;  // not reached for a consistent plan
+  }
+
+  // Next segment of this CTA's range; false when the range is exhausted.
+  __device__ bool next(Segment& s) {
+    if (pos >= end) return false;
+    const long long left = end - pos;
+    const int lt1 = (ti - lt <= left) ? ti : lt + static_cast<int>(left);
+    s.i = i;
+    s.j = j;
+    s.lt0 = lt;
+    s.lt1 = lt1;
+    s.L = L;
+    s.ti = ti;
+    pos += lt1 - lt;
+    lt = lt1;
+    if (lt == ti && pos < end) {
+      lt = 0;
+      if (++j == g) {
+        j = 0;
+        do {
+          ++i;
+          L = (i < b) ? __ldg(lens + i) : 0;
+          ti = (i < b) ? seq_tiles(L, cap, T) : 0;
+        } while (i < b && ti == 0);
+      }
+    }
+    return true;
+  }
+};
+
+}  // namespace gqa

@@ -1,0 +1,42 @@
+// gqa_internal.h - host-side interface between the C-ABI layer and the
+// kernel translation units (not installed, not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+// Arguments of one decode-attention launch, already validated by the ABI.
+struct DecodeLaunch {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int* seq_lens;
+  int b, h, g, d, cap, dtype;
+  float scale_log2;      // scale * log2(e): logits are kept in base 2
+  void* out;
+  float* part_o;         // [slots, r, d] unnormalised partial outputs
+  float* part_ml;        // [slots, r, 2] running max (base 2) and sum
+  unsigned int* status;  // device status word
+  long long budget;      // wait limit in SM cycles
+  int nc;                // persistent CTAs
+  cudaStream_t stream;
+};
+
+// CUDA-core kernel (fp32, and bf16 with d = 64)
+bool simt_supported(int dtype, int d, int r);
+int simt_tile(int dtype, int d);
+int simt_ctas_per_sm(int dtype, int d, int r);
+cudaError_t launch_decode_simt(const DecodeLaunch& a);
+
+// tcgen05 tensor-core kernel (bf16, d = 128)
+bool tc_supported(int dtype, int d, int r);
+int tc_tile();
+int tc_ctas_per_sm(int r);
+cudaError_t launch_decode_tc(const DecodeLaunch& a);
+
+// log-sum-exp merge of the partials of units split across CTAs
+cudaError_t launch_combine(const DecodeLaunch& a, int tile);
+
+}  // namespace gqa

@@ -1,0 +1,152 @@
+/*
+ * gqa.h - C ABI of libgqa.so: one incremental-decoding attention step over a
+ * KV cache with grouped key/value heads, for NVIDIA GB300 (sm_103a).
+ *
+ * h query heads share g KV heads (g = h is multi-head attention, g = 1 is
+ * multi-query attention, h must be divisible by g).  Query head a reads KV
+ * head a / (h / g): the query heads of one KV head form a contiguous block.
+ *
+ * Sources (page title, then section):
+ *   "[논문 리뷰] Fast Transformer Decoding: One Write-Head is All You Need"
+ *       (velog review of Shazeer 2019): §2.4 Multi-head Attention
+ *       (Incremental) and §3 Multi Query Attention give the step: concat the
+ *       new K/V row on the position axis, logits "bhk,bhmk->bhm" (or
+ *       "bhk,bmk->bhm" with one KV head), softmax over positions, output
+ *       "bhm,bhmv->bhv" (or "bhm,bmv->bhv").
+ *   "クエリヘッドはそのまま、キー・バリューヘッドだけ減らす" (ttlab lesson
+ *       r-tf2-gqa): the g knob between MHA and MQA, the rule that h must be
+ *       divisible by g, contiguous grouping of query heads.
+ *   "한 번 한 계산은 다시 하지 않기" (albangk notes 05-faster-repetition):
+ *       the per-layer decode order (push K, push V, then attend).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers (memory the GPU can address,
+ *     e.g. from cudaMalloc or torch), row-major and contiguous, 16-byte
+ *     aligned.  The caller owns every buffer; the library never frees one.
+ *   - seq_lens is a device array of b int32: L_i, the number of attended
+ *     positions of sequence i AFTER the new token is appended.  Append writes
+ *     row L_i - 1; attention reads rows [0, L_i).  Neither call changes
+ *     seq_lens: the caller advances it once per decode step (it is shared by
+ *     all layers).  A value outside [1, cap] is a device-side error: the call
+ *     skips that sequence (writes nothing for it) and sets
+ *     GQA_DEV_BAD_SEQ_LEN in the device status word.
+ *   - dtype is GQA_F32 or GQA_BF16 and applies to every tensor of the call
+ *     (q, caches, new rows, out).  Arithmetic is fp32 for both.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous on it: arguments the host can check are checked
+ *     before any launch and reported by the return code; errors only the
+ *     device can see go to the device status word (gqa_device_status).
+ *     Kernels never trap and every wait inside them is bounded.
+ *   - Calls that overlap on the GPU (different streams) must not share
+ *     output buffers.  gqa_decode_attn keeps one split workspace per
+ *     (device, stream), grown on demand with cudaMalloc (so the first call
+ *     with a new largest size on a stream must not be made during stream
+ *     capture).
+ */
+#ifndef GQA_H
+#define GQA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types (the `dtype` argument) */
+#define GQA_F32  0
+#define GQA_BF16 1
+
+/* return codes */
+#define GQA_OK               0
+#define GQA_ERR_NULL        -1  /* a required pointer is NULL */
+#define GQA_ERR_SHAPE       -2  /* b, h, g, d_k, d_v < 1; cap < 1; h % g != 0;
+                                   sizes whose index range exceeds int32 */
+#define GQA_ERR_DTYPE       -3  /* dtype is neither GQA_F32 nor GQA_BF16 */
+#define GQA_ERR_ALIGN       -4  /* a tensor pointer is not 16-byte aligned */
+#define GQA_ERR_UNSUPPORTED -5  /* a shape this build has no kernel for
+                                   (d_k != d_v, head dim not 64/128, too many
+                                   query heads per KV head, b > 65535) */
+#define GQA_ERR_CUDA        -6  /* a CUDA runtime call failed */
+#define GQA_ERR_DEVICE      -7  /* current device is not sm_103 */
+
+/* bits of the device status word */
+#define GQA_DEV_BAD_SEQ_LEN  1u /* some seq_lens[i] was outside [1, cap] */
+#define GQA_DEV_WAIT_TIMEOUT 2u /* a bounded in-kernel wait gave up */
+
+/*
+ * gqa_kv_append - write the new token's K and V rows into the caches.
+ *
+ * The concat on the position axis of §2.4 / §3 ("new_K = concat(prev_K,
+ * k_new)"), and kCache.push / vCache.push of the decode notes, done in place:
+ *     k_cache[i, j, L_i - 1, :] = k_new[i, j, :]
+ *     v_cache[i, j, L_i - 1, :] = v_new[i, j, :]
+ * for every sequence i < b and KV head j < g.  The copy is bit-exact and
+ * touches no other row.
+ *
+ *   k_new    [b, g, d_k]        v_new    [b, g, d_v]          (read)
+ *   k_cache  [b, g, cap, d_k]   v_cache  [b, g, cap, d_v]     (written)
+ *   seq_lens [b] int32, post-append lengths (read)
+ *
+ * Requires d_k * elt and d_v * elt to be multiples of 16 bytes.
+ * Returns GQA_OK or an error code (nothing is launched on error).
+ */
+int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache,
+                  void* v_cache, const int32_t* seq_lens, int b, int g,
+                  int d_k, int d_v, int cap, int dtype, void* stream);
+
+/*
+ * gqa_decode_attn - attention of one new query per head over the cache.
+ *
+ * For every sequence i and query head a, with r = h / g and j = a / r:
+ *     s[p]       = scale * sum_c q[i, a, c] * k_cache[i, j, p, c],  p < L_i
+ *     w          = softmax(s)      (over p < L_i)
+ *     out[i,a,:] = sum_p w[p] * v_cache[i, j, p, :]
+ * ("bhk,bhmk->bhm", softmax, "bhm,bhmv->bhv" of §2.4 with the KV-head axis
+ * reduced to g; scale = 1 is the pages' literal form).  Run it after
+ * gqa_kv_append of the same step, on the same stream.
+ *
+ *   q        [b, h, d_k]                       (read)
+ *   k_cache  [b, g, cap, d_k], v_cache [b, g, cap, d_v]   (read)
+ *   seq_lens [b] int32                          (read)
+ *   out      [b, h, d_v], same dtype as q       (written; rows of a sequence
+ *                                                with a bad length are left
+ *                                                as they were)
+ *
+ * Rows p >= L_i of the caches are never used in the result, whatever they
+ * hold.  fp32 accumulation; bf16 output is rounded to nearest even.
+ * Supported: d_k == d_v in {64, 128}; bf16 with d = 128 and h / g <= 32
+ * (tensor-core kernel); fp32 with h / g <= 16 and bf16 with d = 64 and
+ * h / g <= 8 (CUDA-core kernel).  b <= 65535.
+ * Returns GQA_OK or an error code (nothing is launched on error).
+ */
+int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* seq_lens, int b, int h, int g, int d_k,
+                    int d_v, float scale, void* out, int cap, int dtype,
+                    void* stream);
+
+/*
+ * gqa_device_status - read and clear the device status word of the current
+ * device.  Synchronizes `stream` first, so the word covers every call queued
+ * on it before.  *bits_out receives an OR of GQA_DEV_* bits (0 = clean).
+ */
+int gqa_device_status(void* stream, uint32_t* bits_out);
+
+/*
+ * gqa_selftest_wait_timeout - launch one small kernel whose single mbarrier
+ * wait can never complete, with a limit of `budget_cycles` SM clock cycles,
+ * to exercise the bounded-wait error path: afterwards gqa_device_status
+ * reports GQA_DEV_WAIT_TIMEOUT.  Nothing else is touched.
+ */
+int gqa_selftest_wait_timeout(long long budget_cycles, void* stream);
+
+/* Name of a return code, for messages. */
+const char* gqa_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H */

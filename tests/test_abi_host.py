@@ -1,0 +1,106 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/gqa.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa.h")
+
+
+def _lib():
+    from gqa_kv_cache_append_gb300 import build
+    build.build()
+    from gqa_kv_cache_append_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gqa_kv_append", "gqa_decode_attn", "gqa_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    b = _lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", b.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, flags=re.M))
+    for n in declared_functions():
+        assert n in exported, n
+        assert n in b.SIGNATURES, n
+        getattr(b.lib, n)
+
+
+def test_status_strings_and_version():
+    b = _lib()
+    assert b.status_string(0) == "GQA_OK"
+    assert b.status_string(-2) == "GQA_ERR_SHAPE"
+    assert b.gqa_version() >= 100
+
+
+A = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+def _attn(lib_, **kw):
+    args = dict(q=A, k=A, v=A, lens=A, b=2, h=8, g=2, dk=128, dv=128, scale=0.1,
+                out=A, cap=64, dtype=1)
+    args.update(kw)
+    return lib_.lib.gqa_decode_attn(args["q"], args["k"], args["v"], args["lens"], args["b"],
+                                 args["h"], args["g"], args["dk"], args["dv"],
+                                 args["scale"], args["out"], args["cap"], args["dtype"],
+                                 None)
+
+
+def _app(lib_, **kw):
+    args = dict(kn=A, vn=A, k=A, v=A, lens=A, b=2, g=2, dk=128, dv=128, cap=64, dtype=1)
+    args.update(kw)
+    return lib_.lib.gqa_kv_append(args["kn"], args["vn"], args["k"], args["v"], args["lens"],
+                               args["b"], args["g"], args["dk"], args["dv"], args["cap"],
+                               args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), -1), (dict(out=0), -1), (dict(lens=0), -1),
+    (dict(dtype=2), -3), (dict(dtype=-1), -3),
+    (dict(h=6, g=4), -2), (dict(b=0), -2), (dict(g=0), -2), (dict(cap=0), -2),
+    (dict(dk=0), -2), (dict(b=40000, g=8, h=8, cap=8000), -2),
+    (dict(q=A + 8), -4), (dict(k=A + 2), -4), (dict(out=A + 4), -4), (dict(lens=A + 2), -4),
+    (dict(dk=128, dv=64), -5), (dict(dk=96, dv=96), -5), (dict(h=64, g=1), -5),
+    (dict(dtype=0, h=34, g=1), -5), (dict(dtype=1, dk=64, dv=64, h=16, g=1), -5),
+])
+def test_decode_attn_host_checks(kw, code):
+    assert _attn(_lib(), **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kn=0), -1), (dict(lens=0), -1), (dict(dtype=7), -3),
+    (dict(b=0), -2), (dict(cap=0), -2), (dict(dv=0), -2),
+    (dict(dk=4, dtype=1), -5), (dict(k=A + 4), -4),
+])
+def test_kv_append_host_checks(kw, code):
+    assert _app(_lib(), **kw) == code
+
+
+def test_null_status_pointer():
+    b = _lib()
+    assert b.lib.gqa_device_status(None, None) == -1
+
+
+def test_valid_arguments_without_a_gpu_report_a_cuda_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    b = _lib()
+    assert _attn(b) in (-6, -7)
+    assert _app(b) in (-6, -7)

@@ -1,0 +1,165 @@
+"""Decode attention through the C ABI against the float64 oracle on the same
+inputs (fp32: max-abs 1e-5; bf16 with fp32 accumulation: 2e-2 + 1e-2 |ref|).
+
+Cases span several tiles and a ragged tail: lengths of 1, tile - 1, tile,
+tile + 1, ragged batches, units split across many CTAs and units held by one,
+MHA (g = h), MQA (g = 1), r = 7 (not a power of two), NaN in the padding rows,
+a peaked softmax, and the error paths (device status word, bounded wait)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_kv_cache_append_gb300.inputs import DecodeConfig, make_layer
+from tests.util import assert_close, bits, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _b():
+    from gqa_kv_cache_append_gb300 import binding
+    return binding
+
+
+def run_step(cfg: DecodeConfig, lens, pad_fill=None, layer=0, check=True):
+    """Append + attend on the GPU, oracle on the same host inputs; returns the
+    max error."""
+    B = _b()
+    x = make_layer(cfg, layer, "cpu", lens=np.asarray(lens, dtype=np.int32), pad_fill=pad_fill)
+    d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    out = torch.full((cfg.b, cfg.h, cfg.d), 3.0, dtype=cfg.torch_dtype, device="cuda")
+    B.decode_step(d["q"], d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], d["seq_lens"],
+                  cfg.g, cfg.scale, out)
+    assert B.gqa_device_status() == 0
+    tag = to_np(x["q"])[1]
+    args = [to_np(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
+    if pad_fill is not None:
+        # the oracle reads no row >= L_i either; hand it finite padding so the
+        # comparison does not depend on that
+        args[1] = np.where(np.isfinite(oracle.widen(args[1], tag)), args[1], 0).astype(args[1].dtype)
+        args[2] = np.where(np.isfinite(oracle.widen(args[2], tag)), args[2], 0).astype(args[2].dtype)
+    ref, kc, vc = oracle.decode_step(*args, np.asarray(lens), cfg.g, cfg.scale, dtype=tag)
+    got = oracle.widen(to_np(out)[0], tag)
+    if pad_fill is None:
+        assert np.array_equal(bits(d["k_cache"]), kc) and np.array_equal(bits(d["v_cache"]), vc)
+    return assert_close(got, ref, tag, cfg.name) if check else (got, ref)
+
+
+def cfg_of(dtype, b, h, g, d, cap, seed=0, kind="plain"):
+    return DecodeConfig(f"{dtype}_b{b}_h{h}_g{g}_d{d}_c{cap}", 1, b, h, g, d, cap, dtype,
+                        1.0 / math.sqrt(d), 100 + seed, kind=kind)
+
+
+# ---- CUDA-core kernel: fp32 (tile 64 at d=64, 32 at d=128), bf16 d=64 (tile 128)
+@pytest.mark.parametrize("b,h,g,d,cap,lens", [
+    (1, 8, 1, 64, 256, [256]),                  # the fp32 MQA workload shape
+    (2, 8, 2, 64, 200, [1, 200]),
+    (3, 6, 3, 64, 130, [63, 64, 65]),
+    (2, 16, 1, 64, 300, [129, 300]),            # r = 16
+    (2, 12, 4, 128, 100, [31, 33]),             # fp32 d=128, tile 32
+    (4, 5, 5, 128, 97, [97, 1, 50, 32]),        # MHA
+])
+def test_simt_fp32(b, h, g, d, cap, lens):
+    run_step(cfg_of("f32", b, h, g, d, cap, seed=b + h), lens)
+
+
+@pytest.mark.parametrize("b,h,g,cap,lens", [
+    (2, 8, 1, 300, [300, 127]), (3, 4, 4, 260, [128, 129, 1]), (2, 14, 2, 513, [513, 200]),
+])
+def test_simt_bf16_d64(b, h, g, cap, lens):
+    run_step(cfg_of("bf16", b, h, g, 64, cap, seed=cap), lens)
+
+
+# ---- tensor-core kernel: bf16 d=128, tile 128, r padded to 16 or 32
+@pytest.mark.parametrize("b,h,g,cap,lens", [
+    (1, 8, 1, 1, [1]),
+    (1, 8, 8, 127, [127]),                      # MHA, one partial tile
+    (2, 16, 2, 128, [128, 1]),
+    (2, 16, 2, 129, [129, 2]),
+    (1, 32, 1, 1000, [1000]),                   # MQA, r = 32
+    (2, 28, 4, 700, [700, 385]),                # r = 7
+    (3, 64, 8, 300, [300, 256, 255]),           # r = 8
+    (2, 48, 2, 257, [257, 129]),                # r = 24 -> 32 columns
+    (4, 17, 1, 200, [200, 199, 131, 5]),        # r = 17
+])
+def test_tc_bf16(b, h, g, cap, lens):
+    run_step(cfg_of("bf16", b, h, g, 128, cap, seed=b * cap), lens)
+
+
+def test_tc_many_splits_long_sequence():
+    # one unit of 40 tiles spread over many CTAs: exercises the combine
+    run_step(cfg_of("bf16", 1, 8, 1, 128, 5000, seed=3), [5000])
+
+
+def test_tc_ragged_batch_with_nan_padding():
+    lens = [1, 127, 128, 129, 1000, 2049, 3, 700]
+    run_step(cfg_of("bf16", 8, 28, 4, 128, 2100, seed=9), lens, pad_fill=float("nan"))
+
+
+def test_simt_ragged_batch_with_nan_padding():
+    lens = [1, 63, 64, 65, 300]
+    run_step(cfg_of("f32", 5, 8, 2, 64, 320, seed=4), lens, pad_fill=float("nan"))
+
+
+def test_tc_peaked_softmax():
+    cfg = DecodeConfig("peaked", 1, 4, 32, 1, 128, 3000, "bf16", 1 / math.sqrt(128), 77,
+                       kind="boost")
+    run_step(cfg, [3000, 2999, 1500, 64])
+
+
+def test_results_are_deterministic():
+    B = _b()
+    cfg = cfg_of("bf16", 4, 32, 4, 128, 2000, seed=1)
+    x = make_layer(cfg, 0, "cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.empty((cfg.b, cfg.h, cfg.d), dtype=torch.bfloat16, device="cuda")
+        B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.h,
+                          cfg.g, 128, 128, cfg.scale, out)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_bad_length_is_reported_and_other_rows_are_right():
+    B = _b()
+    cfg = cfg_of("bf16", 3, 16, 2, 128, 300, seed=2)
+    x = make_layer(cfg, 0, "cpu", lens=np.array([300, 300, 300], dtype=np.int32))
+    d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    lens = torch.tensor([300, 301, 0], dtype=torch.int32, device="cuda")
+    sentinel = torch.full((cfg.b, cfg.h, cfg.d), 5.0, dtype=torch.bfloat16, device="cuda")
+    B.gqa_decode_attn(d["q"], d["k_cache"], d["v_cache"], lens, cfg.b, cfg.h, cfg.g, 128, 128,
+                      cfg.scale, sentinel)
+    assert B.gqa_device_status() == B.GQA_DEV_BAD_SEQ_LEN
+    assert torch.all(sentinel[1:] == 5.0)
+    args = [to_np(x[k])[0] for k in ("q", "k_cache", "v_cache")]
+    ref = oracle.grouped_decode_attention(args[0][:1], args[1][:1], args[2][:1], [300], cfg.g,
+                                          cfg.scale, dtype="bf16")
+    assert_close(oracle.widen(to_np(sentinel[:1])[0], "bf16"), ref, "bf16")
+
+
+def test_bounded_wait_reports_timeout():
+    B = _b()
+    assert B.gqa_device_status() == 0
+    B.gqa_selftest_wait_timeout(1 << 20)
+    assert B.gqa_device_status() == B.GQA_DEV_WAIT_TIMEOUT
+    assert B.gqa_device_status() == 0
+
+
+def test_error_codes_reach_python():
+    B = _b()
+    q = torch.zeros((1, 6, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 4, 8, 128), dtype=torch.bfloat16, device="cuda")
+    lens = torch.ones(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(B.GqaError) as e:
+        B.gqa_decode_attn(q, k, k, lens, 1, 6, 4, 128, 128, 1.0, out)
+    assert e.value.code == B.GQA_ERR_SHAPE
+    with pytest.raises(B.GqaError) as e:
+        B.gqa_decode_attn(q.half(), k.half(), k.half(), lens, 1, 6, 2, 128, 128, 1.0, out.half())
+    assert e.value.code == B.GQA_ERR_DTYPE
+    raw = torch.zeros(1 * 6 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.GqaError) as e:
+        B.gqa_decode_attn(raw[1:], k, k, lens, 1, 6, 2, 128, 128, 1.0, out)
+    assert e.value.code == B.GQA_ERR_ALIGN
