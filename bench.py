@@ -241,6 +241,8 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
     base = workload(args.workload)
+    if args.layers:
+        base = dataclasses.replace(base, layers=min(args.layers, base.layers))
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
     lens = seq_lens_for(cfg)
     layers = [make_layer(cfg, l, dev) for l in range(cfg.layers)]
@@ -433,6 +435,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (small profiling cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed steps
     rank, local_rank, world = dist_env()

@@ -60,12 +60,15 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
 // unnormalised outputs O_c of the same softmax over disjoint position ranges:
 //     M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,
 // which is the softmax-weighted sum over the whole range.  Units covered by
-// one CTA were written directly by the decode kernel and are skipped.
+// one CTA were written directly by the decode kernel and are skipped.  This
+// kernel (one CTA per unit) also reports sequences whose length is outside
+// [1, cap] on the device status word.
 // ---------------------------------------------------------------------------
 template <typename DT>
 __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g, int cap,
                                int d, int tile, int nc, const float* __restrict__ part_o,
-                               const float* __restrict__ part_ml, DT* __restrict__ out) {
+                               const float* __restrict__ part_ml, DT* __restrict__ out,
+                               unsigned int* status) {
   __shared__ long long s_u0, s_W;
   __shared__ int s_ti;
   const int u = blockIdx.x;
@@ -86,7 +89,10 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
       before += __shfl_xor_sync(0xffffffffu, before, o);
     }
     if (lane == 0) {
-      const int ti = seq_tiles(__ldg(lens + i), cap, tile);
+      const int Li = __ldg(lens + i);
+      const int ti = seq_tiles(Li, cap, tile);
+      // one report per bad sequence; its output rows are left untouched
+      if (ti == 0 && j == 0) atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
       s_ti = ti;
       s_u0 = before * g + static_cast<long long>(j) * ti;
       s_W = all * g;
@@ -359,11 +365,11 @@ cudaError_t launch_combine(const DecodeLaunch& a, int tile) {
   if (a.dtype == GQA_BF16)
     combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(units), 128, 0, a.stream>>>(
         a.seq_lens, a.b, a.h, a.g, a.cap, a.d, tile, a.nc, a.part_o, a.part_ml,
-        static_cast<__nv_bfloat16*>(a.out));
+        static_cast<__nv_bfloat16*>(a.out), a.status);
   else
     combine_kernel<float><<<static_cast<unsigned>(units), 128, 0, a.stream>>>(
         a.seq_lens, a.b, a.h, a.g, a.cap, a.d, tile, a.nc, a.part_o, a.part_ml,
-        static_cast<float*>(a.out));
+        static_cast<float*>(a.out), a.status);
   return cudaGetLastError();
 }
 
