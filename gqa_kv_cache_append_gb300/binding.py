@@ -26,6 +26,7 @@ GQA_ERR_ALIGN = -4
 GQA_ERR_UNSUPPORTED = -5
 GQA_ERR_CUDA = -6
 GQA_ERR_DEVICE = -7
+GQA_ERR_SCRATCH_LIMIT = -8
 
 GQA_DEV_BAD_SEQ_LEN = 1
 GQA_DEV_WAIT_TIMEOUT = 2
@@ -35,6 +36,8 @@ _VP, _I, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longl
 SIGNATURES = {
     "gqa_kv_append": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
     "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I, _VP]),
+    "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I,
+                                     _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -116,6 +119,21 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
     if cap is None:
         cap = k_cache.shape[2]
     _check("gqa_decode_attn", lib.gqa_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
+        _dtype(q, dtype), _stream(stream)))
+
+
+def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
+                            out, cap=None, dtype=None, stream=None) -> None:
+    """gqa_decode_attn for callers that cannot allocate device memory: the
+    split partials live in the library's fixed 4 MiB device array instead of
+    a cudaMalloc'd workspace.  Calls share that array, so calls that overlap
+    on the GPU race; make the first call on a device before any stream
+    capture (it looks up the array's device address)."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_decode_attn_noalloc", lib.gqa_decode_attn_noalloc(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(h),
         int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
         _dtype(q, dtype), _stream(stream)))

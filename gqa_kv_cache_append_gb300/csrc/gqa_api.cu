@@ -242,6 +242,7 @@ const char* gqa_status_string(int s) {
     case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
     case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
     case GQA_ERR_DEVICE: return "GQA_ERR_DEVICE";
+    case GQA_ERR_SCRATCH_LIMIT: return "GQA_ERR_SCRATCH_LIMIT";
     default: return "GQA_ERR_UNKNOWN";
   }
 }
@@ -374,3 +375,122 @@ cudaError_t launch_combine(const DecodeLaunch& a, int tile) {
 }
 
 }  // namespace gqa
+
+// ---------------------------------------------------------------------------
+// gqa_decode_attn_noalloc: the same decode, with the split partials in a
+// fixed device array instead of a cudaMalloc'd workspace, for callers that
+// cannot allocate device memory (see include/gqa.h).
+// ---------------------------------------------------------------------------
+namespace gqa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
+
+// Every GPU that loads the library holds this array until the process exits.
+// Host code must not use its name as an address: the device address comes
+// from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  bool ready;
+  int num_sms;
+  unsigned int* status;
+  unsigned char* scratch;
+};
+
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];  // zero-initialised, no heap
+std::mutex g_noalloc_mu;
+
+// One-time set-up per device, run with that device current: check the
+// architecture and look up the device addresses of the scratch array and of
+// the status word.
+int noalloc_setup(NoAllocDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return GQA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocDevice& nd = g_noalloc_devices[dev];
+  if (!nd.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    if (major != 10 || minor != 3) return GQA_ERR_DEVICE;
+    void* scratch = nullptr;
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess ||
+        cudaGetSymbolAddress(&status, g_status_word) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    nd.num_sms = sms;
+    nd.scratch = static_cast<unsigned char*>(scratch);
+    nd.status = static_cast<unsigned int*>(status);
+    nd.ready = true;
+  }
+  *out = &nd;
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* seq_lens, int b, int h, int g, int d_k,
+                                       int d_v, float scale, void* out, int cap, int dtype,
+                                       void* stream) {
+  using namespace gqa;
+  if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (b < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0)
+    return GQA_ERR_SHAPE;
+  if (static_cast<long long>(b) * g * cap + 256 > 0x7FFFFFFFll ||
+      static_cast<long long>(b) * h > 0x7FFFFFFFll)
+    return GQA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return GQA_ERR_ALIGN;
+  const int r = h / g;
+  const int d = d_k;
+  if (d_k != d_v || b > 65535) return GQA_ERR_UNSUPPORTED;
+  const bool use_tc = tc_supported(dtype, d, r);
+  if (!use_tc && !simt_supported(dtype, d, r)) return GQA_ERR_UNSUPPORTED;
+  NoAllocDevice* nd = nullptr;
+  if (int e = noalloc_setup(&nd)) return e;
+
+  const int tile = use_tc ? tc_tile() : simt_tile(dtype, d);
+  const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(dtype, d, r);
+  const long long max_tiles = static_cast<long long>(b) * g * ((cap + tile - 1) / tile);
+  long long nc = static_cast<long long>(nd->num_sms) * per_sm;
+  if (nc > max_tiles) nc = max_tiles;
+  if (nc < 1) nc = 1;
+  const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
+  const size_t o_bytes = slots * r * d * sizeof(float);
+  const size_t ml_bytes = slots * r * 2 * sizeof(float);
+  if (o_bytes + ml_bytes > kNoAllocScratchBytes) return GQA_ERR_SCRATCH_LIMIT;
+
+  DecodeLaunch a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seq_lens = seq_lens;
+  a.b = b;
+  a.h = h;
+  a.g = g;
+  a.d = d;
+  a.cap = cap;
+  a.dtype = dtype;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.out = out;
+  a.part_o = reinterpret_cast<float*>(nd->scratch);
+  a.part_ml = reinterpret_cast<float*>(nd->scratch + o_bytes);
+  a.status = nd->status;
+  a.budget = kWaitBudget;
+  a.nc = static_cast<int>(nc);
+  a.stream = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e = use_tc ? launch_decode_tc(a) : launch_decode_simt(a);
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  e = launch_combine(a, tile);
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}

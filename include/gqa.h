@@ -68,6 +68,8 @@ extern "C" {
                                    query heads per KV head, b > 65535) */
 #define GQA_ERR_CUDA        -6  /* a CUDA runtime call failed */
 #define GQA_ERR_DEVICE      -7  /* current device is not sm_103 */
+#define GQA_ERR_SCRATCH_LIMIT -8 /* gqa_decode_attn_noalloc: the call needs more
+                                    scratch than its fixed device buffer holds */
 
 /* bits of the device status word */
 #define GQA_DEV_BAD_SEQ_LEN  1u /* some seq_lens[i] was outside [1, cap] */
@@ -138,6 +140,39 @@ int gqa_device_status(void* stream, uint32_t* bits_out);
  * reports GQA_DEV_WAIT_TIMEOUT.  Nothing else is touched.
  */
 int gqa_selftest_wait_timeout(long long budget_cycles, void* stream);
+
+/*
+ * gqa_decode_attn_noalloc - gqa_decode_attn without any device allocation.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot call cudaMalloc: serving engines that hand all free device memory
+ * to their own KV-cache pool up front (so a later cudaMalloc fails or eats
+ * into the pool), and latency-critical decode loops that must not take the
+ * device-wide synchronisation cudaMalloc / cudaFree imply.  gqa_decode_attn
+ * grows its split workspace with cudaMalloc; this variant instead keeps the
+ * split partials in one fixed, file-scope device array of 4 MiB that every
+ * GPU which loads libgqa.so holds until the process exits.
+ *
+ * Arguments, layouts, results and error codes are those of gqa_decode_attn,
+ * and the two give the same output.  The caller still passes every input
+ * and output buffer.  Limit: a call needs (b*g + C) * (h/g) * (d_v + 2) * 4
+ * bytes of scratch, C being the number of CTAs (at most the SM count, 152 on
+ * GB300); a larger call returns GQA_ERR_SCRATCH_LIMIT and launches nothing.
+ * (The Llama-3-70B-shaped layer, b=32 h=64 g=8 d=128, needs 1.7 MB.)
+ *
+ * The first call on a device does a one-time set-up with that device current
+ * (it looks up the device address of the array); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents; nothing in it needs to start at zero (each call
+ * writes every partial it later reads).  Calls that overlap on the GPU (on
+ * different streams, or from different threads) race on the array and must
+ * be serialised by the caller.  No cudaMalloc, cudaFree or other allocating
+ * routine is called.
+ */
+int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* seq_lens, int b, int h, int g, int d_k,
+                            int d_v, float scale, void* out, int cap, int dtype,
+                            void* stream);
 
 /* Name of a return code, for messages. */
 const char* gqa_status_string(int status);
