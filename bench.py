@@ -241,24 +241,42 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
     base = workload(args.workload)
+    if args.g:
+        base = dataclasses.replace(base, g=args.g)
     if args.layers:
         base = dataclasses.replace(base, layers=min(args.layers, base.layers))
+    lens = seq_lens_for(base)
+    # a workload whose layers all fit in L2 is rotated through independent
+    # replicas (extra layers of the same shape) until one step streams at
+    # least 4x the L2 size, so every step reads K/V from HBM
+    from gqa_kv_cache_append_gb300.inputs import layer_bytes as _lb
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_layer = _lb(base, lens)
+    if base.layers * per_layer < 4 * l2 and not args.layers:
+        base = dataclasses.replace(base, layers=-(-4 * l2 // per_layer))
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
-    lens = seq_lens_for(cfg)
     layers = [make_layer(cfg, l, dev) for l in range(cfg.layers)]
     outs = [torch.empty((cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device=dev)
             for _ in range(cfg.layers)]
     stream = torch.cuda.current_stream(dev)
     sb = step_bytes(cfg, lens)
 
-    def step(ev=None):
-        for l, x in enumerate(layers):
+    def layer_call(l, x):
+        if args.separate:
             B.gqa_kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"],
                             cfg.b, cfg.g, cfg.d, cfg.d, stream=stream)
-            if ev is not None:
-                ev[l][0].record(stream)
             B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
                               cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l], stream=stream)
+        else:
+            B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                              x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale,
+                              outs[l], stream=stream)
+
+    def step(ev=None):
+        for l, x in enumerate(layers):
+            if ev is not None:
+                ev[l][0].record(stream)
+            layer_call(l, x)
             if ev is not None:
                 ev[l][1].record(stream)
 
@@ -303,10 +321,7 @@ def run_ours(args, rank, local_rank, world):
             x["q"].copy_(hq[l], non_blocking=True)
             x["k_new"].copy_(hk[l], non_blocking=True)
             x["v_new"].copy_(hv[l], non_blocking=True)
-            B.gqa_kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"],
-                            cfg.b, cfg.g, cfg.d, cfg.d, stream=stream)
-            B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
-                              cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l], stream=stream)
+            layer_call(l, x)
             ho[l].copy_(outs[l], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -327,10 +342,11 @@ def run_ours(args, rank, local_rank, world):
     if rank != 0:
         return None
     peaks = measured_peaks()
-    achieved = sb["attn_per_layer"] / (attn_avg_ms * 1e-3) / 1e9
+    call_bytes = sb["attn_per_layer"] + sb["append_per_layer"]
+    achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
     traffic = profiled_traffic(src, args.workload)
-    launches_per_step = 3 * cfg.layers   # append, attention, combine per layer
+    launches_per_step = (2 if args.separate else 1) * cfg.layers
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -350,22 +366,23 @@ def run_ours(args, rank, local_rank, world):
             "d_head": cfg.d, "seq_len": int(np.max(lens)), "cap": cfg.cap,
             "sum_seq_lens": int(np.sum(lens)),
             "l2": "inputs larger than L2: every step streams all layers' K/V "
-                  f"({sb['step'] / 2**30:.1f} GiB)",
+                  f"({sb['step'] / 2**30:.2f} GiB, L2 {l2 / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
         },
         "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
-        "attn_gbs_per_gpu": round(achieved, 2),
+        "layer_call_gbs_per_gpu": round(achieved, 2),
         "pct_of_nominal_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "gqa_decode_attn (decode_tc_kernel + combine_kernel)",
+            "kernel": ("gqa_kv_append + gqa_decode_attn" if args.separate else "gqa_decode_step")
+                      + f" ({'decode_tc_kernel' if cfg.dtype == 'bf16' and cfg.d == 128 else 'decode_simt_kernel'})",
             "achieved": round(achieved, 2),
             "peak": peaks["hbm_gbs"],
             "peak_source": peaks["source"],
             "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": sb["attn_per_layer"],
+            "algorithmic_bytes_per_launch": call_bytes,
             "avg_launch_ms": round(attn_avg_ms, 5),
         },
         "e2e": {
@@ -435,6 +452,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--g", type=int, default=None, help="KV heads (for the g-knob sweep)")
+    ap.add_argument("--separate", action="store_true",
+                    help="time gqa_kv_append + gqa_decode_attn instead of gqa_decode_step")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small profiling cases)")
     args = ap.parse_args(argv)

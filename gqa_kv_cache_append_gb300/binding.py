@@ -38,6 +38,8 @@ SIGNATURES = {
     "gqa_decode_attn": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I, _VP]),
     "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I,
                                      _VP]),
+    "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I,
+                             _I, _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -124,6 +126,17 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
         _dtype(q, dtype), _stream(stream)))
 
 
+def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v,
+                    scale, out, cap=None, dtype=None, stream=None) -> None:
+    """Append k_new / v_new at row seq_lens[i] - 1 and attend, in one launch."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_decode_step", lib.gqa_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        int(b), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
+        _dtype(q, dtype), _stream(stream)))
+
+
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
                             out, cap=None, dtype=None, stream=None) -> None:
     """gqa_decode_attn for callers that cannot allocate device memory: the
@@ -156,10 +169,15 @@ def gqa_version() -> int:
 
 
 def decode_step(q, k_cache, v_cache, k_new, v_new, seq_lens, g, scale, out,
-                stream=None) -> None:
+                stream=None, fused=False) -> None:
     """One layer's decode step in the order of the decode notes: push the new
-    K/V rows, then attend (two C-ABI calls on the same stream)."""
+    K/V rows, then attend.  fused=False makes the two C-ABI calls
+    (gqa_kv_append, gqa_decode_attn); fused=True makes one gqa_decode_step."""
     b, h, d = q.shape
+    if fused:
+        gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d,
+                        v_cache.shape[-1], scale, out, stream=stream)
+        return
     gqa_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, b, g, d, v_new.shape[-1],
                   stream=stream)
     gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d, v_cache.shape[-1],

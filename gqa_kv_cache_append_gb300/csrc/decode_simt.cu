@@ -14,8 +14,11 @@
 //      warp sum;
 //   C  weighted sum of V rows into fp32 register accumulators ("bhm,bhmv->
 //      bhv"), rescaled by each tile's factor.
-// A segment's end writes the normalised output, or a partial for the
-// combine kernel when the unit is split across CTAs.
+// A segment's end writes the normalised output; a unit split across CTAs
+// writes a partial instead, and the CTA that finishes the unit last merges
+// the partials (log-sum-exp).  With k_new / v_new given, the KV append is
+// fused in: the CTA owning a unit's last tile patches row L_i - 1 of its
+// staged tile with the new token and writes that row to the cache.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -82,7 +85,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const DT* __restrict__ vc, const int* __restrict__ lens, int b, int h,
                        int g, int cap, float scale_log2, DT* __restrict__ out,
                        float* __restrict__ part_o, float* __restrict__ part_ml,
-                       unsigned int* status, long long budget) {
+                       int* __restrict__ counters, const uint4* __restrict__ k_new,
+                       const uint4* __restrict__ v_new, uint4* __restrict__ k_cache_w,
+                       uint4* __restrict__ v_cache_w, unsigned int* status, long long budget) {
   using C = SimtCfg<DT, D, RMAX>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -94,12 +99,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sA = sL + RMAX;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
+  int* last_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + C::STAGES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -108,12 +115,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  pdl_wait();  // inputs and the split workspace are read only after this
   if (threadIdx.x >= 32 && threadIdx.x < 32 + RMAX) {
     const int t = threadIdx.x - 32;
     sM[t] = -INFINITY;
     sL[t] = 0.f;
     sA[t] = 0.f;
   }
+  if (warp == 1 && blockIdx.x == 0) report_bad_lengths(lens, b, cap, status);
   __syncthreads();
 
   Walker w;
@@ -172,6 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n = 0;
     while (w.next(seg)) {
       const int a0 = seg.i * h + seg.j * r;  // first query head of the group
+      const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
+      // fused append: threads 0..CH-1 carry one 16-byte chunk of the new
+      // token's K and V rows to the unit's last tile
+      const bool append_here = k_new != nullptr && seg.lt1 == seg.ti;
+      uint4 knew = make_uint4(0u, 0u, 0u, 0u), vnew = knew;
+      if (append_here && ct < C::CH) {
+        knew = __ldg(k_new + unit * C::CH + ct);
+        vnew = __ldg(v_new + unit * C::CH + ct);
+      }
 #pragma unroll
       for (int t = 0; t < RMAX; ++t) {
         if (t < r) {
@@ -190,6 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   budget);
         const DT* sK = reinterpret_cast<const DT*>(sm + st * C::STAGE_BYTES);
         const DT* sV = sK + C::T * D;
+        if (append_here && lt == seg.ti - 1) {
+          // row L_i - 1 is the new token: use k_new / v_new there and store
+          // them into the cache (the append)
+          if (ok && ct < C::CH) {
+            const int rho = valid - 1;
+            reinterpret_cast<uint4*>(const_cast<DT*>(sK) + rho * D)[ct] = knew;
+            reinterpret_cast<uint4*>(const_cast<DT*>(sV) + rho * D)[ct] = vnew;
+            const size_t crow = unit * cap + (seg.L - 1);
+            k_cache_w[crow * C::CH + ct] = knew;
+            v_cache_w[crow * C::CH + ct] = vnew;
+          }
+          named_bar_sync(1, 128);
+        }
         // A: logits
 #pragma unroll 2
         for (int step = 0; step < C::T / (4 * C::PPW); ++step) {
@@ -306,6 +337,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (!whole) {
+        // the unit is split across CTAs: the last one to finish merges
+        long long c0, c1;
+        unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
+        const int np = unit_parts(c0, c1, w.W, w.nc);
+        if (counters != nullptr && arrive_last(counters, u, np, last_flag, ct == 0, 1, 128)) {
+          // merge the other CTAs' partials into this CTA's own (still in
+          // shared memory)
+          for (int idx = ct; idx < r * D; idx += 128) {
+            const int t = idx / D, dd = idx % D;
+            float o = sRed[(0 * RMAX + t) * D + dd] + sRed[(1 * RMAX + t) * D + dd] +
+                      sRed[(2 * RMAX + t) * D + dd] + sRed[(3 * RMAX + t) * D + dd];
+            float M = sM[t], den = sL[t];
+            for (long long c = c0; c <= c1; ++c) {
+              if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
+              const long long sl = (u + c) * r + t;
+              const float mc = __ldcg(part_ml + sl * 2), lc = __ldcg(part_ml + sl * 2 + 1);
+              const float oc = __ldcg(part_o + sl * D + dd);
+              const float mn = fmaxf(M, mc);
+              const float sa = ex2(M - mn), sb = ex2(mc - mn);
+              o = o * sa + oc * sb;
+              den = den * sa + lc * sb;
+              M = mn;
+            }
+            Elt<DT>::store(out + static_cast<size_t>(a0 + t) * D + dd, o / den);
+          }
+        }
+      }
       named_bar_sync(1, 128);
       if (ct < RMAX) {
         sM[ct] = -INFINITY;
@@ -325,11 +384,22 @@ cudaError_t launch_t(const DecodeLaunch& a) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<a.nc, kThreads, C::SMEM, a.stream>>>(
-      static_cast<const DT*>(a.q), static_cast<const DT*>(a.k_cache),
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nc);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(
+      &cfg, kern, static_cast<const DT*>(a.q), static_cast<const DT*>(a.k_cache),
       static_cast<const DT*>(a.v_cache), a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
-      static_cast<DT*>(a.out), a.part_o, a.part_ml, a.status, a.budget);
-  return cudaGetLastError();
+      static_cast<DT*>(a.out), a.part_o, a.part_ml, a.counters,
+      static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
+      static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget);
 }
 
 }  // namespace

@@ -24,11 +24,18 @@
 //              exchange), exp2, write P in the MMA's MN-major swizzled
 //              layout, then fold the previous tile's O into fp32 registers
 //              with its rescale factor.  Segment end: sum the per-thread
-//              softmax denominators and write the output or a partial.
+//              softmax denominators and write the output; a unit split
+//              across CTAs writes a partial instead, and the CTA that
+//              finishes the unit last merges the partials (log-sum-exp).
 //
 // Rows >= L_i of the last tile of a unit are masked out of S, and their V
 // rows are zeroed in shared memory before the O product reads them, so
 // whatever the cache holds there never reaches the result.
+//
+// With k_new / v_new given, the KV append of the step is fused in: the CTA
+// that owns a unit's last tile (the one holding row L_i - 1) puts the new
+// token's K and V into that row of its staged tile and writes them to the
+// cache, so one launch does append + attention.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,7 +61,8 @@ struct TcCfg {
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;   // float [2][4][NP]
   static constexpr int OFF_LRED = OFF_RED + 2 * 4 * NP * 4;  // float [4][NP]
-  static constexpr int OFF_BAR = OFF_LRED + 4 * NP * 4;
+  static constexpr int OFF_ALPHA = OFF_LRED + 4 * NP * 4;    // float [2][NP] rescale factors
+  static constexpr int OFF_BAR = OFF_ALPHA + 2 * NP * 4;
   static constexpr int NBAR = 3 * kStages + 2 * 7 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for 1024-B alignment
@@ -89,7 +97,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ lens,
                      int b, int h, int g, int cap, float scale_log2,
                      __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
-                     float* __restrict__ part_ml, unsigned int* status, long long budget) {
+                     float* __restrict__ part_ml, int* __restrict__ counters,
+                     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                     uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
+                     unsigned int* status, long long budget) {
   using C = TcCfg<NP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -97,14 +108,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_base = smem_u32(sm);
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
   float* lred = reinterpret_cast<float*>(sm + C::OFF_LRED);
+  float* alpha_sm = reinterpret_cast<float*>(sm + C::OFF_ALPHA);
   const uint32_t bar0 = s_base + C::OFF_BAR;
   auto BAR = [&](int k) -> uint32_t { return bar0 + 8u * k; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
+  int* last_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int k = 0; k < C::NBAR; ++k) {
       uint32_t cnt = 1;
@@ -122,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::NCOLS);
+  pdl_wait();  // everything above touched only this CTA's shared and tensor memory
+  if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, cap, status);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -195,16 +211,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    if (lane == 0) {
-      const uint32_t tS = tmem, tO = tmem + 2 * NP;
-      auto issue_o = [&](uint32_t m) {
-        const int st = m % kStages;
-        const uint32_t nb = m & 1;
-        bool ok = mbar_wait(BAR(B_P_READY + nb), (m >> 1) & 1, abort_flag, status, budget);
-        ok = ok && mbar_wait(BAR(B_FULL_V + st), (m / kStages) & 1, abort_flag, status, budget);
-        ok = ok &&
-             mbar_wait(BAR(B_O_FREE + nb), ((m >> 1) & 1) ^ 1, abort_flag, status, budget);
-        tc_fence_after();
+    // Lane 0 issues the MMAs.  With the append fused in, lanes 0-15 also
+    // carry the new token's K row (one 16-byte chunk each) from the segment
+    // start to the unit's last tile, where they patch it into the staged
+    // tile and write it to the cache.
+    const bool leader = lane == 0;
+    const uint32_t tS = tmem, tO = tmem + 2 * NP;
+    auto issue_o = [&](uint32_t m) {
+      const int st = m % kStages;
+      const uint32_t nb = m & 1;
+      bool ok = mbar_wait(BAR(B_P_READY + nb), (m >> 1) & 1, abort_flag, status, budget);
+      ok = ok && mbar_wait(BAR(B_FULL_V + st), (m / kStages) & 1, abort_flag, status, budget);
+      ok = ok && mbar_wait(BAR(B_O_FREE + nb), ((m >> 1) & 1) ^ 1, abort_flag, status, budget);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      if (leader) {
         if (ok) {
           const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
           const uint32_t pbase = s_base + C::OFF_P + nb * C::P_BYTES;
@@ -221,23 +242,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(BAR(B_O_FULL + nb));
         mma_commit(BAR(B_EMPTY + st));
-      };
-      uint32_t n = 0, k = 0, prev = 0;
-      bool have_prev = false;
-      while (w.next(seg)) {
-        const uint32_t qs = k & 1;
-        const bool qok = mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget);
-        const uint32_t qbase = s_base + C::OFF_Q + qs * C::Q_BYTES;
-        for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
-          const int st = n % kStages;
-          const uint32_t nb = n & 1;
-          bool ok = qok && mbar_wait(BAR(B_FULL_K + st), (n / kStages) & 1, abort_flag, status,
-                                     budget);
-          ok = ok &&
-               mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
-          tc_fence_after();
+      }
+      __syncwarp();
+    };
+    uint32_t n = 0, k = 0, prev = 0;
+    bool have_prev = false;
+    while (w.next(seg)) {
+      const uint32_t qs = k & 1;
+      const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
+      const bool append_here = k_new != nullptr && seg.lt1 == seg.ti;
+      uint4 knew = make_uint4(0u, 0u, 0u, 0u);
+      if (append_here && lane < 16) knew = __ldg(k_new + unit * 16 + lane);
+      const bool qok = __all_sync(
+          0xffffffffu, mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget));
+      const uint32_t qbase = s_base + C::OFF_Q + qs * C::Q_BYTES;
+      for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+        const int st = n % kStages;
+        const uint32_t nb = n & 1;
+        bool ok = qok && mbar_wait(BAR(B_FULL_K + st), (n / kStages) & 1, abort_flag, status,
+                                   budget);
+        ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
+        ok = __all_sync(0xffffffffu, ok);
+        const uint32_t kbase = s_base + st * C::KV_BYTES;
+        if (append_here && lt == seg.ti - 1) {
+          // row L_i - 1 of this tile is the new token: use k_new there, and
+          // store it into the cache (the append)
+          if (ok && lane < 16) {
+            const int rho = seg.L - 1 - lt * kT;
+            const uint32_t dst = kbase + (lane >> 3) * kBoxBytes + rho * 128 +
+                                 (((lane & 7) ^ (rho & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(knew.x),
+                         "r"(knew.y), "r"(knew.z), "r"(knew.w)
+                         : "memory");
+            k_cache_w[(unit * cap + seg.L - 1) * 16 + lane] = knew;
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (leader) {
           if (ok) {
-            const uint32_t kbase = s_base + st * C::KV_BYTES;
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               // A = K tile, K-major: 128 rows, 16 head-dim columns per step;
@@ -251,13 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(BAR(B_S_FULL + nb));
           if (lt == seg.lt1 - 1) mma_commit(BAR(B_Q_EMPTY + qs));
-          if (have_prev) issue_o(prev);
-          have_prev = true;
-          prev = n;
         }
-        ++k;
+        __syncwarp();
+        if (have_prev) issue_o(prev);
+        have_prev = true;
+        prev = n;
       }
-      if (have_prev) issue_o(prev);
+      ++k;
+    }
+    if (have_prev) issue_o(prev);
+    if (leader) {
       // every MMA must be finished before tensor memory is released
       mma_commit(BAR(B_DRAIN));
       const long long t0 = clock64();
@@ -273,16 +320,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const uint32_t tS = tmem + lane_off, tO = tmem + 2 * NP + lane_off;
 
-    float m[NP], l[NP], o[NP], alpha_prev[NP];
+    float m[NP], l[NP], o[NP];
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
       m[t] = -INFINITY;
       l[t] = 0.f;
       o[t] = 0.f;
-      alpha_prev[t] = 0.f;
     }
 
-    auto correct = [&](uint32_t mt, const float(&al)[NP]) {
+    // fold O of tile mt into the registers: o = o * alpha + O_tile.  The
+    // factors come from registers (al) or, for the previous tile, from
+    // shared memory (all threads hold the same factors; thread t stored
+    // head t's after the tile's max exchange)
+    auto correct = [&](uint32_t mt, const float* al) {
       const uint32_t nb = mt & 1;
       const bool ok = mbar_wait(BAR(B_O_FULL + nb), (mt >> 1) & 1, abort_flag, status, budget);
       float ov[NP];
@@ -308,6 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t n = 0;
     while (w.next(seg)) {
+      const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
+      // fused append: threads 0-15 carry the new token's V row, one chunk each
+      const bool append_here = v_new != nullptr && seg.lt1 == seg.ti;
+      uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
+      if (append_here && row < 16) vnew = __ldg(v_new + unit * 16 + row);
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         const uint32_t nb = n & 1;
         const int st = n % kStages;
@@ -341,25 +396,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float wm = warp_max(x[t]);
           if (lane == t) mine = wm;
         }
+        // head-major [NP][4 warps]: one 16-byte load per head afterwards
         float* rb = red + nb * 4 * NP;
-        if (lane < NP) rb[wq * NP + lane] = mine;
+        if (lane < NP) rb[lane * 4 + wq] = mine;
         named_bar_sync(1, 128);
-        float alpha[NP], p[NP];
+        // new running max, rescale factor and probabilities per head; x[t]
+        // becomes p[t].  Thread t keeps head t's factor (selected into a
+        // register, stored once after the loop) for this tile's correction.
+        float a_mine = 1.f;
 #pragma unroll
         for (int t = 0; t < NP; ++t) {
           if (t < r) {
-            const float tm =
-                fmaxf(fmaxf(rb[t], rb[NP + t]), fmaxf(rb[2 * NP + t], rb[3 * NP + t]));
-            const float mn = fmaxf(m[t], tm);
-            alpha[t] = ex2(m[t] - mn);
+            const float4 v = *reinterpret_cast<const float4*>(rb + 4 * t);
+            const float mn = fmaxf(m[t], fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            const float a = ex2(m[t] - mn);
             m[t] = mn;
-            p[t] = ex2(x[t] - mn);
-            l[t] = fmaf(l[t], alpha[t], p[t]);
+            x[t] = ex2(x[t] - mn);
+            l[t] = fmaf(l[t], a, x[t]);
+            a_mine = (row == t) ? a : a_mine;
           } else {
-            alpha[t] = 1.f;
-            p[t] = 0.f;
+            x[t] = 0.f;
           }
         }
+        if (row < NP) alpha_sm[nb * NP + row] = a_mine;
+        const float* p = x;
         // ---- P^T row `row` into the MN-major swizzled B operand ----
         {
           const uint32_t prow = s_base + C::OFF_P + nb * C::P_BYTES + row * (NP * 2);
@@ -377,12 +437,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
           }
         }
-        // ---- ragged last tile: zero the V rows past L_i ----
-        if (valid < kT) {
+        // ---- last tile of a unit: zero the V rows past L_i; with the
+        // append fused in, put v_new into row L_i - 1 and into the cache ----
+        const bool patch = append_here && lt == seg.ti - 1;
+        if (valid < kT || patch) {
           const bool vok =
               mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
+          const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
           if (vok && !live) {
-            const uint32_t vrow = s_base + st * C::KV_BYTES + 2 * kBoxBytes + row * 128;
+            const uint32_t vrow = vbase + row * 128;
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
@@ -392,15 +455,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                              "r"(0u)
                              : "memory");
           }
+          if (vok && patch && row < 16) {
+            const int rho = valid - 1;
+            const uint32_t dst =
+                vbase + (row >> 3) * kBoxBytes + rho * 128 + (((row & 7) ^ (rho & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(vnew.x),
+                         "r"(vnew.y), "r"(vnew.z), "r"(vnew.w)
+                         : "memory");
+            v_cache_w[(unit * cap + seg.L - 1) * 16 + row] = vnew;
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_P_READY + nb));
         // ---- fold the previous tile's O into the registers ----
-        if (lt > seg.lt0) correct(n - 1, alpha_prev);
-#pragma unroll
-        for (int t = 0; t < NP; ++t) alpha_prev[t] = alpha[t];
-        if (lt == seg.lt1 - 1) correct(n, alpha);
+        if (lt > seg.lt0) correct(n - 1, alpha_sm + ((n - 1) & 1) * NP);
+        if (lt == seg.lt1 - 1) {
+          named_bar_sync(1, 128);  // this tile's factors, written above, are visible
+          correct(n, alpha_sm + nb * NP);
+        }
       }
 
       // ---- segment end: softmax denominators, output or partial ----
@@ -415,21 +488,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
         const int a0 = seg.i * h + seg.j * r;
-        const size_t slot = static_cast<size_t>(seg.i * g + seg.j) + blockIdx.x;
+        const int u = seg.i * g + seg.j;
+        const size_t slot = static_cast<size_t>(u) + blockIdx.x;
+        // l[t] becomes the CTA-wide softmax denominator of head t
 #pragma unroll
-        for (int t = 0; t < NP; ++t) {
-          if (t < r) {
-            const float ltot = lred[t] + lred[NP + t] + lred[2 * NP + t] + lred[3 * NP + t];
-            if (whole) {
-              out[static_cast<size_t>(a0 + t) * kD + row] = __float2bfloat16_rn(o[t] / ltot);
-            } else {
+        for (int t = 0; t < NP; ++t)
+          l[t] = lred[t] + lred[NP + t] + lred[2 * NP + t] + lred[3 * NP + t];
+        if (whole) {
+#pragma unroll
+          for (int t = 0; t < NP; ++t)
+            if (t < r)
+              out[static_cast<size_t>(a0 + t) * kD + row] = __float2bfloat16_rn(o[t] / l[t]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < NP; ++t) {
+            if (t < r) {
               part_o[(slot * r + t) * kD + row] = o[t];
               if (row == 0) {
                 part_ml[(slot * r + t) * 2 + 0] = m[t];
-                part_ml[(slot * r + t) * 2 + 1] = ltot;
+                part_ml[(slot * r + t) * 2 + 1] = l[t];
               }
             }
           }
+          // the unit is split across CTAs: the one that finishes last merges
+          // the other partials into its own (still in registers)
+          long long c0, c1;
+          unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
+          const int np = unit_parts(c0, c1, w.W, w.nc);
+          if (counters != nullptr && arrive_last(counters, u, np, last_flag, row == 0, 1, 128)) {
+            for (long long c = c0; c <= c1; ++c) {
+              if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
+              // eight heads at a time: their loads go out together
+#pragma unroll
+              for (int t0 = 0; t0 < NP; t0 += 8) {
+                float mc[8], lc[8], oc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  if (t0 + e < r) {
+                    const long long sl = (u + c) * r + t0 + e;
+                    mc[e] = __ldcg(part_ml + sl * 2);
+                    lc[e] = __ldcg(part_ml + sl * 2 + 1);
+                    oc[e] = __ldcg(part_o + sl * kD + row);
+                  }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int t = t0 + e;
+                  if (t < r) {
+                    const float mn = fmaxf(m[t], mc[e]);
+                    const float sa = ex2(m[t] - mn), sb = ex2(mc[e] - mn);
+                    o[t] = o[t] * sa + oc[e] * sb;
+                    l[t] = l[t] * sa + lc[e] * sb;
+                    m[t] = mn;
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < NP; ++t)
+              if (t < r)
+                out[static_cast<size_t>(a0 + t) * kD + row] = __float2bfloat16_rn(o[t] / l[t]);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < NP; ++t) {
           m[t] = -INFINITY;
           l[t] = 0.f;
           o[t] = 0.f;
@@ -494,10 +616,21 @@ cudaError_t launch_np(const DecodeLaunch& a) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<a.nc, kThreads, C::SMEM, a.stream>>>(
-      mq, mk, mv, a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
-      static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.status, a.budget);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nc);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(
+      &cfg, kern, mq, mk, mv, a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
+      static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.counters,
+      static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
+      static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget);
 }
 
 }  // namespace

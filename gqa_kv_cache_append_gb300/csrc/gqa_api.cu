@@ -1,12 +1,13 @@
 // gqa_api.cu - the C ABI of libgqa.so (declared in include/gqa.h): argument
 // checks, kernel selection, the split workspace, the device status word, and
-// the small kernels (KV append, log-sum-exp combine, wait self-test).
+// the small kernels (KV append, wait self-test).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -55,33 +56,34 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp combine of the partials of one unit (sequence i, KV head j)
-// split across CTAs.  With per-CTA maxima m_c (base 2), sums l_c and
+// Log-sum-exp combine for launches with many more CTAs than units (a few
+// long sequences, e.g. one MQA head over 131k positions spread over 19
+// CTAs): the decode kernel then only writes partials, and this kernel merges
+// them with the whole GPU, one CTA per (unit, query head), one thread per
+// output column.  With per-CTA maxima m_c (base 2), sums l_c and
 // unnormalised outputs O_c of the same softmax over disjoint position ranges:
-//     M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,
-// which is the softmax-weighted sum over the whole range.  Units covered by
-// one CTA were written directly by the decode kernel and are skipped.  This
-// kernel (one CTA per unit) also reports sequences whose length is outside
-// [1, cap] on the device status word.
+//     M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+// Units held whole by one CTA were written by the decode kernel.
 // ---------------------------------------------------------------------------
 template <typename DT>
 __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g, int cap,
                                int d, int tile, int nc, const float* __restrict__ part_o,
-                               const float* __restrict__ part_ml, DT* __restrict__ out,
-                               unsigned int* status) {
+                               const float* __restrict__ part_ml, DT* __restrict__ out) {
   __shared__ long long s_u0, s_W;
   __shared__ int s_ti;
-  const int u = blockIdx.x;
-  const int i = u / g, j = u % g;
+  pdl_launch_dependents();
+  pdl_wait();  // the partials come from the decode kernel just before
   const int r = h / g;
+  const int u = blockIdx.x / r, t = blockIdx.x % r;
+  const int i = u / g, j = u % g;
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     long long before = 0, all = 0;
     for (int base = 0; base < b; base += 32) {
       const int idx = base + lane;
-      const int t = (idx < b) ? seq_tiles(__ldg(lens + idx), cap, tile) : 0;
-      all += t;
-      if (idx < i) before += t;
+      const int tt = (idx < b) ? seq_tiles(__ldg(lens + idx), cap, tile) : 0;
+      all += tt;
+      if (idx < i) before += tt;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -89,10 +91,7 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
       before += __shfl_xor_sync(0xffffffffu, before, o);
     }
     if (lane == 0) {
-      const int Li = __ldg(lens + i);
-      const int ti = seq_tiles(Li, cap, tile);
-      // one report per bad sequence; its output rows are left untouched
-      if (ti == 0 && j == 0) atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
+      const int ti = seq_tiles(__ldg(lens + i), cap, tile);
       s_ti = ti;
       s_u0 = before * g + static_cast<long long>(j) * ti;
       s_W = all * g;
@@ -101,39 +100,46 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
   __syncthreads();
   const int ti = s_ti;
   if (ti == 0) return;
-  const long long W = s_W, u0 = s_u0, u1 = u0 + ti;
-  const long long c0 = ((u0 + 1) * nc - 1) / W;
-  const long long c1 = (u1 * nc - 1) / W;
+  const long long W = s_W;
+  long long c0, c1;
+  unit_ctas(s_u0, s_u0 + ti, W, nc, c0, c1);
   if (c0 == c1) return;
-  // a CTA between c0 and c1 with an empty range (possible when W < nc)
-  // wrote no partial
-  auto empty_cta = [&](long long c) { return (c * W) / nc == ((c + 1) * W) / nc; };
-  for (int t = 0; t < r; ++t) {
-    float M = -INFINITY;
-    for (long long c = c0; c <= c1; ++c)
-      if (!empty_cta(c)) M = fmaxf(M, part_ml[((u + c) * r + t) * 2]);
-    float den = 0.f;
-    for (long long c = c0; c <= c1; ++c) {
-      if (empty_cta(c)) continue;
-      const float* ml = part_ml + ((u + c) * r + t) * 2;
-      den += exp2f(ml[0] - M) * ml[1];
+  const int col = threadIdx.x;
+  // pieces in batches of 16, every load of a batch issued before any use;
+  // batches merge online (running max M, sums num / den)
+  constexpr int kBatch = 16;
+  float M = -INFINITY, num = 0.f, den = 0.f;
+  for (long long cb = c0; cb <= c1; cb += kBatch) {
+    float mc[kBatch], lc[kBatch], oc[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const long long c = cb + k;
+      const bool use = c <= c1 && (W >= nc || !cta_empty(c, W, nc));
+      const long long sl = (u + c) * r + t;
+      mc[k] = use ? __ldg(part_ml + sl * 2) : -INFINITY;
+      lc[k] = use ? __ldg(part_ml + sl * 2 + 1) : 0.f;
+      oc[k] = use ? __ldg(part_o + sl * d + col) : 0.f;
     }
-    const float inv = 1.f / den;
-    for (int dd = threadIdx.x; dd < d; dd += blockDim.x) {
-      float num = 0.f;
-      for (long long c = c0; c <= c1; ++c) {
-        if (empty_cta(c)) continue;
-        const float wgt = exp2f(part_ml[((u + c) * r + t) * 2] - M);
-        num = fmaf(wgt, part_o[((u + c) * r + t) * d + dd], num);
-      }
-      const float v = num * inv;
-      DT* dst = out + (static_cast<size_t>(i) * h + j * r + t) * d + dd;
-      if constexpr (sizeof(DT) == 2)
-        *dst = __float2bfloat16_rn(v);
-      else
-        *dst = v;
+    float mb = M;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, mc[k]);
+    const float sc = ex2(M - mb);  // 0 on the first batch (M = -inf)
+    num *= sc;
+    den *= sc;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const float wgt = ex2(mc[k] - mb);  // 0 for unused slots
+      den = fmaf(wgt, lc[k], den);
+      num = fmaf(wgt, oc[k], num);
     }
+    M = mb;
   }
+  const float v = num / den;
+  DT* dst = out + (static_cast<size_t>(i) * h + j * r + t) * d + col;
+  if constexpr (sizeof(DT) == 2)
+    *dst = __float2bfloat16_rn(v);
+  else
+    *dst = v;
 }
 
 // One mbarrier that nothing ever arrives on; the bounded wait must give up.
@@ -159,10 +165,19 @@ struct DeviceInfo {
   unsigned int* status = nullptr;
 };
 
+// Split workspace of one (device, stream): partials, rewritten by every call,
+// and per-unit arrival counters, which must be zero before a launch.  The
+// kernels put every counter they use back to zero; after a wait timeout (a
+// launch that gave up half way) the counters are cleared again.
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  int* counters = nullptr;
+  size_t units = 0;
+  unsigned epoch = 0;
 };
+
+std::atomic<unsigned> g_reset_epoch{0};
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
@@ -195,31 +210,89 @@ int device_info(DeviceInfo** out) {
   return GQA_OK;
 }
 
-int workspace(cudaStream_t stream, size_t bytes, void** ptr) {
+int workspace(cudaStream_t stream, size_t bytes, size_t units, void** ptr, int** counters) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GQA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace& ws = g_ws[{dev, stream}];
-  if (ws.bytes < bytes) {
-    if (ws.ptr) {
-      // the previous buffer may still be read by queued work on `stream`
-      if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(ws.ptr) != cudaSuccess)
-        return GQA_ERR_CUDA;
+  if (ws.bytes < bytes || ws.units < units) {
+    // the previous buffers may still be used by queued work on `stream`
+    if ((ws.ptr || ws.counters) && cudaStreamSynchronize(stream) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    if (ws.bytes < bytes) {
+      if (ws.ptr && cudaFree(ws.ptr) != cudaSuccess) return GQA_ERR_CUDA;
       ws.ptr = nullptr;
       ws.bytes = 0;
+      const size_t grow = bytes + bytes / 4;
+      if (cudaMalloc(&ws.ptr, grow) != cudaSuccess) {
+        ws.ptr = nullptr;
+        return GQA_ERR_CUDA;
+      }
+      ws.bytes = grow;
     }
-    const size_t grow = bytes + bytes / 4;
-    if (cudaMalloc(&ws.ptr, grow) != cudaSuccess) {
-      ws.ptr = nullptr;
+    if (ws.units < units) {
+      if (ws.counters && cudaFree(ws.counters) != cudaSuccess) return GQA_ERR_CUDA;
+      ws.counters = nullptr;
+      ws.units = 0;
+      const size_t grow = units + units / 4;
+      if (cudaMalloc(&ws.counters, grow * sizeof(int)) != cudaSuccess ||
+          cudaMemset(ws.counters, 0, grow * sizeof(int)) != cudaSuccess) {
+        ws.counters = nullptr;
+        return GQA_ERR_CUDA;
+      }
+      ws.units = grow;
+      ws.epoch = g_reset_epoch.load();
+    }
+  }
+  const unsigned epoch = g_reset_epoch.load();
+  if (ws.epoch != epoch) {
+    if (cudaMemsetAsync(ws.counters, 0, ws.units * sizeof(int), stream) != cudaSuccess)
       return GQA_ERR_CUDA;
-    }
-    ws.bytes = grow;
+    ws.epoch = epoch;
   }
   *ptr = ws.ptr;
+  *counters = ws.counters;
   return GQA_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// With more than twice as many CTAs as units, every unit is cut into three
+// or more pieces and a merge by the last CTA to finish would serialise many
+// partial reads at the end of the launch: those launches hand the merge to
+// the combine kernel instead (counters = null tells the decode kernel).
+bool use_combine_kernel(const DecodeLaunch& a) {
+  return static_cast<long long>(a.nc) > 2ll * a.b * a.g;
+}
+
+int launch_all(DecodeLaunch& a, int tile) {
+  const bool separate = use_combine_kernel(a);
+  if (separate) a.counters = nullptr;
+  const bool tc = tc_supported(a.dtype, a.d, a.h / a.g);
+  cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  if (separate) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.b) * a.h));
+    cfg.blockDim = dim3(a.d);
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.dtype == GQA_BF16)
+      e = cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a.seq_lens, a.b, a.h, a.g,
+                             a.cap, a.d, tile, a.nc, static_cast<const float*>(a.part_o),
+                             static_cast<const float*>(a.part_ml),
+                             static_cast<__nv_bfloat16*>(a.out));
+    else
+      e = cudaLaunchKernelEx(&cfg, combine_kernel<float>, a.seq_lens, a.b, a.h, a.g, a.cap, a.d,
+                             tile, a.nc, static_cast<const float*>(a.part_o),
+                             static_cast<const float*>(a.part_ml), static_cast<float*>(a.out));
+  }
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
 
 int elt_bytes(int dtype) { return dtype == GQA_F32 ? 4 : 2; }
 
@@ -273,9 +346,16 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_c
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
-                    const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v, float scale,
-                    void* out, int cap, int dtype, void* stream) {
+}  // extern "C"
+
+namespace gqa {
+namespace {
+
+// gqa_decode_attn and gqa_decode_step: checks, kernel choice, workspace,
+// launch.  k_new / v_new null means attention only.
+int decode(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+           const void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v,
+           float scale, void* out, int cap, int dtype, void* stream) {
   if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
   if (b < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0)
@@ -284,7 +364,7 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
       static_cast<long long>(b) * h > 0x7FFFFFFFll)
     return GQA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+      !aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return GQA_ERR_ALIGN;
   const int r = h / g;
   const int d = d_k;
@@ -306,7 +386,9 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
   const size_t o_bytes = slots * r * d * sizeof(float);
   const size_t ml_bytes = slots * r * 2 * sizeof(float);
   void* ws = nullptr;
-  if (int e = workspace(st, o_bytes + ml_bytes, &ws)) return e;
+  int* counters = nullptr;
+  if (int e = workspace(st, o_bytes + ml_bytes, static_cast<size_t>(b) * g, &ws, &counters))
+    return e;
 
   DecodeLaunch a;
   a.q = q;
@@ -323,15 +405,37 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
   a.out = out;
   a.part_o = static_cast<float*>(ws);
   a.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+  a.counters = counters;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache_w = const_cast<void*>(k_cache);
+  a.v_cache_w = const_cast<void*>(v_cache);
   a.status = di->status;
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(nc);
   a.stream = st;
 
-  cudaError_t e = use_tc ? launch_decode_tc(a) : launch_decode_simt(a);
-  if (e != cudaSuccess) return GQA_ERR_CUDA;
-  e = launch_combine(a, tile);
-  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return launch_all(a, tile);
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v, float scale,
+                    void* out, int cap, int dtype, void* stream) {
+  return gqa::decode(q, nullptr, nullptr, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
+                     out, cap, dtype, stream);
+}
+
+int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k,
+                    int d_v, float scale, void* out, int cap, int dtype, void* stream) {
+  if (!k_new || !v_new) return GQA_ERR_NULL;
+  return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale, out,
+                     cap, dtype, stream);
 }
 
 int gqa_device_status(void* stream, uint32_t* bits_out) {
@@ -344,6 +448,8 @@ int gqa_device_status(void* stream, uint32_t* bits_out) {
   if (cudaMemcpy(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemset(di->status, 0, sizeof(v)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return GQA_ERR_CUDA;
+  // a launch that gave up waiting may have left split counters raised
+  if (v & GQA_DEV_WAIT_TIMEOUT) g_reset_epoch.fetch_add(1);
   *bits_out = v;
   return GQA_OK;
 }
@@ -359,22 +465,6 @@ int gqa_selftest_wait_timeout(long long budget_cycles, void* stream) {
 
 }  // extern "C"
 
-namespace gqa {
-
-cudaError_t launch_combine(const DecodeLaunch& a, int tile) {
-  const long long units = static_cast<long long>(a.b) * a.g;
-  if (a.dtype == GQA_BF16)
-    combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(units), 128, 0, a.stream>>>(
-        a.seq_lens, a.b, a.h, a.g, a.cap, a.d, tile, a.nc, a.part_o, a.part_ml,
-        static_cast<__nv_bfloat16*>(a.out), a.status);
-  else
-    combine_kernel<float><<<static_cast<unsigned>(units), 128, 0, a.stream>>>(
-        a.seq_lens, a.b, a.h, a.g, a.cap, a.d, tile, a.nc, a.part_o, a.part_ml,
-        static_cast<float*>(a.out), a.status);
-  return cudaGetLastError();
-}
-
-}  // namespace gqa
 
 // ---------------------------------------------------------------------------
 // gqa_decode_attn_noalloc: the same decode, with the split partials in a
@@ -385,6 +475,8 @@ namespace gqa {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
+constexpr size_t kNoAllocCounterBytes = size_t(256) << 10;  // first 256 KiB: unit counters
+constexpr size_t kNoAllocMaxUnits = kNoAllocCounterBytes / sizeof(int);
 
 // Every GPU that loads the library holds this array until the process exits.
 // Host code must not use its name as an address: the device address comes
@@ -467,7 +559,15 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
   const size_t o_bytes = slots * r * d * sizeof(float);
   const size_t ml_bytes = slots * r * 2 * sizeof(float);
-  if (o_bytes + ml_bytes > kNoAllocScratchBytes) return GQA_ERR_SCRATCH_LIMIT;
+  if (static_cast<size_t>(b) * g > kNoAllocMaxUnits ||
+      o_bytes + ml_bytes > kNoAllocScratchBytes - kNoAllocCounterBytes)
+    return GQA_ERR_SCRATCH_LIMIT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* counters = reinterpret_cast<int*>(nd->scratch);
+  unsigned char* parts = nd->scratch + kNoAllocCounterBytes;
+  // the per-unit arrival counters must start at zero
+  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(b) * g * sizeof(int), st) != cudaSuccess)
+    return GQA_ERR_CUDA;
 
   DecodeLaunch a;
   a.q = q;
@@ -482,15 +582,16 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   a.dtype = dtype;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out = out;
-  a.part_o = reinterpret_cast<float*>(nd->scratch);
-  a.part_ml = reinterpret_cast<float*>(nd->scratch + o_bytes);
+  a.part_o = reinterpret_cast<float*>(parts);
+  a.part_ml = reinterpret_cast<float*>(parts + o_bytes);
+  a.counters = counters;
+  a.k_new = nullptr;
+  a.v_new = nullptr;
+  a.k_cache_w = nullptr;
+  a.v_cache_w = nullptr;
   a.status = nd->status;
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(nc);
-  a.stream = static_cast<cudaStream_t>(stream);
-
-  cudaError_t e = use_tc ? launch_decode_tc(a) : launch_decode_simt(a);
-  if (e != cudaSuccess) return GQA_ERR_CUDA;
-  e = launch_combine(a, tile);
-  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  a.stream = st;
+  return launch_all(a, tile);
 }

@@ -113,6 +113,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream be scheduled as SMs free up; wait blocks until the previous
+// kernel of the stream has completed and its writes are visible (a no-op
+// when the launch had no programmatic dependency).  Every input and the
+// split workspace are read only after the wait.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -246,15 +257,74 @@ __device__ __forceinline__ int seq_tiles(int L, int cap, int T) {
 }
 
 struct Segment {
-  int i, j;      // sequence, KV head
-  int lt0, lt1;  // local tile range within the unit
-  int L;         // post-append length of sequence i
-  int ti;        // tiles of the unit
+  int i, j;       // sequence, KV head
+  int lt0, lt1;   // local tile range within the unit
+  int L;          // post-append length of sequence i
+  int ti;         // tiles of the unit
+  long long u0;   // global index of the unit's first tile
 };
+
+// CTA c's range is empty when W < nc leaves it no tile.
+__device__ __forceinline__ bool cta_empty(long long c, long long W, int nc) {
+  return (c * W) / nc == ((c + 1) * W) / nc;
+}
+
+// First and last CTA holding tiles of the unit that spans global tiles
+// [u0, u1): the largest c with floor(c W / nc) <= u0, and the same for u1 - 1.
+__device__ __forceinline__ void unit_ctas(long long u0, long long u1, long long W, int nc,
+                                          long long& c0, long long& c1) {
+  c0 = ((u0 + 1) * nc - 1) / W;
+  c1 = (u1 * nc - 1) / W;
+}
+
+// Number of CTAs that write a partial for the unit (non-empty ranges only).
+__device__ __forceinline__ int unit_parts(long long c0, long long c1, long long W, int nc) {
+  if (W >= nc) return static_cast<int>(c1 - c0 + 1);
+  int n = 0;
+  for (long long c = c0; c <= c1; ++c) n += cta_empty(c, W, nc) ? 0 : 1;
+  return n;
+}
+
+// Split units are merged by the CTA that finishes its share last.  Every CTA
+// that wrote a partial of unit u calls this with all `nthreads` threads of its
+// epilogue group: the partial stores are fenced, one leader thread counts the
+// arrival, and the CTA whose arrival completes the count gets true (and puts
+// the counter back to zero for the next launch).  No CTA ever waits for
+// another.
+__device__ __forceinline__ bool arrive_last(int* counters, int u, int nparts, int* s_flag,
+                                            bool leader, int bar_id, int nthreads) {
+  __threadfence();
+  named_bar_sync(bar_id, nthreads);
+  if (leader) {
+    const int old = atomicAdd(counters + u, 1);
+    const int last = (old == nparts - 1) ? 1 : 0;
+    if (last) {
+      counters[u] = 0;
+      __threadfence();
+    }
+    *reinterpret_cast<volatile int*>(s_flag) = last;
+  }
+  named_bar_sync(bar_id, nthreads);
+  return *reinterpret_cast<volatile int*>(s_flag) != 0;
+}
+
+// Warp-cooperative: flag every sequence whose length is outside [1, cap].
+__device__ __forceinline__ void report_bad_lengths(const int* lens, int b, int cap,
+                                                   unsigned int* status) {
+  bool bad = false;
+  for (int idx = threadIdx.x & 31; idx < b; idx += 32) {
+    const int L = __ldg(lens + idx);
+    bad |= (L < 1 || L > cap);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
+    atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
+}
 
 struct Walker {
   const int* lens;
   int b, g, cap, T;
+  long long W;         // total tiles of the launch
+  int nc;              // CTAs of the launch
   long long pos, end;  // global tile cursor and end of this CTA's range
   int i, j, lt, ti, L;
 
@@ -280,7 +350,8 @@ struct Walker {
     g = g_;
     cap = cap_;
     T = T_;
-    const long long W = total_tiles(lens, b, g, cap, T);
+    W = total_tiles(lens, b, g, cap, T);
+    this->nc = nc;
     pos = (W * c) / nc;
     end = (W * (c + 1)) / nc;
     i = b;
@@ -336,6 +407,7 @@ struct Walker {
     s.lt1 = lt1;
     s.L = L;
     s.ti = ti;
+    s.u0 = pos - lt;
     pos += lt1 - lt;
     lt = lt1;
     if (lt == ti && pos < end) {

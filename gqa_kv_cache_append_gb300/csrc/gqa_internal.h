@@ -18,6 +18,11 @@ struct DecodeLaunch {
   void* out;
   float* part_o;         // [slots, r, d] unnormalised partial outputs
   float* part_ml;        // [slots, r, 2] running max (base 2) and sum
+  int* counters;         // [b * g] arrivals per split unit; zero between launches
+  const void* k_new;     // fused append: new K/V rows [b, g, d], or null
+  const void* v_new;
+  void* k_cache_w;       // the caches, written at row L_i - 1 when appending
+  void* v_cache_w;
   unsigned int* status;  // device status word
   long long budget;      // wait limit in SM cycles
   int nc;                // persistent CTAs
@@ -36,7 +41,5 @@ int tc_tile();
 int tc_ctas_per_sm(int r);
 cudaError_t launch_decode_tc(const DecodeLaunch& a);
 
-// log-sum-exp merge of the partials of units split across CTAs
-cudaError_t launch_combine(const DecodeLaunch& a, int tile);
 
 }  // namespace gqa

@@ -39,9 +39,9 @@
  *     Kernels never trap and every wait inside them is bounded.
  *   - Calls that overlap on the GPU (different streams) must not share
  *     output buffers.  gqa_decode_attn keeps one split workspace per
- *     (device, stream), grown on demand with cudaMalloc (so the first call
- *     with a new largest size on a stream must not be made during stream
- *     capture).
+ *     (device, stream): partials plus one arrival counter per (sequence, KV
+ *     head), grown on demand with cudaMalloc (so the first call with a new
+ *     largest size on a stream must not be made during stream capture).
  */
 #ifndef GQA_H
 #define GQA_H
@@ -127,6 +127,23 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                     void* stream);
 
 /*
+ * gqa_decode_step - the whole step of one layer in one launch: the append of
+ * gqa_kv_append followed by the attention of gqa_decode_attn, in the order of
+ * the decode notes' pseudo code (push K, push V, attend).
+ *
+ * Same arguments as gqa_decode_attn plus k_new [b, g, d_k] and v_new
+ * [b, g, d_v] (read; same dtype).  k_cache and v_cache are written at row
+ * L_i - 1 of every (i, j), exactly as gqa_kv_append writes them, and out
+ * equals what gqa_kv_append followed by gqa_decode_attn would give (the same
+ * kernel arithmetic): the CTA that streams a unit's last tile puts the new
+ * row into its staged copy of that tile and into the cache.  Same limits,
+ * errors and workspace as gqa_decode_attn; a bad L_i appends nothing.
+ */
+int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k,
+                    int d_v, float scale, void* out, int cap, int dtype, void* stream);
+
+/*
  * gqa_device_status - read and clear the device status word of the current
  * device.  Synchronizes `stream` first, so the word covers every call queued
  * on it before.  *bits_out receives an OR of GQA_DEV_* bits (0 = clean).
@@ -155,19 +172,22 @@ int gqa_selftest_wait_timeout(long long budget_cycles, void* stream);
  *
  * Arguments, layouts, results and error codes are those of gqa_decode_attn,
  * and the two give the same output.  The caller still passes every input
- * and output buffer.  Limit: a call needs (b*g + C) * (h/g) * (d_v + 2) * 4
- * bytes of scratch, C being the number of CTAs (at most the SM count, 152 on
- * GB300); a larger call returns GQA_ERR_SCRATCH_LIMIT and launches nothing.
- * (The Llama-3-70B-shaped layer, b=32 h=64 g=8 d=128, needs 1.7 MB.)
+ * and output buffer.  Limits: the first 256 KiB of the array hold one int
+ * counter per (sequence, KV head), so b*g <= 65536; the remaining 3.75 MiB
+ * hold the partials, (b*g + C) * (h/g) * (d_v + 2) * 4 bytes, C being the
+ * number of CTAs (at most the SM count, 152 on GB300).  A larger call returns
+ * GQA_ERR_SCRATCH_LIMIT and launches nothing.  (The Llama-3-70B-shaped
+ * layer, b=32 h=64 g=8 d=128, needs 256 counters and 1.7 MB of partials.)
  *
  * The first call on a device does a one-time set-up with that device current
  * (it looks up the device address of the array); make that first call
  * before any stream capture.  All calls share the one array and it keeps the
- * last call's contents; nothing in it needs to start at zero (each call
- * writes every partial it later reads).  Calls that overlap on the GPU (on
- * different streams, or from different threads) race on the array and must
- * be serialised by the caller.  No cudaMalloc, cudaFree or other allocating
- * routine is called.
+ * last call's contents: each call clears the b*g counters it uses (an async
+ * memset on `stream`, before its launch); the partials need no clearing
+ * (each call writes every partial it later reads).  Calls that overlap on the
+ * GPU (on different streams, or from different threads) race on the array
+ * and must be serialised by the caller.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
  */
 int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* seq_lens, int b, int h, int g, int d_k,

@@ -92,6 +92,19 @@ def test_kv_append_host_checks(kw, code):
     assert _app(_lib(), **kw) == code
 
 
+def test_decode_step_host_checks():
+    b = _lib()
+    f = b.lib.gqa_decode_step
+    args = [A, A, A, A, A, A, 2, 8, 2, 128, 128, 0.1, A, 64, 1, None]
+    assert f(*args[:1], 0, *args[2:]) == -1          # k_new null
+    assert f(*args[:2], 0, *args[3:]) == -1          # v_new null
+    assert f(*args[:1], A + 8, *args[2:]) == -4      # k_new misaligned
+    bad = list(args)
+    bad[7] = 6
+    bad[8] = 4
+    assert f(*bad) == -2                             # h % g
+
+
 def test_null_status_pointer():
     b = _lib()
     assert b.lib.gqa_device_status(None, None) == -1

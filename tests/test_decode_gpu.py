@@ -23,15 +23,15 @@ def _b():
     return binding
 
 
-def run_step(cfg: DecodeConfig, lens, pad_fill=None, layer=0, check=True):
-    """Append + attend on the GPU, oracle on the same host inputs; returns the
-    max error."""
+def run_step(cfg: DecodeConfig, lens, pad_fill=None, layer=0, check=True, fused=False):
+    """Append + attend on the GPU (two calls, or one fused gqa_decode_step),
+    oracle on the same host inputs; returns the max error."""
     B = _b()
     x = make_layer(cfg, layer, "cpu", lens=np.asarray(lens, dtype=np.int32), pad_fill=pad_fill)
     d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
     out = torch.full((cfg.b, cfg.h, cfg.d), 3.0, dtype=cfg.torch_dtype, device="cuda")
     B.decode_step(d["q"], d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], d["seq_lens"],
-                  cfg.g, cfg.scale, out)
+                  cfg.g, cfg.scale, out, fused=fused)
     assert B.gqa_device_status() == 0
     tag = to_np(x["q"])[1]
     args = [to_np(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
@@ -89,9 +89,66 @@ def test_tc_bf16(b, h, g, cap, lens):
     run_step(cfg_of("bf16", b, h, g, 128, cap, seed=b * cap), lens)
 
 
+# ---- fused append + attention (one launch): same cache bits, same bound
+@pytest.mark.parametrize("dtype,b,h,g,d,cap,lens", [
+    ("bf16", 3, 64, 8, 128, 300, [300, 256, 128]),      # new row at a tile's last row
+    ("bf16", 2, 28, 4, 128, 700, [700, 1]),
+    ("bf16", 1, 32, 1, 128, 5000, [4097]),              # split unit, new row alone in its tile
+    ("bf16", 4, 16, 16, 128, 129, [129, 127, 64, 2]),
+    ("f32", 2, 8, 1, 64, 256, [256, 65]),
+    ("f32", 3, 12, 4, 128, 100, [32, 33, 1]),
+    ("bf16", 2, 8, 1, 64, 300, [300, 128]),
+])
+def test_fused_step(dtype, b, h, g, d, cap, lens):
+    run_step(cfg_of(dtype, b, h, g, d, cap, seed=7 * b + cap), lens, fused=True)
+
+
+def test_fused_step_matches_two_calls_bitwise():
+    B = _b()
+    cfg = cfg_of("bf16", 6, 64, 8, 128, 3000, seed=31)
+    lens = np.array([3000, 1, 128, 2049, 777, 2560], dtype=np.int32)
+    x = make_layer(cfg, 0, "cuda", lens=lens)
+    outs, caches = [], []
+    for fused in (False, True):
+        kc, vc = x["k_cache"].clone(), x["v_cache"].clone()
+        out = torch.empty((cfg.b, cfg.h, cfg.d), dtype=torch.bfloat16, device="cuda")
+        B.decode_step(x["q"], kc, vc, x["k_new"], x["v_new"], x["seq_lens"], cfg.g, cfg.scale,
+                      out, fused=fused)
+        outs.append(out)
+        caches.append((kc, vc))
+    assert B.gqa_device_status() == 0
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
+
+
+def test_fused_step_bad_length_appends_nothing():
+    B = _b()
+    cfg = cfg_of("bf16", 3, 16, 2, 128, 300, seed=8)
+    x = make_layer(cfg, 0, "cuda", lens=np.array([300, 300, 300], dtype=np.int32))
+    before_k = x["k_cache"].clone()
+    lens = torch.tensor([300, 0, 301], dtype=torch.int32, device="cuda")
+    out = torch.full((cfg.b, cfg.h, cfg.d), 5.0, dtype=torch.bfloat16, device="cuda")
+    B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], lens, cfg.b,
+                      cfg.h, cfg.g, 128, 128, cfg.scale, out)
+    assert B.gqa_device_status() == B.GQA_DEV_BAD_SEQ_LEN
+    assert torch.equal(x["k_cache"][1:], before_k[1:])
+    assert torch.all(out[1:] == 5.0)
+    assert torch.equal(x["k_cache"][0, :, 299], x["k_new"][0])
+
+
 def test_tc_many_splits_long_sequence():
     # one unit of 40 tiles spread over many CTAs: exercises the combine
     run_step(cfg_of("bf16", 1, 8, 1, 128, 5000, seed=3), [5000])
+
+
+@pytest.mark.parametrize("dtype,d,cap,lens", [
+    ("bf16", 128, 20000, [5000]),          # 40 tiles over 152 CTAs: most ranges empty
+    ("bf16", 128, 9000, [300, 1, 4000]),
+    ("f32", 64, 12000, [1000, 3]),         # CUDA-core kernel, same situation
+])
+def test_fewer_tiles_than_ctas(dtype, d, cap, lens):
+    h, g = (8, 1) if dtype == "bf16" else (4, 2)
+    run_step(cfg_of(dtype, len(lens), h, g, d, cap, seed=cap % 97), lens)
 
 
 def test_tc_ragged_batch_with_nan_padding():
