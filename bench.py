@@ -243,6 +243,8 @@ def run_ours(args, rank, local_rank, world):
     base = workload(args.workload)
     if args.g:
         base = dataclasses.replace(base, g=args.g)
+    if args.h:
+        base = dataclasses.replace(base, h=args.h)
     if args.layers:
         base = dataclasses.replace(base, layers=min(args.layers, base.layers))
     lens = seq_lens_for(base)
@@ -256,8 +258,15 @@ def run_ours(args, rank, local_rank, world):
         base = dataclasses.replace(base, layers=-(-4 * l2 // per_layer))
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
     layers = [make_layer(cfg, l, dev) for l in range(cfg.layers)]
-    outs = [torch.empty((cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device=dev)
-            for _ in range(cfg.layers)]
+    # the step's per-layer inputs and outputs live in one packed buffer each
+    # (layer-major), so the end-to-end leg moves them with one copy apiece
+    packed = {}
+    for key in ("q", "k_new", "v_new"):
+        packed[key] = torch.stack([x[key] for x in layers]).contiguous()
+        for l, x in enumerate(layers):
+            x[key] = packed[key][l]
+    out_all = torch.empty((cfg.layers, cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device=dev)
+    outs = [out_all[l] for l in range(cfg.layers)]
     stream = torch.cuda.current_stream(dev)
     sb = step_bytes(cfg, lens)
 
@@ -268,9 +277,13 @@ def run_ours(args, rank, local_rank, world):
             B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
                               cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l], stream=stream)
         else:
+            # layers are independent buffers and seq_lens is fixed for the
+            # step, so each layer may start streaming while the one before
+            # finishes (GQA_STEP_EARLY_STREAM's contract)
             B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
                               x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale,
-                              outs[l], stream=stream)
+                              outs[l], flags=0 if args.ordered else B.GQA_STEP_EARLY_STREAM,
+                              stream=stream)
 
     def step(ev=None):
         for l, x in enumerate(layers):
@@ -285,9 +298,11 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize(dev)
     assert B.gqa_device_status(stream) == 0
 
-    # ---- device-resident timing, with per-launch events on the attention ----
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            for _ in range(cfg.layers)] for _ in range(args.steps)]
+    # ---- device-resident timing: K steps back to back, CUDA events on the
+    # launching stream around the whole region.  Nothing is recorded between
+    # the layer calls: an event between two launches would remove the
+    # overlap their programmatic dependency allows.  Each step is only its
+    # layer calls, so the time of one call is the step time / layers. ----
     clocks = ClockSampler(smi_id(dev.index))
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
@@ -297,32 +312,39 @@ def run_ours(args, rank, local_rank, world):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        step(evs[k])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(dist, dev)
     ms_local = t_start.elapsed_time(t_end) / args.steps
-    attn_ms = [e[0].elapsed_time(e[1]) for per in evs for e in per]
     ms = max_over_ranks(dist, ms_local)
-    attn_avg_ms = max_over_ranks(dist, float(np.mean(attn_ms)))
+    attn_avg_ms = ms / cfg.layers
+    # ---- the same calls one at a time, events around each (no overlap) ----
+    n_iso = max(1, min(args.steps, 5))
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            for _ in range(cfg.layers)] for _ in range(n_iso)]
+    for k in range(n_iso):
+        step(evs[k])
+    torch.cuda.synchronize(dev)
+    iso_ms = max_over_ranks(dist, float(np.mean([e[0].elapsed_time(e[1])
+                                                 for per in evs for e in per])))
     status = B.gqa_device_status(stream)
 
-    # ---- end to end: pinned host inputs in, result out, every step ----
-    hq = [x["q"].cpu().pin_memory() for x in layers]
-    hk = [x["k_new"].cpu().pin_memory() for x in layers]
-    hv = [x["v_new"].cpu().pin_memory() for x in layers]
-    ho = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
-    d2h = sum(t.numel() * t.element_size() for t in ho)
+    # ---- end to end: every step copies all layers' q, k_new, v_new in from
+    # pinned host memory (one copy per tensor), runs the layers, and copies
+    # all outputs back ----
+    host_in = {k: v.cpu().pin_memory() for k, v in packed.items()}
+    host_out = torch.empty_like(out_all, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
+        for key, t in host_in.items():
+            packed[key].copy_(t, non_blocking=True)
         for l, x in enumerate(layers):
-            x["q"].copy_(hq[l], non_blocking=True)
-            x["k_new"].copy_(hk[l], non_blocking=True)
-            x["v_new"].copy_(hv[l], non_blocking=True)
             layer_call(l, x)
-            ho[l].copy_(outs[l], non_blocking=True)
+        host_out.copy_(out_all, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -384,6 +406,8 @@ def run_ours(args, rank, local_rank, world):
             "traffic": traffic,
             "algorithmic_bytes_per_launch": call_bytes,
             "avg_launch_ms": round(attn_avg_ms, 5),
+            "avg_launch_ms_how": "timed region / layer calls (back-to-back launches)",
+            "isolated_launch_ms": round(iso_ms, 5),
         },
         "e2e": {
             "value": round(world * sb["step"] / (e2e_ms * 1e-3) / 1e9, 2),
@@ -453,6 +477,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--g", type=int, default=None, help="KV heads (for the g-knob sweep)")
+    ap.add_argument("--h", type=int, default=None, help="query heads (shape studies)")
+    ap.add_argument("--ordered", action="store_true",
+                    help="no early streaming: each layer waits for the previous one")
     ap.add_argument("--separate", action="store_true",
                     help="time gqa_kv_append + gqa_decode_attn instead of gqa_decode_step")
     ap.add_argument("--layers", type=int, default=None,

@@ -28,6 +28,8 @@ GQA_ERR_CUDA = -6
 GQA_ERR_DEVICE = -7
 GQA_ERR_SCRATCH_LIMIT = -8
 
+GQA_STEP_EARLY_STREAM = 1
+
 GQA_DEV_BAD_SEQ_LEN = 1
 GQA_DEV_WAIT_TIMEOUT = 2
 
@@ -39,7 +41,7 @@ SIGNATURES = {
     "gqa_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I,
                                      _VP]),
     "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I,
-                             _I, _VP]),
+                             _I, _I, _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -127,14 +129,16 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
 
 
 def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v,
-                    scale, out, cap=None, dtype=None, stream=None) -> None:
-    """Append k_new / v_new at row seq_lens[i] - 1 and attend, in one launch."""
+                    scale, out, cap=None, dtype=None, flags=0, stream=None) -> None:
+    """Append k_new / v_new at row seq_lens[i] - 1 and attend, in one launch.
+    flags=GQA_STEP_EARLY_STREAM: see include/gqa.h (the kernels still running
+    ahead on the stream must not write seq_lens or this call's older rows)."""
     if cap is None:
         cap = k_cache.shape[2]
     _check("gqa_decode_step", lib.gqa_decode_step(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
         int(b), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
-        _dtype(q, dtype), _stream(stream)))
+        _dtype(q, dtype), int(flags), _stream(stream)))
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
@@ -169,14 +173,14 @@ def gqa_version() -> int:
 
 
 def decode_step(q, k_cache, v_cache, k_new, v_new, seq_lens, g, scale, out,
-                stream=None, fused=False) -> None:
+                stream=None, fused=False, flags=0) -> None:
     """One layer's decode step in the order of the decode notes: push the new
     K/V rows, then attend.  fused=False makes the two C-ABI calls
     (gqa_kv_append, gqa_decode_attn); fused=True makes one gqa_decode_step."""
     b, h, d = q.shape
     if fused:
         gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d,
-                        v_cache.shape[-1], scale, out, stream=stream)
+                        v_cache.shape[-1], scale, out, flags=flags, stream=stream)
         return
     gqa_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, b, g, d, v_new.shape[-1],
                   stream=stream)

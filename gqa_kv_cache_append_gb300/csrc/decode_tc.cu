@@ -49,19 +49,19 @@ namespace {
 constexpr int kT = 128;       // positions per tile (MMA M of the S product)
 constexpr int kD = 128;       // head dim (MMA M of the O product)
 constexpr int kStages = 3;    // K/V ring depth
-constexpr int kThreads = 192;
 constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 
-template <int NP>
+template <int NP, int NWG>
 struct TcCfg {
+  static constexpr int THREADS = 64 + 128 * NWG;  // producer, MMA, NWG softmax warpgroups
   static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
   static constexpr int Q_BYTES = NP * 256;         // two [NP x 64] boxes
   static constexpr int P_BYTES = kT * NP * 2;      // [T rows x NP] bf16
   static constexpr int OFF_Q = kStages * KV_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;   // float [2][4][NP]
-  static constexpr int OFF_LRED = OFF_RED + 2 * 4 * NP * 4;  // float [4][NP]
-  static constexpr int OFF_ALPHA = OFF_LRED + 4 * NP * 4;    // float [2][NP] rescale factors
+  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;       // float [2][NP][4] warp maxima
+  static constexpr int OFF_MAX = OFF_RED + 2 * 4 * NP * 4;   // float [2][NP] running max
+  static constexpr int OFF_ALPHA = OFF_MAX + 2 * NP * 4;     // float [2][NP] rescale factors
   static constexpr int OFF_BAR = OFF_ALPHA + 2 * NP * 4;
   static constexpr int NBAR = 3 * kStages + 2 * 7 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -73,6 +73,7 @@ struct TcCfg {
   static constexpr uint32_t IDESC_O = idesc_bf16(128, NP, 1, 1);   // O: MN-major A, B
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
+  static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
 };
 
 // barrier slots
@@ -90,8 +91,8 @@ enum {
   B_DRAIN = B_O_FREE + 2,
 };
 
-template <int NP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NP, int NWG>
+__global__ void __launch_bounds__(64 + 128 * NWG, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ lens,
@@ -100,14 +101,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                      float* __restrict__ part_ml, int* __restrict__ counters,
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
-                     unsigned int* status, long long budget) {
-  using C = TcCfg<NP>;
+                     unsigned int* status, long long budget, int early) {
+  using C = TcCfg<NP, NWG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
-  float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
-  float* lred = reinterpret_cast<float*>(sm + C::OFF_LRED);
+  float* red = reinterpret_cast<float*>(sm + C::OFF_RED);  // [NWG][2][HP][4]
+  float* max_sm = reinterpret_cast<float*>(sm + C::OFF_MAX);
   float* alpha_sm = reinterpret_cast<float*>(sm + C::OFF_ALPHA);
   const uint32_t bar0 = s_base + C::OFF_BAR;
   auto BAR = [&](int k) -> uint32_t { return bar0 + 8u * k; };
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if ((k >= B_S_FREE && k < B_S_FREE + 2) || (k >= B_P_READY && k < B_P_READY + 2) ||
           (k >= B_O_FREE && k < B_O_FREE + 2))
-        cnt = 4;  // one arrival per softmax warp
+        cnt = 4 * NWG;  // one arrival per softmax warp
       mbar_init(BAR(k), cnt);
     }
     *abort_flag = 0;
@@ -136,11 +137,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::NCOLS);
-  pdl_wait();  // everything above touched only this CTA's shared and tensor memory
-  if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, cap, status);
-  __syncthreads();
+  __syncthreads();  // barrier inits and the TMEM address (this CTA's own state)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: every thread waits for the previous
+  // kernel of the stream before touching memory it may write.  With `early`
+  // set, the caller guarantees that no kernel still running writes seq_lens
+  // or the cache rows below L_i - 1 (e.g. it is another layer's step), so
+  // the producer plans and streams its first tiles before the wait, and
+  // waits before loading q; the other warps wait at once.
+  if (!early || warp != 0) pdl_wait();
+  if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, cap, status);
 
   Walker w;
   w.init(lens, b, g, cap, kT, blockIdx.x, gridDim.x);
@@ -154,18 +161,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n = 0, k = 0;
       int last_n[kStages] = {-1, -1, -1};
       int last_q[2] = {-1, -1};
-      while (w.next(seg)) {
-        const uint32_t qs = k & 1;
-        if (mbar_wait(BAR(B_Q_EMPTY + qs), ((k >> 1) & 1) ^ 1, abort_flag, status, budget)) {
+      auto load_q = [&](uint32_t kk, const Segment& sg) {
+        const uint32_t qs = kk & 1;
+        if (mbar_wait(BAR(B_Q_EMPTY + qs), ((kk >> 1) & 1) ^ 1, abort_flag, status, budget)) {
           const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
-          const int qrow = seg.i * h + seg.j * r;
+          const int qrow = sg.i * h + sg.j * r;
           mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), C::Q_BYTES);
           tma_load_2d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, qrow, pol_keep);
           tma_load_2d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, qrow, pol_keep);
-          last_q[qs] = static_cast<int>(k);
+          last_q[qs] = static_cast<int>(kk);
         }
+      };
+      bool waited = !early;  // has this thread passed the dependency wait?
+      while (w.next(seg)) {
+        // q comes from the previous kernel: load it only after the wait
+        // (early mode: after the first ring's worth of K/V tiles)
+        if (waited) load_q(k, seg);
         const int unit_row = (seg.i * g + seg.j) * cap;
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          if (!waited && (lt - seg.lt0 == kStages)) {
+            pdl_wait();
+            waited = true;
+            load_q(k, seg);
+          }
           const int st = n % kStages;
           if (!mbar_wait(BAR(B_EMPTY + st), ((n / kStages) & 1) ^ 1, abort_flag, status,
                          budget))
@@ -180,8 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
           last_n[st] = static_cast<int>(n);
         }
+        if (!waited) {  // a first segment shorter than the ring
+          pdl_wait();
+          waited = true;
+          load_q(k, seg);
+        }
         ++k;
       }
+      if (!waited) pdl_wait();  // a CTA with no tiles
       if (*abort_flag) {  // copies in flight must land before the CTA exits
         for (int s = 0; s < kStages + 2; ++s) {
           int idx;
@@ -314,31 +338,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ====================== softmax / correction ========================
+    // NWG warpgroups of four warps; warpgroup wg owns heads
+    // [wg * HP, wg * HP + HP) and runs on its own (own exchanges, named
+    // barrier 1 + wg, own split counter); the warpgroups share only the
+    // staged tiles and the MMAs.
+    constexpr int HP = NP / NWG;
+    const int wg = (warp - 2) >> 2;   // warpgroup
+    const int wq = (warp - 2) & 3;    // warp within the warpgroup
     const int qd = warp & 3;          // TMEM lane quarter this warp may access
-    const int wq = warp - 2;          // index among the four softmax warps
     const int row = qd * 32 + lane;   // tile position (S) / head-dim column (O)
+    const int h0 = wg * HP;           // first head of this warpgroup
+    const int bar_id = 1 + wg;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tO = tmem + 2 * NP + lane_off;
+    const uint32_t tS = tmem + lane_off + h0, tO = tmem + 2 * NP + lane_off + h0;
+    float* red_wg = red + wg * 2 * HP * 4;   // [2][HP][4]
+    int* last_flag_wg = last_flag + wg;
 
-    float m[NP], l[NP], o[NP];
+    // l[e], o[e]: this thread's softmax sum (its positions) and output column
+    // for head h0 + e.  The running max of a head is uniform across the CTA:
+    // thread e of the warpgroup keeps head h0 + e's (m_own) and publishes it
+    // with its rescale factor through max_sm / alpha_sm each tile.
+    float l[HP], o[HP];
+    float m_own = -INFINITY;
 #pragma unroll
-    for (int t = 0; t < NP; ++t) {
-      m[t] = -INFINITY;
-      l[t] = 0.f;
-      o[t] = 0.f;
+    for (int e = 0; e < HP; ++e) {
+      l[e] = 0.f;
+      o[e] = 0.f;
     }
 
-    // fold O of tile mt into the registers: o = o * alpha + O_tile.  The
-    // factors come from registers (al) or, for the previous tile, from
-    // shared memory (all threads hold the same factors; thread t stored
-    // head t's after the tile's max exchange)
+    // fold O of tile mt into the registers: o = o * alpha + O_tile
     auto correct = [&](uint32_t mt, const float* al) {
       const uint32_t nb = mt & 1;
       const bool ok = mbar_wait(BAR(B_O_FULL + nb), (mt >> 1) & 1, abort_flag, status, budget);
-      float ov[NP];
+      float ov[HP];
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < NP; c += 16) {
+        for (int c = 0; c < HP; c += 16) {
           float tmp[16];
           tmem_ld16(tO + nb * NP + c, tmp);
 #pragma unroll
@@ -347,32 +382,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int t = 0; t < NP; ++t) ov[t] = 0.f;
+        for (int e = 0; e < HP; ++e) ov[e] = 0.f;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_O_FREE + nb));
 #pragma unroll
-      for (int t = 0; t < NP; ++t) o[t] = fmaf(o[t], al[t], ov[t]);
+      for (int e = 0; e < HP; ++e) o[e] = fmaf(o[e], al[h0 + e], ov[e]);
     };
 
     uint32_t n = 0;
     while (w.next(seg)) {
       const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
-      // fused append: threads 0-15 carry the new token's V row, one chunk each
+      // fused append: threads 0-15 of warpgroup 0 carry the new token's V
+      // row, one chunk each
       const bool append_here = v_new != nullptr && seg.lt1 == seg.ti;
       uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
-      if (append_here && row < 16) vnew = __ldg(v_new + unit * 16 + row);
+      if (wg == 0 && append_here && row < 16) vnew = __ldg(v_new + unit * 16 + row);
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         const uint32_t nb = n & 1;
         const int st = n % kStages;
         const int valid = min(kT, seg.L - lt * kT);
         // ---- logits from TMEM ----
         const bool ok = mbar_wait(BAR(B_S_FULL + nb), (n >> 1) & 1, abort_flag, status, budget);
-        float x[NP];
+        float x[HP];
         if (ok) {
 #pragma unroll
-          for (int c = 0; c < NP; c += 16) {
+          for (int c = 0; c < HP; c += 16) {
             float tmp[16];
             tmem_ld16(tS + nb * NP + c, tmp);
 #pragma unroll
@@ -381,66 +417,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int t = 0; t < NP; ++t) x[t] = 0.f;
+          for (int e = 0; e < HP; ++e) x[e] = 0.f;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_S_FREE + nb));
         const bool live = row < valid;
 #pragma unroll
-        for (int t = 0; t < NP; ++t) x[t] = (live && t < r) ? x[t] * scale_log2 : -INFINITY;
+        for (int e = 0; e < HP; ++e)
+          x[e] = (live && h0 + e < r) ? x[e] * scale_log2 : -INFINITY;
         // ---- per-head max over the tile's 128 positions ----
         float mine = -INFINITY;
 #pragma unroll
-        for (int t = 0; t < NP; ++t) {
-          const float wm = warp_max(x[t]);
-          if (lane == t) mine = wm;
+        for (int e = 0; e < HP; ++e) {
+          const float wm = warp_max(x[e]);
+          if (lane == e) mine = wm;
         }
-        // head-major [NP][4 warps]: one 16-byte load per head afterwards
-        float* rb = red + nb * 4 * NP;
-        if (lane < NP) rb[lane * 4 + wq] = mine;
-        named_bar_sync(1, 128);
-        // new running max, rescale factor and probabilities per head; x[t]
-        // becomes p[t].  Thread t keeps head t's factor (selected into a
-        // register, stored once after the loop) for this tile's correction.
-        float a_mine = 1.f;
-#pragma unroll
-        for (int t = 0; t < NP; ++t) {
-          if (t < r) {
-            const float4 v = *reinterpret_cast<const float4*>(rb + 4 * t);
-            const float mn = fmaxf(m[t], fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-            const float a = ex2(m[t] - mn);
-            m[t] = mn;
-            x[t] = ex2(x[t] - mn);
-            l[t] = fmaf(l[t], a, x[t]);
-            a_mine = (row == t) ? a : a_mine;
+        // head-major [HP][4 warps]; thread e folds head h0 + e's four warp
+        // maxima into the running max, forms the rescale factor and
+        // publishes both
+        float* rb = red_wg + nb * HP * 4;
+        if (lane < HP) rb[lane * 4 + wq] = mine;
+        named_bar_sync(bar_id, 128);
+        if (row < HP) {
+          if (h0 + row < r) {
+            const float4 v = *reinterpret_cast<const float4*>(rb + 4 * row);
+            const float mn = fmaxf(m_own, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            alpha_sm[nb * NP + h0 + row] = ex2(m_own - mn);
+            max_sm[nb * NP + h0 + row] = mn;
+            m_own = mn;
           } else {
-            x[t] = 0.f;
+            alpha_sm[nb * NP + h0 + row] = 1.f;
+            max_sm[nb * NP + h0 + row] = 0.f;
           }
         }
-        if (row < NP) alpha_sm[nb * NP + row] = a_mine;
-        const float* p = x;
-        // ---- P^T row `row` into the MN-major swizzled B operand ----
+        named_bar_sync(bar_id, 128);
+        // probabilities (x[e] becomes p[e]) and this thread's sums
+#pragma unroll
+        for (int e4 = 0; e4 < HP; e4 += 4) {
+          const float4 mv = *reinterpret_cast<const float4*>(max_sm + nb * NP + h0 + e4);
+          const float4 av = *reinterpret_cast<const float4*>(alpha_sm + nb * NP + h0 + e4);
+          const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+          const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = e4 + k;
+            x[e] = (h0 + e < r) ? ex2(x[e] - mm[k]) : 0.f;
+            l[e] = fmaf(l[e], aa[k], x[e]);
+          }
+        }
+        // ---- P^T row `row`, this warpgroup's heads, into the MN-major
+        // swizzled B operand (16-byte chunks of 8 heads) ----
         {
           const uint32_t prow = s_base + C::OFF_P + nb * C::P_BYTES + row * (NP * 2);
 #pragma unroll
-          for (int c = 0; c < NP / 8; ++c) {
+          for (int c = 0; c < HP / 8; ++c) {
             uint32_t wv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 pr = __floats2bfloat162_rn(p[8 * c + 2 * e], p[8 * c + 2 * e + 1]);
-              wv[e] = *reinterpret_cast<const uint32_t*>(&pr);
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 pr =
+                  __floats2bfloat162_rn(x[8 * c + 2 * k], x[8 * c + 2 * k + 1]);
+              wv[k] = *reinterpret_cast<const uint32_t*>(&pr);
             }
-            const int phys = (NP == 16) ? (c ^ ((row >> 2) & 1)) : (c ^ ((row >> 1) & 3));
+            const int cg = h0 / 8 + c;  // chunk index within the row
+            const int phys = (NP == 16) ? (cg ^ ((row >> 2) & 1)) : (cg ^ ((row >> 1) & 3));
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys * 16),
                          "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
                          : "memory");
           }
         }
-        // ---- last tile of a unit: zero the V rows past L_i; with the
-        // append fused in, put v_new into row L_i - 1 and into the cache ----
+        // ---- last tile of a unit (warpgroup 0): zero the V rows past L_i;
+        // with the append fused in, put v_new into row L_i - 1 and into the
+        // cache ----
         const bool patch = append_here && lt == seg.ti - 1;
-        if (valid < kT || patch) {
+        if (wg == 0 && (valid < kT || patch)) {
           const bool vok =
               mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
           const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
@@ -468,93 +518,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_P_READY + nb));
-        // ---- fold the previous tile's O into the registers ----
+        // ---- fold O into the registers: the previous tile's, and at the
+        // segment end this one's ----
         if (lt > seg.lt0) correct(n - 1, alpha_sm + ((n - 1) & 1) * NP);
-        if (lt == seg.lt1 - 1) {
-          named_bar_sync(1, 128);  // this tile's factors, written above, are visible
-          correct(n, alpha_sm + nb * NP);
-        }
+        if (lt == seg.lt1 - 1) correct(n, alpha_sm + nb * NP);
       }
 
       // ---- segment end: softmax denominators, output or partial ----
       {
         float mine = 0.f;
 #pragma unroll
-        for (int t = 0; t < NP; ++t) {
-          const float s = warp_sum(l[t]);
-          if (lane == t) mine = s;
+        for (int e = 0; e < HP; ++e) {
+          const float sum = warp_sum(l[e]);
+          if (lane == e) mine = sum;
         }
-        if (lane < NP) lred[wq * NP + lane] = mine;
-        named_bar_sync(1, 128);
+        // the warp-maxima slot of the segment's last tile is free here (its
+        // readers all passed that tile's second barrier); the next tile uses
+        // the other slot, and the one after waits at its first barrier
+        const uint32_t nlast = n - 1;
+        float* lred = red_wg + (nlast & 1) * HP * 4;
+        const float* mfin = max_sm + (nlast & 1) * NP + h0;
+        if (lane < HP) lred[wq * HP + lane] = mine;
+        named_bar_sync(bar_id, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
-        const int a0 = seg.i * h + seg.j * r;
+        const int a0 = seg.i * h + seg.j * r + h0;  // first head of this warpgroup
         const int u = seg.i * g + seg.j;
         const size_t slot = static_cast<size_t>(u) + blockIdx.x;
-        // l[t] becomes the CTA-wide softmax denominator of head t
+        // l[e] becomes the CTA-wide softmax denominator of head h0 + e
 #pragma unroll
-        for (int t = 0; t < NP; ++t)
-          l[t] = lred[t] + lred[NP + t] + lred[2 * NP + t] + lred[3 * NP + t];
+        for (int e = 0; e < HP; ++e)
+          l[e] = lred[e] + lred[HP + e] + lred[2 * HP + e] + lred[3 * HP + e];
         if (whole) {
 #pragma unroll
-          for (int t = 0; t < NP; ++t)
-            if (t < r)
-              out[static_cast<size_t>(a0 + t) * kD + row] = __float2bfloat16_rn(o[t] / l[t]);
+          for (int e = 0; e < HP; ++e)
+            if (h0 + e < r)
+              out[static_cast<size_t>(a0 + e) * kD + row] = __float2bfloat16_rn(o[e] / l[e]);
         } else {
 #pragma unroll
-          for (int t = 0; t < NP; ++t) {
-            if (t < r) {
-              part_o[(slot * r + t) * kD + row] = o[t];
+          for (int e = 0; e < HP; ++e) {
+            if (h0 + e < r) {
+              const size_t sl = slot * r + h0 + e;
+              part_o[sl * kD + row] = o[e];
               if (row == 0) {
-                part_ml[(slot * r + t) * 2 + 0] = m[t];
-                part_ml[(slot * r + t) * 2 + 1] = l[t];
+                part_ml[sl * 2 + 0] = mfin[e];
+                part_ml[sl * 2 + 1] = l[e];
               }
             }
           }
-          // the unit is split across CTAs: the one that finishes last merges
-          // the other partials into its own (still in registers)
+          // the unit is split across CTAs: for its heads, the warpgroup that
+          // finishes last merges the other partials into its own (still in
+          // registers)
           long long c0, c1;
           unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
           const int np = unit_parts(c0, c1, w.W, w.nc);
-          if (counters != nullptr && arrive_last(counters, u, np, last_flag, row == 0, 1, 128)) {
+          if (counters != nullptr && h0 < r &&
+              arrive_last(counters, u * NWG + wg, np, last_flag_wg, row == 0, bar_id, 128)) {
+            float m[HP];
+#pragma unroll
+            for (int e = 0; e < HP; ++e) m[e] = mfin[e];
             for (long long c = c0; c <= c1; ++c) {
               if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
               // eight heads at a time: their loads go out together
 #pragma unroll
-              for (int t0 = 0; t0 < NP; t0 += 8) {
+              for (int e0 = 0; e0 < HP; e0 += 8) {
                 float mc[8], lc[8], oc[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  if (t0 + e < r) {
-                    const long long sl = (u + c) * r + t0 + e;
-                    mc[e] = __ldcg(part_ml + sl * 2);
-                    lc[e] = __ldcg(part_ml + sl * 2 + 1);
-                    oc[e] = __ldcg(part_o + sl * kD + row);
+                for (int k = 0; k < 8; ++k) {
+                  if (h0 + e0 + k < r) {
+                    const long long sl = (u + c) * r + h0 + e0 + k;
+                    mc[k] = __ldcg(part_ml + sl * 2);
+                    lc[k] = __ldcg(part_ml + sl * 2 + 1);
+                    oc[k] = __ldcg(part_o + sl * kD + row);
                   }
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const int t = t0 + e;
-                  if (t < r) {
-                    const float mn = fmaxf(m[t], mc[e]);
-                    const float sa = ex2(m[t] - mn), sb = ex2(mc[e] - mn);
-                    o[t] = o[t] * sa + oc[e] * sb;
-                    l[t] = l[t] * sa + lc[e] * sb;
-                    m[t] = mn;
+                for (int k = 0; k < 8; ++k) {
+                  const int e = e0 + k;
+                  if (h0 + e < r) {
+                    const float mn = fmaxf(m[e], mc[k]);
+                    const float sa = ex2(m[e] - mn), sb = ex2(mc[k] - mn);
+                    o[e] = o[e] * sa + oc[k] * sb;
+                    l[e] = l[e] * sa + lc[k] * sb;
+                    m[e] = mn;
                   }
                 }
               }
             }
 #pragma unroll
-            for (int t = 0; t < NP; ++t)
-              if (t < r)
-                out[static_cast<size_t>(a0 + t) * kD + row] = __float2bfloat16_rn(o[t] / l[t]);
+            for (int e = 0; e < HP; ++e)
+              if (h0 + e < r)
+                out[static_cast<size_t>(a0 + e) * kD + row] = __float2bfloat16_rn(o[e] / l[e]);
           }
         }
+        m_own = -INFINITY;
 #pragma unroll
-        for (int t = 0; t < NP; ++t) {
-          m[t] = -INFINITY;
-          l[t] = 0.f;
-          o[t] = 0.f;
+        for (int e = 0; e < HP; ++e) {
+          l[e] = 0.f;
+          o[e] = 0.f;
         }
       }
     }
@@ -604,21 +664,21 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NP>
+template <int NP, int NWG>
 cudaError_t launch_np(const DecodeLaunch& a) {
-  using C = TcCfg<NP>;
+  using C = TcCfg<NP, NWG>;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, static_cast<uint64_t>(a.b) * a.h, NP) ||
       !make_map(&mk, a.k_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT) ||
       !make_map(&mv, a.v_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT))
     return cudaErrorInvalidValue;
-  auto kern = decode_tc_kernel<NP>;
+  auto kern = decode_tc_kernel<NP, NWG>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nc);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
@@ -630,7 +690,8 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       &cfg, kern, mq, mk, mv, a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
       static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
-      static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget);
+      static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
+      a.early ? 1 : 0);
 }
 
 }  // namespace
@@ -645,7 +706,7 @@ int tc_ctas_per_sm(int) { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeLaunch& a) {
   const int r = a.h / a.g;
-  return r <= 16 ? launch_np<16>(a) : launch_np<32>(a);
+  return r <= 16 ? launch_np<16, 1>(a) : launch_np<32, 2>(a);
 }
 
 }  // namespace gqa

@@ -355,7 +355,8 @@ namespace {
 // launch.  k_new / v_new null means attention only.
 int decode(const void* q, const void* k_new, const void* v_new, const void* k_cache,
            const void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v,
-           float scale, void* out, int cap, int dtype, void* stream) {
+           float scale, void* out, int cap, int dtype, void* stream, int flags) {
+  if (flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
   if (b < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0)
@@ -387,7 +388,9 @@ int decode(const void* q, const void* k_new, const void* v_new, const void* k_ca
   const size_t ml_bytes = slots * r * 2 * sizeof(float);
   void* ws = nullptr;
   int* counters = nullptr;
-  if (int e = workspace(st, o_bytes + ml_bytes, static_cast<size_t>(b) * g, &ws, &counters))
+  // two arrival counters per unit: the tensor-core kernel may run two
+  // softmax warpgroups, each with its own
+  if (int e = workspace(st, o_bytes + ml_bytes, 2 * static_cast<size_t>(b) * g, &ws, &counters))
     return e;
 
   DecodeLaunch a;
@@ -410,6 +413,7 @@ int decode(const void* q, const void* k_new, const void* v_new, const void* k_ca
   a.v_new = v_new;
   a.k_cache_w = const_cast<void*>(k_cache);
   a.v_cache_w = const_cast<void*>(v_cache);
+  a.early = (flags & GQA_STEP_EARLY_STREAM) != 0;
   a.status = di->status;
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(nc);
@@ -427,15 +431,16 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v, float scale,
                     void* out, int cap, int dtype, void* stream) {
   return gqa::decode(q, nullptr, nullptr, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
-                     out, cap, dtype, stream);
+                     out, cap, dtype, stream, 0);
 }
 
 int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
                     void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k,
-                    int d_v, float scale, void* out, int cap, int dtype, void* stream) {
+                    int d_v, float scale, void* out, int cap, int dtype, int flags,
+                    void* stream) {
   if (!k_new || !v_new) return GQA_ERR_NULL;
   return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale, out,
-                     cap, dtype, stream);
+                     cap, dtype, stream, flags);
 }
 
 int gqa_device_status(void* stream, uint32_t* bits_out) {
@@ -559,14 +564,15 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
   const size_t o_bytes = slots * r * d * sizeof(float);
   const size_t ml_bytes = slots * r * 2 * sizeof(float);
-  if (static_cast<size_t>(b) * g > kNoAllocMaxUnits ||
+  if (2 * static_cast<size_t>(b) * g > kNoAllocMaxUnits ||
       o_bytes + ml_bytes > kNoAllocScratchBytes - kNoAllocCounterBytes)
     return GQA_ERR_SCRATCH_LIMIT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* counters = reinterpret_cast<int*>(nd->scratch);
   unsigned char* parts = nd->scratch + kNoAllocCounterBytes;
   // the per-unit arrival counters must start at zero
-  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(b) * g * sizeof(int), st) != cudaSuccess)
+  if (cudaMemsetAsync(counters, 0, 2 * static_cast<size_t>(b) * g * sizeof(int), st) !=
+      cudaSuccess)
     return GQA_ERR_CUDA;
 
   DecodeLaunch a;
@@ -589,6 +595,7 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   a.v_new = nullptr;
   a.k_cache_w = nullptr;
   a.v_cache_w = nullptr;
+  a.early = false;
   a.status = nd->status;
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(nc);

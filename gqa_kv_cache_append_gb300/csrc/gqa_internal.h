@@ -23,6 +23,7 @@ struct DecodeLaunch {
   const void* v_new;
   void* k_cache_w;       // the caches, written at row L_i - 1 when appending
   void* v_cache_w;
+  bool early;            // stream the first tiles before the dependency wait
   unsigned int* status;  // device status word
   long long budget;      // wait limit in SM cycles
   int nc;                // persistent CTAs

@@ -39,7 +39,7 @@
  *     Kernels never trap and every wait inside them is bounded.
  *   - Calls that overlap on the GPU (different streams) must not share
  *     output buffers.  gqa_decode_attn keeps one split workspace per
- *     (device, stream): partials plus one arrival counter per (sequence, KV
+ *     (device, stream): partials plus two arrival counters per (sequence, KV
  *     head), grown on demand with cudaMalloc (so the first call with a new
  *     largest size on a stream must not be made during stream capture).
  */
@@ -70,6 +70,9 @@ extern "C" {
 #define GQA_ERR_DEVICE      -7  /* current device is not sm_103 */
 #define GQA_ERR_SCRATCH_LIMIT -8 /* gqa_decode_attn_noalloc: the call needs more
                                     scratch than its fixed device buffer holds */
+
+/* flags of gqa_decode_step */
+#define GQA_STEP_EARLY_STREAM 1 /* see gqa_decode_step */
 
 /* bits of the device status word */
 #define GQA_DEV_BAD_SEQ_LEN  1u /* some seq_lens[i] was outside [1, cap] */
@@ -138,10 +141,22 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
  * kernel arithmetic): the CTA that streams a unit's last tile puts the new
  * row into its staged copy of that tile and into the cache.  Same limits,
  * errors and workspace as gqa_decode_attn; a bad L_i appends nothing.
+ *
+ * flags: 0, or GQA_STEP_EARLY_STREAM.  Kernels of this library let the next
+ * launch on the stream be scheduled while they finish, and every launch
+ * waits for its predecessor before reading anything (so by default a call
+ * is ordered after all earlier work, as usual).  With GQA_STEP_EARLY_STREAM
+ * the call may start streaming the cache before the kernels launched ahead
+ * of it on the stream have completed.  The caller guarantees that none of
+ * those kernels writes seq_lens or the rows below L_i - 1 of this call's
+ * caches - true when they are the steps of other layers, whose caches are
+ * other buffers.  q, k_new, v_new and every buffer this call writes are
+ * still used only after the wait.  Other bits: GQA_ERR_UNSUPPORTED.
  */
 int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
                     void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k,
-                    int d_v, float scale, void* out, int cap, int dtype, void* stream);
+                    int d_v, float scale, void* out, int cap, int dtype, int flags,
+                    void* stream);
 
 /*
  * gqa_device_status - read and clear the device status word of the current
@@ -172,8 +187,8 @@ int gqa_selftest_wait_timeout(long long budget_cycles, void* stream);
  *
  * Arguments, layouts, results and error codes are those of gqa_decode_attn,
  * and the two give the same output.  The caller still passes every input
- * and output buffer.  Limits: the first 256 KiB of the array hold one int
- * counter per (sequence, KV head), so b*g <= 65536; the remaining 3.75 MiB
+ * and output buffer.  Limits: the first 256 KiB of the array hold two int
+ * counters per (sequence, KV head), so b*g <= 32768; the remaining 3.75 MiB
  * hold the partials, (b*g + C) * (h/g) * (d_v + 2) * 4 bytes, C being the
  * number of CTAs (at most the SM count, 152 on GB300).  A larger call returns
  * GQA_ERR_SCRATCH_LIMIT and launches nothing.  (The Llama-3-70B-shaped
@@ -182,7 +197,7 @@ int gqa_selftest_wait_timeout(long long budget_cycles, void* stream);
  * The first call on a device does a one-time set-up with that device current
  * (it looks up the device address of the array); make that first call
  * before any stream capture.  All calls share the one array and it keeps the
- * last call's contents: each call clears the b*g counters it uses (an async
+ * last call's contents: each call clears the 2*b*g counters it uses (an async
  * memset on `stream`, before its launch); the partials need no clearing
  * (each call writes every partial it later reads).  Calls that overlap on the
  * GPU (on different streams, or from different threads) race on the array

@@ -95,7 +95,7 @@ def test_kv_append_host_checks(kw, code):
 def test_decode_step_host_checks():
     b = _lib()
     f = b.lib.gqa_decode_step
-    args = [A, A, A, A, A, A, 2, 8, 2, 128, 128, 0.1, A, 64, 1, None]
+    args = [A, A, A, A, A, A, 2, 8, 2, 128, 128, 0.1, A, 64, 1, 0, None]
     assert f(*args[:1], 0, *args[2:]) == -1          # k_new null
     assert f(*args[:2], 0, *args[3:]) == -1          # v_new null
     assert f(*args[:1], A + 8, *args[2:]) == -4      # k_new misaligned
@@ -103,6 +103,9 @@ def test_decode_step_host_checks():
     bad[7] = 6
     bad[8] = 4
     assert f(*bad) == -2                             # h % g
+    bad = list(args)
+    bad[15] = 6
+    assert f(*bad) == -5                             # unknown flag bits
 
 
 def test_null_status_pointer():

@@ -121,6 +121,41 @@ def test_fused_step_matches_two_calls_bitwise():
     assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
 
 
+@pytest.mark.parametrize("b,h,g,cap,lens", [
+    (8, 64, 8, 2000, None),                  # units split in-kernel
+    (2, 32, 1, 9000, [9000, 4500]),          # few long units: combine kernel
+])
+def test_early_stream_matches_ordered_calls(b, h, g, cap, lens):
+    """Six layers back to back with GQA_STEP_EARLY_STREAM give the same
+    outputs and caches, bit for bit, as the default ordered calls."""
+    B = _b()
+    cfg = cfg_of("bf16", b, h, g, 128, cap, seed=b + g)
+    lens = np.asarray(lens if lens is not None else [cap - 37 * i for i in range(b)], np.int32)
+    layers = [make_layer(cfg, l, "cuda", lens=lens) for l in range(6)]
+    results = []
+    for flags in (0, B.GQA_STEP_EARLY_STREAM):
+        kcs = [x["k_cache"].clone() for x in layers]
+        vcs = [x["v_cache"].clone() for x in layers]
+        outs = [torch.empty((b, h, 128), dtype=torch.bfloat16, device="cuda") for _ in layers]
+        torch.cuda.synchronize()
+        for rep in range(3):
+            for l, x in enumerate(layers):
+                B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], kcs[l], vcs[l], x["seq_lens"],
+                                  b, h, g, 128, 128, cfg.scale, outs[l], flags=flags)
+        torch.cuda.synchronize()
+        results.append((outs, kcs, vcs))
+    assert B.gqa_device_status() == 0
+    for l in range(len(layers)):
+        assert torch.equal(results[0][0][l], results[1][0][l])
+        assert torch.equal(results[0][1][l], results[1][1][l])
+        assert torch.equal(results[0][2][l], results[1][2][l])
+    # and the ordered result is right
+    x = layers[0]
+    args = [to_np(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
+    ref, _, _ = oracle.decode_step(*args, lens, g, cfg.scale, dtype="bf16")
+    assert_close(oracle.widen(to_np(results[1][0][0])[0], "bf16"), ref, "bf16")
+
+
 def test_fused_step_bad_length_appends_nothing():
     B = _b()
     cfg = cfg_of("bf16", 3, 16, 2, 128, 300, seed=8)
