@@ -245,6 +245,10 @@ def run_ours(args, rank, local_rank, world):
         base = dataclasses.replace(base, g=args.g)
     if args.h:
         base = dataclasses.replace(base, h=args.h)
+    if args.b:
+        base = dataclasses.replace(base, b=args.b)
+    if args.cap:
+        base = dataclasses.replace(base, cap=args.cap)
     if args.layers:
         base = dataclasses.replace(base, layers=min(args.layers, base.layers))
     lens = seq_lens_for(base)
@@ -478,6 +482,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--g", type=int, default=None, help="KV heads (for the g-knob sweep)")
     ap.add_argument("--h", type=int, default=None, help="query heads (shape studies)")
+    ap.add_argument("--b", type=int, default=None, help="sequences (shape studies)")
+    ap.add_argument("--cap", type=int, default=None,
+                    help="cache capacity = length of full sequences (shape studies)")
     ap.add_argument("--ordered", action="store_true",
                     help="no early streaming: each layer waits for the previous one")
     ap.add_argument("--separate", action="store_true",
