@@ -32,6 +32,7 @@ GQA_STEP_EARLY_STREAM = 1
 
 GQA_DEV_BAD_SEQ_LEN = 1
 GQA_DEV_WAIT_TIMEOUT = 2
+GQA_DEV_INTERNAL = 4
 
 # every function the header declares, with its C signature
 _VP, _I, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong

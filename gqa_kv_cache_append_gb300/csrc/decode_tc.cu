@@ -65,7 +65,10 @@ struct TcCfg {
   static constexpr int OFF_BAR = OFF_ALPHA + 2 * NP * 4;
   static constexpr int NBAR = 3 * kStages + 2 * 7 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for 1024-B alignment
+  // The dynamic shared-memory base is 1024-byte aligned (the swizzled
+  // layouts need it; the kernel checks), so no slack is requested: leaving
+  // room on the SM lets small kernels (the combine) run beside a decode CTA.
+  static constexpr int SMEM = OFF_MISC + 16;
   static constexpr int NCOLS = 4 * NP;               // S0 S1 O0 O1
   // P rows are NP * 2 bytes: 32 B (NP=16) or 64 B (NP=32) swizzle atoms
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
@@ -103,10 +106,13 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
                      unsigned int* status, long long budget, int early) {
   using C = TcCfg<NP, NWG>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   const uint32_t s_base = smem_u32(sm);
+  if (s_base & 1023u) {  // never seen; the layout would not fit the allocation
+    if (threadIdx.x == 0) atomicOr(status, GQA_DEV_INTERNAL);
+    return;
+  }
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);  // [NWG][2][HP][4]
   float* max_sm = reinterpret_cast<float*>(sm + C::OFF_MAX);
   float* alpha_sm = reinterpret_cast<float*>(sm + C::OFF_ALPHA);

@@ -77,6 +77,8 @@ extern "C" {
 /* bits of the device status word */
 #define GQA_DEV_BAD_SEQ_LEN  1u /* some seq_lens[i] was outside [1, cap] */
 #define GQA_DEV_WAIT_TIMEOUT 2u /* a bounded in-kernel wait gave up */
+#define GQA_DEV_INTERNAL     4u /* a launch found its shared memory misaligned
+                                   and did nothing (not expected to happen) */
 
 /*
  * gqa_kv_append - write the new token's K and V rows into the caches.
