@@ -271,7 +271,10 @@ def run_ours(args, rank, local_rank, world):
             x[key] = packed[key][l]
     out_all = torch.empty((cfg.layers, cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device=dev)
     outs = [out_all[l] for l in range(cfg.layers)]
-    stream = torch.cuda.current_stream(dev)
+    # --graph: the step is captured once in a CUDA graph and replayed; the
+    # capture needs a stream of its own (and calls warmed up on it first)
+    stream = torch.cuda.Stream(dev) if args.graph else torch.cuda.current_stream(dev)
+    torch.cuda.set_stream(stream)
     sb = step_bytes(cfg, lens)
 
     def layer_call(l, x):
@@ -301,6 +304,15 @@ def run_ours(args, rank, local_rank, world):
         step()
     torch.cuda.synchronize(dev)
     assert B.gqa_device_status(stream) == 0
+    run_step = step
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        run_step = graph.replay
+        for _ in range(args.warmup):
+            run_step()
+        torch.cuda.synchronize(dev)
 
     # ---- device-resident timing: K steps back to back, CUDA events on the
     # launching stream around the whole region.  Nothing is recorded between
@@ -316,7 +328,7 @@ def run_ours(args, rank, local_rank, world):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        step()
+        run_step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
@@ -350,15 +362,23 @@ def run_ours(args, rank, local_rank, world):
             layer_call(l, x)
         host_out.copy_(out_all, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
+    run_e2e = e2e_step
+    if args.graph:
         e2e_step()
+        torch.cuda.synchronize(dev)
+        graph_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_e2e, stream=stream):
+            e2e_step()
+        run_e2e = graph_e2e.replay
+    for _ in range(max(1, args.warmup)):
+        run_e2e()
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        e2e_step()
+        run_e2e()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist, dev)
@@ -394,6 +414,7 @@ def run_ours(args, rank, local_rank, world):
             "l2": "inputs larger than L2: every step streams all layers' K/V "
                   f"({sb['step'] / 2**30:.2f} GiB, L2 {l2 / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
+            "launch": "CUDA graph" if args.graph else "stream",
         },
         "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
         "layer_call_gbs_per_gpu": round(achieved, 2),
@@ -485,6 +506,8 @@ def main(argv=None):
     ap.add_argument("--b", type=int, default=None, help="sequences (shape studies)")
     ap.add_argument("--cap", type=int, default=None,
                     help="cache capacity = length of full sequences (shape studies)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the step (and the end-to-end step) in a CUDA graph")
     ap.add_argument("--ordered", action="store_true",
                     help="no early streaming: each layer waits for the previous one")
     ap.add_argument("--separate", action="store_true",

@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gqa_device.cuh"
 #include "gqa_internal.h"
 
@@ -381,9 +383,16 @@ template <typename DT, int D, int RMAX>
 cudaError_t launch_t(const DecodeLaunch& a) {
   using C = SimtCfg<DT, D, RMAX>;
   auto kern = decode_simt_kernel<DT, D, RMAX>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is set once per device (not during a capture)
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(configured.load() & (1ull << dev))) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(1ull << dev);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nc);
   cfg.blockDim = dim3(kThreads);

@@ -40,6 +40,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gqa_device.cuh"
 #include "gqa_internal.h"
 
@@ -679,9 +681,16 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       !make_map(&mv, a.v_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT))
     return cudaErrorInvalidValue;
   auto kern = decode_tc_kernel<NP, NWG>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is set once per device (not during a capture)
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(configured.load() & (1ull << dev))) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(1ull << dev);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nc);
   cfg.blockDim = dim3(C::THREADS);

@@ -216,6 +216,11 @@ int workspace(cudaStream_t stream, size_t bytes, size_t units, void** ptr, int**
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace& ws = g_ws[{dev, stream}];
   if (ws.bytes < bytes || ws.units < units) {
+    // growing needs cudaMalloc, which a stream capture forbids: a captured
+    // call must be preceded by an uncaptured one of at least its size
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      return GQA_ERR_CUDA;
     // the previous buffers may still be used by queued work on `stream`
     if ((ws.ptr || ws.counters) && cudaStreamSynchronize(stream) != cudaSuccess)
       return GQA_ERR_CUDA;
@@ -246,6 +251,7 @@ int workspace(cudaStream_t stream, size_t bytes, size_t units, void** ptr, int**
   }
   const unsigned epoch = g_reset_epoch.load();
   if (ws.epoch != epoch) {
+    // (an async memset; allowed in a capture, where it becomes a graph node)
     if (cudaMemsetAsync(ws.counters, 0, ws.units * sizeof(int), stream) != cudaSuccess)
       return GQA_ERR_CUDA;
     ws.epoch = epoch;

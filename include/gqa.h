@@ -40,8 +40,11 @@
  *   - Calls that overlap on the GPU (different streams) must not share
  *     output buffers.  gqa_decode_attn keeps one split workspace per
  *     (device, stream): partials plus two arrival counters per (sequence, KV
- *     head), grown on demand with cudaMalloc (so the first call with a new
- *     largest size on a stream must not be made during stream capture).
+ *     head), grown on demand with cudaMalloc.  Calls can be captured in a
+ *     CUDA graph (stream capture): make one uncaptured call of at least the
+ *     captured size on the stream first; a captured call that would have to
+ *     grow the workspace returns GQA_ERR_CUDA.  Launches keep their
+ *     programmatic dependencies in the graph.
  */
 #ifndef GQA_H
 #define GQA_H

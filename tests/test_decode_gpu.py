@@ -156,6 +156,38 @@ def test_early_stream_matches_ordered_calls(b, h, g, cap, lens):
     assert_close(oracle.widen(to_np(results[1][0][0])[0], "bf16"), ref, "bf16")
 
 
+@pytest.mark.parametrize("b,h,g,cap", [(4, 64, 8, 1500), (2, 32, 1, 6000)])
+def test_graph_capture_replay(b, h, g, cap):
+    """Several layers' steps captured in a CUDA graph and replayed give the
+    same outputs, bit for bit, as the same calls made eagerly (the append is
+    idempotent for fixed lengths)."""
+    B = _b()
+    cfg = cfg_of("bf16", b, h, g, 128, cap, seed=h + g)
+    lens = np.asarray([cap - 71 * i for i in range(b)], np.int32)
+    layers = [make_layer(cfg, l, "cuda", lens=lens) for l in range(4)]
+    s = torch.cuda.Stream()
+    eager = [torch.empty((b, h, 128), dtype=torch.bfloat16, device="cuda") for _ in layers]
+    replayed = [torch.full_like(o, 9.0) for o in eager]
+
+    def step(outs):
+        for x, o in zip(layers, outs):
+            B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                              x["seq_lens"], b, h, g, 128, 128, cfg.scale, o,
+                              flags=B.GQA_STEP_EARLY_STREAM, stream=s)
+    with torch.cuda.stream(s):
+        step(eager)            # grows the workspace of stream s before the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step(replayed)
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    assert B.gqa_device_status(s) == 0
+    for e, r_ in zip(eager, replayed):
+        assert torch.equal(e, r_)
+
+
 def test_fused_step_bad_length_appends_nothing():
     B = _b()
     cfg = cfg_of("bf16", 3, 16, 2, 128, 300, seed=8)
