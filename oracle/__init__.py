@@ -15,4 +15,7 @@ from .oracle import (  # noqa: F401
     kv_cache_bytes_per_token,
     kv_cache_bytes,
     attention_multiplications,
+    kv_append_multi,
+    grouped_decode_attention_multi,
+    decode_step_multi,
 )

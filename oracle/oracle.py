@@ -55,6 +55,9 @@ __all__ = [
     "kv_cache_bytes_per_token",
     "kv_cache_bytes",
     "attention_multiplications",
+    "kv_append_multi",
+    "grouped_decode_attention_multi",
+    "decode_step_multi",
 ]
 
 
@@ -195,6 +198,71 @@ def decode_step(q, k_cache, v_cache, k_new, v_new, seq_lens, g: int,
     """
     kc, vc = kv_append(k_cache, v_cache, k_new, v_new, seq_lens)
     o = grouped_decode_attention(q, kc, vc, seq_lens, g, scale, dtype)
+    return o, kc, vc
+
+
+# ---------------------------------------------------------------------------
+# n new tokens per step ([MQA review] §2.3: n queries per sequence in one
+# step with an additive mask [b, h, n, m]; causal self-attention: the query
+# at position P attends positions <= P)
+# ---------------------------------------------------------------------------
+def kv_append_multi(k_cache, v_cache, k_new, v_new, seq_lens):
+    """Write n new K/V rows per (sequence, KV head): k_new [b, n, g, d_k],
+    v_new [b, n, g, d_v]; row L_i - n + s of the cache receives token s.
+    Bit-exact copies; every other row is left as it was."""
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    b, g, cap, _ = kc.shape
+    n = np.asarray(k_new).shape[1]
+    lens = _check_lens(seq_lens, b, cap)
+    if np.any(lens < n):
+        raise ValueError("every seq_len must be at least the number of new tokens")
+    for i in range(b):
+        for s_ in range(n):
+            row = int(lens[i]) - n + s_
+            for j in range(g):
+                kc[i, j, row, :] = k_new[i, s_, j, :]
+                vc[i, j, row, :] = v_new[i, s_, j, :]
+    return kc, vc
+
+
+def grouped_decode_attention_multi(q, k_cache, v_cache, seq_lens, g: int,
+                                   scale: float, dtype: str = "f64") -> np.ndarray:
+    """o [b, n, h, d_v] for n queries per sequence at positions
+    L_i - n + s (s = 0..n-1), each attending the cached positions p <= its
+    own (the additive causal mask of [MQA review] §2.3: 0 where p <= P,
+    -inf elsewhere), heads grouped as in grouped_decode_attention."""
+    q64 = widen(q, dtype)
+    k64 = widen(k_cache, dtype)
+    v64 = widen(v_cache, dtype)
+    b, n, h, dk = q64.shape
+    dv = v64.shape[-1]
+    cap = k64.shape[2]
+    lens = _check_lens(seq_lens, b, cap)
+    if np.any(lens < n):
+        raise ValueError("every seq_len must be at least the number of queries")
+    r = h // g
+    o = np.empty((b, n, h, dv), dtype=np.float64)
+    for i in range(b):
+        L = int(lens[i])
+        qg = q64[i].reshape(n, g, r, dk)                       # [n, g, r, dk]
+        s = scale * np.einsum("sjtc,jpc->sjtp", qg, k64[i, :, :L, :])
+        pos = np.arange(L)[None, :]
+        own = (L - n + np.arange(n))[:, None]
+        mask = np.where(pos <= own, 0.0, -np.inf)              # [n, L]
+        s = s + mask[:, None, None, :]
+        s = s - s.max(axis=-1, keepdims=True)
+        e = np.exp(s)
+        w = e / e.sum(axis=-1, keepdims=True)
+        o[i] = np.einsum("sjtp,jpv->sjtv", w, v64[i, :, :L, :]).reshape(n, h, dv)
+    return o
+
+
+def decode_step_multi(q, k_cache, v_cache, k_new, v_new, seq_lens, g: int,
+                      scale: float, dtype: str = "f64"):
+    """Append the n new rows, then attend causally (one step, n tokens)."""
+    kc, vc = kv_append_multi(k_cache, v_cache, k_new, v_new, seq_lens)
+    o = grouped_decode_attention_multi(q, kc, vc, seq_lens, g, scale, dtype)
     return o, kc, vc
 
 

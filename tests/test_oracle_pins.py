@@ -436,3 +436,83 @@ def test_pins_catch_appending_at_the_wrong_row(monkeypatch):
         return kc, vc
     monkeypatch.setattr(orc, "kv_append", wrong)
     assert not _pins_pass()
+
+
+# --------------------------------------------------------------------------
+# n new tokens per step (causal): the batched masked form of §2.3
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("b,h,g,n,cap", [(2, 4, 2, 3, 9), (1, 6, 1, 4, 4), (2, 8, 8, 2, 11),
+                                         (3, 6, 3, 1, 7)])
+def test_multi_token_step_is_the_batched_causal_rows(b, h, g, n, cap):
+    """Appending n tokens and attending causally equals the last n rows of
+    the §2.3 batched form over the whole sequence with its causal mask."""
+    rng = np.random.default_rng(100 + n * h)
+    lens = rng.integers(n, cap + 1, size=b)
+    r = h // g
+    scale = 0.35
+    kc = rng.standard_normal((b, g, cap, 5))
+    vc = rng.standard_normal((b, g, cap, 4))
+    kn = rng.standard_normal((b, n, g, 5))
+    vn = rng.standard_normal((b, n, g, 4))
+    q = rng.standard_normal((b, n, h, 5))
+    o, k2, v2 = oracle.decode_step_multi(q, kc, vc, kn, vn, lens, g, scale)
+    for i in range(b):
+        L = int(lens[i])
+        # the full sequence as the batched form sees it: old rows then new
+        K = k2[i:i + 1, :, :L]
+        V = v2[i:i + 1, :, :L]
+        Q = np.zeros((1, h, L, 5))
+        Q[0, :, L - n:] = q[i].transpose(1, 0, 2)
+        full = _batched_causal(Q, np.repeat(K, r, axis=1), np.repeat(V, r, axis=1), scale)
+        for s_ in range(n):
+            assert np.max(np.abs(o[i, s_] - full[0, :, L - n + s_])) < TOL
+        # the appended rows and nothing else changed
+        for j in range(g):
+            for p in range(cap):
+                if L - n <= p < L:
+                    assert np.array_equal(k2[i, j, p], kn[i, p - (L - n), j])
+                else:
+                    assert np.array_equal(k2[i, j, p], kc[i, j, p])
+
+
+def test_multi_token_step_with_one_token_is_the_single_step():
+    rng = np.random.default_rng(55)
+    b, h, g, cap = 3, 8, 2, 10
+    lens = np.array([1, 10, 6])
+    kc = rng.standard_normal((b, g, cap, 6))
+    vc = rng.standard_normal((b, g, cap, 6))
+    kn = rng.standard_normal((b, 1, g, 6))
+    vn = rng.standard_normal((b, 1, g, 6))
+    q = rng.standard_normal((b, 1, h, 6))
+    o1, k1, v1 = oracle.decode_step_multi(q, kc, vc, kn, vn, lens, g, 0.5)
+    o2, k2, v2 = oracle.decode_step(q[:, 0], kc, vc, kn[:, 0], vn[:, 0], lens, g, 0.5)
+    assert np.max(np.abs(o1[:, 0] - o2)) < TOL
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+
+
+def test_multi_token_bruteforce_loops():
+    rng = np.random.default_rng(66)
+    b, h, g, n, cap = 2, 4, 2, 3, 8
+    lens = np.array([3, 8])
+    q = rng.standard_normal((b, n, h, 3))
+    k = rng.standard_normal((b, g, cap, 3))
+    v = rng.standard_normal((b, g, cap, 2))
+    o = oracle.grouped_decode_attention_multi(q, k, v, lens, g, 0.8)
+    r = h // g
+    for i in range(b):
+        L = int(lens[i])
+        for s_ in range(n):
+            P = L - n + s_
+            for a in range(h):
+                j = a // r
+                want = _dot_product_attention_loops(
+                    [0.8 * x for x in q[i, s_, a]], k[i, j, :P + 1].tolist(),
+                    v[i, j, :P + 1].tolist())
+                assert np.max(np.abs(np.array(want) - o[i, s_, a])) < TOL
+
+
+def test_multi_token_rejects_lengths_below_n():
+    kc = np.zeros((1, 1, 5, 2))
+    kn = np.zeros((1, 3, 1, 2))
+    with pytest.raises(ValueError):
+        oracle.kv_append_multi(kc, kc, kn, kn, [2])
