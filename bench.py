@@ -151,10 +151,10 @@ def smi_id(local_index: int) -> str:
 # ---------------------------------------------------------------------------
 # byte counts
 # ---------------------------------------------------------------------------
-def step_bytes(cfg, lens) -> dict:
+def step_bytes(cfg, lens, n: int = 1) -> dict:
     from gqa_kv_cache_append_gb300.inputs import layer_bytes
-    attn = layer_bytes(cfg, lens)
-    append = 2 * 2 * cfg.b * cfg.g * cfg.d * cfg.elt   # read + write of k_new, v_new rows
+    attn = layer_bytes(cfg, lens, n)
+    append = 2 * 2 * cfg.b * n * cfg.g * cfg.d * cfg.elt   # read + write of the new K/V rows
     return {"attn_per_layer": attn, "append_per_layer": append,
             "step": cfg.layers * (attn + append)}
 
@@ -168,10 +168,11 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profiled_traffic(kernel_src: str, workload: str):
+def profiled_traffic(kernel_src: str, workload: str, n: int = 1):
     """dram bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (matched by hash), else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
+    tag = workload if n == 1 else f"{workload}_n{n}"
+    path = os.path.join(ROOT, "profiles", f"decode_tc_{tag}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -188,14 +189,15 @@ def profiled_traffic(kernel_src: str, workload: str):
 # ---------------------------------------------------------------------------
 # the oracle on a bounded sample (CPU baseline and reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096):
+def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096, n: int = 1):
     """Time the float64 oracle's decode step on whole units (one sequence, one
-    KV head, its r query heads) of layer 0 of the workload, drawn on the CPU
-    with the same generator recipe, until about target_s seconds of work.
-    Returns (GB/s of algorithmic bytes, seconds, units, bytes)."""
+    KV head, its r query heads; n new tokens each) of layer 0 of the
+    workload, drawn on the CPU with the same generator recipe, until about
+    target_s seconds of work.  Returns (GB/s of algorithmic bytes, seconds,
+    units, bytes)."""
     import torch
     import oracle
-    from gqa_kv_cache_append_gb300.inputs import make_layer, seq_lens_for
+    from gqa_kv_cache_append_gb300.inputs import make_layer, make_layer_multi, seq_lens_for
     import dataclasses
 
     lens = seq_lens_for(cfg)
@@ -205,7 +207,10 @@ def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096):
     while spent < target_s and done_units < max_units:
         L = int(lens[i % len(lens)])
         sub = dataclasses.replace(one, seed=cfg.seed * 7919 + i)
-        x = make_layer(sub, 0, "cpu", lens=np.array([L], dtype=np.int32))
+        if n == 1:
+            x = make_layer(sub, 0, "cpu", lens=np.array([L], dtype=np.int32))
+        else:
+            x = make_layer_multi(sub, n, 0, "cpu", lens=np.array([L], dtype=np.int32))
 
         def np_(t):
             t = t.contiguous()
@@ -215,10 +220,13 @@ def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096):
         tag = np_(x["q"])[1]
         arrs = [np_(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
         t0 = time.perf_counter()
-        oracle.decode_step(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
+        if n == 1:
+            oracle.decode_step(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
+        else:
+            oracle.decode_step_multi(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
         spent += time.perf_counter() - t0
         done_units += cfg.g
-        done_bytes += L * cfg.g * 2 * cfg.d * cfg.elt + 2 * cfg.h * cfg.d * cfg.elt
+        done_bytes += L * cfg.g * 2 * cfg.d * cfg.elt + 2 * n * cfg.h * cfg.d * cfg.elt
         i += 1
     return done_bytes / spent / 1e9, spent, done_units, done_bytes
 
@@ -234,9 +242,10 @@ def blas_threads() -> int:
 def run_ours(args, rank, local_rank, world):
     import torch
     from gqa_kv_cache_append_gb300 import binding as B
-    from gqa_kv_cache_append_gb300.inputs import make_layer, seq_lens_for, workload
+    from gqa_kv_cache_append_gb300.inputs import make_layer, make_layer_multi, seq_lens_for, workload
     import dataclasses
 
+    n = args.tokens
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
@@ -251,17 +260,21 @@ def run_ours(args, rank, local_rank, world):
         base = dataclasses.replace(base, cap=args.cap)
     if args.layers:
         base = dataclasses.replace(base, layers=min(args.layers, base.layers))
+    if n > 1:
+        # n new tokens per step: the workload's shapes with plain N(0, 1) data
+        base = dataclasses.replace(base, kind="plain")
     lens = seq_lens_for(base)
     # a workload whose layers all fit in L2 is rotated through independent
     # replicas (extra layers of the same shape) until one step streams at
     # least 4x the L2 size, so every step reads K/V from HBM
-    from gqa_kv_cache_append_gb300.inputs import layer_bytes as _lb
+    from gqa_kv_cache_append_gb300.inputs import layer_bytes as _lb, layer_flops
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_layer = _lb(base, lens)
+    per_layer = _lb(base, lens, n)
     if base.layers * per_layer < 4 * l2 and not args.layers:
         base = dataclasses.replace(base, layers=-(-4 * l2 // per_layer))
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
-    layers = [make_layer(cfg, l, dev) for l in range(cfg.layers)]
+    layers = [make_layer(cfg, l, dev) if n == 1 else make_layer_multi(cfg, n, l, dev)
+              for l in range(cfg.layers)]
     # the step's per-layer inputs and outputs live in one packed buffer each
     # (layer-major), so the end-to-end leg moves them with one copy apiece
     packed = {}
@@ -269,16 +282,30 @@ def run_ours(args, rank, local_rank, world):
         packed[key] = torch.stack([x[key] for x in layers]).contiguous()
         for l, x in enumerate(layers):
             x[key] = packed[key][l]
-    out_all = torch.empty((cfg.layers, cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device=dev)
+    out_shape = (cfg.b, cfg.h, cfg.d) if n == 1 else (cfg.b, n, cfg.h, cfg.d)
+    out_all = torch.empty((cfg.layers, *out_shape), dtype=cfg.torch_dtype, device=dev)
     outs = [out_all[l] for l in range(cfg.layers)]
     # --graph: the step is captured once in a CUDA graph and replayed; the
     # capture needs a stream of its own (and calls warmed up on it first)
     stream = torch.cuda.Stream(dev) if args.graph else torch.cuda.current_stream(dev)
     torch.cuda.set_stream(stream)
-    sb = step_bytes(cfg, lens)
+    sb = step_bytes(cfg, lens, n)
+    early = 0 if args.ordered else B.GQA_STEP_EARLY_STREAM
 
     def layer_call(l, x):
-        if args.separate:
+        if n > 1:
+            if args.separate:
+                B.gqa_kv_append_multi(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                      x["seq_lens"], cfg.b, n, cfg.g, cfg.d, cfg.d, stream=stream)
+                B.gqa_decode_attn_multi(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
+                                        n, cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l],
+                                        stream=stream)
+            else:
+                B.gqa_decode_step_multi(x["q"], x["k_new"], x["v_new"], x["k_cache"],
+                                        x["v_cache"], x["seq_lens"], cfg.b, n, cfg.h, cfg.g,
+                                        cfg.d, cfg.d, cfg.scale, outs[l], flags=early,
+                                        stream=stream)
+        elif args.separate:
             B.gqa_kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"],
                             cfg.b, cfg.g, cfg.d, cfg.d, stream=stream)
             B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
@@ -289,8 +316,7 @@ def run_ours(args, rank, local_rank, world):
             # finishes (GQA_STEP_EARLY_STREAM's contract)
             B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
                               x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale,
-                              outs[l], flags=0 if args.ordered else B.GQA_STEP_EARLY_STREAM,
-                              stream=stream)
+                              outs[l], flags=early, stream=stream)
 
     def step(ev=None):
         for l, x in enumerate(layers):
@@ -391,7 +417,7 @@ def run_ours(args, rank, local_rank, world):
     call_bytes = sb["attn_per_layer"] + sb["append_per_layer"]
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
-    traffic = profiled_traffic(src, args.workload)
+    traffic = profiled_traffic(src, args.workload, n)
     launches_per_step = (2 if args.separate else 1) * cfg.layers
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     line = {
@@ -415,13 +441,16 @@ def run_ours(args, rank, local_rank, world):
                   f"({sb['step'] / 2**30:.2f} GiB, L2 {l2 / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
             "launch": "CUDA graph" if args.graph else "stream",
+            "tokens_per_step": n,
         },
         "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
+        "attn_tflops_per_gpu": round(layer_flops(cfg, lens, n) / (attn_avg_ms * 1e-3) / 1e12, 2),
         "layer_call_gbs_per_gpu": round(achieved, 2),
         "pct_of_nominal_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
         "roofline": {
             "bound": "hbm",
             "kernel": ("gqa_kv_append + gqa_decode_attn" if args.separate else "gqa_decode_step")
+                      + ("_multi" if n > 1 else "")
                       + f" ({'decode_tc_kernel' if cfg.dtype == 'bf16' and cfg.d == 128 else 'decode_simt_kernel'})",
             "achieved": round(achieved, 2),
             "peak": peaks["hbm_gbs"],
@@ -447,7 +476,7 @@ def run_ours(args, rank, local_rank, world):
         "device_status": status,
     }
     if not args.no_cpu_baseline:
-        gbs, spent, units, nbytes = oracle_sample(base, target_s=args.cpu_seconds)
+        gbs, spent, units, nbytes = oracle_sample(base, target_s=args.cpu_seconds, n=n)
         line["cpu_baseline"] = {
             "value": round(gbs, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{units} (sequence, KV head) units of {cfg.name} layer-shaped data "
@@ -460,14 +489,18 @@ def run_reference(args, rank, world):
     """The reference arm: the float64 oracle on the host cores, timed per
     step on a bounded sample of the workload; rank 0 only."""
     from gqa_kv_cache_append_gb300.inputs import seq_lens_for, workload
+    import dataclasses
     if rank != 0:
         return None
     cfg = workload(args.workload)
+    n = args.tokens
+    if n > 1:
+        cfg = dataclasses.replace(cfg, kind="plain")
     per_step_s = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     vals = []
     total_units = total_bytes = 0
     for k in range(args.warmup + args.steps):
-        gbs, spent, units, nbytes = oracle_sample(cfg, target_s=per_step_s)
+        gbs, spent, units, nbytes = oracle_sample(cfg, target_s=per_step_s, n=n)
         if k >= args.warmup:
             vals.append(gbs)
             total_units += units
@@ -482,7 +515,7 @@ def run_reference(args, rank, world):
         "data": "synthetic (seeded N(0,1), shapes of the workload)",
         "config": {"workload": cfg.name, "layers": cfg.layers, "b": cfg.b, "h": cfg.h,
                    "g": cfg.g, "d_head": cfg.d, "seq_len": int(np.max(lens)),
-                   "parallelism": "host cores"},
+                   "parallelism": "host cores", "tokens_per_step": n},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle",
                          "sample": f"{total_units} (sequence, KV head) units over {args.steps} "
@@ -512,6 +545,8 @@ def main(argv=None):
                     help="no early streaming: each layer waits for the previous one")
     ap.add_argument("--separate", action="store_true",
                     help="time gqa_kv_append + gqa_decode_attn instead of gqa_decode_step")
+    ap.add_argument("--tokens", type=int, default=1,
+                    help="new tokens per sequence per step (causal; speculative / chunked decode)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small profiling cases)")
     args = ap.parse_args(argv)

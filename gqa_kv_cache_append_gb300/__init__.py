@@ -5,7 +5,8 @@ sm_103a under csrc/).  ``binding`` is its ctypes binding, loaded on first use
 of one of the names below; ``inputs`` holds the seeded synthetic workloads.
 """
 _BINDING = {
-    "gqa_kv_append", "gqa_decode_attn", "gqa_decode_step", "gqa_decode_attn_noalloc", "gqa_device_status",
+    "gqa_kv_append", "gqa_decode_attn", "gqa_decode_step", "gqa_decode_attn_noalloc",
+    "gqa_kv_append_multi", "gqa_decode_attn_multi", "gqa_decode_step_multi", "gqa_device_status",
     "gqa_selftest_wait_timeout", "gqa_version", "decode_step", "GqaError",
     "status_string",
 }

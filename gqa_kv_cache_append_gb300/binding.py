@@ -43,6 +43,11 @@ SIGNATURES = {
                                      _VP]),
     "gqa_decode_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I,
                              _I, _I, _VP]),
+    "gqa_kv_append_multi": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "gqa_decode_attn_multi": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _I, _I,
+                                   _VP]),
+    "gqa_decode_step_multi": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F,
+                                   _VP, _I, _I, _I, _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -155,6 +160,42 @@ def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, sc
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(h),
         int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
         _dtype(q, dtype), _stream(stream)))
+
+
+def gqa_kv_append_multi(k_new, v_new, k_cache, v_cache, seq_lens, b, n, g, d_k, d_v,
+                        cap=None, dtype=None, stream=None) -> None:
+    """Write rows seq_lens[i] - n .. seq_lens[i] - 1 of every (i, j) of the
+    caches from k_new / v_new [b, n, g, d] (in place)."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_kv_append_multi", lib.gqa_kv_append_multi(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        int(b), int(n), int(g), int(d_k), int(d_v), int(cap), _dtype(k_cache, dtype),
+        _stream(stream)))
+
+
+def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v, scale,
+                          out, cap=None, dtype=None, stream=None) -> None:
+    """n queries per sequence (q, out [b, n, h, d]) with the causal mask:
+    token s sees positions p <= seq_lens[i] - n + s."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_decode_attn_multi", lib.gqa_decode_attn_multi(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(n), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
+        _dtype(q, dtype), _stream(stream)))
+
+
+def gqa_decode_step_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, g, d_k,
+                          d_v, scale, out, cap=None, dtype=None, flags=0,
+                          stream=None) -> None:
+    """Append the n new rows and attend causally, in one launch."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_decode_step_multi", lib.gqa_decode_step_multi(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out),
+        int(cap), _dtype(q, dtype), int(flags), _stream(stream)))
 
 
 def gqa_device_status(stream=None) -> int:

@@ -16,9 +16,12 @@
 //      bhv"), rescaled by each tile's factor.
 // A segment's end writes the normalised output; a unit split across CTAs
 // writes a partial instead, and the CTA that finishes the unit last merges
-// the partials (log-sum-exp).  With k_new / v_new given, the KV append is
-// fused in: the CTA owning a unit's last tile patches row L_i - 1 of its
-// staged tile with the new token and writes that row to the cache.
+// the partials (log-sum-exp).  With n new tokens per sequence the "heads"
+// are the n * r query rows of the group (token-major) and token s, at
+// position L_i - n + s, sees positions p <= L_i - n + s (the causal mask of
+// the batched form, §2.3).  With k_new / v_new given, the KV append is
+// fused in: the CTA owning a tile that holds rows L_i - n .. L_i - 1 patches
+// them in its staged tile with the new tokens and writes them to the cache.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -89,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float* __restrict__ part_o, float* __restrict__ part_ml,
                        int* __restrict__ counters, const uint4* __restrict__ k_new,
                        const uint4* __restrict__ v_new, uint4* __restrict__ k_cache_w,
-                       uint4* __restrict__ v_cache_w, unsigned int* status, long long budget) {
+                       uint4* __restrict__ v_cache_w, unsigned int* status, long long budget,
+                       int nq) {
   using C = SimtCfg<DT, D, RMAX>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
+  const int nr = nq * r;  // query rows ("heads" below) per KV head: t = s * r + head
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -124,11 +129,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sL[t] = 0.f;
     sA[t] = 0.f;
   }
-  if (warp == 1 && blockIdx.x == 0) report_bad_lengths(lens, b, cap, status);
+  if (warp == 1 && blockIdx.x == 0) report_bad_lengths(lens, b, nq, cap, status);
   __syncthreads();
 
   Walker w;
-  w.init(lens, b, g, cap, C::T, blockIdx.x, gridDim.x);
+  w.init(lens, b, g, nq, cap, C::T, blockIdx.x, gridDim.x);
   Segment seg;
 
   if (warp == 0) {
@@ -182,21 +187,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t n = 0;
     while (w.next(seg)) {
-      const int a0 = seg.i * h + seg.j * r;  // first query head of the group
+      // query row t = s * r + head: q / out row (i * n + s) * h + j * r + head
+      const size_t obase = static_cast<size_t>(seg.i) * nq * h + seg.j * r;
       const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
-      // fused append: threads 0..CH-1 carry one 16-byte chunk of the new
-      // token's K and V rows to the unit's last tile
-      const bool append_here = k_new != nullptr && seg.lt1 == seg.ti;
+      // fused append: the new tokens whose rows fall in this segment,
+      // 16-byte chunks idx < nchunk; thread ct carries chunk ct from here
+      const int first_new = seg.L - nq;
+      int s_lo = 0, nchunk = 0;
+      if (k_new != nullptr) {
+        const int p_lo = max(first_new, seg.lt0 * C::T), p_hi = min(seg.L, seg.lt1 * C::T);
+        if (p_lo < p_hi) {
+          s_lo = p_lo - first_new;
+          nchunk = (p_hi - p_lo) * C::CH;
+        }
+      }
+      auto new_chunk = [&](int idx) -> size_t {
+        return ((static_cast<size_t>(seg.i) * nq + s_lo + idx / C::CH) * g + seg.j) * C::CH +
+               idx % C::CH;
+      };
       uint4 knew = make_uint4(0u, 0u, 0u, 0u), vnew = knew;
-      if (append_here && ct < C::CH) {
-        knew = __ldg(k_new + unit * C::CH + ct);
-        vnew = __ldg(v_new + unit * C::CH + ct);
+      if (ct < nchunk) {
+        knew = __ldg(k_new + new_chunk(ct));
+        vnew = __ldg(v_new + new_chunk(ct));
       }
 #pragma unroll
       for (int t = 0; t < RMAX; ++t) {
-        if (t < r) {
-          const uint4 u =
-              *reinterpret_cast<const uint4*>(q + static_cast<size_t>(a0 + t) * D + ch * C::EPC);
+        if (t < nr) {
+          const int s_ = t / r;
+          const uint4 u = *reinterpret_cast<const uint4*>(
+              q + (obase + s_ * h + (t - s_ * r)) * D + ch * C::EPC);
           Elt<DT>::unpack(u, qreg[t]);
         } else {
 #pragma unroll
@@ -210,16 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   budget);
         const DT* sK = reinterpret_cast<const DT*>(sm + st * C::STAGE_BYTES);
         const DT* sV = sK + C::T * D;
-        if (append_here && lt == seg.ti - 1) {
-          // row L_i - 1 is the new token: use k_new / v_new there and store
-          // them into the cache (the append)
-          if (ok && ct < C::CH) {
-            const int rho = valid - 1;
-            reinterpret_cast<uint4*>(const_cast<DT*>(sK) + rho * D)[ct] = knew;
-            reinterpret_cast<uint4*>(const_cast<DT*>(sV) + rho * D)[ct] = vnew;
-            const size_t crow = unit * cap + (seg.L - 1);
-            k_cache_w[crow * C::CH + ct] = knew;
-            v_cache_w[crow * C::CH + ct] = vnew;
+        if (nchunk > 0 && (lt + 1) * C::T > first_new) {
+          // rows L_i - n .. L_i - 1 are the new tokens: use k_new / v_new
+          // there and store them into the cache (the append)
+          if (ok) {
+            for (int idx = ct; idx < nchunk; idx += 128) {
+              const int pos = first_new + s_lo + idx / C::CH, c16 = idx % C::CH;
+              if (pos < lt * C::T || pos >= (lt + 1) * C::T) continue;
+              const uint4 kv = idx == ct ? knew : __ldg(k_new + new_chunk(idx));
+              const uint4 vv = idx == ct ? vnew : __ldg(v_new + new_chunk(idx));
+              const int rho = pos - lt * C::T;
+              reinterpret_cast<uint4*>(const_cast<DT*>(sK) + rho * D)[c16] = kv;
+              reinterpret_cast<uint4*>(const_cast<DT*>(sV) + rho * D)[c16] = vv;
+              const size_t crow = unit * cap + pos;
+              k_cache_w[crow * C::CH + c16] = kv;
+              v_cache_w[crow * C::CH + c16] = vv;
+            }
           }
           named_bar_sync(1, 128);
         }
@@ -237,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int t = 0; t < RMAX; ++t) {
-            if (t < r) {
+            if (t < nr) {
               float part = 0.f;
 #pragma unroll
               for (int e = 0; e < C::EPC; ++e) part = fmaf(qreg[t][e], kf[e], part);
@@ -249,24 +274,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         named_bar_sync(1, 128);
-        // B: online softmax, one warp per head
-        for (int t = cw; t < r; t += 4) {
+        // B: online softmax, one warp per query row; row t (token s) sees
+        // tile positions p <= lim
+        for (int t = cw; t < nr; t += 4) {
+          const int lim = min(valid - 1, first_new + t / r - lt * C::T);
           float x[C::PPL];
           float mx = -INFINITY;
 #pragma unroll
           for (int k = 0; k < C::PPL; ++k) {
             const int p = lane + 32 * k;
-            x[k] = (p < valid) ? sP[t * C::T + p] : -INFINITY;
+            x[k] = (p <= lim) ? sP[t * C::T + p] : -INFINITY;
             mx = fmaxf(mx, x[k]);
           }
           mx = warp_max(mx);
           const float m_old = sM[t];
           const float m_new = fmaxf(m_old, mx);
-          const float alpha = ex2(m_old - m_new);
+          // a row that has seen no position yet keeps a finite reference
+          const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+          const float alpha = ex2(m_old - mref);
           float sum = 0.f;
 #pragma unroll
           for (int k = 0; k < C::PPL; ++k) {
-            const float pv = ex2(x[k] - m_new);
+            const float pv = ex2(x[k] - mref);
             sum += pv;
             sP[t * C::T + lane + 32 * k] = pv;
           }
@@ -282,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // C: weighted sum of V
 #pragma unroll
         for (int t = 0; t < RMAX; ++t) {
-          if (t < r) {
+          if (t < nr) {
             const float al = sA[t];
 #pragma unroll
             for (int e = 0; e < C::EPC; ++e) acc[t][e] *= al;
@@ -295,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Elt<DT>::unpack(u, vf);
 #pragma unroll
             for (int t = 0; t < RMAX; ++t) {
-              if (t < r) {
+              if (t < nr) {
                 const float wgt = sP[t * C::T + p];
 #pragma unroll
                 for (int e = 0; e < C::EPC; ++e) acc[t][e] = fmaf(wgt, vf[e], acc[t][e]);
@@ -310,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- segment end: reduce the position groups, write out ----
 #pragma unroll
       for (int t = 0; t < RMAX; ++t) {
-        if (t < r) {
+        if (t < nr) {
 #pragma unroll
           for (int e = 0; e < C::EPC; ++e) {
             float v = acc[t][e];
@@ -325,17 +354,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
       const int u = seg.i * g + seg.j;
       const size_t slot = static_cast<size_t>(u) + blockIdx.x;
-      for (int idx = ct; idx < r * D; idx += 128) {
+      auto out_row = [&](int t) -> size_t {
+        const int s_ = t / r;
+        return obase + s_ * h + (t - s_ * r);
+      };
+      for (int idx = ct; idx < nr * D; idx += 128) {
         const int t = idx / D, dd = idx % D;
         const float o = sRed[(0 * RMAX + t) * D + dd] + sRed[(1 * RMAX + t) * D + dd] +
                         sRed[(2 * RMAX + t) * D + dd] + sRed[(3 * RMAX + t) * D + dd];
         if (whole) {
-          Elt<DT>::store(out + static_cast<size_t>(a0 + t) * D + dd, o / sL[t]);
+          Elt<DT>::store(out + out_row(t) * D + dd, o / sL[t]);
         } else {
-          part_o[(slot * r + t) * D + dd] = o;
+          // (a row that saw none of this CTA's positions has max -inf, sum 0)
+          part_o[(slot * nr + t) * D + dd] = o;
           if (dd == 0) {
-            part_ml[(slot * r + t) * 2 + 0] = sM[t];
-            part_ml[(slot * r + t) * 2 + 1] = sL[t];
+            part_ml[(slot * nr + t) * 2 + 0] = sM[t];
+            part_ml[(slot * nr + t) * 2 + 1] = sL[t];
           }
         }
       }
@@ -347,23 +381,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (counters != nullptr && arrive_last(counters, u, np, last_flag, ct == 0, 1, 128)) {
           // merge the other CTAs' partials into this CTA's own (still in
           // shared memory)
-          for (int idx = ct; idx < r * D; idx += 128) {
+          for (int idx = ct; idx < nr * D; idx += 128) {
             const int t = idx / D, dd = idx % D;
             float o = sRed[(0 * RMAX + t) * D + dd] + sRed[(1 * RMAX + t) * D + dd] +
                       sRed[(2 * RMAX + t) * D + dd] + sRed[(3 * RMAX + t) * D + dd];
             float M = sM[t], den = sL[t];
             for (long long c = c0; c <= c1; ++c) {
               if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
-              const long long sl = (u + c) * r + t;
+              const long long sl = (u + c) * nr + t;
               const float mc = __ldcg(part_ml + sl * 2), lc = __ldcg(part_ml + sl * 2 + 1);
               const float oc = __ldcg(part_o + sl * D + dd);
               const float mn = fmaxf(M, mc);
-              const float sa = ex2(M - mn), sb = ex2(mc - mn);
+              const float mr = (mn == -INFINITY) ? 0.f : mn;  // both pieces empty
+              const float sa = ex2(M - mr), sb = ex2(mc - mr);
               o = o * sa + oc * sb;
               den = den * sa + lc * sb;
               M = mn;
             }
-            Elt<DT>::store(out + static_cast<size_t>(a0 + t) * D + dd, o / den);
+            Elt<DT>::store(out + out_row(t) * D + dd, o / den);
           }
         }
       }
@@ -408,14 +443,15 @@ cudaError_t launch_t(const DecodeLaunch& a) {
       static_cast<const DT*>(a.v_cache), a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
       static_cast<DT*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
-      static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget);
+      static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
+      a.nq);
 }
 
 }  // namespace
 
-bool simt_supported(int dtype, int d, int r) {
-  if (dtype == GQA_F32) return (d == 64 || d == 128) && r >= 1 && r <= 16;
-  if (dtype == GQA_BF16) return (d == 64 || d == 128) && r >= 1 && r <= 8;
+bool simt_supported(int dtype, int d, int cols) {
+  if (dtype == GQA_F32) return (d == 64 || d == 128) && cols >= 1 && cols <= 16;
+  if (dtype == GQA_BF16) return (d == 64 || d == 128) && cols >= 1 && cols <= 8;
   return false;
 }
 
@@ -424,7 +460,7 @@ int simt_tile(int dtype, int d) { return 16384 / (d * (dtype == GQA_F32 ? 4 : 2)
 int simt_ctas_per_sm(int, int, int) { return 1; }
 
 cudaError_t launch_decode_simt(const DecodeLaunch& a) {
-  const int r = a.h / a.g;
+  const int r = a.nq * (a.h / a.g);  // query rows per KV head
   if (a.dtype == GQA_F32) {
     if (a.d == 64) return r <= 8 ? launch_t<float, 64, 8>(a) : launch_t<float, 64, 16>(a);
     return r <= 8 ? launch_t<float, 128, 8>(a) : launch_t<float, 128, 16>(a);

@@ -3,7 +3,10 @@
 //
 // The step of the MQA review §2.4 / §3 per (sequence i, KV head j) tile of
 // T = 128 cached positions, with the r = h/g query heads of the group padded
-// to NP columns (16 or 32) and positions on the MMA's M axis:
+// to NP columns (16 or 32) and positions on the MMA's M axis.  With n new
+// tokens per sequence (the batched form of §2.3 restricted to the new
+// rows), the columns are the n * r query rows of the group, token-major,
+// and token s (at position L_i - n + s) sees positions p <= L_i - n + s:
 //
 //   S^T [T x NP]  = K_tile [T x 128] . Q_g^T          (tcgen05.mma, M=128)
 //   P^T [T x NP]  = exp2(S^T * scale*log2e - m)        (CUDA cores, per head)
@@ -30,11 +33,12 @@
 //
 // Rows >= L_i of the last tile of a unit are masked out of S, and their V
 // rows are zeroed in shared memory before the O product reads them, so
-// whatever the cache holds there never reaches the result.
+// whatever the cache holds there never reaches the result.  The causal mask
+// of the new tokens touches only the tiles holding rows >= L_i - n.
 //
 // With k_new / v_new given, the KV append of the step is fused in: the CTA
-// that owns a unit's last tile (the one holding row L_i - 1) puts the new
-// token's K and V into that row of its staged tile and writes them to the
+// that owns a tile holding one of the rows L_i - n .. L_i - 1 puts the new
+// tokens' K and V into those rows of its staged tile and writes them to the
 // cache, so one launch does append + attention.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -53,7 +57,10 @@ constexpr int kD = 128;       // head dim (MMA M of the O product)
 constexpr int kStages = 3;    // K/V ring depth
 constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 
-template <int NP, int NWG>
+// MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
+// The one-token kernel keeps the lighter code (no mask table, one new row)
+// because the 32-column variant runs at its register limit.
+template <int NP, int NWG, bool MULTI>
 struct TcCfg {
   static constexpr int THREADS = 64 + 128 * NWG;  // producer, MMA, NWG softmax warpgroups
   static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
@@ -64,7 +71,8 @@ struct TcCfg {
   static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;       // float [2][NP][4] warp maxima
   static constexpr int OFF_MAX = OFF_RED + 2 * 4 * NP * 4;   // float [2][NP] running max
   static constexpr int OFF_ALPHA = OFF_MAX + 2 * NP * 4;     // float [2][NP] rescale factors
-  static constexpr int OFF_BAR = OFF_ALPHA + 2 * NP * 4;
+  static constexpr int OFF_COL = OFF_ALPHA + 2 * NP * 4;     // int [NP] token, int [NP] out row
+  static constexpr int OFF_BAR = OFF_COL + 2 * NP * 4;
   static constexpr int NBAR = 3 * kStages + 2 * 7 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // The dynamic shared-memory base is 1024-byte aligned (the swizzled
@@ -76,6 +84,10 @@ struct TcCfg {
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
   static constexpr uint32_t IDESC = idesc_bf16(128, NP, 0, 0);     // S: K-major A, B
   static constexpr uint32_t IDESC_O = idesc_bf16(128, NP, 1, 1);   // O: MN-major A, B
+  // new-row chunks the MMA warp carries in registers per lane for the fused
+  // append (one token: K only, lanes 0-15; n tokens: 4 rows of K and of V);
+  // further rows are loaded when patched
+  static constexpr int KCH = MULTI ? 2 : 1;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
   static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
@@ -96,7 +108,7 @@ enum {
   B_DRAIN = B_O_FREE + 2,
 };
 
-template <int NP, int NWG>
+template <int NP, int NWG, bool MULTI>
 __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -106,8 +118,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                      float* __restrict__ part_ml, int* __restrict__ counters,
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
-                     unsigned int* status, long long budget, int early) {
-  using C = TcCfg<NP, NWG>;
+                     unsigned int* status, long long budget, int early, int nq) {
+  using C = TcCfg<NP, NWG, MULTI>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   const uint32_t s_base = smem_u32(sm);
@@ -126,8 +138,19 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
+  const int nr = nq * r;  // query rows (columns) per KV head
+  // column c = s * r + t is head t of new token s; padded columns never see
+  // a position
+  int* col_tok = reinterpret_cast<int*>(sm + C::OFF_COL);
+  int* col_off = col_tok + NP;  // element offset of column c's output row
 
   pdl_launch_dependents();
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + NP) {
+    const int c = threadIdx.x - 64;
+    const int s = c / r;
+    col_tok[c] = c < nr ? s : -(1 << 24);
+    col_off[c] = c < nr ? (s * h + (c - s * r)) * kD : 0;
+  }
   if (threadIdx.x == 0) {
     for (int k = 0; k < C::NBAR; ++k) {
       uint32_t cnt = 1;
@@ -155,10 +178,10 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
   // the producer plans and streams its first tiles before the wait, and
   // waits before loading q; the other warps wait at once.
   if (!early || warp != 0) pdl_wait();
-  if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, cap, status);
+  if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, nq, cap, status);
 
   Walker w;
-  w.init(lens, b, g, cap, kT, blockIdx.x, gridDim.x);
+  w.init(lens, b, g, nq, cap, kT, blockIdx.x, gridDim.x);
   Segment seg;
 
   if (warp == 0) {
@@ -173,10 +196,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         const uint32_t qs = kk & 1;
         if (mbar_wait(BAR(B_Q_EMPTY + qs), ((kk >> 1) & 1) ^ 1, abort_flag, status, budget)) {
           const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
-          const int qrow = sg.i * h + sg.j * r;
-          mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), C::Q_BYTES);
-          tma_load_2d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, qrow, pol_keep);
-          tma_load_2d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, qrow, pol_keep);
+          // box [n tokens][r heads][64]: rows s * r + t of the operand
+          mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 256);
+          tma_load_3d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, sg.j * r, sg.i * nq, pol_keep);
+          tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
+                      pol_keep);
           last_q[qs] = static_cast<int>(kk);
         }
       };
@@ -243,10 +267,10 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    // Lane 0 issues the MMAs.  With the append fused in, lanes 0-15 also
-    // carry the new token's K row (one 16-byte chunk each) from the segment
-    // start to the unit's last tile, where they patch it into the staged
-    // tile and write it to the cache.
+    // Lane 0 issues the MMAs.  With the append fused in, the warp also
+    // carries the new tokens' K rows that fall in the segment (16-byte
+    // chunks, loaded at the segment start) to their tiles, where it patches
+    // them into the staged tile and writes them to the cache.
     const bool leader = lane == 0;
     const uint32_t tS = tmem, tO = tmem + 2 * NP;
     auto issue_o = [&](uint32_t m) {
@@ -282,9 +306,66 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     while (w.next(seg)) {
       const uint32_t qs = k & 1;
       const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
-      const bool append_here = k_new != nullptr && seg.lt1 == seg.ti;
-      uint4 knew = make_uint4(0u, 0u, 0u, 0u);
-      if (append_here && lane < 16) knew = __ldg(k_new + unit * 16 + lane);
+      // new tokens s_lo .. s_lo + nchunk / 16 - 1 have their rows here
+      const int first_new = seg.L - nq;
+      int s_lo = 0, nchunk = 0;
+      if (k_new != nullptr) {
+        const int p_lo = max(first_new, seg.lt0 * kT), p_hi = min(seg.L, seg.lt1 * kT);
+        if (p_lo < p_hi) {
+          s_lo = p_lo - first_new;
+          nchunk = (p_hi - p_lo) * 16;
+        }
+      }
+      // chunk idx of the segment's new rows: token s_lo + idx / 16, 16 bytes
+      // (idx % 16) of its row [b, n, g, 128] of k_new / v_new
+      auto new_off = [&](int idx) {
+        return ((static_cast<size_t>(seg.i) * nq + s_lo + (idx >> 4)) * g + seg.j) * 16 +
+               (idx & 15);
+      };
+      // (one token: the softmax warps carry and patch the V row)
+      constexpr int VCH = MULTI ? C::KCH : 1;
+      uint4 knew[C::KCH], vnew[VCH];
+#pragma unroll
+      for (int c4 = 0; c4 < C::KCH; ++c4) {
+        const int idx = lane + 32 * c4;
+        knew[c4] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < nchunk) knew[c4] = __ldg(k_new + new_off(idx));
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < VCH; ++c4) {
+        const int idx = lane + 32 * c4;
+        vnew[c4] = make_uint4(0u, 0u, 0u, 0u);
+        if (MULTI && idx < nchunk) vnew[c4] = __ldg(v_new + new_off(idx));
+      }
+      // put chunk idx (value v) into row `rho` of a staged [128 x 128] tile
+      // (two 64-column boxes, 128-byte swizzle) and into the cache at `pos`
+      auto put = [&](uint32_t tile_base, uint4* cache, int idx, int pos, int rho, const uint4& v) {
+        const int ch = idx & 15;
+        const uint32_t dst =
+            tile_base + (ch >> 3) * kBoxBytes + rho * 128 + (((ch & 7) ^ (rho & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+        cache[(unit * cap + pos) * 16 + ch] = v;
+      };
+      // patch the new rows that fall in tile lt (K or V half of the stage)
+      auto patch = [&](uint32_t tile_base, uint4* cache, const uint4* src, const uint4* regs,
+                       int nregs, int lt) {
+#pragma unroll
+        for (int c4 = 0; c4 < C::KCH; ++c4) {
+          if (c4 >= nregs) break;
+          const int idx = lane + 32 * c4;
+          const int pos = first_new + s_lo + (idx >> 4);
+          if (idx < nchunk && pos >= lt * kT && pos < (lt + 1) * kT)
+            put(tile_base, cache, idx, pos, pos - lt * kT, regs[c4]);
+        }
+        for (int idx = lane + 32 * nregs; idx < nchunk; idx += 32) {
+          const int pos = first_new + s_lo + (idx >> 4);
+          if (pos >= lt * kT && pos < (lt + 1) * kT)
+            put(tile_base, cache, idx, pos, pos - lt * kT, __ldg(src + new_off(idx)));
+        }
+        fence_proxy_async_smem();
+      };
       const bool qok = __all_sync(
           0xffffffffu, mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget));
       const uint32_t qbase = s_base + C::OFF_Q + qs * C::Q_BYTES;
@@ -296,19 +377,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
         ok = __all_sync(0xffffffffu, ok);
         const uint32_t kbase = s_base + st * C::KV_BYTES;
-        if (append_here && lt == seg.ti - 1) {
-          // row L_i - 1 of this tile is the new token: use k_new there, and
-          // store it into the cache (the append)
-          if (ok && lane < 16) {
-            const int rho = seg.L - 1 - lt * kT;
-            const uint32_t dst = kbase + (lane >> 3) * kBoxBytes + rho * 128 +
-                                 (((lane & 7) ^ (rho & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(knew.x),
-                         "r"(knew.y), "r"(knew.z), "r"(knew.w)
-                         : "memory");
-            k_cache_w[(unit * cap + seg.L - 1) * 16 + lane] = knew;
-            fence_proxy_async_smem();
-          }
+        const bool new_rows = nchunk > 0 && (lt + 1) * kT > first_new;
+        if (new_rows) {
+          // rows L_i - n .. L_i - 1 of this tile are the new tokens: use
+          // k_new there, and store them into the cache (the append)
+          if (ok) patch(kbase, k_cache_w, k_new, knew, C::KCH, lt);
           __syncwarp();
         }
         tc_fence_after();
@@ -330,6 +403,15 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         }
         __syncwarp();
         if (have_prev) issue_o(prev);
+        if (MULTI && new_rows) {
+          // the same for v_new, before this tile's O product is issued (the
+          // softmax warps zero the rows past L_i, which are other rows)
+          const bool vok = __all_sync(
+              0xffffffffu,
+              mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget));
+          if (vok) patch(kbase + 2 * kBoxBytes, v_cache_w, v_new, vnew, VCH, lt);
+          __syncwarp();
+        }
         have_prev = true;
         prev = n;
       }
@@ -401,12 +483,13 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 
     uint32_t n = 0;
     while (w.next(seg)) {
-      const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
-      // fused append: threads 0-15 of warpgroup 0 carry the new token's V
-      // row, one chunk each
-      const bool append_here = v_new != nullptr && seg.lt1 == seg.ti;
+      const int first_new = seg.L - nq;  // position of new token 0
+      // one token: threads 0-15 of warpgroup 0 carry the new V row (one
+      // 16-byte chunk each) to the unit's last tile
+      const bool append_v = !MULTI && v_new != nullptr && seg.lt1 == seg.ti;
       uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
-      if (wg == 0 && append_here && row < 16) vnew = __ldg(v_new + unit * 16 + row);
+      if (append_v && wg == 0 && row < 16)
+        vnew = __ldg(v_new + (static_cast<size_t>(seg.i) * g + seg.j) * 16 + row);
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         const uint32_t nb = n & 1;
         const int st = n % kStages;
@@ -431,9 +514,27 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_S_FREE + nb));
         const bool live = row < valid;
+        if (!MULTI) {
 #pragma unroll
-        for (int e = 0; e < HP; ++e)
-          x[e] = (live && h0 + e < r) ? x[e] * scale_log2 : -INFINITY;
+          for (int e = 0; e < HP; ++e)
+            x[e] = (live && h0 + e < nr) ? x[e] * scale_log2 : -INFINITY;
+        } else if ((lt + 1) * kT <= first_new + 1) {
+          // (uniform) every new token sees every position of the tile
+#pragma unroll
+          for (int e = 0; e < HP; ++e) x[e] = (h0 + e < nr) ? x[e] * scale_log2 : -INFINITY;
+        } else {
+          // token s sees this position iff s >= -vis (the causal mask; for
+          // n = 1 it is the p < L_i mask; padded columns see nothing)
+          const int vis = first_new - lt * kT - row;
+#pragma unroll
+          for (int e4 = 0; e4 < HP; e4 += 4) {
+            const int4 tk = *reinterpret_cast<const int4*>(col_tok + h0 + e4);
+            const int tt[4] = {tk.x, tk.y, tk.z, tk.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              x[e4 + k] = (tt[k] >= -vis) ? x[e4 + k] * scale_log2 : -INFINITY;
+          }
+        }
         // ---- per-head max over the tile's 128 positions ----
         float mine = -INFINITY;
 #pragma unroll
@@ -448,11 +549,14 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (lane < HP) rb[lane * 4 + wq] = mine;
         named_bar_sync(bar_id, 128);
         if (row < HP) {
-          if (h0 + row < r) {
+          if (h0 + row < nr) {
             const float4 v = *reinterpret_cast<const float4*>(rb + 4 * row);
             const float mn = fmaxf(m_own, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-            alpha_sm[nb * NP + h0 + row] = ex2(m_own - mn);
-            max_sm[nb * NP + h0 + row] = mn;
+            // a token that has seen no position yet (causal mask) keeps a
+            // finite reference so that exp2 gives 0, not NaN
+            const float mref = (mn == -INFINITY) ? 0.f : mn;
+            alpha_sm[nb * NP + h0 + row] = ex2(m_own - mref);
+            max_sm[nb * NP + h0 + row] = mref;
             m_own = mn;
           } else {
             alpha_sm[nb * NP + h0 + row] = 1.f;
@@ -470,7 +574,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int e = e4 + k;
-            x[e] = (h0 + e < r) ? ex2(x[e] - mm[k]) : 0.f;
+            x[e] = (h0 + e < nr) ? ex2(x[e] - mm[k]) : 0.f;
             l[e] = fmaf(l[e], aa[k], x[e]);
           }
         }
@@ -495,13 +599,23 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           }
         }
         // ---- last tile of a unit (warpgroup 0): zero the V rows past L_i;
-        // with the append fused in, put v_new into row L_i - 1 and into the
-        // cache ----
-        const bool patch = append_here && lt == seg.ti - 1;
-        if (wg == 0 && (valid < kT || patch)) {
+        // one token: put v_new into row L_i - 1 and into the cache (n
+        // tokens: the MMA warp patches the new rows) ----
+        const bool patch_v = append_v && lt == seg.ti - 1;
+        if (wg == 0 && (valid < kT || patch_v)) {
           const bool vok =
               mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
           const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
+          if (vok && patch_v && row < 16) {
+            const int rho = valid - 1;
+            const uint32_t dst =
+                vbase + (row >> 3) * kBoxBytes + rho * 128 + (((row & 7) ^ (rho & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(vnew.x),
+                         "r"(vnew.y), "r"(vnew.z), "r"(vnew.w)
+                         : "memory");
+            v_cache_w[((static_cast<size_t>(seg.i) * g + seg.j) * cap + seg.L - 1) * 16 + row] =
+                vnew;
+          }
           if (vok && !live) {
             const uint32_t vrow = vbase + row * 128;
 #pragma unroll
@@ -512,15 +626,6 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                                  vrow + hb * kBoxBytes + c * 16),
                              "r"(0u)
                              : "memory");
-          }
-          if (vok && patch && row < 16) {
-            const int rho = valid - 1;
-            const uint32_t dst =
-                vbase + (row >> 3) * kBoxBytes + rho * 128 + (((row & 7) ^ (rho & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(vnew.x),
-                         "r"(vnew.y), "r"(vnew.z), "r"(vnew.w)
-                         : "memory");
-            v_cache_w[(unit * cap + seg.L - 1) * 16 + row] = vnew;
           }
         }
         fence_proxy_async_smem();
@@ -549,7 +654,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (lane < HP) lred[wq * HP + lane] = mine;
         named_bar_sync(bar_id, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
-        const int a0 = seg.i * h + seg.j * r + h0;  // first head of this warpgroup
+        // output row of column c: (i * n + s) * h + j * r + t
+        __nv_bfloat16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * kD + row;
         const int u = seg.i * g + seg.j;
         const size_t slot = static_cast<size_t>(u) + blockIdx.x;
         // l[e] becomes the CTA-wide softmax denominator of head h0 + e
@@ -559,16 +665,17 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (whole) {
 #pragma unroll
           for (int e = 0; e < HP; ++e)
-            if (h0 + e < r)
-              out[static_cast<size_t>(a0 + e) * kD + row] = __float2bfloat16_rn(o[e] / l[e]);
+            if (h0 + e < nr)
+              obase[col_off[h0 + e]] = __float2bfloat16_rn(o[e] / l[e]);
         } else {
 #pragma unroll
           for (int e = 0; e < HP; ++e) {
-            if (h0 + e < r) {
-              const size_t sl = slot * r + h0 + e;
+            if (h0 + e < nr) {
+              const size_t sl = slot * nr + h0 + e;
               part_o[sl * kD + row] = o[e];
               if (row == 0) {
-                part_ml[sl * 2 + 0] = mfin[e];
+                // a token that saw none of this CTA's positions: empty partial
+                part_ml[sl * 2 + 0] = l[e] > 0.f ? mfin[e] : -INFINITY;
                 part_ml[sl * 2 + 1] = l[e];
               }
             }
@@ -579,11 +686,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           long long c0, c1;
           unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
           const int np = unit_parts(c0, c1, w.W, w.nc);
-          if (counters != nullptr && h0 < r &&
+          if (counters != nullptr && h0 < nr &&
               arrive_last(counters, u * NWG + wg, np, last_flag_wg, row == 0, bar_id, 128)) {
             float m[HP];
 #pragma unroll
-            for (int e = 0; e < HP; ++e) m[e] = mfin[e];
+            for (int e = 0; e < HP; ++e) m[e] = l[e] > 0.f ? mfin[e] : -INFINITY;
             for (long long c = c0; c <= c1; ++c) {
               if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
               // eight heads at a time: their loads go out together
@@ -592,8 +699,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                 float mc[8], lc[8], oc[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                  if (h0 + e0 + k < r) {
-                    const long long sl = (u + c) * r + h0 + e0 + k;
+                  if (h0 + e0 + k < nr) {
+                    const long long sl = (u + c) * nr + h0 + e0 + k;
                     mc[k] = __ldcg(part_ml + sl * 2);
                     lc[k] = __ldcg(part_ml + sl * 2 + 1);
                     oc[k] = __ldcg(part_o + sl * kD + row);
@@ -602,9 +709,10 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                   const int e = e0 + k;
-                  if (h0 + e < r) {
+                  if (h0 + e < nr) {
                     const float mn = fmaxf(m[e], mc[k]);
-                    const float sa = ex2(m[e] - mn), sb = ex2(mc[k] - mn);
+                    const float mr = (mn == -INFINITY) ? 0.f : mn;  // both pieces empty
+                    const float sa = ex2(m[e] - mr), sb = ex2(mc[k] - mr);
                     o[e] = o[e] * sa + oc[k] * sb;
                     l[e] = l[e] * sa + lc[k] * sb;
                     m[e] = mn;
@@ -614,8 +722,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             }
 #pragma unroll
             for (int e = 0; e < HP; ++e)
-              if (h0 + e < r)
-                out[static_cast<size_t>(a0 + e) * kD + row] = __float2bfloat16_rn(o[e] / l[e]);
+              if (h0 + e < nr)
+                obase[col_off[h0 + e]] = __float2bfloat16_rn(o[e] / l[e]);
           }
         }
         m_own = -INFINITY;
@@ -658,7 +766,8 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D map over a row-major [rows x 128] bf16 tensor, box [box_rows x 64],
-// 128-byte swizzle, zero fill outside.
+// 128-byte swizzle, zero fill outside.  (The query map is 3-D:
+// [b * n tokens][h heads][128], box [n][r][64].)
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -672,15 +781,30 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NP, int NWG>
+bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h),
+                              static_cast<cuuint64_t>(b) * nq};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(h) * kD * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(r), static_cast<cuuint32_t>(nq)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NP, int NWG, bool MULTI>
 cudaError_t launch_np(const DecodeLaunch& a) {
-  using C = TcCfg<NP, NWG>;
+  using C = TcCfg<NP, NWG, MULTI>;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, static_cast<uint64_t>(a.b) * a.h, NP) ||
+  if (!make_q_map(&mq, a.q, a.b, a.nq, a.h, a.h / a.g) ||
       !make_map(&mk, a.k_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT) ||
       !make_map(&mv, a.v_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT))
     return cudaErrorInvalidValue;
-  auto kern = decode_tc_kernel<NP, NWG>;
+  auto kern = decode_tc_kernel<NP, NWG, MULTI>;
   // the shared-memory opt-in is set once per device (not during a capture)
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -706,13 +830,13 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
-      a.early ? 1 : 0);
+      a.early ? 1 : 0, a.nq);
 }
 
 }  // namespace
 
-bool tc_supported(int dtype, int d, int r) {
-  return dtype == GQA_BF16 && d == kD && r >= 1 && r <= 32;
+bool tc_supported(int dtype, int d, int cols) {
+  return dtype == GQA_BF16 && d == kD && cols >= 1 && cols <= 32;
 }
 
 int tc_tile() { return kT; }
@@ -720,8 +844,9 @@ int tc_tile() { return kT; }
 int tc_ctas_per_sm(int) { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeLaunch& a) {
-  const int r = a.h / a.g;
-  return r <= 16 ? launch_np<16, 1>(a) : launch_np<32, 2>(a);
+  const int cols = a.nq * (a.h / a.g);
+  if (a.nq == 1) return cols <= 16 ? launch_np<16, 1, false>(a) : launch_np<32, 2, false>(a);
+  return cols <= 16 ? launch_np<16, 1, true>(a) : launch_np<32, 2, true>(a);
 }
 
 }  // namespace gqa

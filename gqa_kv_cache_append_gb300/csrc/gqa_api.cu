@@ -27,26 +27,29 @@ constexpr long long kWaitBudget = 1ll << 31;  // ~1 s of SM cycles per wait
 
 // ---------------------------------------------------------------------------
 // KV append: one thread per 16-byte chunk of the new rows.
-// The concat of the new K/V row on the position axis (MQA review §2.4, §3),
-// done in place at row L_i - 1 (decode notes: kCache.push, vCache.push).
+// The concat of the new K/V rows on the position axis (MQA review §2.4, §3),
+// done in place at rows L_i - n .. L_i - 1 (decode notes: kCache.push,
+// vCache.push; n = 1 for one token per step).
 // ---------------------------------------------------------------------------
 __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                                  uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                 const int* __restrict__ lens, int b, int g, int ck, int cv,
-                                 int cap, unsigned int* status) {
+                                 const int* __restrict__ lens, int b, int nq, int g, int ck,
+                                 int cv, int cap, unsigned int* status) {
   const long long per = ck + cv;
-  const long long total = static_cast<long long>(b) * g * per;
+  const long long total = static_cast<long long>(b) * nq * g * per;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= total) return;
-  const long long row = idx / per;  // (i, j) row of k_new / v_new
+  const long long row = idx / per;  // (i, s, j) row of k_new / v_new
   const int c = static_cast<int>(idx % per);
-  const int i = static_cast<int>(row / g);
+  const int j = static_cast<int>(row % g);
+  const int s = static_cast<int>((row / g) % nq);
+  const int i = static_cast<int>(row / (static_cast<long long>(g) * nq));
   const int L = __ldg(lens + i);
-  if (L < 1 || L > cap) {
+  if (L < 1 || L < nq || L > cap) {
     if (c == 0) atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
     return;
   }
-  const long long dst_row = row * cap + (L - 1);
+  const long long dst_row = (static_cast<long long>(i) * g + j) * cap + (L - nq + s);
   if (c < ck) {
     k_cache[dst_row * ck + c] = __ldg(k_new + row * ck + c);
   } else {
@@ -59,29 +62,31 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
 // Log-sum-exp combine for launches with many more CTAs than units (a few
 // long sequences, e.g. one MQA head over 131k positions spread over 19
 // CTAs): the decode kernel then only writes partials, and this kernel merges
-// them with the whole GPU, one CTA per (unit, query head), one thread per
-// output column.  With per-CTA maxima m_c (base 2), sums l_c and
+// them with the whole GPU, one CTA per (unit, query row), one thread per
+// output column.  Query row t = s * r + head of a unit is head j * r + head
+// of new token s.  With per-CTA maxima m_c (base 2), sums l_c and
 // unnormalised outputs O_c of the same softmax over disjoint position ranges:
 //     M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 // Units held whole by one CTA were written by the decode kernel.
 // ---------------------------------------------------------------------------
 template <typename DT>
 __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g, int cap,
-                               int d, int tile, int nc, const float* __restrict__ part_o,
+                               int d, int tile, int nc, int nq, const float* __restrict__ part_o,
                                const float* __restrict__ part_ml, DT* __restrict__ out) {
   __shared__ long long s_u0, s_W;
   __shared__ int s_ti;
   pdl_launch_dependents();
   pdl_wait();  // the partials come from the decode kernel just before
   const int r = h / g;
-  const int u = blockIdx.x / r, t = blockIdx.x % r;
+  const int nr = nq * r;
+  const int u = blockIdx.x / nr, t = blockIdx.x % nr;
   const int i = u / g, j = u % g;
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     long long before = 0, all = 0;
     for (int base = 0; base < b; base += 32) {
       const int idx = base + lane;
-      const int tt = (idx < b) ? seq_tiles(__ldg(lens + idx), cap, tile) : 0;
+      const int tt = (idx < b) ? seq_tiles(__ldg(lens + idx), nq, cap, tile) : 0;
       all += tt;
       if (idx < i) before += tt;
     }
@@ -91,7 +96,7 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
       before += __shfl_xor_sync(0xffffffffu, before, o);
     }
     if (lane == 0) {
-      const int ti = seq_tiles(__ldg(lens + i), cap, tile);
+      const int ti = seq_tiles(__ldg(lens + i), nq, cap, tile);
       s_ti = ti;
       s_u0 = before * g + static_cast<long long>(j) * ti;
       s_W = all * g;
@@ -115,7 +120,7 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
     for (int k = 0; k < kBatch; ++k) {
       const long long c = cb + k;
       const bool use = c <= c1 && (W >= nc || !cta_empty(c, W, nc));
-      const long long sl = (u + c) * r + t;
+      const long long sl = (u + c) * nr + t;
       mc[k] = use ? __ldg(part_ml + sl * 2) : -INFINITY;
       lc[k] = use ? __ldg(part_ml + sl * 2 + 1) : 0.f;
       oc[k] = use ? __ldg(part_o + sl * d + col) : 0.f;
@@ -123,19 +128,22 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
     float mb = M;
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) mb = fmaxf(mb, mc[k]);
-    const float sc = ex2(M - mb);  // 0 on the first batch (M = -inf)
+    // pieces that saw no position of this row (causal mask) have max -inf
+    const float mbr = (mb == -INFINITY) ? 0.f : mb;
+    const float sc = ex2(M - mbr);  // 0 while M = -inf
     num *= sc;
     den *= sc;
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
-      const float wgt = ex2(mc[k] - mb);  // 0 for unused slots
+      const float wgt = ex2(mc[k] - mbr);  // 0 for unused slots and empty pieces
       den = fmaf(wgt, lc[k], den);
       num = fmaf(wgt, oc[k], num);
     }
     M = mb;
   }
   const float v = num / den;
-  DT* dst = out + (static_cast<size_t>(i) * h + j * r + t) * d + col;
+  const int s = t / r;
+  DT* dst = out + ((static_cast<size_t>(i) * nq + s) * h + j * r + (t - s * r)) * d + col;
   if constexpr (sizeof(DT) == 2)
     *dst = __float2bfloat16_rn(v);
   else
@@ -274,12 +282,12 @@ bool use_combine_kernel(const DecodeLaunch& a) {
 int launch_all(DecodeLaunch& a, int tile) {
   const bool separate = use_combine_kernel(a);
   if (separate) a.counters = nullptr;
-  const bool tc = tc_supported(a.dtype, a.d, a.h / a.g);
+  const bool tc = tc_supported(a.dtype, a.d, a.nq * (a.h / a.g));
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   if (separate) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.b) * a.h));
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.b) * a.h * a.nq));
     cfg.blockDim = dim3(a.d);
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
@@ -289,12 +297,12 @@ int launch_all(DecodeLaunch& a, int tile) {
     cfg.numAttrs = 1;
     if (a.dtype == GQA_BF16)
       e = cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a.seq_lens, a.b, a.h, a.g,
-                             a.cap, a.d, tile, a.nc, static_cast<const float*>(a.part_o),
+                             a.cap, a.d, tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
                              static_cast<const float*>(a.part_ml),
                              static_cast<__nv_bfloat16*>(a.out));
     else
       e = cudaLaunchKernelEx(&cfg, combine_kernel<float>, a.seq_lens, a.b, a.h, a.g, a.cap, a.d,
-                             tile, a.nc, static_cast<const float*>(a.part_o),
+                             tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
                              static_cast<const float*>(a.part_ml), static_cast<float*>(a.out));
   }
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
@@ -326,12 +334,12 @@ const char* gqa_status_string(int s) {
   }
 }
 
-int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                  const int32_t* seq_lens, int b, int g, int d_k, int d_v, int cap, int dtype,
-                  void* stream) {
+int gqa_kv_append_multi(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                        const int32_t* seq_lens, int b, int n, int g, int d_k, int d_v, int cap,
+                        int dtype, void* stream) {
   if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens) return GQA_ERR_NULL;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
-  if (b < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1) return GQA_ERR_SHAPE;
+  if (b < 1 || n < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || n > cap) return GQA_ERR_SHAPE;
   const int elt = elt_bytes(dtype);
   if ((d_k * elt) % 16 != 0 || (d_v * elt) % 16 != 0) return GQA_ERR_UNSUPPORTED;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
@@ -340,16 +348,23 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_c
   DeviceInfo* di = nullptr;
   if (int e = device_info(&di)) return e;
   const int ck = d_k * elt / 16, cv = d_v * elt / 16;
-  const long long total = static_cast<long long>(b) * g * (ck + cv);
+  const long long total = static_cast<long long>(b) * n * g * (ck + cv);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   if (blocks > 0x7FFFFFFFll) return GQA_ERR_SHAPE;
   kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0,
                      static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), seq_lens, b, g, ck, cv, cap,
-      di->status);
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), seq_lens, b, n, g, ck, cv,
+      cap, di->status);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                  const int32_t* seq_lens, int b, int g, int d_k, int d_v, int cap, int dtype,
+                  void* stream) {
+  return gqa_kv_append_multi(k_new, v_new, k_cache, v_cache, seq_lens, b, 1, g, d_k, d_v, cap,
+                             dtype, stream);
 }
 
 }  // extern "C"
@@ -360,24 +375,26 @@ namespace {
 // gqa_decode_attn and gqa_decode_step: checks, kernel choice, workspace,
 // launch.  k_new / v_new null means attention only.
 int decode(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-           const void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v,
-           float scale, void* out, int cap, int dtype, void* stream, int flags) {
+           const void* v_cache, const int32_t* seq_lens, int b, int nq, int h, int g, int d_k,
+           int d_v, float scale, void* out, int cap, int dtype, void* stream, int flags) {
   if (flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
-  if (b < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0)
+  if (b < 1 || nq < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0 ||
+      nq > cap)
     return GQA_ERR_SHAPE;
   if (static_cast<long long>(b) * g * cap + 256 > 0x7FFFFFFFll ||
-      static_cast<long long>(b) * h > 0x7FFFFFFFll)
+      static_cast<long long>(b) * nq * h > 0x7FFFFFFFll)
     return GQA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return GQA_ERR_ALIGN;
   const int r = h / g;
   const int d = d_k;
-  if (d_k != d_v || b > 65535) return GQA_ERR_UNSUPPORTED;
-  const bool use_tc = tc_supported(dtype, d, r);
-  if (!use_tc && !simt_supported(dtype, d, r)) return GQA_ERR_UNSUPPORTED;
+  if (d_k != d_v || b > 65535 || static_cast<long long>(nq) * r > 32) return GQA_ERR_UNSUPPORTED;
+  const int cols = nq * r;  // query rows per KV head
+  const bool use_tc = tc_supported(dtype, d, cols);
+  if (!use_tc && !simt_supported(dtype, d, cols)) return GQA_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   if (int e = device_info(&di)) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -390,8 +407,8 @@ int decode(const void* q, const void* k_new, const void* v_new, const void* k_ca
   if (nc < 1) nc = 1;
 
   const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
-  const size_t o_bytes = slots * r * d * sizeof(float);
-  const size_t ml_bytes = slots * r * 2 * sizeof(float);
+  const size_t o_bytes = slots * cols * d * sizeof(float);
+  const size_t ml_bytes = slots * cols * 2 * sizeof(float);
   void* ws = nullptr;
   int* counters = nullptr;
   // two arrival counters per unit: the tensor-core kernel may run two
@@ -410,6 +427,7 @@ int decode(const void* q, const void* k_new, const void* v_new, const void* k_ca
   a.d = d;
   a.cap = cap;
   a.dtype = dtype;
+  a.nq = nq;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out = out;
   a.part_o = static_cast<float*>(ws);
@@ -436,8 +454,8 @@ extern "C" {
 int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* seq_lens, int b, int h, int g, int d_k, int d_v, float scale,
                     void* out, int cap, int dtype, void* stream) {
-  return gqa::decode(q, nullptr, nullptr, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
-                     out, cap, dtype, stream, 0);
+  return gqa::decode(q, nullptr, nullptr, k_cache, v_cache, seq_lens, b, 1, h, g, d_k, d_v,
+                     scale, out, cap, dtype, stream, 0);
 }
 
 int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -445,8 +463,24 @@ int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k
                     int d_v, float scale, void* out, int cap, int dtype, int flags,
                     void* stream) {
   if (!k_new || !v_new) return GQA_ERR_NULL;
-  return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale, out,
-                     cap, dtype, stream, flags);
+  return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, 1, h, g, d_k, d_v, scale,
+                     out, cap, dtype, stream, flags);
+}
+
+int gqa_decode_attn_multi(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* seq_lens, int b, int n, int h, int g, int d_k, int d_v,
+                          float scale, void* out, int cap, int dtype, void* stream) {
+  return gqa::decode(q, nullptr, nullptr, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v,
+                     scale, out, cap, dtype, stream, 0);
+}
+
+int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                          void* v_cache, const int32_t* seq_lens, int b, int n, int h, int g,
+                          int d_k, int d_v, float scale, void* out, int cap, int dtype,
+                          int flags, void* stream) {
+  if (!k_new || !v_new) return GQA_ERR_NULL;
+  return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v, scale,
+                     out, cap, dtype, stream, flags);
 }
 
 int gqa_device_status(void* stream, uint32_t* bits_out) {
@@ -592,6 +626,7 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   a.d = d;
   a.cap = cap;
   a.dtype = dtype;
+  a.nq = 1;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out = out;
   a.part_o = reinterpret_cast<float*>(parts);

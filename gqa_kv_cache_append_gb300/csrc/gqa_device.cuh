@@ -90,6 +90,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// 3-D tiled load (e.g. the query rows of one KV head for n new tokens):
+// the box lands as [z][y][x] rows of the swizzled layout.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar,
+                                            int x, int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap))
                : "memory");
@@ -240,7 +251,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Work walker.
 //
 // A "unit" is one (sequence i, KV head j); it holds t_i = ceil(L_i / T) tiles
-// of T positions (0 when L_i is outside [1, cap]).  Units are ordered
+// of T positions (0 when L_i is outside [n, cap], n being the number of new
+// tokens per sequence of the step, usually 1).  Units are ordered
 // u = i * g + j and their tiles laid end to end, W tiles in all.  CTA c of NC
 // takes the tile range [c * W / NC, (c + 1) * W / NC), so every CTA streams
 // the same number of tiles (to within one) whatever the length mix.  A CTA's
@@ -252,8 +264,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 //
 // Every warp runs its own walker (warp-uniform values, no shared state).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int seq_tiles(int L, int cap, int T) {
-  return (L >= 1 && L <= cap) ? (L + T - 1) / T : 0;
+__device__ __forceinline__ int seq_tiles(int L, int lmin, int cap, int T) {
+  return (L >= lmin && L >= 1 && L <= cap) ? (L + T - 1) / T : 0;
 }
 
 struct Segment {
@@ -308,13 +320,14 @@ __device__ __forceinline__ bool arrive_last(int* counters, int u, int nparts, in
   return *reinterpret_cast<volatile int*>(s_flag) != 0;
 }
 
-// Warp-cooperative: flag every sequence whose length is outside [1, cap].
-__device__ __forceinline__ void report_bad_lengths(const int* lens, int b, int cap,
+// Warp-cooperative: flag every sequence whose length is outside [lmin, cap]
+// (lmin = max(1, new tokens per sequence)).
+__device__ __forceinline__ void report_bad_lengths(const int* lens, int b, int lmin, int cap,
                                                    unsigned int* status) {
   bool bad = false;
   for (int idx = threadIdx.x & 31; idx < b; idx += 32) {
     const int L = __ldg(lens + idx);
-    bad |= (L < 1 || L > cap);
+    bad |= (L < 1 || L < lmin || L > cap);
   }
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
     atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
@@ -322,20 +335,21 @@ __device__ __forceinline__ void report_bad_lengths(const int* lens, int b, int c
 
 struct Walker {
   const int* lens;
-  int b, g, cap, T;
+  int b, g, lmin, cap, T;
   long long W;         // total tiles of the launch
   int nc;              // CTAs of the launch
   long long pos, end;  // global tile cursor and end of this CTA's range
   int i, j, lt, ti, L;
 
   // total tiles W (warp-cooperative; all lanes get the result)
-  __device__ static long long total_tiles(const int* lens, int b, int g, int cap, int T) {
+  __device__ static long long total_tiles(const int* lens, int b, int g, int lmin, int cap,
+                                         int T) {
     const int lane = threadIdx.x & 31;
     long long acc = 0;
     for (int base = 0; base < b; base += 32) {
       const int idx = base + lane;
       int t = 0;
-      if (idx < b) t = seq_tiles(__ldg(lens + idx), cap, T);
+      if (idx < b) t = seq_tiles(__ldg(lens + idx), lmin, cap, T);
       acc += t;
     }
 #pragma unroll
@@ -343,14 +357,17 @@ struct Walker {
     return acc * g;
   }
 
-  // Position the walker at CTA `c` of `nc`.  Warp-cooperative.
-  __device__ void init(const int* lens_, int b_, int g_, int cap_, int T_, int c, int nc) {
+  // Position the walker at CTA `c` of `nc`; sequences shorter than lmin
+  // (the step's new tokens) are skipped.  Warp-cooperative.
+  __device__ void init(const int* lens_, int b_, int g_, int lmin_, int cap_, int T_, int c,
+                       int nc) {
     lens = lens_;
     b = b_;
     g = g_;
+    lmin = lmin_;
     cap = cap_;
     T = T_;
-    W = total_tiles(lens, b, g, cap, T);
+    W = total_tiles(lens, b, g, lmin, cap, T);
     this->nc = nc;
     pos = (W * c) / nc;
     end = (W * (c + 1)) / nc;
@@ -368,7 +385,7 @@ struct Walker {
       int Lx = 0, t = 0;
       if (idx < b) {
         Lx = __ldg(lens + idx);
-        t = seq_tiles(Lx, cap, T);
+        t = seq_tiles(Lx, lmin, cap, T);
       }
       long long incl = static_cast<long long>(t) * g;
 #pragma unroll
@@ -417,7 +434,7 @@ struct Walker {
         do {
           ++i;
           L = (i < b) ? __ldg(lens + i) : 0;
-          ti = (i < b) ? seq_tiles(L, cap, T) : 0;
+          ti = (i < b) ? seq_tiles(L, lmin, cap, T) : 0;
         } while (i < b && ti == 0);
       }
     }

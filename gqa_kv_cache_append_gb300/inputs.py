@@ -25,6 +25,11 @@ Recipe (per layer l of a workload with seed s):
     hi, size=b, endpoint=True); the others use L_i = cap for every sequence.
 Rows at or beyond L_i are padding; ``pad_fill`` can fill them with NaN (or a
 large value) to check that nothing reads them into the result.
+
+Steps with n new tokens per sequence (make_layer_multi, 'plain' workloads
+only) draw in the same order from a generator seeded s * 1000 + l + 100000 * n:
+the K cache, the V cache, q [b, n, h, d], k_new [b, n, g, d], v_new
+[b, n, g, d].
 """
 from __future__ import annotations
 
@@ -36,7 +41,7 @@ import numpy as np
 import torch
 
 __all__ = ["DecodeConfig", "WORKLOADS", "workload", "seq_lens_for",
-           "make_layer", "layer_bytes", "layer_flops"]
+           "make_layer", "make_layer_multi", "layer_bytes", "layer_flops"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -110,18 +115,21 @@ def seq_lens_for(cfg: DecodeConfig) -> np.ndarray:
     return np.minimum(lens, cfg.cap).astype(np.int32)
 
 
-def layer_bytes(cfg: DecodeConfig, lens: np.ndarray) -> int:
+def layer_bytes(cfg: DecodeConfig, lens: np.ndarray, n: int = 1) -> int:
     """Algorithmic bytes of one decode-attention call: the K and V rows below
-    L_i of every KV head, plus q and out (padding and split partials are not
-    counted)."""
+    L_i of every KV head, plus q and out of the n new tokens (padding and
+    split partials are not counted)."""
     kv = int(np.sum(lens, dtype=np.int64)) * cfg.g * 2 * cfg.d * cfg.elt
-    return kv + 2 * cfg.b * cfg.h * cfg.d * cfg.elt
+    return kv + 2 * cfg.b * n * cfg.h * cfg.d * cfg.elt
 
 
-def layer_flops(cfg: DecodeConfig, lens: np.ndarray) -> int:
+def layer_flops(cfg: DecodeConfig, lens: np.ndarray, n: int = 1) -> int:
     """Multiply-add flops of one decode-attention call (2 per product, for
-    q.K and for w.V)."""
-    return 4 * cfg.h * cfg.d * int(np.sum(lens, dtype=np.int64))
+    q.K and for w.V); with n new tokens the causal mask leaves token s the
+    positions below L_i - n + s + 1."""
+    lens = np.asarray(lens, dtype=np.int64)
+    seen = int(np.sum(lens)) * n - cfg.b * (n * (n - 1) // 2)
+    return 4 * cfg.h * cfg.d * seen
 
 
 def _randn(shape, gen, device):
@@ -193,6 +201,46 @@ def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
         "q": q.contiguous(), "k_cache": k_cache.contiguous(),
         "v_cache": v_cache.contiguous(), "k_new": k_new.contiguous(),
         "v_new": v_new.contiguous(),
+        "seq_lens": torch.from_numpy(lens.copy()).to(device),
+        "lens": lens,
+    }
+
+
+def make_layer_multi(cfg: DecodeConfig, n: int, layer: int = 0, device="cpu",
+                     lens: Optional[np.ndarray] = None, pad_fill=None) -> dict:
+    """Inputs of one layer's step with n new tokens per sequence: q
+    [b, n, h, d], k_cache / v_cache [b, g, cap, d], k_new / v_new [b, n, g, d]
+    in the storage dtype, seq_lens int32 [b] (post-append, >= n) on
+    ``device``, plus the host copy ``lens``.  'plain' workloads only."""
+    if cfg.kind != "plain":
+        raise ValueError("multi-token inputs are drawn for plain workloads only")
+    if cfg.h % cfg.g != 0 or n < 1:
+        raise ValueError("h must be divisible by g and n >= 1")
+    device = torch.device(device)
+    if lens is None:
+        lens = seq_lens_for(cfg)
+    lens = np.asarray(lens, dtype=np.int32)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed * 1000 + layer + 100000 * n)
+    b, h, g, d, cap = cfg.b, cfg.h, cfg.g, cfg.d, cfg.cap
+    dt = cfg.torch_dtype
+    k_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
+    v_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
+    for dst in (k_cache, v_cache):
+        for i in range(b):
+            dst[i].copy_(_randn((g, cap, d), gen, device))
+    q = _randn((b, n, h, d), gen, device).to(dt)
+    k_new = _randn((b, n, g, d), gen, device).to(dt)
+    v_new = _randn((b, n, g, d), gen, device).to(dt)
+    if pad_fill is not None:
+        for i in range(b):
+            L = int(lens[i])
+            if L < cap:
+                k_cache[i, :, L:, :] = pad_fill
+                v_cache[i, :, L:, :] = pad_fill
+    return {
+        "q": q.contiguous(), "k_cache": k_cache, "v_cache": v_cache,
+        "k_new": k_new.contiguous(), "v_new": v_new.contiguous(),
         "seq_lens": torch.from_numpy(lens.copy()).to(device),
         "lens": lens,
     }

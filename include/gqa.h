@@ -164,6 +164,57 @@ int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k
                     void* stream);
 
 /*
+ * n new tokens per sequence in one step (speculative or chunked decoding):
+ * the batched form of §2.3 ("MultiheadAttentionBatched", n queries per
+ * sequence with an additive mask [b, h, n, m]) restricted to the new rows,
+ * with the causal mask (0 where the position is at or before the query's,
+ * -inf after it).  With n = 1 each call equals its one-token counterpart.
+ *
+ * seq_lens holds L_i AFTER the n tokens are appended; token s (0 <= s < n)
+ * sits at position L_i - n + s.  A value outside [n, cap] is a device-side
+ * error, handled as for one token (GQA_DEV_BAD_SEQ_LEN, nothing written for
+ * that sequence).
+ *
+ * gqa_kv_append_multi - write the new tokens' rows:
+ *     k_cache[i, j, L_i - n + s, :] = k_new[i, s, j, :]   (likewise v)
+ *   k_new [b, n, g, d_k], v_new [b, n, g, d_v]      (read)
+ * Bit-exact, no other row touched.  Same requirements as gqa_kv_append.
+ *
+ * gqa_decode_attn_multi - for every sequence i, token s and query head a
+ * (r = h / g, j = a / r, P = L_i - n + s):
+ *     s[p]          = scale * sum_c q[i, s, a, c] * k_cache[i, j, p, c],  p <= P
+ *     out[i, s, a, :] = sum_{p <= P} softmax(s)[p] * v_cache[i, j, p, :]
+ *   q   [b, n, h, d_k]   (read)
+ *   out [b, n, h, d_v]   (written)
+ * The n * r query rows of one KV head share each K/V tile read (one pass
+ * over the cache for all n tokens).  Supported: n * (h / g) <= 32 with bf16
+ * and d = 128 (tensor-core kernel); n * (h / g) <= 16 with fp32 and
+ * n * (h / g) <= 8 with bf16 and d = 64 (CUDA-core kernel); otherwise
+ * GQA_ERR_UNSUPPORTED.  Other limits, errors and the workspace are those of
+ * gqa_decode_attn (the partials grow by the factor n).
+ *
+ * gqa_decode_step_multi - append and attention in one launch, as
+ * gqa_decode_step does for one token: k_cache / v_cache are written at rows
+ * L_i - n .. L_i - 1 exactly as gqa_kv_append_multi writes them, and out
+ * equals gqa_kv_append_multi followed by gqa_decode_attn_multi.  flags as
+ * for gqa_decode_step (GQA_STEP_EARLY_STREAM: the kernels ahead of it on the
+ * stream must not write seq_lens or the rows below L_i - n).
+ */
+int gqa_kv_append_multi(const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int32_t* seq_lens, int b, int n, int g,
+                        int d_k, int d_v, int cap, int dtype, void* stream);
+
+int gqa_decode_attn_multi(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* seq_lens, int b, int n, int h, int g, int d_k,
+                          int d_v, float scale, void* out, int cap, int dtype,
+                          void* stream);
+
+int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new,
+                          void* k_cache, void* v_cache, const int32_t* seq_lens, int b,
+                          int n, int h, int g, int d_k, int d_v, float scale, void* out,
+                          int cap, int dtype, int flags, void* stream);
+
+/*
  * gqa_device_status - read and clear the device status word of the current
  * device.  Synchronizes `stream` first, so the word covers every call queued
  * on it before.  *bits_out receives an OR of GQA_DEV_* bits (0 = clean).

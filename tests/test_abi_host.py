@@ -120,3 +120,49 @@ def test_valid_arguments_without_a_gpu_report_a_cuda_error():
     b = _lib()
     assert _attn(b) in (-6, -7)
     assert _app(b) in (-6, -7)
+
+
+def _attn_multi(lib_, **kw):
+    args = dict(q=A, k=A, v=A, lens=A, b=2, n=3, h=8, g=2, dk=128, dv=128, scale=0.1,
+                out=A, cap=64, dtype=1)
+    args.update(kw)
+    return lib_.lib.gqa_decode_attn_multi(
+        args["q"], args["k"], args["v"], args["lens"], args["b"], args["n"], args["h"],
+        args["g"], args["dk"], args["dv"], args["scale"], args["out"], args["cap"],
+        args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), -1), (dict(n=0), -2), (dict(n=-1), -2), (dict(n=65, cap=64), -2),
+    (dict(h=6, g=4), -2), (dict(q=A + 8), -4),
+    (dict(n=9, h=8, g=2), -5),                  # 9 * 4 query rows > 32
+    (dict(n=3, dtype=0, h=12, g=2), -5),        # fp32: 18 rows > 16
+    (dict(n=2, dtype=1, dk=64, dv=64, h=10, g=2), -5),  # bf16 d=64: 10 rows > 8
+    (dict(dtype=3), -3),
+])
+def test_decode_attn_multi_host_checks(kw, code):
+    assert _attn_multi(_lib(), **kw) == code
+
+
+def test_multi_step_and_append_host_checks():
+    b = _lib()
+    f = b.lib.gqa_decode_step_multi
+    args = [A, A, A, A, A, A, 2, 3, 8, 2, 128, 128, 0.1, A, 64, 1, 0, None]
+    assert f(*args[:1], 0, *args[2:]) == -1          # k_new null
+    bad = list(args)
+    bad[7] = 0
+    assert f(*bad) == -2                             # n < 1
+    bad = list(args)
+    bad[16] = 2
+    assert f(*bad) == -5                             # unknown flag bits
+    app = b.lib.gqa_kv_append_multi
+    aargs = [A, A, A, A, A, 2, 3, 2, 128, 128, 64, 1, None]
+    bad = list(aargs)
+    bad[6] = 0
+    assert app(*bad) == -2                           # n < 1
+    bad = list(aargs)
+    bad[6] = 65
+    assert app(*bad) == -2                           # n > cap
+    bad = list(aargs)
+    bad[0] = 0
+    assert app(*bad) == -1
