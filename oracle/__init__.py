@@ -18,4 +18,8 @@ from .oracle import (  # noqa: F401
     kv_append_multi,
     grouped_decode_attention_multi,
     decode_step_multi,
+    to_storage,
+    project_qkv,
+    project_out,
+    decode_layer,
 )

@@ -58,6 +58,10 @@ __all__ = [
     "kv_append_multi",
     "grouped_decode_attention_multi",
     "decode_step_multi",
+    "to_storage",
+    "project_qkv",
+    "project_out",
+    "decode_layer",
 ]
 
 
@@ -264,6 +268,68 @@ def decode_step_multi(q, k_cache, v_cache, k_new, v_new, seq_lens, g: int,
     kc, vc = kv_append_multi(k_cache, v_cache, k_new, v_new, seq_lens)
     o = grouped_decode_attention_multi(q, kc, vc, seq_lens, g, scale, dtype)
     return o, kc, vc
+
+
+# ---------------------------------------------------------------------------
+# the layer around the step ([MQA review] §2.4 MultiheadSelfAttentionIncremental
+# and §3 MultiquerySelfAttentionIncremental): projections of x into q and the
+# new K/V rows, the step, and the output projection
+# ---------------------------------------------------------------------------
+def to_storage(a64, dtype: str):
+    """Round float64 values to the storage encoding named by ``dtype``:
+    'bf16' -> uint16 bit patterns of the round-to-nearest-even bfloat16,
+    'f32' -> float32 (numpy's conversion rounds to nearest even), 'f64' ->
+    unchanged.  The bf16 rounding keeps 8 significant bits of the float64
+    value directly (no intermediate float32); it is exact for magnitudes in
+    the normal bfloat16 range [2^-126, 2^128) and for 0."""
+    a = np.asarray(a64, dtype=np.float64)
+    if dtype == "f64":
+        return a.copy()
+    if dtype == "f32":
+        return a.astype(np.float32)
+    if dtype != "bf16":
+        raise ValueError(f"unknown dtype {dtype!r}")
+    m, e = np.frexp(a)                       # a = m * 2^e, 0.5 <= |m| < 1
+    r = np.round(np.ldexp(m, 8))             # 8 significant bits, ties to even
+    v = np.ldexp(r, e - 8).astype(np.float32)   # exact: 8 bits fit a float32
+    return (v.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def project_qkv(x, P_q, P_k, P_v, dtype: str = "f64"):
+    """q = "bd,hdk->bhk"(x, P_q), k_new = "bd,gdk->bgk"(x, P_k), v_new =
+    "bd,gdv->bgv"(x, P_v) in float64 ([MQA review] §2.4, with the KV-head
+    axis of P_k / P_v reduced to g as §3 reduces it to one: P_q [h, D, d_k],
+    P_k [g, D, d_k], P_v [g, D, d_v], x [b, D] in the ``dtype`` encoding)."""
+    x64 = widen(x, dtype)
+    q = np.einsum("bd,hdk->bhk", x64, widen(P_q, dtype))
+    kn = np.einsum("bd,gdk->bgk", x64, widen(P_k, dtype))
+    vn = np.einsum("bd,gdv->bgv", x64, widen(P_v, dtype))
+    return q, kn, vn
+
+
+def project_out(o, P_o, dtype: str = "f64"):
+    """y = "bhv,hdv->bd"(o, P_o) in float64 ([MQA review] §2.4 / §3):
+    o [b, h, d_v], P_o [h, D, d_v]."""
+    return np.einsum("bhv,hdv->bd", widen(o, dtype), widen(P_o, dtype))
+
+
+def decode_layer(x, P_q, P_k, P_v, P_o, k_cache, v_cache, seq_lens, g: int,
+                 scale: float, dtype: str = "f64"):
+    """One incremental layer: project x, append the new K/V rows, attend,
+    project the output ([MQA review] §2.4 / §3, grouped KV heads).
+
+    The tensors the layer stores (q, the new K/V rows, o) are held in the
+    storage encoding ``dtype``: each is computed in float64 and rounded once
+    to it (``to_storage``) before the next step reads it; y is returned in
+    float64.  Returns (y [b, D], k_cache', v_cache', q, o) with the caches,
+    q and o in the storage encoding.
+    """
+    q, kn, vn = project_qkv(x, P_q, P_k, P_v, dtype)
+    q_s, kn_s, vn_s = (to_storage(t, dtype) for t in (q, kn, vn))
+    o, kc, vc = decode_step(q_s, k_cache, v_cache, kn_s, vn_s, seq_lens, g, scale, dtype)
+    o_s = to_storage(o, dtype)
+    y = project_out(o_s, P_o, dtype)
+    return y, kc, vc, q_s, o_s
 
 
 # ---------------------------------------------------------------------------
