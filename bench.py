@@ -242,10 +242,15 @@ def blas_threads() -> int:
 def run_ours(args, rank, local_rank, world):
     import torch
     from gqa_kv_cache_append_gb300 import binding as B
-    from gqa_kv_cache_append_gb300.inputs import make_layer, make_layer_multi, seq_lens_for, workload
+    from gqa_kv_cache_append_gb300.inputs import (make_layer, make_layer_multi,
+                                                  make_layer_weights, projection_bytes,
+                                                  seq_lens_for, workload)
     import dataclasses
 
     n = args.tokens
+    full_layer = args.layer
+    if full_layer and n > 1:
+        raise SystemExit("--layer runs one new token per step")
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
@@ -269,20 +274,28 @@ def run_ours(args, rank, local_rank, world):
     # least 4x the L2 size, so every step reads K/V from HBM
     from gqa_kv_cache_append_gb300.inputs import layer_bytes as _lb, layer_flops
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_layer = _lb(base, lens, n)
+    per_layer = _lb(base, lens, n) + (projection_bytes(base) if full_layer else 0)
     if base.layers * per_layer < 4 * l2 and not args.layers:
         base = dataclasses.replace(base, layers=-(-4 * l2 // per_layer))
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
     layers = [make_layer(cfg, l, dev) if n == 1 else make_layer_multi(cfg, n, l, dev)
               for l in range(cfg.layers)]
+    if full_layer:
+        # the layer's input is x; q / k_new / v_new come from the projections
+        for l, x in enumerate(layers):
+            for key in ("q", "k_new", "v_new"):
+                del x[key]
+            x.update(make_layer_weights(cfg, l, dev))
     # the step's per-layer inputs and outputs live in one packed buffer each
     # (layer-major), so the end-to-end leg moves them with one copy apiece
     packed = {}
-    for key in ("q", "k_new", "v_new"):
+    for key in (("x",) if full_layer else ("q", "k_new", "v_new")):
         packed[key] = torch.stack([x[key] for x in layers]).contiguous()
         for l, x in enumerate(layers):
             x[key] = packed[key][l]
     out_shape = (cfg.b, cfg.h, cfg.d) if n == 1 else (cfg.b, n, cfg.h, cfg.d)
+    if full_layer:
+        out_shape = (cfg.b, cfg.D)
     out_all = torch.empty((cfg.layers, *out_shape), dtype=cfg.torch_dtype, device=dev)
     outs = [out_all[l] for l in range(cfg.layers)]
     # --graph: the step is captured once in a CUDA graph and replayed; the
@@ -290,10 +303,17 @@ def run_ours(args, rank, local_rank, world):
     stream = torch.cuda.Stream(dev) if args.graph else torch.cuda.current_stream(dev)
     torch.cuda.set_stream(stream)
     sb = step_bytes(cfg, lens, n)
+    if full_layer:
+        sb["proj_per_layer"] = projection_bytes(cfg)
+        sb["step"] += cfg.layers * sb["proj_per_layer"]
     early = 0 if args.ordered else B.GQA_STEP_EARLY_STREAM
 
     def layer_call(l, x):
-        if n > 1:
+        if full_layer:
+            B.gqa_decode_layer(x["x"], x["P_q"], x["P_k"], x["P_v"], x["P_o"], x["k_cache"],
+                               x["v_cache"], x["seq_lens"], cfg.b, cfg.D, cfg.h, cfg.g, cfg.d,
+                               cfg.d, cfg.scale, outs[l], flags=early, stream=stream)
+        elif n > 1:
             if args.separate:
                 B.gqa_kv_append_multi(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
                                       x["seq_lens"], cfg.b, n, cfg.g, cfg.d, cfg.d, stream=stream)
@@ -414,11 +434,11 @@ def run_ours(args, rank, local_rank, world):
     if rank != 0:
         return None
     peaks = measured_peaks()
-    call_bytes = sb["attn_per_layer"] + sb["append_per_layer"]
+    call_bytes = sb["attn_per_layer"] + sb["append_per_layer"] + sb.get("proj_per_layer", 0)
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
-    traffic = profiled_traffic(src, args.workload, n)
-    launches_per_step = (2 if args.separate else 1) * cfg.layers
+    traffic = None if full_layer else profiled_traffic(src, args.workload, n)
+    launches_per_step = (3 if full_layer else (2 if args.separate else 1)) * cfg.layers
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -442,6 +462,8 @@ def run_ours(args, rank, local_rank, world):
             "parallelism": f"replicas x{world}",
             "launch": "CUDA graph" if args.graph else "stream",
             "tokens_per_step": n,
+            "scope": "whole layer: projections + append + attention" if full_layer
+                     else "append + attention",
         },
         "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
         "attn_tflops_per_gpu": round(layer_flops(cfg, lens, n) / (attn_avg_ms * 1e-3) / 1e12, 2),
@@ -449,8 +471,9 @@ def run_ours(args, rank, local_rank, world):
         "pct_of_nominal_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": ("gqa_kv_append + gqa_decode_attn" if args.separate else "gqa_decode_step")
-                      + ("_multi" if n > 1 else "")
+            "kernel": ("gqa_decode_layer (proj_tc_kernel x2 + " if full_layer else "")
+                      + ("gqa_kv_append + gqa_decode_attn" if args.separate else "gqa_decode_step")
+                      + ("_multi" if n > 1 else "") + (")" if full_layer else "")
                       + f" ({'decode_tc_kernel' if cfg.dtype == 'bf16' and cfg.d == 128 else 'decode_simt_kernel'})",
             "achieved": round(achieved, 2),
             "peak": peaks["hbm_gbs"],
@@ -475,7 +498,10 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clk,
         "device_status": status,
     }
-    if not args.no_cpu_baseline:
+    if full_layer and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {"skipped": "the oracle baseline is timed on the step "
+                                           "(run without --layer)"}
+    elif not args.no_cpu_baseline:
         gbs, spent, units, nbytes = oracle_sample(base, target_s=args.cpu_seconds, n=n)
         line["cpu_baseline"] = {
             "value": round(gbs, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
@@ -547,6 +573,9 @@ def main(argv=None):
                     help="time gqa_kv_append + gqa_decode_attn instead of gqa_decode_step")
     ap.add_argument("--tokens", type=int, default=1,
                     help="new tokens per sequence per step (causal; speculative / chunked decode)")
+    ap.add_argument("--layer", action="store_true",
+                    help="time the whole incremental layer (q/k/v projection, step, output "
+                         "projection) through gqa_decode_layer")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small profiling cases)")
     args = ap.parse_args(argv)

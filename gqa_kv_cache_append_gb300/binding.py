@@ -48,6 +48,11 @@ SIGNATURES = {
                                    _VP]),
     "gqa_decode_step_multi": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F,
                                    _VP, _I, _I, _I, _VP]),
+    "gqa_project_qkv": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
+                             _I, _VP]),
+    "gqa_project_out": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
+    "gqa_decode_layer": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                              _F, _VP, _I, _I, _I, _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -196,6 +201,33 @@ def gqa_decode_step_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, 
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
         int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out),
         int(cap), _dtype(q, dtype), int(flags), _stream(stream)))
+
+
+def gqa_project_qkv(x, w_q, w_k, w_v, q, k_new, v_new, b, d_model, h, g, d_k, d_v,
+                    dtype=None, flags=0, stream=None) -> None:
+    """q / k_new / v_new = x . P_q / P_k / P_v ("bd,hdk->bhk" and its KV forms)."""
+    _check("gqa_project_qkv", lib.gqa_project_qkv(
+        _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(q), _ptr(k_new), _ptr(v_new),
+        int(b), int(d_model), int(h), int(g), int(d_k), int(d_v), _dtype(x, dtype),
+        int(flags), _stream(stream)))
+
+
+def gqa_project_out(o, w_o, y, b, d_model, h, d_v, dtype=None, flags=0, stream=None) -> None:
+    """y = "bhv,hdv->bd"(o, P_o)."""
+    _check("gqa_project_out", lib.gqa_project_out(
+        _ptr(o), _ptr(w_o), _ptr(y), int(b), int(d_model), int(h), int(d_v),
+        _dtype(o, dtype), int(flags), _stream(stream)))
+
+
+def gqa_decode_layer(x, w_q, w_k, w_v, w_o, k_cache, v_cache, seq_lens, b, d_model, h, g,
+                     d_k, d_v, scale, y, cap=None, dtype=None, flags=0, stream=None) -> None:
+    """The incremental layer: project x, append, attend, project the output."""
+    if cap is None:
+        cap = k_cache.shape[2]
+    _check("gqa_decode_layer", lib.gqa_decode_layer(
+        _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(w_o), _ptr(k_cache), _ptr(v_cache),
+        _ptr(seq_lens), int(b), int(d_model), int(h), int(g), int(d_k), int(d_v),
+        float(scale), _ptr(y), int(cap), _dtype(x, dtype), int(flags), _stream(stream)))
 
 
 def gqa_device_status(stream=None) -> int:

@@ -746,54 +746,23 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
 // 2-D map over a row-major [rows x 128] bf16 tensor, box [box_rows x 64],
 // 128-byte swizzle, zero fill outside.  (The query map is 3-D:
 // [b * n tokens][h heads][128], box [n][r][64].)
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
-  const cuuint32_t box[2] = {64u, box_rows};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[2] = {static_cast<uint64_t>(kD), rows};
+  const uint64_t strides[1] = {static_cast<uint64_t>(kD) * 2};
+  const uint32_t box[2] = {64u, box_rows};
+  return encode_bf16_map(map, base, 2, dims, strides, box);
 }
 
 bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h),
-                              static_cast<cuuint64_t>(b) * nq};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                                 static_cast<cuuint64_t>(h) * kD * 2};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(r), static_cast<cuuint32_t>(nq)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(h),
+                            static_cast<uint64_t>(b) * nq};
+  const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2,
+                               static_cast<uint64_t>(h) * kD * 2};
+  const uint32_t box[3] = {64u, static_cast<uint32_t>(r), static_cast<uint32_t>(nq)};
+  return encode_bf16_map(map, base, 3, dims, strides, box);
 }
 
 template <int NP, int NWG, bool MULTI>

@@ -310,7 +310,45 @@ int launch_all(DecodeLaunch& a, int tile) {
 
 int elt_bytes(int dtype) { return dtype == GQA_F32 ? 4 : 2; }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
 }  // namespace
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int k = 0; k < rank; ++k) {
+    d[k] = dims[k];
+    bx[k] = box[k];
+    es[k] = 1u;
+    if (k > 0) st[k - 1] = strides[k - 1];
+  }
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+             const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gqa
 
 using namespace gqa;
@@ -372,78 +410,118 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_c
 namespace gqa {
 namespace {
 
-// gqa_decode_attn and gqa_decode_step: checks, kernel choice, workspace,
-// launch.  k_new / v_new null means attention only.
+// The arguments of one decode launch and its plan (kernel, CTAs, partials).
+struct DecodeArgs {
+  const void* q;
+  const void* k_new;     // null: attention only
+  const void* v_new;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* seq_lens;
+  int b, nq, h, g, d_k, d_v;
+  float scale;
+  void* out;
+  int cap, dtype, flags;
+};
+
+struct DecodePlan {
+  int tile = 0;
+  long long nc = 0;
+  size_t o_bytes = 0;     // partial outputs
+  size_t ml_bytes = 0;    // partial max / sum
+  size_t units = 0;       // arrival counters
+};
+
+// Host checks of a decode call (no CUDA call): GQA_OK or an error code.
+int decode_check(const DecodeArgs& x) {
+  if (x.flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
+  if (!x.q || !x.k_cache || !x.v_cache || !x.seq_lens || !x.out) return GQA_ERR_NULL;
+  if (x.dtype != GQA_F32 && x.dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (x.b < 1 || x.nq < 1 || x.h < 1 || x.g < 1 || x.d_k < 1 || x.d_v < 1 || x.cap < 1 ||
+      x.h % x.g != 0 || x.nq > x.cap)
+    return GQA_ERR_SHAPE;
+  if (static_cast<long long>(x.b) * x.g * x.cap + 256 > 0x7FFFFFFFll ||
+      static_cast<long long>(x.b) * x.nq * x.h > 0x7FFFFFFFll)
+    return GQA_ERR_SHAPE;
+  if (!aligned16(x.q) || !aligned16(x.k_cache) || !aligned16(x.v_cache) || !aligned16(x.out) ||
+      !aligned16(x.k_new) || !aligned16(x.v_new) ||
+      (reinterpret_cast<uintptr_t>(x.seq_lens) & 3u))
+    return GQA_ERR_ALIGN;
+  const int r = x.h / x.g;
+  if (x.d_k != x.d_v || x.b > 65535 || static_cast<long long>(x.nq) * r > 32)
+    return GQA_ERR_UNSUPPORTED;
+  const int cols = x.nq * r;  // query rows per KV head
+  if (!tc_supported(x.dtype, x.d_k, cols) && !simt_supported(x.dtype, x.d_k, cols))
+    return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+DecodePlan decode_plan(const DecodeArgs& x, int num_sms) {
+  const int r = x.h / x.g, d = x.d_k, cols = x.nq * r;
+  const bool use_tc = tc_supported(x.dtype, d, cols);
+  DecodePlan p;
+  p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, d);
+  const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(x.dtype, d, r);
+  const long long max_tiles = static_cast<long long>(x.b) * x.g * ((x.cap + p.tile - 1) / p.tile);
+  p.nc = static_cast<long long>(num_sms) * per_sm;
+  if (p.nc > max_tiles) p.nc = max_tiles;
+  if (p.nc < 1) p.nc = 1;
+  const size_t slots = static_cast<size_t>(x.b) * x.g + static_cast<size_t>(p.nc);
+  p.o_bytes = slots * cols * d * sizeof(float);
+  p.ml_bytes = slots * cols * 2 * sizeof(float);
+  // two arrival counters per unit: the tensor-core kernel may run two
+  // softmax warpgroups, each with its own
+  p.units = 2 * static_cast<size_t>(x.b) * x.g;
+  return p;
+}
+
+int decode_run(const DecodeArgs& x, const DecodePlan& p, const DeviceInfo* di, void* parts,
+               int* counters, cudaStream_t st) {
+  DecodeLaunch a;
+  a.q = x.q;
+  a.k_cache = x.k_cache;
+  a.v_cache = x.v_cache;
+  a.seq_lens = x.seq_lens;
+  a.b = x.b;
+  a.h = x.h;
+  a.g = x.g;
+  a.d = x.d_k;
+  a.cap = x.cap;
+  a.dtype = x.dtype;
+  a.nq = x.nq;
+  a.scale_log2 = static_cast<float>(static_cast<double>(x.scale) * 1.4426950408889634);
+  a.out = x.out;
+  a.part_o = static_cast<float*>(parts);
+  a.part_ml = reinterpret_cast<float*>(static_cast<char*>(parts) + p.o_bytes);
+  a.counters = counters;
+  a.k_new = x.k_new;
+  a.v_new = x.v_new;
+  a.k_cache_w = const_cast<void*>(x.k_cache);
+  a.v_cache_w = const_cast<void*>(x.v_cache);
+  a.early = (x.flags & GQA_STEP_EARLY_STREAM) != 0;
+  a.status = di->status;
+  a.budget = kWaitBudget;
+  a.nc = static_cast<int>(p.nc);
+  a.stream = st;
+  return launch_all(a, p.tile);
+}
+
+// gqa_decode_attn and gqa_decode_step (and their n-token forms): checks,
+// kernel choice, workspace, launch.
 int decode(const void* q, const void* k_new, const void* v_new, const void* k_cache,
            const void* v_cache, const int32_t* seq_lens, int b, int nq, int h, int g, int d_k,
            int d_v, float scale, void* out, int cap, int dtype, void* stream, int flags) {
-  if (flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
-  if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
-  if (b < 1 || nq < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0 ||
-      nq > cap)
-    return GQA_ERR_SHAPE;
-  if (static_cast<long long>(b) * g * cap + 256 > 0x7FFFFFFFll ||
-      static_cast<long long>(b) * nq * h > 0x7FFFFFFFll)
-    return GQA_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      !aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-    return GQA_ERR_ALIGN;
-  const int r = h / g;
-  const int d = d_k;
-  if (d_k != d_v || b > 65535 || static_cast<long long>(nq) * r > 32) return GQA_ERR_UNSUPPORTED;
-  const int cols = nq * r;  // query rows per KV head
-  const bool use_tc = tc_supported(dtype, d, cols);
-  if (!use_tc && !simt_supported(dtype, d, cols)) return GQA_ERR_UNSUPPORTED;
+  const DecodeArgs x{q, k_new, v_new, k_cache, v_cache, seq_lens, b, nq, h, g, d_k, d_v,
+                     scale, out, cap, dtype, flags};
+  if (int e = decode_check(x)) return e;
   DeviceInfo* di = nullptr;
   if (int e = device_info(&di)) return e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  const int tile = use_tc ? tc_tile() : simt_tile(dtype, d);
-  const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(dtype, d, r);
-  const long long max_tiles = static_cast<long long>(b) * g * ((cap + tile - 1) / tile);
-  long long nc = static_cast<long long>(di->num_sms) * per_sm;
-  if (nc > max_tiles) nc = max_tiles;
-  if (nc < 1) nc = 1;
-
-  const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
-  const size_t o_bytes = slots * cols * d * sizeof(float);
-  const size_t ml_bytes = slots * cols * 2 * sizeof(float);
+  const DecodePlan p = decode_plan(x, di->num_sms);
   void* ws = nullptr;
   int* counters = nullptr;
-  // two arrival counters per unit: the tensor-core kernel may run two
-  // softmax warpgroups, each with its own
-  if (int e = workspace(st, o_bytes + ml_bytes, 2 * static_cast<size_t>(b) * g, &ws, &counters))
-    return e;
-
-  DecodeLaunch a;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.seq_lens = seq_lens;
-  a.b = b;
-  a.h = h;
-  a.g = g;
-  a.d = d;
-  a.cap = cap;
-  a.dtype = dtype;
-  a.nq = nq;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  a.out = out;
-  a.part_o = static_cast<float*>(ws);
-  a.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
-  a.counters = counters;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.k_cache_w = const_cast<void*>(k_cache);
-  a.v_cache_w = const_cast<void*>(v_cache);
-  a.early = (flags & GQA_STEP_EARLY_STREAM) != 0;
-  a.status = di->status;
-  a.budget = kWaitBudget;
-  a.nc = static_cast<int>(nc);
-  a.stream = st;
-
-  return launch_all(a, tile);
+  if (int e = workspace(st, p.o_bytes + p.ml_bytes, p.units, &ws, &counters)) return e;
+  return decode_run(x, p, di, ws, counters, st);
 }
 
 }  // namespace
@@ -510,6 +588,174 @@ int gqa_selftest_wait_timeout(long long budget_cycles, void* stream) {
 
 }  // extern "C"
 
+
+// ---------------------------------------------------------------------------
+// the projections around the step and the whole layer (tcgen05 GEMMs in
+// proj_tc.cu): bf16, 128-wide heads, d_model a multiple of 128, b <= 128
+// ---------------------------------------------------------------------------
+namespace gqa {
+namespace {
+
+constexpr int kProjMaxBatch = 128;
+
+int proj_shape_check(int b, int D, int h, int g, int d_k, int d_v, int dtype) {
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (b < 1 || D < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || h % g != 0)
+    return GQA_ERR_SHAPE;
+  if (static_cast<long long>(h + 2 * g) * D > 0x7FFFFFFFll ||
+      static_cast<long long>(b) * D > 0x7FFFFFFFll)
+    return GQA_ERR_SHAPE;
+  if (dtype != GQA_BF16 || d_k != 128 || d_v != 128 || D % 128 != 0 || b > kProjMaxBatch)
+    return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct ProjPlan {
+  long long nc = 0;
+  size_t part_bytes = 0;
+  size_t units = 0;
+};
+
+ProjPlan proj_plan(int mode, int b, int D, int h, int g, int num_sms) {
+  ProjPlan p;
+  const long long W = proj_work(mode, D, h, g);
+  p.nc = W < num_sms ? W : num_sms;
+  const int tiles = proj_tiles(mode, D, h, g);
+  p.part_bytes = (static_cast<size_t>(tiles) + p.nc) * proj_nb(b) * 128 * sizeof(float);
+  p.units = static_cast<size_t>(tiles);
+  return p;
+}
+
+int proj_run(int mode, const void* w0, const void* w1, const void* w2, const void* x,
+             void* out0, void* out1, void* out2, int b, int D, int h, int g, bool early,
+             const ProjPlan& p, const DeviceInfo* di, void* parts, int* counters,
+             cudaStream_t st) {
+  ProjLaunch a;
+  a.mode = mode;
+  a.w0 = w0;
+  a.w1 = w1;
+  a.w2 = w2;
+  a.x = x;
+  a.out0 = out0;
+  a.out1 = out1;
+  a.out2 = out2;
+  a.b = b;
+  a.D = D;
+  a.h = h;
+  a.g = g;
+  a.part = static_cast<float*>(parts);
+  a.counters = counters;
+  a.status = di->status;
+  a.budget = kWaitBudget;
+  a.early = early;
+  a.nc = static_cast<int>(p.nc);
+  a.stream = st;
+  return launch_proj(a) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+int gqa_project_qkv(const void* x, const void* w_q, const void* w_k, const void* w_v, void* q,
+                    void* k_new, void* v_new, int b, int d_model, int h, int g, int d_k,
+                    int d_v, int dtype, int flags, void* stream) {
+  using namespace gqa;
+  if (flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
+  if (!x || !w_q || !w_k || !w_v || !q || !k_new || !v_new) return GQA_ERR_NULL;
+  if (int e = proj_shape_check(b, d_model, h, g, d_k, d_v, dtype)) return e;
+  if (!aligned16(x) || !aligned16(w_q) || !aligned16(w_k) || !aligned16(w_v) ||
+      !aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+    return GQA_ERR_ALIGN;
+  DeviceInfo* di = nullptr;
+  if (int e = device_info(&di)) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ProjPlan p = proj_plan(0, b, d_model, h, g, di->num_sms);
+  void* ws = nullptr;
+  int* counters = nullptr;
+  if (int e = workspace(st, p.part_bytes, p.units, &ws, &counters)) return e;
+  return proj_run(0, w_q, w_k, w_v, x, q, k_new, v_new, b, d_model, h, g,
+                  (flags & GQA_STEP_EARLY_STREAM) != 0, p, di, ws, counters, st);
+}
+
+int gqa_project_out(const void* o, const void* w_o, void* y, int b, int d_model, int h,
+                    int d_v, int dtype, int flags, void* stream) {
+  using namespace gqa;
+  if (flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
+  if (!o || !w_o || !y) return GQA_ERR_NULL;
+  if (int e = proj_shape_check(b, d_model, h, 1, 128, d_v, dtype)) return e;
+  if (!aligned16(o) || !aligned16(w_o) || !aligned16(y)) return GQA_ERR_ALIGN;
+  DeviceInfo* di = nullptr;
+  if (int e = device_info(&di)) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ProjPlan p = proj_plan(1, b, d_model, h, 1, di->num_sms);
+  void* ws = nullptr;
+  int* counters = nullptr;
+  if (int e = workspace(st, p.part_bytes, p.units, &ws, &counters)) return e;
+  return proj_run(1, w_o, nullptr, nullptr, o, y, nullptr, nullptr, b, d_model, h, 1,
+                  (flags & GQA_STEP_EARLY_STREAM) != 0, p, di, ws, counters, st);
+}
+
+int gqa_decode_layer(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                     const void* w_o, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                     int b, int d_model, int h, int g, int d_k, int d_v, float scale, void* y,
+                     int cap, int dtype, int flags, void* stream) {
+  using namespace gqa;
+  if (flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
+  if (!x || !w_q || !w_k || !w_v || !w_o || !y) return GQA_ERR_NULL;
+  if (int e = proj_shape_check(b, d_model, h, g, d_k, d_v, dtype)) return e;
+  if (!aligned16(x) || !aligned16(w_q) || !aligned16(w_k) || !aligned16(w_v) ||
+      !aligned16(w_o) || !aligned16(y))
+    return GQA_ERR_ALIGN;
+  // the step's own checks, with stand-in (aligned, non-null) addresses for
+  // the intermediate tensors the library keeps in its workspace
+  const void* stand_in = reinterpret_cast<const void*>(uintptr_t(256));
+  DecodeArgs dx{stand_in, stand_in, stand_in, k_cache, v_cache, seq_lens, b, 1, h, g,
+                d_k, d_v, scale, const_cast<void*>(stand_in), cap, dtype, flags};
+  if (int e = decode_check(dx)) return e;
+  DeviceInfo* di = nullptr;
+  if (int e = device_info(&di)) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ProjPlan p0 = proj_plan(0, b, d_model, h, g, di->num_sms);
+  const ProjPlan p1 = proj_plan(1, b, d_model, h, 1, di->num_sms);
+  const DecodePlan pd = decode_plan(dx, di->num_sms);
+  // workspace: q | k_new | v_new | o | partials (the largest of the three)
+  const size_t qb = align256(static_cast<size_t>(b) * h * 128 * 2);
+  const size_t kb = align256(static_cast<size_t>(b) * g * 128 * 2);
+  size_t parts = p0.part_bytes;
+  if (p1.part_bytes > parts) parts = p1.part_bytes;
+  if (pd.o_bytes + pd.ml_bytes > parts) parts = pd.o_bytes + pd.ml_bytes;
+  size_t units = p0.units;
+  if (p1.units > units) units = p1.units;
+  if (pd.units > units) units = pd.units;
+  void* ws = nullptr;
+  int* counters = nullptr;
+  if (int e = workspace(st, 2 * qb + 2 * kb + parts, units, &ws, &counters)) return e;
+  char* base = static_cast<char*>(ws);
+  void* q = base;
+  void* kn = base + qb;
+  void* vn = base + qb + kb;
+  void* o = base + qb + 2 * kb;
+  void* part = base + 2 * qb + 2 * kb;
+  const bool early = (flags & GQA_STEP_EARLY_STREAM) != 0;
+  if (int e = proj_run(0, w_q, w_k, w_v, x, q, kn, vn, b, d_model, h, g, early, p0, di, part,
+                       counters, st))
+    return e;
+  dx.q = q;
+  dx.k_new = kn;
+  dx.v_new = vn;
+  dx.out = o;
+  // (early streaming only with the caller's consent: a kernel that started
+  // before the projection, e.g. one writing this cache, may still run)
+  if (int e = decode_run(dx, pd, di, part, counters, st)) return e;
+  return proj_run(1, w_o, nullptr, nullptr, o, y, nullptr, nullptr, b, d_model, h, 1, early,
+                  p1, di, part, counters, st);
+}
+
+}  // extern "C"
 
 // ---------------------------------------------------------------------------
 // gqa_decode_attn_noalloc: the same decode, with the split partials in a

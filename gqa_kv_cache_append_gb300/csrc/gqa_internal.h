@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace gqa {
@@ -31,6 +32,12 @@ struct DecodeLaunch {
   cudaStream_t stream;
 };
 
+// Tiled TMA map over a row-major bf16 tensor: dims[0] is the contiguous
+// (innermost) extent, strides[k] the byte stride of dimension k + 1, box the
+// copied box; 128-byte swizzle, 256-byte L2 promotion, zero fill outside.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box);
+
 // CUDA-core kernel (fp32, and bf16 with d = 64); `cols` = nq * r query rows
 // per KV head
 bool simt_supported(int dtype, int d, int cols);
@@ -44,5 +51,30 @@ int tc_tile();
 int tc_ctas_per_sm(int r);
 cudaError_t launch_decode_tc(const DecodeLaunch& a);
 
+// tcgen05 projection GEMMs around the step (bf16, 128-wide heads):
+// mode 0: q / k_new / v_new = x . P_q / P_k / P_v; mode 1: y = o . P_o
+struct ProjLaunch {
+  int mode;
+  const void* w0;        // P_q (mode 0) or P_o (mode 1), [heads, D, 128]
+  const void* w1;        // P_k [g, D, 128] (mode 0)
+  const void* w2;        // P_v [g, D, 128] (mode 0)
+  const void* x;         // x [b, D] (mode 0) or o [b, h, 128] (mode 1)
+  void* out0;            // q [b, h, 128] (mode 0) or y [b, D] (mode 1)
+  void* out1;            // k_new [b, g, 128] (mode 0)
+  void* out2;            // v_new [b, g, 128] (mode 0)
+  int b, D, h, g;
+  float* part;           // [tiles + nc, NB, 128] fp32 partial sums
+  int* counters;         // [tiles] arrivals; zero between launches
+  unsigned int* status;
+  long long budget;
+  bool early;            // stream the weights before the dependency wait
+  int nc;
+  cudaStream_t stream;
+};
+
+int proj_nb(int b);                                   // batch columns of the MMA
+long long proj_work(int mode, int D, int h, int g);   // K chunks of the launch
+int proj_tiles(int mode, int D, int h, int g);
+cudaError_t launch_proj(const ProjLaunch& a);
 
 }  // namespace gqa

@@ -30,6 +30,12 @@ Steps with n new tokens per sequence (make_layer_multi, 'plain' workloads
 only) draw in the same order from a generator seeded s * 1000 + l + 100000 * n:
 the K cache, the V cache, q [b, n, h, d], k_new [b, n, g, d], v_new
 [b, n, g, d].
+
+The projections of a whole layer (make_layer_weights) come from a generator
+seeded s * 1000 + l + 500000: P_q [h, D, d], P_k [g, D, d], P_v [g, D, d],
+each N(0, 1/D); P_o [h, D, d], N(0, 1/(h d)); then x [b, D], N(0, 1); all
+rounded to the storage dtype.  D is the model width of the workload (the
+pages' d), so q, the new rows and y stay of order one.
 """
 from __future__ import annotations
 
@@ -41,7 +47,8 @@ import numpy as np
 import torch
 
 __all__ = ["DecodeConfig", "WORKLOADS", "workload", "seq_lens_for",
-           "make_layer", "make_layer_multi", "layer_bytes", "layer_flops"]
+           "make_layer", "make_layer_multi", "make_layer_weights", "layer_bytes",
+           "layer_flops", "projection_bytes"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -60,10 +67,15 @@ class DecodeConfig:
     ragged: Optional[tuple] = None   # (lo, hi) inclusive, or None = full
     boost: float = 8.0
     boost_frac: float = 0.01
+    d_model: int = 0           # model width D; 0 means h * d
 
     @property
     def r(self) -> int:
         return self.h // self.g
+
+    @property
+    def D(self) -> int:
+        return self.d_model if self.d_model else self.h * self.d
 
     @property
     def elt(self) -> int:
@@ -85,13 +97,15 @@ WORKLOADS = {
     "gqa_sweep_b16_h32_d128_m4096": DecodeConfig(
         "gqa_sweep_b16_h32_d128_m4096", 1, 16, 32, 8, 128, 4096, "bf16",
         _S128, 2, kind="meanpool"),
-    # Llama-3-70B-shaped step: 80 layers, 64 query / 8 KV heads
+    # Llama-3-70B-shaped step: 80 layers, 64 query / 8 KV heads, width 8192
     "llama3_70b_b32_m8192": DecodeConfig(
-        "llama3_70b_b32_m8192", 80, 32, 64, 8, 128, 8192, "bf16", _S128, 3),
-    # Qwen2.5-7B-shaped ragged batch: 28 layers, 28 query / 4 KV heads
+        "llama3_70b_b32_m8192", 80, 32, 64, 8, 128, 8192, "bf16", _S128, 3,
+        d_model=8192),
+    # Qwen2.5-7B-shaped ragged batch: 28 layers, 28 query / 4 KV heads,
+    # width 3584
     "qwen25_7b_b64_ragged": DecodeConfig(
         "qwen25_7b_b64_ragged", 28, 64, 28, 4, 128, 32768, "bf16", _S128, 4,
-        ragged=(512, 32768)),
+        ragged=(512, 32768), d_model=3584),
     # long-context MQA with a peaked softmax
     "long_mqa_b8_m131072": DecodeConfig(
         "long_mqa_b8_m131072", 1, 8, 32, 1, 128, 131072, "bf16", _S128, 5,
@@ -244,6 +258,35 @@ def make_layer_multi(cfg: DecodeConfig, n: int, layer: int = 0, device="cpu",
         "seq_lens": torch.from_numpy(lens.copy()).to(device),
         "lens": lens,
     }
+
+
+def make_layer_weights(cfg: DecodeConfig, layer: int = 0, device="cpu") -> dict:
+    """Projection weights of one layer in the pages' layouts and the layer
+    input: P_q [h, D, d], P_k [g, D, d], P_v [g, D, d], P_o [h, D, d],
+    x [b, D], in the storage dtype on ``device``."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed * 1000 + layer + 500000)
+    b, h, g, d, D = cfg.b, cfg.h, cfg.g, cfg.d, cfg.D
+    dt = cfg.torch_dtype
+    out = {}
+    for name, shape, std in (("P_q", (h, D, d), D ** -0.5), ("P_k", (g, D, d), D ** -0.5),
+                             ("P_v", (g, D, d), D ** -0.5), ("P_o", (h, D, d), (h * d) ** -0.5)):
+        w = torch.empty(shape, dtype=dt, device=device)
+        for a in range(shape[0]):
+            w[a].copy_(_randn(shape[1:], gen, device) * std)
+        out[name] = w
+    out["x"] = _randn((b, D), gen, device).to(dt)
+    return out
+
+
+def projection_bytes(cfg: DecodeConfig) -> int:
+    """Algorithmic bytes of the projections of one layer: the weights P_q,
+    P_k, P_v, P_o once, x and y, and q / k_new / v_new / o written and read."""
+    w = (2 * cfg.h + 2 * cfg.g) * cfg.D * cfg.d * cfg.elt
+    act = 2 * cfg.b * cfg.D * cfg.elt
+    inter = 2 * cfg.b * (2 * cfg.h + 2 * cfg.g) * cfg.d * cfg.elt
+    return w + act + inter
 
 
 def _boost(cfg, layer, q, k_cache, k_new, lens):

@@ -215,6 +215,46 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new,
                           int cap, int dtype, int flags, void* stream);
 
 /*
+ * The projections around the step and the whole incremental layer: the
+ * einsums of MultiheadSelfAttentionIncremental (MQA review §2.4) and
+ * MultiquerySelfAttentionIncremental (§3), with the KV-head axis of P_k and
+ * P_v reduced to g:
+ *     q     = "bd,hdk->bhk"(x, P_q)      k_new = "bd,gdk->bgk"(x, P_k)
+ *     v_new = "bd,gdv->bgv"(x, P_v)      y     = "bhv,hdv->bd"(o, P_o)
+ * Weights keep the pages' layouts, row-major: P_q [h, D, d_k], P_k [g, D, d_k],
+ * P_v [g, D, d_v], P_o [h, D, d_v] (D = d_model); x [b, D], y [b, D].
+ * Arithmetic: bf16 inputs, fp32 accumulation, each output rounded once to
+ * bf16 (nearest even).  Supported: dtype GQA_BF16, d_k = d_v = 128, D a
+ * multiple of 128, 1 <= b <= 128; otherwise GQA_ERR_UNSUPPORTED (GQA_F32
+ * included).  Weights are read from HBM once per call (tensor-core GEMMs with
+ * the batch on the MMA's N axis); the split partials use the per-(device,
+ * stream) workspace described above.  flags: 0 or GQA_STEP_EARLY_STREAM (the
+ * weights may be streamed before the kernels ahead on the stream complete;
+ * the caller guarantees none of them writes the weights).
+ *
+ * gqa_project_qkv - q [b, h, d_k], k_new [b, g, d_k], v_new [b, g, d_v]
+ *                   (written) from x and P_q, P_k, P_v (read).
+ * gqa_project_out - y [b, D] (written) from o [b, h, d_v] and P_o (read).
+ * gqa_decode_layer - the layer in three launches: gqa_project_qkv, then
+ *     gqa_decode_step (append at row L_i - 1, attention), then
+ *     gqa_project_out, with q, k_new, v_new and o kept in the library's
+ *     workspace (bf16).  k_cache / v_cache / seq_lens / scale / cap as for
+ *     gqa_decode_step; with GQA_STEP_EARLY_STREAM the step's contract applies
+ *     too (no kernel ahead writes seq_lens or the cache rows below L_i - 1).
+ */
+int gqa_project_qkv(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                    void* q, void* k_new, void* v_new, int b, int d_model, int h, int g,
+                    int d_k, int d_v, int dtype, int flags, void* stream);
+
+int gqa_project_out(const void* o, const void* w_o, void* y, int b, int d_model, int h,
+                    int d_v, int dtype, int flags, void* stream);
+
+int gqa_decode_layer(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                     const void* w_o, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                     int b, int d_model, int h, int g, int d_k, int d_v, float scale,
+                     void* y, int cap, int dtype, int flags, void* stream);
+
+/*
  * gqa_device_status - read and clear the device status word of the current
  * device.  Synchronizes `stream` first, so the word covers every call queued
  * on it before.  *bits_out receives an OR of GQA_DEV_* bits (0 = clean).

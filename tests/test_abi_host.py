@@ -166,3 +166,38 @@ def test_multi_step_and_append_host_checks():
     bad = list(aargs)
     bad[0] = 0
     assert app(*bad) == -1
+
+
+def test_projection_and_layer_host_checks():
+    b = _lib()
+    pq = b.lib.gqa_project_qkv
+    # x, wq, wk, wv, q, kn, vn, b, D, h, g, dk, dv, dtype, flags, stream
+    args = [A, A, A, A, A, A, A, 4, 256, 8, 2, 128, 128, 1, 0, None]
+
+    def call(f, base, **idx):
+        a = list(base)
+        for k, v in idx.items():
+            a[int(k[1:])] = v
+        return f(*a)
+    assert call(pq, args, i0=0) == -1                 # x null
+    assert call(pq, args, i13=0) == -5                # fp32: no projection kernel
+    assert call(pq, args, i13=5) == -3
+    assert call(pq, args, i8=200) == -5               # D not a multiple of 128
+    assert call(pq, args, i7=129) == -5               # b > 128
+    assert call(pq, args, i7=0) == -2
+    assert call(pq, args, i11=64, i12=64) == -5       # head dim 64
+    assert call(pq, args, i9=6, i10=4) == -2          # h % g
+    assert call(pq, args, i4=A + 2) == -4
+    assert call(pq, args, i14=4) == -5                # unknown flag
+    po = b.lib.gqa_project_out
+    oargs = [A, A, A, 4, 256, 8, 128, 1, 0, None]
+    assert call(po, oargs, i1=0) == -1
+    assert call(po, oargs, i6=64) == -5
+    assert call(po, oargs, i2=A + 8) == -4
+    dl = b.lib.gqa_decode_layer
+    largs = [A, A, A, A, A, A, A, A, 4, 256, 8, 2, 128, 128, 0.1, A, 64, 1, 0, None]
+    assert call(dl, largs, i4=0) == -1                # w_o null
+    assert call(dl, largs, i5=0) == -1                # k_cache null
+    assert call(dl, largs, i16=0) == -2               # cap
+    assert call(dl, largs, i7=A + 2) == -4            # seq_lens misaligned
+    assert call(dl, largs, i17=0) == -5
