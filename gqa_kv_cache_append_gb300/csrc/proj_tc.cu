@@ -41,6 +41,7 @@ namespace {
 constexpr int kM = 128;                  // output features per tile
 constexpr int kKc = 128;                 // reduction depth per chunk
 constexpr int kBox = 128 * 64 * 2;       // one [128 rows x 64 cols] bf16 box
+constexpr int kPrefetchChunks = 8;       // weight chunks sent to L2 ahead of the ring
 
 template <int NB>
 struct PCfg {
@@ -160,6 +161,22 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(dst, wm, FULL(st), 0, row, pol_stream);
         tma_load_2d(dst + kBox, wm, FULL(st), 64, row, pol_stream);
         if (!waited && n + 1 >= C::STAGES) {
+          // before waiting, have L2 fetch the weights of the next chunks as
+          // well, so HBM stays busy while the kernel ahead finishes
+          for (long long pf = p + 1; pf < pos1 && pf <= p + kPrefetchChunks; ++pf) {
+            const int tf = static_cast<int>(pf / chunks), cf = static_cast<int>(pf % chunks);
+            const CUtensorMap* wf = &tm_w0;
+            int rf;
+            if (MODE == 0) {
+              const QkvHead hd = qkv_head(tf, h, g);
+              wf = hd.which == 0 ? &tm_w0 : (hd.which == 1 ? &tm_w1 : &tm_w2);
+              rf = hd.head * D + cf * kKc;
+            } else {
+              rf = cf * D + tf * kM;
+            }
+            tma_prefetch_l2_2d(wf, 0, rf);
+            tma_prefetch_l2_2d(wf, 64, rf);
+          }
           // the activations of the stages issued so far, after the wait
           pdl_wait();
           waited = true;
@@ -310,25 +327,33 @@ __global__ void __launch_bounds__(192, 1)
         unit_ctas(tile0, tile1, W, nc, c0, c1);
         const int np = static_cast<int>(c1 - c0 + 1);
         if (arrive_last(counters, t, np, last_flag, row == 0, 1, 128)) {
-          // every piece, this CTA's included, summed in CTA order; one
-          // piece's columns (up to 64) are loaded at once
+          // every piece, this CTA's included, summed in CTA order; the
+          // loads of PB pieces x HC columns (16 or 32 float4) go out together
           constexpr int HC = NB < 64 ? NB : 64;
+          constexpr int PB = HC >= 64 ? 1 : 128 / HC;
           for (int c_lo = 0; c_lo < NB && c_lo < b; c_lo += HC) {
             float acc[HC];
 #pragma unroll
             for (int e = 0; e < HC; ++e) acc[e] = 0.f;
-            for (long long c = c0; c <= c1; ++c) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  part + ((static_cast<size_t>(t) + c) * kM + row) * NB + c_lo);
-              float4 w4[HC / 4];
+            for (long long cb = c0; cb <= c1; cb += PB) {
+              float4 w4[PB][HC / 4];
 #pragma unroll
-              for (int e = 0; e < HC / 4; ++e) w4[e] = __ldcg(src + e);
+              for (int k = 0; k < PB; ++k) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    part + ((static_cast<size_t>(t) + cb + k) * kM + row) * NB + c_lo);
 #pragma unroll
-              for (int e = 0; e < HC / 4; ++e) {
-                acc[4 * e] += w4[e].x;
-                acc[4 * e + 1] += w4[e].y;
-                acc[4 * e + 2] += w4[e].z;
-                acc[4 * e + 3] += w4[e].w;
+                for (int e = 0; e < HC / 4; ++e)
+                  w4[k][e] = (cb + k <= c1) ? __ldcg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int k = 0; k < PB; ++k) {
+#pragma unroll
+                for (int e = 0; e < HC / 4; ++e) {
+                  acc[4 * e] += w4[k][e].x;
+                  acc[4 * e + 1] += w4[k][e].y;
+                  acc[4 * e + 2] += w4[k][e].z;
+                  acc[4 * e + 3] += w4[k][e].w;
+                }
               }
             }
 #pragma unroll
