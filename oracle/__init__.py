@@ -22,4 +22,8 @@ from .oracle import (  # noqa: F401
     project_qkv,
     project_out,
     decode_layer,
+    paged_rows,
+    gather_paged,
+    kv_append_paged,
+    decode_step_paged,
 )

@@ -62,6 +62,10 @@ __all__ = [
     "project_qkv",
     "project_out",
     "decode_layer",
+    "paged_rows",
+    "gather_paged",
+    "kv_append_paged",
+    "decode_step_paged",
 ]
 
 
@@ -330,6 +334,79 @@ def decode_layer(x, P_q, P_k, P_v, P_o, k_cache, v_cache, seq_lens, g: int,
     o_s = to_storage(o, dtype)
     y = project_out(o_s, P_o, dtype)
     return y, kc, vc, q_s, o_s
+
+
+# ---------------------------------------------------------------------------
+# paged KV cache ([Decode notes] memory section: serving engines keep the KV
+# cache in GPU memory, the vLLM PagedAttention paper it cites; the block
+# table is that paper's mapping): the cache of every layer is a pool of
+# fixed-size blocks, pool [num_blocks, g, B, d]; logical position p of
+# sequence i lives in row p mod B of block block_table[i, p div B].
+# ---------------------------------------------------------------------------
+def paged_rows(block_table, seq_len_i: int, i: int, block_size: int) -> np.ndarray:
+    """Physical (block, row-in-block) of the positions 0 .. L_i - 1 of
+    sequence i, as an int array [L_i, 2]."""
+    p = np.arange(int(seq_len_i))
+    blocks = np.asarray(block_table)[i, p // block_size]
+    return np.stack([blocks, p % block_size], axis=1)
+
+
+def _check_paged(pool, block_table, seq_lens, block_size):
+    nb, g, bs, _ = np.asarray(pool).shape
+    if bs != block_size:
+        raise ValueError("pool rows per block differ from block_size")
+    bt = np.asarray(block_table)
+    b, max_blocks = bt.shape
+    lens = _check_lens(seq_lens, b, max_blocks * block_size)
+    for i in range(b):
+        used = bt[i, : (int(lens[i]) + block_size - 1) // block_size]
+        if np.any(used < 0) or np.any(used >= nb):
+            raise ValueError("block table entry outside the pool")
+    return lens
+
+
+def gather_paged(pool, block_table, seq_lens, block_size: int):
+    """The contiguous cache [b, g, max_blocks * B, d] that the pool and the
+    table describe; rows at or beyond L_i are zero."""
+    pool = np.asarray(pool)
+    lens = _check_paged(pool, block_table, seq_lens, block_size)
+    b, max_blocks = np.asarray(block_table).shape
+    nb, g, bs, d = pool.shape
+    out = np.zeros((b, g, max_blocks * block_size, d), dtype=pool.dtype)
+    for i in range(b):
+        rows = paged_rows(block_table, lens[i], i, block_size)
+        for p, (blk, r) in enumerate(rows):
+            out[i, :, p, :] = pool[blk, :, r, :]
+    return out
+
+
+def kv_append_paged(k_pool, v_pool, k_new, v_new, block_table, seq_lens, block_size: int):
+    """Write the new token's rows at position L_i - 1 of every (i, j): row
+    (L_i - 1) mod B of block block_table[i, (L_i - 1) div B].  Bit-exact;
+    every other pool row is left as it was."""
+    kp = np.array(k_pool, copy=True)
+    vp = np.array(v_pool, copy=True)
+    lens = _check_paged(kp, block_table, seq_lens, block_size)
+    bt = np.asarray(block_table)
+    for i in range(bt.shape[0]):
+        p = int(lens[i]) - 1
+        blk, r = bt[i, p // block_size], p % block_size
+        for j in range(kp.shape[1]):
+            kp[blk, j, r, :] = k_new[i, j, :]
+            vp[blk, j, r, :] = v_new[i, j, :]
+    return kp, vp
+
+
+def decode_step_paged(q, k_pool, v_pool, k_new, v_new, block_table, seq_lens, g: int,
+                      scale: float, block_size: int, dtype: str = "f64"):
+    """One decode step on a paged cache: append, then attend over the
+    positions the table maps (the same arithmetic as decode_step on the
+    gathered cache).  Returns (o, k_pool', v_pool')."""
+    kp, vp = kv_append_paged(k_pool, v_pool, k_new, v_new, block_table, seq_lens, block_size)
+    kc = gather_paged(kp, block_table, seq_lens, block_size)
+    vc = gather_paged(vp, block_table, seq_lens, block_size)
+    o = grouped_decode_attention(q, kc, vc, seq_lens, g, scale, dtype)
+    return o, kp, vp
 
 
 # ---------------------------------------------------------------------------

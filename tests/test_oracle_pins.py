@@ -516,3 +516,62 @@ def test_multi_token_rejects_lengths_below_n():
     kn = np.zeros((1, 3, 1, 2))
     with pytest.raises(ValueError):
         oracle.kv_append_multi(kc, kc, kn, kn, [2])
+
+
+# --------------------------------------------------------------------------
+# paged KV cache: the block table is a relabelling of the contiguous cache
+# --------------------------------------------------------------------------
+def _paged_case(rng, b, g, d, bs, max_blocks, lens, spare=3):
+    """A contiguous cache and the same data scattered over a shuffled pool."""
+    nb = b * max_blocks + spare
+    perm = rng.permutation(nb)
+    table = perm[: b * max_blocks].reshape(b, max_blocks)
+    kc = rng.standard_normal((b, g, max_blocks * bs, d))
+    vc = rng.standard_normal((b, g, max_blocks * bs, d))
+    kp = rng.standard_normal((nb, g, bs, d))        # unrelated data everywhere else
+    vp = rng.standard_normal((nb, g, bs, d))
+    for i in range(b):
+        for m in range(max_blocks):
+            kp[table[i, m]] = kc[i, :, m * bs:(m + 1) * bs]
+            vp[table[i, m]] = vc[i, :, m * bs:(m + 1) * bs]
+    return table, kc, vc, kp, vp
+
+
+@pytest.mark.parametrize("bs,max_blocks,lens", [(4, 3, [1, 12, 5]), (2, 5, [10, 2, 7]),
+                                                (8, 1, [8, 3, 1])])
+def test_paged_step_equals_the_contiguous_step(bs, max_blocks, lens):
+    rng = np.random.default_rng(900 + bs)
+    b, h, g, d = 3, 4, 2, 5
+    table, kc, vc, kp, vp = _paged_case(rng, b, g, d, bs, max_blocks, lens)
+    q = rng.standard_normal((b, h, d))
+    kn = rng.standard_normal((b, g, d))
+    vn = rng.standard_normal((b, g, d))
+    o1, kp2, vp2 = oracle.decode_step_paged(q, kp, vp, kn, vn, table, lens, g, 0.6, bs)
+    o2, kc2, vc2 = oracle.decode_step(q, kc, vc, kn, vn, lens, g, 0.6)
+    assert np.max(np.abs(o1 - o2)) < TOL
+    # exactly one row changed per (i, j): the block and row the table names
+    changed = np.argwhere(np.any(kp2 != kp, axis=-1))
+    want = {(table[i, (L - 1) // bs], j, (L - 1) % bs) for i, L in enumerate(lens)
+            for j in range(g)}
+    assert {tuple(c) for c in changed} == want
+    for i, L in enumerate(lens):
+        blk, r = table[i, (L - 1) // bs], (L - 1) % bs
+        assert np.array_equal(kp2[blk, :, r], kn[i]) and np.array_equal(vp2[blk, :, r], vn[i])
+    assert np.array_equal(oracle.gather_paged(kp2, table, lens, bs)[:, :, :max(lens)],
+                          np.where(np.arange(max(lens))[None, None, :, None] <
+                                   np.array(lens)[:, None, None, None], kc2[:, :, :max(lens)], 0))
+
+
+def test_paged_rows_bruteforce():
+    table = np.array([[5, 2, 7], [0, 1, 3]])
+    rows = oracle.paged_rows(table, 7, 0, 3)
+    assert rows.tolist() == [[5, 0], [5, 1], [5, 2], [2, 0], [2, 1], [2, 2], [7, 0]]
+    assert oracle.paged_rows(table, 1, 1, 3).tolist() == [[0, 0]]
+
+
+def test_paged_rejects_bad_tables():
+    kp = np.zeros((4, 1, 2, 3))
+    with pytest.raises(ValueError):
+        oracle.gather_paged(kp, np.array([[0, 9]]), [3], 2)      # block 9 outside the pool
+    with pytest.raises(ValueError):
+        oracle.gather_paged(kp, np.array([[0, 1]]), [5], 2)      # length beyond the table
