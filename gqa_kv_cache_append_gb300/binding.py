@@ -33,6 +33,7 @@ GQA_STEP_EARLY_STREAM = 1
 GQA_DEV_BAD_SEQ_LEN = 1
 GQA_DEV_WAIT_TIMEOUT = 2
 GQA_DEV_INTERNAL = 4
+GQA_DEV_BAD_BLOCK = 8
 
 # every function the header declares, with its C signature
 _VP, _I, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
@@ -53,6 +54,12 @@ SIGNATURES = {
     "gqa_project_out": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
     "gqa_decode_layer": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
                               _F, _VP, _I, _I, _I, _VP]),
+    "gqa_kv_append_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I,
+                                 _VP]),
+    "gqa_decode_attn_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I,
+                                   _I, _I, _VP]),
+    "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F,
+                                   _VP, _I, _I, _I, _I, _I, _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -228,6 +235,37 @@ def gqa_decode_layer(x, w_q, w_k, w_v, w_o, k_cache, v_cache, seq_lens, b, d_mod
         _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(w_o), _ptr(k_cache), _ptr(v_cache),
         _ptr(seq_lens), int(b), int(d_model), int(h), int(g), int(d_k), int(d_v),
         float(scale), _ptr(y), int(cap), _dtype(x, dtype), int(flags), _stream(stream)))
+
+
+def gqa_kv_append_paged(k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, g, d_k, d_v,
+                        block_size=None, dtype=None, stream=None) -> None:
+    """Append into a paged cache (pools [num_blocks, g, block_size, d])."""
+    nb, _, bs, _ = k_pool.shape
+    _check("gqa_kv_append_paged", lib.gqa_kv_append_paged(
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+        int(b), int(g), int(d_k), int(d_v), int(block_size or bs), int(block_table.shape[1]),
+        int(nb), _dtype(k_pool, dtype), _stream(stream)))
+
+
+def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k, d_v, scale,
+                          out, dtype=None, stream=None) -> None:
+    """gqa_decode_attn over a paged cache."""
+    nb, _, bs, _ = k_pool.shape
+    _check("gqa_decode_attn_paged", lib.gqa_decode_attn_paged(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens), int(b), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(bs),
+        int(block_table.shape[1]), int(nb), _dtype(q, dtype), _stream(stream)))
+
+
+def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k,
+                          d_v, scale, out, dtype=None, flags=0, stream=None) -> None:
+    """Append and attend over a paged cache in one launch."""
+    nb, _, bs, _ = k_pool.shape
+    _check("gqa_decode_step_paged", lib.gqa_decode_step_paged(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+        _ptr(seq_lens), int(b), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out),
+        int(bs), int(block_table.shape[1]), int(nb), _dtype(q, dtype), int(flags),
+        _stream(stream)))
 
 
 def gqa_device_status(stream=None) -> int:

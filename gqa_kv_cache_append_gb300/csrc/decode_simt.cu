@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int* __restrict__ counters, const uint4* __restrict__ k_new,
                        const uint4* __restrict__ v_new, uint4* __restrict__ k_cache_w,
                        uint4* __restrict__ v_cache_w, unsigned int* status, long long budget,
-                       int nq) {
+                       int nq, const int* __restrict__ table, int bsz, int max_blocks,
+                       int num_blocks) {
   using C = SimtCfg<DT, D, RMAX>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -138,7 +139,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- producer ----------------
-    if (lane == 0) {
+    if (table != nullptr) {
+      // paged cache: the whole warp walks the tiles (block-table lookups
+      // over its lanes), lane 0 issues one copy per block piece of a tile;
+      // pieces in bad blocks are not copied (the status word says so)
+      uint32_t n = 0;
+      int last_n[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) last_n[s] = -1;
+      const int piece = bsz < C::T ? bsz : C::T;
+      PageCursor pc;
+      while (w.next(seg)) {
+        pc.start(table + static_cast<size_t>(seg.i) * max_blocks, (seg.L + bsz - 1) / bsz,
+                 (seg.lt0 * C::T) / bsz);
+        for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          const int st = n % C::STAGES;
+          const bool ok = __all_sync(0xffffffffu,
+                                     mbar_wait(empty0 + 8 * st, ((n / C::STAGES) & 1) ^ 1,
+                                               abort_flag, status, budget));
+          if (!ok) continue;
+          const int p0 = lt * C::T;
+          int blk[C::T / 16];
+          uint32_t total = 0;
+          bool bad = false;
+          for (int mm = 0; mm * piece < C::T; ++mm) {
+            const int p = p0 + mm * piece;
+            blk[mm] = -1;
+            if (p < seg.L) {
+              const int e = pc.get(p / bsz);
+              if (e >= 0 && e < num_blocks) {
+                blk[mm] = e;
+                total += 2u * min(piece, seg.L - p) * D * C::ELT;
+              } else {
+                bad = true;
+              }
+            }
+          }
+          if (lane == 0) {
+            if (bad) atomicOr(status, GQA_DEV_BAD_BLOCK);
+            uint8_t* stage = sm + st * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(full0 + 8 * st, total);
+            for (int mm = 0; mm * piece < C::T; ++mm) {
+              const int p = p0 + mm * piece;
+              if (blk[mm] < 0) continue;
+              const uint32_t bytes = static_cast<uint32_t>(min(piece, seg.L - p)) * D * C::ELT;
+              const size_t prow = (static_cast<size_t>(blk[mm]) * g + seg.j) * bsz + p % bsz;
+              const uint32_t o = mm * piece * D * C::ELT;
+              bulk_load(smem_u32(stage + o), kc + prow * D, bytes, full0 + 8 * st);
+              bulk_load(smem_u32(stage + C::T * D * C::ELT + o), vc + prow * D, bytes,
+                        full0 + 8 * st);
+            }
+          }
+          last_n[st] = static_cast<int>(n);
+        }
+      }
+      if (*abort_flag && lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (last_n[s] < 0) continue;
+          const uint32_t par = (last_n[s] / C::STAGES) & 1;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(full0 + 8 * s, par) && clock64() - t0 < budget) {
+          }
+        }
+      }
+    } else if (lane == 0) {
       uint32_t n = 0;
       int last_n[C::STAGES];
 #pragma unroll
@@ -241,9 +305,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int rho = pos - lt * C::T;
               reinterpret_cast<uint4*>(const_cast<DT*>(sK) + rho * D)[c16] = kv;
               reinterpret_cast<uint4*>(const_cast<DT*>(sV) + rho * D)[c16] = vv;
-              const size_t crow = unit * cap + pos;
-              k_cache_w[crow * C::CH + c16] = kv;
-              v_cache_w[crow * C::CH + c16] = vv;
+              long long crow = static_cast<long long>(unit) * cap + pos;
+              if (table != nullptr) {
+                const int e = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + pos / bsz);
+                crow = (e >= 0 && e < num_blocks)
+                           ? (static_cast<long long>(e) * g + seg.j) * bsz + pos % bsz
+                           : -1;
+              }
+              if (crow >= 0) {
+                k_cache_w[crow * C::CH + c16] = kv;
+                v_cache_w[crow * C::CH + c16] = vv;
+              }
             }
           }
           named_bar_sync(1, 128);
@@ -444,7 +516,7 @@ cudaError_t launch_t(const DecodeLaunch& a) {
       static_cast<DT*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
-      a.nq);
+      a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks);
 }
 
 }  // namespace

@@ -60,7 +60,7 @@ constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
 // because the 32-column variant runs at its register limit.
-template <int NP, int NWG, bool MULTI>
+template <int NP, int NWG, bool MULTI, bool PAGED = false>
 struct TcCfg {
   static constexpr int THREADS = 64 + 128 * NWG;  // producer, MMA, NWG softmax warpgroups
   static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
@@ -91,6 +91,7 @@ struct TcCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
   static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
+  static_assert(!(MULTI && PAGED), "the paged cache takes one new token per step");
 };
 
 // barrier slots
@@ -108,7 +109,7 @@ enum {
   B_DRAIN = B_O_FREE + 2,
 };
 
-template <int NP, int NWG, bool MULTI>
+template <int NP, int NWG, bool MULTI, bool PAGED>
 __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -118,8 +119,9 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                      float* __restrict__ part_ml, int* __restrict__ counters,
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
-                     unsigned int* status, long long budget, int early, int nq) {
-  using C = TcCfg<NP, NWG, MULTI>;
+                     unsigned int* status, long long budget, int early, int nq,
+                     const int* __restrict__ table, int bsz, int max_blocks, int num_blocks) {
+  using C = TcCfg<NP, NWG, MULTI, PAGED>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   const uint32_t s_base = smem_u32(sm);
@@ -184,7 +186,114 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
   w.init(lens, b, g, nq, cap, kT, blockIdx.x, gridDim.x);
   Segment seg;
 
-  if (warp == 0) {
+  if (warp == 0 && PAGED) {
+    // ===================== TMA producer, paged cache =====================
+    // The whole warp walks the tiles (block-table lookups are spread over
+    // its lanes); lane 0 issues the copies.  A tile of 128 positions is one
+    // box per 64-column half when blocks hold 128 rows or more, else one box
+    // per block.  Blocks past L_i, and bad entries, are read out of range
+    // (zero fill).
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const int oob_row = num_blocks * g * bsz;
+    const int sub = bsz < kT ? kT / bsz : 1;      // boxes per half-tile
+    const int box_rows = bsz < kT ? bsz : kT;
+    uint32_t n = 0, k = 0;
+    int last_n[kStages] = {-1, -1, -1};
+    int last_q[2] = {-1, -1};
+    auto load_q = [&](uint32_t kk, const Segment& sg) {
+      const uint32_t qs = kk & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_Q_EMPTY + qs), ((kk >> 1) & 1) ^ 1,
+                                                        abort_flag, status, budget));
+      if (ok && lane == 0) {
+        const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
+        mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 256);
+        tma_load_3d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, sg.j * r, sg.i * nq, pol_keep);
+        tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
+                    pol_keep);
+      }
+      if (ok) last_q[qs] = static_cast<int>(kk);
+    };
+    bool waited = !early;
+    PageCursor pc;
+    while (w.next(seg)) {
+      if (waited) load_q(k, seg);
+      pc.start(table + static_cast<size_t>(seg.i) * max_blocks, (seg.L + bsz - 1) / bsz,
+               (seg.lt0 * kT) / bsz);
+      for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+        if (!waited && (lt - seg.lt0 == kStages)) {
+          pdl_wait();
+          waited = true;
+          load_q(k, seg);
+        }
+        const int st = n % kStages;
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait(BAR(B_EMPTY + st), ((n / kStages) & 1) ^ 1,
+                                             abort_flag, status, budget));
+        if (!ok) continue;
+        const uint32_t dst = s_base + st * C::KV_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(BAR(B_FULL_K + st), 2 * kBoxBytes);
+          mbar_arrive_expect_tx(BAR(B_FULL_V + st), 2 * kBoxBytes);
+        }
+        bool bad = false;
+        for (int mm = 0; mm < sub; ++mm) {
+          const int p0 = lt * kT + mm * box_rows;
+          int row = oob_row;
+          if (p0 < seg.L) {
+            const int blk = pc.get(p0 / bsz);
+            if (blk >= 0 && blk < num_blocks)
+              row = (blk * g + seg.j) * bsz + p0 % bsz;
+            else
+              bad = true;
+          }
+          if (lane == 0) {
+            const uint32_t o = mm * box_rows * 128;
+            tma_load_2d(dst + o, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
+            tma_load_2d(dst + kBoxBytes + o, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
+            tma_load_2d(dst + 2 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
+            tma_load_2d(dst + 3 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 64, row,
+                        pol_stream);
+          }
+        }
+        if (bad && lane == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
+        last_n[st] = static_cast<int>(n);
+      }
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+        load_q(k, seg);
+      }
+      ++k;
+    }
+    if (!waited) pdl_wait();
+    if (*abort_flag && lane == 0) {
+      for (int s = 0; s < kStages + 2; ++s) {
+        int idx;
+        uint32_t b0, b1 = 0;
+        bool two = false;
+        if (s < kStages) {
+          idx = last_n[s];
+          if (idx < 0) continue;
+          b0 = BAR(B_FULL_K + s);
+          b1 = BAR(B_FULL_V + s);
+          two = true;
+          idx /= kStages;
+        } else {
+          idx = last_q[s - kStages];
+          if (idx < 0) continue;
+          b0 = BAR(B_Q_FULL + s - kStages);
+          idx >>= 1;
+        }
+        const long long t0 = clock64();
+        while (!mbar_try_wait(b0, idx & 1) && clock64() - t0 < budget) {
+        }
+        while (two && !mbar_try_wait(b1, idx & 1) && clock64() - t0 < budget) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // =========================== TMA producer ===========================
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
@@ -322,6 +431,16 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         return ((static_cast<size_t>(seg.i) * nq + s_lo + (idx >> 4)) * g + seg.j) * 16 +
                (idx & 15);
       };
+      // paged cache (one token): the physical row of position L_i - 1, or -1
+      // for a bad table entry (then nothing is written)
+      long long prow = -1;
+      if (PAGED && nchunk > 0) {
+        const int blk = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + (seg.L - 1) / bsz);
+        if (blk >= 0 && blk < num_blocks)
+          prow = (static_cast<long long>(blk) * g + seg.j) * bsz + (seg.L - 1) % bsz;
+        else if (lane == 0)
+          atomicOr(status, GQA_DEV_BAD_BLOCK);
+      }
       // (one token: the softmax warps carry and patch the V row)
       constexpr int VCH = MULTI ? C::KCH : 1;
       uint4 knew[C::KCH], vnew[VCH];
@@ -346,7 +465,10 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
-        cache[(unit * cap + pos) * 16 + ch] = v;
+        if (!PAGED)
+          cache[(unit * cap + pos) * 16 + ch] = v;
+        else if (prow >= 0)
+          cache[prow * 16 + ch] = v;
       };
       // patch the new rows that fall in tile lt (K or V half of the stage)
       auto patch = [&](uint32_t tile_base, uint4* cache, const uint4* src, const uint4* regs,
@@ -488,8 +610,18 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       // 16-byte chunk each) to the unit's last tile
       const bool append_v = !MULTI && v_new != nullptr && seg.lt1 == seg.ti;
       uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
-      if (append_v && wg == 0 && row < 16)
+      long long vrow_w = -1;  // cache row written by the append
+      if (append_v && wg == 0 && row < 16) {
         vnew = __ldg(v_new + (static_cast<size_t>(seg.i) * g + seg.j) * 16 + row);
+        if (!PAGED) {
+          vrow_w = (static_cast<long long>(seg.i) * g + seg.j) * cap + seg.L - 1;
+        } else {
+          const int blk =
+              __ldg(table + static_cast<size_t>(seg.i) * max_blocks + (seg.L - 1) / bsz);
+          if (blk >= 0 && blk < num_blocks)
+            vrow_w = (static_cast<long long>(blk) * g + seg.j) * bsz + (seg.L - 1) % bsz;
+        }
+      }
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         const uint32_t nb = n & 1;
         const int st = n % kStages;
@@ -613,8 +745,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(vnew.x),
                          "r"(vnew.y), "r"(vnew.z), "r"(vnew.w)
                          : "memory");
-            v_cache_w[((static_cast<size_t>(seg.i) * g + seg.j) * cap + seg.L - 1) * 16 + row] =
-                vnew;
+            if (vrow_w >= 0) v_cache_w[vrow_w * 16 + row] = vnew;
           }
           if (vok && !live) {
             const uint32_t vrow = vbase + row * 128;
@@ -765,15 +896,18 @@ bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r)
   return encode_bf16_map(map, base, 3, dims, strides, box);
 }
 
-template <int NP, int NWG, bool MULTI>
+template <int NP, int NWG, bool MULTI, bool PAGED>
 cudaError_t launch_np(const DecodeLaunch& a) {
-  using C = TcCfg<NP, NWG, MULTI>;
+  using C = TcCfg<NP, NWG, MULTI, PAGED>;
   CUtensorMap mq, mk, mv;
+  // contiguous caches: [b * g * cap rows x 128]; pools: [num_blocks * g * block_size rows]
+  const uint64_t kv_rows = PAGED ? static_cast<uint64_t>(a.num_blocks) * a.g * a.block_size
+                                 : static_cast<uint64_t>(a.b) * a.g * a.cap;
+  const uint32_t box_rows = (PAGED && a.block_size < kT) ? a.block_size : kT;
   if (!make_q_map(&mq, a.q, a.b, a.nq, a.h, a.h / a.g) ||
-      !make_map(&mk, a.k_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT) ||
-      !make_map(&mv, a.v_cache, static_cast<uint64_t>(a.b) * a.g * a.cap, kT))
+      !make_map(&mk, a.k_cache, kv_rows, box_rows) || !make_map(&mv, a.v_cache, kv_rows, box_rows))
     return cudaErrorInvalidValue;
-  auto kern = decode_tc_kernel<NP, NWG, MULTI>;
+  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED>;
   // the shared-memory opt-in is set once per device (not during a capture)
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -799,7 +933,7 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
-      a.early ? 1 : 0, a.nq);
+      a.early ? 1 : 0, a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks);
 }
 
 }  // namespace
@@ -814,8 +948,13 @@ int tc_ctas_per_sm(int) { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeLaunch& a) {
   const int cols = a.nq * (a.h / a.g);
-  if (a.nq == 1) return cols <= 16 ? launch_np<16, 1, false>(a) : launch_np<32, 2, false>(a);
-  return cols <= 16 ? launch_np<16, 1, true>(a) : launch_np<32, 2, true>(a);
+  if (a.block_table != nullptr) {
+    if (a.nq != 1) return cudaErrorInvalidValue;  // (the ABI rejects it first)
+    return cols <= 16 ? launch_np<16, 1, false, true>(a) : launch_np<32, 2, false, true>(a);
+  }
+  if (a.nq == 1)
+    return cols <= 16 ? launch_np<16, 1, false, false>(a) : launch_np<32, 2, false, false>(a);
+  return cols <= 16 ? launch_np<16, 1, true, false>(a) : launch_np<32, 2, true, false>(a);
 }
 
 }  // namespace gqa

@@ -58,6 +58,41 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
   }
 }
 
+// The same for a paged cache: position L_i - 1 lives in row (L_i - 1) % B of
+// block block_table[i, (L_i - 1) / B] of the pools [num_blocks, g, B, d].
+__global__ void kv_append_paged_kernel(const uint4* __restrict__ k_new,
+                                       const uint4* __restrict__ v_new, uint4* __restrict__ k_pool,
+                                       uint4* __restrict__ v_pool, const int* __restrict__ table,
+                                       const int* __restrict__ lens, int b, int g, int ck, int cv,
+                                       int bsz, int max_blocks, int num_blocks,
+                                       unsigned int* status) {
+  const long long per = ck + cv;
+  const long long total = static_cast<long long>(b) * g * per;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const long long row = idx / per;  // (i, j) row of k_new / v_new
+  const int c = static_cast<int>(idx % per);
+  const int j = static_cast<int>(row % g);
+  const int i = static_cast<int>(row / g);
+  const int L = __ldg(lens + i);
+  if (L < 1 || L > static_cast<long long>(max_blocks) * bsz) {
+    if (c == 0) atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int blk = __ldg(table + static_cast<size_t>(i) * max_blocks + (L - 1) / bsz);
+  if (blk < 0 || blk >= num_blocks) {
+    if (c == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
+    return;
+  }
+  const long long dst_row = (static_cast<long long>(blk) * g + j) * bsz + (L - 1) % bsz;
+  if (c < ck) {
+    k_pool[dst_row * ck + c] = __ldg(k_new + row * ck + c);
+  } else {
+    const int cc = c - ck;
+    v_pool[dst_row * cv + cc] = __ldg(v_new + row * cv + cc);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Log-sum-exp combine for launches with many more CTAs than units (a few
 // long sequences, e.g. one MQA head over 131k positions spread over 19
@@ -310,6 +345,23 @@ int launch_all(DecodeLaunch& a, int tile) {
 
 int elt_bytes(int dtype) { return dtype == GQA_F32 ? 4 : 2; }
 
+// Host checks of the paged-cache arguments (a decode_check follows).
+int paged_check(const int32_t* block_table, int g, int block_size, int max_blocks,
+                int num_blocks, int nq) {
+  if (!block_table) return GQA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(block_table) & 3u) return GQA_ERR_ALIGN;
+  if (block_size < 1 || max_blocks < 1 || num_blocks < 1 || g < 1) return GQA_ERR_SHAPE;
+  if (static_cast<long long>(max_blocks) * block_size > 0x7FFFFF00ll ||
+      static_cast<long long>(num_blocks) * g * block_size > 0x7FFFFF00ll)
+    return GQA_ERR_SHAPE;
+  // powers of two from 16: a block is a whole number of tiles or a tile a
+  // whole number of blocks
+  if (block_size < 16 || (block_size & (block_size - 1)) != 0 || block_size > 65536)
+    return GQA_ERR_UNSUPPORTED;
+  if (nq != 1) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave,
@@ -405,6 +457,34 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_c
                              dtype, stream);
 }
 
+int gqa_kv_append_paged(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                        const int32_t* block_table, const int32_t* seq_lens, int b, int g,
+                        int d_k, int d_v, int block_size, int max_blocks, int num_blocks,
+                        int dtype, void* stream) {
+  if (!k_new || !v_new || !k_pool || !v_pool || !seq_lens) return GQA_ERR_NULL;
+  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (b < 1 || d_k < 1 || d_v < 1) return GQA_ERR_SHAPE;
+  if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks, 1)) return e;
+  const int elt = elt_bytes(dtype);
+  if ((d_k * elt) % 16 != 0 || (d_v * elt) % 16 != 0) return GQA_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return GQA_ERR_ALIGN;
+  DeviceInfo* di = nullptr;
+  if (int e = device_info(&di)) return e;
+  const int ck = d_k * elt / 16, cv = d_v * elt / 16;
+  const long long total = static_cast<long long>(b) * g * (ck + cv);
+  const int threads = 256;
+  const long long blocks = (total + threads - 1) / threads;
+  if (blocks > 0x7FFFFFFFll) return GQA_ERR_SHAPE;
+  kv_append_paged_kernel<<<static_cast<unsigned>(blocks), threads, 0,
+                           static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, seq_lens, b, g, ck,
+      cv, block_size, max_blocks, num_blocks, di->status);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace gqa {
@@ -415,13 +495,15 @@ struct DecodeArgs {
   const void* q;
   const void* k_new;     // null: attention only
   const void* v_new;
-  const void* k_cache;
+  const void* k_cache;   // contiguous caches, or the pools of a paged cache
   const void* v_cache;
   const int32_t* seq_lens;
   int b, nq, h, g, d_k, d_v;
   float scale;
   void* out;
-  int cap, dtype, flags;
+  int cap, dtype, flags;  // cap: rows per (sequence, KV head); paged: max_blocks * block_size
+  const int32_t* block_table = nullptr;  // paged cache
+  int block_size = 0, max_blocks = 0, num_blocks = 0;
 };
 
 struct DecodePlan {
@@ -440,9 +522,9 @@ int decode_check(const DecodeArgs& x) {
   if (x.b < 1 || x.nq < 1 || x.h < 1 || x.g < 1 || x.d_k < 1 || x.d_v < 1 || x.cap < 1 ||
       x.h % x.g != 0 || x.nq > x.cap)
     return GQA_ERR_SHAPE;
-  if (static_cast<long long>(x.b) * x.g * x.cap + 256 > 0x7FFFFFFFll ||
-      static_cast<long long>(x.b) * x.nq * x.h > 0x7FFFFFFFll)
+  if (x.block_table == nullptr && static_cast<long long>(x.b) * x.g * x.cap + 256 > 0x7FFFFFFFll)
     return GQA_ERR_SHAPE;
+  if (static_cast<long long>(x.b) * x.nq * x.h > 0x7FFFFFFFll) return GQA_ERR_SHAPE;
   if (!aligned16(x.q) || !aligned16(x.k_cache) || !aligned16(x.v_cache) || !aligned16(x.out) ||
       !aligned16(x.k_new) || !aligned16(x.v_new) ||
       (reinterpret_cast<uintptr_t>(x.seq_lens) & 3u))
@@ -503,8 +585,14 @@ int decode_run(const DecodeArgs& x, const DecodePlan& p, const DeviceInfo* di, v
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(p.nc);
   a.stream = st;
+  a.block_table = x.block_table;
+  a.block_size = x.block_size;
+  a.max_blocks = x.max_blocks;
+  a.num_blocks = x.num_blocks;
   return launch_all(a, p.tile);
 }
+
+
 
 // gqa_decode_attn and gqa_decode_step (and their n-token forms): checks,
 // kernel choice, workspace, launch.
@@ -559,6 +647,48 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new, v
   if (!k_new || !v_new) return GQA_ERR_NULL;
   return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v, scale,
                      out, cap, dtype, stream, flags);
+}
+
+static int decode_paged(const void* q, const void* k_new, const void* v_new, const void* k_pool,
+                        const void* v_pool, const int32_t* block_table, const int32_t* seq_lens,
+                        int b, int h, int g, int d_k, int d_v, float scale, void* out,
+                        int block_size, int max_blocks, int num_blocks, int dtype, int flags,
+                        void* stream) {
+  using namespace gqa;
+  if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks, 1)) return e;
+  DecodeArgs x{q, k_new, v_new, k_pool, v_pool, seq_lens, b, 1, h, g, d_k, d_v, scale, out,
+               max_blocks * block_size, dtype, flags};
+  x.block_table = block_table;
+  x.block_size = block_size;
+  x.max_blocks = max_blocks;
+  x.num_blocks = num_blocks;
+  if (int e = decode_check(x)) return e;
+  DeviceInfo* di = nullptr;
+  if (int e = device_info(&di)) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const DecodePlan p = decode_plan(x, di->num_sms);
+  void* ws = nullptr;
+  int* counters = nullptr;
+  if (int e = workspace(st, p.o_bytes + p.ml_bytes, p.units, &ws, &counters)) return e;
+  return decode_run(x, p, di, ws, counters, st);
+}
+
+int gqa_decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, const int32_t* seq_lens, int b, int h,
+                          int g, int d_k, int d_v, float scale, void* out, int block_size,
+                          int max_blocks, int num_blocks, int dtype, void* stream) {
+  return decode_paged(q, nullptr, nullptr, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k,
+                      d_v, scale, out, block_size, max_blocks, num_blocks, dtype, 0, stream);
+}
+
+int gqa_decode_step_paged(const void* q, const void* k_new, const void* v_new, void* k_pool,
+                          void* v_pool, const int32_t* block_table, const int32_t* seq_lens,
+                          int b, int h, int g, int d_k, int d_v, float scale, void* out,
+                          int block_size, int max_blocks, int num_blocks, int dtype, int flags,
+                          void* stream) {
+  if (!k_new || !v_new) return GQA_ERR_NULL;
+  return decode_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k, d_v,
+                      scale, out, block_size, max_blocks, num_blocks, dtype, flags, stream);
 }
 
 int gqa_device_status(void* stream, uint32_t* bits_out) {

@@ -341,6 +341,39 @@ __device__ __forceinline__ void report_bad_lengths(const int* lens, int b, int l
     atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
 }
 
+// Block-table lookups of a paged cache for one warp walking a sequence's
+// blocks in increasing order: lane l holds entries base + l and base + 32 + l
+// (the next chunk is loaded while the current one is used).  Entries past
+// the sequence's used blocks read as -1.  Every lane must call get() with the
+// same, non-decreasing block index.
+struct PageCursor {
+  const int* row;  // the sequence's table row
+  int nvalid;      // blocks in use
+  int base;
+  int cur, nxt;
+
+  __device__ int load(int k) const {
+    return k < nvalid ? __ldg(row + k) : -1;
+  }
+  __device__ void start(const int* table_row, int blocks_in_use, int first_block) {
+    const int lane = threadIdx.x & 31;
+    row = table_row;
+    nvalid = blocks_in_use;
+    base = first_block & ~31;
+    cur = load(base + lane);
+    nxt = load(base + 32 + lane);
+  }
+  __device__ int get(int m) {
+    const int lane = threadIdx.x & 31;
+    while (m >= base + 32) {
+      base += 32;
+      cur = nxt;
+      nxt = load(base + 32 + lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, m - base);
+  }
+};
+
 struct Walker {
   const int* lens;
   int b, g, lmin, cap, T;

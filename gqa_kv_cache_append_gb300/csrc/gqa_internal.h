@@ -30,6 +30,11 @@ struct DecodeLaunch {
   long long budget;      // wait limit in SM cycles
   int nc;                // persistent CTAs
   cudaStream_t stream;
+  // paged cache (null table: contiguous [b, g, cap, d]): the caches are pools
+  // [num_blocks, g, block_size, d]; position p of sequence i is row
+  // p % block_size of block block_table[i * max_blocks + p / block_size]
+  const int* block_table = nullptr;
+  int block_size = 0, max_blocks = 0, num_blocks = 0;
 };
 
 // Tiled TMA map over a row-major bf16 tensor: dims[0] is the contiguous

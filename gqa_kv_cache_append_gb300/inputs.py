@@ -47,7 +47,7 @@ import numpy as np
 import torch
 
 __all__ = ["DecodeConfig", "WORKLOADS", "workload", "seq_lens_for",
-           "make_layer", "make_layer_multi", "make_layer_weights", "layer_bytes",
+           "make_layer", "make_layer_multi", "make_layer_weights", "to_paged", "layer_bytes",
            "layer_flops", "projection_bytes"]
 
 
@@ -278,6 +278,34 @@ def make_layer_weights(cfg: DecodeConfig, layer: int = 0, device="cpu") -> dict:
         out[name] = w
     out["x"] = _randn((b, D), gen, device).to(dt)
     return out
+
+
+def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, block_size: int, seed: int,
+             spare: int = 3, fill=None):
+    """Lay a contiguous cache [b, g, cap, d] out as a paged one: pools
+    [num_blocks, g, block_size, d] with num_blocks = b * cap / block_size +
+    spare, and a block table [b, cap / block_size] int32 that maps the blocks
+    of every sequence to a seeded random permutation of the pool
+    (torch.randperm on a CPU generator seeded ``seed``).  Unused blocks hold
+    ``fill`` (default zeros).  A pure relabelling: no arithmetic."""
+    b, g, cap, d = k_cache.shape
+    if cap % block_size:
+        raise ValueError("cap must be a multiple of block_size")
+    mb = cap // block_size
+    nb = b * mb + spare
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    perm = torch.randperm(nb, generator=gen)
+    table = perm[: b * mb].reshape(b, mb).to(torch.int32)
+    pools = []
+    for cache in (k_cache, v_cache):
+        pool = torch.zeros((nb, g, block_size, d), dtype=cache.dtype, device=cache.device)
+        if fill is not None:
+            pool.fill_(fill)
+        blocks = cache.reshape(b, g, mb, block_size, d).permute(0, 2, 1, 3, 4)
+        pool[table.reshape(-1).long().to(cache.device)] = blocks.reshape(b * mb, g, block_size, d)
+        pools.append(pool)
+    return pools[0], pools[1], table.to(k_cache.device)
 
 
 def projection_bytes(cfg: DecodeConfig) -> int:

@@ -82,6 +82,8 @@ extern "C" {
 #define GQA_DEV_WAIT_TIMEOUT 2u /* a bounded in-kernel wait gave up */
 #define GQA_DEV_INTERNAL     4u /* a launch found its shared memory misaligned
                                    and did nothing (not expected to happen) */
+#define GQA_DEV_BAD_BLOCK    8u /* paged cache: a block-table entry in use was
+                                   outside [0, num_blocks) */
 
 /*
  * gqa_kv_append - write the new token's K and V rows into the caches.
@@ -213,6 +215,44 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new,
                           void* k_cache, void* v_cache, const int32_t* seq_lens, int b,
                           int n, int h, int g, int d_k, int d_v, float scale, void* out,
                           int cap, int dtype, int flags, void* stream);
+
+/*
+ * Paged KV cache.  The pages note that serving engines keep the KV cache in
+ * GPU memory (vLLM's PagedAttention, which they cite); there the cache of a
+ * layer is a pool of fixed-size blocks and a block table maps each
+ * sequence's positions to blocks:
+ *   k_pool, v_pool  [num_blocks, g, block_size, d]   (one block holds
+ *                   block_size consecutive positions of every KV head)
+ *   block_table     [b, max_blocks] int32 (device): position p of sequence i
+ *                   is row p % block_size of block block_table[i, p / block_size]
+ * Only the entries of the blocks in use (p < L_i) are read.  seq_lens as
+ * above with cap = max_blocks * block_size.  An entry in use outside
+ * [0, num_blocks) is a device-side error: GQA_DEV_BAD_BLOCK is set, nothing
+ * is written through it, and that sequence's output is unspecified (no
+ * access leaves the pools).  block_size: a power of two in [16, 65536]
+ * (GQA_ERR_UNSUPPORTED otherwise).  One new token per step.  Kernels and
+ * limits otherwise as for the contiguous calls; with GQA_STEP_EARLY_STREAM
+ * the kernels ahead must not write the block table either.
+ *
+ * gqa_kv_append_paged   - the append of gqa_kv_append into the pools.
+ * gqa_decode_attn_paged - the attention of gqa_decode_attn over the pools.
+ * gqa_decode_step_paged - append and attention in one launch.
+ */
+int gqa_kv_append_paged(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                        const int32_t* block_table, const int32_t* seq_lens, int b, int g,
+                        int d_k, int d_v, int block_size, int max_blocks, int num_blocks,
+                        int dtype, void* stream);
+
+int gqa_decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, const int32_t* seq_lens, int b, int h,
+                          int g, int d_k, int d_v, float scale, void* out, int block_size,
+                          int max_blocks, int num_blocks, int dtype, void* stream);
+
+int gqa_decode_step_paged(const void* q, const void* k_new, const void* v_new, void* k_pool,
+                          void* v_pool, const int32_t* block_table, const int32_t* seq_lens,
+                          int b, int h, int g, int d_k, int d_v, float scale, void* out,
+                          int block_size, int max_blocks, int num_blocks, int dtype, int flags,
+                          void* stream);
 
 /*
  * The projections around the step and the whole incremental layer: the
