@@ -244,13 +244,16 @@ def run_ours(args, rank, local_rank, world):
     from gqa_kv_cache_append_gb300 import binding as B
     from gqa_kv_cache_append_gb300.inputs import (make_layer, make_layer_multi,
                                                   make_layer_weights, projection_bytes,
-                                                  seq_lens_for, workload)
+                                                  seq_lens_for, to_paged, workload)
     import dataclasses
 
     n = args.tokens
     full_layer = args.layer
-    if full_layer and n > 1:
-        raise SystemExit("--layer runs one new token per step")
+    paged = args.paged
+    if (full_layer or paged) and n > 1:
+        raise SystemExit("--layer and --paged run one new token per step")
+    if full_layer and paged:
+        raise SystemExit("--layer uses the contiguous cache")
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
@@ -280,6 +283,11 @@ def run_ours(args, rank, local_rank, world):
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
     layers = [make_layer(cfg, l, dev) if n == 1 else make_layer_multi(cfg, n, l, dev)
               for l in range(cfg.layers)]
+    if paged:
+        # the caches become block pools with a shuffled block table
+        for l, x in enumerate(layers):
+            x["k_cache"], x["v_cache"], x["table"] = to_paged(
+                x["k_cache"], x["v_cache"], paged, seed=cfg.seed * 1000 + l)
     if full_layer:
         # the layer's input is x; q / k_new / v_new come from the projections
         for l, x in enumerate(layers):
@@ -313,6 +321,10 @@ def run_ours(args, rank, local_rank, world):
             B.gqa_decode_layer(x["x"], x["P_q"], x["P_k"], x["P_v"], x["P_o"], x["k_cache"],
                                x["v_cache"], x["seq_lens"], cfg.b, cfg.D, cfg.h, cfg.g, cfg.d,
                                cfg.d, cfg.scale, outs[l], flags=early, stream=stream)
+        elif paged:
+            B.gqa_decode_step_paged(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                    x["table"], x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d,
+                                    cfg.scale, outs[l], flags=early, stream=stream)
         elif n > 1:
             if args.separate:
                 B.gqa_kv_append_multi(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
@@ -437,7 +449,7 @@ def run_ours(args, rank, local_rank, world):
     call_bytes = sb["attn_per_layer"] + sb["append_per_layer"] + sb.get("proj_per_layer", 0)
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
-    traffic = None if full_layer else profiled_traffic(src, args.workload, n)
+    traffic = None if (full_layer or paged) else profiled_traffic(src, args.workload, n)
     launches_per_step = (3 if full_layer else (2 if args.separate else 1)) * cfg.layers
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     line = {
@@ -464,6 +476,8 @@ def run_ours(args, rank, local_rank, world):
             "tokens_per_step": n,
             "scope": "whole layer: projections + append + attention" if full_layer
                      else "append + attention",
+            "kv_layout": f"paged, block {paged} rows, shuffled block table" if paged
+                         else "contiguous",
         },
         "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
         "attn_tflops_per_gpu": round(layer_flops(cfg, lens, n) / (attn_avg_ms * 1e-3) / 1e12, 2),
@@ -473,7 +487,8 @@ def run_ours(args, rank, local_rank, world):
             "bound": "hbm",
             "kernel": ("gqa_decode_layer (proj_tc_kernel x2 + " if full_layer else "")
                       + ("gqa_kv_append + gqa_decode_attn" if args.separate else "gqa_decode_step")
-                      + ("_multi" if n > 1 else "") + (")" if full_layer else "")
+                      + ("_multi" if n > 1 else "") + ("_paged" if paged else "")
+                      + (")" if full_layer else "")
                       + f" ({'decode_tc_kernel' if cfg.dtype == 'bf16' and cfg.d == 128 else 'decode_simt_kernel'})",
             "achieved": round(achieved, 2),
             "peak": peaks["hbm_gbs"],
@@ -576,6 +591,8 @@ def main(argv=None):
     ap.add_argument("--layer", action="store_true",
                     help="time the whole incremental layer (q/k/v projection, step, output "
                          "projection) through gqa_decode_layer")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK",
+                    help="paged KV cache with this block size (rows per block)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small profiling cases)")
     args = ap.parse_args(argv)

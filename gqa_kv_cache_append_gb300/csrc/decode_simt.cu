@@ -159,36 +159,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                abort_flag, status, budget));
           if (!ok) continue;
           const int p0 = lt * C::T;
-          int blk[C::T / 16];
-          uint32_t total = 0;
-          bool bad = false;
-          for (int mm = 0; mm * piece < C::T; ++mm) {
-            const int p = p0 + mm * piece;
-            blk[mm] = -1;
-            if (p < seg.L) {
-              const int e = pc.get(p / bsz);
-              if (e >= 0 && e < num_blocks) {
-                blk[mm] = e;
-                total += 2u * min(piece, seg.L - p) * D * C::ELT;
-              } else {
-                bad = true;
-              }
-            }
-          }
-          if (lane == 0) {
-            if (bad) atomicOr(status, GQA_DEV_BAD_BLOCK);
-            uint8_t* stage = sm + st * C::STAGE_BYTES;
-            mbar_arrive_expect_tx(full0 + 8 * st, total);
-            for (int mm = 0; mm * piece < C::T; ++mm) {
-              const int p = p0 + mm * piece;
-              if (blk[mm] < 0) continue;
-              const uint32_t bytes = static_cast<uint32_t>(min(piece, seg.L - p)) * D * C::ELT;
-              const size_t prow = (static_cast<size_t>(blk[mm]) * g + seg.j) * bsz + p % bsz;
-              const uint32_t o = mm * piece * D * C::ELT;
-              bulk_load(smem_u32(stage + o), kc + prow * D, bytes, full0 + 8 * st);
-              bulk_load(smem_u32(stage + C::T * D * C::ELT + o), vc + prow * D, bytes,
-                        full0 + 8 * st);
-            }
+          // lane mm < T / piece copies piece mm (one block's rows) of the tile
+          const int e = pc.get_lanes(p0 / bsz);
+          const int pm = p0 + lane * piece;
+          const bool mine = lane * piece < C::T && pm < seg.L;
+          const bool good = mine && e >= 0 && e < num_blocks;
+          const uint32_t bytes = good ? static_cast<uint32_t>(min(piece, seg.L - pm)) * D * C::ELT : 0u;
+          const uint32_t total = __reduce_add_sync(0xffffffffu, 2u * bytes);
+          if (__any_sync(0xffffffffu, mine && !good) && lane == 0)
+            atomicOr(status, GQA_DEV_BAD_BLOCK);
+          uint8_t* stage = sm + st * C::STAGE_BYTES;
+          if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, total);
+          __syncwarp();
+          if (good) {
+            const size_t prow = (static_cast<size_t>(e) * g + seg.j) * bsz + pm % bsz;
+            const uint32_t o = lane * piece * D * C::ELT;
+            bulk_load(smem_u32(stage + o), kc + prow * D, bytes, full0 + 8 * st);
+            bulk_load(smem_u32(stage + C::T * D * C::ELT + o), vc + prow * D, bytes,
+                      full0 + 8 * st);
           }
           last_n[st] = static_cast<int>(n);
         }

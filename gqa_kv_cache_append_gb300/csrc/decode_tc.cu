@@ -236,27 +236,27 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           mbar_arrive_expect_tx(BAR(B_FULL_K + st), 2 * kBoxBytes);
           mbar_arrive_expect_tx(BAR(B_FULL_V + st), 2 * kBoxBytes);
         }
+        __syncwarp();
+        // lane mm < sub copies box mm of the tile (its block's rows)
+        const int p_first = lt * kT;
+        const int blk = pc.get_lanes(p_first / bsz);
+        const int pm = p_first + lane * box_rows;
         bool bad = false;
-        for (int mm = 0; mm < sub; ++mm) {
-          const int p0 = lt * kT + mm * box_rows;
+        if (lane < sub) {
           int row = oob_row;
-          if (p0 < seg.L) {
-            const int blk = pc.get(p0 / bsz);
+          if (pm < seg.L) {
             if (blk >= 0 && blk < num_blocks)
-              row = (blk * g + seg.j) * bsz + p0 % bsz;
+              row = (blk * g + seg.j) * bsz + pm % bsz;
             else
               bad = true;
           }
-          if (lane == 0) {
-            const uint32_t o = mm * box_rows * 128;
-            tma_load_2d(dst + o, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
-            tma_load_2d(dst + kBoxBytes + o, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
-            tma_load_2d(dst + 2 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
-            tma_load_2d(dst + 3 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 64, row,
-                        pol_stream);
-          }
+          const uint32_t o = lane * box_rows * 128;
+          tma_load_2d(dst + o, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
+          tma_load_2d(dst + kBoxBytes + o, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
+          tma_load_2d(dst + 2 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
+          tma_load_2d(dst + 3 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
         }
-        if (bad && lane == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
         last_n[st] = static_cast<int>(n);
       }
       if (!waited) {

@@ -363,14 +363,26 @@ struct PageCursor {
     cur = load(base + lane);
     nxt = load(base + 32 + lane);
   }
-  __device__ int get(int m) {
+  __device__ void advance_to(int m) {
     const int lane = threadIdx.x & 31;
     while (m >= base + 32) {
       base += 32;
       cur = nxt;
       nxt = load(base + 32 + lane);
     }
+  }
+  __device__ int get(int m) {
+    advance_to(m);
     return __shfl_sync(0xffffffffu, cur, m - base);
+  }
+  // Lane l gets entry m + l, for l < 32 (m + l may lie in the next chunk).
+  __device__ int get_lanes(int m) {
+    const int lane = threadIdx.x & 31;
+    advance_to(m);
+    const int k = m - base + lane;  // 0 .. 62
+    const int a = __shfl_sync(0xffffffffu, cur, k & 31);
+    const int c = __shfl_sync(0xffffffffu, nxt, k & 31);
+    return k < 32 ? a : c;
   }
 };
 
