@@ -61,30 +61,36 @@ struct Elt<__nv_bfloat16> {
   __device__ static void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
 
-template <typename DT, int D, int RMAX>
+// DK / DV: head dims of K (and q) and of V (and out); they may differ.
+template <typename DT, int DK, int DV, int RMAX>
 struct SimtCfg {
   static constexpr int ELT = Elt<DT>::size;
-  static constexpr int CH = D * ELT / 16;      // 16-byte chunks per row
+  static constexpr int CHK = DK * ELT / 16;    // 16-byte chunks per K row
+  static constexpr int CHV = DV * ELT / 16;    // ... per V row
   static constexpr int EPC = 16 / ELT;         // elements per chunk
-  static constexpr int PPW = 32 / CH;          // rows per warp step
-  static constexpr int T = 16384 / (D * ELT);  // positions per tile (32 KiB K+V)
+  static constexpr int PPW = 32 / CHK;         // K rows per warp step
+  static constexpr int DM = DK > DV ? DK : DV;
+  static constexpr int T = 16384 / (DM * ELT); // positions per tile (up to 32 KiB K+V)
   static constexpr int PPL = T / 32;           // positions per lane in softmax
-  static constexpr int NPG = 128 / CH;         // position groups in the V pass
+  static constexpr int NPG = 128 / CHV;        // position groups in the V pass
   static constexpr int STAGES = 3;
-  static constexpr int STAGE_BYTES = 2 * T * D * ELT;
+  static constexpr int K_BYTES = T * DK * ELT;
+  static constexpr int STAGE_BYTES = T * (DK + DV) * ELT;
   static constexpr int OFF_P = STAGES * STAGE_BYTES;          // float [RMAX][T]
-  static constexpr int OFF_RED = OFF_P + RMAX * T * 4;        // float [4][RMAX][D]
-  static constexpr int OFF_ML = OFF_RED + 4 * RMAX * D * 4;   // float m,l,alpha [RMAX]
+  static constexpr int OFF_RED = OFF_P + RMAX * T * 4;        // float [4][RMAX][DV]
+  static constexpr int OFF_ML = OFF_RED + 4 * RMAX * DV * 4;  // float m,l,alpha [RMAX]
   static constexpr int OFF_BAR = OFF_ML + 3 * RMAX * 4;
   static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 128;
-  static_assert(CH <= 32 && 32 % CH == 0, "row must split evenly over lanes");
+  static_assert(CHK <= 32 && 32 % CHK == 0 && CHV <= 32 && 32 % CHV == 0,
+                "rows must split evenly over lanes");
   static_assert(T % (4 * PPW) == 0 && T % 32 == 0, "tile shape");
+  static_assert(K_BYTES % 16 == 0, "16-byte aligned V tile");
 };
 
 constexpr int kThreads = 160;  // warp 0 copies, warps 1-4 compute
 
-template <typename DT, int D, int RMAX>
+template <typename DT, int DK, int DV, int RMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_simt_kernel(const DT* __restrict__ q, const DT* __restrict__ kc,
                        const DT* __restrict__ vc, const int* __restrict__ lens, int b, int h,
@@ -95,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        uint4* __restrict__ v_cache_w, unsigned int* status, long long budget,
                        int nq, const int* __restrict__ table, int bsz, int max_blocks,
                        int num_blocks) {
-  using C = SimtCfg<DT, D, RMAX>;
+  using C = SimtCfg<DT, DK, DV, RMAX>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                            ~uintptr_t(127));
@@ -164,8 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pm = p0 + lane * piece;
           const bool mine = lane * piece < C::T && pm < seg.L;
           const bool good = mine && e >= 0 && e < num_blocks;
-          const uint32_t bytes = good ? static_cast<uint32_t>(min(piece, seg.L - pm)) * D * C::ELT : 0u;
-          const uint32_t total = __reduce_add_sync(0xffffffffu, 2u * bytes);
+          const uint32_t rows_m = good ? static_cast<uint32_t>(min(piece, seg.L - pm)) : 0u;
+          const uint32_t total =
+              __reduce_add_sync(0xffffffffu, rows_m * (DK + DV) * C::ELT);
           if (__any_sync(0xffffffffu, mine && !good) && lane == 0)
             atomicOr(status, GQA_DEV_BAD_BLOCK);
           uint8_t* stage = sm + st * C::STAGE_BYTES;
@@ -173,10 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (good) {
             const size_t prow = (static_cast<size_t>(e) * g + seg.j) * bsz + pm % bsz;
-            const uint32_t o = lane * piece * D * C::ELT;
-            bulk_load(smem_u32(stage + o), kc + prow * D, bytes, full0 + 8 * st);
-            bulk_load(smem_u32(stage + C::T * D * C::ELT + o), vc + prow * D, bytes,
-                      full0 + 8 * st);
+            bulk_load(smem_u32(stage + lane * piece * DK * C::ELT), kc + prow * DK,
+                      rows_m * DK * C::ELT, full0 + 8 * st);
+            bulk_load(smem_u32(stage + C::K_BYTES + lane * piece * DV * C::ELT), vc + prow * DV,
+                      rows_m * DV * C::ELT, full0 + 8 * st);
           }
           last_n[st] = static_cast<int>(n);
         }
@@ -204,12 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) continue;
           const int p0 = lt * C::T;
           const int rows = min(C::T, seg.L - p0);
-          const uint32_t bytes = static_cast<uint32_t>(rows) * D * C::ELT;
           uint8_t* stage = sm + st * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(full0 + 8 * st, 2 * bytes);
-          bulk_load(smem_u32(stage), kc + (unit_row + p0) * D, bytes, full0 + 8 * st);
-          bulk_load(smem_u32(stage + C::T * D * C::ELT), vc + (unit_row + p0) * D, bytes,
-                    full0 + 8 * st);
+          mbar_arrive_expect_tx(full0 + 8 * st, static_cast<uint32_t>(rows) * (DK + DV) * C::ELT);
+          bulk_load(smem_u32(stage), kc + (unit_row + p0) * DK,
+                    static_cast<uint32_t>(rows) * DK * C::ELT, full0 + 8 * st);
+          bulk_load(smem_u32(stage + C::K_BYTES), vc + (unit_row + p0) * DV,
+                    static_cast<uint32_t>(rows) * DV * C::ELT, full0 + 8 * st);
           last_n[st] = static_cast<int>(n);
         }
       }
@@ -228,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- compute (128 threads) ----------------
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
-    const int sub = lane / C::CH, ch = lane % C::CH;  // logits mapping
-    const int pg = ct / C::CH;                         // V-pass mapping (chunk = ch)
+    const int sub = lane / C::CHK, ch = lane % C::CHK;  // logits mapping
+    const int pg = ct / C::CHV, chv = lane % C::CHV;     // V-pass mapping
     float qreg[RMAX][C::EPC];
     float acc[RMAX][C::EPC];
 #pragma unroll
@@ -245,29 +252,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fused append: the new tokens whose rows fall in this segment,
       // 16-byte chunks idx < nchunk; thread ct carries chunk ct from here
       const int first_new = seg.L - nq;
-      int s_lo = 0, nchunk = 0;
+      int s_lo = 0, nrows = 0;
       if (k_new != nullptr) {
         const int p_lo = max(first_new, seg.lt0 * C::T), p_hi = min(seg.L, seg.lt1 * C::T);
         if (p_lo < p_hi) {
           s_lo = p_lo - first_new;
-          nchunk = (p_hi - p_lo) * C::CH;
+          nrows = p_hi - p_lo;
         }
       }
-      auto new_chunk = [&](int idx) -> size_t {
-        return ((static_cast<size_t>(seg.i) * nq + s_lo + idx / C::CH) * g + seg.j) * C::CH +
-               idx % C::CH;
+      // chunk idx of the new rows of a tensor with `cpr` chunks per row
+      auto new_chunk = [&](int idx, int cpr) -> size_t {
+        return ((static_cast<size_t>(seg.i) * nq + s_lo + idx / cpr) * g + seg.j) * cpr +
+               idx % cpr;
       };
       uint4 knew = make_uint4(0u, 0u, 0u, 0u), vnew = knew;
-      if (ct < nchunk) {
-        knew = __ldg(k_new + new_chunk(ct));
-        vnew = __ldg(v_new + new_chunk(ct));
-      }
+      if (ct < nrows * C::CHK) knew = __ldg(k_new + new_chunk(ct, C::CHK));
+      if (ct < nrows * C::CHV) vnew = __ldg(v_new + new_chunk(ct, C::CHV));
 #pragma unroll
       for (int t = 0; t < RMAX; ++t) {
         if (t < nr) {
           const int s_ = t / r;
           const uint4 u = *reinterpret_cast<const uint4*>(
-              q + (obase + s_ * h + (t - s_ * r)) * D + ch * C::EPC);
+              q + (obase + s_ * h + (t - s_ * r)) * DK + ch * C::EPC);
           Elt<DT>::unpack(u, qreg[t]);
         } else {
 #pragma unroll
@@ -280,30 +286,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool ok = mbar_wait(full0 + 8 * st, (n / C::STAGES) & 1, abort_flag, status,
                                   budget);
         const DT* sK = reinterpret_cast<const DT*>(sm + st * C::STAGE_BYTES);
-        const DT* sV = sK + C::T * D;
-        if (nchunk > 0 && (lt + 1) * C::T > first_new) {
+        const DT* sV = reinterpret_cast<const DT*>(sm + st * C::STAGE_BYTES + C::K_BYTES);
+        if (nrows > 0 && (lt + 1) * C::T > first_new) {
           // rows L_i - n .. L_i - 1 are the new tokens: use k_new / v_new
           // there and store them into the cache (the append)
+          auto cache_row = [&](int pos) -> long long {
+            if (table == nullptr) return static_cast<long long>(unit) * cap + pos;
+            const int e = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + pos / bsz);
+            return (e >= 0 && e < num_blocks)
+                       ? (static_cast<long long>(e) * g + seg.j) * bsz + pos % bsz
+                       : -1;
+          };
           if (ok) {
-            for (int idx = ct; idx < nchunk; idx += 128) {
-              const int pos = first_new + s_lo + idx / C::CH, c16 = idx % C::CH;
+            for (int idx = ct; idx < nrows * C::CHK; idx += 128) {
+              const int pos = first_new + s_lo + idx / C::CHK, c16 = idx % C::CHK;
               if (pos < lt * C::T || pos >= (lt + 1) * C::T) continue;
-              const uint4 kv = idx == ct ? knew : __ldg(k_new + new_chunk(idx));
-              const uint4 vv = idx == ct ? vnew : __ldg(v_new + new_chunk(idx));
-              const int rho = pos - lt * C::T;
-              reinterpret_cast<uint4*>(const_cast<DT*>(sK) + rho * D)[c16] = kv;
-              reinterpret_cast<uint4*>(const_cast<DT*>(sV) + rho * D)[c16] = vv;
-              long long crow = static_cast<long long>(unit) * cap + pos;
-              if (table != nullptr) {
-                const int e = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + pos / bsz);
-                crow = (e >= 0 && e < num_blocks)
-                           ? (static_cast<long long>(e) * g + seg.j) * bsz + pos % bsz
-                           : -1;
-              }
-              if (crow >= 0) {
-                k_cache_w[crow * C::CH + c16] = kv;
-                v_cache_w[crow * C::CH + c16] = vv;
-              }
+              const uint4 kv = idx == ct ? knew : __ldg(k_new + new_chunk(idx, C::CHK));
+              reinterpret_cast<uint4*>(const_cast<DT*>(sK) + (pos - lt * C::T) * DK)[c16] = kv;
+              const long long crow = cache_row(pos);
+              if (crow >= 0) k_cache_w[crow * C::CHK + c16] = kv;
+            }
+            for (int idx = ct; idx < nrows * C::CHV; idx += 128) {
+              const int pos = first_new + s_lo + idx / C::CHV, c16 = idx % C::CHV;
+              if (pos < lt * C::T || pos >= (lt + 1) * C::T) continue;
+              const uint4 vv = idx == ct ? vnew : __ldg(v_new + new_chunk(idx, C::CHV));
+              reinterpret_cast<uint4*>(const_cast<DT*>(sV) + (pos - lt * C::T) * DV)[c16] = vv;
+              const long long crow = cache_row(pos);
+              if (crow >= 0) v_cache_w[crow * C::CHV + c16] = vv;
             }
           }
           named_bar_sync(1, 128);
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int p = step * (4 * C::PPW) + cw * C::PPW + sub;
           float kf[C::EPC];
           if (ok && p < valid) {
-            const uint4 u = *reinterpret_cast<const uint4*>(sK + p * D + ch * C::EPC);
+            const uint4 u = *reinterpret_cast<const uint4*>(sK + p * DK + ch * C::EPC);
             Elt<DT>::unpack(u, kf);
           } else {
 #pragma unroll
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < C::EPC; ++e) part = fmaf(qreg[t][e], kf[e], part);
 #pragma unroll
-              for (int o = C::CH / 2; o > 0; o >>= 1)
+              for (int o = C::CHK / 2; o > 0; o >>= 1)
                 part += __shfl_xor_sync(0xffffffffu, part, o);
               if (ch == 0 && p < valid) sP[t * C::T + p] = part * scale_log2;
             }
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           for (int p = pg; p < valid; p += C::NPG) {
             float vf[C::EPC];
-            const uint4 u = *reinterpret_cast<const uint4*>(sV + p * D + ch * C::EPC);
+            const uint4 u = *reinterpret_cast<const uint4*>(sV + p * DV + chv * C::EPC);
             Elt<DT>::unpack(u, vf);
 #pragma unroll
             for (int t = 0; t < RMAX; ++t) {
@@ -404,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < C::EPC; ++e) {
             float v = acc[t][e];
 #pragma unroll
-            for (int o = C::CH; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane < C::CH) sRed[(cw * RMAX + t) * D + ch * C::EPC + e] = v;
+            for (int o = C::CHV; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane < C::CHV) sRed[(cw * RMAX + t) * DV + chv * C::EPC + e] = v;
             acc[t][e] = 0.f;
           }
         }
@@ -418,15 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s_ = t / r;
         return obase + s_ * h + (t - s_ * r);
       };
-      for (int idx = ct; idx < nr * D; idx += 128) {
-        const int t = idx / D, dd = idx % D;
-        const float o = sRed[(0 * RMAX + t) * D + dd] + sRed[(1 * RMAX + t) * D + dd] +
-                        sRed[(2 * RMAX + t) * D + dd] + sRed[(3 * RMAX + t) * D + dd];
+      for (int idx = ct; idx < nr * DV; idx += 128) {
+        const int t = idx / DV, dd = idx % DV;
+        const float o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
+                        sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
         if (whole) {
-          Elt<DT>::store(out + out_row(t) * D + dd, o / sL[t]);
+          Elt<DT>::store(out + out_row(t) * DV + dd, o / sL[t]);
         } else {
           // (a row that saw none of this CTA's positions has max -inf, sum 0)
-          part_o[(slot * nr + t) * D + dd] = o;
+          part_o[(slot * nr + t) * DV + dd] = o;
           if (dd == 0) {
             part_ml[(slot * nr + t) * 2 + 0] = sM[t];
             part_ml[(slot * nr + t) * 2 + 1] = sL[t];
@@ -441,16 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (counters != nullptr && arrive_last(counters, u, np, last_flag, ct == 0, 1, 128)) {
           // merge the other CTAs' partials into this CTA's own (still in
           // shared memory)
-          for (int idx = ct; idx < nr * D; idx += 128) {
-            const int t = idx / D, dd = idx % D;
-            float o = sRed[(0 * RMAX + t) * D + dd] + sRed[(1 * RMAX + t) * D + dd] +
-                      sRed[(2 * RMAX + t) * D + dd] + sRed[(3 * RMAX + t) * D + dd];
+          for (int idx = ct; idx < nr * DV; idx += 128) {
+            const int t = idx / DV, dd = idx % DV;
+            float o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
+                      sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
             float M = sM[t], den = sL[t];
             for (long long c = c0; c <= c1; ++c) {
               if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
               const long long sl = (u + c) * nr + t;
               const float mc = __ldcg(part_ml + sl * 2), lc = __ldcg(part_ml + sl * 2 + 1);
-              const float oc = __ldcg(part_o + sl * D + dd);
+              const float oc = __ldcg(part_o + sl * DV + dd);
               const float mn = fmaxf(M, mc);
               const float mr = (mn == -INFINITY) ? 0.f : mn;  // both pieces empty
               const float sa = ex2(M - mr), sb = ex2(mc - mr);
@@ -458,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               den = den * sa + lc * sb;
               M = mn;
             }
-            Elt<DT>::store(out + out_row(t) * D + dd, o / den);
+            Elt<DT>::store(out + out_row(t) * DV + dd, o / den);
           }
         }
       }
@@ -474,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 }
 
-template <typename DT, int D, int RMAX>
+template <typename DT, int DK, int DV, int RMAX>
 cudaError_t launch_t(const DecodeLaunch& a) {
-  using C = SimtCfg<DT, D, RMAX>;
-  auto kern = decode_simt_kernel<DT, D, RMAX>;
+  using C = SimtCfg<DT, DK, DV, RMAX>;
+  auto kern = decode_simt_kernel<DT, DK, DV, RMAX>;
   // the shared-memory opt-in is set once per device (not during a capture)
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -509,24 +518,37 @@ cudaError_t launch_t(const DecodeLaunch& a) {
 
 }  // namespace
 
-bool simt_supported(int dtype, int d, int cols) {
-  if (dtype == GQA_F32) return (d == 64 || d == 128) && cols >= 1 && cols <= 16;
-  if (dtype == GQA_BF16) return (d == 64 || d == 128) && cols >= 1 && cols <= 8;
+bool simt_supported(int dtype, int d_k, int d_v, int cols) {
+  const bool dims = (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128);
+  if (dtype == GQA_F32) return dims && cols >= 1 && cols <= 16;
+  if (dtype == GQA_BF16) return dims && cols >= 1 && cols <= 8;
   return false;
 }
 
-int simt_tile(int dtype, int d) { return 16384 / (d * (dtype == GQA_F32 ? 4 : 2)); }
+int simt_tile(int dtype, int d_k, int d_v) {
+  return 16384 / ((d_k > d_v ? d_k : d_v) * (dtype == GQA_F32 ? 4 : 2));
+}
 
 int simt_ctas_per_sm(int, int, int) { return 1; }
 
+template <typename DT, int DK, int DV>
+cudaError_t launch_dims(const DecodeLaunch& a, int r) {
+  if constexpr (sizeof(DT) == 4) {
+    if (r > 8) return launch_t<DT, DK, DV, 16>(a);
+  }
+  return launch_t<DT, DK, DV, 8>(a);
+}
+
+template <typename DT>
+cudaError_t launch_dtype(const DecodeLaunch& a, int r) {
+  if (a.d == 64) return a.dv == 64 ? launch_dims<DT, 64, 64>(a, r) : launch_dims<DT, 64, 128>(a, r);
+  return a.dv == 64 ? launch_dims<DT, 128, 64>(a, r) : launch_dims<DT, 128, 128>(a, r);
+}
+
 cudaError_t launch_decode_simt(const DecodeLaunch& a) {
   const int r = a.nq * (a.h / a.g);  // query rows per KV head
-  if (a.dtype == GQA_F32) {
-    if (a.d == 64) return r <= 8 ? launch_t<float, 64, 8>(a) : launch_t<float, 64, 16>(a);
-    return r <= 8 ? launch_t<float, 128, 8>(a) : launch_t<float, 128, 16>(a);
-  }
-  if (a.d == 64) return launch_t<__nv_bfloat16, 64, 8>(a);
-  return launch_t<__nv_bfloat16, 128, 8>(a);
+  if (a.dtype == GQA_F32) return launch_dtype<float>(a, r);
+  return launch_dtype<__nv_bfloat16>(a, r);
 }
 
 }  // namespace gqa

@@ -317,13 +317,13 @@ bool use_combine_kernel(const DecodeLaunch& a) {
 int launch_all(DecodeLaunch& a, int tile) {
   const bool separate = use_combine_kernel(a);
   if (separate) a.counters = nullptr;
-  const bool tc = tc_supported(a.dtype, a.d, a.nq * (a.h / a.g));
+  const bool tc = a.d == a.dv && tc_supported(a.dtype, a.d, a.nq * (a.h / a.g));
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   if (separate) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.b) * a.h * a.nq));
-    cfg.blockDim = dim3(a.d);
+    cfg.blockDim = dim3(a.dv);
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -332,11 +332,11 @@ int launch_all(DecodeLaunch& a, int tile) {
     cfg.numAttrs = 1;
     if (a.dtype == GQA_BF16)
       e = cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a.seq_lens, a.b, a.h, a.g,
-                             a.cap, a.d, tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
+                             a.cap, a.dv, tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
                              static_cast<const float*>(a.part_ml),
                              static_cast<__nv_bfloat16*>(a.out));
     else
-      e = cudaLaunchKernelEx(&cfg, combine_kernel<float>, a.seq_lens, a.b, a.h, a.g, a.cap, a.d,
+      e = cudaLaunchKernelEx(&cfg, combine_kernel<float>, a.seq_lens, a.b, a.h, a.g, a.cap, a.dv,
                              tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
                              static_cast<const float*>(a.part_ml), static_cast<float*>(a.out));
   }
@@ -530,26 +530,25 @@ int decode_check(const DecodeArgs& x) {
       (reinterpret_cast<uintptr_t>(x.seq_lens) & 3u))
     return GQA_ERR_ALIGN;
   const int r = x.h / x.g;
-  if (x.d_k != x.d_v || x.b > 65535 || static_cast<long long>(x.nq) * r > 32)
-    return GQA_ERR_UNSUPPORTED;
+  if (x.b > 65535 || static_cast<long long>(x.nq) * r > 32) return GQA_ERR_UNSUPPORTED;
   const int cols = x.nq * r;  // query rows per KV head
-  if (!tc_supported(x.dtype, x.d_k, cols) && !simt_supported(x.dtype, x.d_k, cols))
-    return GQA_ERR_UNSUPPORTED;
+  const bool tc = x.d_k == x.d_v && tc_supported(x.dtype, x.d_k, cols);
+  if (!tc && !simt_supported(x.dtype, x.d_k, x.d_v, cols)) return GQA_ERR_UNSUPPORTED;
   return GQA_OK;
 }
 
 DecodePlan decode_plan(const DecodeArgs& x, int num_sms) {
   const int r = x.h / x.g, d = x.d_k, cols = x.nq * r;
-  const bool use_tc = tc_supported(x.dtype, d, cols);
+  const bool use_tc = x.d_k == x.d_v && tc_supported(x.dtype, d, cols);
   DecodePlan p;
-  p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, d);
+  p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, x.d_k, x.d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(x.dtype, d, r);
   const long long max_tiles = static_cast<long long>(x.b) * x.g * ((x.cap + p.tile - 1) / p.tile);
   p.nc = static_cast<long long>(num_sms) * per_sm;
   if (p.nc > max_tiles) p.nc = max_tiles;
   if (p.nc < 1) p.nc = 1;
   const size_t slots = static_cast<size_t>(x.b) * x.g + static_cast<size_t>(p.nc);
-  p.o_bytes = slots * cols * d * sizeof(float);
+  p.o_bytes = slots * cols * x.d_v * sizeof(float);
   p.ml_bytes = slots * cols * 2 * sizeof(float);
   // two arrival counters per unit: the tensor-core kernel may run two
   // softmax warpgroups, each with its own
@@ -568,6 +567,7 @@ int decode_run(const DecodeArgs& x, const DecodePlan& p, const DeviceInfo* di, v
   a.h = x.h;
   a.g = x.g;
   a.d = x.d_k;
+  a.dv = x.d_v;
   a.cap = x.cap;
   a.dtype = x.dtype;
   a.nq = x.nq;
@@ -965,20 +965,20 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
     return GQA_ERR_ALIGN;
   const int r = h / g;
   const int d = d_k;
-  if (d_k != d_v || b > 65535) return GQA_ERR_UNSUPPORTED;
-  const bool use_tc = tc_supported(dtype, d, r);
-  if (!use_tc && !simt_supported(dtype, d, r)) return GQA_ERR_UNSUPPORTED;
+  if (b > 65535) return GQA_ERR_UNSUPPORTED;
+  const bool use_tc = d_k == d_v && tc_supported(dtype, d, r);
+  if (!use_tc && !simt_supported(dtype, d_k, d_v, r)) return GQA_ERR_UNSUPPORTED;
   NoAllocDevice* nd = nullptr;
   if (int e = noalloc_setup(&nd)) return e;
 
-  const int tile = use_tc ? tc_tile() : simt_tile(dtype, d);
+  const int tile = use_tc ? tc_tile() : simt_tile(dtype, d_k, d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(dtype, d, r);
   const long long max_tiles = static_cast<long long>(b) * g * ((cap + tile - 1) / tile);
   long long nc = static_cast<long long>(nd->num_sms) * per_sm;
   if (nc > max_tiles) nc = max_tiles;
   if (nc < 1) nc = 1;
   const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
-  const size_t o_bytes = slots * r * d * sizeof(float);
+  const size_t o_bytes = slots * r * d_v * sizeof(float);
   const size_t ml_bytes = slots * r * 2 * sizeof(float);
   if (2 * static_cast<size_t>(b) * g > kNoAllocMaxUnits ||
       o_bytes + ml_bytes > kNoAllocScratchBytes - kNoAllocCounterBytes)
@@ -1000,6 +1000,7 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   a.h = h;
   a.g = g;
   a.d = d;
+  a.dv = d_v;
   a.cap = cap;
   a.dtype = dtype;
   a.nq = 1;

@@ -14,11 +14,12 @@ struct DecodeLaunch {
   const void* k_cache;
   const void* v_cache;
   const int* seq_lens;
-  int b, h, g, d, cap, dtype;
+  int b, h, g, d, cap, dtype;  // d: head dim of q and K (d_k)
+  int dv = 0;            // head dim of V and out (d_v)
   int nq;                // new tokens (queries) per sequence, >= 1
   float scale_log2;      // scale * log2(e): logits are kept in base 2
   void* out;
-  float* part_o;         // [slots, nq * r, d] unnormalised partial outputs
+  float* part_o;         // [slots, nq * r, dv] unnormalised partial outputs
   float* part_ml;        // [slots, nq * r, 2] running max (base 2) and sum
   int* counters;         // [b * g] arrivals per split unit; zero between launches
   const void* k_new;     // fused append: new K/V rows [b, nq, g, d], or null
@@ -43,10 +44,10 @@ struct DecodeLaunch {
 bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides, const uint32_t* box);
 
-// CUDA-core kernel (fp32, and bf16 with d = 64); `cols` = nq * r query rows
-// per KV head
-bool simt_supported(int dtype, int d, int cols);
-int simt_tile(int dtype, int d);
+// CUDA-core kernel (fp32 and bf16, d_k and d_v in {64, 128}); `cols` = nq * r
+// query rows per KV head
+bool simt_supported(int dtype, int d_k, int d_v, int cols);
+int simt_tile(int dtype, int d_k, int d_v);
 int simt_ctas_per_sm(int dtype, int d, int r);
 cudaError_t launch_decode_simt(const DecodeLaunch& a);
 

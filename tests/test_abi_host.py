@@ -76,7 +76,8 @@ def _app(lib_, **kw):
     (dict(h=6, g=4), -2), (dict(b=0), -2), (dict(g=0), -2), (dict(cap=0), -2),
     (dict(dk=0), -2), (dict(b=40000, g=8, h=8, cap=8000), -2),
     (dict(q=A + 8), -4), (dict(k=A + 2), -4), (dict(out=A + 4), -4), (dict(lens=A + 2), -4),
-    (dict(dk=128, dv=64), -5), (dict(dk=96, dv=96), -5), (dict(h=64, g=1), -5),
+    (dict(dk=128, dv=32), -5), (dict(dk=96, dv=96), -5), (dict(h=64, g=1), -5),
+    (dict(dk=128, dv=64, h=32, g=2), -5),       # d_k != d_v: CUDA-core kernel, r <= 8 in bf16
     (dict(dtype=0, h=34, g=1), -5), (dict(dtype=1, dk=64, dv=64, h=16, g=1), -5),
 ])
 def test_decode_attn_host_checks(kw, code):
