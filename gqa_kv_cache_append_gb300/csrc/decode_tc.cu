@@ -56,6 +56,10 @@ constexpr int kT = 128;       // positions per tile (MMA M of the S product)
 constexpr int kD = 128;       // head dim (MMA M of the O product)
 constexpr int kStages = 3;    // K/V ring depth
 constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
+// early streaming: tiles past the ring that L2 is asked for before the wait
+// (launches whose merge runs in a separate combine kernel skip it: there the
+// prefetch competes with the combine's reads of the partials in L2)
+constexpr int kPrefetchTiles = 3;
 
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
@@ -321,6 +325,15 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         const int unit_row = (seg.i * g + seg.j) * cap;
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
           if (!waited && (lt - seg.lt0 == kStages)) {
+            // the ring is full: have L2 fetch the next tiles too, so HBM stays
+            // busy until the kernel ahead completes
+            for (int lp = lt; lp < seg.lt1 && lp < lt + (counters ? kPrefetchTiles : 0); ++lp) {
+              const int rp = unit_row + lp * kT;
+              tma_prefetch_l2_2d(&tm_k, 0, rp);
+              tma_prefetch_l2_2d(&tm_k, 64, rp);
+              tma_prefetch_l2_2d(&tm_v, 0, rp);
+              tma_prefetch_l2_2d(&tm_v, 64, rp);
+            }
             pdl_wait();
             waited = true;
             load_q(k, seg);
