@@ -97,60 +97,61 @@ __global__ void kv_append_paged_kernel(const uint4* __restrict__ k_new,
 // Log-sum-exp combine for launches with many more CTAs than units (a few
 // long sequences, e.g. one MQA head over 131k positions spread over 19
 // CTAs): the decode kernel then only writes partials, and this kernel merges
-// them with the whole GPU, one CTA per (unit, query row), one thread per
-// output column.  Query row t = s * r + head of a unit is head j * r + head
-// of new token s.  With per-CTA maxima m_c (base 2), sums l_c and
-// unnormalised outputs O_c of the same softmax over disjoint position ranges:
+// them with the whole GPU, one warp per (unit, query row), each lane holding
+// CPL = d / 32 consecutive output columns.  Query row t = s * r + head of a
+// unit is head j * r + head of new token s.  With per-CTA maxima m_c (base
+// 2), sums l_c and unnormalised outputs O_c of the same softmax over disjoint
+// position ranges:
 //     M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 // Units held whole by one CTA were written by the decode kernel.
 // ---------------------------------------------------------------------------
-template <typename DT>
-__global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g, int cap,
-                               int d, int tile, int nc, int nq, const float* __restrict__ part_o,
-                               const float* __restrict__ part_ml, DT* __restrict__ out) {
-  __shared__ long long s_u0, s_W;
-  __shared__ int s_ti;
+constexpr int kCombineWarps = 4;
+
+template <typename DT, int CPL>
+__global__ void __launch_bounds__(32 * kCombineWarps)
+    combine_kernel(const int* __restrict__ lens, int b, int h, int g, int cap, int tile, int nc,
+                   int nq, const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                   DT* __restrict__ out) {
+  constexpr int d = 32 * CPL;
   pdl_launch_dependents();
   pdl_wait();  // the partials come from the decode kernel just before
   const int r = h / g;
   const int nr = nq * r;
-  const int u = blockIdx.x / nr, t = blockIdx.x % nr;
+  const int lane = threadIdx.x & 31;
+  const long long row_id = static_cast<long long>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  if (row_id >= static_cast<long long>(b) * g * nr) return;
+  const int u = static_cast<int>(row_id / nr), t = static_cast<int>(row_id % nr);
   const int i = u / g, j = u % g;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    long long before = 0, all = 0;
-    for (int base = 0; base < b; base += 32) {
-      const int idx = base + lane;
-      const int tt = (idx < b) ? seq_tiles(__ldg(lens + idx), nq, cap, tile) : 0;
-      all += tt;
-      if (idx < i) before += tt;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      all += __shfl_xor_sync(0xffffffffu, all, o);
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-    }
-    if (lane == 0) {
-      const int ti = seq_tiles(__ldg(lens + i), nq, cap, tile);
-      s_ti = ti;
-      s_u0 = before * g + static_cast<long long>(j) * ti;
-      s_W = all * g;
-    }
+  // the unit's tile range (warp-cooperative scan of the lengths)
+  long long before = 0, all = 0;
+  int ti = 0;
+  for (int base = 0; base < b; base += 32) {
+    const int idx = base + lane;
+    const int tt = (idx < b) ? seq_tiles(__ldg(lens + idx), nq, cap, tile) : 0;
+    all += tt;
+    if (idx < i) before += tt;
+    if (idx == i) ti = tt;
   }
-  __syncthreads();
-  const int ti = s_ti;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    all += __shfl_xor_sync(0xffffffffu, all, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    ti += __shfl_xor_sync(0xffffffffu, ti, o);
+  }
   if (ti == 0) return;
-  const long long W = s_W;
+  const long long W = all * g;
+  const long long u0 = before * g + static_cast<long long>(j) * ti;
   long long c0, c1;
-  unit_ctas(s_u0, s_u0 + ti, W, nc, c0, c1);
+  unit_ctas(u0, u0 + ti, W, nc, c0, c1);
   if (c0 == c1) return;
-  const int col = threadIdx.x;
-  // pieces in batches of 16, every load of a batch issued before any use;
+  // pieces in batches of 8, every load of a batch issued before any use;
   // batches merge online (running max M, sums num / den)
-  constexpr int kBatch = 16;
-  float M = -INFINITY, num = 0.f, den = 0.f;
+  constexpr int kBatch = 8;
+  float M = -INFINITY, den = 0.f, num[CPL];
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) num[e] = 0.f;
   for (long long cb = c0; cb <= c1; cb += kBatch) {
-    float mc[kBatch], lc[kBatch], oc[kBatch];
+    float mc[kBatch], lc[kBatch], oc[kBatch][CPL];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const long long c = cb + k;
@@ -158,7 +159,19 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
       const long long sl = (u + c) * nr + t;
       mc[k] = use ? __ldg(part_ml + sl * 2) : -INFINITY;
       lc[k] = use ? __ldg(part_ml + sl * 2 + 1) : 0.f;
-      oc[k] = use ? __ldg(part_o + sl * d + col) : 0.f;
+      if constexpr (CPL == 4) {
+        const float4 v = use ? __ldg(reinterpret_cast<const float4*>(part_o + sl * d) + lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        oc[k][0] = v.x;
+        oc[k][1] = v.y;
+        oc[k][2] = v.z;
+        oc[k][3] = v.w;
+      } else {
+        const float2 v = use ? __ldg(reinterpret_cast<const float2*>(part_o + sl * d) + lane)
+                             : make_float2(0.f, 0.f);
+        oc[k][0] = v.x;
+        oc[k][1] = v.y;
+      }
     }
     float mb = M;
 #pragma unroll
@@ -166,23 +179,28 @@ __global__ void combine_kernel(const int* __restrict__ lens, int b, int h, int g
     // pieces that saw no position of this row (causal mask) have max -inf
     const float mbr = (mb == -INFINITY) ? 0.f : mb;
     const float sc = ex2(M - mbr);  // 0 while M = -inf
-    num *= sc;
     den *= sc;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) num[e] *= sc;
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const float wgt = ex2(mc[k] - mbr);  // 0 for unused slots and empty pieces
       den = fmaf(wgt, lc[k], den);
-      num = fmaf(wgt, oc[k], num);
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) num[e] = fmaf(wgt, oc[k][e], num[e]);
     }
     M = mb;
   }
-  const float v = num / den;
   const int s = t / r;
-  DT* dst = out + ((static_cast<size_t>(i) * nq + s) * h + j * r + (t - s * r)) * d + col;
-  if constexpr (sizeof(DT) == 2)
-    *dst = __float2bfloat16_rn(v);
-  else
-    *dst = v;
+  DT* dst = out + ((static_cast<size_t>(i) * nq + s) * h + j * r + (t - s * r)) * d + lane * CPL;
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) {
+    const float v = num[e] / den;
+    if constexpr (sizeof(DT) == 2)
+      dst[e] = __float2bfloat16_rn(v);
+    else
+      dst[e] = v;
+  }
 }
 
 // One mbarrier that nothing ever arrives on; the bounded wait must give up.
@@ -321,24 +339,31 @@ int launch_all(DecodeLaunch& a, int tile) {
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   if (separate) {
+    const long long rows = static_cast<long long>(a.b) * a.h * a.nq;  // (unit, query row) pairs
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.b) * a.h * a.nq));
-    cfg.blockDim = dim3(a.dv);
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps));
+    cfg.blockDim = dim3(32 * kCombineWarps);
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (a.dtype == GQA_BF16)
-      e = cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a.seq_lens, a.b, a.h, a.g,
-                             a.cap, a.dv, tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
-                             static_cast<const float*>(a.part_ml),
-                             static_cast<__nv_bfloat16*>(a.out));
-    else
-      e = cudaLaunchKernelEx(&cfg, combine_kernel<float>, a.seq_lens, a.b, a.h, a.g, a.cap, a.dv,
-                             tile, a.nc, a.nq, static_cast<const float*>(a.part_o),
-                             static_cast<const float*>(a.part_ml), static_cast<float*>(a.out));
+    const float* po = static_cast<const float*>(a.part_o);
+    const float* pml = static_cast<const float*>(a.part_ml);
+    if (a.dtype == GQA_BF16) {
+      auto* o = static_cast<__nv_bfloat16*>(a.out);
+      e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 4>, a.seq_lens,
+                                           a.b, a.h, a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
+                      : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 2>, a.seq_lens,
+                                           a.b, a.h, a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
+    } else {
+      auto* o = static_cast<float*>(a.out);
+      e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 4>, a.seq_lens, a.b, a.h,
+                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
+                      : cudaLaunchKernelEx(&cfg, combine_kernel<float, 2>, a.seq_lens, a.b, a.h,
+                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
+    }
   }
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
