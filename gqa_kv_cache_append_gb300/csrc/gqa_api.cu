@@ -97,11 +97,13 @@ __global__ void kv_append_paged_kernel(const uint4* __restrict__ k_new,
 // Log-sum-exp combine for launches with many more CTAs than units (a few
 // long sequences, e.g. one MQA head over 131k positions spread over 19
 // CTAs): the decode kernel then only writes partials, and this kernel merges
-// them with the whole GPU, one warp per (unit, query row), each lane holding
-// CPL = d / 32 consecutive output columns.  Query row t = s * r + head of a
-// unit is head j * r + head of new token s.  With per-CTA maxima m_c (base
-// 2), sums l_c and unnormalised outputs O_c of the same softmax over disjoint
-// position ranges:
+// them with the whole GPU, one CTA per (unit, query row).  Its four warps
+// take every fourth piece each (the loads of all pieces go out at once),
+// each lane holding CPL = d / 32 consecutive output columns; the warps'
+// results are merged in shared memory in warp order.  Query row t = s * r +
+// head of a unit is head j * r + head of new token s.  With per-CTA maxima
+// m_c (base 2), sums l_c and unnormalised outputs O_c of the same softmax
+// over disjoint position ranges:
 //     M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 // Units held whole by one CTA were written by the decode kernel.
 // ---------------------------------------------------------------------------
@@ -113,16 +115,16 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
                    int nq, const float* __restrict__ part_o, const float* __restrict__ part_ml,
                    DT* __restrict__ out) {
   constexpr int d = 32 * CPL;
+  __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+  __shared__ float s_o[kCombineWarps][d];
   pdl_launch_dependents();
   pdl_wait();  // the partials come from the decode kernel just before
   const int r = h / g;
   const int nr = nq * r;
-  const int lane = threadIdx.x & 31;
-  const long long row_id = static_cast<long long>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
-  if (row_id >= static_cast<long long>(b) * g * nr) return;
-  const int u = static_cast<int>(row_id / nr), t = static_cast<int>(row_id % nr);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int u = blockIdx.x / nr, t = blockIdx.x % nr;
   const int i = u / g, j = u % g;
-  // the unit's tile range (warp-cooperative scan of the lengths)
+  // the unit's tile range (warp-cooperative scan of the lengths, every warp)
   long long before = 0, all = 0;
   int ti = 0;
   for (int base = 0; base < b; base += 32) {
@@ -138,23 +140,23 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     before += __shfl_xor_sync(0xffffffffu, before, o);
     ti += __shfl_xor_sync(0xffffffffu, ti, o);
   }
-  if (ti == 0) return;
+  if (ti == 0) return;  // (uniform across the CTA)
   const long long W = all * g;
   const long long u0 = before * g + static_cast<long long>(j) * ti;
   long long c0, c1;
   unit_ctas(u0, u0 + ti, W, nc, c0, c1);
   if (c0 == c1) return;
-  // pieces in batches of 8, every load of a batch issued before any use;
-  // batches merge online (running max M, sums num / den)
+  // this warp's pieces c0 + wid + 4k, in batches of 8 (every load of a batch
+  // issued before any use); batches merge online (running max M, sums)
   constexpr int kBatch = 8;
   float M = -INFINITY, den = 0.f, num[CPL];
 #pragma unroll
   for (int e = 0; e < CPL; ++e) num[e] = 0.f;
-  for (long long cb = c0; cb <= c1; cb += kBatch) {
+  for (long long cb = c0 + wid; cb <= c1; cb += kBatch * kCombineWarps) {
     float mc[kBatch], lc[kBatch], oc[kBatch][CPL];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
-      const long long c = cb + k;
+      const long long c = cb + k * kCombineWarps;
       const bool use = c <= c1 && (W >= nc || !cta_empty(c, W, nc));
       const long long sl = (u + c) * nr + t;
       mc[k] = use ? __ldg(part_ml + sl * 2) : -INFINITY;
@@ -191,11 +193,36 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     }
     M = mb;
   }
+  if (lane == 0) {
+    s_m[wid] = M;
+    s_l[wid] = den;
+  }
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) s_o[wid][lane * CPL + e] = num[e];
+  __syncthreads();
+  if (wid != 0) return;
+  float mw[kCombineWarps], mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    mw[w] = s_m[w];
+    mx = fmaxf(mx, mw[w]);
+  }
+  const float mref = (mx == -INFINITY) ? 0.f : mx;
+  float dsum = 0.f, o[CPL];
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) o[e] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    const float wgt = ex2(mw[w] - mref);
+    dsum = fmaf(wgt, s_l[w], dsum);
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) o[e] = fmaf(wgt, s_o[w][lane * CPL + e], o[e]);
+  }
   const int s = t / r;
   DT* dst = out + ((static_cast<size_t>(i) * nq + s) * h + j * r + (t - s * r)) * d + lane * CPL;
 #pragma unroll
   for (int e = 0; e < CPL; ++e) {
-    const float v = num[e] / den;
+    const float v = o[e] / dsum;
     if constexpr (sizeof(DT) == 2)
       dst[e] = __float2bfloat16_rn(v);
     else
@@ -341,7 +368,7 @@ int launch_all(DecodeLaunch& a, int tile) {
   if (separate) {
     const long long rows = static_cast<long long>(a.b) * a.h * a.nq;  // (unit, query row) pairs
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows));
     cfg.blockDim = dim3(32 * kCombineWarps);
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
