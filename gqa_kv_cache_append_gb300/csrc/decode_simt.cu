@@ -448,15 +448,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
         const int np = unit_parts(c0, c1, w.W, w.nc);
         if (counters != nullptr && arrive_last(counters, u, np, last_flag, ct == 0, 1, 128)) {
-          // merge the other CTAs' partials into this CTA's own (still in
-          // shared memory)
+          // merge the partials in CTA order whichever CTA merges (the same
+          // bits every run): this CTA's own (still in shared memory) is used
+          // in place only when it is the first piece, else read back
+          long long cfirst = c0;
+          if (w.W < w.nc)
+            while (cfirst < c1 && cta_empty(cfirst, w.W, w.nc)) ++cfirst;
+          const bool own_first = cfirst == blockIdx.x;
           for (int idx = ct; idx < nr * DV; idx += 128) {
             const int t = idx / DV, dd = idx % DV;
-            float o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
-                      sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
-            float M = sM[t], den = sL[t];
+            float o = 0.f, M = -INFINITY, den = 0.f;
+            if (own_first) {
+              o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
+                  sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
+              M = sM[t];
+              den = sL[t];
+            }
             for (long long c = c0; c <= c1; ++c) {
-              if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
+              if ((own_first && c == blockIdx.x) || (w.W < w.nc && cta_empty(c, w.W, w.nc)))
+                continue;
               const long long sl = (u + c) * nr + t;
               const float mc = __ldcg(part_ml + sl * 2), lc = __ldcg(part_ml + sl * 2 + 1);
               const float oc = __ldcg(part_o + sl * DV + dd);

@@ -832,11 +832,29 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           const int np = unit_parts(c0, c1, w.W, w.nc);
           if (counters != nullptr && h0 < nr &&
               arrive_last(counters, u * NWG + wg, np, last_flag_wg, row == 0, bar_id, 128)) {
+            // pieces merge in CTA order whichever CTA merges (the same bits
+            // every run).  This CTA's piece is used from registers when it
+            // is the first (one warpgroup: registers to spare), else read
+            // back like the others.
+            bool own_first = false;
+            if constexpr (NWG == 1) {
+              long long cfirst = c0;
+              if (w.W < w.nc)
+                while (cfirst < c1 && cta_empty(cfirst, w.W, w.nc)) ++cfirst;
+              own_first = cfirst == blockIdx.x;
+            }
             float m[HP];
 #pragma unroll
-            for (int e = 0; e < HP; ++e) m[e] = l[e] > 0.f ? mfin[e] : -INFINITY;
+            for (int e = 0; e < HP; ++e) {
+              m[e] = (own_first && l[e] > 0.f) ? mfin[e] : -INFINITY;
+              if (!own_first) {
+                o[e] = 0.f;
+                l[e] = 0.f;
+              }
+            }
             for (long long c = c0; c <= c1; ++c) {
-              if (c == blockIdx.x || (w.W < w.nc && cta_empty(c, w.W, w.nc))) continue;
+              if ((own_first && c == blockIdx.x) || (w.W < w.nc && cta_empty(c, w.W, w.nc)))
+                continue;
               // eight heads at a time: their loads go out together
 #pragma unroll
               for (int e0 = 0; e0 < HP; e0 += 8) {

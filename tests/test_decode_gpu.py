@@ -247,6 +247,26 @@ def test_results_are_deterministic():
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("dtype,h,g,d", [("bf16", 64, 8, 128), ("bf16", 32, 1, 128),
+                                         ("f32", 8, 2, 64)])
+def test_in_kernel_merge_is_deterministic(dtype, h, g, d):
+    """Units split across CTAs and merged by the last CTA to finish (few
+    pieces per unit): the pieces are merged in CTA order whichever CTA
+    merges, so repeated runs give the same bits."""
+    B = _b()
+    b = 96 if g == 1 else 24
+    cfg = cfg_of(dtype, b, h, g, d, 700, seed=3)
+    x = make_layer(cfg, 0, "cuda", lens=np.random.default_rng(8).integers(1, 701, b).astype(np.int32))
+    outs = []
+    for _ in range(3):
+        out = torch.empty((cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device="cuda")
+        B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.h,
+                          cfg.g, d, d, cfg.scale, out)
+        outs.append(bits(out))
+    assert B.gqa_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
 def test_bad_length_is_reported_and_other_rows_are_right():
     B = _b()
     cfg = cfg_of("bf16", 3, 16, 2, 128, 300, seed=2)
