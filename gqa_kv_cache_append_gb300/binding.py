@@ -55,11 +55,11 @@ SIGNATURES = {
     "gqa_decode_layer": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
                               _F, _VP, _I, _I, _I, _VP]),
     "gqa_kv_append_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I,
-                                 _VP]),
-    "gqa_decode_attn_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _VP, _I, _I,
-                                   _I, _I, _VP]),
-    "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F,
-                                   _VP, _I, _I, _I, _I, _I, _VP]),
+                                 _I, _VP]),
+    "gqa_decode_attn_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _I,
+                                   _I, _I, _I, _VP]),
+    "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                                   _F, _VP, _I, _I, _I, _I, _I, _VP]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -238,33 +238,34 @@ def gqa_decode_layer(x, w_q, w_k, w_v, w_o, k_cache, v_cache, seq_lens, b, d_mod
 
 
 def gqa_kv_append_paged(k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, g, d_k, d_v,
-                        block_size=None, dtype=None, stream=None) -> None:
-    """Append into a paged cache (pools [num_blocks, g, block_size, d])."""
+                        n=1, dtype=None, stream=None) -> None:
+    """Append n new rows per sequence into a paged cache (pools
+    [num_blocks, g, block_size, d], block_table [b, max_blocks])."""
     nb, _, bs, _ = k_pool.shape
     _check("gqa_kv_append_paged", lib.gqa_kv_append_paged(
         _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
-        int(b), int(g), int(d_k), int(d_v), int(block_size or bs), int(block_table.shape[1]),
-        int(nb), _dtype(k_pool, dtype), _stream(stream)))
+        int(b), int(n), int(g), int(d_k), int(d_v), int(bs), int(block_table.shape[1]), int(nb),
+        _dtype(k_pool, dtype), _stream(stream)))
 
 
 def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k, d_v, scale,
-                          out, dtype=None, stream=None) -> None:
-    """gqa_decode_attn over a paged cache."""
+                          out, n=1, dtype=None, stream=None) -> None:
+    """gqa_decode_attn (n = 1) or gqa_decode_attn_multi over a paged cache."""
     nb, _, bs, _ = k_pool.shape
     _check("gqa_decode_attn_paged", lib.gqa_decode_attn_paged(
-        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens), int(b), int(h),
-        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(bs),
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens), int(b), int(n),
+        int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(bs),
         int(block_table.shape[1]), int(nb), _dtype(q, dtype), _stream(stream)))
 
 
 def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k,
-                          d_v, scale, out, dtype=None, flags=0, stream=None) -> None:
-    """Append and attend over a paged cache in one launch."""
+                          d_v, scale, out, n=1, dtype=None, flags=0, stream=None) -> None:
+    """Append and attend over a paged cache in one launch (n new tokens)."""
     nb, _, bs, _ = k_pool.shape
     _check("gqa_decode_step_paged", lib.gqa_decode_step_paged(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
-        _ptr(seq_lens), int(b), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out),
-        int(bs), int(block_table.shape[1]), int(nb), _dtype(q, dtype), int(flags),
+        _ptr(seq_lens), int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale),
+        _ptr(out), int(bs), int(block_table.shape[1]), int(nb), _dtype(q, dtype), int(flags),
         _stream(stream)))
 
 

@@ -95,7 +95,6 @@ struct TcCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
   static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
-  static_assert(!(MULTI && PAGED), "the paged cache takes one new token per step");
 };
 
 // barrier slots
@@ -447,7 +446,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       // paged cache (one token): the physical row of position L_i - 1, or -1
       // for a bad table entry (then nothing is written)
       long long prow = -1;
-      if (PAGED && nchunk > 0) {
+      if (PAGED && !MULTI && nchunk > 0) {
         const int blk = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + (seg.L - 1) / bsz);
         if (blk >= 0 && blk < num_blocks)
           prow = (static_cast<long long>(blk) * g + seg.j) * bsz + (seg.L - 1) % bsz;
@@ -478,10 +477,18 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
-        if (!PAGED)
+        if (!PAGED) {
           cache[(unit * cap + pos) * 16 + ch] = v;
-        else if (prow >= 0)
-          cache[prow * 16 + ch] = v;
+        } else if (!MULTI) {
+          if (prow >= 0) cache[prow * 16 + ch] = v;
+        } else {
+          // n new rows: each through its own block-table entry
+          const int blk = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + pos / bsz);
+          if (blk >= 0 && blk < num_blocks)
+            cache[((static_cast<long long>(blk) * g + seg.j) * bsz + pos % bsz) * 16 + ch] = v;
+          else
+            atomicOr(status, GQA_DEV_BAD_BLOCK);
+        }
       };
       // patch the new rows that fall in tile lt (K or V half of the stage)
       auto patch = [&](uint32_t tile_base, uint4* cache, const uint4* src, const uint4* regs,
@@ -980,8 +987,9 @@ int tc_ctas_per_sm(int) { return 1; }
 cudaError_t launch_decode_tc(const DecodeLaunch& a) {
   const int cols = a.nq * (a.h / a.g);
   if (a.block_table != nullptr) {
-    if (a.nq != 1) return cudaErrorInvalidValue;  // (the ABI rejects it first)
-    return cols <= 16 ? launch_np<16, 1, false, true>(a) : launch_np<32, 2, false, true>(a);
+    if (a.nq == 1)
+      return cols <= 16 ? launch_np<16, 1, false, true>(a) : launch_np<32, 2, false, true>(a);
+    return cols <= 16 ? launch_np<16, 1, true, true>(a) : launch_np<32, 2, true, true>(a);
   }
   if (a.nq == 1)
     return cols <= 16 ? launch_np<16, 1, false, false>(a) : launch_np<32, 2, false, false>(a);

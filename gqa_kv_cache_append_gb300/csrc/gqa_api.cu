@@ -63,28 +63,30 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k_new, const uint4* _
 __global__ void kv_append_paged_kernel(const uint4* __restrict__ k_new,
                                        const uint4* __restrict__ v_new, uint4* __restrict__ k_pool,
                                        uint4* __restrict__ v_pool, const int* __restrict__ table,
-                                       const int* __restrict__ lens, int b, int g, int ck, int cv,
-                                       int bsz, int max_blocks, int num_blocks,
+                                       const int* __restrict__ lens, int b, int nq, int g, int ck,
+                                       int cv, int bsz, int max_blocks, int num_blocks,
                                        unsigned int* status) {
   const long long per = ck + cv;
-  const long long total = static_cast<long long>(b) * g * per;
+  const long long total = static_cast<long long>(b) * nq * g * per;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= total) return;
-  const long long row = idx / per;  // (i, j) row of k_new / v_new
+  const long long row = idx / per;  // (i, s, j) row of k_new / v_new
   const int c = static_cast<int>(idx % per);
   const int j = static_cast<int>(row % g);
-  const int i = static_cast<int>(row / g);
+  const int s = static_cast<int>((row / g) % nq);
+  const int i = static_cast<int>(row / (static_cast<long long>(g) * nq));
   const int L = __ldg(lens + i);
-  if (L < 1 || L > static_cast<long long>(max_blocks) * bsz) {
+  if (L < 1 || L < nq || L > static_cast<long long>(max_blocks) * bsz) {
     if (c == 0) atomicOr(status, GQA_DEV_BAD_SEQ_LEN);
     return;
   }
-  const int blk = __ldg(table + static_cast<size_t>(i) * max_blocks + (L - 1) / bsz);
+  const int p = L - nq + s;  // this row's position
+  const int blk = __ldg(table + static_cast<size_t>(i) * max_blocks + p / bsz);
   if (blk < 0 || blk >= num_blocks) {
     if (c == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
     return;
   }
-  const long long dst_row = (static_cast<long long>(blk) * g + j) * bsz + (L - 1) % bsz;
+  const long long dst_row = (static_cast<long long>(blk) * g + j) * bsz + p % bsz;
   if (c < ck) {
     k_pool[dst_row * ck + c] = __ldg(k_new + row * ck + c);
   } else {
@@ -399,7 +401,7 @@ int elt_bytes(int dtype) { return dtype == GQA_F32 ? 4 : 2; }
 
 // Host checks of the paged-cache arguments (a decode_check follows).
 int paged_check(const int32_t* block_table, int g, int block_size, int max_blocks,
-                int num_blocks, int nq) {
+                int num_blocks) {
   if (!block_table) return GQA_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(block_table) & 3u) return GQA_ERR_ALIGN;
   if (block_size < 1 || max_blocks < 1 || num_blocks < 1 || g < 1) return GQA_ERR_SHAPE;
@@ -410,7 +412,6 @@ int paged_check(const int32_t* block_table, int g, int block_size, int max_block
   // whole number of blocks
   if (block_size < 16 || (block_size & (block_size - 1)) != 0 || block_size > 65536)
     return GQA_ERR_UNSUPPORTED;
-  if (nq != 1) return GQA_ERR_UNSUPPORTED;
   return GQA_OK;
 }
 
@@ -510,13 +511,15 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_c
 }
 
 int gqa_kv_append_paged(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
-                        const int32_t* block_table, const int32_t* seq_lens, int b, int g,
+                        const int32_t* block_table, const int32_t* seq_lens, int b, int n, int g,
                         int d_k, int d_v, int block_size, int max_blocks, int num_blocks,
                         int dtype, void* stream) {
   if (!k_new || !v_new || !k_pool || !v_pool || !seq_lens) return GQA_ERR_NULL;
   if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
-  if (b < 1 || d_k < 1 || d_v < 1) return GQA_ERR_SHAPE;
-  if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks, 1)) return e;
+  if (b < 1 || n < 1 || d_k < 1 || d_v < 1) return GQA_ERR_SHAPE;
+  if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks)) return e;
+  if (static_cast<long long>(n) > static_cast<long long>(max_blocks) * block_size)
+    return GQA_ERR_SHAPE;
   const int elt = elt_bytes(dtype);
   if ((d_k * elt) % 16 != 0 || (d_v * elt) % 16 != 0) return GQA_ERR_UNSUPPORTED;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
@@ -525,15 +528,15 @@ int gqa_kv_append_paged(const void* k_new, const void* v_new, void* k_pool, void
   DeviceInfo* di = nullptr;
   if (int e = device_info(&di)) return e;
   const int ck = d_k * elt / 16, cv = d_v * elt / 16;
-  const long long total = static_cast<long long>(b) * g * (ck + cv);
+  const long long total = static_cast<long long>(b) * n * g * (ck + cv);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   if (blocks > 0x7FFFFFFFll) return GQA_ERR_SHAPE;
   kv_append_paged_kernel<<<static_cast<unsigned>(blocks), threads, 0,
                            static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, seq_lens, b, g, ck,
-      cv, block_size, max_blocks, num_blocks, di->status);
+      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), block_table, seq_lens, b, n, g,
+      ck, cv, block_size, max_blocks, num_blocks, di->status);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -703,12 +706,12 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new, v
 
 static int decode_paged(const void* q, const void* k_new, const void* v_new, const void* k_pool,
                         const void* v_pool, const int32_t* block_table, const int32_t* seq_lens,
-                        int b, int h, int g, int d_k, int d_v, float scale, void* out,
+                        int b, int n, int h, int g, int d_k, int d_v, float scale, void* out,
                         int block_size, int max_blocks, int num_blocks, int dtype, int flags,
                         void* stream) {
   using namespace gqa;
-  if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks, 1)) return e;
-  DecodeArgs x{q, k_new, v_new, k_pool, v_pool, seq_lens, b, 1, h, g, d_k, d_v, scale, out,
+  if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks)) return e;
+  DecodeArgs x{q, k_new, v_new, k_pool, v_pool, seq_lens, b, n, h, g, d_k, d_v, scale, out,
                max_blocks * block_size, dtype, flags};
   x.block_table = block_table;
   x.block_size = block_size;
@@ -726,21 +729,21 @@ static int decode_paged(const void* q, const void* k_new, const void* v_new, con
 }
 
 int gqa_decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
-                          const int32_t* block_table, const int32_t* seq_lens, int b, int h,
-                          int g, int d_k, int d_v, float scale, void* out, int block_size,
+                          const int32_t* block_table, const int32_t* seq_lens, int b, int n,
+                          int h, int g, int d_k, int d_v, float scale, void* out, int block_size,
                           int max_blocks, int num_blocks, int dtype, void* stream) {
-  return decode_paged(q, nullptr, nullptr, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k,
-                      d_v, scale, out, block_size, max_blocks, num_blocks, dtype, 0, stream);
+  return decode_paged(q, nullptr, nullptr, k_pool, v_pool, block_table, seq_lens, b, n, h, g,
+                      d_k, d_v, scale, out, block_size, max_blocks, num_blocks, dtype, 0, stream);
 }
 
 int gqa_decode_step_paged(const void* q, const void* k_new, const void* v_new, void* k_pool,
                           void* v_pool, const int32_t* block_table, const int32_t* seq_lens,
-                          int b, int h, int g, int d_k, int d_v, float scale, void* out,
+                          int b, int n, int h, int g, int d_k, int d_v, float scale, void* out,
                           int block_size, int max_blocks, int num_blocks, int dtype, int flags,
                           void* stream) {
   if (!k_new || !v_new) return GQA_ERR_NULL;
-  return decode_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k, d_v,
-                      scale, out, block_size, max_blocks, num_blocks, dtype, flags, stream);
+  return decode_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, n, h, g, d_k,
+                      d_v, scale, out, block_size, max_blocks, num_blocks, dtype, flags, stream);
 }
 
 int gqa_device_status(void* stream, uint32_t* bits_out) {

@@ -230,27 +230,29 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new,
  * [0, num_blocks) is a device-side error: GQA_DEV_BAD_BLOCK is set, nothing
  * is written through it, and that sequence's output is unspecified (no
  * access leaves the pools).  block_size: a power of two in [16, 65536]
- * (GQA_ERR_UNSUPPORTED otherwise).  One new token per step.  Kernels and
- * limits otherwise as for the contiguous calls; with GQA_STEP_EARLY_STREAM
- * the kernels ahead must not write the block table either.
+ * (GQA_ERR_UNSUPPORTED otherwise).  n new tokens per sequence (n = 1: one
+ * token; n > 1: the causal n-token step of gqa_decode_*_multi, with q / out
+ * [b, n, h, d] and k_new / v_new [b, n, g, d]).  Kernels and limits
+ * otherwise as for the contiguous calls; with GQA_STEP_EARLY_STREAM the
+ * kernels ahead must not write the block table either.
  *
- * gqa_kv_append_paged   - the append of gqa_kv_append into the pools.
- * gqa_decode_attn_paged - the attention of gqa_decode_attn over the pools.
+ * gqa_kv_append_paged   - the append of gqa_kv_append(_multi) into the pools.
+ * gqa_decode_attn_paged - the attention of gqa_decode_attn(_multi) over the pools.
  * gqa_decode_step_paged - append and attention in one launch.
  */
 int gqa_kv_append_paged(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
-                        const int32_t* block_table, const int32_t* seq_lens, int b, int g,
-                        int d_k, int d_v, int block_size, int max_blocks, int num_blocks,
+                        const int32_t* block_table, const int32_t* seq_lens, int b, int n,
+                        int g, int d_k, int d_v, int block_size, int max_blocks, int num_blocks,
                         int dtype, void* stream);
 
 int gqa_decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
-                          const int32_t* block_table, const int32_t* seq_lens, int b, int h,
-                          int g, int d_k, int d_v, float scale, void* out, int block_size,
+                          const int32_t* block_table, const int32_t* seq_lens, int b, int n,
+                          int h, int g, int d_k, int d_v, float scale, void* out, int block_size,
                           int max_blocks, int num_blocks, int dtype, void* stream);
 
 int gqa_decode_step_paged(const void* q, const void* k_new, const void* v_new, void* k_pool,
                           void* v_pool, const int32_t* block_table, const int32_t* seq_lens,
-                          int b, int h, int g, int d_k, int d_v, float scale, void* out,
+                          int b, int n, int h, int g, int d_k, int d_v, float scale, void* out,
                           int block_size, int max_blocks, int num_blocks, int dtype, int flags,
                           void* stream);
 

@@ -26,4 +26,6 @@ from .oracle import (  # noqa: F401
     gather_paged,
     kv_append_paged,
     decode_step_paged,
+    kv_append_paged_multi,
+    decode_step_paged_multi,
 )

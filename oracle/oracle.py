@@ -66,6 +66,8 @@ __all__ = [
     "gather_paged",
     "kv_append_paged",
     "decode_step_paged",
+    "kv_append_paged_multi",
+    "decode_step_paged_multi",
 ]
 
 
@@ -395,6 +397,39 @@ def kv_append_paged(k_pool, v_pool, k_new, v_new, block_table, seq_lens, block_s
             kp[blk, j, r, :] = k_new[i, j, :]
             vp[blk, j, r, :] = v_new[i, j, :]
     return kp, vp
+
+
+def kv_append_paged_multi(k_pool, v_pool, k_new, v_new, block_table, seq_lens,
+                          block_size: int):
+    """n new rows per (sequence, KV head): token s goes to position
+    L_i - n + s, i.e. row (L_i - n + s) mod B of block
+    block_table[i, (L_i - n + s) div B]; k_new / v_new [b, n, g, d]."""
+    kp = np.array(k_pool, copy=True)
+    vp = np.array(v_pool, copy=True)
+    lens = _check_paged(kp, block_table, seq_lens, block_size)
+    bt = np.asarray(block_table)
+    n = np.asarray(k_new).shape[1]
+    if np.any(lens < n):
+        raise ValueError("every seq_len must be at least the number of new tokens")
+    for i in range(bt.shape[0]):
+        for s_ in range(n):
+            p = int(lens[i]) - n + s_
+            blk, r = bt[i, p // block_size], p % block_size
+            for j in range(kp.shape[1]):
+                kp[blk, j, r, :] = k_new[i, s_, j, :]
+                vp[blk, j, r, :] = v_new[i, s_, j, :]
+    return kp, vp
+
+
+def decode_step_paged_multi(q, k_pool, v_pool, k_new, v_new, block_table, seq_lens, g: int,
+                            scale: float, block_size: int, dtype: str = "f64"):
+    """The n-token causal step (decode_step_multi) on a paged cache."""
+    kp, vp = kv_append_paged_multi(k_pool, v_pool, k_new, v_new, block_table, seq_lens,
+                                   block_size)
+    kc = gather_paged(kp, block_table, seq_lens, block_size)
+    vc = gather_paged(vp, block_table, seq_lens, block_size)
+    o = grouped_decode_attention_multi(q, kc, vc, seq_lens, g, scale, dtype)
+    return o, kp, vp
 
 
 def decode_step_paged(q, k_pool, v_pool, k_new, v_new, block_table, seq_lens, g: int,

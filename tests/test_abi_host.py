@@ -207,8 +207,9 @@ def test_projection_and_layer_host_checks():
 def test_paged_host_checks():
     b = _lib()
     f = b.lib.gqa_decode_attn_paged
-    # q, kp, vp, table, lens, b, h, g, dk, dv, scale, out, bs, max_blocks, num_blocks, dtype, stream
-    args = [A, A, A, A, A, 2, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, None]
+    # q, kp, vp, table, lens, b, n, h, g, dk, dv, scale, out, bs, max_blocks, num_blocks, dtype,
+    # stream
+    args = [A, A, A, A, A, 2, 1, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, None]
 
     def call(fn, base, **idx):
         a = list(base)
@@ -217,16 +218,19 @@ def test_paged_host_checks():
         return fn(*a)
     assert call(f, args, i3=0) == -1                  # table null
     assert call(f, args, i3=A + 2) == -4              # table misaligned
-    assert call(f, args, i12=24) == -5                # block size not a power of two
-    assert call(f, args, i12=8) == -5                 # below 16
-    assert call(f, args, i13=0) == -2
+    assert call(f, args, i13=24) == -5                # block size not a power of two
+    assert call(f, args, i13=8) == -5                 # below 16
     assert call(f, args, i14=0) == -2
-    assert call(f, args, i15=4) == -3
+    assert call(f, args, i15=0) == -2
+    assert call(f, args, i16=4) == -3
+    assert call(f, args, i6=0) == -2                  # n < 1
+    assert call(f, args, i6=9) == -5                  # 9 tokens x 4 heads > 32 rows
     st = b.lib.gqa_decode_step_paged
-    sargs = [A, A, A, A, A, A, A, 2, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, 0, None]
+    sargs = [A, A, A, A, A, A, A, 2, 1, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, 0, None]
     assert call(st, sargs, i1=0) == -1
-    assert call(st, sargs, i18=2) == -5               # unknown flag
+    assert call(st, sargs, i19=2) == -5               # unknown flag
     ap = b.lib.gqa_kv_append_paged
-    aargs = [A, A, A, A, A, A, 2, 2, 128, 128, 64, 4, 16, 1, None]
+    aargs = [A, A, A, A, A, A, 2, 1, 2, 128, 128, 64, 4, 16, 1, None]
     assert call(ap, aargs, i4=0) == -1
-    assert call(ap, aargs, i10=48) == -5
+    assert call(ap, aargs, i11=48) == -5
+    assert call(ap, aargs, i7=0) == -2

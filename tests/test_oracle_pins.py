@@ -575,3 +575,20 @@ def test_paged_rejects_bad_tables():
         oracle.gather_paged(kp, np.array([[0, 9]]), [3], 2)      # block 9 outside the pool
     with pytest.raises(ValueError):
         oracle.gather_paged(kp, np.array([[0, 1]]), [5], 2)      # length beyond the table
+
+
+@pytest.mark.parametrize("bs,n", [(4, 3), (2, 5), (8, 1)])
+def test_paged_multi_step_equals_the_contiguous_multi_step(bs, n):
+    rng = np.random.default_rng(950 + bs * n)
+    b, h, g, d, max_blocks = 3, 4, 2, 5, 4
+    lens = [n, bs * max_blocks, n + bs]
+    table, kc, vc, kp, vp = _paged_case(rng, b, g, d, bs, max_blocks, lens)
+    q = rng.standard_normal((b, n, h, d))
+    kn = rng.standard_normal((b, n, g, d))
+    vn = rng.standard_normal((b, n, g, d))
+    o1, kp2, _ = oracle.decode_step_paged_multi(q, kp, vp, kn, vn, table, lens, g, 0.6, bs)
+    o2, kc2, _ = oracle.decode_step_multi(q, kc, vc, kn, vn, lens, g, 0.6)
+    assert np.max(np.abs(o1 - o2)) < TOL
+    got = oracle.gather_paged(kp2, table, lens, bs)
+    for i, L in enumerate(lens):
+        assert np.array_equal(got[i, :, :L], kc2[i, :, :L])

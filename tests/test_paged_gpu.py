@@ -8,7 +8,8 @@ table would show).  Cases: block sizes 16..256 on the tensor-core kernel
 kernel (fp32 and bf16), ragged lengths at block and tile edges, units split
 across CTAs (merged in the decode kernel and in the combine kernel), the
 fused step against the two calls and against the contiguous cache (same
-bits), and a bad table entry."""
+bits), a bad table entry, and steps with n new tokens (the causal n-token
+step through the table)."""
 import math
 
 import numpy as np
@@ -139,3 +140,38 @@ def test_bad_block_entry_is_reported(dtype, d):
     # sequence 0's append landed; sequence 1's (through the bad entry) did not
     got = to_np(kp_d)[0]
     assert got.tobytes() == kp2.tobytes()
+
+
+@pytest.mark.parametrize("dtype,d,b,n,h,g,cap,lens,bs", [
+    ("bf16", 128, 3, 4, 16, 2, 512, [4, 130, 512], 16),       # new rows straddle blocks/tiles
+    ("bf16", 128, 2, 4, 64, 8, 1024, [1024, 257], 64),        # 32 query rows per KV head
+    ("bf16", 128, 1, 4, 8, 1, 16384, [99 * 128 + 2], 128),    # combine kernel, unseen tiles
+    ("f32", 64, 3, 3, 8, 2, 256, [3, 65, 256], 16),           # CUDA-core kernel
+])
+@pytest.mark.parametrize("fused", [True, False])
+def test_paged_multi_token(dtype, d, b, n, h, g, cap, lens, bs, fused):
+    from gqa_kv_cache_append_gb300.inputs import make_layer_multi
+    B = _b()
+    cfg = cfg_of(dtype, b, h, g, d, cap, seed=n + bs)
+    lens = np.asarray(lens, dtype=np.int32)
+    x = make_layer_multi(cfg, n, 0, "cpu", lens=lens)
+    kp, vp, table = to_paged(x["k_cache"], x["v_cache"], bs, seed=cfg.seed, fill=float("nan"))
+    dd = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    kp_d, vp_d, t_d = kp.cuda(), vp.cuda(), table.cuda()
+    out = torch.full((b, n, h, d), 3.0, dtype=cfg.torch_dtype, device="cuda")
+    if fused:
+        B.gqa_decode_step_paged(dd["q"], dd["k_new"], dd["v_new"], kp_d, vp_d, t_d,
+                                dd["seq_lens"], b, h, g, d, d, cfg.scale, out, n=n)
+    else:
+        B.gqa_kv_append_paged(dd["k_new"], dd["v_new"], kp_d, vp_d, t_d, dd["seq_lens"], b, g, d,
+                              d, n=n)
+        B.gqa_decode_attn_paged(dd["q"], kp_d, vp_d, t_d, dd["seq_lens"], b, h, g, d, d,
+                                cfg.scale, out, n=n)
+    assert B.gqa_device_status() == 0
+    tag = to_np(x["q"])[1]
+    ref, kp2, vp2 = oracle.decode_step_paged_multi(
+        to_np(x["q"])[0], to_np(kp)[0], to_np(vp)[0], to_np(x["k_new"])[0], to_np(x["v_new"])[0],
+        table.numpy(), lens, g, cfg.scale, bs, dtype=tag)
+    assert to_np(kp_d)[0].tobytes() == kp2.tobytes()
+    assert to_np(vp_d)[0].tobytes() == vp2.tobytes()
+    assert_close(oracle.widen(to_np(out)[0], tag), ref, tag, f"paged n={n} bs={bs}")
