@@ -403,6 +403,47 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize(dev)
     iso_ms = max_over_ranks(dist, float(np.mean([e[0].elapsed_time(e[1])
                                                  for per in evs for e in per])))
+    # ---- per-step spread: the same steps with an event between steps ----
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sev[0].record(stream)
+    for k in range(args.steps):
+        run_step()
+        sev[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    step_times = [sev[k].elapsed_time(sev[k + 1]) for k in range(args.steps)]
+    # ---- the append and the attention as separate calls (the one-token,
+    # contiguous, projection-free step): each timed over all layers ----
+    split = None
+    if n == 1 and not paged and not full_layer:
+        def timed(fn):
+            for _ in range(2):
+                for l, x in enumerate(layers):
+                    fn(l, x)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                for l, x in enumerate(layers):
+                    fn(l, x)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1) / (args.steps * cfg.layers)
+
+        app_ms = timed(lambda l, x: B.gqa_kv_append(
+            x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.g,
+            cfg.d, cfg.d, stream=stream))
+        att_ms = timed(lambda l, x: B.gqa_decode_attn(
+            x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d,
+            cfg.scale, outs[l], stream=stream))
+        split = {
+            "append_us_per_call": round(app_ms * 1000, 3),
+            "append_bytes_per_call": sb["append_per_layer"],
+            "attn_only_us_per_call": round(att_ms * 1000, 3),
+            "attn_only_gbs": round(sb["attn_per_layer"] / (att_ms * 1e-3) / 1e9, 2),
+            "attn_only_frac_of_measured": None,  # filled below
+            "how": "gqa_kv_append alone and gqa_decode_attn alone, each back to back over all "
+                   "layers (no early streaming)",
+        }
     status = B.gqa_device_status(stream)
 
     # ---- end to end: every step copies all layers' q, k_new, v_new in from
@@ -508,11 +549,16 @@ def run_ours(args, rank, local_rank, world):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
+        "step_ms_median": round(float(np.median(step_times)), 4),
+        "step_ms_best": round(float(np.min(step_times)), 4),
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_per_step": launches_per_step,
         "clocks": clk,
         "device_status": status,
     }
+    if split is not None:
+        split["attn_only_frac_of_measured"] = round(split["attn_only_gbs"] / peaks["hbm_gbs"], 4)
+        line["separate_calls"] = split
     if full_layer and not args.no_cpu_baseline:
         line["cpu_baseline"] = {"skipped": "the oracle baseline is timed on the step "
                                            "(run without --layer)"}
