@@ -17,6 +17,7 @@ from .build import LIB
 
 GQA_F32 = 0
 GQA_BF16 = 1
+GQA_F16 = 2
 
 GQA_OK = 0
 GQA_ERR_NULL = -1
@@ -107,6 +108,8 @@ def _dtype(x, dtype) -> int:
             return GQA_BF16
         if x.dtype == torch.float32:
             return GQA_F32
+        if x.dtype == torch.float16:
+            return GQA_F16
         return -99  # the library rejects it with GQA_ERR_DTYPE
     raise ValueError("dtype must be given when passing raw pointers")
 

@@ -8,8 +8,8 @@ CUDA path on them.
 Recipe (per layer l of a workload with seed s):
   * a torch.Generator on the target device, seeded with s * 1000 + l, draws
     in this order: the K cache, the V cache, q, k_new, v_new, each N(0, 1)
-    in float32 and then rounded to the storage dtype (bf16 round-to-nearest-
-    even, or kept as fp32);
+    in float32 and then rounded to the storage dtype (bf16 or fp16 round-to-
+    nearest-even, or kept as fp32);
   * 'meanpool' workloads first draw an h-head (MHA) K/V cache, k_new and
     v_new, then average every contiguous block of h/g heads in float32 before
     the rounding (the MHA -> GQA conversion by group mean, from the GQA
@@ -60,7 +60,7 @@ class DecodeConfig:
     g: int
     d: int
     cap: int
-    dtype: str                 # 'bf16' or 'f32'
+    dtype: str                 # 'bf16', 'f16' or 'f32'
     scale: float
     seed: int
     kind: str = "plain"        # 'plain' | 'meanpool' | 'boost'
@@ -79,11 +79,11 @@ class DecodeConfig:
 
     @property
     def elt(self) -> int:
-        return 2 if self.dtype == "bf16" else 4
+        return 4 if self.dtype == "f32" else 2
 
     @property
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[self.dtype]
 
 
 _S128 = 1.0 / math.sqrt(128.0)
@@ -181,7 +181,7 @@ def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
         k_new = _pool(_randn((b, h, d), gen, device), g).to(dt)
         v_new = _pool(_randn((b, h, d), gen, device), g).to(dt)
     elif cfg.kind in ("plain", "boost"):
-        if cfg.kind == "plain" and dt == torch.bfloat16:
+        if cfg.kind == "plain" and dt != torch.float32:
             # draw and round block by block to bound the float32 temporary
             k_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
             v_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)

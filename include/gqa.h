@@ -30,8 +30,10 @@
  *     all layers).  A value outside [1, cap] is a device-side error: the call
  *     skips that sequence (writes nothing for it) and sets
  *     GQA_DEV_BAD_SEQ_LEN in the device status word.
- *   - dtype is GQA_F32 or GQA_BF16 and applies to every tensor of the call
- *     (q, caches, new rows, out).  Arithmetic is fp32 for both.
+ *   - dtype is GQA_F32, GQA_BF16 or GQA_F16 and applies to every tensor of
+ *     the call (q, caches, new rows, out).  Arithmetic is fp32 for all (the
+ *     16-bit types feed the tensor cores as they are, with fp32 accumulation;
+ *     the softmax weights are rounded to the same 16-bit type for P.V).
  *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call is asynchronous on it: arguments the host can check are checked
  *     before any launch and reported by the return code; errors only the
@@ -58,13 +60,14 @@ extern "C" {
 /* element types (the `dtype` argument) */
 #define GQA_F32  0
 #define GQA_BF16 1
+#define GQA_F16  2   /* IEEE half */
 
 /* return codes */
 #define GQA_OK               0
 #define GQA_ERR_NULL        -1  /* a required pointer is NULL */
 #define GQA_ERR_SHAPE       -2  /* b, h, g, d_k, d_v < 1; cap < 1; h % g != 0;
                                    sizes whose index range exceeds int32 */
-#define GQA_ERR_DTYPE       -3  /* dtype is neither GQA_F32 nor GQA_BF16 */
+#define GQA_ERR_DTYPE       -3  /* dtype is not GQA_F32, GQA_BF16 or GQA_F16 */
 #define GQA_ERR_ALIGN       -4  /* a tensor pointer is not 16-byte aligned */
 #define GQA_ERR_UNSUPPORTED -5  /* a shape this build has no kernel for
                                    (d_k != d_v, head dim not 64/128, too many

@@ -89,10 +89,16 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def widen(x, dtype: str) -> np.ndarray:
-    """Return ``x`` as float64.  ``dtype`` is 'f32' (x holds float32 values)
-    or 'bf16' (x holds uint16 bit patterns)."""
+    """Return ``x`` as float64.  ``dtype`` is 'f32' (x holds float32 values),
+    'f16' (float16 values) or 'bf16' (x holds uint16 bit patterns); every
+    widening is exact."""
     if dtype == "bf16":
         return bf16_bits_to_f64(x)
+    if dtype == "f16":
+        a = np.asarray(x)
+        if a.dtype != np.float16:
+            raise TypeError("f16 input must be a float16 array")
+        return a.astype(np.float64)
     if dtype == "f32":
         a = np.asarray(x)
         if a.dtype != np.float32:
@@ -284,8 +290,8 @@ def decode_step_multi(q, k_cache, v_cache, k_new, v_new, seq_lens, g: int,
 def to_storage(a64, dtype: str):
     """Round float64 values to the storage encoding named by ``dtype``:
     'bf16' -> uint16 bit patterns of the round-to-nearest-even bfloat16,
-    'f32' -> float32 (numpy's conversion rounds to nearest even), 'f64' ->
-    unchanged.  The bf16 rounding keeps 8 significant bits of the float64
+    'f32' -> float32 and 'f16' -> float16 (numpy's conversions round to
+    nearest even), 'f64' -> unchanged.  The bf16 rounding keeps 8 significant bits of the float64
     value directly (no intermediate float32); it is exact for magnitudes in
     the normal bfloat16 range [2^-126, 2^128) and for 0."""
     a = np.asarray(a64, dtype=np.float64)
@@ -293,6 +299,8 @@ def to_storage(a64, dtype: str):
         return a.copy()
     if dtype == "f32":
         return a.astype(np.float32)
+    if dtype == "f16":
+        return a.astype(np.float16)
     if dtype != "bf16":
         raise ValueError(f"unknown dtype {dtype!r}")
     m, e = np.frexp(a)                       # a = m * 2^e, 0.5 <= |m| < 1

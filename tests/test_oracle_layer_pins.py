@@ -210,3 +210,20 @@ def test_pins_catch_an_output_projection_over_the_wrong_axis(monkeypatch):
                             "bhv,hdv->bd", orc.widen(o, dtype)[:, ::-1], orc.widen(P_o, dtype)))
     with pytest.raises(AssertionError):
         test_layer_bruteforce_loops()
+
+
+def test_f16_rounding_matches_torch_and_nearest_even():
+    rng = np.random.default_rng(8)
+    f = (rng.standard_normal(20000) * 10.0 ** rng.integers(-3, 4, 20000)).astype(np.float32)
+    want = torch.from_numpy(f.copy()).to(torch.float16).numpy()
+    got = oracle.to_storage(f.astype(np.float64), "f16")
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+    # float64 values between float16 neighbours: nearest, ties to even
+    a = rng.standard_normal(5000) * 3.0
+    h = oracle.to_storage(a, "f16")
+    bits = h.view(np.uint16).astype(np.int32)
+    up = (bits + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    dn = (bits - 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    err = np.abs(a - h.astype(np.float64))
+    assert np.all(err <= np.abs(a - up)) and np.all(err <= np.abs(a - dn))
+    assert np.array_equal(oracle.widen(h, "f16"), h.astype(np.float64))
