@@ -268,6 +268,8 @@ def run_ours(args, rank, local_rank, world):
         base = dataclasses.replace(base, cap=args.cap)
     if args.layers:
         base = dataclasses.replace(base, layers=min(args.layers, base.layers))
+    if args.dtype:
+        base = dataclasses.replace(base, dtype=args.dtype)
     if n > 1:
         # n new tokens per step: the workload's shapes with plain N(0, 1) data
         base = dataclasses.replace(base, kind="plain")
@@ -637,6 +639,8 @@ def main(argv=None):
     ap.add_argument("--layer", action="store_true",
                     help="time the whole incremental layer (q/k/v projection, step, output "
                          "projection) through gqa_decode_layer")
+    ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default=None,
+                    help="storage type override (shape studies)")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK",
                     help="paged KV cache with this block size (rows per block)")
     ap.add_argument("--layers", type=int, default=None,

@@ -1,5 +1,5 @@
-// decode_simt.cu - CUDA-core split-KV decode attention (fp32 inputs, and bf16
-// with head dim 64).
+// decode_simt.cu - CUDA-core split-KV decode attention (fp32 inputs, and the
+// 16-bit types with head dim 64 or with different K and V head dims).
 //
 // One persistent CTA per SM streams its share of the (sequence, KV head)
 // tiles (see Walker).  Warp 0 copies each K/V tile of T positions from HBM
@@ -59,6 +59,20 @@ struct Elt<__nv_bfloat16> {
     }
   }
   __device__ static void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+template <>
+struct Elt<__half> {
+  static constexpr int size = 2;
+  __device__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+      f[2 * k] = v.x;
+      f[2 * k + 1] = v.y;
+    }
+  }
+  __device__ static void store(__half* p, float v) { *p = __float2half_rn(v); }
 };
 
 // DK / DV: head dims of K (and q) and of V (and out); they may differ.
@@ -531,7 +545,7 @@ cudaError_t launch_t(const DecodeLaunch& a) {
 bool simt_supported(int dtype, int d_k, int d_v, int cols) {
   const bool dims = (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128);
   if (dtype == GQA_F32) return dims && cols >= 1 && cols <= 16;
-  if (dtype == GQA_BF16) return dims && cols >= 1 && cols <= 8;
+  if (dtype == GQA_BF16 || dtype == GQA_F16) return dims && cols >= 1 && cols <= 8;
   return false;
 }
 
@@ -558,6 +572,7 @@ cudaError_t launch_dtype(const DecodeLaunch& a, int r) {
 cudaError_t launch_decode_simt(const DecodeLaunch& a) {
   const int r = a.nq * (a.h / a.g);  // query rows per KV head
   if (a.dtype == GQA_F32) return launch_dtype<float>(a, r);
+  if (a.dtype == GQA_F16) return launch_dtype<__half>(a, r);
   return launch_dtype<__nv_bfloat16>(a, r);
 }
 

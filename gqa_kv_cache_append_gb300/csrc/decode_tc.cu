@@ -1,5 +1,5 @@
 // decode_tc.cu - tensor-core (tcgen05 + TMEM) split-KV decode attention for
-// bf16 caches with head dim 128.
+// bf16 or fp16 caches with head dim 128.
 //
 // The step of the MQA review §2.4 / §3 per (sequence i, KV head j) tile of
 // T = 128 cached positions, with the r = h/g query heads of the group padded
@@ -64,7 +64,7 @@ constexpr int kPrefetchTiles = 3;
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
 // because the 32-column variant runs at its register limit.
-template <int NP, int NWG, bool MULTI, bool PAGED = false>
+template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true>
 struct TcCfg {
   static constexpr int THREADS = 64 + 128 * NWG;  // producer, MMA, NWG softmax warpgroups
   static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
@@ -86,8 +86,8 @@ struct TcCfg {
   static constexpr int NCOLS = 4 * NP;               // S0 S1 O0 O1
   // P rows are NP * 2 bytes: 32 B (NP=16) or 64 B (NP=32) swizzle atoms
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
-  static constexpr uint32_t IDESC = idesc_bf16(128, NP, 0, 0);     // S: K-major A, B
-  static constexpr uint32_t IDESC_O = idesc_bf16(128, NP, 1, 1);   // O: MN-major A, B
+  static constexpr uint32_t IDESC = idesc_bf16(128, NP, 0, 0, BF16);    // S: K-major A, B
+  static constexpr uint32_t IDESC_O = idesc_bf16(128, NP, 1, 1, BF16);  // O: MN-major A, B
   // new-row chunks the MMA warp carries in registers per lane for the fused
   // append (one token: K only, lanes 0-15; n tokens: 4 rows of K and of V);
   // further rows are loaded when patched
@@ -112,19 +112,19 @@ enum {
   B_DRAIN = B_O_FREE + 2,
 };
 
-template <int NP, int NWG, bool MULTI, bool PAGED>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
 __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ lens,
                      int b, int h, int g, int cap, float scale_log2,
-                     __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
+                     T16* __restrict__ out, float* __restrict__ part_o,
                      float* __restrict__ part_ml, int* __restrict__ counters,
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
                      unsigned int* status, long long budget, int early, int nq,
                      const int* __restrict__ table, int bsz, int max_blocks, int num_blocks) {
-  using C = TcCfg<NP, NWG, MULTI, PAGED>;
+  using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   const uint32_t s_base = smem_u32(sm);
@@ -739,9 +739,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             uint32_t wv[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const __nv_bfloat162 pr =
-                  __floats2bfloat162_rn(x[8 * c + 2 * k], x[8 * c + 2 * k + 1]);
-              wv[k] = *reinterpret_cast<const uint32_t*>(&pr);
+              wv[k] = Half16<T16>::pack2(x[8 * c + 2 * k], x[8 * c + 2 * k + 1]);
             }
             const int cg = h0 / 8 + c;  // chunk index within the row
             const int phys = (NP == 16) ? (cg ^ ((row >> 2) & 1)) : (cg ^ ((row >> 1) & 3));
@@ -806,7 +804,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         named_bar_sync(bar_id, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
         // output row of column c: (i * n + s) * h + j * r + t
-        __nv_bfloat16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * kD + row;
+        T16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * kD + row;
         const int u = seg.i * g + seg.j;
         const size_t slot = static_cast<size_t>(u) + blockIdx.x;
         // l[e] becomes the CTA-wide softmax denominator of head h0 + e
@@ -817,7 +815,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 #pragma unroll
           for (int e = 0; e < HP; ++e)
             if (h0 + e < nr)
-              obase[col_off[h0 + e]] = __float2bfloat16_rn(o[e] / l[e]);
+              obase[col_off[h0 + e]] = Half16<T16>::from(o[e] / l[e]);
         } else {
 #pragma unroll
           for (int e = 0; e < HP; ++e) {
@@ -892,7 +890,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 #pragma unroll
             for (int e = 0; e < HP; ++e)
               if (h0 + e < nr)
-                obase[col_off[h0 + e]] = __float2bfloat16_rn(o[e] / l[e]);
+                obase[col_off[h0 + e]] = Half16<T16>::from(o[e] / l[e]);
           }
         }
         m_own = -INFINITY;
@@ -918,34 +916,36 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 // 2-D map over a row-major [rows x 128] bf16 tensor, box [box_rows x 64],
 // 128-byte swizzle, zero fill outside.  (The query map is 3-D:
 // [b * n tokens][h heads][128], box [n][r][64].)
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows, bool bf16) {
   const uint64_t dims[2] = {static_cast<uint64_t>(kD), rows};
   const uint64_t strides[1] = {static_cast<uint64_t>(kD) * 2};
   const uint32_t box[2] = {64u, box_rows};
-  return encode_bf16_map(map, base, 2, dims, strides, box);
+  return encode_bf16_map(map, base, 2, dims, strides, box, bf16);
 }
 
-bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r) {
+bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r, bool bf16) {
   const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(h),
                             static_cast<uint64_t>(b) * nq};
   const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2,
                                static_cast<uint64_t>(h) * kD * 2};
   const uint32_t box[3] = {64u, static_cast<uint32_t>(r), static_cast<uint32_t>(nq)};
-  return encode_bf16_map(map, base, 3, dims, strides, box);
+  return encode_bf16_map(map, base, 3, dims, strides, box, bf16);
 }
 
-template <int NP, int NWG, bool MULTI, bool PAGED>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
 cudaError_t launch_np(const DecodeLaunch& a) {
-  using C = TcCfg<NP, NWG, MULTI, PAGED>;
+  constexpr bool kBf16 = Half16<T16>::kBf16;
+  using C = TcCfg<NP, NWG, MULTI, PAGED, kBf16>;
   CUtensorMap mq, mk, mv;
   // contiguous caches: [b * g * cap rows x 128]; pools: [num_blocks * g * block_size rows]
   const uint64_t kv_rows = PAGED ? static_cast<uint64_t>(a.num_blocks) * a.g * a.block_size
                                  : static_cast<uint64_t>(a.b) * a.g * a.cap;
   const uint32_t box_rows = (PAGED && a.block_size < kT) ? a.block_size : kT;
-  if (!make_q_map(&mq, a.q, a.b, a.nq, a.h, a.h / a.g) ||
-      !make_map(&mk, a.k_cache, kv_rows, box_rows) || !make_map(&mv, a.v_cache, kv_rows, box_rows))
+  if (!make_q_map(&mq, a.q, a.b, a.nq, a.h, a.h / a.g, kBf16) ||
+      !make_map(&mk, a.k_cache, kv_rows, box_rows, kBf16) ||
+      !make_map(&mv, a.v_cache, kv_rows, box_rows, kBf16))
     return cudaErrorInvalidValue;
-  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED>;
+  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16>;
   // the shared-memory opt-in is set once per device (not during a capture)
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -968,16 +968,32 @@ cudaError_t launch_np(const DecodeLaunch& a) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(
       &cfg, kern, mq, mk, mv, a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
-      static_cast<__nv_bfloat16*>(a.out), a.part_o, a.part_ml, a.counters,
+      static_cast<T16*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
       a.early ? 1 : 0, a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks);
 }
 
+template <typename T16>
+cudaError_t launch_type(const DecodeLaunch& a) {
+  const int cols = a.nq * (a.h / a.g);
+  const bool one = a.nq == 1;
+  if (a.block_table != nullptr) {
+    if (one)
+      return cols <= 16 ? launch_np<16, 1, false, true, T16>(a)
+                        : launch_np<32, 2, false, true, T16>(a);
+    return cols <= 16 ? launch_np<16, 1, true, true, T16>(a) : launch_np<32, 2, true, true, T16>(a);
+  }
+  if (one)
+    return cols <= 16 ? launch_np<16, 1, false, false, T16>(a)
+                      : launch_np<32, 2, false, false, T16>(a);
+  return cols <= 16 ? launch_np<16, 1, true, false, T16>(a) : launch_np<32, 2, true, false, T16>(a);
+}
+
 }  // namespace
 
 bool tc_supported(int dtype, int d, int cols) {
-  return dtype == GQA_BF16 && d == kD && cols >= 1 && cols <= 32;
+  return (dtype == GQA_BF16 || dtype == GQA_F16) && d == kD && cols >= 1 && cols <= 32;
 }
 
 int tc_tile() { return kT; }
@@ -985,15 +1001,7 @@ int tc_tile() { return kT; }
 int tc_ctas_per_sm(int) { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeLaunch& a) {
-  const int cols = a.nq * (a.h / a.g);
-  if (a.block_table != nullptr) {
-    if (a.nq == 1)
-      return cols <= 16 ? launch_np<16, 1, false, true>(a) : launch_np<32, 2, false, true>(a);
-    return cols <= 16 ? launch_np<16, 1, true, true>(a) : launch_np<32, 2, true, true>(a);
-  }
-  if (a.nq == 1)
-    return cols <= 16 ? launch_np<16, 1, false, false>(a) : launch_np<32, 2, false, false>(a);
-  return cols <= 16 ? launch_np<16, 1, true, false>(a) : launch_np<32, 2, true, false>(a);
+  return a.dtype == GQA_F16 ? launch_type<__half>(a) : launch_type<__nv_bfloat16>(a);
 }
 
 }  // namespace gqa

@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -225,8 +226,10 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
 #pragma unroll
   for (int e = 0; e < CPL; ++e) {
     const float v = o[e] / dsum;
-    if constexpr (sizeof(DT) == 2)
+    if constexpr (std::is_same<DT, __nv_bfloat16>::value)
       dst[e] = __float2bfloat16_rn(v);
+    else if constexpr (std::is_same<DT, __half>::value)
+      dst[e] = __float2half_rn(v);
     else
       dst[e] = v;
   }
@@ -386,6 +389,12 @@ int launch_all(DecodeLaunch& a, int tile) {
                                            a.b, a.h, a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
                       : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 2>, a.seq_lens,
                                            a.b, a.h, a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
+    } else if (a.dtype == GQA_F16) {
+      auto* o = static_cast<__half*>(a.out);
+      e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__half, 4>, a.seq_lens, a.b, a.h,
+                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
+                      : cudaLaunchKernelEx(&cfg, combine_kernel<__half, 2>, a.seq_lens, a.b, a.h,
+                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
     } else {
       auto* o = static_cast<float*>(a.out);
       e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 4>, a.seq_lens, a.b, a.h,
@@ -437,7 +446,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                     const uint64_t* strides, const uint32_t* box) {
+                     const uint64_t* strides, const uint32_t* box, bool bf16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || rank < 1 || rank > 5) return false;
   cuuint64_t d[5], st[4];
@@ -448,7 +457,8 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_
     es[k] = 1u;
     if (k > 0) st[k - 1] = strides[k - 1];
   }
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+             static_cast<cuuint32_t>(rank),
              const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -481,7 +491,7 @@ int gqa_kv_append_multi(const void* k_new, const void* v_new, void* k_cache, voi
                         const int32_t* seq_lens, int b, int n, int g, int d_k, int d_v, int cap,
                         int dtype, void* stream) {
   if (!k_new || !v_new || !k_cache || !v_cache || !seq_lens) return GQA_ERR_NULL;
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (dtype != GQA_F32 && dtype != GQA_BF16 && dtype != GQA_F16) return GQA_ERR_DTYPE;
   if (b < 1 || n < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || n > cap) return GQA_ERR_SHAPE;
   const int elt = elt_bytes(dtype);
   if ((d_k * elt) % 16 != 0 || (d_v * elt) % 16 != 0) return GQA_ERR_UNSUPPORTED;
@@ -515,7 +525,7 @@ int gqa_kv_append_paged(const void* k_new, const void* v_new, void* k_pool, void
                         int d_k, int d_v, int block_size, int max_blocks, int num_blocks,
                         int dtype, void* stream) {
   if (!k_new || !v_new || !k_pool || !v_pool || !seq_lens) return GQA_ERR_NULL;
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (dtype != GQA_F32 && dtype != GQA_BF16 && dtype != GQA_F16) return GQA_ERR_DTYPE;
   if (b < 1 || n < 1 || d_k < 1 || d_v < 1) return GQA_ERR_SHAPE;
   if (int e = paged_check(block_table, g, block_size, max_blocks, num_blocks)) return e;
   if (static_cast<long long>(n) > static_cast<long long>(max_blocks) * block_size)
@@ -573,7 +583,7 @@ struct DecodePlan {
 int decode_check(const DecodeArgs& x) {
   if (x.flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
   if (!x.q || !x.k_cache || !x.v_cache || !x.seq_lens || !x.out) return GQA_ERR_NULL;
-  if (x.dtype != GQA_F32 && x.dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (x.dtype != GQA_F32 && x.dtype != GQA_BF16 && x.dtype != GQA_F16) return GQA_ERR_DTYPE;
   if (x.b < 1 || x.nq < 1 || x.h < 1 || x.g < 1 || x.d_k < 1 || x.d_v < 1 || x.cap < 1 ||
       x.h % x.g != 0 || x.nq > x.cap)
     return GQA_ERR_SHAPE;
@@ -784,7 +794,7 @@ namespace {
 constexpr int kProjMaxBatch = 128;
 
 int proj_shape_check(int b, int D, int h, int g, int d_k, int d_v, int dtype) {
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (dtype != GQA_F32 && dtype != GQA_BF16 && dtype != GQA_F16) return GQA_ERR_DTYPE;
   if (b < 1 || D < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || h % g != 0)
     return GQA_ERR_SHAPE;
   if (static_cast<long long>(h + 2 * g) * D > 0x7FFFFFFFll ||
@@ -1009,7 +1019,7 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
                                        void* stream) {
   using namespace gqa;
   if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
-  if (dtype != GQA_F32 && dtype != GQA_BF16) return GQA_ERR_DTYPE;
+  if (dtype != GQA_F32 && dtype != GQA_BF16 && dtype != GQA_F16) return GQA_ERR_DTYPE;
   if (b < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0)
     return GQA_ERR_SHAPE;
   if (static_cast<long long>(b) * g * cap + 256 > 0x7FFFFFFFll ||

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/gqa.h"
 
@@ -225,17 +226,40 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
-// A/B K-major (0) or MN-major (1), shape M x N.
+// Instruction descriptor of tcgen05.mma kind::f16: A and B both bf16 (or
+// both fp16 with bf16 = false), fp32 D, A/B K-major (0) or MN-major (1),
+// shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn_major,
-                                                  int b_mn_major) {
-  return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+                                                  int b_mn_major, bool bf16 = true) {
+  return (1u << 4)                                      // D format: f32
+         | (static_cast<uint32_t>(bf16 ? 1 : 0) << 7)   // A format: bf16 (1) or f16 (0)
+         | (static_cast<uint32_t>(bf16 ? 1 : 0) << 10)  // B format: the same
          | (static_cast<uint32_t>(a_mn_major) << 15) |
          (static_cast<uint32_t>(b_mn_major) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
+
+// The two 16-bit storage types of the tensor-core paths.
+template <typename T>
+struct Half16;
+template <>
+struct Half16<__nv_bfloat16> {
+  static constexpr bool kBf16 = true;
+  __device__ static uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  __device__ static __nv_bfloat16 from(float v) { return __float2bfloat16_rn(v); }
+};
+template <>
+struct Half16<__half> {
+  static constexpr bool kBf16 = false;
+  __device__ static uint32_t pack2(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  __device__ static __half from(float v) { return __float2half_rn(v); }
+};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -42,7 +42,7 @@ struct DecodeLaunch {
 // (innermost) extent, strides[k] the byte stride of dimension k + 1, box the
 // copied box; 128-byte swizzle, 256-byte L2 promotion, zero fill outside.
 bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                     const uint64_t* strides, const uint32_t* box);
+                     const uint64_t* strides, const uint32_t* box, bool bf16 = true);
 
 // CUDA-core kernel (fp32 and bf16, d_k and d_v in {64, 128}); `cols` = nq * r
 // query rows per KV head

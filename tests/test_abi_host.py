@@ -72,7 +72,7 @@ def _app(lib_, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=0), -1), (dict(out=0), -1), (dict(lens=0), -1),
-    (dict(dtype=2), -3), (dict(dtype=-1), -3),
+    (dict(dtype=3), -3), (dict(dtype=-1), -3),
     (dict(h=6, g=4), -2), (dict(b=0), -2), (dict(g=0), -2), (dict(cap=0), -2),
     (dict(dk=0), -2), (dict(b=40000, g=8, h=8, cap=8000), -2),
     (dict(q=A + 8), -4), (dict(k=A + 2), -4), (dict(out=A + 4), -4), (dict(lens=A + 2), -4),

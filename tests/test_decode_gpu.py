@@ -302,7 +302,8 @@ def test_error_codes_reach_python():
         B.gqa_decode_attn(q, k, k, lens, 1, 6, 4, 128, 128, 1.0, out)
     assert e.value.code == B.GQA_ERR_SHAPE
     with pytest.raises(B.GqaError) as e:
-        B.gqa_decode_attn(q.half(), k.half(), k.half(), lens, 1, 6, 2, 128, 128, 1.0, out.half())
+        B.gqa_decode_attn(q.double(), k.double(), k.double(), lens, 1, 6, 2, 128, 128, 1.0,
+                          out.double())
     assert e.value.code == B.GQA_ERR_DTYPE
     raw = torch.zeros(1 * 6 * 128 + 8, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(B.GqaError) as e:
