@@ -129,9 +129,9 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache,
  *
  * Rows p >= L_i of the caches are never used in the result, whatever they
  * hold.  fp32 accumulation; bf16 output is rounded to nearest even.
- * Supported: d_k == d_v in {64, 128}; bf16 with d = 128 and h / g <= 32
- * (tensor-core kernel); fp32 with h / g <= 16 and bf16 with d = 64 and
- * h / g <= 8 (CUDA-core kernel).  b <= 65535.
+ * Supported: bf16 / fp16 with d_k = d_v = 128 and h / g <= 32 (tensor-core
+ * kernel); otherwise d_k, d_v in {64, 128} (they may differ) with h / g <= 16
+ * for fp32 and h / g <= 8 for bf16 / fp16 (CUDA-core kernel).  b <= 65535.
  * Returns GQA_OK or an error code (nothing is launched on error).
  */
 int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
