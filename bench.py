@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-cpu-baseline]
 
-One step = every layer of the workload: gqa_kv_append then gqa_decode_attn
+One step = every layer of the workload: gqa_decode_step (the append fused
+into the decode attention; --separate: gqa_kv_append then gqa_decode_attn)
 through the C ABI, on one stream, with all inputs resident in HBM.  Timing:
 W untimed steps, then K steps between a barrier + synchronize on both sides,
 CUDA events on the launching stream, max over ranks.  Prints one JSON line
@@ -493,7 +494,11 @@ def run_ours(args, rank, local_rank, world):
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
     traffic = None if (full_layer or paged) else profiled_traffic(src, args.workload, n)
-    launches_per_step = (3 if full_layer else (2 if args.separate else 1)) * cfg.layers
+    plan = B.gqa_decode_plan(cfg.b, n, cfg.h, cfg.g, cfg.d, cfg.d, cfg.cap, cfg.dtype)
+    # per layer: the decode call's kernels (decode, plus combine when the
+    # split partials are merged apart), + 2 projections or + 1 separate append
+    launches_per_step = (plan["kernels"] + (2 if full_layer else (1 if args.separate else 0))
+                         ) * cfg.layers
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,

@@ -6,8 +6,10 @@ of one of the names below; ``inputs`` holds the seeded synthetic workloads.
 """
 _BINDING = {
     "gqa_kv_append", "gqa_decode_attn", "gqa_decode_step", "gqa_decode_attn_noalloc",
-    "gqa_kv_append_multi", "gqa_decode_attn_multi", "gqa_decode_step_multi", "gqa_device_status",
-    "gqa_kv_append_paged", "gqa_decode_attn_paged", "gqa_decode_step_paged", "gqa_project_qkv", "gqa_project_out", "gqa_decode_layer", "gqa_selftest_wait_timeout", "gqa_version", "decode_step", "GqaError",
+    "gqa_kv_append_multi", "gqa_decode_attn_multi", "gqa_decode_step_multi",
+    "gqa_kv_append_paged", "gqa_decode_attn_paged", "gqa_decode_step_paged",
+    "gqa_project_qkv", "gqa_project_out", "gqa_decode_layer", "gqa_decode_plan",
+    "gqa_device_status", "gqa_selftest_wait_timeout", "gqa_version", "decode_step", "GqaError",
     "status_string",
 }
 

@@ -61,6 +61,9 @@ SIGNATURES = {
                                    _I, _I, _I, _VP]),
     "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
                                    _F, _VP, _I, _I, _I, _I, _I, _VP]),
+    "gqa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
+                             ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
+                             ctypes.POINTER(_LL)]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -270,6 +273,23 @@ def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens
         _ptr(seq_lens), int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale),
         _ptr(out), int(bs), int(block_table.shape[1]), int(nb), _dtype(q, dtype), int(flags),
         _stream(stream)))
+
+
+_DTYPES = {"f32": GQA_F32, "bf16": GQA_BF16, "f16": GQA_F16}
+
+
+def gqa_decode_plan(b, n, h, g, d_k, d_v, cap, dtype, num_sms=0) -> dict:
+    """How a decode call with these shapes runs (host only when num_sms > 0):
+    kernels per call, decode CTAs, positions per tile, tensor-core kernel or
+    not, split workspace bytes.  dtype: GQA_* code or "f32"/"bf16"/"f16"."""
+    dt = _DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    k, c, t, tc = (ctypes.c_int(0) for _ in range(4))
+    ws = ctypes.c_longlong(0)
+    _check("gqa_decode_plan", lib.gqa_decode_plan(
+        int(b), int(n), int(h), int(g), int(d_k), int(d_v), int(cap), dt, int(num_sms),
+        ctypes.byref(k), ctypes.byref(c), ctypes.byref(t), ctypes.byref(tc), ctypes.byref(ws)))
+    return {"kernels": k.value, "ctas": c.value, "tile": t.value, "tensor_core": bool(tc.value),
+            "workspace_bytes": ws.value}
 
 
 def gqa_device_status(stream=None) -> int:

@@ -360,12 +360,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // or more pieces and a merge by the last CTA to finish would serialise many
 // partial reads at the end of the launch: those launches hand the merge to
 // the combine kernel instead (counters = null tells the decode kernel).
-bool use_combine_kernel(const DecodeLaunch& a) {
-  return static_cast<long long>(a.nc) > 2ll * a.b * a.g;
-}
+// Units split over more CTAs than twice the unit count are merged by the
+// combine kernel; fewer splits are merged inside the decode kernel.
+bool use_combine_kernel(long long nc, int b, int g) { return nc > 2ll * b * g; }
 
 int launch_all(DecodeLaunch& a, int tile) {
-  const bool separate = use_combine_kernel(a);
+  const bool separate = use_combine_kernel(a.nc, a.b, a.g);
   if (separate) a.counters = nullptr;
   const bool tc = a.d == a.dv && tc_supported(a.dtype, a.d, a.nq * (a.h / a.g));
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
@@ -712,6 +712,31 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new, v
   if (!k_new || !v_new) return GQA_ERR_NULL;
   return gqa::decode(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v, scale,
                      out, cap, dtype, stream, flags);
+}
+
+int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int dtype,
+                    int num_sms, int* kernels, int* ctas, int* tile, int* tensor_core,
+                    long long* workspace_bytes) {
+  using namespace gqa;
+  // stand-in pointers: only the shapes are checked
+  const void* p = reinterpret_cast<const void*>(uintptr_t(256));
+  DecodeArgs x{p, p, p, p, p, static_cast<const int32_t*>(p), b, n, h, g, d_k, d_v, 1.f,
+               const_cast<void*>(p), cap, dtype, 0};
+  if (int e = decode_check(x)) return e;
+  if (num_sms < 0) return GQA_ERR_SHAPE;
+  if (num_sms == 0) {
+    DeviceInfo* di = nullptr;
+    if (int e = device_info(&di)) return e;
+    num_sms = di->num_sms;
+  }
+  const DecodePlan pl = decode_plan(x, num_sms);
+  if (kernels) *kernels = use_combine_kernel(pl.nc, b, g) ? 2 : 1;
+  if (ctas) *ctas = static_cast<int>(pl.nc);
+  if (tile) *tile = pl.tile;
+  if (tensor_core) *tensor_core = d_k == d_v && tc_supported(dtype, d_k, n * (h / g)) ? 1 : 0;
+  if (workspace_bytes)
+    *workspace_bytes = static_cast<long long>(pl.o_bytes + pl.ml_bytes + pl.units * sizeof(int));
+  return GQA_OK;
 }
 
 static int decode_paged(const void* q, const void* k_new, const void* v_new, const void* k_pool,

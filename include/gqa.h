@@ -350,6 +350,31 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
                             int d_v, float scale, void* out, int cap, int dtype,
                             void* stream);
 
+/*
+ * gqa_decode_plan - how a decode call with these shapes would run, without
+ * running it.  Host only: no launch, no allocation, no device access when
+ * num_sms > 0.
+ *
+ * b, n, h, g, d_k, d_v, cap, dtype: as for gqa_decode_attn_multi (n = 1 for
+ * the one-token calls; for the paged calls cap = max_blocks * block_size).
+ * num_sms: SM count of the target device; 0 = that of the current device
+ * (which then needs a GPU).  Outputs, each optional (NULL = not wanted):
+ *   kernels          kernels one gqa_decode_attn* call launches: 1, or 2 when
+ *                    the units are split over more CTAs than 2*b*g and the
+ *                    split partials are merged by the separate combine
+ *                    kernel (gqa_decode_step* launch the same number; the
+ *                    append is fused)
+ *   ctas             CTAs of the decode kernel (persistent: at most num_sms)
+ *   tile             cache positions per tile
+ *   tensor_core      1 for the tcgen05 kernel, 0 for the CUDA-core kernel
+ *   workspace_bytes  split partials + arrival counters the call uses
+ * Returns the code the decode call would return for these shapes (its
+ * pointer and alignment checks aside), or GQA_ERR_SHAPE for num_sms < 0.
+ */
+int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int dtype,
+                    int num_sms, int* kernels, int* ctas, int* tile, int* tensor_core,
+                    long long* workspace_bytes);
+
 /* Name of a return code, for messages. */
 const char* gqa_status_string(int status);
 

@@ -234,3 +234,35 @@ def test_paged_host_checks():
     assert call(ap, aargs, i4=0) == -1
     assert call(ap, aargs, i11=48) == -5
     assert call(ap, aargs, i7=0) == -2
+
+
+def test_decode_plan_query():
+    """gqa_decode_plan on the host (SM count given): persistent grid of at
+    most one CTA per SM and at most one per tile, the combine kernel exactly
+    when the CTAs outnumber twice the units, the workspace of the partials
+    ((b*g + C) * rows * (d_v + 2) floats) plus 2*b*g counters."""
+    b = _lib()
+    p = b.gqa_decode_plan(32, 1, 64, 8, 128, 128, 8192, "bf16", num_sms=152)
+    assert p["tensor_core"] and p["tile"] == 128 and p["ctas"] == 152 and p["kernels"] == 1
+    assert p["workspace_bytes"] == (32 * 8 + 152) * 8 * 130 * 4 + 2 * 32 * 8 * 4
+    p = b.gqa_decode_plan(8, 1, 32, 1, 128, 128, 131072, "bf16", num_sms=152)
+    assert p["ctas"] == 152 and p["kernels"] == 2
+    p = b.gqa_decode_plan(32, 4, 64, 8, 128, 128, 8192, "f16", num_sms=152)
+    assert p["tensor_core"] and p["kernels"] == 1
+    for (bb, n, h, g, dk, dv, cap, dt) in [(1, 1, 8, 1, 64, 64, 256, "f32"),
+                                           (3, 1, 8, 2, 128, 64, 1000, "bf16"),
+                                           (64, 1, 28, 4, 128, 128, 32768, "bf16"),
+                                           (1, 1, 8, 8, 128, 128, 1, "bf16")]:
+        p = b.gqa_decode_plan(bb, n, h, g, dk, dv, cap, dt, num_sms=152)
+        tiles = bb * g * -(-cap // p["tile"])
+        assert 1 <= p["ctas"] == min(152, tiles)
+        assert p["kernels"] == (2 if p["ctas"] > 2 * bb * g else 1)
+        assert p["tensor_core"] == (dt != "f32" and dk == dv == 128)
+        rows = n * h // g
+        assert p["workspace_bytes"] == ((bb * g + p["ctas"]) * rows * (dv + 2) * 4
+                                        + 2 * bb * g * 4)
+    plan = b.lib.gqa_decode_plan
+    assert plan(2, 1, 8, 3, 128, 128, 64, 1, 152, None, None, None, None, None) == -2
+    assert plan(2, 1, 8, 2, 128, 128, 64, 7, 152, None, None, None, None, None) == -3
+    assert plan(2, 1, 8, 2, 96, 96, 64, 1, 152, None, None, None, None, None) == -5
+    assert plan(2, 1, 8, 2, 128, 128, 64, 1, -1, None, None, None, None, None) == -2
