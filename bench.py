@@ -155,7 +155,7 @@ def smi_id(local_index: int) -> str:
 def step_bytes(cfg, lens, n: int = 1) -> dict:
     from gqa_kv_cache_append_gb300.inputs import layer_bytes
     attn = layer_bytes(cfg, lens, n)
-    append = 2 * 2 * cfg.b * n * cfg.g * cfg.d * cfg.elt   # read + write of the new K/V rows
+    append = 2 * cfg.b * n * cfg.g * (cfg.d + cfg.dv) * cfg.elt  # read + write of the new rows
     return {"attn_per_layer": attn, "append_per_layer": append,
             "step": cfg.layers * (attn + append)}
 
@@ -217,7 +217,7 @@ def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096, n: int = 1
             t = t.contiguous()
             if t.dtype == torch.bfloat16:
                 return t.view(torch.int16).numpy().view(np.uint16), "bf16"
-            return t.numpy(), "f32"
+            return t.numpy(), ("f16" if t.dtype == torch.float16 else "f32")
         tag = np_(x["q"])[1]
         arrs = [np_(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
         t0 = time.perf_counter()
@@ -227,7 +227,7 @@ def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096, n: int = 1
             oracle.decode_step_multi(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
         spent += time.perf_counter() - t0
         done_units += cfg.g
-        done_bytes += L * cfg.g * 2 * cfg.d * cfg.elt + 2 * n * cfg.h * cfg.d * cfg.elt
+        done_bytes += (L * cfg.g + n * cfg.h) * (cfg.d + cfg.dv) * cfg.elt
         i += 1
     return done_bytes / spent / 1e9, spent, done_units, done_bytes
 
@@ -271,6 +271,12 @@ def run_ours(args, rank, local_rank, world):
         base = dataclasses.replace(base, layers=min(args.layers, base.layers))
     if args.dtype:
         base = dataclasses.replace(base, dtype=args.dtype)
+    if args.d:
+        base = dataclasses.replace(base, d=args.d, scale=1.0 / math.sqrt(args.d))
+    if args.dv:
+        base = dataclasses.replace(base, d_v=args.dv)
+    if (full_layer or paged) and base.dv != base.d:
+        raise SystemExit("--layer and --paged use one head dim")
     if n > 1:
         # n new tokens per step: the workload's shapes with plain N(0, 1) data
         base = dataclasses.replace(base, kind="plain")
@@ -304,7 +310,7 @@ def run_ours(args, rank, local_rank, world):
         packed[key] = torch.stack([x[key] for x in layers]).contiguous()
         for l, x in enumerate(layers):
             x[key] = packed[key][l]
-    out_shape = (cfg.b, cfg.h, cfg.d) if n == 1 else (cfg.b, n, cfg.h, cfg.d)
+    out_shape = (cfg.b, cfg.h, cfg.dv) if n == 1 else (cfg.b, n, cfg.h, cfg.dv)
     if full_layer:
         out_shape = (cfg.b, cfg.D)
     out_all = torch.empty((cfg.layers, *out_shape), dtype=cfg.torch_dtype, device=dev)
@@ -318,6 +324,10 @@ def run_ours(args, rank, local_rank, world):
         sb["proj_per_layer"] = projection_bytes(cfg)
         sb["step"] += cfg.layers * sb["proj_per_layer"]
     early = 0 if args.ordered else B.GQA_STEP_EARLY_STREAM
+    # --cuda-cores: the CUDA-core kernel on shapes the tensor-core kernel takes
+    cuda_cores = B.GQA_STEP_CUDA_CORES if args.cuda_cores else 0
+    if cuda_cores and (args.separate or full_layer):
+        raise SystemExit("--cuda-cores applies to the fused step calls")
 
     def layer_call(l, x):
         if full_layer:
@@ -326,32 +336,32 @@ def run_ours(args, rank, local_rank, world):
                                cfg.d, cfg.scale, outs[l], flags=early, stream=stream)
         elif paged:
             B.gqa_decode_step_paged(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
-                                    x["table"], x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d,
-                                    cfg.scale, outs[l], flags=early, stream=stream)
+                                    x["table"], x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.dv,
+                                    cfg.scale, outs[l], flags=early | cuda_cores, stream=stream)
         elif n > 1:
             if args.separate:
                 B.gqa_kv_append_multi(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
-                                      x["seq_lens"], cfg.b, n, cfg.g, cfg.d, cfg.d, stream=stream)
+                                      x["seq_lens"], cfg.b, n, cfg.g, cfg.d, cfg.dv, stream=stream)
                 B.gqa_decode_attn_multi(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
-                                        n, cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l],
+                                        n, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.scale, outs[l],
                                         stream=stream)
             else:
                 B.gqa_decode_step_multi(x["q"], x["k_new"], x["v_new"], x["k_cache"],
                                         x["v_cache"], x["seq_lens"], cfg.b, n, cfg.h, cfg.g,
-                                        cfg.d, cfg.d, cfg.scale, outs[l], flags=early,
-                                        stream=stream)
+                                        cfg.d, cfg.dv, cfg.scale, outs[l],
+                                        flags=early | cuda_cores, stream=stream)
         elif args.separate:
             B.gqa_kv_append(x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"],
-                            cfg.b, cfg.g, cfg.d, cfg.d, stream=stream)
+                            cfg.b, cfg.g, cfg.d, cfg.dv, stream=stream)
             B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b,
-                              cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale, outs[l], stream=stream)
+                              cfg.h, cfg.g, cfg.d, cfg.dv, cfg.scale, outs[l], stream=stream)
         else:
             # layers are independent buffers and seq_lens is fixed for the
             # step, so each layer may start streaming while the one before
             # finishes (GQA_STEP_EARLY_STREAM's contract)
             B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
-                              x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d, cfg.scale,
-                              outs[l], flags=early, stream=stream)
+                              x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.scale,
+                              outs[l], flags=early | cuda_cores, stream=stream)
 
     def step(ev=None):
         for l, x in enumerate(layers):
@@ -434,9 +444,9 @@ def run_ours(args, rank, local_rank, world):
 
         app_ms = timed(lambda l, x: B.gqa_kv_append(
             x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.g,
-            cfg.d, cfg.d, stream=stream))
+            cfg.d, cfg.dv, stream=stream))
         att_ms = timed(lambda l, x: B.gqa_decode_attn(
-            x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.d,
+            x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.dv,
             cfg.scale, outs[l], stream=stream))
         split = {
             "append_us_per_call": round(app_ms * 1000, 3),
@@ -494,7 +504,8 @@ def run_ours(args, rank, local_rank, world):
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
     traffic = None if (full_layer or paged) else profiled_traffic(src, args.workload, n)
-    plan = B.gqa_decode_plan(cfg.b, n, cfg.h, cfg.g, cfg.d, cfg.d, cfg.cap, cfg.dtype)
+    plan = B.gqa_decode_plan(cfg.b, n, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.cap, cfg.dtype,
+                             flags=cuda_cores)
     # per layer: the decode call's kernels (decode, plus combine when the
     # split partials are merged apart), + 2 projections or + 1 separate append
     launches_per_step = (plan["kernels"] + (2 if full_layer else (1 if args.separate else 0))
@@ -515,8 +526,9 @@ def run_ours(args, rank, local_rank, world):
         "data": "synthetic (seeded N(0,1), shapes of the workload)",
         "config": {
             "workload": cfg.name, "layers": cfg.layers, "b": cfg.b, "h": cfg.h, "g": cfg.g,
-            "d_head": cfg.d, "seq_len": int(np.max(lens)), "cap": cfg.cap,
+            "d_head": cfg.d, "d_v": cfg.dv, "seq_len": int(np.max(lens)), "cap": cfg.cap,
             "sum_seq_lens": int(np.sum(lens)),
+            "kernel": "tensor cores" if plan["tensor_core"] else "CUDA cores",
             "l2": "inputs larger than L2: every step streams all layers' K/V "
                   f"({sb['step'] / 2**30:.2f} GiB, L2 {l2 / 2**20:.0f} MiB)",
             "parallelism": f"replicas x{world}",
@@ -537,7 +549,7 @@ def run_ours(args, rank, local_rank, world):
                       + ("gqa_kv_append + gqa_decode_attn" if args.separate else "gqa_decode_step")
                       + ("_multi" if n > 1 else "") + ("_paged" if paged else "")
                       + (")" if full_layer else "")
-                      + f" ({'decode_tc_kernel' if cfg.dtype == 'bf16' and cfg.d == 128 else 'decode_simt_kernel'})",
+                      + f" ({'decode_tc_kernel' if plan['tensor_core'] else 'decode_simt_kernel'})",
             "achieved": round(achieved, 2),
             "peak": peaks["hbm_gbs"],
             "peak_source": peaks["source"],
@@ -646,6 +658,10 @@ def main(argv=None):
                          "projection) through gqa_decode_layer")
     ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default=None,
                     help="storage type override (shape studies)")
+    ap.add_argument("--d", type=int, default=None, help="head dim d_k (and d_v) override")
+    ap.add_argument("--dv", type=int, default=None, help="head dim d_v override")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="the CUDA-core kernel where the tensor-core kernel would run")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK",
                     help="paged KV cache with this block size (rows per block)")
     ap.add_argument("--layers", type=int, default=None,

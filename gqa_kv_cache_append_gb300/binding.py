@@ -30,6 +30,7 @@ GQA_ERR_DEVICE = -7
 GQA_ERR_SCRATCH_LIMIT = -8
 
 GQA_STEP_EARLY_STREAM = 1
+GQA_STEP_CUDA_CORES = 2
 
 GQA_DEV_BAD_SEQ_LEN = 1
 GQA_DEV_WAIT_TIMEOUT = 2
@@ -61,7 +62,7 @@ SIGNATURES = {
                                    _I, _I, _I, _VP]),
     "gqa_decode_step_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I,
                                    _F, _VP, _I, _I, _I, _I, _I, _VP]),
-    "gqa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
+    "gqa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
                              ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(_LL)]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
@@ -278,15 +279,17 @@ def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens
 _DTYPES = {"f32": GQA_F32, "bf16": GQA_BF16, "f16": GQA_F16}
 
 
-def gqa_decode_plan(b, n, h, g, d_k, d_v, cap, dtype, num_sms=0) -> dict:
+def gqa_decode_plan(b, n, h, g, d_k, d_v, cap, dtype, num_sms=0, flags=0) -> dict:
     """How a decode call with these shapes runs (host only when num_sms > 0):
     kernels per call, decode CTAs, positions per tile, tensor-core kernel or
-    not, split workspace bytes.  dtype: GQA_* code or "f32"/"bf16"/"f16"."""
+    not, split workspace bytes.  dtype: GQA_* code or "f32"/"bf16"/"f16";
+    flags: as for gqa_decode_step."""
     dt = _DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     k, c, t, tc = (ctypes.c_int(0) for _ in range(4))
     ws = ctypes.c_longlong(0)
     _check("gqa_decode_plan", lib.gqa_decode_plan(
-        int(b), int(n), int(h), int(g), int(d_k), int(d_v), int(cap), dt, int(num_sms),
+        int(b), int(n), int(h), int(g), int(d_k), int(d_v), int(cap), dt, int(flags),
+        int(num_sms),
         ctypes.byref(k), ctypes.byref(c), ctypes.byref(t), ctypes.byref(tc), ctypes.byref(ws)))
     return {"kernels": k.value, "ctas": c.value, "tile": t.value, "tensor_core": bool(tc.value),
             "workspace_bytes": ws.value}

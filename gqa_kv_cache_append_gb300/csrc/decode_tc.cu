@@ -1,5 +1,5 @@
 // decode_tc.cu - tensor-core (tcgen05 + TMEM) split-KV decode attention for
-// bf16 or fp16 caches with head dim 128.
+// bf16 or fp16 caches with head dims d_k, d_v in {64, 128}.
 //
 // The step of the MQA review §2.4 / §3 per (sequence i, KV head j) tile of
 // T = 128 cached positions, with the r = h/g query heads of the group padded
@@ -8,13 +8,18 @@
 // rows), the columns are the n * r query rows of the group, token-major,
 // and token s (at position L_i - n + s) sees positions p <= L_i - n + s:
 //
-//   S^T [T x NP]  = K_tile [T x 128] . Q_g^T          (tcgen05.mma, M=128)
+//   S^T [T x NP]  = K_tile [T x d_k] . Q_g^T          (tcgen05.mma, M=128)
 //   P^T [T x NP]  = exp2(S^T * scale*log2e - m)        (CUDA cores, per head)
-//   O^T [128 x NP] = V_tile^T [128 x T] . P^T          (tcgen05.mma, M=128)
+//   O^T [d_v x NP] = V_tile^T [d_v x T] . P^T          (tcgen05.mma, M=128)
+//
+// Head dims of 64 use one 64-column box where 128 use two: the S product
+// runs over d_k / 16 steps, and with d_v = 64 the O product still has M =
+// 128 (the unloaded half of the V stage feeds output rows 64-127, which
+// are never read).
 //
 // Roles (192 threads, one persistent CTA per SM):
 //   warp 0     TMA producer: Q block once per segment, then K and V tiles
-//              (two 64-column boxes each, 128-byte swizzle) into a 3-stage
+//              (64-column boxes, 128-byte swizzle) into a 3-stage
 //              ring, completing on mbarriers.  Each K/V byte is read from
 //              HBM once and serves all r query heads.
 //   warp 1     allocates tensor memory; one lane issues the MMAs:
@@ -123,7 +128,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                      const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
                      unsigned int* status, long long budget, int early, int nq,
-                     const int* __restrict__ table, int bsz, int max_blocks, int num_blocks) {
+                     const int* __restrict__ table, int bsz, int max_blocks, int num_blocks,
+                     int kh, int vh) {
   using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -144,6 +150,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
   const int nr = nq * r;  // query rows (columns) per KV head
+  // head dims d_k = 64 * kh and d_v = 64 * vh (kh, vh = 1 or 2): one or two
+  // 64-column boxes of K (and q) and of V; a new row is 2^sh chunks of 16
+  // bytes (sh = 3 or 4)
+  const int shk = kh + 2, shv = vh + 2;
+  const int dv = vh * 64;
   // column c = s * r + t is head t of new token s; padded columns never see
   // a position
   int* col_tok = reinterpret_cast<int*>(sm + C::OFF_COL);
@@ -154,7 +165,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     const int c = threadIdx.x - 64;
     const int s = c / r;
     col_tok[c] = c < nr ? s : -(1 << 24);
-    col_off[c] = c < nr ? (s * h + (c - s * r)) * kD : 0;
+    col_off[c] = c < nr ? (s * h + (c - s * r)) * dv : 0;
   }
   if (threadIdx.x == 0) {
     for (int k = 0; k < C::NBAR; ++k) {
@@ -210,10 +221,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                                                         abort_flag, status, budget));
       if (ok && lane == 0) {
         const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
-        mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 256);
+        mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 128 * kh);
         tma_load_3d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, sg.j * r, sg.i * nq, pol_keep);
-        tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
-                    pol_keep);
+        if (kh == 2)
+          tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
+                      pol_keep);
       }
       if (ok) last_q[qs] = static_cast<int>(kk);
     };
@@ -236,8 +248,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (!ok) continue;
         const uint32_t dst = s_base + st * C::KV_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(BAR(B_FULL_K + st), 2 * kBoxBytes);
-          mbar_arrive_expect_tx(BAR(B_FULL_V + st), 2 * kBoxBytes);
+          mbar_arrive_expect_tx(BAR(B_FULL_K + st), kh * kBoxBytes);
+          mbar_arrive_expect_tx(BAR(B_FULL_V + st), vh * kBoxBytes);
         }
         __syncwarp();
         // lane mm < sub copies box mm of the tile (its block's rows)
@@ -255,9 +267,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           }
           const uint32_t o = lane * box_rows * 128;
           tma_load_2d(dst + o, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
-          tma_load_2d(dst + kBoxBytes + o, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
+          if (kh == 2)
+            tma_load_2d(dst + kBoxBytes + o, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
           tma_load_2d(dst + 2 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
-          tma_load_2d(dst + 3 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
+          if (vh == 2)
+            tma_load_2d(dst + 3 * kBoxBytes + o, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
         last_n[st] = static_cast<int>(n);
@@ -309,10 +323,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (mbar_wait(BAR(B_Q_EMPTY + qs), ((kk >> 1) & 1) ^ 1, abort_flag, status, budget)) {
           const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
           // box [n tokens][r heads][64]: rows s * r + t of the operand
-          mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 256);
+          mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 128 * kh);
           tma_load_3d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, sg.j * r, sg.i * nq, pol_keep);
-          tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
-                      pol_keep);
+          if (kh == 2)
+            tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
+                        pol_keep);
           last_q[qs] = static_cast<int>(kk);
         }
       };
@@ -329,9 +344,9 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             for (int lp = lt; lp < seg.lt1 && lp < lt + (counters ? kPrefetchTiles : 0); ++lp) {
               const int rp = unit_row + lp * kT;
               tma_prefetch_l2_2d(&tm_k, 0, rp);
-              tma_prefetch_l2_2d(&tm_k, 64, rp);
+              if (kh == 2) tma_prefetch_l2_2d(&tm_k, 64, rp);
               tma_prefetch_l2_2d(&tm_v, 0, rp);
-              tma_prefetch_l2_2d(&tm_v, 64, rp);
+              if (vh == 2) tma_prefetch_l2_2d(&tm_v, 64, rp);
             }
             pdl_wait();
             waited = true;
@@ -343,12 +358,13 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             continue;
           const int row = unit_row + lt * kT;
           const uint32_t dst = s_base + st * C::KV_BYTES;
-          mbar_arrive_expect_tx(BAR(B_FULL_K + st), 2 * kBoxBytes);
+          mbar_arrive_expect_tx(BAR(B_FULL_K + st), kh * kBoxBytes);
           tma_load_2d(dst, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
-          tma_load_2d(dst + kBoxBytes, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
-          mbar_arrive_expect_tx(BAR(B_FULL_V + st), 2 * kBoxBytes);
+          if (kh == 2) tma_load_2d(dst + kBoxBytes, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
+          mbar_arrive_expect_tx(BAR(B_FULL_V + st), vh * kBoxBytes);
           tma_load_2d(dst + 2 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
-          tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
+          if (vh == 2)
+            tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
           last_n[st] = static_cast<int>(n);
         }
         if (!waited) {  // a first segment shorter than the ring
@@ -409,7 +425,9 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
             // A = V^T: M = 128 head-dim columns (two 64-column boxes, LBO
-            // apart), K = 16 positions (two 8-row groups, SBO apart)
+            // apart), K = 16 positions (two 8-row groups, SBO apart).  With
+            // d_v = 64 the second box is not loaded: output rows 64-127 are
+            // never read.
             const uint64_t a = smem_desc(vbase + kk * 2048, kBoxBytes, 1024, SWZ_128B);
             // B = P^T: N = NP heads contiguous per row, K = 16 position rows
             const uint64_t bd =
@@ -427,26 +445,28 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     while (w.next(seg)) {
       const uint32_t qs = k & 1;
       const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
-      // new tokens s_lo .. s_lo + nchunk / 16 - 1 have their rows here
+      // new tokens s_lo .. s_lo + nrows - 1 have their rows here
       const int first_new = seg.L - nq;
-      int s_lo = 0, nchunk = 0;
+      int s_lo = 0, nrows = 0;
       if (k_new != nullptr) {
         const int p_lo = max(first_new, seg.lt0 * kT), p_hi = min(seg.L, seg.lt1 * kT);
         if (p_lo < p_hi) {
           s_lo = p_lo - first_new;
-          nchunk = (p_hi - p_lo) * 16;
+          nrows = p_hi - p_lo;
         }
       }
-      // chunk idx of the segment's new rows: token s_lo + idx / 16, 16 bytes
-      // (idx % 16) of its row [b, n, g, 128] of k_new / v_new
-      auto new_off = [&](int idx) {
-        return ((static_cast<size_t>(seg.i) * nq + s_lo + (idx >> 4)) * g + seg.j) * 16 +
-               (idx & 15);
+      const int nchunk_k = nrows << shk, nchunk_v = nrows << shv;
+      // chunk idx of the segment's new rows (2^sh chunks of 16 bytes a row):
+      // token s_lo + (idx >> sh), chunk idx & (2^sh - 1) of its row
+      // [b, n, g, d] of k_new / v_new
+      auto new_off = [&](int idx, int sh) {
+        return (((static_cast<size_t>(seg.i) * nq + s_lo + (idx >> sh)) * g + seg.j) << sh) +
+               (idx & ((1 << sh) - 1));
       };
       // paged cache (one token): the physical row of position L_i - 1, or -1
       // for a bad table entry (then nothing is written)
       long long prow = -1;
-      if (PAGED && !MULTI && nchunk > 0) {
+      if (PAGED && !MULTI && nrows > 0) {
         const int blk = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + (seg.L - 1) / bsz);
         if (blk >= 0 && blk < num_blocks)
           prow = (static_cast<long long>(blk) * g + seg.j) * bsz + (seg.L - 1) % bsz;
@@ -460,51 +480,54 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       for (int c4 = 0; c4 < C::KCH; ++c4) {
         const int idx = lane + 32 * c4;
         knew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < nchunk) knew[c4] = __ldg(k_new + new_off(idx));
+        if (idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, shk));
       }
 #pragma unroll
       for (int c4 = 0; c4 < VCH; ++c4) {
         const int idx = lane + 32 * c4;
         vnew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (MULTI && idx < nchunk) vnew[c4] = __ldg(v_new + new_off(idx));
+        if (MULTI && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
       }
-      // put chunk idx (value v) into row `rho` of a staged [128 x 128] tile
-      // (two 64-column boxes, 128-byte swizzle) and into the cache at `pos`
-      auto put = [&](uint32_t tile_base, uint4* cache, int idx, int pos, int rho, const uint4& v) {
-        const int ch = idx & 15;
+      // put chunk ch (value v) into row `rho` of a staged tile (64-column
+      // boxes, 128-byte swizzle) and into the cache at `pos` (rows of 2^sh
+      // chunks)
+      auto put = [&](uint32_t tile_base, uint4* cache, int ch, int sh, int pos, int rho,
+                     const uint4& v) {
         const uint32_t dst =
             tile_base + (ch >> 3) * kBoxBytes + rho * 128 + (((ch & 7) ^ (rho & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
         if (!PAGED) {
-          cache[(unit * cap + pos) * 16 + ch] = v;
+          cache[((unit * cap + pos) << sh) + ch] = v;
         } else if (!MULTI) {
-          if (prow >= 0) cache[prow * 16 + ch] = v;
+          if (prow >= 0) cache[(prow << sh) + ch] = v;
         } else {
           // n new rows: each through its own block-table entry
           const int blk = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + pos / bsz);
           if (blk >= 0 && blk < num_blocks)
-            cache[((static_cast<long long>(blk) * g + seg.j) * bsz + pos % bsz) * 16 + ch] = v;
+            cache[(((static_cast<long long>(blk) * g + seg.j) * bsz + pos % bsz) << sh) + ch] = v;
           else
             atomicOr(status, GQA_DEV_BAD_BLOCK);
         }
       };
-      // patch the new rows that fall in tile lt (K or V half of the stage)
+      // patch the new rows that fall in tile lt (K or V part of the stage)
       auto patch = [&](uint32_t tile_base, uint4* cache, const uint4* src, const uint4* regs,
-                       int nregs, int lt) {
+                       int nregs, int lt, int sh) {
+        const int nchunk = nrows << sh;
 #pragma unroll
         for (int c4 = 0; c4 < C::KCH; ++c4) {
           if (c4 >= nregs) break;
           const int idx = lane + 32 * c4;
-          const int pos = first_new + s_lo + (idx >> 4);
+          const int pos = first_new + s_lo + (idx >> sh);
           if (idx < nchunk && pos >= lt * kT && pos < (lt + 1) * kT)
-            put(tile_base, cache, idx, pos, pos - lt * kT, regs[c4]);
+            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * kT, regs[c4]);
         }
         for (int idx = lane + 32 * nregs; idx < nchunk; idx += 32) {
-          const int pos = first_new + s_lo + (idx >> 4);
+          const int pos = first_new + s_lo + (idx >> sh);
           if (pos >= lt * kT && pos < (lt + 1) * kT)
-            put(tile_base, cache, idx, pos, pos - lt * kT, __ldg(src + new_off(idx)));
+            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * kT,
+                __ldg(src + new_off(idx, sh)));
         }
         fence_proxy_async_smem();
       };
@@ -519,11 +542,11 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
         ok = __all_sync(0xffffffffu, ok);
         const uint32_t kbase = s_base + st * C::KV_BYTES;
-        const bool new_rows = nchunk > 0 && (lt + 1) * kT > first_new;
+        const bool new_rows = nrows > 0 && (lt + 1) * kT > first_new;
         if (new_rows) {
           // rows L_i - n .. L_i - 1 of this tile are the new tokens: use
           // k_new there, and store them into the cache (the append)
-          if (ok) patch(kbase, k_cache_w, k_new, knew, C::KCH, lt);
+          if (ok) patch(kbase, k_cache_w, k_new, knew, C::KCH, lt, shk);
           __syncwarp();
         }
         tc_fence_after();
@@ -533,6 +556,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             for (int kk = 0; kk < kD / 16; ++kk) {
               // A = K tile, K-major: 128 rows, 16 head-dim columns per step;
               // steps 0-3 in the first 64-column box, 4-7 in the second
+              // (d_k = 128 only)
+              if (kk >= 4 * kh) break;
               const uint64_t a =
                   smem_desc(kbase + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024, SWZ_128B);
               const uint64_t bq =
@@ -551,7 +576,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           const bool vok = __all_sync(
               0xffffffffu,
               mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget));
-          if (vok) patch(kbase + 2 * kBoxBytes, v_cache_w, v_new, vnew, VCH, lt);
+          if (vok) patch(kbase + 2 * kBoxBytes, v_cache_w, v_new, vnew, VCH, lt, shv);
           __syncwarp();
         }
         have_prev = true;
@@ -626,13 +651,14 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     uint32_t n = 0;
     while (w.next(seg)) {
       const int first_new = seg.L - nq;  // position of new token 0
-      // one token: threads 0-15 of warpgroup 0 carry the new V row (one
-      // 16-byte chunk each) to the unit's last tile
+      // one token: threads 0 .. d_v/8 - 1 of warpgroup 0 carry the new V
+      // row (one 16-byte chunk each) to the unit's last tile
       const bool append_v = !MULTI && v_new != nullptr && seg.lt1 == seg.ti;
+      const int vch = 1 << shv;
       uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
       long long vrow_w = -1;  // cache row written by the append
-      if (append_v && wg == 0 && row < 16) {
-        vnew = __ldg(v_new + (static_cast<size_t>(seg.i) * g + seg.j) * 16 + row);
+      if (append_v && wg == 0 && row < vch) {
+        vnew = __ldg(v_new + ((static_cast<size_t>(seg.i) * g + seg.j) << shv) + row);
         if (!PAGED) {
           vrow_w = (static_cast<long long>(seg.i) * g + seg.j) * cap + seg.L - 1;
         } else {
@@ -756,14 +782,14 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           const bool vok =
               mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
           const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
-          if (vok && patch_v && row < 16) {
+          if (vok && patch_v && row < vch) {
             const int rho = valid - 1;
             const uint32_t dst =
                 vbase + (row >> 3) * kBoxBytes + rho * 128 + (((row & 7) ^ (rho & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(vnew.x),
                          "r"(vnew.y), "r"(vnew.z), "r"(vnew.w)
                          : "memory");
-            if (vrow_w >= 0) v_cache_w[vrow_w * 16 + row] = vnew;
+            if (vrow_w >= 0) v_cache_w[(vrow_w << shv) + row] = vnew;
           }
           if (vok && !live) {
             const uint32_t vrow = vbase + row * 128;
@@ -803,8 +829,10 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (lane < HP) lred[wq * HP + lane] = mine;
         named_bar_sync(bar_id, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
-        // output row of column c: (i * n + s) * h + j * r + t
-        T16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * kD + row;
+        // output row of column c: (i * n + s) * h + j * r + t; thread `row`
+        // holds output column `row` (none past d_v)
+        const bool has_col = row < dv;
+        T16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * dv + row;
         const int u = seg.i * g + seg.j;
         const size_t slot = static_cast<size_t>(u) + blockIdx.x;
         // l[e] becomes the CTA-wide softmax denominator of head h0 + e
@@ -814,14 +842,14 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         if (whole) {
 #pragma unroll
           for (int e = 0; e < HP; ++e)
-            if (h0 + e < nr)
+            if (h0 + e < nr && has_col)
               obase[col_off[h0 + e]] = Half16<T16>::from(o[e] / l[e]);
         } else {
 #pragma unroll
           for (int e = 0; e < HP; ++e) {
             if (h0 + e < nr) {
               const size_t sl = slot * nr + h0 + e;
-              part_o[sl * kD + row] = o[e];
+              if (has_col) part_o[sl * dv + row] = o[e];
               if (row == 0) {
                 // a token that saw none of this CTA's positions: empty partial
                 part_ml[sl * 2 + 0] = l[e] > 0.f ? mfin[e] : -INFINITY;
@@ -870,7 +898,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                     const long long sl = (u + c) * nr + h0 + e0 + k;
                     mc[k] = __ldcg(part_ml + sl * 2);
                     lc[k] = __ldcg(part_ml + sl * 2 + 1);
-                    oc[k] = __ldcg(part_o + sl * kD + row);
+                    // (threads past d_v read a valid column and drop it)
+                    oc[k] = __ldcg(part_o + sl * dv + (row & (dv - 1)));
                   }
                 }
 #pragma unroll
@@ -889,7 +918,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
             }
 #pragma unroll
             for (int e = 0; e < HP; ++e)
-              if (h0 + e < nr)
+              if (h0 + e < nr && has_col)
                 obase[col_off[h0 + e]] = Half16<T16>::from(o[e] / l[e]);
           }
         }
@@ -913,21 +942,23 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// 2-D map over a row-major [rows x 128] bf16 tensor, box [box_rows x 64],
-// 128-byte swizzle, zero fill outside.  (The query map is 3-D:
-// [b * n tokens][h heads][128], box [n][r][64].)
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows, bool bf16) {
-  const uint64_t dims[2] = {static_cast<uint64_t>(kD), rows};
-  const uint64_t strides[1] = {static_cast<uint64_t>(kD) * 2};
+// 2-D map over a row-major [rows x d] 16-bit tensor (d = 64 or 128), box
+// [box_rows x 64], 128-byte swizzle, zero fill outside.  (The query map is
+// 3-D: [b * n tokens][h heads][d_k], box [n][r][64].)
+bool make_map(CUtensorMap* map, const void* base, int d, uint64_t rows, uint32_t box_rows,
+              bool bf16) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(d), rows};
+  const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
   const uint32_t box[2] = {64u, box_rows};
   return encode_bf16_map(map, base, 2, dims, strides, box, bf16);
 }
 
-bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r, bool bf16) {
-  const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(h),
+bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r, int d,
+                bool bf16) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(h),
                             static_cast<uint64_t>(b) * nq};
-  const uint64_t strides[2] = {static_cast<uint64_t>(kD) * 2,
-                               static_cast<uint64_t>(h) * kD * 2};
+  const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2,
+                               static_cast<uint64_t>(h) * d * 2};
   const uint32_t box[3] = {64u, static_cast<uint32_t>(r), static_cast<uint32_t>(nq)};
   return encode_bf16_map(map, base, 3, dims, strides, box, bf16);
 }
@@ -941,9 +972,9 @@ cudaError_t launch_np(const DecodeLaunch& a) {
   const uint64_t kv_rows = PAGED ? static_cast<uint64_t>(a.num_blocks) * a.g * a.block_size
                                  : static_cast<uint64_t>(a.b) * a.g * a.cap;
   const uint32_t box_rows = (PAGED && a.block_size < kT) ? a.block_size : kT;
-  if (!make_q_map(&mq, a.q, a.b, a.nq, a.h, a.h / a.g, kBf16) ||
-      !make_map(&mk, a.k_cache, kv_rows, box_rows, kBf16) ||
-      !make_map(&mv, a.v_cache, kv_rows, box_rows, kBf16))
+  if (!make_q_map(&mq, a.q, a.b, a.nq, a.h, a.h / a.g, a.d, kBf16) ||
+      !make_map(&mk, a.k_cache, a.d, kv_rows, box_rows, kBf16) ||
+      !make_map(&mv, a.v_cache, a.dv, kv_rows, box_rows, kBf16))
     return cudaErrorInvalidValue;
   auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16>;
   // the shared-memory opt-in is set once per device (not during a capture)
@@ -971,7 +1002,8 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       static_cast<T16*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
-      a.early ? 1 : 0, a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks);
+      a.early ? 1 : 0, a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks, a.d / 64,
+      a.dv / 64);
 }
 
 template <typename T16>
@@ -992,8 +1024,9 @@ cudaError_t launch_type(const DecodeLaunch& a) {
 
 }  // namespace
 
-bool tc_supported(int dtype, int d, int cols) {
-  return (dtype == GQA_BF16 || dtype == GQA_F16) && d == kD && cols >= 1 && cols <= 32;
+bool tc_supported(int dtype, int d_k, int d_v, int cols) {
+  return (dtype == GQA_BF16 || dtype == GQA_F16) && (d_k == 64 || d_k == 128) &&
+         (d_v == 64 || d_v == 128) && cols >= 1 && cols <= 32;
 }
 
 int tc_tile() { return kT; }

@@ -1,3 +1,4 @@
+#include <cstdlib>
 // gqa_api.cu - the C ABI of libgqa.so (declared in include/gqa.h): argument
 // checks, kernel selection, the split workspace, the device status word, and
 // the small kernels (KV append, wait self-test).
@@ -362,12 +363,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // the combine kernel instead (counters = null tells the decode kernel).
 // Units split over more CTAs than twice the unit count are merged by the
 // combine kernel; fewer splits are merged inside the decode kernel.
-bool use_combine_kernel(long long nc, int b, int g) { return nc > 2ll * b * g; }
+bool use_combine_kernel(long long nc, int b, int g) {
+  static const long long f = getenv("GQA_XFACTOR") ? atoll(getenv("GQA_XFACTOR")) : 2;
+  return nc > f * b * g;
+}
 
 int launch_all(DecodeLaunch& a, int tile) {
   const bool separate = use_combine_kernel(a.nc, a.b, a.g);
   if (separate) a.counters = nullptr;
-  const bool tc = a.d == a.dv && tc_supported(a.dtype, a.d, a.nq * (a.h / a.g));
+  const bool tc = !a.cuda_cores && tc_supported(a.dtype, a.d, a.dv, a.nq * (a.h / a.g));
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   if (separate) {
@@ -580,8 +584,14 @@ struct DecodePlan {
 };
 
 // Host checks of a decode call (no CUDA call): GQA_OK or an error code.
+// The tensor-core kernel wherever it takes the shape, unless the caller asks
+// for the CUDA-core kernel.
+bool use_tensor_cores(const DecodeArgs& x, int cols) {
+  return !(x.flags & GQA_STEP_CUDA_CORES) && tc_supported(x.dtype, x.d_k, x.d_v, cols);
+}
+
 int decode_check(const DecodeArgs& x) {
-  if (x.flags & ~GQA_STEP_EARLY_STREAM) return GQA_ERR_UNSUPPORTED;
+  if (x.flags & ~(GQA_STEP_EARLY_STREAM | GQA_STEP_CUDA_CORES)) return GQA_ERR_UNSUPPORTED;
   if (!x.q || !x.k_cache || !x.v_cache || !x.seq_lens || !x.out) return GQA_ERR_NULL;
   if (x.dtype != GQA_F32 && x.dtype != GQA_BF16 && x.dtype != GQA_F16) return GQA_ERR_DTYPE;
   if (x.b < 1 || x.nq < 1 || x.h < 1 || x.g < 1 || x.d_k < 1 || x.d_v < 1 || x.cap < 1 ||
@@ -597,14 +607,14 @@ int decode_check(const DecodeArgs& x) {
   const int r = x.h / x.g;
   if (x.b > 65535 || static_cast<long long>(x.nq) * r > 32) return GQA_ERR_UNSUPPORTED;
   const int cols = x.nq * r;  // query rows per KV head
-  const bool tc = x.d_k == x.d_v && tc_supported(x.dtype, x.d_k, cols);
+  const bool tc = use_tensor_cores(x, cols);
   if (!tc && !simt_supported(x.dtype, x.d_k, x.d_v, cols)) return GQA_ERR_UNSUPPORTED;
   return GQA_OK;
 }
 
 DecodePlan decode_plan(const DecodeArgs& x, int num_sms) {
   const int r = x.h / x.g, d = x.d_k, cols = x.nq * r;
-  const bool use_tc = x.d_k == x.d_v && tc_supported(x.dtype, d, cols);
+  const bool use_tc = use_tensor_cores(x, cols);
   DecodePlan p;
   p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, x.d_k, x.d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(x.dtype, d, r);
@@ -646,6 +656,7 @@ int decode_run(const DecodeArgs& x, const DecodePlan& p, const DeviceInfo* di, v
   a.k_cache_w = const_cast<void*>(x.k_cache);
   a.v_cache_w = const_cast<void*>(x.v_cache);
   a.early = (x.flags & GQA_STEP_EARLY_STREAM) != 0;
+  a.cuda_cores = (x.flags & GQA_STEP_CUDA_CORES) != 0;
   a.status = di->status;
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(p.nc);
@@ -715,13 +726,13 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new, v
 }
 
 int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int dtype,
-                    int num_sms, int* kernels, int* ctas, int* tile, int* tensor_core,
-                    long long* workspace_bytes) {
+                    int flags, int num_sms, int* kernels, int* ctas, int* tile,
+                    int* tensor_core, long long* workspace_bytes) {
   using namespace gqa;
   // stand-in pointers: only the shapes are checked
   const void* p = reinterpret_cast<const void*>(uintptr_t(256));
   DecodeArgs x{p, p, p, p, p, static_cast<const int32_t*>(p), b, n, h, g, d_k, d_v, 1.f,
-               const_cast<void*>(p), cap, dtype, 0};
+               const_cast<void*>(p), cap, dtype, flags};
   if (int e = decode_check(x)) return e;
   if (num_sms < 0) return GQA_ERR_SHAPE;
   if (num_sms == 0) {
@@ -733,7 +744,7 @@ int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int d
   if (kernels) *kernels = use_combine_kernel(pl.nc, b, g) ? 2 : 1;
   if (ctas) *ctas = static_cast<int>(pl.nc);
   if (tile) *tile = pl.tile;
-  if (tensor_core) *tensor_core = d_k == d_v && tc_supported(dtype, d_k, n * (h / g)) ? 1 : 0;
+  if (tensor_core) *tensor_core = use_tensor_cores(x, n * (h / g)) ? 1 : 0;
   if (workspace_bytes)
     *workspace_bytes = static_cast<long long>(pl.o_bytes + pl.ml_bytes + pl.units * sizeof(int));
   return GQA_OK;
@@ -1056,7 +1067,7 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   const int r = h / g;
   const int d = d_k;
   if (b > 65535) return GQA_ERR_UNSUPPORTED;
-  const bool use_tc = d_k == d_v && tc_supported(dtype, d, r);
+  const bool use_tc = tc_supported(dtype, d_k, d_v, r);
   if (!use_tc && !simt_supported(dtype, d_k, d_v, r)) return GQA_ERR_UNSUPPORTED;
   NoAllocDevice* nd = nullptr;
   if (int e = noalloc_setup(&nd)) return e;

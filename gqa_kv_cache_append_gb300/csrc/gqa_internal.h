@@ -27,6 +27,7 @@ struct DecodeLaunch {
   void* k_cache_w;       // the caches, written at rows L_i - nq .. L_i - 1
   void* v_cache_w;
   bool early;            // stream the first tiles before the dependency wait
+  bool cuda_cores = false;  // the CUDA-core kernel even where tensor cores apply
   unsigned int* status;  // device status word
   long long budget;      // wait limit in SM cycles
   int nc;                // persistent CTAs
@@ -51,8 +52,9 @@ int simt_tile(int dtype, int d_k, int d_v);
 int simt_ctas_per_sm(int dtype, int d, int r);
 cudaError_t launch_decode_simt(const DecodeLaunch& a);
 
-// tcgen05 tensor-core kernel (bf16, d = 128)
-bool tc_supported(int dtype, int d, int cols);
+// tcgen05 tensor-core kernel (bf16 and fp16, d_k and d_v in {64, 128}, up to
+// 32 query rows per KV head)
+bool tc_supported(int dtype, int d_k, int d_v, int cols);
 int tc_tile();
 int tc_ctas_per_sm(int r);
 cudaError_t launch_decode_tc(const DecodeLaunch& a);

@@ -68,10 +68,15 @@ class DecodeConfig:
     boost: float = 8.0
     boost_frac: float = 0.01
     d_model: int = 0           # model width D; 0 means h * d
+    d_v: int = 0               # head dim of V and out; 0 means d (d is d_k)
 
     @property
     def r(self) -> int:
         return self.h // self.g
+
+    @property
+    def dv(self) -> int:
+        return self.d_v if self.d_v else self.d
 
     @property
     def D(self) -> int:
@@ -133,17 +138,17 @@ def layer_bytes(cfg: DecodeConfig, lens: np.ndarray, n: int = 1) -> int:
     """Algorithmic bytes of one decode-attention call: the K and V rows below
     L_i of every KV head, plus q and out of the n new tokens (padding and
     split partials are not counted)."""
-    kv = int(np.sum(lens, dtype=np.int64)) * cfg.g * 2 * cfg.d * cfg.elt
-    return kv + 2 * cfg.b * n * cfg.h * cfg.d * cfg.elt
+    kv = int(np.sum(lens, dtype=np.int64)) * cfg.g * (cfg.d + cfg.dv) * cfg.elt
+    return kv + cfg.b * n * cfg.h * (cfg.d + cfg.dv) * cfg.elt
 
 
 def layer_flops(cfg: DecodeConfig, lens: np.ndarray, n: int = 1) -> int:
     """Multiply-add flops of one decode-attention call (2 per product, for
-    q.K and for w.V); with n new tokens the causal mask leaves token s the
-    positions below L_i - n + s + 1."""
+    q.K over d_k and for w.V over d_v); with n new tokens the causal mask
+    leaves token s the positions below L_i - n + s + 1."""
     lens = np.asarray(lens, dtype=np.int64)
     seen = int(np.sum(lens)) * n - cfg.b * (n * (n - 1) // 2)
-    return 4 * cfg.h * cfg.d * seen
+    return 2 * cfg.h * (cfg.d + cfg.dv) * seen
 
 
 def _randn(shape, gen, device):
@@ -160,9 +165,9 @@ def _pool(x: torch.Tensor, g: int) -> torch.Tensor:
 
 def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
                lens: Optional[np.ndarray] = None, pad_fill=None) -> dict:
-    """Inputs of one layer: q [b,h,d], k_cache/v_cache [b,g,cap,d],
-    k_new/v_new [b,g,d] in the storage dtype, seq_lens int32 [b] on
-    ``device``, plus the host copy ``lens``."""
+    """Inputs of one layer: q [b,h,d], k_cache [b,g,cap,d], v_cache
+    [b,g,cap,d_v], k_new [b,g,d], v_new [b,g,d_v] in the storage dtype,
+    seq_lens int32 [b] on ``device``, plus the host copy ``lens``."""
     if cfg.h % cfg.g != 0:
         raise ValueError("h must be divisible by g")
     device = torch.device(device)
@@ -172,9 +177,12 @@ def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
     gen = torch.Generator(device=device)
     gen.manual_seed(cfg.seed * 1000 + layer)
     b, h, g, d, cap = cfg.b, cfg.h, cfg.g, cfg.d, cfg.cap
+    dv = cfg.dv
     dt = cfg.torch_dtype
 
     if cfg.kind == "meanpool":
+        if dv != d:
+            raise ValueError("the mean-pooled workload has one head dim")
         k_cache = _pool(_randn((b, h, cap, d), gen, device), g).to(dt)
         v_cache = _pool(_randn((b, h, cap, d), gen, device), g).to(dt)
         q = _randn((b, h, d), gen, device).to(dt)
@@ -184,16 +192,16 @@ def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
         if cfg.kind == "plain" and dt != torch.float32:
             # draw and round block by block to bound the float32 temporary
             k_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
-            v_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
+            v_cache = torch.empty((b, g, cap, dv), dtype=dt, device=device)
             for dst in (k_cache, v_cache):
                 for i in range(b):
-                    dst[i].copy_(_randn((g, cap, d), gen, device))
+                    dst[i].copy_(_randn((g, cap, dst.shape[-1]), gen, device))
         else:
             k_cache = _randn((b, g, cap, d), gen, device)
-            v_cache = _randn((b, g, cap, d), gen, device)
+            v_cache = _randn((b, g, cap, dv), gen, device)
         q = _randn((b, h, d), gen, device).to(dt)
         k_new = _randn((b, g, d), gen, device)
-        v_new = _randn((b, g, d), gen, device).to(dt)
+        v_new = _randn((b, g, dv), gen, device).to(dt)
         if cfg.kind == "boost":
             if g != 1:
                 raise ValueError("the boosted workload is MQA (g = 1)")
@@ -223,9 +231,10 @@ def make_layer(cfg: DecodeConfig, layer: int = 0, device="cpu",
 def make_layer_multi(cfg: DecodeConfig, n: int, layer: int = 0, device="cpu",
                      lens: Optional[np.ndarray] = None, pad_fill=None) -> dict:
     """Inputs of one layer's step with n new tokens per sequence: q
-    [b, n, h, d], k_cache / v_cache [b, g, cap, d], k_new / v_new [b, n, g, d]
-    in the storage dtype, seq_lens int32 [b] (post-append, >= n) on
-    ``device``, plus the host copy ``lens``.  'plain' workloads only."""
+    [b, n, h, d], k_cache [b, g, cap, d], v_cache [b, g, cap, d_v], k_new
+    [b, n, g, d], v_new [b, n, g, d_v] in the storage dtype, seq_lens int32
+    [b] (post-append, >= n) on ``device``, plus the host copy ``lens``.
+    'plain' workloads only."""
     if cfg.kind != "plain":
         raise ValueError("multi-token inputs are drawn for plain workloads only")
     if cfg.h % cfg.g != 0 or n < 1:
@@ -237,15 +246,16 @@ def make_layer_multi(cfg: DecodeConfig, n: int, layer: int = 0, device="cpu",
     gen = torch.Generator(device=device)
     gen.manual_seed(cfg.seed * 1000 + layer + 100000 * n)
     b, h, g, d, cap = cfg.b, cfg.h, cfg.g, cfg.d, cfg.cap
+    dv = cfg.dv
     dt = cfg.torch_dtype
     k_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
-    v_cache = torch.empty((b, g, cap, d), dtype=dt, device=device)
+    v_cache = torch.empty((b, g, cap, dv), dtype=dt, device=device)
     for dst in (k_cache, v_cache):
         for i in range(b):
-            dst[i].copy_(_randn((g, cap, d), gen, device))
+            dst[i].copy_(_randn((g, cap, dst.shape[-1]), gen, device))
     q = _randn((b, n, h, d), gen, device).to(dt)
     k_new = _randn((b, n, g, d), gen, device).to(dt)
-    v_new = _randn((b, n, g, d), gen, device).to(dt)
+    v_new = _randn((b, n, g, dv), gen, device).to(dt)
     if pad_fill is not None:
         for i in range(b):
             L = int(lens[i])
@@ -282,13 +292,14 @@ def make_layer_weights(cfg: DecodeConfig, layer: int = 0, device="cpu") -> dict:
 
 def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, block_size: int, seed: int,
              spare: int = 3, fill=None):
-    """Lay a contiguous cache [b, g, cap, d] out as a paged one: pools
-    [num_blocks, g, block_size, d] with num_blocks = b * cap / block_size +
-    spare, and a block table [b, cap / block_size] int32 that maps the blocks
+    """Lay a contiguous cache [b, g, cap, d] (V: [b, g, cap, d_v]) out as a
+    paged one: pools [num_blocks, g, block_size, d] with num_blocks =
+    b * cap / block_size + spare, and a block table [b, cap / block_size]
+    int32 that maps the blocks
     of every sequence to a seeded random permutation of the pool
     (torch.randperm on a CPU generator seeded ``seed``).  Unused blocks hold
     ``fill`` (default zeros).  A pure relabelling: no arithmetic."""
-    b, g, cap, d = k_cache.shape
+    b, g, cap, _ = k_cache.shape
     if cap % block_size:
         raise ValueError("cap must be a multiple of block_size")
     mb = cap // block_size
@@ -299,6 +310,7 @@ def to_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, block_size: int, seed
     table = perm[: b * mb].reshape(b, mb).to(torch.int32)
     pools = []
     for cache in (k_cache, v_cache):
+        d = cache.shape[-1]
         pool = torch.zeros((nb, g, block_size, d), dtype=cache.dtype, device=cache.device)
         if fill is not None:
             pool.fill_(fill)

@@ -79,6 +79,7 @@ extern "C" {
 
 /* flags of gqa_decode_step */
 #define GQA_STEP_EARLY_STREAM 1 /* see gqa_decode_step */
+#define GQA_STEP_CUDA_CORES   2 /* see gqa_decode_step */
 
 /* bits of the device status word */
 #define GQA_DEV_BAD_SEQ_LEN  1u /* some seq_lens[i] was outside [1, cap] */
@@ -129,9 +130,9 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache,
  *
  * Rows p >= L_i of the caches are never used in the result, whatever they
  * hold.  fp32 accumulation; bf16 output is rounded to nearest even.
- * Supported: bf16 / fp16 with d_k = d_v = 128 and h / g <= 32 (tensor-core
- * kernel); otherwise d_k, d_v in {64, 128} (they may differ) with h / g <= 16
- * for fp32 and h / g <= 8 for bf16 / fp16 (CUDA-core kernel).  b <= 65535.
+ * Supported: d_k, d_v in {64, 128} (they may differ); bf16 / fp16 with
+ * h / g <= 32 (tensor-core kernel), fp32 with h / g <= 16 (CUDA-core
+ * kernel).  b <= 65535.
  * Returns GQA_OK or an error code (nothing is launched on error).
  */
 int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -161,7 +162,14 @@ int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
  * those kernels writes seq_lens or the rows below L_i - 1 of this call's
  * caches - true when they are the steps of other layers, whose caches are
  * other buffers.  q, k_new, v_new and every buffer this call writes are
- * still used only after the wait.  Other bits: GQA_ERR_UNSUPPORTED.
+ * still used only after the wait.
+ *
+ * GQA_STEP_CUDA_CORES (may be combined with the other flag): run the
+ * CUDA-core kernel even where the tensor-core kernel takes the shape (bf16 /
+ * fp16; for comparisons and checks: same results within the dtype's
+ * tolerance, far lower bandwidth).  The CUDA-core kernel takes 16-bit data
+ * with n * (h / g) <= 8; larger shapes return GQA_ERR_UNSUPPORTED.
+ * Other bits: GQA_ERR_UNSUPPORTED.
  */
 int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
                     void* v_cache, const int32_t* seq_lens, int b, int h, int g, int d_k,
@@ -192,11 +200,11 @@ int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k
  *   q   [b, n, h, d_k]   (read)
  *   out [b, n, h, d_v]   (written)
  * The n * r query rows of one KV head share each K/V tile read (one pass
- * over the cache for all n tokens).  Supported: n * (h / g) <= 32 with bf16
- * and d = 128 (tensor-core kernel); n * (h / g) <= 16 with fp32 and
- * n * (h / g) <= 8 with bf16 and d = 64 (CUDA-core kernel); otherwise
- * GQA_ERR_UNSUPPORTED.  Other limits, errors and the workspace are those of
- * gqa_decode_attn (the partials grow by the factor n).
+ * over the cache for all n tokens).  Supported: d_k, d_v in {64, 128};
+ * n * (h / g) <= 32 with bf16 / fp16 (tensor-core kernel), n * (h / g) <= 16
+ * with fp32 (CUDA-core kernel); otherwise GQA_ERR_UNSUPPORTED.  Other
+ * limits, errors and the workspace are those of gqa_decode_attn (the
+ * partials grow by the factor n).
  *
  * gqa_decode_step_multi - append and attention in one launch, as
  * gqa_decode_step does for one token: k_cache / v_cache are written at rows
@@ -356,7 +364,8 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  * num_sms > 0.
  *
  * b, n, h, g, d_k, d_v, cap, dtype: as for gqa_decode_attn_multi (n = 1 for
- * the one-token calls; for the paged calls cap = max_blocks * block_size).
+ * the one-token calls; for the paged calls cap = max_blocks * block_size);
+ * flags as for gqa_decode_step (0 for the calls without flags).
  * num_sms: SM count of the target device; 0 = that of the current device
  * (which then needs a GPU).  Outputs, each optional (NULL = not wanted):
  *   kernels          kernels one gqa_decode_attn* call launches: 1, or 2 when
@@ -372,8 +381,8 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  * pointer and alignment checks aside), or GQA_ERR_SHAPE for num_sms < 0.
  */
 int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int dtype,
-                    int num_sms, int* kernels, int* ctas, int* tile, int* tensor_core,
-                    long long* workspace_bytes);
+                    int flags, int num_sms, int* kernels, int* ctas, int* tile,
+                    int* tensor_core, long long* workspace_bytes);
 
 /* Name of a return code, for messages. */
 const char* gqa_status_string(int status);

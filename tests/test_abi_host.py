@@ -77,8 +77,8 @@ def _app(lib_, **kw):
     (dict(dk=0), -2), (dict(b=40000, g=8, h=8, cap=8000), -2),
     (dict(q=A + 8), -4), (dict(k=A + 2), -4), (dict(out=A + 4), -4), (dict(lens=A + 2), -4),
     (dict(dk=128, dv=32), -5), (dict(dk=96, dv=96), -5), (dict(h=64, g=1), -5),
-    (dict(dk=128, dv=64, h=32, g=2), -5),       # d_k != d_v: CUDA-core kernel, r <= 8 in bf16
-    (dict(dtype=0, h=34, g=1), -5), (dict(dtype=1, dk=64, dv=64, h=16, g=1), -5),
+    (dict(dk=128, dv=64, h=66, g=2), -5),       # 33 query rows per KV head
+    (dict(dtype=0, h=34, g=1), -5), (dict(dtype=0, dk=64, dv=128, h=17, g=1), -5),
 ])
 def test_decode_attn_host_checks(kw, code):
     assert _attn(_lib(), **kw) == code
@@ -138,7 +138,7 @@ def _attn_multi(lib_, **kw):
     (dict(h=6, g=4), -2), (dict(q=A + 8), -4),
     (dict(n=9, h=8, g=2), -5),                  # 9 * 4 query rows > 32
     (dict(n=3, dtype=0, h=12, g=2), -5),        # fp32: 18 rows > 16
-    (dict(n=2, dtype=1, dk=64, dv=64, h=10, g=2), -5),  # bf16 d=64: 10 rows > 8
+    (dict(n=3, dtype=1, dk=64, dv=128, h=22, g=2), -5),  # bf16: 33 rows > 32
     (dict(dtype=3), -3),
 ])
 def test_decode_attn_multi_host_checks(kw, code):
@@ -154,8 +154,10 @@ def test_multi_step_and_append_host_checks():
     bad[7] = 0
     assert f(*bad) == -2                             # n < 1
     bad = list(args)
-    bad[16] = 2
+    bad[16] = 4
     assert f(*bad) == -5                             # unknown flag bits
+    bad[16] = 2                                      # CUDA-core kernel: 12 rows > 8 in bf16
+    assert f(*bad) == -5
     app = b.lib.gqa_kv_append_multi
     aargs = [A, A, A, A, A, 2, 3, 2, 128, 128, 64, 1, None]
     bad = list(aargs)
@@ -228,7 +230,7 @@ def test_paged_host_checks():
     st = b.lib.gqa_decode_step_paged
     sargs = [A, A, A, A, A, A, A, 2, 1, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, 0, None]
     assert call(st, sargs, i1=0) == -1
-    assert call(st, sargs, i19=2) == -5               # unknown flag
+    assert call(st, sargs, i19=4) == -5               # unknown flag
     ap = b.lib.gqa_kv_append_paged
     aargs = [A, A, A, A, A, A, 2, 1, 2, 128, 128, 64, 4, 16, 1, None]
     assert call(ap, aargs, i4=0) == -1
@@ -257,12 +259,18 @@ def test_decode_plan_query():
         tiles = bb * g * -(-cap // p["tile"])
         assert 1 <= p["ctas"] == min(152, tiles)
         assert p["kernels"] == (2 if p["ctas"] > 2 * bb * g else 1)
-        assert p["tensor_core"] == (dt != "f32" and dk == dv == 128)
+        assert p["tensor_core"] == (dt != "f32")
         rows = n * h // g
         assert p["workspace_bytes"] == ((bb * g + p["ctas"]) * rows * (dv + 2) * 4
                                         + 2 * bb * g * 4)
+    # the CUDA-core kernel on request: bf16 up to 8 query rows per KV head
+    p = b.gqa_decode_plan(32, 1, 64, 8, 128, 128, 8192, "bf16", num_sms=152,
+                          flags=b.GQA_STEP_CUDA_CORES)
+    assert not p["tensor_core"] and p["tile"] == 64
     plan = b.lib.gqa_decode_plan
-    assert plan(2, 1, 8, 3, 128, 128, 64, 1, 152, None, None, None, None, None) == -2
-    assert plan(2, 1, 8, 2, 128, 128, 64, 7, 152, None, None, None, None, None) == -3
-    assert plan(2, 1, 8, 2, 96, 96, 64, 1, 152, None, None, None, None, None) == -5
-    assert plan(2, 1, 8, 2, 128, 128, 64, 1, -1, None, None, None, None, None) == -2
+    assert plan(2, 1, 8, 3, 128, 128, 64, 1, 0, 152, None, None, None, None, None) == -2
+    assert plan(2, 1, 8, 2, 128, 128, 64, 7, 0, 152, None, None, None, None, None) == -3
+    assert plan(2, 1, 8, 2, 96, 96, 64, 1, 0, 152, None, None, None, None, None) == -5
+    assert plan(2, 1, 8, 2, 128, 128, 64, 1, 0, -1, None, None, None, None, None) == -2
+    assert plan(2, 1, 32, 2, 128, 128, 64, 1, 2, 152, None, None, None, None, None) == -5
+    assert plan(2, 1, 8, 2, 128, 128, 64, 1, 4, 152, None, None, None, None, None) == -5

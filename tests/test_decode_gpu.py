@@ -23,15 +23,15 @@ def _b():
     return binding
 
 
-def run_step(cfg: DecodeConfig, lens, pad_fill=None, layer=0, check=True, fused=False):
-    """Append + attend on the GPU (two calls, or one fused gqa_decode_step),
-    oracle on the same host inputs; returns the max error."""
+def run_step(cfg: DecodeConfig, lens, pad_fill=None, layer=0, check=True, fused=False, flags=0):
+    """Append + attend on the GPU (two calls, or one fused gqa_decode_step
+    with `flags`), oracle on the same host inputs; returns the max error."""
     B = _b()
     x = make_layer(cfg, layer, "cpu", lens=np.asarray(lens, dtype=np.int32), pad_fill=pad_fill)
     d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
     out = torch.full((cfg.b, cfg.h, cfg.d), 3.0, dtype=cfg.torch_dtype, device="cuda")
     B.decode_step(d["q"], d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], d["seq_lens"],
-                  cfg.g, cfg.scale, out, fused=fused)
+                  cfg.g, cfg.scale, out, fused=fused, flags=flags)
     assert B.gqa_device_status() == 0
     tag = to_np(x["q"])[1]
     args = [to_np(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
@@ -53,7 +53,8 @@ def cfg_of(dtype, b, h, g, d, cap, seed=0, kind="plain"):
                         1.0 / math.sqrt(d), 100 + seed, kind=kind)
 
 
-# ---- CUDA-core kernel: fp32 (tile 64 at d=64, 32 at d=128), bf16 d=64 (tile 128)
+# ---- CUDA-core kernel: fp32 (tile 64 at d=64, 32 at d=128); 16-bit data on
+# request (tile 128 at d=64)
 @pytest.mark.parametrize("b,h,g,d,cap,lens", [
     (1, 8, 1, 64, 256, [256]),                  # the fp32 MQA workload shape
     (2, 8, 2, 64, 200, [1, 200]),
@@ -69,8 +70,13 @@ def test_simt_fp32(b, h, g, d, cap, lens):
 @pytest.mark.parametrize("b,h,g,cap,lens", [
     (2, 8, 1, 300, [300, 127]), (3, 4, 4, 260, [128, 129, 1]), (2, 14, 2, 513, [513, 200]),
 ])
-def test_simt_bf16_d64(b, h, g, cap, lens):
-    run_step(cfg_of("bf16", b, h, g, 64, cap, seed=cap), lens)
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_bf16_d64(b, h, g, cap, lens, cuda_cores):
+    """Head dim 64: the tensor-core kernel, and the CUDA-core kernel on
+    request (GQA_STEP_CUDA_CORES, fused step)."""
+    from gqa_kv_cache_append_gb300 import binding as B
+    flags = B.GQA_STEP_CUDA_CORES if cuda_cores else 0
+    run_step(cfg_of("bf16", b, h, g, 64, cap, seed=cap), lens, fused=cuda_cores, flags=flags)
 
 
 # ---- tensor-core kernel: bf16 d=128, tile 128, r padded to 16 or 32

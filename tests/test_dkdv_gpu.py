@@ -2,7 +2,7 @@
 P_v [h, d, v] let them), through the C ABI against the float64 oracle:
 contiguous and paged caches, fused and two-call steps, units held whole and
 split across CTAs (merged in the decode kernel and in the combine kernel),
-fp32 and bf16, on the CUDA-core kernel."""
+fp32 (CUDA-core kernel) and bf16 (tensor-core kernel)."""
 import math
 
 import numpy as np

@@ -1,7 +1,7 @@
 """fp16 storage (IEEE half, the other 2-byte format the pages name beside
 bf16) through the C ABI against the float64 oracle: the tensor-core kernel
 (one and n tokens, split units merged in the kernel and in the combine
-kernel), the CUDA-core kernel (head dim 64, d_k != d_v), the paged cache,
+kernel), head dim 64 and d_k != d_v, the paged cache,
 and the append (bit copies).  Bound: 1e-2 + 5e-3 |ref| (fp32 accumulation,
 fp16 inputs and softmax weights)."""
 import numpy as np
@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
     (3, 32, 1, 128, 2048, [2048, 1, 700]),     # r = 32
     (1, 8, 1, 128, 16384, [99 * 128 + 2]),     # one unit over many CTAs: combine kernel
     (96, 8, 1, 128, 384, [258] * 96),          # split units merged in the decode kernel
-    (3, 8, 2, 64, 300, [1, 65, 300]),          # head dim 64: CUDA-core kernel
+    (3, 8, 2, 64, 300, [1, 65, 300]),          # head dim 64
 ])
 @pytest.mark.parametrize("fused", [True, False])
 def test_f16_step(b, h, g, d, cap, lens, fused):

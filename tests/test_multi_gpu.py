@@ -99,7 +99,8 @@ def test_tc_multi_nan_padding():
               pad_fill=float("nan"))
 
 
-# ---- CUDA-core kernel: fp32 (tile 64 at d = 64, 32 at d = 128), bf16 d = 64
+# ---- CUDA-core kernel: fp32 (tile 64 at d = 64, 32 at d = 128); bf16 d = 64
+# (tensor-core kernel)
 @pytest.mark.parametrize("dtype,b,n,h,g,d,cap,lens", [
     ("f32", 3, 4, 8, 4, 64, 200, [4, 66, 200]),    # rows 62..65 straddle tiles
     ("f32", 2, 3, 5, 1, 128, 100, [3, 34]),        # 15 rows, tile 32

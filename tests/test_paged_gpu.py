@@ -4,8 +4,8 @@ against the float64 oracle on the same pool and table.
 The pools are the contiguous test caches scattered over a seeded random
 permutation of blocks (unused blocks filled with NaN, so a read outside the
 table would show).  Cases: block sizes 16..256 on the tensor-core kernel
-(several blocks per tile, and several tiles per block) and on the CUDA-core
-kernel (fp32 and bf16), ragged lengths at block and tile edges, units split
+(several blocks per tile, and several tiles per block) and with fp32 and
+head dim 64, ragged lengths at block and tile edges, units split
 across CTAs (merged in the decode kernel and in the combine kernel), the
 fused step against the two calls and against the contiguous cache (same
 bits), a bad table entry, and steps with n new tokens (the causal n-token
@@ -86,7 +86,8 @@ def test_tc_paged_two_calls():
     run_paged(cfg_of("bf16", 3, 16, 4, 128, 640, seed=5), [640, 300, 17], 64, fused=False)
 
 
-# ---- CUDA-core kernel: fp32 (tile 64 at d = 64, 32 at d = 128), bf16 d = 64 (tile 128)
+# ---- CUDA-core kernel: fp32 (tile 64 at d = 64, 32 at d = 128); bf16 d = 64 on
+# the tensor-core kernel
 @pytest.mark.parametrize("dtype,d,bs", [("f32", 64, 16), ("f32", 64, 64), ("f32", 64, 256),
                                         ("f32", 128, 16), ("bf16", 64, 32), ("bf16", 64, 128)])
 def test_simt_paged(dtype, d, bs):
