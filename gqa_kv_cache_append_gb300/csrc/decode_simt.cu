@@ -134,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = h / g;
   const int nr = nq * r;  // query rows ("heads" below) per KV head: t = s * r + head
 
-  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -143,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  pdl_wait();  // inputs and the split workspace are read only after this
+  pdl_wait_then_release();  // inputs and the split workspace are read only after this
   if (threadIdx.x >= 32 && threadIdx.x < 32 + RMAX) {
     const int t = threadIdx.x - 32;
     sM[t] = -INFINITY;

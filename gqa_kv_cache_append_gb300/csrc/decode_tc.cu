@@ -160,7 +160,6 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
   int* col_tok = reinterpret_cast<int*>(sm + C::OFF_COL);
   int* col_off = col_tok + NP;  // element offset of column c's output row
 
-  pdl_launch_dependents();
   if (threadIdx.x >= 64 && threadIdx.x < 64 + NP) {
     const int c = threadIdx.x - 64;
     const int s = c / r;
@@ -193,7 +192,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
   // or the cache rows below L_i - 1 (e.g. it is another layer's step), so
   // the producer plans and streams its first tiles before the wait, and
   // waits before loading q; the other warps wait at once.
-  if (!early || warp != 0) pdl_wait();
+  if (!early || warp != 0) pdl_wait_then_release();
   if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, nq, cap, status);
 
   Walker w;
@@ -237,7 +236,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
                (seg.lt0 * kT) / bsz);
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         if (!waited && (lt - seg.lt0 == kStages)) {
-          pdl_wait();
+          pdl_wait_then_release();
           waited = true;
           load_q(k, seg);
         }
@@ -277,13 +276,13 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         last_n[st] = static_cast<int>(n);
       }
       if (!waited) {
-        pdl_wait();
+        pdl_wait_then_release();
         waited = true;
         load_q(k, seg);
       }
       ++k;
     }
-    if (!waited) pdl_wait();
+    if (!waited) pdl_wait_then_release();
     if (*abort_flag && lane == 0) {
       for (int s = 0; s < kStages + 2; ++s) {
         int idx;
@@ -348,7 +347,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
               tma_prefetch_l2_2d(&tm_v, 0, rp);
               if (vh == 2) tma_prefetch_l2_2d(&tm_v, 64, rp);
             }
-            pdl_wait();
+            pdl_wait_then_release();
             waited = true;
             load_q(k, seg);
           }
@@ -368,13 +367,13 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
           last_n[st] = static_cast<int>(n);
         }
         if (!waited) {  // a first segment shorter than the ring
-          pdl_wait();
+          pdl_wait_then_release();
           waited = true;
           load_q(k, seg);
         }
         ++k;
       }
-      if (!waited) pdl_wait();  // a CTA with no tiles
+      if (!waited) pdl_wait_then_release();  // a CTA with no tiles
       if (*abort_flag) {  // copies in flight must land before the CTA exits
         for (int s = 0; s < kStages + 2; ++s) {
           int idx;

@@ -122,7 +122,6 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
   __shared__ float s_o[kCombineWarps][d];
   pdl_launch_dependents();
-  pdl_wait();  // the partials come from the decode kernel just before
   const int r = h / g;
   const int nr = nq * r;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -150,6 +149,10 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   long long c0, c1;
   unit_ctas(u0, u0 + ti, W, nc, c0, c1);
   if (c0 == c1) return;
+  // the lengths were read before the wait: the decode kernel releases this
+  // launch only after the kernel ahead of it (which may write seq_lens) has
+  // completed.  The partials come from the decode kernel itself.
+  pdl_wait();
   // this warp's pieces c0 + wid + 4k, in batches of 8 (every load of a batch
   // issued before any use); batches merge online (running max M, sums)
   constexpr int kBatch = 8;

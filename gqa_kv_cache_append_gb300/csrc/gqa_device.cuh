@@ -144,6 +144,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// The decode kernels let their dependents launch only once the kernel ahead
+// of them has completed, so a dependent may read before its own wait what
+// that kernel wrote (the combine kernel reads seq_lens so).  A decode CTA
+// cannot leave room for the next decode kernel before it exits anyway.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
