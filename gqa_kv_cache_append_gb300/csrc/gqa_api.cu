@@ -1,4 +1,3 @@
-#include <cstdlib>
 // gqa_api.cu - the C ABI of libgqa.so (declared in include/gqa.h): argument
 // checks, kernel selection, the split workspace, the device status word, and
 // the small kernels (KV append, wait self-test).
@@ -366,10 +365,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // the combine kernel instead (counters = null tells the decode kernel).
 // Units split over more CTAs than twice the unit count are merged by the
 // combine kernel; fewer splits are merged inside the decode kernel.
-bool use_combine_kernel(long long nc, int b, int g) {
-  static const long long f = getenv("GQA_XFACTOR") ? atoll(getenv("GQA_XFACTOR")) : 2;
-  return nc > f * b * g;
-}
+bool use_combine_kernel(long long nc, int b, int g) { return nc > 2ll * b * g; }
 
 int launch_all(DecodeLaunch& a, int tile) {
   const bool separate = use_combine_kernel(a.nc, a.b, a.g);

@@ -273,6 +273,25 @@ def test_in_kernel_merge_is_deterministic(dtype, h, g, d):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
+@pytest.mark.parametrize("b,h,g,cap", [(1, 8, 1, 20000), (8, 32, 1, 8192), (5, 16, 2, 6000)])
+def test_combine_kernel_is_deterministic(b, h, g, cap):
+    """Units over many CTAs merged by the combine kernel (up to ~150 pieces a
+    unit, ragged lengths): fixed merge order, the same bits every run."""
+    B = _b()
+    assert B.gqa_decode_plan(b, 1, h, g, 128, 128, cap, "bf16")["kernels"] == 2
+    cfg = cfg_of("bf16", b, h, g, 128, cap, seed=b + h)
+    lens = np.random.default_rng(b).integers(cap // 2, cap + 1, b).astype(np.int32)
+    x = make_layer(cfg, 0, "cuda", lens=lens)
+    outs = []
+    for _ in range(3):
+        out = torch.empty((cfg.b, cfg.h, cfg.d), dtype=cfg.torch_dtype, device="cuda")
+        B.gqa_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], cfg.b, cfg.h,
+                          cfg.g, 128, 128, cfg.scale, out)
+        outs.append(bits(out))
+    assert B.gqa_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
 def test_bad_length_is_reported_and_other_rows_are_right():
     B = _b()
     cfg = cfg_of("bf16", 3, 16, 2, 128, 300, seed=2)
