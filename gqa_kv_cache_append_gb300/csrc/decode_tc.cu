@@ -17,15 +17,20 @@
 // 128 (the unloaded half of the V stage feeds output rows 64-127, which
 // are never read).
 //
-// Roles (192 threads, one persistent CTA per SM):
+// Roles (224 or 352 threads, one persistent CTA per SM):
 //   warp 0     TMA producer: Q block once per segment, then K and V tiles
 //              (64-column boxes, 128-byte swizzle) into a 3-stage
 //              ring, completing on mbarriers.  Each K/V byte is read from
 //              HBM once and serves all r query heads.
-//   warp 1     allocates tensor memory; one lane issues the MMAs:
-//              S(n) before O(n-1), so the softmax of tile n overlaps the
-//              V product of tile n-1.  S and O are double-buffered in TMEM.
-//   warps 2-5  softmax and correction (128 threads): thread x owns TMEM lane
+//   warp 1     allocates tensor memory; one lane issues the S products as
+//              soon as a tile's K has landed, so the softmax of tile n
+//              overlaps the V product of tile n-1.
+//   warp 2     one lane issues the O products as soon as a tile's P is
+//              ready, independently of warp 1 (a stage is freed for the
+//              next copy without waiting for the following tile's K).
+//              S and O are double-buffered in TMEM.
+//   warps 3-6  softmax and correction (128 threads; a second warpgroup,
+//              warps 7-10, for 32 query rows): thread x owns TMEM lane
 //              x, i.e. position x of the tile for S and output column x for
 //              O.  Per tile: load S, mask p >= L_i, per-head max across the
 //              128 positions (redux.sync.max.f32 + one shared-memory
@@ -71,7 +76,7 @@ constexpr int kPrefetchTiles = 3;
 // because the 32-column variant runs at its register limit.
 template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true>
 struct TcCfg {
-  static constexpr int THREADS = 64 + 128 * NWG;  // producer, MMA, NWG softmax warpgroups
+  static constexpr int THREADS = 96 + 128 * NWG;  // producer, 2 MMA issuers, NWG softmax warpgroups
   static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
   static constexpr int Q_BYTES = NP * 256;         // two [NP x 64] boxes
   static constexpr int P_BYTES = kT * NP * 2;      // [T rows x NP] bf16
@@ -118,7 +123,7 @@ enum {
 };
 
 template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
-__global__ void __launch_bounds__(64 + 128 * NWG, 1)
+__global__ void __launch_bounds__(96 + 128 * NWG, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ lens,
@@ -172,6 +177,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       if ((k >= B_S_FREE && k < B_S_FREE + 2) || (k >= B_P_READY && k < B_P_READY + 2) ||
           (k >= B_O_FREE && k < B_O_FREE + 2))
         cnt = 4 * NWG;  // one arrival per softmax warp
+      if (k == B_DRAIN) cnt = 2;  // one per MMA issuer
       mbar_init(BAR(k), cnt);
     }
     *abort_flag = 0;
@@ -401,14 +407,25 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ============================ MMA issuer ============================
-    // Lane 0 issues the MMAs.  With the append fused in, the warp also
-    // carries the new tokens' K rows that fall in the segment (16-byte
-    // chunks, loaded at the segment start) to their tiles, where it patches
-    // them into the staged tile and writes them to the cache.
+  } else if (warp == 1 || warp == 2) {
+    // ============================ MMA issuers ===========================
+    // Lane 0 of warp 1 issues the S products, lane 0 of warp 2 the O
+    // products: each waits only for its own operands, so a tile's O product
+    // (which frees its stage for the next copy) never queues behind the next
+    // tile's K.  With the append fused in, warp 1 also carries the new
+    // tokens' K rows that fall in the segment (16-byte chunks, loaded at the
+    // segment start) to their tiles, where it patches them into the staged
+    // tile and writes them to the cache; with n tokens warp 2 does the same
+    // for V before the tile's O product.
+    const bool s_role = warp == 1;
     const bool leader = lane == 0;
     const uint32_t tS = tmem, tO = tmem + 2 * NP;
+    // operand descriptors, built once: a stage, a buffer or a k-step only
+    // moves the start-address field (16-byte units, no carry out of it)
+    const uint64_t dk0 = smem_desc(s_base, 16, 1024, SWZ_128B);               // K tiles
+    const uint64_t dq0 = smem_desc(s_base + C::OFF_Q, 16, 1024, SWZ_128B);    // q blocks
+    const uint64_t dv0 = smem_desc(s_base + 2 * kBoxBytes, kBoxBytes, 1024, SWZ_128B);  // V^T
+    const uint64_t dp0 = smem_desc(s_base + C::OFF_P, C::P_BYTES, 8 * NP * 2, C::P_SWZ);  // P^T
     auto issue_o = [&](uint32_t m) {
       const int st = m % kStages;
       const uint32_t nb = m & 1;
@@ -419,19 +436,17 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       tc_fence_after();
       if (leader) {
         if (ok) {
-          const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
-          const uint32_t pbase = s_base + C::OFF_P + nb * C::P_BYTES;
+          const uint64_t a0 = dv0 + ((st * C::KV_BYTES) >> 4);
+          const uint64_t b0 = dp0 + ((nb * C::P_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
             // A = V^T: M = 128 head-dim columns (two 64-column boxes, LBO
-            // apart), K = 16 positions (two 8-row groups, SBO apart).  With
-            // d_v = 64 the second box is not loaded: output rows 64-127 are
-            // never read.
-            const uint64_t a = smem_desc(vbase + kk * 2048, kBoxBytes, 1024, SWZ_128B);
-            // B = P^T: N = NP heads contiguous per row, K = 16 position rows
-            const uint64_t bd =
-                smem_desc(pbase + kk * 16 * NP * 2, C::P_BYTES, 8 * NP * 2, C::P_SWZ);
-            mma_bf16(tO + nb * NP, a, bd, C::IDESC_O, kk > 0 ? 1u : 0u);
+            // apart), K = 16 positions (two 8-row groups, SBO apart; 2 KiB
+            // a step).  With d_v = 64 the second box is not loaded: output
+            // rows 64-127 are never read.  B = P^T: N = NP heads contiguous
+            // per row, K = 16 position rows (16 * NP * 2 bytes a step).
+            mma_bf16(tO + nb * NP, a0 + kk * (2048 >> 4), b0 + kk * ((16 * NP * 2) >> 4),
+                     C::IDESC_O, kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(BAR(B_O_FULL + nb));
@@ -439,8 +454,7 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       }
       __syncwarp();
     };
-    uint32_t n = 0, k = 0, prev = 0;
-    bool have_prev = false;
+    uint32_t n = 0, k = 0;
     while (w.next(seg)) {
       const uint32_t qs = k & 1;
       const size_t unit = static_cast<size_t>(seg.i) * g + seg.j;
@@ -479,13 +493,13 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
       for (int c4 = 0; c4 < C::KCH; ++c4) {
         const int idx = lane + 32 * c4;
         knew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, shk));
+        if (s_role && idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, shk));
       }
 #pragma unroll
       for (int c4 = 0; c4 < VCH; ++c4) {
         const int idx = lane + 32 * c4;
         vnew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (MULTI && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
+        if (MULTI && !s_role && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
       }
       // put chunk ch (value v) into row `rho` of a staged tile (64-column
       // boxes, 128-byte swizzle) and into the cache at `pos` (rows of 2^sh
@@ -530,9 +544,28 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         }
         fence_proxy_async_smem();
       };
+      if (!s_role) {
+        // O products, in tile order
+        for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          const bool new_rows = nrows > 0 && (lt + 1) * kT > first_new;
+          if (MULTI && new_rows) {
+            // the tile's new V rows, before its O product (the softmax
+            // warps zero the rows past L_i, which are other rows)
+            const int st = n % kStages;
+            const bool vok = __all_sync(
+                0xffffffffu,
+                mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget));
+            if (vok) patch(s_base + st * C::KV_BYTES + 2 * kBoxBytes, v_cache_w, v_new, vnew,
+                           VCH, lt, shv);
+            __syncwarp();
+          }
+          issue_o(n);
+        }
+        ++k;
+        continue;
+      }
       const bool qok = __all_sync(
           0xffffffffu, mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget));
-      const uint32_t qbase = s_base + C::OFF_Q + qs * C::Q_BYTES;
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         const int st = n % kStages;
         const uint32_t nb = n & 1;
@@ -551,41 +584,30 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
         tc_fence_after();
         if (leader) {
           if (ok) {
+            const uint64_t a0 = dk0 + ((st * C::KV_BYTES) >> 4);
+            const uint64_t b0 = dq0 + ((qs * C::Q_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
-              // A = K tile, K-major: 128 rows, 16 head-dim columns per step;
-              // steps 0-3 in the first 64-column box, 4-7 in the second
-              // (d_k = 128 only)
+              // A = K tile, K-major: 128 rows, 16 head-dim columns (32
+              // bytes) per step; steps 0-3 in the first 64-column box, 4-7
+              // in the second (d_k = 128 only).  B = the q block, the same
+              // way ([NP x 64] boxes).
               if (kk >= 4 * kh) break;
-              const uint64_t a =
-                  smem_desc(kbase + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024, SWZ_128B);
-              const uint64_t bq =
-                  smem_desc(qbase + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024, SWZ_128B);
-              mma_bf16(tS + nb * NP, a, bq, C::IDESC, kk > 0 ? 1u : 0u);
+              mma_bf16(tS + nb * NP, a0 + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
+                       b0 + (((kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4), C::IDESC,
+                       kk > 0 ? 1u : 0u);
             }
           }
           mma_commit(BAR(B_S_FULL + nb));
           if (lt == seg.lt1 - 1) mma_commit(BAR(B_Q_EMPTY + qs));
         }
         __syncwarp();
-        if (have_prev) issue_o(prev);
-        if (MULTI && new_rows) {
-          // the same for v_new, before this tile's O product is issued (the
-          // softmax warps zero the rows past L_i, which are other rows)
-          const bool vok = __all_sync(
-              0xffffffffu,
-              mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget));
-          if (vok) patch(kbase + 2 * kBoxBytes, v_cache_w, v_new, vnew, VCH, lt, shv);
-          __syncwarp();
-        }
-        have_prev = true;
-        prev = n;
       }
       ++k;
     }
-    if (have_prev) issue_o(prev);
     if (leader) {
-      // every MMA must be finished before tensor memory is released
+      // every MMA of both issuers must be finished before tensor memory is
+      // released (the drain barrier takes one arrival from each)
       mma_commit(BAR(B_DRAIN));
       const long long t0 = clock64();
       while (!mbar_try_wait(BAR(B_DRAIN), 0) && clock64() - t0 < budget) {
@@ -599,8 +621,8 @@ __global__ void __launch_bounds__(64 + 128 * NWG, 1)
     // barrier 1 + wg, own split counter); the warpgroups share only the
     // staged tiles and the MMAs.
     constexpr int HP = NP / NWG;
-    const int wg = (warp - 2) >> 2;   // warpgroup
-    const int wq = (warp - 2) & 3;    // warp within the warpgroup
+    const int wg = (warp - 3) >> 2;   // warpgroup
+    const int wq = (warp - 3) & 3;    // warp within the warpgroup
     const int qd = warp & 3;          // TMEM lane quarter this warp may access
     const int row = qd * 32 + lane;   // tile position (S) / head-dim column (O)
     const int h0 = wg * HP;           // first head of this warpgroup
