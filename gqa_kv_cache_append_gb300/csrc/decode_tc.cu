@@ -70,6 +70,12 @@ constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 // (launches whose merge runs in a separate combine kernel skip it: there the
 // prefetch competes with the combine's reads of the partials in L2)
 constexpr int kPrefetchTiles = 3;
+// steady state with d_k = d_v = 64 (half-size tiles, the ring holds half
+// the bytes): when tile t's copies are issued, L2 is asked for tile
+// t + kL2Ahead of the same segment, so a copy that a freed stage starts
+// later finds its bytes in L2.  (With 128-wide heads HBM is already busy
+// and the extra requests made every measured shape slower.)
+constexpr int kL2Ahead = 3;
 
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
@@ -123,7 +129,9 @@ enum {
 };
 
 template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
-__global__ void __launch_bounds__(96 + 128 * NWG, 1)
+// (register cap: 11 warps put 3 on a sub-partition, 3 x 32 x 168 of its
+// 16384 registers; 7 warps put 2, so 200 fit)
+__global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ lens,
@@ -371,6 +379,13 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
           if (vh == 2)
             tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
           last_n[st] = static_cast<int>(n);
+          if (kh + vh == 2 && waited && lt + kL2Ahead < seg.lt1) {
+            const int rp = row + kL2Ahead * kT;
+            tma_prefetch_l2_2d(&tm_k, 0, rp);
+            if (kh == 2) tma_prefetch_l2_2d(&tm_k, 64, rp);
+            tma_prefetch_l2_2d(&tm_v, 0, rp);
+            if (vh == 2) tma_prefetch_l2_2d(&tm_v, 64, rp);
+          }
         }
         if (!waited) {  // a first segment shorter than the ring
           pdl_wait_then_release();
@@ -420,12 +435,8 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
     const bool s_role = warp == 1;
     const bool leader = lane == 0;
     const uint32_t tS = tmem, tO = tmem + 2 * NP;
-    // operand descriptors, built once: a stage, a buffer or a k-step only
-    // moves the start-address field (16-byte units, no carry out of it)
-    const uint64_t dk0 = smem_desc(s_base, 16, 1024, SWZ_128B);               // K tiles
-    const uint64_t dq0 = smem_desc(s_base + C::OFF_Q, 16, 1024, SWZ_128B);    // q blocks
-    const uint64_t dv0 = smem_desc(s_base + 2 * kBoxBytes, kBoxBytes, 1024, SWZ_128B);  // V^T
-    const uint64_t dp0 = smem_desc(s_base + C::OFF_P, C::P_BYTES, 8 * NP * 2, C::P_SWZ);  // P^T
+    // operand descriptors: a stage, a buffer or a k-step only moves the
+    // start-address field (16-byte units, no carry out of it)
     auto issue_o = [&](uint32_t m) {
       const int st = m % kStages;
       const uint32_t nb = m & 1;
@@ -436,8 +447,10 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
       tc_fence_after();
       if (leader) {
         if (ok) {
-          const uint64_t a0 = dv0 + ((st * C::KV_BYTES) >> 4);
-          const uint64_t b0 = dp0 + ((nb * C::P_BYTES) >> 4);
+          const uint64_t a0 =
+              smem_desc(s_base + st * C::KV_BYTES + 2 * kBoxBytes, kBoxBytes, 1024, SWZ_128B);
+          const uint64_t b0 =
+              smem_desc(s_base + C::OFF_P + nb * C::P_BYTES, C::P_BYTES, 8 * NP * 2, C::P_SWZ);
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
             // A = V^T: M = 128 head-dim columns (two 64-column boxes, LBO
@@ -488,19 +501,6 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
       }
       // (one token: the softmax warps carry and patch the V row)
       constexpr int VCH = MULTI ? C::KCH : 1;
-      uint4 knew[C::KCH], vnew[VCH];
-#pragma unroll
-      for (int c4 = 0; c4 < C::KCH; ++c4) {
-        const int idx = lane + 32 * c4;
-        knew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (s_role && idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, shk));
-      }
-#pragma unroll
-      for (int c4 = 0; c4 < VCH; ++c4) {
-        const int idx = lane + 32 * c4;
-        vnew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (MULTI && !s_role && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
-      }
       // put chunk ch (value v) into row `rho` of a staged tile (64-column
       // boxes, 128-byte swizzle) and into the cache at `pos` (rows of 2^sh
       // chunks)
@@ -546,6 +546,13 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
       };
       if (!s_role) {
         // O products, in tile order
+        uint4 vnew[VCH];
+#pragma unroll
+        for (int c4 = 0; c4 < VCH; ++c4) {
+          const int idx = lane + 32 * c4;
+          vnew[c4] = make_uint4(0u, 0u, 0u, 0u);
+          if (MULTI && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
+        }
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
           const bool new_rows = nrows > 0 && (lt + 1) * kT > first_new;
           if (MULTI && new_rows) {
@@ -563,6 +570,13 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
         }
         ++k;
         continue;
+      }
+      uint4 knew[C::KCH];
+#pragma unroll
+      for (int c4 = 0; c4 < C::KCH; ++c4) {
+        const int idx = lane + 32 * c4;
+        knew[c4] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, shk));
       }
       const bool qok = __all_sync(
           0xffffffffu, mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget));
@@ -584,8 +598,8 @@ __global__ void __launch_bounds__(96 + 128 * NWG, 1)
         tc_fence_after();
         if (leader) {
           if (ok) {
-            const uint64_t a0 = dk0 + ((st * C::KV_BYTES) >> 4);
-            const uint64_t b0 = dq0 + ((qs * C::Q_BYTES) >> 4);
+            const uint64_t a0 = smem_desc(s_base + st * C::KV_BYTES, 16, 1024, SWZ_128B);
+            const uint64_t b0 = smem_desc(s_base + C::OFF_Q + qs * C::Q_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               // A = K tile, K-major: 128 rows, 16 head-dim columns (32
