@@ -611,6 +611,13 @@ int decode_check(const DecodeArgs& x) {
   return GQA_OK;
 }
 
+// Fewer (sequence, KV head) units than CTAs: a whole number of CTAs per
+// unit, so that every unit is cut into the same number of equal pieces and
+// no CTA spans two units (fewer pieces to merge, no CTA waiting on two).
+long long aligned_ctas(long long ctas, long long units) {
+  return (units < ctas && 2 * units <= ctas) ? units * (ctas / units) : ctas;
+}
+
 DecodePlan decode_plan(const DecodeArgs& x, int num_sms) {
   const int r = x.h / x.g, d = x.d_k, cols = x.nq * r;
   const bool use_tc = use_tensor_cores(x, cols);
@@ -618,7 +625,7 @@ DecodePlan decode_plan(const DecodeArgs& x, int num_sms) {
   p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, x.d_k, x.d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(x.dtype, d, r);
   const long long max_tiles = static_cast<long long>(x.b) * x.g * ((x.cap + p.tile - 1) / p.tile);
-  p.nc = static_cast<long long>(num_sms) * per_sm;
+  p.nc = aligned_ctas(static_cast<long long>(num_sms) * per_sm, static_cast<long long>(x.b) * x.g);
   if (p.nc > max_tiles) p.nc = max_tiles;
   if (p.nc < 1) p.nc = 1;
   const size_t slots = static_cast<size_t>(x.b) * x.g + static_cast<size_t>(p.nc);
@@ -1074,7 +1081,8 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
   const int tile = use_tc ? tc_tile() : simt_tile(dtype, d_k, d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(dtype, d, r);
   const long long max_tiles = static_cast<long long>(b) * g * ((cap + tile - 1) / tile);
-  long long nc = static_cast<long long>(nd->num_sms) * per_sm;
+  long long nc = aligned_ctas(static_cast<long long>(nd->num_sms) * per_sm,
+                             static_cast<long long>(b) * g);
   if (nc > max_tiles) nc = max_tiles;
   if (nc < 1) nc = 1;
   const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);

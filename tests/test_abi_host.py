@@ -240,7 +240,8 @@ def test_paged_host_checks():
 
 def test_decode_plan_query():
     """gqa_decode_plan on the host (SM count given): persistent grid of at
-    most one CTA per SM and at most one per tile, the combine kernel exactly
+    most one CTA per SM and at most one per tile (with fewer (sequence, KV
+    head) units than SMs, a whole number of CTAs per unit), the combine kernel exactly
     when the CTAs outnumber twice the units, the workspace of the partials
     ((b*g + C) * rows * (d_v + 2) floats) plus 2*b*g counters."""
     b = _lib()
@@ -253,11 +254,15 @@ def test_decode_plan_query():
     assert p["tensor_core"] and p["kernels"] == 1
     for (bb, n, h, g, dk, dv, cap, dt) in [(1, 1, 8, 1, 64, 64, 256, "f32"),
                                            (3, 1, 8, 2, 128, 64, 1000, "bf16"),
+                                           (5, 1, 8, 2, 128, 128, 20000, "bf16"),
                                            (64, 1, 28, 4, 128, 128, 32768, "bf16"),
                                            (1, 1, 8, 8, 128, 128, 1, "bf16")]:
         p = b.gqa_decode_plan(bb, n, h, g, dk, dv, cap, dt, num_sms=152)
         tiles = bb * g * -(-cap // p["tile"])
-        assert 1 <= p["ctas"] == min(152, tiles)
+        units = bb * g
+        # fewer units than SMs: a whole number of CTAs per unit
+        aligned = units * (152 // units) if 2 * units <= 152 else 152
+        assert 1 <= p["ctas"] == min(aligned, tiles)
         assert p["kernels"] == (2 if p["ctas"] > 2 * bb * g else 1)
         assert p["tensor_core"] == (dt != "f32")
         rows = n * h // g
