@@ -104,9 +104,9 @@ struct TcCfg {
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
   static constexpr uint32_t IDESC = idesc_bf16(128, NP, 0, 0, BF16);    // S: K-major A, B
   static constexpr uint32_t IDESC_O = idesc_bf16(128, NP, 1, 1, BF16);  // O: MN-major A, B
-  // new-row chunks the MMA warp carries in registers per lane for the fused
-  // append (one token: K only, lanes 0-15; n tokens: 4 rows of K and of V);
-  // further rows are loaded when patched
+  // new-row chunks an MMA-issuing warp carries in registers per lane for the
+  // fused append (one token: K only, d_k / 8 lanes; n tokens: up to 4 rows
+  // of K in warp 1 and of V in warp 2); further rows are loaded when patched
   static constexpr int KCH = MULTI ? 2 : 1;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
@@ -811,7 +811,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         }
         // ---- last tile of a unit (warpgroup 0): zero the V rows past L_i;
         // one token: put v_new into row L_i - 1 and into the cache (n
-        // tokens: the MMA warp patches the new rows) ----
+        // tokens: the O-issuing warp patches the new rows) ----
         const bool patch_v = append_v && lt == seg.ti - 1;
         if (wg == 0 && (valid < kT || patch_v)) {
           const bool vok =
