@@ -170,10 +170,12 @@ def measured_peaks() -> dict:
 
 
 def profiled_traffic(kernel_src: str, workload: str, n: int = 1):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (matched by hash), else None."""
+    """dram bytes per launch from the committed ncu summary of the kernel in
+    `kernel_src` (profiles/<kernel>_<workload>.md), if it was taken on the
+    current kernel source (matched by hash), else None."""
     tag = workload if n == 1 else f"{workload}_n{n}"
-    path = os.path.join(ROOT, "profiles", f"decode_tc_{tag}.md")
+    kernel = os.path.splitext(os.path.basename(kernel_src))[0]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{tag}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -502,14 +504,15 @@ def run_ours(args, rank, local_rank, world):
     peaks = measured_peaks()
     call_bytes = sb["attn_per_layer"] + sb["append_per_layer"] + sb.get("proj_per_layer", 0)
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
-    src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", "decode_tc.cu")
+    plan = B.gqa_decode_plan(cfg.b, n, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.cap, cfg.dtype,
+                             flags=cuda_cores)
+    src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc",
+                       "decode_tc.cu" if plan["tensor_core"] else "decode_simt.cu")
     # the committed ncu summary covers the named workload's own shapes only
     reshaped = any(v is not None for v in (args.g, args.h, args.b, args.cap, args.d, args.dv,
                                            args.dtype)) or args.cuda_cores
     traffic = (None if (full_layer or paged or reshaped)
                else profiled_traffic(src, args.workload, n))
-    plan = B.gqa_decode_plan(cfg.b, n, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.cap, cfg.dtype,
-                             flags=cuda_cores)
     # per layer: the decode call's kernels (decode, plus combine when the
     # split partials are merged apart), + 2 projections or + 1 separate append
     launches_per_step = (plan["kernels"] + (2 if full_layer else (1 if args.separate else 0))

@@ -71,7 +71,7 @@ def test_ragged_lengths_bytes():
 
 
 def test_traffic_lookup_requires_matching_source(tmp_path, monkeypatch):
-    src = tmp_path / "k.cu"
+    src = tmp_path / "decode_tc.cu"
     src.write_text("kernel v1")
     prof = tmp_path / "profiles"
     prof.mkdir()
@@ -82,6 +82,10 @@ def test_traffic_lookup_requires_matching_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic(str(src), "w") == 1234
     src.write_text("kernel v2")
     assert bench.profiled_traffic(str(src), "w") is None
+    # the summary is looked up by the kernel's own name
+    other = tmp_path / "decode_simt.cu"
+    other.write_text("kernel v1")
+    assert bench.profiled_traffic(str(other), "w") is None
 
 
 def test_reference_arm_line(capsys):
