@@ -611,9 +611,11 @@ int decode_check(const DecodeArgs& x) {
   return GQA_OK;
 }
 
-// Fewer (sequence, KV head) units than CTAs: a whole number of CTAs per
-// unit, so that every unit is cut into the same number of equal pieces and
-// no CTA spans two units (fewer pieces to merge, no CTA waiting on two).
+// Fewer (sequence, KV head) units than CTAs, at most half as many: a whole
+// number of CTAs per unit, so that every unit is cut into the same number
+// of equal pieces and no CTA spans two units.  (With at least 70 % as many
+// units as CTAs and equal lengths, the kernels themselves take one CTA per
+// unit; see Walker::init.)
 long long aligned_ctas(long long ctas, long long units) {
   return (units < ctas && 2 * units <= ctas) ? units * (ctas / units) : ctas;
 }

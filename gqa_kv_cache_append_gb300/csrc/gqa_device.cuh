@@ -427,19 +427,30 @@ struct Walker {
   long long pos, end;  // global tile cursor and end of this CTA's range
   int i, j, lt, ti, L;
 
-  // total tiles W (warp-cooperative; all lanes get the result)
+  // total tiles W (warp-cooperative; all lanes get the result); `equal`:
+  // every sequence has the same, nonzero, number of tiles
   __device__ static long long total_tiles(const int* lens, int b, int g, int lmin, int cap,
-                                         int T) {
+                                         int T, bool* equal = nullptr) {
     const int lane = threadIdx.x & 31;
     long long acc = 0;
+    int tmin = 0x7fffffff, tmax = 0;
     for (int base = 0; base < b; base += 32) {
       const int idx = base + lane;
       int t = 0;
-      if (idx < b) t = seq_tiles(__ldg(lens + idx), lmin, cap, T);
+      if (idx < b) {
+        t = seq_tiles(__ldg(lens + idx), lmin, cap, T);
+        tmin = min(tmin, t);
+        tmax = max(tmax, t);
+      }
       acc += t;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+      tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    }
+    if (equal) *equal = tmin == tmax && tmin > 0;
     return acc * g;
   }
 
@@ -453,10 +464,18 @@ struct Walker {
     lmin = lmin_;
     cap = cap_;
     T = T_;
-    W = total_tiles(lens, b, g, lmin, cap, T);
+    bool equal = false;
+    W = total_tiles(lens, b, g, lmin, cap, T, &equal);
+    // Equal lengths and at least 70 % as many units as CTAs: one CTA per
+    // unit, the CTAs past the units idle (no piece to merge; measured faster
+    // than cutting the units over every SM: 128 units on 152 SMs 46.9 ->
+    // 42.5 us per call, while with ragged lengths it was slower)
+    const long long units = static_cast<long long>(b) * g;
+    if (equal && units < nc && 10 * units >= 7 * static_cast<long long>(nc))
+      nc = static_cast<int>(units);
     this->nc = nc;
-    pos = (W * c) / nc;
-    end = (W * (c + 1)) / nc;
+    pos = c < nc ? (W * c) / nc : W;
+    end = c < nc ? (W * (c + 1)) / nc : W;
     i = b;
     j = 0;
     lt = 0;

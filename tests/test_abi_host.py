@@ -255,12 +255,15 @@ def test_decode_plan_query():
     for (bb, n, h, g, dk, dv, cap, dt) in [(1, 1, 8, 1, 64, 64, 256, "f32"),
                                            (3, 1, 8, 2, 128, 64, 1000, "bf16"),
                                            (5, 1, 8, 2, 128, 128, 20000, "bf16"),
+                                           (16, 1, 32, 8, 128, 128, 4096, "bf16"),
+                                           (12, 1, 32, 8, 128, 128, 4096, "bf16"),
                                            (64, 1, 28, 4, 128, 128, 32768, "bf16"),
                                            (1, 1, 8, 8, 128, 128, 1, "bf16")]:
         p = b.gqa_decode_plan(bb, n, h, g, dk, dv, cap, dt, num_sms=152)
         tiles = bb * g * -(-cap // p["tile"])
         units = bb * g
-        # fewer units than SMs: a whole number of CTAs per unit
+        # fewer units than SMs, at most half as many: a whole number of CTAs
+        # per unit
         aligned = units * (152 // units) if 2 * units <= 152 else 152
         assert 1 <= p["ctas"] == min(aligned, tiles)
         assert p["kernels"] == (2 if p["ctas"] > 2 * bb * g else 1)
