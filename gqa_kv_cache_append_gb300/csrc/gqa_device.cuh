@@ -455,9 +455,11 @@ struct Walker {
   }
 
   // Position the walker at CTA `c` of `nc`; sequences shorter than lmin
-  // (the step's new tokens) are skipped.  Warp-cooperative.
+  // (the step's new tokens) are skipped.  whole_max: with equal lengths,
+  // CTAs may take up to this many whole units each (0: never).
+  // Warp-cooperative.
   __device__ void init(const int* lens_, int b_, int g_, int lmin_, int cap_, int T_, int c,
-                       int nc) {
+                       int nc, int whole_max = 0) {
     lens = lens_;
     b = b_;
     g = g_;
@@ -466,13 +468,20 @@ struct Walker {
     T = T_;
     bool equal = false;
     W = total_tiles(lens, b, g, lmin, cap, T, &equal);
-    // Equal lengths and at least 70 % as many units as CTAs: one CTA per
-    // unit, the CTAs past the units idle (no piece to merge; measured faster
-    // than cutting the units over every SM: 128 units on 152 SMs 46.9 ->
-    // 42.5 us per call, while with ragged lengths it was slower)
+    // Equal lengths: k = 1 or 2 whole units per CTA when that still uses at
+    // least 70 % of the CTAs, the rest idle (no piece to merge).  Measured on
+    // the tensor-core kernel: 128 units on 152 SMs 46.9 -> 42.5 us per call
+    // (64-wide heads 35.5 -> 31.1), 256 units of 128-wide heads two per CTA
+    // 153.2 -> 151.2; slower with two per CTA at 64-wide heads (a CTA's own
+    // loop is the limit there), with four per CTA, and, decided on the host,
+    // with ragged lengths.
     const long long units = static_cast<long long>(b) * g;
-    if (equal && units < nc && 10 * units >= 7 * static_cast<long long>(nc))
-      nc = static_cast<int>(units);
+    if (equal && whole_max > 0) {
+      const long long k = (units + nc - 1) / nc;  // units per CTA
+      if (k <= whole_max && units % k == 0 && units / k < nc &&
+          10 * (units / k) >= 7 * static_cast<long long>(nc))
+        nc = static_cast<int>(units / k);
+    }
     this->nc = nc;
     pos = c < nc ? (W * c) / nc : W;
     end = c < nc ? (W * (c + 1)) / nc : W;

@@ -374,10 +374,12 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  *                    kernel (gqa_decode_step* launch the same number; the
  *                    append is fused)
  *   ctas             CTAs the decode kernel is launched with (persistent: at
- *                    most num_sms).  When all sequences have the same number
- *                    of tiles and there are at least 70 % as many (sequence,
- *                    KV head) units as CTAs, the kernel gives each unit one
- *                    CTA and the others exit at once.
+ *                    most num_sms).  On the tensor-core kernel, when all
+ *                    sequences have the same number of tiles and one whole
+ *                    (sequence, KV head) unit per CTA (or two, with d_k =
+ *                    d_v = 128) still uses at least 70 % of the CTAs, the
+ *                    kernel gives each CTA whole units and the others exit
+ *                    at once.
  *   tile             cache positions per tile
  *   tensor_core      1 for the tcgen05 kernel, 0 for the CUDA-core kernel
  *   workspace_bytes  split partials + arrival counters the call uses
