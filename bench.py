@@ -183,10 +183,20 @@ def profiled_traffic(kernel_src: str, workload: str, n: int = 1):
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     if not (m_hash and m_bytes):
         return None
-    src = open(kernel_src, "rb").read()
-    if hashlib.sha256(src).hexdigest() != m_hash.group(1):
+    if kernel_source_hash(kernel_src) != m_hash.group(1):
         return None
     return int(m_bytes.group(1))
+
+
+def kernel_source_hash(kernel_src: str) -> str:
+    """sha256 of the kernel's source followed by the device header it
+    includes (gqa_device.cuh, next to it: the tile walker, the merge
+    protocol and the barrier helpers live there)."""
+    h = hashlib.sha256(open(kernel_src, "rb").read())
+    header = os.path.join(os.path.dirname(kernel_src), "gqa_device.cuh")
+    if os.path.exists(header):
+        h.update(open(header, "rb").read())
+    return h.hexdigest()
 
 
 # ---------------------------------------------------------------------------

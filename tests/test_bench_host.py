@@ -73,12 +73,18 @@ def test_ragged_lengths_bytes():
 def test_traffic_lookup_requires_matching_source(tmp_path, monkeypatch):
     src = tmp_path / "decode_tc.cu"
     src.write_text("kernel v1")
+    (tmp_path / "gqa_device.cuh").write_text("header v1")
     prof = tmp_path / "profiles"
     prof.mkdir()
     import hashlib
-    h = hashlib.sha256(b"kernel v1").hexdigest()
+    h = hashlib.sha256(b"kernel v1header v1").hexdigest()
+    assert bench.kernel_source_hash(str(src)) == h
     (prof / "decode_tc_w.md").write_text(f"source_sha256: {h}\ntraffic_bytes_per_launch: 1234\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic(str(src), "w") == 1234
+    (tmp_path / "gqa_device.cuh").write_text("header v2")
+    assert bench.profiled_traffic(str(src), "w") is None   # the header changed
+    (tmp_path / "gqa_device.cuh").write_text("header v1")
     assert bench.profiled_traffic(str(src), "w") == 1234
     src.write_text("kernel v2")
     assert bench.profiled_traffic(str(src), "w") is None
