@@ -210,8 +210,10 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, nq, cap, status);
 
   Walker w;
-  // (two whole units per CTA only with 128-wide heads: see Walker::init)
-  w.init(lens, b, g, nq, cap, kT, blockIdx.x, gridDim.x, (kh == 2 && vh == 2) ? 2 : 1);
+  // (two whole units per CTA only with 128-wide heads, none on a paged
+  // cache, whose per-block copies need every SM: see Walker::init)
+  w.init(lens, b, g, nq, cap, kT, blockIdx.x, gridDim.x,
+         PAGED ? 0 : ((kh == 2 && vh == 2) ? 2 : 1));
   Segment seg;
 
   if (warp == 0 && PAGED) {

@@ -374,7 +374,8 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  *                    kernel (gqa_decode_step* launch the same number; the
  *                    append is fused)
  *   ctas             CTAs the decode kernel is launched with (persistent: at
- *                    most num_sms).  On the tensor-core kernel, when all
+ *                    most num_sms).  On the tensor-core kernel over a
+ *                    contiguous cache, when all
  *                    sequences have the same number of tiles and one whole
  *                    (sequence, KV head) unit per CTA (or two, with d_k =
  *                    d_v = 128) still uses at least 70 % of the CTAs, the
