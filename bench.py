@@ -619,7 +619,9 @@ def run_reference(args, rank, world):
     n = args.tokens
     if n > 1:
         cfg = dataclasses.replace(cfg, kind="plain")
-    per_step_s = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    # ~40 s of oracle work over the whole run: drawing each sample's inputs
+    # costs about twice that again, so the run ends in about two minutes
+    per_step_s = max(0.25, min(20.0, 40.0 / max(1, args.steps + args.warmup)))
     vals = []
     total_units = total_bytes = 0
     for k in range(args.warmup + args.steps):
