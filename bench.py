@@ -521,8 +521,8 @@ def run_ours(args, rank, local_rank, world):
     # the committed ncu summary covers the named workload's own shapes only
     reshaped = any(v is not None for v in (args.g, args.h, args.b, args.cap, args.d, args.dv,
                                            args.dtype)) or args.cuda_cores
-    traffic = (None if (full_layer or paged or reshaped)
-               else profiled_traffic(src, args.workload, n))
+    traffic = (None if (full_layer or reshaped)
+               else profiled_traffic(src, args.workload + (f"_paged{paged}" if paged else ""), n))
     # per layer: the decode call's kernels (decode, plus combine when the
     # split partials are merged apart), + 2 projections or + 1 separate append
     launches_per_step = (plan["kernels"] + (2 if full_layer else (1 if args.separate else 0))
