@@ -98,10 +98,59 @@ def status_string(code: int) -> str:
     return lib.gqa_status_string(int(code)).decode()
 
 
-def _ptr(x) -> int:
+def _ptr(x, name: str = "tensor", nbytes: int = 0, index: bool = False) -> int:
+    """Device address of a tensor argument (raw integers pass through
+    unchecked).  The kernels read and write whole extents through it, so a
+    host tensor, a strided view, a tensor smaller than the shapes passed
+    (nbytes) or, for lengths and block tables (index), another type than
+    int32 is refused here, before anything is launched."""
     if isinstance(x, torch.Tensor):
+        if not x.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous")
+        if index and x.dtype != torch.int32:
+            raise ValueError(f"{name}: must be int32, got {x.dtype}")
+        have = x.numel() * x.element_size()
+        if have < nbytes:
+            raise ValueError(f"{name}: holds {have} bytes, the shapes passed need {nbytes}")
+        if not x.is_cuda:
+            # reported by _call once every argument has been checked
+            return _HostTensor(name, x.device)
         return x.data_ptr()
     return int(x) if x is not None else 0
+
+
+class _HostTensor:
+    """Stands for a tensor argument that is not on a CUDA device."""
+
+    def __init__(self, name, device):
+        self.name, self.device = name, device
+
+
+def _call(fn_name: str, fn, *args) -> None:
+    """Call a library entry point once no argument is a host tensor; raise
+    GqaError on a non-zero return code."""
+    for a in args:
+        if isinstance(a, _HostTensor):
+            raise ValueError(f"{a.name}: a CUDA tensor is required, got one on {a.device}")
+    _check(fn_name, fn(*args))
+
+
+def _elt(code: int) -> int:
+    """Bytes per element of a dtype code (0 for an unknown code, which the
+    library rejects)."""
+    return {GQA_F32: 4, GQA_BF16: 2, GQA_F16: 2}.get(code, 0)
+
+
+def _n(*dims) -> int:
+    """Product of the dims, 0 when one is not positive (the library then
+    reports the shape error)."""
+    out = 1
+    for d in dims:
+        d = int(d)
+        if d <= 0:
+            return 0
+        out *= d
+    return out
 
 
 def _dtype(x, dtype) -> int:
@@ -136,10 +185,14 @@ def gqa_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, b, g, d_k, d_v,
     """Write row seq_lens[i] - 1 of every (i, j) of the caches (in place)."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_kv_append", lib.gqa_kv_append(
-        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
-        int(b), int(g), int(d_k), int(d_v), int(cap), _dtype(k_cache, dtype),
-        _stream(stream)))
+    dt = _dtype(k_cache, dtype)
+    e = _elt(dt)
+    _call("gqa_kv_append", lib.gqa_kv_append,
+        _ptr(k_new, "k_new", _n(b, g, d_k) * e), _ptr(v_new, "v_new", _n(b, g, d_v) * e),
+        _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True),
+        int(b), int(g), int(d_k), int(d_v), int(cap), dt, _stream(stream))
 
 
 def gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
@@ -147,10 +200,14 @@ def gqa_decode_attn(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
     """out[i, a, :] = softmax_p(scale * q[i, a] . K[i, a // (h/g), p]) V[...]."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_decode_attn", lib.gqa_decode_attn(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(h),
-        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
-        _dtype(q, dtype), _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    _call("gqa_decode_attn", lib.gqa_decode_attn,
+        _ptr(q, "q", _n(b, h, d_k) * e), _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True), int(b), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out, "out", _n(b, h, d_v) * e), int(cap),
+        dt, _stream(stream))
 
 
 def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v,
@@ -160,10 +217,15 @@ def gqa_decode_step(q, k_new, v_new, k_cache, v_cache, seq_lens, b, h, g, d_k, d
     ahead on the stream must not write seq_lens or this call's older rows)."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_decode_step", lib.gqa_decode_step(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
-        int(b), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
-        _dtype(q, dtype), int(flags), _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    _call("gqa_decode_step", lib.gqa_decode_step,
+        _ptr(q, "q", _n(b, h, d_k) * e), _ptr(k_new, "k_new", _n(b, g, d_k) * e),
+        _ptr(v_new, "v_new", _n(b, g, d_v) * e), _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True),
+        int(b), int(h), int(g), int(d_k), int(d_v), float(scale),
+        _ptr(out, "out", _n(b, h, d_v) * e), int(cap), dt, int(flags), _stream(stream))
 
 
 def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, scale,
@@ -175,10 +237,14 @@ def gqa_decode_attn_noalloc(q, k_cache, v_cache, seq_lens, b, h, g, d_k, d_v, sc
     capture (it looks up the array's device address)."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_decode_attn_noalloc", lib.gqa_decode_attn_noalloc(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(h),
-        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
-        _dtype(q, dtype), _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    _call("gqa_decode_attn_noalloc", lib.gqa_decode_attn_noalloc,
+        _ptr(q, "q", _n(b, h, d_k) * e), _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True), int(b), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out, "out", _n(b, h, d_v) * e), int(cap),
+        dt, _stream(stream))
 
 
 def gqa_kv_append_multi(k_new, v_new, k_cache, v_cache, seq_lens, b, n, g, d_k, d_v,
@@ -187,10 +253,14 @@ def gqa_kv_append_multi(k_new, v_new, k_cache, v_cache, seq_lens, b, n, g, d_k, 
     caches from k_new / v_new [b, n, g, d] (in place)."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_kv_append_multi", lib.gqa_kv_append_multi(
-        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
-        int(b), int(n), int(g), int(d_k), int(d_v), int(cap), _dtype(k_cache, dtype),
-        _stream(stream)))
+    dt = _dtype(k_cache, dtype)
+    e = _elt(dt)
+    _call("gqa_kv_append_multi", lib.gqa_kv_append_multi,
+        _ptr(k_new, "k_new", _n(b, n, g, d_k) * e), _ptr(v_new, "v_new", _n(b, n, g, d_v) * e),
+        _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True),
+        int(b), int(n), int(g), int(d_k), int(d_v), int(cap), dt, _stream(stream))
 
 
 def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v, scale,
@@ -199,10 +269,14 @@ def gqa_decode_attn_multi(q, k_cache, v_cache, seq_lens, b, n, h, g, d_k, d_v, s
     token s sees positions p <= seq_lens[i] - n + s."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_decode_attn_multi", lib.gqa_decode_attn_multi(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), int(b), int(n), int(h),
-        int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(cap),
-        _dtype(q, dtype), _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    _call("gqa_decode_attn_multi", lib.gqa_decode_attn_multi,
+        _ptr(q, "q", _n(b, n, h, d_k) * e), _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True), int(b), int(n), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(out, "out", _n(b, n, h, d_v) * e),
+        int(cap), dt, _stream(stream))
 
 
 def gqa_decode_step_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, g, d_k,
@@ -211,26 +285,40 @@ def gqa_decode_step_multi(q, k_new, v_new, k_cache, v_cache, seq_lens, b, n, h, 
     """Append the n new rows and attend causally, in one launch."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_decode_step_multi", lib.gqa_decode_step_multi(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
-        int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out),
-        int(cap), _dtype(q, dtype), int(flags), _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    _call("gqa_decode_step_multi", lib.gqa_decode_step_multi,
+        _ptr(q, "q", _n(b, n, h, d_k) * e), _ptr(k_new, "k_new", _n(b, n, g, d_k) * e),
+        _ptr(v_new, "v_new", _n(b, n, g, d_v) * e),
+        _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True),
+        int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale),
+        _ptr(out, "out", _n(b, n, h, d_v) * e), int(cap), dt, int(flags), _stream(stream))
 
 
 def gqa_project_qkv(x, w_q, w_k, w_v, q, k_new, v_new, b, d_model, h, g, d_k, d_v,
                     dtype=None, flags=0, stream=None) -> None:
     """q / k_new / v_new = x . P_q / P_k / P_v ("bd,hdk->bhk" and its KV forms)."""
-    _check("gqa_project_qkv", lib.gqa_project_qkv(
-        _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(q), _ptr(k_new), _ptr(v_new),
-        int(b), int(d_model), int(h), int(g), int(d_k), int(d_v), _dtype(x, dtype),
-        int(flags), _stream(stream)))
+    dt = _dtype(x, dtype)
+    e, D = _elt(dt), d_model
+    _call("gqa_project_qkv", lib.gqa_project_qkv,
+        _ptr(x, "x", _n(b, D) * e), _ptr(w_q, "w_q", _n(h, D, d_k) * e),
+        _ptr(w_k, "w_k", _n(g, D, d_k) * e), _ptr(w_v, "w_v", _n(g, D, d_v) * e),
+        _ptr(q, "q", _n(b, h, d_k) * e), _ptr(k_new, "k_new", _n(b, g, d_k) * e),
+        _ptr(v_new, "v_new", _n(b, g, d_v) * e),
+        int(b), int(d_model), int(h), int(g), int(d_k), int(d_v), dt, int(flags),
+        _stream(stream))
 
 
 def gqa_project_out(o, w_o, y, b, d_model, h, d_v, dtype=None, flags=0, stream=None) -> None:
     """y = "bhv,hdv->bd"(o, P_o)."""
-    _check("gqa_project_out", lib.gqa_project_out(
-        _ptr(o), _ptr(w_o), _ptr(y), int(b), int(d_model), int(h), int(d_v),
-        _dtype(o, dtype), int(flags), _stream(stream)))
+    dt = _dtype(o, dtype)
+    e, D = _elt(dt), d_model
+    _call("gqa_project_out", lib.gqa_project_out,
+        _ptr(o, "o", _n(b, h, d_v) * e), _ptr(w_o, "w_o", _n(h, D, d_v) * e),
+        _ptr(y, "y", _n(b, D) * e), int(b), int(d_model), int(h), int(d_v), dt, int(flags),
+        _stream(stream))
 
 
 def gqa_decode_layer(x, w_q, w_k, w_v, w_o, k_cache, v_cache, seq_lens, b, d_model, h, g,
@@ -238,42 +326,67 @@ def gqa_decode_layer(x, w_q, w_k, w_v, w_o, k_cache, v_cache, seq_lens, b, d_mod
     """The incremental layer: project x, append, attend, project the output."""
     if cap is None:
         cap = k_cache.shape[2]
-    _check("gqa_decode_layer", lib.gqa_decode_layer(
-        _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(w_o), _ptr(k_cache), _ptr(v_cache),
-        _ptr(seq_lens), int(b), int(d_model), int(h), int(g), int(d_k), int(d_v),
-        float(scale), _ptr(y), int(cap), _dtype(x, dtype), int(flags), _stream(stream)))
+    dt = _dtype(x, dtype)
+    e, D = _elt(dt), d_model
+    _call("gqa_decode_layer", lib.gqa_decode_layer,
+        _ptr(x, "x", _n(b, D) * e), _ptr(w_q, "w_q", _n(h, D, d_k) * e),
+        _ptr(w_k, "w_k", _n(g, D, d_k) * e), _ptr(w_v, "w_v", _n(g, D, d_v) * e),
+        _ptr(w_o, "w_o", _n(h, D, d_v) * e), _ptr(k_cache, "k_cache", _n(b, g, cap, d_k) * e),
+        _ptr(v_cache, "v_cache", _n(b, g, cap, d_v) * e),
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True), int(b), int(d_model), int(h),
+        int(g), int(d_k), int(d_v), float(scale), _ptr(y, "y", _n(b, D) * e), int(cap), dt,
+        int(flags), _stream(stream))
+
+
+def _paged_ptrs(k_pool, v_pool, block_table, b, g, d_k, d_v, e):
+    """Checked pool and table pointers, and (block_size, max_blocks,
+    num_blocks) read from the pool [num_blocks, g, block_size, d_k] and the
+    table [b, max_blocks]."""
+    nb, _, bs, _ = k_pool.shape
+    mb = block_table.shape[1]
+    return (_ptr(k_pool, "k_pool", _n(nb, g, bs, d_k) * e),
+            _ptr(v_pool, "v_pool", _n(nb, g, bs, d_v) * e),
+            _ptr(block_table, "block_table", _n(b, mb) * 4, index=True), int(bs), int(mb), int(nb))
 
 
 def gqa_kv_append_paged(k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, g, d_k, d_v,
                         n=1, dtype=None, stream=None) -> None:
     """Append n new rows per sequence into a paged cache (pools
     [num_blocks, g, block_size, d], block_table [b, max_blocks])."""
-    nb, _, bs, _ = k_pool.shape
-    _check("gqa_kv_append_paged", lib.gqa_kv_append_paged(
-        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
-        int(b), int(n), int(g), int(d_k), int(d_v), int(bs), int(block_table.shape[1]), int(nb),
-        _dtype(k_pool, dtype), _stream(stream)))
+    dt = _dtype(k_pool, dtype)
+    e = _elt(dt)
+    kp, vp, tp, bs, mb, nb = _paged_ptrs(k_pool, v_pool, block_table, b, g, d_k, d_v, e)
+    _call("gqa_kv_append_paged", lib.gqa_kv_append_paged,
+        _ptr(k_new, "k_new", _n(b, n, g, d_k) * e), _ptr(v_new, "v_new", _n(b, n, g, d_v) * e),
+        kp, vp, tp, _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True),
+        int(b), int(n), int(g), int(d_k), int(d_v), bs, mb, nb, dt, _stream(stream))
 
 
 def gqa_decode_attn_paged(q, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k, d_v, scale,
                           out, n=1, dtype=None, stream=None) -> None:
     """gqa_decode_attn (n = 1) or gqa_decode_attn_multi over a paged cache."""
-    nb, _, bs, _ = k_pool.shape
-    _check("gqa_decode_attn_paged", lib.gqa_decode_attn_paged(
-        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens), int(b), int(n),
-        int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out), int(bs),
-        int(block_table.shape[1]), int(nb), _dtype(q, dtype), _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    kp, vp, tp, bs, mb, nb = _paged_ptrs(k_pool, v_pool, block_table, b, g, d_k, d_v, e)
+    _call("gqa_decode_attn_paged", lib.gqa_decode_attn_paged,
+        _ptr(q, "q", _n(b, n, h, d_k) * e), kp, vp, tp,
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True), int(b), int(n),
+        int(h), int(g), int(d_k), int(d_v), float(scale), _ptr(out, "out", _n(b, n, h, d_v) * e),
+        bs, mb, nb, dt, _stream(stream))
 
 
 def gqa_decode_step_paged(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, b, h, g, d_k,
                           d_v, scale, out, n=1, dtype=None, flags=0, stream=None) -> None:
     """Append and attend over a paged cache in one launch (n new tokens)."""
-    nb, _, bs, _ = k_pool.shape
-    _check("gqa_decode_step_paged", lib.gqa_decode_step_paged(
-        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
-        _ptr(seq_lens), int(b), int(n), int(h), int(g), int(d_k), int(d_v), float(scale),
-        _ptr(out), int(bs), int(block_table.shape[1]), int(nb), _dtype(q, dtype), int(flags),
-        _stream(stream)))
+    dt = _dtype(q, dtype)
+    e = _elt(dt)
+    kp, vp, tp, bs, mb, nb = _paged_ptrs(k_pool, v_pool, block_table, b, g, d_k, d_v, e)
+    _call("gqa_decode_step_paged", lib.gqa_decode_step_paged,
+        _ptr(q, "q", _n(b, n, h, d_k) * e), _ptr(k_new, "k_new", _n(b, n, g, d_k) * e),
+        _ptr(v_new, "v_new", _n(b, n, g, d_v) * e), kp, vp, tp,
+        _ptr(seq_lens, "seq_lens", _n(b) * 4, index=True), int(b), int(n), int(h), int(g),
+        int(d_k), int(d_v), float(scale), _ptr(out, "out", _n(b, n, h, d_v) * e), bs, mb, nb,
+        dt, int(flags), _stream(stream))
 
 
 _DTYPES = {"f32": GQA_F32, "bf16": GQA_BF16, "f16": GQA_F16}
