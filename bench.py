@@ -200,53 +200,440 @@ def kernel_source_hash(kernel_src: str) -> str:
 
 
 # ---------------------------------------------------------------------------
-# the oracle on a bounded sample (CPU baseline and reference arm)
+# ncu summary mode: --ncu-summary KERNEL profiles one launch of a kernel of
+# this library on a small case of the workload and writes the summary that
+# profiled_traffic reads (plus the launch list of a step)
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg, target_s: float = 12.0, max_units: int = 4096, n: int = 1):
-    """Time the float64 oracle's decode step on whole units (one sequence, one
-    KV head, its r query heads; n new tokens each) of layer 0 of the
-    workload, drawn on the CPU with the same generator recipe, until about
-    target_s seconds of work.  Returns (GB/s of algorithmic bytes, seconds,
-    units, bytes)."""
-    import torch
-    import oracle
-    from gqa_kv_cache_append_gb300.inputs import make_layer, make_layer_multi, seq_lens_for
+NCU_KERNELS = {  # --ncu-summary name -> (kernel name regex, source file)
+    "decode_tc": ("decode_tc_kernel", "decode_tc.cu"),
+    "decode_simt": ("decode_simt_kernel", "decode_simt.cu"),
+    "combine": ("combine_kernel", "gqa_api.cu"),
+    "proj_tc": ("proj_tc_kernel", "proj_tc.cu"),
+}
+# the counters the summary quotes: one launch, a handful of hardware units
+NCU_METRICS = [
+    "gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
+    "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed",
+    "dram__bytes_read.sum.per_second",
+    "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed",
+    "smsp__issue_active.avg.pct_of_peak_sustained_active",
+    "sm__warps_active.avg.pct_of_peak_sustained_active",
+    "lts__throughput.avg.pct_of_peak_sustained_elapsed",
+    "launch__grid_size", "launch__block_size", "launch__registers_per_thread",
+    "launch__shared_mem_per_block_dynamic", "gpc__cycles_elapsed.avg.per_second",
+]
+OUR_KERNELS = "regex:decode_tc|decode_simt|combine|kv_append|proj_tc|wait_selftest"
+
+
+def ncu_case_args(args) -> list:
+    """bench.py arguments of the small case profiled for args: the same
+    workload and overrides, few enough layers to hold at most ~2.5 GB of
+    cache on the device (one layer where a layer holds more) and at most 32,
+    but where that allows at least 4 x L2 of K/V per step; two timed steps
+    after three warm-up steps, nothing else."""
+    from gqa_kv_cache_append_gb300.inputs import bench_layers, seq_lens_for, workload
     import dataclasses
-
+    cfg = workload(args.workload)
+    for k in ("g", "h", "b", "cap"):
+        if getattr(args, k):
+            cfg = dataclasses.replace(cfg, **{k: getattr(args, k)})
+    if args.d:
+        cfg = dataclasses.replace(cfg, d=args.d)
+    if args.dv:
+        cfg = dataclasses.replace(cfg, d_v=args.dv)
+    if args.dtype:
+        cfg = dataclasses.replace(cfg, dtype=args.dtype)
     lens = seq_lens_for(cfg)
-    one = dataclasses.replace(cfg, b=1, layers=1)
-    done_units, done_bytes, spent = 0, 0, 0.0
-    i = 0
-    while spent < target_s and done_units < max_units:
-        L = int(lens[i % len(lens)])
-        sub = dataclasses.replace(one, seed=cfg.seed * 7919 + i)
-        if n == 1:
-            x = make_layer(sub, 0, "cpu", lens=np.array([L], dtype=np.int32))
-        else:
-            x = make_layer_multi(sub, n, 0, "cpu", lens=np.array([L], dtype=np.int32))
+    per_layer_cap = cfg.b * cfg.g * cfg.cap * (cfg.d + cfg.dv) * cfg.elt
+    l2 = 129 << 20  # GB300's L2 as the device reports it (no CUDA call in this process)
+    # (at most 32 layers: few launches before the profiled one)
+    layers = args.layers or max(1, min(bench_layers(cfg, lens, l2, args.tokens),
+                                       int(2.5e9 // per_layer_cap), 32))
+    out = ["--workload", args.workload, "--layers", str(layers), "--steps", "2", "--warmup", "3",
+           "--no-cpu-baseline", "--no-workloads"]
+    for k in ("g", "h", "b", "cap", "d", "dv", "dtype"):
+        v = getattr(args, k)
+        if v:
+            out += [f"--{k}", str(v)]
+    if args.tokens != 1:
+        out += ["--tokens", str(args.tokens)]
+    if args.paged:
+        out += ["--paged", str(args.paged)]
+    for flag in ("layer", "cuda_cores", "separate", "ordered"):
+        if getattr(args, flag):
+            out.append("--" + flag.replace("_", "-"))
+    return out
 
-        def np_(t):
-            t = t.contiguous()
-            if t.dtype == torch.bfloat16:
-                return t.view(torch.int16).numpy().view(np.uint16), "bf16"
-            return t.numpy(), ("f16" if t.dtype == torch.float16 else "f32")
-        tag = np_(x["q"])[1]
-        arrs = [np_(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
-        t0 = time.perf_counter()
+
+def ncu_tag(args) -> str:
+    """Summary name suffix: the workload, then whatever differs from it."""
+    tag = args.workload
+    for k in ("g", "h", "b", "cap", "d", "dv", "dtype"):
+        v = getattr(args, k)
+        if v:
+            tag += f"_{k}{v}"
+    if args.tokens != 1:
+        tag += f"_n{args.tokens}"
+    if args.paged:
+        tag += f"_paged{args.paged}"
+    for flag in ("layer", "cuda_cores", "separate", "ordered"):
+        if getattr(args, flag):
+            tag += "_" + flag
+    return tag
+
+
+def _ncu_rows(csv_path: str) -> list:
+    """Rows of an `ncu --page raw --csv --print-units base` table (the second
+    line, the units, is skipped)."""
+    import csv
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rows = list(csv.reader(lines))
+    if len(rows) < 2:
+        return []
+    hdr = rows[0]
+    return [dict(zip(hdr, r)) for r in rows[2:]]
+
+
+def _num(row, key):
+    try:
+        return float(str(row.get(key, "")).replace(",", ""))
+    except ValueError:
+        return None
+
+
+def run_ncu_summary(args) -> int:
+    """Profile KERNEL (args.ncu_summary) on the small case of the workload:
+    (1) run the case without ncu (it must exit 0); (2) the launch list of its
+    steps (gpu__time_duration.sum of every launch of this library's kernels,
+    one pass); (3) one launch of KERNEL in the third warm-up step with the
+    summary's counters.  Raw output goes to --ncu-out; the summaries
+    <kernel>_<tag>.md and launches_<tag>.md are written there too (copy them
+    to profiles/).  Every ncu run keeps the GPU clocks as they are."""
+    import shutil
+    from gqa_kv_cache_append_gb300 import binding as B
+    regex, src_name = NCU_KERNELS[args.ncu_summary]
+    out_dir = os.path.abspath(args.ncu_out)
+    os.makedirs(out_dir, exist_ok=True)
+    case = ncu_case_args(args)
+    tag = ncu_tag(args)
+    py = [sys.executable, os.path.join(ROOT, "bench.py")] + case
+    ncu = shutil.which("ncu") or "/usr/local/cuda/bin/ncu"
+    # (1) the plain run
+    with open(os.path.join(out_dir, f"ncu_plain_{tag}.log"), "w") as f:
+        rc = subprocess.run(py, stdout=f, stderr=subprocess.STDOUT, cwd=ROOT).returncode
+    if rc != 0:
+        print(f"plain run failed (rc {rc}); not profiled", file=sys.stderr)
+        return rc
+    plain = open(os.path.join(out_dir, f"ncu_plain_{tag}.log")).read().strip().splitlines()
+    line = json.loads(plain[-1])
+    layers = int(line["config"]["layers"])
+    per_step = int(line["gpu_launches_per_step"])
+    # launches of KERNEL per step: the decode kernel runs once per layer call;
+    # the combine kernel only where the plan says two kernels per call
+    if args.ncu_summary in ("decode_tc", "decode_simt"):
+        k_per_step = layers
+    elif args.ncu_summary == "combine":
+        k_per_step = max(0, per_step - layers)
+    else:
+        k_per_step = 2 * layers
+    if k_per_step == 0:
+        print(f"{regex} does not run in this case", file=sys.stderr)
+        return 2
+    # (2) launch list of the two timed steps (after the three warm-up steps)
+    list_csv = os.path.join(out_dir, f"ncu_launches_{tag}.csv")
+    cmd_list = [ncu, "--metrics", "gpu__time_duration.sum", "--clock-control", "none",
+                "-k", OUR_KERNELS, "-s", str(3 * per_step), "-c", str(2 * per_step),
+                "--csv", "--page", "raw", "--print-units", "base", "--log-file", list_csv] + py
+    rc = subprocess.run(cmd_list, stdout=subprocess.DEVNULL, stderr=subprocess.STDOUT,
+                        cwd=ROOT).returncode
+    if rc != 0:
+        return rc
+    # (3) one launch of KERNEL (the third warm-up step's first)
+    rep = os.path.join(out_dir, f"ncu_{args.ncu_summary}_{tag}")
+    cmd_one = [ncu, "--clock-control", "none", "--metrics", ",".join(NCU_METRICS),
+               "-k", f"regex:{regex}", "-s", str(2 * k_per_step), "-c", "1",
+               "-o", rep, "-f"] + py
+    rc = subprocess.run(cmd_one, stdout=subprocess.DEVNULL, stderr=subprocess.STDOUT,
+                        cwd=ROOT).returncode
+    if rc != 0:
+        return rc
+    one_csv = rep + ".raw.csv"
+    with open(one_csv, "w") as f:
+        rc = subprocess.run([ncu, "-i", rep + ".ncu-rep", "--page", "raw", "--csv",
+                             "--print-units", "base"], stdout=f, cwd=ROOT).returncode
+    if rc != 0:
+        return rc
+    rows = _ncu_rows(one_csv)
+    if not rows:
+        return 3
+    r = rows[0]
+    rd, wr = _num(r, "dram__bytes_read.sum"), _num(r, "dram__bytes_write.sum")
+    traffic = int(rd + wr)
+    src = os.path.join(ROOT, "gqa_kv_cache_append_gb300", "csrc", src_name)
+    alg = line["roofline"]["algorithmic_bytes_per_launch"]
+    pretty = " ".join(["python bench.py --ncu-summary", args.ncu_summary] +
+                      [a for a in sys.argv[1:] if a not in ("--ncu-summary", args.ncu_summary)])
+    shell = " ".join(["python bench.py"] + case)
+
+    def pct(k):
+        v = _num(r, k)
+        return "-" if v is None else f"{v:.1f} %"
+    md = [
+        f"# {r.get('Kernel Name', regex).split('(')[0]} — {tag}",
+        "",
+        f"Made by `{pretty}` (raw reports in the --ncu-out folder).  Case profiled:",
+        "",
+        f"    {shell}",
+        "",
+        "It ran without ncu first (exit 0).  Then, every run with `--clock-control none`:",
+        "",
+        f"    ncu --metrics gpu__time_duration.sum -k {OUR_KERNELS} -s {3 * per_step} "
+        f"-c {2 * per_step} --csv ... {shell}",
+        f"    ncu --metrics <the rows below> -k regex:{regex} -s {2 * k_per_step} -c 1 ... {shell}",
+        "",
+        "| metric | value |",
+        "|---|---|",
+        f"| gpu__time_duration.sum (isolated, serialised) | {_num(r, 'gpu__time_duration.sum') / 1e3:.2f} us |",
+        f"| dram__bytes_read.sum | {int(rd):,} B |",
+        f"| dram__bytes_write.sum | {int(wr):,} B |",
+        f"| read + write vs algorithmic bytes ({alg:,}) | {traffic / alg:.4f} |",
+        f"| dram read throughput | {(_num(r, 'dram__bytes_read.sum.per_second') or 0) / 1e12:.2f} TB/s |",
+        f"| gpu__dram_throughput (of peak, elapsed) | {pct('gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed')} |",
+        f"| sm__pipe_tensor_cycles_active | {pct('sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed')} |",
+        f"| smsp__issue_active | {pct('smsp__issue_active.avg.pct_of_peak_sustained_active')} |",
+        f"| sm__warps_active | {pct('sm__warps_active.avg.pct_of_peak_sustained_active')} |",
+        f"| lts__throughput | {pct('lts__throughput.avg.pct_of_peak_sustained_elapsed')} |",
+        f"| grid x block, registers, dynamic smem | {r.get('launch__grid_size')} x "
+        f"{r.get('launch__block_size')}, {r.get('launch__registers_per_thread')}, "
+        f"{r.get('launch__shared_mem_per_block_dynamic')} B |",
+        f"| SM clock | {(_num(r, 'gpc__cycles_elapsed.avg.per_second') or 0) / 1e9:.2f} GHz |",
+        "",
+        f"source_sha256: {kernel_source_hash(src)}",
+        f"traffic_bytes_per_launch: {traffic}",
+        "",
+    ]
+    with open(os.path.join(out_dir, f"{args.ncu_summary}_{tag}.md"), "w") as f:
+        f.write("\n".join(md))
+    # launch list: per kernel, launches, total time and share
+    agg = {}
+    for row in _ncu_rows(list_csv):
+        name = row.get("Kernel Name", "?").split("(")[0]
+        t = _num(row, "gpu__time_duration.sum") or 0.0
+        n0, t0 = agg.get(name, (0, 0.0))
+        agg[name] = (n0 + 1, t0 + t)
+    total = sum(t for _, t in agg.values()) or 1.0
+    lm = [f"# Launch list — {tag}", "",
+          f"Made by `{pretty}`; ncu serialises launches with cold caches: compare SHARES.",
+          "Two timed steps of:", "", f"    {shell}", "",
+          "| kernel | launches | total (us) | share | avg (us) |", "|---|---|---|---|---|"]
+    for name, (cnt, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        lm.append(f"| {name} | {cnt} | {t / 1e3:.1f} | {100 * t / total:.1f} % | "
+                  f"{t / cnt / 1e3:.2f} |")
+    with open(os.path.join(out_dir, f"launches_{tag}.md"), "w") as f:
+        f.write("\n".join(lm) + "\n")
+    print(json.dumps({"ncu_summary": args.ncu_summary, "tag": tag, "traffic": traffic,
+                      "algorithmic": alg, "launch_list": agg}))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and reference arm), spread over
+# every host core: one spawned worker process per core, each timing the
+# float64 oracle on whole (sequence, all KV heads) units of the workload
+# ---------------------------------------------------------------------------
+_ORACLE_POOL = None
+
+
+def host_cores() -> int:
+    """Cores this process may run on (the oracle baseline uses all of them)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_pool(workers: int):
+    """(executor, manager) with `workers` spawned processes, made once per
+    run (spawn: safe after CUDA was initialised in this process)."""
+    global _ORACLE_POOL
+    if _ORACLE_POOL is None or _ORACLE_POOL[2] != workers:
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        # one thread per worker process in any BLAS / OpenMP runtime it loads
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        ctx = mp.get_context("spawn")
+        ex = ProcessPoolExecutor(max_workers=workers, mp_context=ctx,
+                                 initializer=_oracle_worker_init)
+        _ORACLE_POOL = (ex, ctx.Manager(), workers)
+    return _ORACLE_POOL[0], _ORACLE_POOL[1]
+
+
+def _oracle_worker_init():
+    import torch
+    torch.set_num_threads(1)
+
+
+def _oracle_unit(cfg, n: int, i: int, L: int):
+    """Host arrays (numpy, bf16 as uint16 patterns) of sample i: one sequence
+    of length L with all its KV heads, drawn with the workload's recipe."""
+    import dataclasses
+    import torch
+    from gqa_kv_cache_append_gb300.inputs import make_layer, make_layer_multi
+    sub = dataclasses.replace(cfg, b=1, layers=1, seed=cfg.seed * 7919 + i)
+    lens = np.array([L], dtype=np.int32)
+    x = (make_layer(sub, 0, "cpu", lens=lens) if n == 1
+         else make_layer_multi(sub, n, 0, "cpu", lens=lens))
+
+    def np_(t):
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16), "bf16"
+        return t.numpy(), ("f16" if t.dtype == torch.float16 else "f32")
+    tag = np_(x["q"])[1]
+    return [np_(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")], tag
+
+
+def _oracle_task(cfg, n: int, samples, reps: int, barrier):
+    """One worker: draw its samples, wait for every worker, then run the
+    oracle's step `reps` times over them.  Returns (bytes, units, t0, t1) on
+    the system-wide monotonic clock."""
+    import oracle
+    data = [(_oracle_unit(cfg, n, i, L), L) for i, L in samples]
+    barrier.wait(timeout=600)
+    nbytes = units = 0
+    t0 = time.monotonic()
+    for k in range(reps):
+        (arrs, tag), L = data[k % len(data)]
         if n == 1:
             oracle.decode_step(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
         else:
             oracle.decode_step_multi(*arrs, np.array([L]), cfg.g, cfg.scale, dtype=tag)
-        spent += time.perf_counter() - t0
-        done_units += cfg.g
-        done_bytes += (L * cfg.g + n * cfg.h) * (cfg.d + cfg.dv) * cfg.elt
-        i += 1
-    return done_bytes / spent / 1e9, spent, done_units, done_bytes
+        nbytes += (L * cfg.g + n * cfg.h) * (cfg.d + cfg.dv) * cfg.elt
+        units += cfg.g
+    return nbytes, units, t0, time.monotonic()
 
 
-def blas_threads() -> int:
-    # numpy.einsum without `optimize` runs its own single-threaded loops
-    return 1
+def oracle_sample(cfg, target_s: float = 12.0, n: int = 1, workers: int = 0):
+    """Time the float64 oracle's decode step (append + attention) on whole
+    units (one sequence, all its KV heads, n new tokens) of layer-0-shaped
+    data of the workload, drawn on the host with the same recipe, on
+    `workers` processes at once (0: every host core), for about target_s
+    seconds of wall time.  Returns (GB/s of algorithmic bytes over the wall
+    time of the timed window, seconds, units, bytes, workers)."""
+    from gqa_kv_cache_append_gb300.inputs import seq_lens_for
+    import oracle
+    workers = workers or host_cores()
+    lens = seq_lens_for(cfg)
+    # one call here sizes the work: reps per worker for ~target_s of wall time
+    (arrs, tag), L0 = _oracle_unit(cfg, n, 0, int(lens[0])), int(lens[0])
+    t = time.perf_counter()
+    if n == 1:
+        oracle.decode_step(*arrs, np.array([L0]), cfg.g, cfg.scale, dtype=tag)
+    else:
+        oracle.decode_step_multi(*arrs, np.array([L0]), cfg.g, cfg.scale, dtype=tag)
+    one = max(time.perf_counter() - t, 1e-4)
+    reps = max(1, int(round(target_s / one)))
+    per = min(reps, 4)  # distinct samples per worker (cycled)
+    ex, mgr = _oracle_pool(workers)
+    barrier = mgr.Barrier(workers)
+    futs = []
+    for w in range(workers):
+        idx = [w * per + k for k in range(per)]
+        samples = [(i, int(lens[i % len(lens)])) for i in idx]
+        futs.append(ex.submit(_oracle_task, cfg, n, samples, reps, barrier))
+    res = [f.result(timeout=900) for f in futs]
+    nbytes = sum(r[0] for r in res)
+    units = sum(r[1] for r in res)
+    wall = max(r[3] for r in res) - min(r[2] for r in res)
+    return nbytes / wall / 1e9, wall, units, nbytes, workers
+
+
+# ---------------------------------------------------------------------------
+# the other workloads, timed after the headline one in the same run
+# ---------------------------------------------------------------------------
+# (name, overrides): the long-context MQA step, the ragged Qwen-shaped batch,
+# the four points of the g sweep and the fp32 MQA step
+EXTRA_WORKLOADS = [
+    ("long_mqa_b8_m131072", {}),
+    ("qwen25_7b_b64_ragged", {}),
+    ("gqa_sweep_b16_h32_d128_m4096", {"g": 32}),
+    ("gqa_sweep_b16_h32_d128_m4096", {"g": 8}),
+    ("gqa_sweep_b16_h32_d128_m4096", {"g": 4}),
+    ("gqa_sweep_b16_h32_d128_m4096", {"g": 1}),
+    ("mqa_f32_b1_h8_d64_m256", {}),
+]
+
+
+def time_workload(name, overrides, dev, stream, steps, warmup, dist, world, rank, peak_gbs):
+    """The bench's default step (one gqa_decode_step per layer, early
+    streaming, every layer back to back on one stream, inputs resident in
+    HBM) on another workload: layers rotated as bench_layers says, W untimed
+    steps, then K steps between CUDA events on the stream, max over ranks,
+    clocks sampled during the timed region.  Returns a summary dict (rank 0)
+    and frees the workload's memory."""
+    import dataclasses
+    import torch
+    from gqa_kv_cache_append_gb300 import binding as B
+    from gqa_kv_cache_append_gb300.inputs import bench_layers, make_layer, seq_lens_for, workload
+    base = workload(name, **overrides)
+    lens = seq_lens_for(base)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cfg = dataclasses.replace(base, layers=bench_layers(base, lens, l2),
+                              seed=replica_seed(base.seed, rank))
+    layers = [make_layer(cfg, l, dev) for l in range(cfg.layers)]
+    outs = [torch.empty((cfg.b, cfg.h, cfg.dv), dtype=cfg.torch_dtype, device=dev)
+            for _ in range(cfg.layers)]
+
+    def step():
+        for l, x in enumerate(layers):
+            B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                              x["seq_lens"], cfg.b, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.scale,
+                              outs[l], flags=B.GQA_STEP_EARLY_STREAM, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(smi_id(dev.index))
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(dist, dev)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1) / steps)
+    status = B.gqa_device_status(stream)
+    plan = B.gqa_decode_plan(cfg.b, 1, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.cap, cfg.dtype)
+    sb = step_bytes(cfg, lens)
+    del layers, outs
+    torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    call_ms = ms / cfg.layers
+    call_bytes = sb["attn_per_layer"] + sb["append_per_layer"]
+    gbs = call_bytes / (call_ms * 1e-3) / 1e9
+    tag = name + "".join(f"_{k}{v}" for k, v in overrides.items())
+    return tag, {
+        "value": round(world * sb["step"] / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "us_per_call": round(call_ms * 1000, 3),
+        "frac_of_measured": round(gbs / peak_gbs, 4),
+        "pct_of_nominal_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+        "layer_steps_per_s": round(world * cfg.layers / (ms * 1e-3), 1),
+        "bytes_per_call": call_bytes, "layers_rotated": cfg.layers, "steps": steps,
+        "dtype": cfg.dtype, "b": cfg.b, "h": cfg.h, "g": cfg.g, "d": cfg.d,
+        "sum_seq_lens": int(np.sum(lens)),
+        "kernel": "tensor cores" if plan["tensor_core"] else "CUDA cores",
+        "kernels_per_call": plan["kernels"], "ctas": plan["ctas"],
+        "clocks": clk, "device_status": status,
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -280,7 +667,8 @@ def run_ours(args, rank, local_rank, world):
     if args.cap:
         base = dataclasses.replace(base, cap=args.cap)
     if args.layers:
-        base = dataclasses.replace(base, layers=min(args.layers, base.layers))
+        # exactly N layers (past a workload's own: seeded replicas of its shape)
+        base = dataclasses.replace(base, layers=args.layers)
     if args.dtype:
         base = dataclasses.replace(base, dtype=args.dtype)
     if args.d:
@@ -296,11 +684,11 @@ def run_ours(args, rank, local_rank, world):
     # a workload whose layers all fit in L2 is rotated through independent
     # replicas (extra layers of the same shape) until one step streams at
     # least 4x the L2 size, so every step reads K/V from HBM
-    from gqa_kv_cache_append_gb300.inputs import layer_bytes as _lb, layer_flops
+    from gqa_kv_cache_append_gb300.inputs import bench_layers, layer_flops
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_layer = _lb(base, lens, n) + (projection_bytes(base) if full_layer else 0)
-    if base.layers * per_layer < 4 * l2 and not args.layers:
-        base = dataclasses.replace(base, layers=-(-4 * l2 // per_layer))
+    if not args.layers:
+        base = dataclasses.replace(base, layers=bench_layers(
+            base, lens, l2, n, projection_bytes(base) if full_layer else 0))
     cfg = dataclasses.replace(base, seed=replica_seed(base.seed, rank))
     layers = [make_layer(cfg, l, dev) if n == 1 else make_layer_multi(cfg, n, l, dev)
               for l in range(cfg.layers)]
@@ -509,9 +897,28 @@ def run_ours(args, rank, local_rank, world):
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
     status |= B.gqa_device_status(stream)
 
+    # ---- the other workloads (the default run only): the headline's
+    # buffers are released first ----
+    peaks = measured_peaks()
+    extra = None
+    if args.workloads:
+        layers.clear()
+        packed.clear()
+        outs.clear()
+        host_in.clear()
+        out_all = host_out = None
+        run_step = run_e2e = None
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        extra = {}
+        for name, over in EXTRA_WORKLOADS:
+            res = time_workload(name, over, dev, stream, args.workload_steps, args.warmup, dist,
+                                world, rank, peaks["hbm_gbs"])
+            if res is not None:
+                extra[res[0]] = res[1]
+
     if rank != 0:
         return None
-    peaks = measured_peaks()
     call_bytes = sb["attn_per_layer"] + sb["append_per_layer"] + sb.get("proj_per_layer", 0)
     achieved = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     plan = B.gqa_decode_plan(cfg.b, n, cfg.h, cfg.g, cfg.d, cfg.dv, cfg.cap, cfg.dtype,
@@ -592,6 +999,8 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clk,
         "device_status": status,
     }
+    if extra is not None:
+        line["workloads"] = extra
     if split is not None:
         split["attn_only_frac_of_measured"] = round(split["attn_only_gbs"] / peaks["hbm_gbs"], 4)
         line["separate_calls"] = split
@@ -599,11 +1008,12 @@ def run_ours(args, rank, local_rank, world):
         line["cpu_baseline"] = {"skipped": "the oracle baseline is timed on the step "
                                            "(run without --layer)"}
     elif not args.no_cpu_baseline:
-        gbs, spent, units, nbytes = oracle_sample(base, target_s=args.cpu_seconds, n=n)
+        gbs, spent, units, nbytes, cores = oracle_sample(base, target_s=args.cpu_seconds, n=n)
         line["cpu_baseline"] = {
-            "value": round(gbs, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+            "value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{units} (sequence, KV head) units of {cfg.name} layer-shaped data "
-                      f"({nbytes / 2**20:.0f} MiB, {spent:.1f} s, float64 numpy oracle: "
+                      f"({nbytes / 2**20:.0f} MiB in {spent:.1f} s of wall time on {cores} "
+                      "worker processes, one per host core; float64 numpy oracle: "
                       "append + attention)"}
     return line
 
@@ -619,13 +1029,14 @@ def run_reference(args, rank, world):
     n = args.tokens
     if n > 1:
         cfg = dataclasses.replace(cfg, kind="plain")
-    # ~40 s of oracle work over the whole run: drawing each sample's inputs
-    # costs about twice that again, so the run ends in about two minutes
-    per_step_s = max(0.25, min(20.0, 40.0 / max(1, args.steps + args.warmup)))
+    # --ref-seconds of timed oracle work (wall time, all host cores) over the
+    # whole run; drawing each step's samples adds about as much again
+    per_step_s = max(0.1, min(20.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     vals = []
     total_units = total_bytes = 0
+    cores = host_cores()
     for k in range(args.warmup + args.steps):
-        gbs, spent, units, nbytes = oracle_sample(cfg, target_s=per_step_s, n=n)
+        gbs, spent, units, nbytes, cores = oracle_sample(cfg, target_s=per_step_s, n=n)
         if k >= args.warmup:
             vals.append(gbs)
             total_units += units
@@ -641,10 +1052,11 @@ def run_reference(args, rank, world):
         "config": {"workload": cfg.name, "layers": cfg.layers, "b": cfg.b, "h": cfg.h,
                    "g": cfg.g, "d_head": cfg.d, "seq_len": int(np.max(lens)),
                    "parallelism": "host cores", "tokens_per_step": n},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
                          "sample": f"{total_units} (sequence, KV head) units over {args.steps} "
-                                   f"steps, {total_bytes / 2**20:.0f} MiB"},
+                                   f"steps, {total_bytes / 2**20:.0f} MiB, on {cores} worker "
+                                   "processes (one per host core)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -658,7 +1070,10 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_70b_b32_m8192")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall time of the oracle baseline (all host cores)")
+    ap.add_argument("--ref-seconds", type=float, default=40.0,
+                    help="--impl reference: timed oracle wall time over the whole run")
     ap.add_argument("--g", type=int, default=None, help="KV heads (for the g-knob sweep)")
     ap.add_argument("--h", type=int, default=None, help="query heads (shape studies)")
     ap.add_argument("--b", type=int, default=None, help="sequences (shape studies)")
@@ -684,9 +1099,28 @@ def main(argv=None):
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK",
                     help="paged KV cache with this block size (rows per block)")
     ap.add_argument("--layers", type=int, default=None,
-                    help="run only the first N layers (small profiling cases)")
+                    help="run exactly N layers (small profiling cases; past the workload's "
+                         "own layers, seeded replicas of its shape)")
+    ap.add_argument("--ncu-summary", choices=sorted(NCU_KERNELS), default=None,
+                    help="profile one launch of this kernel on a small case of the workload "
+                         "(ncu, clocks untouched) and write its summary and launch list")
+    ap.add_argument("--ncu-out", default="gpurun_out",
+                    help="--ncu-summary: folder for the raw reports and the summaries")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other workloads after the headline one")
+    ap.add_argument("--workload-steps", type=int, default=20,
+                    help="timed steps of each of the other workloads")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed steps
+    # the other workloads are timed after a default run only (named
+    # workload, no shape, layout or call overrides)
+    default_run = (args.workload == "llama3_70b_b32_m8192" and not any(
+        v for v in (args.g, args.h, args.b, args.cap, args.layers, args.dtype, args.d, args.dv,
+                    args.paged)) and not (args.graph or args.ordered or args.separate or
+                                          args.layer or args.cuda_cores) and args.tokens == 1)
+    args.workloads = default_run and not args.no_workloads
+    if args.ncu_summary:
+        raise SystemExit(run_ncu_summary(args))
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -48,7 +48,7 @@ import torch
 
 __all__ = ["DecodeConfig", "WORKLOADS", "workload", "seq_lens_for",
            "make_layer", "make_layer_multi", "make_layer_weights", "to_paged", "layer_bytes",
-           "layer_flops", "projection_bytes"]
+           "layer_flops", "projection_bytes", "bench_layers"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -140,6 +140,20 @@ def layer_bytes(cfg: DecodeConfig, lens: np.ndarray, n: int = 1) -> int:
     split partials are not counted)."""
     kv = int(np.sum(lens, dtype=np.int64)) * cfg.g * (cfg.d + cfg.dv) * cfg.elt
     return kv + cfg.b * n * cfg.h * (cfg.d + cfg.dv) * cfg.elt
+
+
+def bench_layers(cfg: DecodeConfig, lens: np.ndarray, l2_bytes: int, n: int = 1,
+                 extra_per_layer: int = 0) -> int:
+    """Layers a timed step rotates through: the workload's own, or, when all
+    of them together fit four times over in an L2 of ``l2_bytes``, enough
+    independent replicas of the layer (same shapes, the next layer seeds)
+    that one step streams at least 4 x L2, so every step reads its K/V from
+    HBM.  ``extra_per_layer``: bytes a layer reads besides the attention
+    call's (e.g. projection weights)."""
+    per_layer = layer_bytes(cfg, lens, n) + extra_per_layer
+    if cfg.layers * per_layer >= 4 * l2_bytes:
+        return cfg.layers
+    return -(-4 * l2_bytes // per_layer)
 
 
 def layer_flops(cfg: DecodeConfig, lens: np.ndarray, n: int = 1) -> int:

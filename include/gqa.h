@@ -70,8 +70,8 @@ extern "C" {
 #define GQA_ERR_DTYPE       -3  /* dtype is not GQA_F32, GQA_BF16 or GQA_F16 */
 #define GQA_ERR_ALIGN       -4  /* a tensor pointer is not 16-byte aligned */
 #define GQA_ERR_UNSUPPORTED -5  /* a shape this build has no kernel for
-                                   (d_k != d_v, head dim not 64/128, too many
-                                   query heads per KV head, b > 65535) */
+                                   (a head dim outside the supported set, too
+                                   many query heads per KV head, b > 65535) */
 #define GQA_ERR_CUDA        -6  /* a CUDA runtime call failed */
 #define GQA_ERR_DEVICE      -7  /* current device is not sm_103 */
 #define GQA_ERR_SCRATCH_LIMIT -8 /* gqa_decode_attn_noalloc: the call needs more
@@ -335,13 +335,17 @@ int gqa_selftest_wait_timeout(long long budget_cycles, void* stream);
  * GPU which loads libgqa.so holds until the process exits.
  *
  * Arguments, layouts, results and error codes are those of gqa_decode_attn,
- * and the two give the same output.  The caller still passes every input
- * and output buffer.  Limits: the first 256 KiB of the array hold two int
- * counters per (sequence, KV head), so b*g <= 32768; the remaining 3.75 MiB
- * hold the partials, (b*g + C) * (h/g) * (d_v + 2) * 4 bytes, C being the
- * number of CTAs (at most the SM count, 152 on GB300).  A larger call returns
+ * and the two give the same output bit for bit (the same kernel, grid and
+ * partial layout).  The caller still passes every input and output buffer.
+ * Limit: the array's last 3.75 MiB (3,932,160 bytes) hold the partials,
+ * (b*g + C) * (h/g) * (d_v + 2) * 4 bytes, C being the number of CTAs the
+ * call launches (at most the SM count, 152 on GB300); this is the bound that
+ * binds.  (The first 256 KiB hold two int counters per (sequence, KV head),
+ * room for b*g up to 32768, more than the partials ever allow.)  For
+ * example, with h/g = 8 and d_v = 128 the partials take 4,160 bytes per slot,
+ * so b*g + C <= 945: b*g <= 793 when C = 152.  A larger call returns
  * GQA_ERR_SCRATCH_LIMIT and launches nothing.  (The Llama-3-70B-shaped
- * layer, b=32 h=64 g=8 d=128, needs 256 counters and 1.7 MB of partials.)
+ * layer, b=32 h=64 g=8 d=128, needs 1.7 MB of partials.)
  *
  * The first call on a device does a one-time set-up with that device current
  * (it looks up the device address of the array); make that first call

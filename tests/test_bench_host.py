@@ -96,7 +96,17 @@ def test_traffic_lookup_requires_matching_source(tmp_path, monkeypatch):
 
 def test_reference_arm_line(capsys):
     bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3",
-                "--workload", "mqa_f32_b1_h8_d64_m256"])
+                "--workload", "mqa_f32_b1_h8_d64_m256", "--ref-seconds", "2"])
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == bench.host_cores()
+
+
+def test_oracle_sample_uses_every_core():
+    cfg = workload("mqa_f32_b1_h8_d64_m256")
+    gbs, wall, units, nbytes, cores = bench.oracle_sample(cfg, target_s=0.3)
+    assert cores == bench.host_cores() and gbs > 0 and wall > 0
+    # every worker ran whole units: bytes are a multiple of one unit's bytes
+    one = (256 * cfg.g + cfg.h) * (cfg.d + cfg.dv) * cfg.elt
+    assert nbytes % one == 0 and nbytes // one == units // cfg.g
