@@ -64,7 +64,7 @@ SIGNATURES = {
                                    _F, _VP, _I, _I, _I, _I, _I, _VP]),
     "gqa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
                              ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
-                             ctypes.POINTER(_LL)]),
+                             ctypes.POINTER(_LL), ctypes.POINTER(_I)]),
     "gqa_device_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "gqa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "gqa_status_string": (ctypes.c_char_p, [_I]),
@@ -395,17 +395,18 @@ _DTYPES = {"f32": GQA_F32, "bf16": GQA_BF16, "f16": GQA_F16}
 def gqa_decode_plan(b, n, h, g, d_k, d_v, cap, dtype, num_sms=0, flags=0) -> dict:
     """How a decode call with these shapes runs (host only when num_sms > 0):
     kernels per call, decode CTAs, positions per tile, tensor-core kernel or
-    not, split workspace bytes.  dtype: GQA_* code or "f32"/"bf16"/"f16";
-    flags: as for gqa_decode_step."""
+    not, split workspace bytes, CTAs per cluster (0: no clusters).  dtype:
+    GQA_* code or "f32"/"bf16"/"f16"; flags: as for gqa_decode_step."""
     dt = _DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
-    k, c, t, tc = (ctypes.c_int(0) for _ in range(4))
+    k, c, t, tc, cl = (ctypes.c_int(0) for _ in range(5))
     ws = ctypes.c_longlong(0)
     _check("gqa_decode_plan", lib.gqa_decode_plan(
         int(b), int(n), int(h), int(g), int(d_k), int(d_v), int(cap), dt, int(flags),
         int(num_sms),
-        ctypes.byref(k), ctypes.byref(c), ctypes.byref(t), ctypes.byref(tc), ctypes.byref(ws)))
+        ctypes.byref(k), ctypes.byref(c), ctypes.byref(t), ctypes.byref(tc), ctypes.byref(ws),
+        ctypes.byref(cl)))
     return {"kernels": k.value, "ctas": c.value, "tile": t.value, "tensor_core": bool(tc.value),
-            "workspace_bytes": ws.value}
+            "workspace_bytes": ws.value, "cluster": cl.value}
 
 
 def gqa_device_status(stream=None) -> int:

@@ -98,7 +98,9 @@ struct TcCfg {
   // The dynamic shared-memory base is 1024-byte aligned (the swizzled
   // layouts need it; the kernel checks), so no slack is requested: leaving
   // room on the SM lets small kernels (the combine) run beside a decode CTA.
-  static constexpr int SMEM = OFF_MISC + 16;
+  // OFF_MISC: TMEM address, abort flag, two split flags, then (ragged
+  // cluster launches) the CTA's split units [2][u, first CTA, last CTA, last]
+  static constexpr int SMEM = OFF_MISC + 48;
   static constexpr int NCOLS = 4 * NP;               // S0 S1 O0 O1
   // P rows are NP * 2 bytes: 32 B (NP=16) or 64 B (NP=32) swizzle atoms
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
@@ -142,12 +144,14 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                      uint4* __restrict__ k_cache_w, uint4* __restrict__ v_cache_w,
                      unsigned int* status, long long budget, int early, int nq,
                      const int* __restrict__ table, int bsz, int max_blocks, int num_blocks,
-                     int kh, int vh) {
+                     int kh, int vh, int cl_size, int cl_k) {
   using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   const uint32_t s_base = smem_u32(sm);
   if (s_base & 1023u) {  // never seen; the layout would not fit the allocation
+    // (the same in every CTA, so no CTA of a cluster is left at a cluster
+    // barrier: all of them return here)
     if (threadIdx.x == 0) atomicOr(status, GQA_DEV_INTERNAL);
     return;
   }
@@ -159,6 +163,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
   int* last_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 8);
+  int* split_list = reinterpret_cast<int*>(sm + C::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
@@ -189,6 +194,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       mbar_init(BAR(k), cnt);
     }
     *abort_flag = 0;
+    split_list[0] = split_list[4] = -1;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -215,6 +221,16 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   w.init(lens, b, g, nq, cap, kT, blockIdx.x, gridDim.x,
          PAGED ? 0 : ((kh == 2 && vh == 2) ? 2 : 1));
   Segment seg;
+  // Cluster merge: the launch is a cluster launch of cl_size CTAs, cl_k
+  // clusters per unit (grid = units * cl_size * cl_k), and every unit has
+  // the same number of tiles, so each CTA's range lies in unit
+  // blockIdx.x / (cl_size * cl_k).  Each CTA leaves its partial (max, sum,
+  // unnormalised output of every query row) in its own shared memory, and
+  // after a cluster barrier the cluster's CTAs merge them over distributed
+  // shared memory, each a slice of the unit's outputs.  (Uniform across the
+  // grid; with ragged lengths a cluster launch takes the global-memory
+  // merge below.)
+  const bool cl_merge = cl_size > 1 && w.equal;
 
   if (warp == 0 && PAGED) {
     // ===================== TMA producer, paged cache =====================
@@ -687,7 +703,13 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     };
 
     uint32_t n = 0;
+    bool had_seg = false;
+    // cluster merge: [NP][d_v] outputs and [NP][2] (max, sum) at the start of
+    // the ring (free once the CTA's last O product has completed)
+    float* cl_o = reinterpret_cast<float*>(sm);
+    float* cl_ml = cl_o + NP * dv;
     while (w.next(seg)) {
+      had_seg = true;
       const int first_new = seg.L - nq;  // position of new token 0
       // one token: threads 0 .. d_v/8 - 1 of warpgroup 0 carry the new V
       // row (one 16-byte chunk each) to the unit's last tile
@@ -877,7 +899,19 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
 #pragma unroll
         for (int e = 0; e < HP; ++e)
           l[e] = lred[e] + lred[HP + e] + lred[2 * HP + e] + lred[3 * HP + e];
-        if (whole) {
+        if (cl_merge) {
+          // this CTA's partial, for the merge across the cluster
+#pragma unroll
+          for (int e = 0; e < HP; ++e) {
+            if (h0 + e < nr) {
+              if (has_col) cl_o[(h0 + e) * dv + row] = o[e];
+              if (row == 0) {
+                cl_ml[2 * (h0 + e)] = l[e] > 0.f ? mfin[e] : -INFINITY;
+                cl_ml[2 * (h0 + e) + 1] = l[e];
+              }
+            }
+          }
+        } else if (whole) {
 #pragma unroll
           for (int e = 0; e < HP; ++e)
             if (h0 + e < nr && has_col)
@@ -901,7 +935,17 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           long long c0, c1;
           unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
           const int np = unit_parts(c0, c1, w.W, w.nc);
-          if (counters != nullptr && h0 < nr &&
+          if (cl_size > 1) {
+            // ragged cluster launch: the cluster holding the unit's last
+            // piece merges it after the kernel's loop (below); list it
+            if (wg == 0 && row == 0) {
+              int* sl4 = split_list + (seg.lt0 == 0 ? 4 : 0);  // unit's first piece: the CTA's last segment
+              sl4[0] = u;
+              sl4[1] = static_cast<int>(c0);
+              sl4[2] = static_cast<int>(c1);
+              sl4[3] = np;
+            }
+          } else if (counters != nullptr && h0 < nr &&
               arrive_last(counters, u * NWG + wg, np, last_flag_wg, row == 0, bar_id, 128)) {
             // pieces merge in CTA order whichever CTA merges (the same bits
             // every run).  This CTA's piece is used from registers when it
@@ -968,6 +1012,225 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         }
       }
     }
+    if (cl_merge && !had_seg) {
+      // a CTA with no tile of its unit: an empty partial
+#pragma unroll
+      for (int e = 0; e < HP; ++e) {
+        if (h0 + e < nr) {
+          if (row < dv) cl_o[(h0 + e) * dv + row] = 0.f;
+          if (row == 0) {
+            cl_ml[2 * (h0 + e)] = -INFINITY;
+            cl_ml[2 * (h0 + e) + 1] = 0.f;
+          }
+        }
+      }
+    }
+  }
+
+  if (cl_merge) {
+    // ====================== merge across the cluster ======================
+    // Unit u's pieces are the partials of its cl_size * cl_k CTAs.  After the
+    // barrier, CTA `rank` of a cluster merges items [rank * N / cl_size,
+    // (rank + 1) * N / cl_size) of the unit's N = nr * d_v / 4 output chunks
+    // (query row e, four columns) over the cluster's CTAs in rank order,
+    // reading their shared memory.  With one cluster per unit that is the
+    // output; with cl_k clusters, each cluster writes its merged slice as a
+    // partial to global memory and, per slice, the CTA that arrives last
+    // merges the cl_k of them in cluster order (the same bits every run).
+    cluster_arrive();
+    cluster_wait();
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int per_unit = cl_size * cl_k;
+    const int u = blockIdx.x / per_unit;
+    const int kc = (blockIdx.x / cl_size) % cl_k;
+    const int ui = u / g, uj = u % g;
+    const int nq4 = dv >> 2;
+    const int items = nr * nq4;
+    const int it0 = (rank * items) / cl_size, it1 = ((rank + 1) * items) / cl_size;
+    const uint32_t o_s = s_base, ml_s = s_base + NP * dv * 4;
+    T16* obase_u = out + (static_cast<size_t>(ui) * nq * h + uj * r) * dv;
+    auto store4 = [&](int e, int q, float4 v) {
+      const uint2 pk = make_uint2(Half16<T16>::pack2(v.x, v.y), Half16<T16>::pack2(v.z, v.w));
+      *reinterpret_cast<uint2*>(obase_u + col_off[e] + 4 * q) = pk;
+    };
+    for (int it = it0 + static_cast<int>(threadIdx.x); it < it1;
+         it += static_cast<int>(blockDim.x)) {
+      const int e = it / nq4, q = it - e * nq4;
+      float mc[16];
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        mc[c] = c < cl_size ? ld_dsmem(dsmem_addr(ml_s + 8 * e, c)) : -INFINITY;
+        M = fmaxf(M, mc[c]);
+      }
+      const float mr = (M == -INFINITY) ? 0.f : M;  // every piece empty
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        if (c < cl_size) {
+          const float wgt = ex2(mc[c] - mr);
+          const float4 ov = ld_dsmem4(dsmem_addr(o_s + (e * dv + 4 * q) * 4, c));
+          const float lc = ld_dsmem(dsmem_addr(ml_s + 8 * e + 4, c));
+          num.x = fmaf(wgt, ov.x, num.x);
+          num.y = fmaf(wgt, ov.y, num.y);
+          num.z = fmaf(wgt, ov.z, num.z);
+          num.w = fmaf(wgt, ov.w, num.w);
+          den = fmaf(wgt, lc, den);
+        }
+      }
+      if (cl_k == 1) {
+        store4(e, q, make_float4(num.x / den, num.y / den, num.z / den, num.w / den));
+      } else {
+        const size_t sl = (static_cast<size_t>(u) * cl_k + kc) * nr + e;
+        __stcg(reinterpret_cast<float4*>(part_o + sl * dv) + q, num);
+        if (q == 0) {
+          __stcg(part_ml + sl * 2, M);
+          __stcg(part_ml + sl * 2 + 1, den);
+        }
+      }
+    }
+    // this CTA's shared memory is no longer read by the cluster once every
+    // CTA passes the wait below
+    cluster_arrive();
+    if (cl_k > 1) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int old = atomicAdd(counters + u * cl_size + rank, 1);
+        const int last = (old == cl_k - 1) ? 1 : 0;
+        if (last) {
+          counters[u * cl_size + rank] = 0;
+          __threadfence();
+        }
+        *reinterpret_cast<volatile int*>(last_flag) = last;
+      }
+      __syncthreads();
+      if (*reinterpret_cast<volatile int*>(last_flag)) {
+        for (int it = it0 + static_cast<int>(threadIdx.x); it < it1;
+             it += static_cast<int>(blockDim.x)) {
+          const int e = it / nq4, q = it - e * nq4;
+          float M = -INFINITY, den = 0.f;
+          float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c0 = 0; c0 < cl_k; c0 += 4) {
+            float mc[4], lc[4];
+            float4 oc[4];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int c = c0 + k4;
+              const size_t sl = (static_cast<size_t>(u) * cl_k + c) * nr + e;
+              mc[k4] = c < cl_k ? __ldcg(part_ml + sl * 2) : -INFINITY;
+              lc[k4] = c < cl_k ? __ldcg(part_ml + sl * 2 + 1) : 0.f;
+              oc[k4] = c < cl_k ? __ldcg(reinterpret_cast<const float4*>(part_o + sl * dv) + q)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float mb = M;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) mb = fmaxf(mb, mc[k4]);
+            const float mbr = (mb == -INFINITY) ? 0.f : mb;
+            const float sc = ex2(M - mbr);  // 0 while M = -inf
+            den *= sc;
+            num.x *= sc;
+            num.y *= sc;
+            num.z *= sc;
+            num.w *= sc;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const float wgt = ex2(mc[k4] - mbr);
+              den = fmaf(wgt, lc[k4], den);
+              num.x = fmaf(wgt, oc[k4].x, num.x);
+              num.y = fmaf(wgt, oc[k4].y, num.y);
+              num.z = fmaf(wgt, oc[k4].z, num.z);
+              num.w = fmaf(wgt, oc[k4].w, num.w);
+            }
+            M = mb;
+          }
+          store4(e, q, make_float4(num.x / den, num.y / den, num.z / den, num.w / den));
+        }
+      }
+    }
+    cluster_wait();
+  } else if (cl_size > 1) {
+    // ============ ragged lengths in a cluster launch: the unit's pieces are
+    // global partials (slots u + c); the CTA whose piece completes a unit's
+    // count marks it, and after the barrier its whole cluster merges that
+    // unit, each CTA a slice of the outputs, the pieces in CTA order ========
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int s2 = 0; s2 < 2; ++s2) {
+        int* e4 = split_list + 4 * s2;
+        if (e4[0] < 0) continue;
+        if (atomicAdd(counters + e4[0], 1) == e4[3] - 1)
+          counters[e4[0]] = 0;  // this CTA completes the unit
+        else
+          e4[0] = -1;
+      }
+      __threadfence();
+    }
+    cluster_arrive();
+    cluster_wait();
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int nq4 = dv >> 2;
+    const int items = nr * nq4;
+    const int it0 = (rank * items) / cl_size, it1 = ((rank + 1) * items) / cl_size;
+    const uint32_t lst = smem_u32(split_list);
+    for (int c = 0; c < cl_size; ++c) {
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const uint32_t ea = dsmem_addr(lst + 16 * s2, c);
+        const int u = ld_dsmem_s32(ea);
+        if (u < 0) continue;
+        const int c0 = ld_dsmem_s32(ea + 4), c1 = ld_dsmem_s32(ea + 8);
+        T16* obase_u = out + (static_cast<size_t>(u / g) * nq * h + (u % g) * r) * dv;
+        for (int it = it0 + static_cast<int>(threadIdx.x); it < it1;
+             it += static_cast<int>(blockDim.x)) {
+          const int e = it / nq4, q = it - e * nq4;
+          float M = -INFINITY, den = 0.f;
+          float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cb = c0; cb <= c1; cb += 8) {
+            float mc[8], lc[8];
+            float4 oc[8];
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int cc = cb + k8;
+              const bool use = cc <= c1 && (w.W >= w.nc || !cta_empty(cc, w.W, w.nc));
+              const size_t sl = (static_cast<size_t>(u) + cc) * nr + e;
+              mc[k8] = use ? __ldcg(part_ml + sl * 2) : -INFINITY;
+              lc[k8] = use ? __ldcg(part_ml + sl * 2 + 1) : 0.f;
+              oc[k8] = use ? __ldcg(reinterpret_cast<const float4*>(part_o + sl * dv) + q)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float mb = M;
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) mb = fmaxf(mb, mc[k8]);
+            const float mbr = (mb == -INFINITY) ? 0.f : mb;
+            const float sc = ex2(M - mbr);  // 0 while M = -inf
+            den *= sc;
+            num.x *= sc;
+            num.y *= sc;
+            num.z *= sc;
+            num.w *= sc;
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const float wgt = ex2(mc[k8] - mbr);  // 0 for unused slots, empty pieces
+              den = fmaf(wgt, lc[k8], den);
+              num.x = fmaf(wgt, oc[k8].x, num.x);
+              num.y = fmaf(wgt, oc[k8].y, num.y);
+              num.z = fmaf(wgt, oc[k8].z, num.z);
+              num.w = fmaf(wgt, oc[k8].w, num.w);
+            }
+            M = mb;
+          }
+          const uint2 pk =
+              make_uint2(Half16<T16>::pack2(num.x / den, num.y / den),
+                         Half16<T16>::pack2(num.z / den, num.w / den));
+          *reinterpret_cast<uint2*>(obase_u + col_off[e] + 4 * q) = pk;
+        }
+      }
+    }
+    // no CTA leaves while another may still read its list
+    cluster_arrive();
+    cluster_wait();
   }
 
   __syncthreads();
@@ -1001,6 +1264,23 @@ bool make_q_map(CUtensorMap* map, const void* base, int b, int nq, int h, int r,
   return encode_bf16_map(map, base, 3, dims, strides, box, bf16);
 }
 
+// The shared-memory opt-in and the permission for clusters of up to 16 CTAs
+// are set once per device and kernel (outside any stream capture: the first
+// call on a device must come before a capture).
+template <typename K>
+cudaError_t configure_kernel(K kern, int smem, std::atomic<unsigned long long>& configured) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(configured.load() & (1ull << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(1ull << dev);
+  }
+  return cudaSuccess;
+}
+
 template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
 cudaError_t launch_np(const DecodeLaunch& a) {
   constexpr bool kBf16 = Half16<T16>::kBf16;
@@ -1015,33 +1295,32 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       !make_map(&mv, a.v_cache, a.dv, kv_rows, box_rows, kBf16))
     return cudaErrorInvalidValue;
   auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16>;
-  // the shared-memory opt-in is set once per device (not during a capture)
-  static std::atomic<unsigned long long> configured{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!(configured.load() & (1ull << dev))) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(1ull << dev);
-  }
+  static std::atomic<unsigned long long> configured{0};  // devices done, this variant
+  if (cudaError_t e = configure_kernel(kern, C::SMEM, configured)) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nc);
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(
       &cfg, kern, mq, mk, mv, a.seq_lens, a.b, a.h, a.g, a.cap, a.scale_log2,
       static_cast<T16*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
       a.early ? 1 : 0, a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks, a.d / 64,
-      a.dv / 64);
+      a.dv / 64, a.cluster > 1 ? a.cluster : 0, a.cluster > 1 ? a.cluster_k : 1);
 }
 
 template <typename T16>
@@ -1068,6 +1347,40 @@ bool tc_supported(int dtype, int d_k, int d_v, int cols) {
 }
 
 int tc_tile() { return kT; }
+
+int tc_max_clusters(int csize) {
+  // One CTA per SM whatever the variant (every one takes over 200 KiB of
+  // shared memory), so the largest variant stands for all.  Cached per device.
+  static std::atomic<int> cache[64][17];
+  static std::atomic<bool> init[64][17];
+  if (csize < 1 || csize > 16) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (init[dev][csize].load()) return cache[dev][csize].load();
+  using C = TcCfg<32, 2, false, false, true>;
+  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16>;
+  static std::atomic<unsigned long long> configured{0};
+  if (configure_kernel(kern, C::SMEM, configured) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize * 64);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // (a query that failed leaves no sticky error)
+    n = 0;
+  }
+  cache[dev][csize].store(n);
+  init[dev][csize].store(true);
+  return n;
+}
 
 int tc_ctas_per_sm(int) { return 1; }
 

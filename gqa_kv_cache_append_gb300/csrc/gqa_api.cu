@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <type_traits>
 #include <atomic>
 #include <map>
@@ -368,7 +369,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool use_combine_kernel(long long nc, int b, int g) { return nc > 2ll * b * g; }
 
 int launch_all(DecodeLaunch& a, int tile) {
-  const bool separate = use_combine_kernel(a.nc, a.b, a.g);
+  // (a cluster launch merges its split units itself)
+  const bool separate = a.cluster <= 1 && use_combine_kernel(a.nc, a.b, a.g);
   if (separate) a.counters = nullptr;
   const bool tc = !a.cuda_cores && tc_supported(a.dtype, a.d, a.dv, a.nq * (a.h / a.g));
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
@@ -577,6 +579,7 @@ struct DecodeArgs {
 struct DecodePlan {
   int tile = 0;
   long long nc = 0;
+  int cluster = 0, cluster_k = 1;  // tensor-core cluster merge (0: none)
   size_t o_bytes = 0;     // partial outputs
   size_t ml_bytes = 0;    // partial max / sum
   size_t units = 0;       // arrival counters
@@ -620,26 +623,97 @@ long long aligned_ctas(long long ctas, long long units) {
   return (units < ctas && 2 * units <= ctas) ? units * (ctas / units) : ctas;
 }
 
-DecodePlan decode_plan(const DecodeArgs& x, int num_sms) {
+// Tuning knobs read from the environment at every call (sweeps only; unset
+// in normal use): GQA_CTAS = CTAs of a decode launch (capped at the tiles of
+// the cache), GQA_CLUSTER = 0 (no cluster merge) or the cluster size 2..16.
+int env_knob(const char* name) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == 0) return -1;
+  char* end = nullptr;
+  const long x = std::strtol(v, &end, 10);
+  return (end != nullptr && *end == 0 && x >= 0 && x <= 1000000) ? static_cast<int>(x) : -1;
+}
+
+// Units cut into three or more pieces on the tensor-core kernel: cluster
+// launches, clusters of C CTAs, k clusters per unit (grid = units * C * k),
+// whose CTAs merge their pieces themselves instead of a combine kernel.
+// Among the sizes for which k >= 1 clusters per unit fit at once (at most
+// `pieces` CTAs per unit), the plan takes the most CTAs, then the fewest
+// clusters per unit.  max_clusters(C): clusters of C that fit at once.
+template <typename F>
+void choose_cluster(long long units, long long pieces, int forced, F max_clusters,
+                    DecodePlan& p) {
+  long long best = 0;
+  int bc = 0, bk = 0;
+  for (int c = 2; c <= 16; ++c) {
+    if (forced >= 2 && c != forced) continue;
+    if (c > pieces) break;
+    const long long fit = max_clusters(c) / units;
+    const long long k = std::min(pieces / c, fit);
+    if (k < 1) continue;
+    const long long ctas = units * c * k;
+    if (ctas > best || (ctas == best && k < bk)) {
+      best = ctas;
+      bc = c;
+      bk = static_cast<int>(k);
+    }
+  }
+  if (best > 0) {
+    p.nc = best;
+    p.cluster = bc;
+    p.cluster_k = bk;
+  }
+}
+
+// query_device: ask the device how many clusters fit at once (else assume
+// every SM can take part in a cluster of any size).
+DecodePlan decode_plan(const DecodeArgs& x, int num_sms, bool query_device = true) {
   const int r = x.h / x.g, d = x.d_k, cols = x.nq * r;
   const bool use_tc = use_tensor_cores(x, cols);
   DecodePlan p;
   p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, x.d_k, x.d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(x.dtype, d, r);
-  const long long max_tiles = static_cast<long long>(x.b) * x.g * ((x.cap + p.tile - 1) / p.tile);
-  p.nc = aligned_ctas(static_cast<long long>(num_sms) * per_sm, static_cast<long long>(x.b) * x.g);
+  const long long units = static_cast<long long>(x.b) * x.g;
+  const long long unit_tiles = (x.cap + p.tile - 1) / p.tile;
+  const long long max_tiles = units * unit_tiles;
+  const long long ctas = static_cast<long long>(num_sms) * per_sm;
+  p.nc = aligned_ctas(ctas, units);
+  const int knob_ctas = env_knob("GQA_CTAS");
+  if (knob_ctas > 0) p.nc = knob_ctas;
   if (p.nc > max_tiles) p.nc = max_tiles;
   if (p.nc < 1) p.nc = 1;
-  const size_t slots = static_cast<size_t>(x.b) * x.g + static_cast<size_t>(p.nc);
+  const int knob_cluster = env_knob("GQA_CLUSTER");
+  if (use_tc && knob_cluster != 0 && use_combine_kernel(p.nc, x.b, x.g)) {
+    // A cluster launch saves the combine kernel (its run and one more grid
+    // completion: about 2 us back to back) but fits fewer CTAs (whole
+    // clusters per unit, as many as the GPCs hold), so it streams slower.
+    // It is taken when the streaming time it gives up, estimated from the
+    // capacity at 7.4 TB/s, is below that; measured: 128 cluster CTAs for
+    // 16 units of 32 tiles 15.7 us per call against 17.0 with the combine
+    // kernel, 144 for 8 units of 1024 tiles 89.4 against 84.4.
+    DecodePlan cl = p;
+    const long long pieces = std::min(p.nc / units, unit_tiles);
+    if (query_device)
+      choose_cluster(units, pieces, knob_cluster, tc_max_clusters, cl);
+    else
+      choose_cluster(units, pieces, knob_cluster, [&](int c) { return ctas / c; }, cl);
+    const double stream_s = static_cast<double>(units) * unit_tiles * p.tile *
+                            (x.d_k + x.d_v) * elt_bytes(x.dtype) / 7.4e12;
+    const double lost_s =
+        stream_s * (1.0 - static_cast<double>(cl.nc) / static_cast<double>(p.nc));
+    if (cl.cluster > 1 && (knob_cluster >= 2 || lost_s < 2e-6)) p = cl;
+  }
+  const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(p.nc);
   p.o_bytes = slots * cols * x.d_v * sizeof(float);
   p.ml_bytes = slots * cols * 2 * sizeof(float);
-  // two arrival counters per unit: the tensor-core kernel may run two
-  // softmax warpgroups, each with its own
-  p.units = 2 * static_cast<size_t>(x.b) * x.g;
+  // arrival counters: two per unit (the tensor-core kernel may run two
+  // softmax warpgroups, each with its own), or one per unit and cluster rank
+  p.units = std::max(2 * static_cast<size_t>(units),
+                     static_cast<size_t>(units) * static_cast<size_t>(p.cluster));
   return p;
 }
 
-int decode_run(const DecodeArgs& x, const DecodePlan& p, const DeviceInfo* di, void* parts,
+int decode_run(const DecodeArgs& x, const DecodePlan& p, unsigned int* status, void* parts,
                int* counters, cudaStream_t st) {
   DecodeLaunch a;
   a.q = x.q;
@@ -665,9 +739,11 @@ int decode_run(const DecodeArgs& x, const DecodePlan& p, const DeviceInfo* di, v
   a.v_cache_w = const_cast<void*>(x.v_cache);
   a.early = (x.flags & GQA_STEP_EARLY_STREAM) != 0;
   a.cuda_cores = (x.flags & GQA_STEP_CUDA_CORES) != 0;
-  a.status = di->status;
+  a.status = status;
   a.budget = kWaitBudget;
   a.nc = static_cast<int>(p.nc);
+  a.cluster = p.cluster;
+  a.cluster_k = p.cluster_k;
   a.stream = st;
   a.block_table = x.block_table;
   a.block_size = x.block_size;
@@ -693,7 +769,7 @@ int decode(const void* q, const void* k_new, const void* v_new, const void* k_ca
   void* ws = nullptr;
   int* counters = nullptr;
   if (int e = workspace(st, p.o_bytes + p.ml_bytes, p.units, &ws, &counters)) return e;
-  return decode_run(x, p, di, ws, counters, st);
+  return decode_run(x, p, di->status, ws, counters, st);
 }
 
 }  // namespace
@@ -735,7 +811,7 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new, v
 
 int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int dtype,
                     int flags, int num_sms, int* kernels, int* ctas, int* tile,
-                    int* tensor_core, long long* workspace_bytes) {
+                    int* tensor_core, long long* workspace_bytes, int* cluster) {
   using namespace gqa;
   // stand-in pointers: only the shapes are checked
   const void* p = reinterpret_cast<const void*>(uintptr_t(256));
@@ -743,13 +819,15 @@ int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int d
                const_cast<void*>(p), cap, dtype, flags};
   if (int e = decode_check(x)) return e;
   if (num_sms < 0) return GQA_ERR_SHAPE;
-  if (num_sms == 0) {
+  const bool on_device = num_sms == 0;
+  if (on_device) {
     DeviceInfo* di = nullptr;
     if (int e = device_info(&di)) return e;
     num_sms = di->num_sms;
   }
-  const DecodePlan pl = decode_plan(x, num_sms);
-  if (kernels) *kernels = use_combine_kernel(pl.nc, b, g) ? 2 : 1;
+  const DecodePlan pl = decode_plan(x, num_sms, on_device);
+  if (kernels) *kernels = (pl.cluster <= 1 && use_combine_kernel(pl.nc, b, g)) ? 2 : 1;
+  if (cluster) *cluster = pl.cluster;
   if (ctas) *ctas = static_cast<int>(pl.nc);
   if (tile) *tile = pl.tile;
   if (tensor_core) *tensor_core = use_tensor_cores(x, n * (h / g)) ? 1 : 0;
@@ -779,7 +857,7 @@ static int decode_paged(const void* q, const void* k_new, const void* v_new, con
   void* ws = nullptr;
   int* counters = nullptr;
   if (int e = workspace(st, p.o_bytes + p.ml_bytes, p.units, &ws, &counters)) return e;
-  return decode_run(x, p, di, ws, counters, st);
+  return decode_run(x, p, di->status, ws, counters, st);
 }
 
 int gqa_decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
@@ -989,7 +1067,7 @@ int gqa_decode_layer(const void* x, const void* w_q, const void* w_k, const void
   dx.out = o;
   // (early streaming only with the caller's consent: a kernel that started
   // before the projection, e.g. one writing this cache, may still run)
-  if (int e = decode_run(dx, pd, di, part, counters, st)) return e;
+  if (int e = decode_run(dx, pd, di->status, part, counters, st)) return e;
   return proj_run(1, w_o, nullptr, nullptr, o, y, nullptr, nullptr, b, d_model, h, 1, early,
                   p1, di, part, counters, st);
 }
@@ -1062,71 +1140,21 @@ extern "C" int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const
                                        int d_v, float scale, void* out, int cap, int dtype,
                                        void* stream) {
   using namespace gqa;
-  if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_NULL;
-  if (dtype != GQA_F32 && dtype != GQA_BF16 && dtype != GQA_F16) return GQA_ERR_DTYPE;
-  if (b < 1 || h < 1 || g < 1 || d_k < 1 || d_v < 1 || cap < 1 || h % g != 0)
-    return GQA_ERR_SHAPE;
-  if (static_cast<long long>(b) * g * cap + 256 > 0x7FFFFFFFll ||
-      static_cast<long long>(b) * h > 0x7FFFFFFFll)
-    return GQA_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-    return GQA_ERR_ALIGN;
-  const int r = h / g;
-  const int d = d_k;
-  if (b > 65535) return GQA_ERR_UNSUPPORTED;
-  const bool use_tc = tc_supported(dtype, d_k, d_v, r);
-  if (!use_tc && !simt_supported(dtype, d_k, d_v, r)) return GQA_ERR_UNSUPPORTED;
+  // the checks and the plan of gqa_decode_attn, so the two launch the same
+  // grid with the same partial layout
+  const DecodeArgs x{q, nullptr, nullptr, k_cache, v_cache, seq_lens, b, 1, h, g, d_k, d_v,
+                     scale, out, cap, dtype, 0};
+  if (int e = decode_check(x)) return e;
   NoAllocDevice* nd = nullptr;
   if (int e = noalloc_setup(&nd)) return e;
-
-  const int tile = use_tc ? tc_tile() : simt_tile(dtype, d_k, d_v);
-  const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(dtype, d, r);
-  const long long max_tiles = static_cast<long long>(b) * g * ((cap + tile - 1) / tile);
-  long long nc = aligned_ctas(static_cast<long long>(nd->num_sms) * per_sm,
-                             static_cast<long long>(b) * g);
-  if (nc > max_tiles) nc = max_tiles;
-  if (nc < 1) nc = 1;
-  const size_t slots = static_cast<size_t>(b) * g + static_cast<size_t>(nc);
-  const size_t o_bytes = slots * r * d_v * sizeof(float);
-  const size_t ml_bytes = slots * r * 2 * sizeof(float);
-  if (2 * static_cast<size_t>(b) * g > kNoAllocMaxUnits ||
-      o_bytes + ml_bytes > kNoAllocScratchBytes - kNoAllocCounterBytes)
+  const DecodePlan p = decode_plan(x, nd->num_sms);
+  if (p.units > kNoAllocMaxUnits ||
+      p.o_bytes + p.ml_bytes > kNoAllocScratchBytes - kNoAllocCounterBytes)
     return GQA_ERR_SCRATCH_LIMIT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* counters = reinterpret_cast<int*>(nd->scratch);
-  unsigned char* parts = nd->scratch + kNoAllocCounterBytes;
-  // the per-unit arrival counters must start at zero
-  if (cudaMemsetAsync(counters, 0, 2 * static_cast<size_t>(b) * g * sizeof(int), st) !=
-      cudaSuccess)
+  // the arrival counters the launch uses must start at zero
+  if (cudaMemsetAsync(counters, 0, p.units * sizeof(int), st) != cudaSuccess)
     return GQA_ERR_CUDA;
-
-  DecodeLaunch a;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.seq_lens = seq_lens;
-  a.b = b;
-  a.h = h;
-  a.g = g;
-  a.d = d;
-  a.dv = d_v;
-  a.cap = cap;
-  a.dtype = dtype;
-  a.nq = 1;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  a.out = out;
-  a.part_o = reinterpret_cast<float*>(parts);
-  a.part_ml = reinterpret_cast<float*>(parts + o_bytes);
-  a.counters = counters;
-  a.k_new = nullptr;
-  a.v_new = nullptr;
-  a.k_cache_w = nullptr;
-  a.v_cache_w = nullptr;
-  a.early = false;
-  a.status = nd->status;
-  a.budget = kWaitBudget;
-  a.nc = static_cast<int>(nc);
-  a.stream = st;
-  return launch_all(a, tile);
+  return decode_run(x, p, nd->status, nd->scratch + kNoAllocCounterBytes, counters, st);
 }

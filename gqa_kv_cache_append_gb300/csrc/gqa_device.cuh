@@ -158,6 +158,57 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // ---------------------------------------------------------------------------
+// thread-block clusters: distributed shared memory and the cluster barrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives (release: this thread's
+// earlier shared-memory writes become visible to the cluster) ...
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+// ... and waits for all of them (acquire).  A hardware barrier, not a spin:
+// it completes once every thread of the cluster has arrived, and every path
+// through the kernels that use it arrives.
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The address, in the cluster's shared window, of the variable at this
+// CTA's shared address `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -424,6 +475,7 @@ struct Walker {
   int b, g, lmin, cap, T;
   long long W;         // total tiles of the launch
   int nc;              // CTAs of the launch
+  bool equal;          // every sequence has the same, nonzero, number of tiles
   long long pos, end;  // global tile cursor and end of this CTA's range
   int i, j, lt, ti, L;
 
@@ -466,7 +518,7 @@ struct Walker {
     lmin = lmin_;
     cap = cap_;
     T = T_;
-    bool equal = false;
+    equal = false;
     W = total_tiles(lens, b, g, lmin, cap, T, &equal);
     // Equal lengths: k = 1 or 2 whole units per CTA when that still uses at
     // least 70 % of the CTAs, the rest idle (no piece to merge).  Measured on

@@ -31,6 +31,11 @@ struct DecodeLaunch {
   unsigned int* status;  // device status word
   long long budget;      // wait limit in SM cycles
   int nc;                // persistent CTAs
+  // tensor-core kernel: clusters of `cluster` CTAs (0: no cluster launch),
+  // cluster_k of them per (sequence, KV head) unit, nc = units * cluster *
+  // cluster_k; with equal lengths the split units are merged across each
+  // cluster in distributed shared memory
+  int cluster = 0, cluster_k = 1;
   cudaStream_t stream;
   // paged cache (null table: contiguous [b, g, cap, d]): the caches are pools
   // [num_blocks, g, block_size, d]; position p of sequence i is row
@@ -56,6 +61,9 @@ cudaError_t launch_decode_simt(const DecodeLaunch& a);
 // 32 query rows per KV head)
 bool tc_supported(int dtype, int d_k, int d_v, int cols);
 int tc_tile();
+// clusters of csize CTAs of the tensor-core kernel that fit on the device
+// at once (one CTA per SM); 0 if none or the query failed
+int tc_max_clusters(int csize);
 int tc_ctas_per_sm(int r);
 cudaError_t launch_decode_tc(const DecodeLaunch& a);
 

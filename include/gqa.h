@@ -373,10 +373,11 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  * num_sms: SM count of the target device; 0 = that of the current device
  * (which then needs a GPU).  Outputs, each optional (NULL = not wanted):
  *   kernels          kernels one gqa_decode_attn* call launches: 1, or 2 when
- *                    the units are split over more CTAs than 2*b*g and the
- *                    split partials are merged by the separate combine
- *                    kernel (gqa_decode_step* launch the same number; the
- *                    append is fused)
+ *                    the CUDA-core kernel splits the units over more CTAs
+ *                    than 2*b*g and the split partials are merged by the
+ *                    separate combine kernel (gqa_decode_step* launch the
+ *                    same number; the append is fused).  The tensor-core
+ *                    kernel merges such splits itself, in clusters (below).
  *   ctas             CTAs the decode kernel is launched with (persistent: at
  *                    most num_sms).  On the tensor-core kernel over a
  *                    contiguous cache, when all
@@ -388,12 +389,27 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  *   tile             cache positions per tile
  *   tensor_core      1 for the tcgen05 kernel, 0 for the CUDA-core kernel
  *   workspace_bytes  split partials + arrival counters the call uses
+ *   cluster          CTAs per thread-block cluster of the decode launch, 0
+ *                    for a launch without clusters.  The tensor-core kernel
+ *                    is launched in clusters when the units would be cut
+ *                    into three or more pieces each (more CTAs than 2*b*g):
+ *                    each unit then gets k whole clusters (ctas = b*g*C*k),
+ *                    C and k chosen for the most CTAs among the sizes of
+ *                    which k clusters per unit fit on the device at once
+ *                    (host only, num_sms > 0: as if any cluster size could
+ *                    use every SM), and the CTAs of a cluster merge their
+ *                    pieces over distributed shared memory (equal lengths)
+ *                    or through the split workspace (ragged lengths).
  * Returns the code the decode call would return for these shapes (its
  * pointer and alignment checks aside), or GQA_ERR_SHAPE for num_sms < 0.
+ *
+ * Tuning knobs (environment, read at every decode call; for sweeps, unset
+ * in normal use): GQA_CTAS = CTAs of the decode launch; GQA_CLUSTER = 0 (no
+ * cluster launch: the combine kernel merges) or a cluster size from 2 to 16.
  */
 int gqa_decode_plan(int b, int n, int h, int g, int d_k, int d_v, int cap, int dtype,
                     int flags, int num_sms, int* kernels, int* ctas, int* tile,
-                    int* tensor_core, long long* workspace_bytes);
+                    int* tensor_core, long long* workspace_bytes, int* cluster);
 
 /* Name of a return code, for messages. */
 const char* gqa_status_string(int status);

@@ -241,15 +241,29 @@ def test_paged_host_checks():
 def test_decode_plan_query():
     """gqa_decode_plan on the host (SM count given): persistent grid of at
     most one CTA per SM and at most one per tile (with fewer (sequence, KV
-    head) units than SMs, a whole number of CTAs per unit), the combine kernel exactly
-    when the CTAs outnumber twice the units, the workspace of the partials
-    ((b*g + C) * rows * (d_v + 2) floats) plus 2*b*g counters."""
+    head) units than SMs, a whole number of CTAs per unit).  Where that cuts
+    every unit into three or more pieces (more CTAs than twice the units),
+    the CUDA-core kernel adds the combine kernel, and the tensor-core kernel
+    is launched in clusters of C CTAs, k per unit (the most CTAs over the
+    sizes 2..16, then the fewest clusters per unit; the host-only plan lets
+    every SM take part in clusters of any size) when the streaming time its
+    fewer CTAs give up, capacity at 7.4 TB/s, is below 2 us; else the
+    combine kernel merges.  The workspace holds the
+    partials ((b*g + C) * rows * (d_v + 2) floats) and the arrival counters
+    (2*b*g, or b*g*C in a cluster launch)."""
     b = _lib()
     p = b.gqa_decode_plan(32, 1, 64, 8, 128, 128, 8192, "bf16", num_sms=152)
     assert p["tensor_core"] and p["tile"] == 128 and p["ctas"] == 152 and p["kernels"] == 1
+    assert p["cluster"] == 0
     assert p["workspace_bytes"] == (32 * 8 + 152) * 8 * 130 * 4 + 2 * 32 * 8 * 4
+    # long-context MQA: 8 units of 1024 tiles; the best cluster plan (two
+    # clusters of 9 per unit, 144 CTAs) would give up ~3.8 us of streaming:
+    # 152 CTAs and the combine kernel
     p = b.gqa_decode_plan(8, 1, 32, 1, 128, 128, 131072, "bf16", num_sms=152)
-    assert p["ctas"] == 152 and p["kernels"] == 2
+    assert (p["ctas"], p["cluster"], p["kernels"]) == (152, 0, 2)
+    # the g = 1 point of the sweep: 16 units of 32 tiles, clusters of 9
+    p = b.gqa_decode_plan(16, 1, 32, 1, 128, 128, 4096, "bf16", num_sms=152)
+    assert (p["ctas"], p["cluster"], p["kernels"]) == (144, 9, 1)
     p = b.gqa_decode_plan(32, 4, 64, 8, 128, 128, 8192, "f16", num_sms=152)
     assert p["tensor_core"] and p["kernels"] == 1
     for (bb, n, h, g, dk, dv, cap, dt) in [(1, 1, 8, 1, 64, 64, 256, "f32"),
@@ -257,28 +271,44 @@ def test_decode_plan_query():
                                            (5, 1, 8, 2, 128, 128, 20000, "bf16"),
                                            (16, 1, 32, 8, 128, 128, 4096, "bf16"),
                                            (12, 1, 32, 8, 128, 128, 4096, "bf16"),
+                                           (16, 1, 32, 1, 128, 128, 4096, "bf16"),
                                            (64, 1, 28, 4, 128, 128, 32768, "bf16"),
+                                           (1, 1, 32, 1, 128, 128, 131072, "f16"),
                                            (1, 1, 8, 8, 128, 128, 1, "bf16")]:
         p = b.gqa_decode_plan(bb, n, h, g, dk, dv, cap, dt, num_sms=152)
-        tiles = bb * g * -(-cap // p["tile"])
+        unit_tiles = -(-cap // p["tile"])
+        tiles = bb * g * unit_tiles
         units = bb * g
         # fewer units than SMs, at most half as many: a whole number of CTAs
         # per unit
-        aligned = units * (152 // units) if 2 * units <= 152 else 152
-        assert 1 <= p["ctas"] == min(aligned, tiles)
-        assert p["kernels"] == (2 if p["ctas"] > 2 * bb * g else 1)
-        assert p["tensor_core"] == (dt != "f32")
+        aligned = min(units * (152 // units) if 2 * units <= 152 else 152, tiles)
         rows = n * h // g
+        assert p["tensor_core"] == (dt != "f32")
+        clustered = False
+        if aligned > 2 * units and p["tensor_core"]:
+            pieces = min(aligned // units, unit_tiles)
+            best = max((units * c * min(pieces // c, (152 // c) // units), c)
+                       for c in range(2, 17) if c <= pieces)
+            stream = units * unit_tiles * p["tile"] * (dk + dv) * 2 / 7.4e12
+            clustered = best[0] > 0 and stream * (1 - best[0] / aligned) < 2e-6
+        if clustered:
+            assert p["ctas"] == best[0] and p["cluster"] == best[1] and p["kernels"] == 1
+            assert p["ctas"] % (units * p["cluster"]) == 0
+            counters = units * p["cluster"]
+        else:
+            assert 1 <= p["ctas"] == aligned and p["cluster"] == 0
+            assert p["kernels"] == (2 if p["ctas"] > 2 * bb * g else 1)
+            counters = 2 * units
         assert p["workspace_bytes"] == ((bb * g + p["ctas"]) * rows * (dv + 2) * 4
-                                        + 2 * bb * g * 4)
+                                        + max(counters, 2 * units) * 4)
     # the CUDA-core kernel on request: bf16 up to 8 query rows per KV head
     p = b.gqa_decode_plan(32, 1, 64, 8, 128, 128, 8192, "bf16", num_sms=152,
                           flags=b.GQA_STEP_CUDA_CORES)
     assert not p["tensor_core"] and p["tile"] == 64
     plan = b.lib.gqa_decode_plan
-    assert plan(2, 1, 8, 3, 128, 128, 64, 1, 0, 152, None, None, None, None, None) == -2
-    assert plan(2, 1, 8, 2, 128, 128, 64, 7, 0, 152, None, None, None, None, None) == -3
-    assert plan(2, 1, 8, 2, 96, 96, 64, 1, 0, 152, None, None, None, None, None) == -5
-    assert plan(2, 1, 8, 2, 128, 128, 64, 1, 0, -1, None, None, None, None, None) == -2
-    assert plan(2, 1, 32, 2, 128, 128, 64, 1, 2, 152, None, None, None, None, None) == -5
-    assert plan(2, 1, 8, 2, 128, 128, 64, 1, 4, 152, None, None, None, None, None) == -5
+    assert plan(2, 1, 8, 3, 128, 128, 64, 1, 0, 152, None, None, None, None, None, None) == -2
+    assert plan(2, 1, 8, 2, 128, 128, 64, 7, 0, 152, None, None, None, None, None, None) == -3
+    assert plan(2, 1, 8, 2, 96, 96, 64, 1, 0, 152, None, None, None, None, None, None) == -5
+    assert plan(2, 1, 8, 2, 128, 128, 64, 1, 0, -1, None, None, None, None, None, None) == -2
+    assert plan(2, 1, 32, 2, 128, 128, 64, 1, 2, 152, None, None, None, None, None, None) == -5
+    assert plan(2, 1, 8, 2, 128, 128, 64, 1, 4, 152, None, None, None, None, None, None) == -5

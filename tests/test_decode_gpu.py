@@ -274,10 +274,12 @@ def test_in_kernel_merge_is_deterministic(dtype, h, g, d):
 
 
 @pytest.mark.parametrize("b,h,g,cap", [(1, 8, 1, 20000), (8, 32, 1, 8192), (5, 16, 2, 6000)])
-def test_combine_kernel_is_deterministic(b, h, g, cap):
+def test_combine_kernel_is_deterministic(b, h, g, cap, monkeypatch):
     """Units over many CTAs merged by the combine kernel (up to ~150 pieces a
-    unit, ragged lengths): fixed merge order, the same bits every run."""
+    unit, ragged lengths; GQA_CLUSTER=0 keeps the tensor-core kernel off its
+    cluster launch): fixed merge order, the same bits every run."""
     B = _b()
+    monkeypatch.setenv("GQA_CLUSTER", "0")
     assert B.gqa_decode_plan(b, 1, h, g, 128, 128, cap, "bf16")["kernels"] == 2
     cfg = cfg_of("bf16", b, h, g, 128, cap, seed=b + h)
     lens = np.random.default_rng(b).integers(cap // 2, cap + 1, b).astype(np.int32)
