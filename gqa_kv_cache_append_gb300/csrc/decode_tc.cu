@@ -80,15 +80,27 @@ constexpr int kL2Ahead = 3;
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
 // because the 32-column variant runs at its register limit.
-template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true>
+// WIDE: d_k = d_v = 64 with tiles of 256 positions: a stage holds K rows
+// 0-255 (two [128 x 64] boxes, one after the other) then V rows 0-255, the
+// bytes of a 128-wide tile, so each pass of the per-tile loop moves as much
+// as with 128-wide heads.  S is two M = 128 products (positions 0-127 and
+// 128-255), each softmax thread owns two positions, and O runs over 256
+// positions.  P is written over the stage's K rows, which the S products
+// no longer need, so no P buffers are kept.
+template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true, bool WIDE = false>
 struct TcCfg {
   static constexpr int THREADS = 96 + 128 * NWG;  // producer, 2 MMA issuers, NWG softmax warpgroups
-  static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1
+  static constexpr int TT = WIDE ? 2 * kT : kT;   // positions per tile
+  static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1 (WIDE: K rows, V rows)
   static constexpr int Q_BYTES = NP * 256;         // two [NP x 64] boxes
-  static constexpr int P_BYTES = kT * NP * 2;      // [T rows x NP] bf16
+  static constexpr int P_BYTES = WIDE ? 0 : kT * NP * 2;  // [T rows x NP] bf16 (WIDE: in the stage)
   static constexpr int OFF_Q = kStages * KV_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;       // float [2][NP][4] warp maxima
+  // (WIDE: the O products' unused upper M half reads up to one box past the
+  // last stage's V rows; the region after the ring is at least that long)
+  static constexpr int OFF_RED_MIN = WIDE ? OFF_Q + kBoxBytes : 0;
+  static constexpr int OFF_RED = (OFF_P + 2 * P_BYTES) > OFF_RED_MIN ? (OFF_P + 2 * P_BYTES)
+                                                                     : OFF_RED_MIN;  // float [2][NP][4] warp maxima
   static constexpr int OFF_MAX = OFF_RED + 2 * 4 * NP * 4;   // float [2][NP] running max
   static constexpr int OFF_ALPHA = OFF_MAX + 2 * NP * 4;     // float [2][NP] rescale factors
   static constexpr int OFF_COL = OFF_ALPHA + 2 * NP * 4;     // int [NP] token, int [NP] out row
@@ -101,7 +113,9 @@ struct TcCfg {
   // OFF_MISC: TMEM address, abort flag, two split flags, then (ragged
   // cluster launches) the CTA's split units [2][u, first CTA, last CTA, last]
   static constexpr int SMEM = OFF_MISC + 48;
-  static constexpr int NCOLS = 4 * NP;               // S0 S1 O0 O1
+  // S0 S1 O0 O1 (WIDE: S0a S0b S1a S1b O0 O1), a power of two
+  static constexpr int NCOLS = WIDE ? (NP == 16 ? 128 : 256) : 4 * NP;
+  static constexpr int OFF_TO = WIDE ? 4 * NP : 2 * NP;  // first O column in TMEM
   // P rows are NP * 2 bytes: 32 B (NP=16) or 64 B (NP=32) swizzle atoms
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
   static constexpr uint32_t IDESC = idesc_bf16(128, NP, 0, 0, BF16);    // S: K-major A, B
@@ -111,7 +125,9 @@ struct TcCfg {
   // of K in warp 1 and of V in warp 2); further rows are loaded when patched
   static constexpr int KCH = MULTI ? 2 : 1;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NCOLS == 64 || NCOLS == 128, "TMEM allocation must be a power of two");
+  static_assert(NCOLS == 64 || NCOLS == 128 || NCOLS == 256,
+                "TMEM allocation must be a power of two");
+  static_assert(NCOLS >= OFF_TO + 2 * NP, "TMEM columns");
   static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
 };
 
@@ -130,7 +146,7 @@ enum {
   B_DRAIN = B_O_FREE + 2,
 };
 
-template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE>
 // (register cap: 11 warps put 3 on a sub-partition, 3 x 32 x 168 of its
 // 16384 registers; 7 warps put 2, so 200 fit)
 __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
@@ -145,7 +161,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                      unsigned int* status, long long budget, int early, int nq,
                      const int* __restrict__ table, int bsz, int max_blocks, int num_blocks,
                      int kh, int vh, int cl_size, int cl_k) {
-  using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16>;
+  using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16, WIDE>;
+  constexpr int TT = C::TT;  // positions per tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   const uint32_t s_base = smem_u32(sm);
@@ -216,10 +233,11 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   if (warp == 2 && blockIdx.x == 0) report_bad_lengths(lens, b, nq, cap, status);
 
   Walker w;
-  // (two whole units per CTA only with 128-wide heads, none on a paged
-  // cache, whose per-block copies need every SM: see Walker::init)
-  w.init(lens, b, g, nq, cap, kT, blockIdx.x, gridDim.x,
-         PAGED ? 0 : ((kh == 2 && vh == 2) ? 2 : 1));
+  // (two whole units per CTA only with 128-wide heads or wide tiles, none
+  // on a paged cache, whose per-block copies need every SM: see
+  // Walker::init)
+  w.init(lens, b, g, nq, cap, TT, blockIdx.x, gridDim.x,
+         PAGED ? 0 : ((WIDE || (kh == 2 && vh == 2)) ? 2 : 1));
   Segment seg;
   // Cluster merge: the launch is a cluster launch of cl_size CTAs, cl_k
   // clusters per unit (grid = units * cl_size * cl_k), and every unit has
@@ -242,8 +260,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     const int oob_row = num_blocks * g * bsz;
-    const int sub = bsz < kT ? kT / bsz : 1;      // boxes per half-tile
     const int box_rows = bsz < kT ? bsz : kT;
+    const int sub = TT / box_rows;  // boxes per tile and 64-column half
     uint32_t n = 0, k = 0;
     int last_n[kStages] = {-1, -1, -1};
     int last_q[2] = {-1, -1};
@@ -266,7 +284,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     while (w.next(seg)) {
       if (waited) load_q(k, seg);
       pc.start(table + static_cast<size_t>(seg.i) * max_blocks, (seg.L + bsz - 1) / bsz,
-               (seg.lt0 * kT) / bsz);
+               (seg.lt0 * TT) / bsz);
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         if (!waited && (lt - seg.lt0 == kStages)) {
           pdl_wait_then_release();
@@ -280,13 +298,15 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         if (!ok) continue;
         const uint32_t dst = s_base + st * C::KV_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(BAR(B_FULL_K + st), kh * kBoxBytes);
-          mbar_arrive_expect_tx(BAR(B_FULL_V + st), vh * kBoxBytes);
+          mbar_arrive_expect_tx(BAR(B_FULL_K + st), kh * kBoxBytes * (TT / kT));
+          mbar_arrive_expect_tx(BAR(B_FULL_V + st), vh * kBoxBytes * (TT / kT));
         }
         __syncwarp();
-        // lane mm < sub copies box mm of the tile (its block's rows)
-        const int p_first = lt * kT;
-        const int blk = pc.get_lanes(p_first / bsz);
+        // lane mm < sub copies box mm of the tile (its block's rows; blocks
+        // longer than a box hold every box of the tile)
+        const int p_first = lt * TT;
+        const int blk_l = pc.get_lanes(p_first / bsz);
+        const int blk = (box_rows == bsz) ? blk_l : __shfl_sync(0xffffffffu, blk_l, 0);
         const int pm = p_first + lane * box_rows;
         bool bad = false;
         if (lane < sub) {
@@ -374,11 +394,13 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             // the ring is full: have L2 fetch the next tiles too, so HBM stays
             // busy until the kernel ahead completes
             for (int lp = lt; lp < seg.lt1 && lp < lt + (counters ? kPrefetchTiles : 0); ++lp) {
-              const int rp = unit_row + lp * kT;
+              const int rp = unit_row + lp * TT;
               tma_prefetch_l2_2d(&tm_k, 0, rp);
               if (kh == 2) tma_prefetch_l2_2d(&tm_k, 64, rp);
+              if (WIDE) tma_prefetch_l2_2d(&tm_k, 0, rp + kT);
               tma_prefetch_l2_2d(&tm_v, 0, rp);
               if (vh == 2) tma_prefetch_l2_2d(&tm_v, 64, rp);
+              if (WIDE) tma_prefetch_l2_2d(&tm_v, 0, rp + kT);
             }
             pdl_wait_then_release();
             waited = true;
@@ -388,17 +410,24 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           if (!mbar_wait(BAR(B_EMPTY + st), ((n / kStages) & 1) ^ 1, abort_flag, status,
                          budget))
             continue;
-          const int row = unit_row + lt * kT;
+          const int row = unit_row + lt * TT;
           const uint32_t dst = s_base + st * C::KV_BYTES;
-          mbar_arrive_expect_tx(BAR(B_FULL_K + st), kh * kBoxBytes);
+          // (WIDE: the second box of each tensor is rows 128-255, not
+          // columns 64-127)
+          mbar_arrive_expect_tx(BAR(B_FULL_K + st), kh * kBoxBytes * (TT / kT));
           tma_load_2d(dst, &tm_k, BAR(B_FULL_K + st), 0, row, pol_stream);
-          if (kh == 2) tma_load_2d(dst + kBoxBytes, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
-          mbar_arrive_expect_tx(BAR(B_FULL_V + st), vh * kBoxBytes);
+          if (WIDE)
+            tma_load_2d(dst + kBoxBytes, &tm_k, BAR(B_FULL_K + st), 0, row + kT, pol_stream);
+          else if (kh == 2)
+            tma_load_2d(dst + kBoxBytes, &tm_k, BAR(B_FULL_K + st), 64, row, pol_stream);
+          mbar_arrive_expect_tx(BAR(B_FULL_V + st), vh * kBoxBytes * (TT / kT));
           tma_load_2d(dst + 2 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 0, row, pol_stream);
-          if (vh == 2)
+          if (WIDE)
+            tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 0, row + kT, pol_stream);
+          else if (vh == 2)
             tma_load_2d(dst + 3 * kBoxBytes, &tm_v, BAR(B_FULL_V + st), 64, row, pol_stream);
           last_n[st] = static_cast<int>(n);
-          if (kh + vh == 2 && waited && lt + kL2Ahead < seg.lt1) {
+          if (!WIDE && kh + vh == 2 && waited && lt + kL2Ahead < seg.lt1) {
             const int rp = row + kL2Ahead * kT;
             tma_prefetch_l2_2d(&tm_k, 0, rp);
             if (kh == 2) tma_prefetch_l2_2d(&tm_k, 64, rp);
@@ -453,7 +482,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     // for V before the tile's O product.
     const bool s_role = warp == 1;
     const bool leader = lane == 0;
-    const uint32_t tS = tmem, tO = tmem + 2 * NP;
+    const uint32_t tS = tmem, tO = tmem + C::OFF_TO;
+    constexpr int NH = WIDE ? 2 : 1;  // S products (128-position halves) per tile
     // operand descriptors: a stage, a buffer or a k-step only moves the
     // start-address field (16-byte units, no carry out of it)
     auto issue_o = [&](uint32_t m) {
@@ -468,15 +498,19 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         if (ok) {
           const uint64_t a0 =
               smem_desc(s_base + st * C::KV_BYTES + 2 * kBoxBytes, kBoxBytes, 1024, SWZ_128B);
-          const uint64_t b0 =
-              smem_desc(s_base + C::OFF_P + nb * C::P_BYTES, C::P_BYTES, 8 * NP * 2, C::P_SWZ);
+          // (WIDE: P lies over the stage's K rows)
+          const uint32_t pbase =
+              WIDE ? s_base + st * C::KV_BYTES : s_base + C::OFF_P + nb * C::P_BYTES;
+          const uint64_t b0 = smem_desc(pbase, TT * NP * 2, 8 * NP * 2, C::P_SWZ);
 #pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk) {
+          for (int kk = 0; kk < TT / 16; ++kk) {
             // A = V^T: M = 128 head-dim columns (two 64-column boxes, LBO
             // apart), K = 16 positions (two 8-row groups, SBO apart; 2 KiB
             // a step).  With d_v = 64 the second box is not loaded: output
-            // rows 64-127 are never read.  B = P^T: N = NP heads contiguous
-            // per row, K = 16 position rows (16 * NP * 2 bytes a step).
+            // rows 64-127 are never read (WIDE: the V rows continue into the
+            // second box, and the upper M half reads the box after the
+            // current one).  B = P^T: N = NP heads contiguous per row, K =
+            // 16 position rows (16 * NP * 2 bytes a step).
             mma_bf16(tO + nb * NP, a0 + kk * (2048 >> 4), b0 + kk * ((16 * NP * 2) >> 4),
                      C::IDESC_O, kk > 0 ? 1u : 0u);
           }
@@ -494,7 +528,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       const int first_new = seg.L - nq;
       int s_lo = 0, nrows = 0;
       if (k_new != nullptr) {
-        const int p_lo = max(first_new, seg.lt0 * kT), p_hi = min(seg.L, seg.lt1 * kT);
+        const int p_lo = max(first_new, seg.lt0 * TT), p_hi = min(seg.L, seg.lt1 * TT);
         if (p_lo < p_hi) {
           s_lo = p_lo - first_new;
           nrows = p_hi - p_lo;
@@ -552,13 +586,13 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           if (c4 >= nregs) break;
           const int idx = lane + 32 * c4;
           const int pos = first_new + s_lo + (idx >> sh);
-          if (idx < nchunk && pos >= lt * kT && pos < (lt + 1) * kT)
-            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * kT, regs[c4]);
+          if (idx < nchunk && pos >= lt * TT && pos < (lt + 1) * TT)
+            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * TT, regs[c4]);
         }
         for (int idx = lane + 32 * nregs; idx < nchunk; idx += 32) {
           const int pos = first_new + s_lo + (idx >> sh);
-          if (pos >= lt * kT && pos < (lt + 1) * kT)
-            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * kT,
+          if (pos >= lt * TT && pos < (lt + 1) * TT)
+            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * TT,
                 __ldg(src + new_off(idx, sh)));
         }
         fence_proxy_async_smem();
@@ -573,7 +607,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           if (MULTI && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
         }
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
-          const bool new_rows = nrows > 0 && (lt + 1) * kT > first_new;
+          const bool new_rows = nrows > 0 && (lt + 1) * TT > first_new;
           if (MULTI && new_rows) {
             // the tile's new V rows, before its O product (the softmax
             // warps zero the rows past L_i, which are other rows)
@@ -607,7 +641,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
         ok = __all_sync(0xffffffffu, ok);
         const uint32_t kbase = s_base + st * C::KV_BYTES;
-        const bool new_rows = nrows > 0 && (lt + 1) * kT > first_new;
+        const bool new_rows = nrows > 0 && (lt + 1) * TT > first_new;
         if (new_rows) {
           // rows L_i - n .. L_i - 1 of this tile are the new tokens: use
           // k_new there, and store them into the cache (the append)
@@ -617,18 +651,25 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         tc_fence_after();
         if (leader) {
           if (ok) {
-            const uint64_t a0 = smem_desc(s_base + st * C::KV_BYTES, 16, 1024, SWZ_128B);
             const uint64_t b0 = smem_desc(s_base + C::OFF_Q + qs * C::Q_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              // A = K tile, K-major: 128 rows, 16 head-dim columns (32
-              // bytes) per step; steps 0-3 in the first 64-column box, 4-7
-              // in the second (d_k = 128 only).  B = the q block, the same
-              // way ([NP x 64] boxes).
-              if (kk >= 4 * kh) break;
-              mma_bf16(tS + nb * NP, a0 + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
-                       b0 + (((kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4), C::IDESC,
-                       kk > 0 ? 1u : 0u);
+            for (int hf = 0; hf < NH; ++hf) {
+              // (WIDE: half hf = positions 128 hf .. 128 hf + 127, the
+              // stage's box hf, into its own accumulator)
+              const uint64_t a0 =
+                  smem_desc(s_base + st * C::KV_BYTES + hf * kBoxBytes, 16, 1024, SWZ_128B);
+#pragma unroll
+              for (int kk = 0; kk < kD / 16; ++kk) {
+                // A = K tile, K-major: 128 rows, 16 head-dim columns (32
+                // bytes) per step; steps 0-3 in the first 64-column box, 4-7
+                // in the second (d_k = 128 only).  B = the q block, the same
+                // way ([NP x 64] boxes).
+                if (kk >= 4 * kh) break;
+                mma_bf16(tS + (nb * NH + hf) * NP,
+                         a0 + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
+                         b0 + (((kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4), C::IDESC,
+                         kk > 0 ? 1u : 0u);
+              }
             }
           }
           mma_commit(BAR(B_S_FULL + nb));
@@ -661,7 +702,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     const int h0 = wg * HP;           // first head of this warpgroup
     const int bar_id = 1 + wg;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tS = tmem + lane_off + h0, tO = tmem + 2 * NP + lane_off + h0;
+    const uint32_t tS = tmem + lane_off + h0, tO = tmem + C::OFF_TO + lane_off + h0;
+    constexpr int NH = WIDE ? 2 : 1;  // positions per thread and tile: row (+ 128)
     float* red_wg = red + wg * 2 * HP * 4;   // [2][HP][4]
     int* last_flag_wg = last_flag + wg;
 
@@ -731,53 +773,63 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         const uint32_t nb = n & 1;
         const int st = n % kStages;
-        const int valid = min(kT, seg.L - lt * kT);
-        // ---- logits from TMEM ----
+        const int valid = min(TT, seg.L - lt * TT);
+        // ---- logits from TMEM (WIDE: both 128-position halves) ----
         const bool ok = mbar_wait(BAR(B_S_FULL + nb), (n >> 1) & 1, abort_flag, status, budget);
-        float x[HP];
+        float x[NH][HP];
         if (ok) {
 #pragma unroll
-          for (int c = 0; c < HP; c += 16) {
-            float tmp[16];
-            tmem_ld16(tS + nb * NP + c, tmp);
+          for (int hf = 0; hf < NH; ++hf) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[c + e] = tmp[e];
+            for (int c = 0; c < HP; c += 16) {
+              float tmp[16];
+              tmem_ld16(tS + (nb * NH + hf) * NP + c, tmp);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) x[hf][c + e] = tmp[e];
+            }
           }
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int e = 0; e < HP; ++e) x[e] = 0.f;
+          for (int hf = 0; hf < NH; ++hf)
+#pragma unroll
+            for (int e = 0; e < HP; ++e) x[hf][e] = 0.f;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_S_FREE + nb));
-        const bool live = row < valid;
-        if (!MULTI) {
 #pragma unroll
-          for (int e = 0; e < HP; ++e)
-            x[e] = (live && h0 + e < nr) ? x[e] * scale_log2 : -INFINITY;
-        } else if ((lt + 1) * kT <= first_new + 1) {
-          // (uniform) every new token sees every position of the tile
+        for (int hf = 0; hf < NH; ++hf) {
+          const int pos = row + hf * kT;  // position within the tile
+          const bool live = pos < valid;
+          if (!MULTI) {
 #pragma unroll
-          for (int e = 0; e < HP; ++e) x[e] = (h0 + e < nr) ? x[e] * scale_log2 : -INFINITY;
-        } else {
-          // token s sees this position iff s >= -vis (the causal mask; for
-          // n = 1 it is the p < L_i mask; padded columns see nothing)
-          const int vis = first_new - lt * kT - row;
+            for (int e = 0; e < HP; ++e)
+              x[hf][e] = (live && h0 + e < nr) ? x[hf][e] * scale_log2 : -INFINITY;
+          } else if ((lt + 1) * TT <= first_new + 1) {
+            // (uniform) every new token sees every position of the tile
 #pragma unroll
-          for (int e4 = 0; e4 < HP; e4 += 4) {
-            const int4 tk = *reinterpret_cast<const int4*>(col_tok + h0 + e4);
-            const int tt[4] = {tk.x, tk.y, tk.z, tk.w};
+            for (int e = 0; e < HP; ++e)
+              x[hf][e] = (h0 + e < nr) ? x[hf][e] * scale_log2 : -INFINITY;
+          } else {
+            // token s sees this position iff s >= -vis (the causal mask; for
+            // n = 1 it is the p < L_i mask; padded columns see nothing)
+            const int vis = first_new - lt * TT - pos;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              x[e4 + k] = (tt[k] >= -vis) ? x[e4 + k] * scale_log2 : -INFINITY;
+            for (int e4 = 0; e4 < HP; e4 += 4) {
+              const int4 tk = *reinterpret_cast<const int4*>(col_tok + h0 + e4);
+              const int tt[4] = {tk.x, tk.y, tk.z, tk.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                x[hf][e4 + k] = (tt[k] >= -vis) ? x[hf][e4 + k] * scale_log2 : -INFINITY;
+            }
           }
         }
-        // ---- per-head max over the tile's 128 positions ----
+        // ---- per-head max over the tile's positions ----
         float mine = -INFINITY;
 #pragma unroll
         for (int e = 0; e < HP; ++e) {
-          const float wm = warp_max(x[e]);
+          const float wm = warp_max(NH == 2 ? fmaxf(x[0][e], x[NH - 1][e]) : x[0][e]);
           if (lane == e) mine = wm;
         }
         // head-major [HP][4 warps]; thread e folds head h0 + e's four warp
@@ -802,7 +854,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           }
         }
         named_bar_sync(bar_id, 128);
-        // probabilities (x[e] becomes p[e]) and this thread's sums
+        // probabilities (x becomes p) and this thread's sums
 #pragma unroll
         for (int e4 = 0; e4 < HP; e4 += 4) {
           const float4 mv = *reinterpret_cast<const float4*>(max_sm + nb * NP + h0 + e4);
@@ -812,37 +864,47 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int e = e4 + k;
-            x[e] = (h0 + e < nr) ? ex2(x[e] - mm[k]) : 0.f;
-            l[e] = fmaf(l[e], aa[k], x[e]);
+#pragma unroll
+            for (int hf = 0; hf < NH; ++hf)
+              x[hf][e] = (h0 + e < nr) ? ex2(x[hf][e] - mm[k]) : 0.f;
+            l[e] = fmaf(l[e], aa[k], NH == 2 ? x[0][e] + x[NH - 1][e] : x[0][e]);
           }
         }
-        // ---- P^T row `row`, this warpgroup's heads, into the MN-major
-        // swizzled B operand (16-byte chunks of 8 heads) ----
+        // ---- P^T rows (position row, + 128), this warpgroup's heads, into
+        // the MN-major swizzled B operand (16-byte chunks of 8 heads; WIDE:
+        // over the stage's K rows, which the S products have finished
+        // reading) ----
         {
-          const uint32_t prow = s_base + C::OFF_P + nb * C::P_BYTES + row * (NP * 2);
+          const uint32_t pbase =
+              WIDE ? s_base + st * C::KV_BYTES : s_base + C::OFF_P + nb * C::P_BYTES;
 #pragma unroll
-          for (int c = 0; c < HP / 8; ++c) {
-            uint32_t wv[4];
+          for (int hf = 0; hf < NH; ++hf) {
+            const uint32_t prow = pbase + (row + hf * kT) * (NP * 2);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              wv[k] = Half16<T16>::pack2(x[8 * c + 2 * k], x[8 * c + 2 * k + 1]);
+            for (int c = 0; c < HP / 8; ++c) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                wv[k] = Half16<T16>::pack2(x[hf][8 * c + 2 * k], x[hf][8 * c + 2 * k + 1]);
+              }
+              const int cg = h0 / 8 + c;  // chunk index within the row
+              const int phys = (NP == 16) ? (cg ^ ((row >> 2) & 1)) : (cg ^ ((row >> 1) & 3));
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys * 16),
+                           "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                           : "memory");
             }
-            const int cg = h0 / 8 + c;  // chunk index within the row
-            const int phys = (NP == 16) ? (cg ^ ((row >> 2) & 1)) : (cg ^ ((row >> 1) & 3));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys * 16),
-                         "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
-                         : "memory");
           }
         }
         // ---- last tile of a unit (warpgroup 0): zero the V rows past L_i;
         // one token: put v_new into row L_i - 1 and into the cache (n
         // tokens: the O-issuing warp patches the new rows) ----
         const bool patch_v = append_v && lt == seg.ti - 1;
-        if (wg == 0 && (valid < kT || patch_v)) {
+        if (wg == 0 && (valid < TT || patch_v)) {
           const bool vok =
               mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
           const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
           if (vok && patch_v && row < vch) {
+            // (WIDE: rows 0-255 run on through the second box)
             const int rho = valid - 1;
             const uint32_t dst =
                 vbase + (row >> 3) * kBoxBytes + rho * 128 + (((row & 7) ^ (rho & 7)) << 4);
@@ -851,16 +913,20 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                          : "memory");
             if (vrow_w >= 0) v_cache_w[(vrow_w << shv) + row] = vnew;
           }
-          if (vok && !live) {
-            const uint32_t vrow = vbase + row * 128;
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
+          for (int hf = 0; hf < NH; ++hf) {
+            const int pos = row + hf * kT;
+            if (vok && pos >= valid) {
+              const uint32_t vrow = vbase + pos * 128;
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
-                                 vrow + hb * kBoxBytes + c * 16),
-                             "r"(0u)
-                             : "memory");
+              for (int hb = 0; hb < (WIDE ? 1 : 2); ++hb)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                   vrow + hb * kBoxBytes + c * 16),
+                               "r"(0u)
+                               : "memory");
+            }
           }
         }
         fence_proxy_async_smem();
@@ -1281,10 +1347,10 @@ cudaError_t configure_kernel(K kern, int smem, std::atomic<unsigned long long>& 
   return cudaSuccess;
 }
 
-template <int NP, int NWG, bool MULTI, bool PAGED, typename T16>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE>
 cudaError_t launch_np(const DecodeLaunch& a) {
   constexpr bool kBf16 = Half16<T16>::kBf16;
-  using C = TcCfg<NP, NWG, MULTI, PAGED, kBf16>;
+  using C = TcCfg<NP, NWG, MULTI, PAGED, kBf16, WIDE>;
   CUtensorMap mq, mk, mv;
   // contiguous caches: [b * g * cap rows x 128]; pools: [num_blocks * g * block_size rows]
   const uint64_t kv_rows = PAGED ? static_cast<uint64_t>(a.num_blocks) * a.g * a.block_size
@@ -1294,7 +1360,7 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       !make_map(&mk, a.k_cache, a.d, kv_rows, box_rows, kBf16) ||
       !make_map(&mv, a.v_cache, a.dv, kv_rows, box_rows, kBf16))
     return cudaErrorInvalidValue;
-  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16>;
+  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16, WIDE>;
   static std::atomic<unsigned long long> configured{0};  // devices done, this variant
   if (cudaError_t e = configure_kernel(kern, C::SMEM, configured)) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1323,21 +1389,26 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       a.dv / 64, a.cluster > 1 ? a.cluster : 0, a.cluster > 1 ? a.cluster_k : 1);
 }
 
-template <typename T16>
+template <typename T16, bool WIDE>
 cudaError_t launch_type(const DecodeLaunch& a) {
   const int cols = a.nq * (a.h / a.g);
   const bool one = a.nq == 1;
   if (a.block_table != nullptr) {
     if (one)
-      return cols <= 16 ? launch_np<16, 1, false, true, T16>(a)
-                        : launch_np<32, 2, false, true, T16>(a);
-    return cols <= 16 ? launch_np<16, 1, true, true, T16>(a) : launch_np<32, 2, true, true, T16>(a);
+      return cols <= 16 ? launch_np<16, 1, false, true, T16, WIDE>(a)
+                        : launch_np<32, 2, false, true, T16, WIDE>(a);
+    return cols <= 16 ? launch_np<16, 1, true, true, T16, WIDE>(a)
+                      : launch_np<32, 2, true, true, T16, WIDE>(a);
   }
   if (one)
-    return cols <= 16 ? launch_np<16, 1, false, false, T16>(a)
-                      : launch_np<32, 2, false, false, T16>(a);
-  return cols <= 16 ? launch_np<16, 1, true, false, T16>(a) : launch_np<32, 2, true, false, T16>(a);
+    return cols <= 16 ? launch_np<16, 1, false, false, T16, WIDE>(a)
+                      : launch_np<32, 2, false, false, T16, WIDE>(a);
+  return cols <= 16 ? launch_np<16, 1, true, false, T16, WIDE>(a)
+                    : launch_np<32, 2, true, false, T16, WIDE>(a);
 }
+
+// d_k = d_v = 64 takes tiles of 256 positions
+bool wide_tiles(int d_k, int d_v) { return d_k == 64 && d_v == 64; }
 
 }  // namespace
 
@@ -1346,7 +1417,7 @@ bool tc_supported(int dtype, int d_k, int d_v, int cols) {
          (d_v == 64 || d_v == 128) && cols >= 1 && cols <= 32;
 }
 
-int tc_tile() { return kT; }
+int tc_tile(int d_k, int d_v) { return wide_tiles(d_k, d_v) ? 2 * kT : kT; }
 
 int tc_max_clusters(int csize) {
   // One CTA per SM whatever the variant (every one takes over 200 KiB of
@@ -1357,8 +1428,8 @@ int tc_max_clusters(int csize) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (init[dev][csize].load()) return cache[dev][csize].load();
-  using C = TcCfg<32, 2, false, false, true>;
-  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16>;
+  using C = TcCfg<32, 2, false, false, true, false>;
+  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16, false>;
   static std::atomic<unsigned long long> configured{0};
   if (configure_kernel(kern, C::SMEM, configured) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
@@ -1385,7 +1456,9 @@ int tc_max_clusters(int csize) {
 int tc_ctas_per_sm(int) { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeLaunch& a) {
-  return a.dtype == GQA_F16 ? launch_type<__half>(a) : launch_type<__nv_bfloat16>(a);
+  if (wide_tiles(a.d, a.dv))
+    return a.dtype == GQA_F16 ? launch_type<__half, true>(a) : launch_type<__nv_bfloat16, true>(a);
+  return a.dtype == GQA_F16 ? launch_type<__half, false>(a) : launch_type<__nv_bfloat16, false>(a);
 }
 
 }  // namespace gqa

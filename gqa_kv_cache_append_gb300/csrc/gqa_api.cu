@@ -671,7 +671,7 @@ DecodePlan decode_plan(const DecodeArgs& x, int num_sms, bool query_device = tru
   const int r = x.h / x.g, d = x.d_k, cols = x.nq * r;
   const bool use_tc = use_tensor_cores(x, cols);
   DecodePlan p;
-  p.tile = use_tc ? tc_tile() : simt_tile(x.dtype, x.d_k, x.d_v);
+  p.tile = use_tc ? tc_tile(x.d_k, x.d_v) : simt_tile(x.dtype, x.d_k, x.d_v);
   const int per_sm = use_tc ? tc_ctas_per_sm(r) : simt_ctas_per_sm(x.dtype, d, r);
   const long long units = static_cast<long long>(x.b) * x.g;
   const long long unit_tiles = (x.cap + p.tile - 1) / p.tile;
@@ -686,11 +686,14 @@ DecodePlan decode_plan(const DecodeArgs& x, int num_sms, bool query_device = tru
   if (use_tc && knob_cluster != 0 && use_combine_kernel(p.nc, x.b, x.g)) {
     // A cluster launch saves the combine kernel (its run and one more grid
     // completion: about 2 us back to back) but fits fewer CTAs (whole
-    // clusters per unit, as many as the GPCs hold), so it streams slower.
-    // It is taken when the streaming time it gives up, estimated from the
-    // capacity at 7.4 TB/s, is below that; measured: 128 cluster CTAs for
-    // 16 units of 32 tiles 15.7 us per call against 17.0 with the combine
-    // kernel, 144 for 8 units of 1024 tiles 89.4 against 84.4.
+    // clusters per unit, as many as the GPCs hold), so it streams slower,
+    // and with more than two clusters per unit the merge of their results
+    // waits for the slowest cluster.  It is taken with at most two clusters
+    // per unit when the streaming time it gives up, estimated from the
+    // capacity at 7.4 TB/s, is below 2 us.  Measured: 128 cluster CTAs (4 x
+    // 2 per unit) for 16 units of 32 tiles 15.7 us per call against 17.0
+    // with the combine kernel; 144 (2 x 9 per unit) for 8 units of 1024
+    // tiles 89.4 against 84.4.
     DecodePlan cl = p;
     const long long pieces = std::min(p.nc / units, unit_tiles);
     if (query_device)
@@ -701,7 +704,7 @@ DecodePlan decode_plan(const DecodeArgs& x, int num_sms, bool query_device = tru
                             (x.d_k + x.d_v) * elt_bytes(x.dtype) / 7.4e12;
     const double lost_s =
         stream_s * (1.0 - static_cast<double>(cl.nc) / static_cast<double>(p.nc));
-    if (cl.cluster > 1 && (knob_cluster >= 2 || lost_s < 2e-6)) p = cl;
+    if (cl.cluster > 1 && (knob_cluster >= 2 || (cl.cluster_k <= 2 && lost_s < 2e-6))) p = cl;
   }
   const size_t slots = static_cast<size_t>(units) + static_cast<size_t>(p.nc);
   p.o_bytes = slots * cols * x.d_v * sizeof(float);

@@ -246,15 +246,19 @@ def test_decode_plan_query():
     the CUDA-core kernel adds the combine kernel, and the tensor-core kernel
     is launched in clusters of C CTAs, k per unit (the most CTAs over the
     sizes 2..16, then the fewest clusters per unit; the host-only plan lets
-    every SM take part in clusters of any size) when the streaming time its
-    fewer CTAs give up, capacity at 7.4 TB/s, is below 2 us; else the
-    combine kernel merges.  The workspace holds the
+    every SM take part in clusters of any size) when k <= 2 and the
+    streaming time its fewer CTAs give up, capacity at 7.4 TB/s, is below
+    2 us; else the combine kernel merges.  The workspace holds the
     partials ((b*g + C) * rows * (d_v + 2) floats) and the arrival counters
     (2*b*g, or b*g*C in a cluster launch)."""
     b = _lib()
     p = b.gqa_decode_plan(32, 1, 64, 8, 128, 128, 8192, "bf16", num_sms=152)
     assert p["tensor_core"] and p["tile"] == 128 and p["ctas"] == 152 and p["kernels"] == 1
     assert p["cluster"] == 0
+    # 64-wide heads: tiles of 256 positions (fp32: the CUDA-core kernel's 64)
+    assert b.gqa_decode_plan(32, 1, 64, 8, 64, 64, 8192, "bf16", num_sms=152)["tile"] == 256
+    assert b.gqa_decode_plan(32, 1, 64, 8, 64, 64, 8192, "f16", num_sms=152)["tile"] == 256
+    assert b.gqa_decode_plan(32, 1, 64, 8, 64, 128, 8192, "bf16", num_sms=152)["tile"] == 128
     assert p["workspace_bytes"] == (32 * 8 + 152) * 8 * 130 * 4 + 2 * 32 * 8 * 4
     # long-context MQA: 8 units of 1024 tiles; the best cluster plan (two
     # clusters of 9 per unit, 144 CTAs) would give up ~3.8 us of streaming:
@@ -274,6 +278,8 @@ def test_decode_plan_query():
                                            (16, 1, 32, 1, 128, 128, 4096, "bf16"),
                                            (64, 1, 28, 4, 128, 128, 32768, "bf16"),
                                            (1, 1, 32, 1, 128, 128, 131072, "f16"),
+                                           (8, 1, 32, 1, 64, 64, 131072, "bf16"),
+                                           (16, 1, 32, 1, 64, 64, 2048, "bf16"),
                                            (1, 1, 8, 8, 128, 128, 1, "bf16")]:
         p = b.gqa_decode_plan(bb, n, h, g, dk, dv, cap, dt, num_sms=152)
         unit_tiles = -(-cap // p["tile"])
@@ -289,8 +295,9 @@ def test_decode_plan_query():
             pieces = min(aligned // units, unit_tiles)
             best = max((units * c * min(pieces // c, (152 // c) // units), c)
                        for c in range(2, 17) if c <= pieces)
+            k = best[0] // (units * best[1])
             stream = units * unit_tiles * p["tile"] * (dk + dv) * 2 / 7.4e12
-            clustered = best[0] > 0 and stream * (1 - best[0] / aligned) < 2e-6
+            clustered = best[0] > 0 and k <= 2 and stream * (1 - best[0] / aligned) < 2e-6
         if clustered:
             assert p["ctas"] == best[0] and p["cluster"] == best[1] and p["kernels"] == 1
             assert p["ctas"] % (units * p["cluster"]) == 0

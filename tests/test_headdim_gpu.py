@@ -230,3 +230,73 @@ def test_cuda_core_multi_token_on_request():
     assert to_np(d["k_cache"])[0].tobytes() == kc.tobytes()
     assert to_np(d["v_cache"])[0].tobytes() == vc.tobytes()
     assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", "CUDA cores, n = 2")
+
+
+# ---- 64-wide heads (d_k = d_v = 64) take tiles of 256 positions: lengths,
+# new rows and paged blocks at the 128- and 256-position edges
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("b,h,g,cap,lens", [
+    (6, 8, 1, 600, [1, 127, 128, 129, 255, 256]),
+    (5, 32, 2, 1100, [257, 383, 384, 385, 1100]),   # r = 16
+    (2, 32, 1, 800, [511, 513]),                     # r = 32: two softmax warpgroups
+    (1, 8, 1, 40000, [40000 - 77]),                  # one unit over many CTAs
+    (128, 8, 1, 1024, [1024] * 128),                 # one whole unit per CTA
+    (256, 8, 1, 512, [512] * 256),                   # two whole units per CTA
+])
+def test_wide_tiles(dtype, b, h, g, cap, lens):
+    from gqa_kv_cache_append_gb300 import binding as B
+    assert B.gqa_decode_plan(b, 1, h, g, 64, 64, cap, dtype)["tile"] == 256
+    run_one(dtype, b, h, g, 64, 64, cap, lens, seed=b + 5 * h + cap)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_wide_tiles_multi_token(fused):
+    """4 new tokens x 8 heads: the new rows straddle the two halves of a tile
+    (L = 130) and two tiles (L = 258)."""
+    B = _b()
+    b, n, h, g, dk, dv, cap, lens = 4, 4, 16, 2, 64, 64, 600, [258, 130, 4, 600]
+    x, _ = _case("bf16", b, n, h, g, dk, dv, cap, lens, seed=91)
+    d = {k: v.cuda() for k, v in x.items()}
+    out = torch.full((b, n, h, dv), 3.0, dtype=torch.bfloat16, device="cuda")
+    if fused:
+        B.gqa_decode_step_multi(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                                d["seq_lens"], b, n, h, g, dk, dv, 0.125, out)
+    else:
+        B.gqa_kv_append_multi(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                              d["seq_lens"], b, n, g, dk, dv)
+        B.gqa_decode_attn_multi(d["q"], d["k_cache"], d["v_cache"], d["seq_lens"], b, n, h, g,
+                                dk, dv, 0.125, out)
+    assert B.gqa_device_status() == 0
+    ref, kc, vc = oracle.decode_step_multi(*(_np(x, k) for k in ("q", "k_cache", "v_cache",
+                                                                   "k_new", "v_new")),
+                                           np.asarray(lens), g, 0.125, dtype="bf16")
+    assert to_np(d["k_cache"])[0].tobytes() == kc.tobytes()
+    assert to_np(d["v_cache"])[0].tobytes() == vc.tobytes()
+    assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", "wide tiles, n = 4")
+
+
+@pytest.mark.parametrize("bs,n", [(16, 1), (64, 3), (128, 1), (256, 1), (512, 3)])
+def test_wide_tiles_paged(bs, n):
+    """Blocks shorter than a 128-row box (one box each), as long as a box
+    (two blocks a tile) and longer than a tile (both boxes from one block)."""
+    from gqa_kv_cache_append_gb300.inputs import to_paged
+    B = _b()
+    b, h, g, dk, dv, cap, lens = 3, 8, 2, 64, 64, 1024, [max(1, n), 385, 1024]
+    x, _ = _case("bf16", b, n if n > 1 else 0, h, g, dk, dv, cap, lens, seed=bs + n)
+    kp, _, table = to_paged(x["k_cache"], x["k_cache"], bs, seed=9, fill=float("nan"))
+    _, vp, _ = to_paged(x["v_cache"], x["v_cache"], bs, seed=9, fill=float("nan"))
+    d = {k: v.cuda() for k, v in x.items()}
+    kp_d, vp_d = kp.cuda(), vp.cuda()
+    out = torch.full(tuple(x["q"].shape[:-1]) + (dv,), 3.0, dtype=torch.bfloat16, device="cuda")
+    B.gqa_decode_step_paged(d["q"], d["k_new"], d["v_new"], kp_d, vp_d, table.cuda(),
+                            d["seq_lens"], b, h, g, dk, dv, 0.1, out, n=n)
+    assert B.gqa_device_status() == 0
+    args = (_np(x, "q"), to_np(kp)[0], to_np(vp)[0], _np(x, "k_new"), _np(x, "v_new"),
+            table.numpy(), np.asarray(lens), g, 0.1, bs)
+    if n == 1:
+        ref, kp2, vp2 = oracle.decode_step_paged(*args, dtype="bf16")
+    else:
+        ref, kp2, vp2 = oracle.decode_step_paged_multi(*args, dtype="bf16")
+    assert to_np(kp_d)[0].tobytes() == kp2.tobytes()
+    assert to_np(vp_d)[0].tobytes() == vp2.tobytes()
+    assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", f"wide paged bs{bs} n{n}")
