@@ -3,13 +3,16 @@
 //
 // One persistent CTA per SM streams its share of the (sequence, KV head)
 // tiles (see Walker).  Warp 0 copies each K/V tile of T positions from HBM
-// into a shared-memory ring with one bulk copy per tensor (the rows of a
-// tile are contiguous in the cache), completing on an mbarrier; only the
-// rows below L_i are copied.  Warps 1-4 serve all r = h/g query heads of the
-// KV head from each tile:
+// into a five-stage shared-memory ring with one bulk copy per tensor (the
+// rows of a tile are contiguous in the cache), completing on an mbarrier;
+// only the rows below L_i are copied.  Warps 1-7 serve all r = h/g query
+// heads of the KV head from each tile:
 //   A  logits: 16-byte vector loads of K, fp32 dot products against q held
-//      in registers, reduced across the lanes that share a row by xor
-//      shuffles (the "bhk,bhmk->bhm" contraction of the MQA review §2.4);
+//      in registers, summed across the lanes that share a row by a
+//      reduce-scatter of xor shuffles (each round trades half of the heads'
+//      partial sums with the partner lane: r - 1 + log2(lanes / r)
+//      shuffles a row instead of r log2(lanes)) (the "bhk,bhmk->bhm"
+//      contraction of the MQA review §2.4);
 //   B  online softmax per head in base 2: warp max, rescale factor, exp2,
 //      warp sum;
 //   C  weighted sum of V rows into fp32 register accumulators ("bhm,bhmv->
@@ -76,8 +79,15 @@ struct Elt<__half> {
 };
 
 // DK / DV: head dims of K (and q) and of V (and out); they may differ.
+// Seven compute warps: eight warps in all, two per SM sub-partition, so a
+// thread may hold up to 255 registers (measured: fifteen compute warps of
+// 128 registers were slower on the fp32 Llama-3-70B shape, 2.0 against 2.6
+// TB/s, their share of the weighted sum taking twice as long).
 template <typename DT, int DK, int DV, int RMAX>
 struct SimtCfg {
+  static constexpr int NCW = 7;
+  static constexpr int NCT = 32 * NCW;          // compute threads
+  static constexpr int THREADS = 32 + NCT;      // warp 0 copies
   static constexpr int ELT = Elt<DT>::size;
   static constexpr int CHK = DK * ELT / 16;    // 16-byte chunks per K row
   static constexpr int CHV = DV * ELT / 16;    // ... per V row
@@ -85,9 +95,9 @@ struct SimtCfg {
   static constexpr int PPW = 32 / CHK;         // K rows per warp step
   static constexpr int DM = DK > DV ? DK : DV;
   static constexpr int T = 16384 / (DM * ELT); // positions per tile (up to 32 KiB K+V)
-  static constexpr int PPL = T / 32;           // positions per lane in softmax
-  static constexpr int NPG = 128 / CHV;        // position groups in the V pass
-  static constexpr int STAGES = 3;
+  static constexpr int PPL = T / 16;           // positions per lane in softmax
+  static constexpr int NPG = NCT / CHV;        // position groups in the V pass
+  static constexpr int STAGES = 5;
   static constexpr int K_BYTES = T * DK * ELT;
   static constexpr int STAGE_BYTES = T * (DK + DV) * ELT;
   static constexpr int OFF_P = STAGES * STAGE_BYTES;          // float [RMAX][T]
@@ -98,14 +108,46 @@ struct SimtCfg {
   static constexpr int SMEM = OFF_MISC + 16 + 128;
   static_assert(CHK <= 32 && 32 % CHK == 0 && CHV <= 32 && 32 % CHV == 0,
                 "rows must split evenly over lanes");
-  static_assert(T % (4 * PPW) == 0 && T % 32 == 0, "tile shape");
+  static_assert(T % 32 == 0, "tile shape");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(RMAX <= CHK, "a row's lanes hold at least one head each after the reduction");
   static_assert(K_BYTES % 16 == 0, "16-byte aligned V tile");
 };
 
-constexpr int kThreads = 160;  // warp 0 copies, warps 1-4 compute
+
+// Sum each of R values across the CHK lanes that share a row (lanes l with
+// the same l / CHK; R <= CHK, both powers of two).  Each round trades half
+// of the values still held with the partner lane l ^ O and adds, so lane l
+// ends with the row total of value (l % CHK) / (CHK / R) in v[0] (the CHK /
+// R lanes that hold it agree); R - 1 + log2(CHK / R) shuffles in all.
+template <int CHK, int R>
+struct RowReduce {
+  template <int O, int NV>
+  __device__ static void step(float (&v)[R], int lane) {
+    if constexpr (O >= 1) {
+      if constexpr (NV > 1) {
+        const bool up = (lane & O) != 0;
+#pragma unroll
+        for (int k = 0; k < NV / 2; ++k) {
+          const float send = up ? v[k] : v[k + NV / 2];
+          const float keep = up ? v[k + NV / 2] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+        }
+        step<O / 2, NV / 2>(v, lane);
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+        step<O / 2, 1>(v, lane);
+      }
+    }
+  }
+  __device__ static void run(float (&v)[R], int lane) { step<CHK / 2, R>(v, lane); }
+  // the value lane l holds, and whether it is the first of its copies
+  __device__ static int head(int lane) { return (lane % CHK) / (CHK / R); }
+  __device__ static bool writer(int lane) { return (lane % (CHK / R)) == 0; }
+};
 
 template <typename DT, int DK, int DV, int RMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
     decode_simt_kernel(const DT* __restrict__ q, const DT* __restrict__ kc,
                        const DT* __restrict__ vc, const int* __restrict__ lens, int b, int h,
                        int g, int cap, float scale_log2, DT* __restrict__ out,
@@ -116,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        int nq, const int* __restrict__ table, int bsz, int max_blocks,
                        int num_blocks) {
   using C = SimtCfg<DT, DK, DV, RMAX>;
+  constexpr int kCompute = C::NCT, kWarps = C::NCW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                            ~uintptr_t(127));
@@ -245,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- compute (128 threads) ----------------
+    // ---------------- compute (NCT threads) ----------------
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
     const int sub = lane / C::CHK, ch = lane % C::CHK;  // logits mapping
@@ -311,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : -1;
           };
           if (ok) {
-            for (int idx = ct; idx < nrows * C::CHK; idx += 128) {
+            for (int idx = ct; idx < nrows * C::CHK; idx += kCompute) {
               const int pos = first_new + s_lo + idx / C::CHK, c16 = idx % C::CHK;
               if (pos < lt * C::T || pos >= (lt + 1) * C::T) continue;
               const uint4 kv = idx == ct ? knew : __ldg(k_new + new_chunk(idx, C::CHK));
@@ -319,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const long long crow = cache_row(pos);
               if (crow >= 0) k_cache_w[crow * C::CHK + c16] = kv;
             }
-            for (int idx = ct; idx < nrows * C::CHV; idx += 128) {
+            for (int idx = ct; idx < nrows * C::CHV; idx += kCompute) {
               const int pos = first_new + s_lo + idx / C::CHV, c16 = idx % C::CHV;
               if (pos < lt * C::T || pos >= (lt + 1) * C::T) continue;
               const uint4 vv = idx == ct ? vnew : __ldg(v_new + new_chunk(idx, C::CHV));
@@ -328,12 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (crow >= 0) v_cache_w[crow * C::CHV + c16] = vv;
             }
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(1, kCompute);
         }
-        // A: logits
-#pragma unroll 2
-        for (int step = 0; step < C::T / (4 * C::PPW); ++step) {
-          const int p = step * (4 * C::PPW) + cw * C::PPW + sub;
+        // A: logits (query rows past nr have q = 0 and are not stored)
+        using RR = RowReduce<C::CHK, RMAX>;
+        const int hd = RR::head(lane);
+        const bool wr = RR::writer(lane) && hd < nr;
+#pragma unroll
+        for (int pb = cw * C::PPW; pb < C::T; pb += kWarps * C::PPW) {
+          const int p = pb + sub;
           float kf[C::EPC];
           if (ok && p < valid) {
             const uint4 u = *reinterpret_cast<const uint4*>(sK + p * DK + ch * C::EPC);
@@ -342,61 +388,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < C::EPC; ++e) kf[e] = 0.f;
           }
+          float part[RMAX];
 #pragma unroll
           for (int t = 0; t < RMAX; ++t) {
-            if (t < nr) {
-              float part = 0.f;
+            part[t] = 0.f;
 #pragma unroll
-              for (int e = 0; e < C::EPC; ++e) part = fmaf(qreg[t][e], kf[e], part);
+            for (int e = 0; e < C::EPC; ++e) part[t] = fmaf(qreg[t][e], kf[e], part[t]);
+          }
+          RR::run(part, lane);
+          if (wr && p < valid) sP[hd * C::T + p] = part[0] * scale_log2;
+        }
+        named_bar_sync(1, kCompute);
+        // B: online softmax, one half-warp per query row (two rows a warp,
+        // the 16 lanes of a half taking T / 16 positions each); row t (token
+        // s) sees tile positions p <= lim
+        {
+          const int hw = lane >> 4, hl = lane & 15;
+          for (int tb = 2 * cw; tb < nr; tb += 2 * kWarps) {
+            const int t = tb + hw;
+            const bool row_ok = t < nr;  // (both halves run the shuffles)
+            const int lim = row_ok ? min(valid - 1, first_new + t / r - lt * C::T) : -1;
+            float x[C::T / 16];
+            float mx = -INFINITY;
 #pragma unroll
-              for (int o = C::CHK / 2; o > 0; o >>= 1)
-                part += __shfl_xor_sync(0xffffffffu, part, o);
-              if (ch == 0 && p < valid) sP[t * C::T + p] = part * scale_log2;
+            for (int k = 0; k < C::T / 16; ++k) {
+              const int p = hl + 16 * k;
+              x[k] = (p <= lim) ? sP[t * C::T + p] : -INFINITY;
+              mx = fmaxf(mx, x[k]);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float m_old = row_ok ? sM[t] : -INFINITY;
+            const float m_new = fmaxf(m_old, mx);
+            // a row that has seen no position yet keeps a finite reference
+            const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2(m_old - mref);
+            float sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < C::T / 16; ++k) {
+              const float pv = ex2(x[k] - mref);
+              sum += pv;
+              if (row_ok) sP[t * C::T + hl + 16 * k] = pv;
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            __syncwarp();
+            if (hl == 0 && row_ok) {
+              sM[t] = m_new;
+              sL[t] = sL[t] * alpha + sum;
+              sA[t] = alpha;
             }
           }
         }
-        named_bar_sync(1, 128);
-        // B: online softmax, one warp per query row; row t (token s) sees
-        // tile positions p <= lim
-        for (int t = cw; t < nr; t += 4) {
-          const int lim = min(valid - 1, first_new + t / r - lt * C::T);
-          float x[C::PPL];
-          float mx = -INFINITY;
+        named_bar_sync(1, kCompute);
+        // C: weighted sum of V (the accumulators are rescaled only when
+        // some row's running max moved: the same branch in every thread)
+        {
+          float al[RMAX];
+          bool moved = false;
 #pragma unroll
-          for (int k = 0; k < C::PPL; ++k) {
-            const int p = lane + 32 * k;
-            x[k] = (p <= lim) ? sP[t * C::T + p] : -INFINITY;
-            mx = fmaxf(mx, x[k]);
+          for (int t = 0; t < RMAX; ++t) {
+            al[t] = t < nr ? sA[t] : 1.f;
+            moved |= al[t] != 1.f;
           }
-          mx = warp_max(mx);
-          const float m_old = sM[t];
-          const float m_new = fmaxf(m_old, mx);
-          // a row that has seen no position yet keeps a finite reference
-          const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-          const float alpha = ex2(m_old - mref);
-          float sum = 0.f;
+          if (moved) {
 #pragma unroll
-          for (int k = 0; k < C::PPL; ++k) {
-            const float pv = ex2(x[k] - mref);
-            sum += pv;
-            sP[t * C::T + lane + 32 * k] = pv;
-          }
-          sum = warp_sum(sum);
-          __syncwarp();
-          if (lane == 0) {
-            sM[t] = m_new;
-            sL[t] = sL[t] * alpha + sum;
-            sA[t] = alpha;
-          }
-        }
-        named_bar_sync(1, 128);
-        // C: weighted sum of V
+            for (int t = 0; t < RMAX; ++t)
 #pragma unroll
-        for (int t = 0; t < RMAX; ++t) {
-          if (t < nr) {
-            const float al = sA[t];
-#pragma unroll
-            for (int e = 0; e < C::EPC; ++e) acc[t][e] *= al;
+              for (int e = 0; e < C::EPC; ++e) acc[t][e] *= al[t];
           }
         }
         if (ok) {
@@ -414,25 +473,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kCompute);
         if (ct == 0) mbar_arrive(empty0 + 8 * st);
       }
 
-      // ---- segment end: reduce the position groups, write out ----
+      // ---- segment end: reduce the position groups, write out: each
+      // warp's groups by shuffles, then the warps four at a time into four
+      // slots ----
 #pragma unroll
       for (int t = 0; t < RMAX; ++t) {
-        if (t < nr) {
 #pragma unroll
-          for (int e = 0; e < C::EPC; ++e) {
-            float v = acc[t][e];
+        for (int e = 0; e < C::EPC; ++e) {
+          float v = acc[t][e];
 #pragma unroll
-            for (int o = C::CHV; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane < C::CHV) sRed[(cw * RMAX + t) * DV + chv * C::EPC + e] = v;
-            acc[t][e] = 0.f;
-          }
+          for (int o = C::CHV; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          acc[t][e] = v;
         }
       }
-      named_bar_sync(1, 128);
+      // (warps 4k .. 4k + 3 add into slots 0-3 in pass k)
+#pragma unroll
+      for (int pass = 0; pass * 4 < kWarps; ++pass) {
+        if (cw / 4 == pass && lane < C::CHV) {
+#pragma unroll
+          for (int t = 0; t < RMAX; ++t)
+            if (t < nr)
+#pragma unroll
+              for (int e = 0; e < C::EPC; ++e) {
+                float* dst = sRed + ((cw % 4) * RMAX + t) * DV + chv * C::EPC + e;
+                *dst = pass == 0 ? acc[t][e] : *dst + acc[t][e];
+              }
+        }
+        if (pass * 4 + 4 < kWarps) named_bar_sync(1, kCompute);
+      }
+#pragma unroll
+      for (int t = 0; t < RMAX; ++t)
+#pragma unroll
+        for (int e = 0; e < C::EPC; ++e) acc[t][e] = 0.f;
+      named_bar_sync(1, kCompute);
       const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
       const int u = seg.i * g + seg.j;
       const size_t slot = static_cast<size_t>(u) + blockIdx.x;
@@ -440,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s_ = t / r;
         return obase + s_ * h + (t - s_ * r);
       };
-      for (int idx = ct; idx < nr * DV; idx += 128) {
+      for (int idx = ct; idx < nr * DV; idx += kCompute) {
         const int t = idx / DV, dd = idx % DV;
         const float o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
                         sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
@@ -460,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long c0, c1;
         unit_ctas(seg.u0, seg.u0 + seg.ti, w.W, w.nc, c0, c1);
         const int np = unit_parts(c0, c1, w.W, w.nc);
-        if (counters != nullptr && arrive_last(counters, u, np, last_flag, ct == 0, 1, 128)) {
+        if (counters != nullptr &&
+            arrive_last(counters, u, np, last_flag, ct == 0, 1, kCompute)) {
           // merge the partials in CTA order whichever CTA merges (the same
           // bits every run): this CTA's own (still in shared memory) is used
           // in place only when it is the first piece, else read back
@@ -468,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (w.W < w.nc)
             while (cfirst < c1 && cta_empty(cfirst, w.W, w.nc)) ++cfirst;
           const bool own_first = cfirst == blockIdx.x;
-          for (int idx = ct; idx < nr * DV; idx += 128) {
+          for (int idx = ct; idx < nr * DV; idx += kCompute) {
             const int t = idx / DV, dd = idx % DV;
             float o = 0.f, M = -INFINITY, den = 0.f;
             if (own_first) {
@@ -494,13 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kCompute);
       if (ct < RMAX) {
         sM[ct] = -INFINITY;
         sL[ct] = 0.f;
         sA[ct] = 0.f;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kCompute);
     }
   }
   __syncthreads();
@@ -522,7 +600,7 @@ cudaError_t launch_t(const DecodeLaunch& a) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nc);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
