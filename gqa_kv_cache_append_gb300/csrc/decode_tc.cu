@@ -77,6 +77,27 @@ constexpr int kPrefetchTiles = 3;
 // and the extra requests made every measured shape slower.)
 constexpr int kL2Ahead = 3;
 
+// Sum each of 16 values across the warp: each round trades half of the
+// values still held with the partner lane x ^ o (o = 16, 8, 4, 2) and adds,
+// then lanes x and x ^ 1 add their single values.  Lane x returns the warp
+// total of value (x >> 1) & 15.
+__device__ __forceinline__ float warp_sum16_scatter(const float (&in)[16], int lane) {
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) v[k] = in[k];
+#pragma unroll
+  for (int o = 16, nv = 16; o >= 2; o >>= 1, nv >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < nv / 2; ++k) {
+      const float send = up ? v[k] : v[k + nv / 2];
+      const float keep = up ? v[k + nv / 2] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
 // because the 32-column variant runs at its register limit.
@@ -282,7 +303,12 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     bool waited = !early;
     PageCursor pc;
     while (w.next(seg)) {
-      if (waited) load_q(k, seg);
+      if (waited) {
+        load_q(k, seg);
+      } else if (lane == 0) {  // (as in the contiguous producer below)
+        tma_prefetch_l2_3d(&tm_q, 0, seg.j * r, seg.i * nq);
+        if (kh == 2) tma_prefetch_l2_3d(&tm_q, 64, seg.j * r, seg.i * nq);
+      }
       pc.start(table + static_cast<size_t>(seg.i) * max_blocks, (seg.L + bsz - 1) / bsz,
                (seg.lt0 * TT) / bsz);
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
@@ -386,8 +412,16 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       bool waited = !early;  // has this thread passed the dependency wait?
       while (w.next(seg)) {
         // q comes from the previous kernel: load it only after the wait
-        // (early mode: after the first ring's worth of K/V tiles)
-        if (waited) load_q(k, seg);
+        // (early mode: after the first ring's worth of K/V tiles).  Before
+        // the wait L2 is asked for it, ahead of the K/V copies: that moves
+        // no data into this CTA, and a write by the kernel ahead lands in
+        // L2 all the same, where the load after the wait finds it.
+        if (waited) {
+          load_q(k, seg);
+        } else {
+          tma_prefetch_l2_3d(&tm_q, 0, seg.j * r, seg.i * nq);
+          if (kh == 2) tma_prefetch_l2_3d(&tm_q, 64, seg.j * r, seg.i * nq);
+        }
         const int unit_row = (seg.i * g + seg.j) * cap;
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
           if (!waited && (lt - seg.lt0 == kStages)) {
@@ -940,19 +974,18 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
 
       // ---- segment end: softmax denominators, output or partial ----
       {
-        float mine = 0.f;
-#pragma unroll
-        for (int e = 0; e < HP; ++e) {
-          const float sum = warp_sum(l[e]);
-          if (lane == e) mine = sum;
-        }
+        // the sixteen heads' sums across the warp, by a reduce-scatter of
+        // shuffles (16 shuffles in five rounds rather than sixteen chains of
+        // five dependent ones): lane x ends with head (x >> 1) & 15's
+        static_assert(HP == 16, "sixteen heads per warpgroup");
+        const float mine = warp_sum16_scatter(l, lane);
         // the warp-maxima slot of the segment's last tile is free here (its
         // readers all passed that tile's second barrier); the next tile uses
         // the other slot, and the one after waits at its first barrier
         const uint32_t nlast = n - 1;
         float* lred = red_wg + (nlast & 1) * HP * 4;
         const float* mfin = max_sm + (nlast & 1) * NP + h0;
-        if (lane < HP) lred[wq * HP + lane] = mine;
+        if ((lane & 1) == 0) lred[wq * HP + (lane >> 1)] = mine;
         named_bar_sync(bar_id, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
         // output row of column c: (i * n + s) * h + j * r + t; thread `row`
@@ -961,10 +994,31 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         T16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * dv + row;
         const int u = seg.i * g + seg.j;
         const size_t slot = static_cast<size_t>(u) + blockIdx.x;
-        // l[e] becomes the CTA-wide softmax denominator of head h0 + e
+        // l[e] becomes the CTA-wide softmax denominator of head h0 + e;
+        // the shared values this thread needs are loaded before any store
+        float mf[HP];
+        int co[HP];
 #pragma unroll
-        for (int e = 0; e < HP; ++e)
-          l[e] = lred[e] + lred[HP + e] + lred[2 * HP + e] + lred[3 * HP + e];
+        for (int e4 = 0; e4 < HP; e4 += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(lred + e4);
+          const float4 b2 = *reinterpret_cast<const float4*>(lred + HP + e4);
+          const float4 c2 = *reinterpret_cast<const float4*>(lred + 2 * HP + e4);
+          const float4 d2 = *reinterpret_cast<const float4*>(lred + 3 * HP + e4);
+          l[e4] = a.x + b2.x + c2.x + d2.x;
+          l[e4 + 1] = a.y + b2.y + c2.y + d2.y;
+          l[e4 + 2] = a.z + b2.z + c2.z + d2.z;
+          l[e4 + 3] = a.w + b2.w + c2.w + d2.w;
+          const float4 mv = *reinterpret_cast<const float4*>(mfin + e4);
+          mf[e4] = mv.x;
+          mf[e4 + 1] = mv.y;
+          mf[e4 + 2] = mv.z;
+          mf[e4 + 3] = mv.w;
+          const int4 cv = *reinterpret_cast<const int4*>(col_off + h0 + e4);
+          co[e4] = cv.x;
+          co[e4 + 1] = cv.y;
+          co[e4 + 2] = cv.z;
+          co[e4 + 3] = cv.w;
+        }
         if (cl_merge) {
           // this CTA's partial, for the merge across the cluster
 #pragma unroll
@@ -972,7 +1026,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (h0 + e < nr) {
               if (has_col) cl_o[(h0 + e) * dv + row] = o[e];
               if (row == 0) {
-                cl_ml[2 * (h0 + e)] = l[e] > 0.f ? mfin[e] : -INFINITY;
+                cl_ml[2 * (h0 + e)] = l[e] > 0.f ? mf[e] : -INFINITY;
                 cl_ml[2 * (h0 + e) + 1] = l[e];
               }
             }
@@ -981,7 +1035,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
 #pragma unroll
           for (int e = 0; e < HP; ++e)
             if (h0 + e < nr && has_col)
-              obase[col_off[h0 + e]] = Half16<T16>::from(o[e] / l[e]);
+              obase[co[e]] = Half16<T16>::from(o[e] / l[e]);
         } else {
 #pragma unroll
           for (int e = 0; e < HP; ++e) {
@@ -990,7 +1044,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
               if (has_col) part_o[sl * dv + row] = o[e];
               if (row == 0) {
                 // a token that saw none of this CTA's positions: empty partial
-                part_ml[sl * 2 + 0] = l[e] > 0.f ? mfin[e] : -INFINITY;
+                part_ml[sl * 2 + 0] = l[e] > 0.f ? mf[e] : -INFINITY;
                 part_ml[sl * 2 + 1] = l[e];
               }
             }
@@ -1027,7 +1081,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             float m[HP];
 #pragma unroll
             for (int e = 0; e < HP; ++e) {
-              m[e] = (own_first && l[e] > 0.f) ? mfin[e] : -INFINITY;
+              m[e] = (own_first && l[e] > 0.f) ? mf[e] : -INFINITY;
               if (!own_first) {
                 o[e] = 0.f;
                 l[e] = 0.f;
@@ -1067,7 +1121,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
 #pragma unroll
             for (int e = 0; e < HP; ++e)
               if (h0 + e < nr && has_col)
-                obase[col_off[h0 + e]] = Half16<T16>::from(o[e] / l[e]);
+                obase[co[e]] = Half16<T16>::from(o[e] / l[e]);
           }
         }
         m_own = -INFINITY;

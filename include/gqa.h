@@ -373,11 +373,11 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  * num_sms: SM count of the target device; 0 = that of the current device
  * (which then needs a GPU).  Outputs, each optional (NULL = not wanted):
  *   kernels          kernels one gqa_decode_attn* call launches: 1, or 2 when
- *                    the CUDA-core kernel splits the units over more CTAs
- *                    than 2*b*g and the split partials are merged by the
- *                    separate combine kernel (gqa_decode_step* launch the
- *                    same number; the append is fused).  The tensor-core
- *                    kernel merges such splits itself, in clusters (below).
+ *                    the units are split over more CTAs than 2*b*g and the
+ *                    split partials are merged by the separate combine
+ *                    kernel (gqa_decode_step* launch the same number; the
+ *                    append is fused).  The tensor-core kernel merges such
+ *                    splits itself where a cluster launch (below) is taken.
  *   ctas             CTAs the decode kernel is launched with (persistent: at
  *                    most num_sms).  On the tensor-core kernel over a
  *                    contiguous cache, when all
@@ -391,13 +391,16 @@ int gqa_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_ca
  *   workspace_bytes  split partials + arrival counters the call uses
  *   cluster          CTAs per thread-block cluster of the decode launch, 0
  *                    for a launch without clusters.  The tensor-core kernel
- *                    is launched in clusters when the units would be cut
- *                    into three or more pieces each (more CTAs than 2*b*g):
+ *                    is launched in clusters when the units are cut into
+ *                    exactly two pieces each (ctas = 2*b*g: clusters of
+ *                    two), or would be cut into three or more (more CTAs
+ *                    than 2*b*g) and at most two clusters per unit lose
+ *                    under 2 us of streaming time against the full grid:
  *                    each unit then gets k whole clusters (ctas = b*g*C*k),
  *                    C and k chosen for the most CTAs among the sizes of
  *                    which k clusters per unit fit on the device at once
  *                    (host only, num_sms > 0: as if any cluster size could
- *                    use every SM), and the CTAs of a cluster merge their
+ *                    use every SM).  The CTAs of a cluster merge their
  *                    pieces over distributed shared memory (equal lengths)
  *                    or through the split workspace (ragged lengths).
  * Returns the code the decode call would return for these shapes (its

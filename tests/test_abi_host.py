@@ -242,7 +242,9 @@ def test_decode_plan_query():
     """gqa_decode_plan on the host (SM count given): persistent grid of at
     most one CTA per SM and at most one per tile (with fewer (sequence, KV
     head) units than SMs, a whole number of CTAs per unit).  Where that cuts
-    every unit into three or more pieces (more CTAs than twice the units),
+    every unit into exactly two pieces, the tensor-core kernel is launched in
+    clusters of two.  Where it cuts every unit into three or more pieces
+    (more CTAs than twice the units),
     the CUDA-core kernel adds the combine kernel, and the tensor-core kernel
     is launched in clusters of C CTAs, k per unit (the most CTAs over the
     sizes 2..16, then the fewest clusters per unit; the host-only plan lets
@@ -280,6 +282,9 @@ def test_decode_plan_query():
                                            (1, 1, 32, 1, 128, 128, 131072, "f16"),
                                            (8, 1, 32, 1, 64, 64, 131072, "bf16"),
                                            (16, 1, 32, 1, 64, 64, 2048, "bf16"),
+                                           (16, 1, 32, 4, 128, 128, 4096, "bf16"),
+                                           (38, 1, 8, 2, 128, 128, 1000, "bf16"),
+                                           (38, 1, 8, 2, 128, 128, 1000, "f32"),
                                            (1, 1, 8, 8, 128, 128, 1, "bf16")]:
         p = b.gqa_decode_plan(bb, n, h, g, dk, dv, cap, dt, num_sms=152)
         unit_tiles = -(-cap // p["tile"])
@@ -298,7 +303,10 @@ def test_decode_plan_query():
             k = best[0] // (units * best[1])
             stream = units * unit_tiles * p["tile"] * (dk + dv) * 2 / 7.4e12
             clustered = best[0] > 0 and k <= 2 and stream * (1 - best[0] / aligned) < 2e-6
-        if clustered:
+        if aligned == 2 * units and p["tensor_core"]:
+            assert (p["ctas"], p["cluster"], p["kernels"]) == (aligned, 2, 1)
+            counters = units * 2
+        elif clustered:
             assert p["ctas"] == best[0] and p["cluster"] == best[1] and p["kernels"] == 1
             assert p["ctas"] % (units * p["cluster"]) == 0
             counters = units * p["cluster"]

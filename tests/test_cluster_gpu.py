@@ -1,8 +1,9 @@
 """Split units merged across thread-block clusters (tensor-core kernel).
 
-When a call would cut every (sequence, KV head) unit into three or more
-pieces, the tensor-core kernel is launched in clusters of C CTAs, k clusters
-per unit, and merges the pieces itself: over distributed shared memory when
+When a call cuts every (sequence, KV head) unit into exactly two pieces,
+the tensor-core kernel is launched in clusters of two; when it would cut
+every unit into three or more pieces, in clusters of C CTAs, k clusters per
+unit.  Either way the kernel merges the pieces itself: over distributed shared memory when
 every unit has the same number of tiles (then, with k > 1, the k cluster
 results through the split workspace), through the split workspace when the
 lengths are ragged.  GQA_CLUSTER=0 takes the combine kernel instead; a size
@@ -61,6 +62,26 @@ def test_cluster_merge(cluster_mode, b, h, g, d, cap, lens):
         assert p["cluster"] == 0
     elif cluster_mode != "auto" and p["ctas"] > 2 * b * g:
         assert p["cluster"] == int(cluster_mode) or p["cluster"] == 0
+    run_step(cfg, lens)
+    run_step(cfg, lens, fused=True)
+
+
+@pytest.mark.parametrize("cluster_mode", ["auto", "0"], indirect=True)
+@pytest.mark.parametrize("b,h,g,d,cap,lens", [
+    (16, 32, 4, 128, 4096, [4096] * 16),          # 64 units of 32 tiles: pairs
+    (16, 32, 4, 128, 4096, [4096, 3000, 4096, 17, 2500, 4096, 4096, 1,
+                            4000, 4096, 129, 4096, 128, 4096, 4096, 3333]),  # ragged
+    (38, 8, 2, 128, 1000, [1000] * 38),           # 76 units: every SM of 152
+    (16, 64, 4, 64, 4096, [4096] * 16),           # 64-wide heads: 256-position tiles
+])
+def test_cluster_pairs(cluster_mode, b, h, g, d, cap, lens):
+    cfg = cfg_of("bf16", b, h, g, d, cap, seed=b * 5 + g)
+    p = _plan(b, 1, h, g, d, cap)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if cluster_mode == "auto" and sms // (b * g) == 2:  # two CTAs per unit
+        assert (p["cluster"], p["ctas"], p["kernels"]) == (2, 2 * b * g, 1)
+    if cluster_mode == "0":
+        assert p["cluster"] == 0
     run_step(cfg, lens)
     run_step(cfg, lens, fused=True)
 
