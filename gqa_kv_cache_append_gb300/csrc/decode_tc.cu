@@ -63,7 +63,6 @@ namespace gqa {
 namespace {
 
 constexpr int kT = 128;       // positions per tile (MMA M of the S product)
-constexpr int kD = 128;       // head dim (MMA M of the O product)
 constexpr int kStages = 3;    // K/V ring depth
 constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 // early streaming: tiles past the ring that L2 is asked for before the wait
@@ -98,6 +97,16 @@ __device__ __forceinline__ float warp_sum16_scatter(const float (&in)[16], int l
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+// d_k = d_v = 64 takes tiles of 256 positions
+bool wide_tiles(int d_k, int d_v) { return d_k == 64 && d_v == 64; }
+// head dims above 128 take the DEEP variant: d_k in {128, 192, 256}, d_v in
+// {128, 192, 256}, not both 128
+bool deep_dims(int d_k, int d_v) {
+  const bool k = d_k == 128 || d_k == 192 || d_k == 256;
+  const bool v = d_v == 128 || d_v == 192 || d_v == 256;
+  return k && v && (d_k > 128 || d_v > 128);
+}
+
 // MULTI: n > 1 new tokens per sequence (causal mask, several new rows).
 // The one-token kernel keeps the lighter code (no mask table, one new row)
 // because the 32-column variant runs at its register limit.
@@ -108,12 +117,23 @@ __device__ __forceinline__ float warp_sum16_scatter(const float (&in)[16], int l
 // 128-255), each softmax thread owns two positions, and O runs over 256
 // positions.  P is written over the stage's K rows, which the S products
 // no longer need, so no P buffers are kept.
-template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true, bool WIDE = false>
+// DEEP: head dims above 128 (d_k, d_v up to 256; 16 query rows): a tile's K
+// rows [128 x d_k] and V rows [128 x d_v] are separate chunks of up to four
+// boxes, each in its own ring slot (chunk 2n: K of tile n, chunk 2n + 1: its
+// V; slot = chunk % 3), so a slot is freed by the product that read it; S
+// runs over d_k / 16 steps, and O is two M = 128 products (output columns
+// 0-127 and 128-255) with d_v > 128.
+template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true, bool WIDE = false,
+          bool DEEP = false>
 struct TcCfg {
   static constexpr int THREADS = 96 + 128 * NWG;  // producer, 2 MMA issuers, NWG softmax warpgroups
   static constexpr int TT = WIDE ? 2 * kT : kT;   // positions per tile
-  static constexpr int KV_BYTES = 4 * kBoxBytes;  // K half 0/1, V half 0/1 (WIDE: K rows, V rows)
-  static constexpr int Q_BYTES = NP * 256;         // two [NP x 64] boxes
+  // K half 0/1, V half 0/1 (WIDE: K rows, V rows; DEEP: one slot of the ring
+  // holds a K or a V chunk of up to four boxes)
+  static constexpr int KV_BYTES = 4 * kBoxBytes;
+  static constexpr int QB = DEEP ? 4 : 2;          // [NP x 64] boxes of q
+  static constexpr int Q_BYTES = NP * 128 * QB;
+  static constexpr int OH = DEEP ? 2 : 1;          // O accumulators of 128 output columns
   static constexpr int P_BYTES = WIDE ? 0 : kT * NP * 2;  // [T rows x NP] bf16 (WIDE: in the stage)
   static constexpr int OFF_Q = kStages * KV_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
@@ -134,8 +154,9 @@ struct TcCfg {
   // OFF_MISC: TMEM address, abort flag, two split flags, then (ragged
   // cluster launches) the CTA's split units [2][u, first CTA, last CTA, last]
   static constexpr int SMEM = OFF_MISC + 48;
-  // S0 S1 O0 O1 (WIDE: S0a S0b S1a S1b O0 O1), a power of two
-  static constexpr int NCOLS = WIDE ? (NP == 16 ? 128 : 256) : 4 * NP;
+  // S0 S1 O0 O1 (WIDE: S0a S0b S1a S1b O0 O1; DEEP: S0 S1 O0a O0b O1a O1b),
+  // a power of two
+  static constexpr int NCOLS = WIDE ? (NP == 16 ? 128 : 256) : (DEEP ? 128 : 4 * NP);
   static constexpr int OFF_TO = WIDE ? 4 * NP : 2 * NP;  // first O column in TMEM
   // P rows are NP * 2 bytes: 32 B (NP=16) or 64 B (NP=32) swizzle atoms
   static constexpr uint32_t P_SWZ = (NP == 16) ? SWZ_32B : SWZ_64B;
@@ -148,7 +169,8 @@ struct TcCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NCOLS == 64 || NCOLS == 128 || NCOLS == 256,
                 "TMEM allocation must be a power of two");
-  static_assert(NCOLS >= OFF_TO + 2 * NP, "TMEM columns");
+  static_assert(NCOLS >= OFF_TO + 2 * OH * NP, "TMEM columns");
+  static_assert(!DEEP || (NP == 16 && NWG == 1 && !WIDE), "DEEP: 16 query rows, 128 positions");
   static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
 };
 
@@ -167,7 +189,7 @@ enum {
   B_DRAIN = B_O_FREE + 2,
 };
 
-template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE, bool DEEP>
 // (register cap: 11 warps put 3 on a sub-partition, 3 x 32 x 168 of its
 // 16384 registers; 7 warps put 2, so 200 fit)
 __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
@@ -182,7 +204,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                      unsigned int* status, long long budget, int early, int nq,
                      const int* __restrict__ table, int bsz, int max_blocks, int num_blocks,
                      int kh, int vh, int cl_size, int cl_k) {
-  using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16, WIDE>;
+  using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16, WIDE, DEEP>;
+  static_assert(!(DEEP && PAGED), "DEEP: contiguous caches");
   constexpr int TT = C::TT;  // positions per tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -206,10 +229,10 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = h / g;
   const int nr = nq * r;  // query rows (columns) per KV head
-  // head dims d_k = 64 * kh and d_v = 64 * vh (kh, vh = 1 or 2): one or two
-  // 64-column boxes of K (and q) and of V; a new row is 2^sh chunks of 16
-  // bytes (sh = 3 or 4)
-  const int shk = kh + 2, shv = vh + 2;
+  // head dims d_k = 64 * kh and d_v = 64 * vh: kh / vh 64-column boxes of K
+  // (and q) and of V (1 or 2; DEEP: 2 to 4); a new row is cpk / cpv chunks
+  // of 16 bytes
+  const int cpk = kh * 8, cpv = vh * 8;
   const int dv = vh * 64;
   // column c = s * r + t is head t of new token s; padded columns never see
   // a position
@@ -258,7 +281,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   // on a paged cache, whose per-block copies need every SM: see
   // Walker::init)
   w.init(lens, b, g, nq, cap, TT, blockIdx.x, gridDim.x,
-         PAGED ? 0 : ((WIDE || (kh == 2 && vh == 2)) ? 2 : 1));
+         PAGED ? 0 : ((WIDE || DEEP || (kh == 2 && vh == 2)) ? 2 : 1));
   Segment seg;
   // Cluster merge: the launch is a cluster launch of cl_size CTAs, cl_k
   // clusters per unit (grid = units * cl_size * cl_k), and every unit has
@@ -293,10 +316,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       if (ok && lane == 0) {
         const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
         mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 128 * kh);
-        tma_load_3d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, sg.j * r, sg.i * nq, pol_keep);
-        if (kh == 2)
-          tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
-                      pol_keep);
+        for (int qb = 0; qb < kh; ++qb)
+          tma_load_3d(qdst + qb * NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64 * qb, sg.j * r,
+                      sg.i * nq, pol_keep);
       }
       if (ok) last_q[qs] = static_cast<int>(kk);
     };
@@ -306,8 +328,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       if (waited) {
         load_q(k, seg);
       } else if (lane == 0) {  // (as in the contiguous producer below)
-        tma_prefetch_l2_3d(&tm_q, 0, seg.j * r, seg.i * nq);
-        if (kh == 2) tma_prefetch_l2_3d(&tm_q, 64, seg.j * r, seg.i * nq);
+        for (int qb = 0; qb < kh; ++qb) tma_prefetch_l2_3d(&tm_q, 64 * qb, seg.j * r, seg.i * nq);
       }
       pc.start(table + static_cast<size_t>(seg.i) * max_blocks, (seg.L + bsz - 1) / bsz,
                (seg.lt0 * TT) / bsz);
@@ -402,10 +423,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           const uint32_t qdst = s_base + C::OFF_Q + qs * C::Q_BYTES;
           // box [n tokens][r heads][64]: rows s * r + t of the operand
           mbar_arrive_expect_tx(BAR(B_Q_FULL + qs), nr * 128 * kh);
-          tma_load_3d(qdst, &tm_q, BAR(B_Q_FULL + qs), 0, sg.j * r, sg.i * nq, pol_keep);
-          if (kh == 2)
-            tma_load_3d(qdst + NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64, sg.j * r, sg.i * nq,
-                        pol_keep);
+          for (int qb = 0; qb < kh; ++qb)
+            tma_load_3d(qdst + qb * NP * 128, &tm_q, BAR(B_Q_FULL + qs), 64 * qb, sg.j * r,
+                        sg.i * nq, pol_keep);
           last_q[qs] = static_cast<int>(kk);
         }
       };
@@ -419,8 +439,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         if (waited) {
           load_q(k, seg);
         } else {
-          tma_prefetch_l2_3d(&tm_q, 0, seg.j * r, seg.i * nq);
-          if (kh == 2) tma_prefetch_l2_3d(&tm_q, 64, seg.j * r, seg.i * nq);
+          for (int qb = 0; qb < kh; ++qb)
+            tma_prefetch_l2_3d(&tm_q, 64 * qb, seg.j * r, seg.i * nq);
         }
         const int unit_row = (seg.i * g + seg.j) * cap;
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
@@ -429,16 +449,45 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             // busy until the kernel ahead completes
             for (int lp = lt; lp < seg.lt1 && lp < lt + (counters ? kPrefetchTiles : 0); ++lp) {
               const int rp = unit_row + lp * TT;
-              tma_prefetch_l2_2d(&tm_k, 0, rp);
-              if (kh == 2) tma_prefetch_l2_2d(&tm_k, 64, rp);
+              for (int bx = 0; bx < kh; ++bx) tma_prefetch_l2_2d(&tm_k, 64 * bx, rp);
               if (WIDE) tma_prefetch_l2_2d(&tm_k, 0, rp + kT);
-              tma_prefetch_l2_2d(&tm_v, 0, rp);
-              if (vh == 2) tma_prefetch_l2_2d(&tm_v, 64, rp);
+              for (int bx = 0; bx < vh; ++bx) tma_prefetch_l2_2d(&tm_v, 64 * bx, rp);
               if (WIDE) tma_prefetch_l2_2d(&tm_v, 0, rp + kT);
             }
             pdl_wait_then_release();
             waited = true;
             load_q(k, seg);
+          }
+          if constexpr (DEEP) {
+            // K chunk 2n, then V chunk 2n + 1, each into the slot its chunk
+            // number gives.  Chunk 3 (tile 1's V) needs slot 0 back, i.e.
+            // tile 0's S product, i.e. q: early streaming stops after tile
+            // 1's K.
+            const int row = unit_row + lt * TT;
+            const uint32_t ck = 2 * n, cv = 2 * n + 1;
+            const int sk = ck % kStages, sv = cv % kStages;
+            if (!mbar_wait(BAR(B_EMPTY + sk), ((ck / kStages) & 1) ^ 1, abort_flag, status,
+                           budget))
+              continue;
+            mbar_arrive_expect_tx(BAR(B_FULL_K + sk), kh * kBoxBytes);
+            for (int bx = 0; bx < kh; ++bx)
+              tma_load_2d(s_base + sk * C::KV_BYTES + bx * kBoxBytes, &tm_k, BAR(B_FULL_K + sk),
+                          64 * bx, row, pol_stream);
+            last_n[sk] = static_cast<int>(ck);  // (DEEP: chunk numbers)
+            if (!waited && lt - seg.lt0 == 1) {
+              pdl_wait_then_release();
+              waited = true;
+              load_q(k, seg);
+            }
+            if (!mbar_wait(BAR(B_EMPTY + sv), ((cv / kStages) & 1) ^ 1, abort_flag, status,
+                           budget))
+              continue;
+            mbar_arrive_expect_tx(BAR(B_FULL_K + sv), vh * kBoxBytes);
+            for (int bx = 0; bx < vh; ++bx)
+              tma_load_2d(s_base + sv * C::KV_BYTES + bx * kBoxBytes, &tm_v, BAR(B_FULL_K + sv),
+                          64 * bx, row, pol_stream);
+            last_n[sv] = static_cast<int>(cv);
+            continue;
           }
           const int st = n % kStages;
           if (!mbar_wait(BAR(B_EMPTY + st), ((n / kStages) & 1) ^ 1, abort_flag, status,
@@ -487,7 +536,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (idx < 0) continue;
             b0 = BAR(B_FULL_K + s);
             b1 = BAR(B_FULL_V + s);
-            two = true;
+            two = !DEEP;  // (DEEP: one barrier a slot)
             idx /= kStages;
           } else {
             idx = last_q[s - kStages];
@@ -520,18 +569,29 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     constexpr int NH = WIDE ? 2 : 1;  // S products (128-position halves) per tile
     // operand descriptors: a stage, a buffer or a k-step only moves the
     // start-address field (16-byte units, no carry out of it)
+    // (DEEP: tile m's V is chunk 2m + 1, in slot (2m + 1) % 3 from its
+    // first box)
+    auto v_slot = [&](uint32_t m) -> int { return DEEP ? (2 * m + 1) % kStages : m % kStages; };
+    auto v_full = [&](uint32_t m) -> uint32_t {
+      return DEEP ? BAR(B_FULL_K + v_slot(m)) : BAR(B_FULL_V + v_slot(m));
+    };
+    auto v_phase = [&](uint32_t m) -> uint32_t {
+      return DEEP ? ((2 * m + 1) / kStages) & 1 : (m / kStages) & 1;
+    };
+    auto v_base = [&](uint32_t m) -> uint32_t {
+      return s_base + v_slot(m) * C::KV_BYTES + (DEEP ? 0 : 2 * kBoxBytes);
+    };
     auto issue_o = [&](uint32_t m) {
-      const int st = m % kStages;
+      const int st = v_slot(m);
       const uint32_t nb = m & 1;
       bool ok = mbar_wait(BAR(B_P_READY + nb), (m >> 1) & 1, abort_flag, status, budget);
-      ok = ok && mbar_wait(BAR(B_FULL_V + st), (m / kStages) & 1, abort_flag, status, budget);
+      ok = ok && mbar_wait(v_full(m), v_phase(m), abort_flag, status, budget);
       ok = ok && mbar_wait(BAR(B_O_FREE + nb), ((m >> 1) & 1) ^ 1, abort_flag, status, budget);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       if (leader) {
         if (ok) {
-          const uint64_t a0 =
-              smem_desc(s_base + st * C::KV_BYTES + 2 * kBoxBytes, kBoxBytes, 1024, SWZ_128B);
+          const uint64_t a0 = smem_desc(v_base(m), kBoxBytes, 1024, SWZ_128B);
           // (WIDE: P lies over the stage's K rows)
           const uint32_t pbase =
               WIDE ? s_base + st * C::KV_BYTES : s_base + C::OFF_P + nb * C::P_BYTES;
@@ -545,8 +605,16 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             // second box, and the upper M half reads the box after the
             // current one).  B = P^T: N = NP heads contiguous per row, K =
             // 16 position rows (16 * NP * 2 bytes a step).
-            mma_bf16(tO + nb * NP, a0 + kk * (2048 >> 4), b0 + kk * ((16 * NP * 2) >> 4),
+            mma_bf16(tO + nb * C::OH * NP, a0 + kk * (2048 >> 4), b0 + kk * ((16 * NP * 2) >> 4),
                      C::IDESC_O, kk > 0 ? 1u : 0u);
+          }
+          if (DEEP && vh > 2) {
+            // output columns 128-255 from V boxes 2 and 3 (with d_v = 192
+            // box 3 is not loaded: rows 192-255 are never read)
+#pragma unroll
+            for (int kk = 0; kk < TT / 16; ++kk)
+              mma_bf16(tO + (nb * C::OH + 1) * NP, a0 + ((2 * kBoxBytes) >> 4) + kk * (2048 >> 4),
+                       b0 + kk * ((16 * NP * 2) >> 4), C::IDESC_O, kk > 0 ? 1u : 0u);
           }
         }
         mma_commit(BAR(B_O_FULL + nb));
@@ -568,13 +636,12 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           nrows = p_hi - p_lo;
         }
       }
-      const int nchunk_k = nrows << shk, nchunk_v = nrows << shv;
-      // chunk idx of the segment's new rows (2^sh chunks of 16 bytes a row):
-      // token s_lo + (idx >> sh), chunk idx & (2^sh - 1) of its row
-      // [b, n, g, d] of k_new / v_new
-      auto new_off = [&](int idx, int sh) {
-        return (((static_cast<size_t>(seg.i) * nq + s_lo + (idx >> sh)) * g + seg.j) << sh) +
-               (idx & ((1 << sh) - 1));
+      const int nchunk_k = nrows * cpk, nchunk_v = nrows * cpv;
+      // chunk idx of the segment's new rows (cp chunks of 16 bytes a row):
+      // token s_lo + idx / cp, chunk idx % cp of its row [b, n, g, d] of
+      // k_new / v_new
+      auto new_off = [&](int idx, int cp) {
+        return ((static_cast<size_t>(seg.i) * nq + s_lo + idx / cp) * g + seg.j) * cp + idx % cp;
       };
       // paged cache (one token): the physical row of position L_i - 1, or -1
       // for a bad table entry (then nothing is written)
@@ -589,9 +656,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       // (one token: the softmax warps carry and patch the V row)
       constexpr int VCH = MULTI ? C::KCH : 1;
       // put chunk ch (value v) into row `rho` of a staged tile (64-column
-      // boxes, 128-byte swizzle) and into the cache at `pos` (rows of 2^sh
+      // boxes, 128-byte swizzle) and into the cache at `pos` (rows of cp
       // chunks)
-      auto put = [&](uint32_t tile_base, uint4* cache, int ch, int sh, int pos, int rho,
+      auto put = [&](uint32_t tile_base, uint4* cache, int ch, int cp, int pos, int rho,
                      const uint4& v) {
         const uint32_t dst =
             tile_base + (ch >> 3) * kBoxBytes + rho * 128 + (((ch & 7) ^ (rho & 7)) << 4);
@@ -599,35 +666,35 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                      "r"(v.z), "r"(v.w)
                      : "memory");
         if (!PAGED) {
-          cache[((unit * cap + pos) << sh) + ch] = v;
+          cache[(unit * cap + pos) * cp + ch] = v;
         } else if (!MULTI) {
-          if (prow >= 0) cache[(prow << sh) + ch] = v;
+          if (prow >= 0) cache[prow * cp + ch] = v;
         } else {
           // n new rows: each through its own block-table entry
           const int blk = __ldg(table + static_cast<size_t>(seg.i) * max_blocks + pos / bsz);
           if (blk >= 0 && blk < num_blocks)
-            cache[(((static_cast<long long>(blk) * g + seg.j) * bsz + pos % bsz) << sh) + ch] = v;
+            cache[((static_cast<long long>(blk) * g + seg.j) * bsz + pos % bsz) * cp + ch] = v;
           else
             atomicOr(status, GQA_DEV_BAD_BLOCK);
         }
       };
       // patch the new rows that fall in tile lt (K or V part of the stage)
       auto patch = [&](uint32_t tile_base, uint4* cache, const uint4* src, const uint4* regs,
-                       int nregs, int lt, int sh) {
-        const int nchunk = nrows << sh;
+                       int nregs, int lt, int cp) {
+        const int nchunk = nrows * cp;
 #pragma unroll
         for (int c4 = 0; c4 < C::KCH; ++c4) {
           if (c4 >= nregs) break;
           const int idx = lane + 32 * c4;
-          const int pos = first_new + s_lo + (idx >> sh);
+          const int pos = first_new + s_lo + idx / cp;
           if (idx < nchunk && pos >= lt * TT && pos < (lt + 1) * TT)
-            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * TT, regs[c4]);
+            put(tile_base, cache, idx % cp, cp, pos, pos - lt * TT, regs[c4]);
         }
         for (int idx = lane + 32 * nregs; idx < nchunk; idx += 32) {
-          const int pos = first_new + s_lo + (idx >> sh);
+          const int pos = first_new + s_lo + idx / cp;
           if (pos >= lt * TT && pos < (lt + 1) * TT)
-            put(tile_base, cache, idx & ((1 << sh) - 1), sh, pos, pos - lt * TT,
-                __ldg(src + new_off(idx, sh)));
+            put(tile_base, cache, idx % cp, cp, pos, pos - lt * TT,
+                __ldg(src + new_off(idx, cp)));
         }
         fence_proxy_async_smem();
       };
@@ -638,19 +705,16 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         for (int c4 = 0; c4 < VCH; ++c4) {
           const int idx = lane + 32 * c4;
           vnew[c4] = make_uint4(0u, 0u, 0u, 0u);
-          if (MULTI && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, shv));
+          if (MULTI && idx < nchunk_v) vnew[c4] = __ldg(v_new + new_off(idx, cpv));
         }
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
           const bool new_rows = nrows > 0 && (lt + 1) * TT > first_new;
           if (MULTI && new_rows) {
             // the tile's new V rows, before its O product (the softmax
             // warps zero the rows past L_i, which are other rows)
-            const int st = n % kStages;
             const bool vok = __all_sync(
-                0xffffffffu,
-                mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget));
-            if (vok) patch(s_base + st * C::KV_BYTES + 2 * kBoxBytes, v_cache_w, v_new, vnew,
-                           VCH, lt, shv);
+                0xffffffffu, mbar_wait(v_full(n), v_phase(n), abort_flag, status, budget));
+            if (vok) patch(v_base(n), v_cache_w, v_new, vnew, VCH, lt, cpv);
             __syncwarp();
           }
           issue_o(n);
@@ -663,15 +727,16 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       for (int c4 = 0; c4 < C::KCH; ++c4) {
         const int idx = lane + 32 * c4;
         knew[c4] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, shk));
+        if (idx < nchunk_k) knew[c4] = __ldg(k_new + new_off(idx, cpk));
       }
       const bool qok = __all_sync(
           0xffffffffu, mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget));
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
-        const int st = n % kStages;
+        // (DEEP: tile n's K is chunk 2n)
+        const int st = DEEP ? (2 * n) % kStages : n % kStages;
+        const uint32_t kph = DEEP ? ((2 * n) / kStages) & 1 : (n / kStages) & 1;
         const uint32_t nb = n & 1;
-        bool ok = qok && mbar_wait(BAR(B_FULL_K + st), (n / kStages) & 1, abort_flag, status,
-                                   budget);
+        bool ok = qok && mbar_wait(BAR(B_FULL_K + st), kph, abort_flag, status, budget);
         ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
         ok = __all_sync(0xffffffffu, ok);
         const uint32_t kbase = s_base + st * C::KV_BYTES;
@@ -679,7 +744,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         if (new_rows) {
           // rows L_i - n .. L_i - 1 of this tile are the new tokens: use
           // k_new there, and store them into the cache (the append)
-          if (ok) patch(kbase, k_cache_w, k_new, knew, C::KCH, lt, shk);
+          if (ok) patch(kbase, k_cache_w, k_new, knew, C::KCH, lt, cpk);
           __syncwarp();
         }
         tc_fence_after();
@@ -693,11 +758,11 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
               const uint64_t a0 =
                   smem_desc(s_base + st * C::KV_BYTES + hf * kBoxBytes, 16, 1024, SWZ_128B);
 #pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk) {
+              for (int kk = 0; kk < (DEEP ? 16 : 8); ++kk) {
                 // A = K tile, K-major: 128 rows, 16 head-dim columns (32
-                // bytes) per step; steps 0-3 in the first 64-column box, 4-7
-                // in the second (d_k = 128 only).  B = the q block, the same
-                // way ([NP x 64] boxes).
+                // bytes) per step; steps 4b .. 4b + 3 in 64-column box b
+                // (b < kh).  B = the q block, the same way ([NP x 64]
+                // boxes).
                 if (kk >= 4 * kh) break;
                 mma_bf16(tS + (nb * NH + hf) * NP,
                          a0 + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
@@ -707,6 +772,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             }
           }
           mma_commit(BAR(B_S_FULL + nb));
+          if (DEEP) mma_commit(BAR(B_EMPTY + st));  // the K chunk's slot
           if (lt == seg.lt1 - 1) mma_commit(BAR(B_Q_EMPTY + qs));
         }
         __syncwarp();
@@ -745,37 +811,39 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     // for head h0 + e.  The running max of a head is uniform across the CTA:
     // thread e of the warpgroup keeps head h0 + e's (m_own) and publishes it
     // with its rescale factor through max_sm / alpha_sm each tile.
-    float l[HP], o[HP];
+    // (DEEP: o[1] holds output column row + 128, for d_v > 128)
+    constexpr int OH = C::OH;
+    float l[HP], o[OH][HP];
     float m_own = -INFINITY;
 #pragma unroll
     for (int e = 0; e < HP; ++e) {
       l[e] = 0.f;
-      o[e] = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < OH; ++hf) o[hf][e] = 0.f;
     }
 
     // fold O of tile mt into the registers: o = o * alpha + O_tile
     auto correct = [&](uint32_t mt, const float* al) {
       const uint32_t nb = mt & 1;
       const bool ok = mbar_wait(BAR(B_O_FULL + nb), (mt >> 1) & 1, abort_flag, status, budget);
-      float ov[HP];
-      if (ok) {
+      float ov[OH][HP];
 #pragma unroll
-        for (int c = 0; c < HP; c += 16) {
-          float tmp[16];
-          tmem_ld16(tO + nb * NP + c, tmp);
+      for (int hf = 0; hf < OH; ++hf) {
+        if (ok && (hf == 0 || vh > 2)) {
+          tmem_ld16(tO + (nb * OH + hf) * NP, ov[hf]);
+        } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ov[c + e] = tmp[e];
+          for (int e = 0; e < HP; ++e) ov[hf][e] = 0.f;
         }
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < HP; ++e) ov[e] = 0.f;
       }
+      if (ok) tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_O_FREE + nb));
 #pragma unroll
-      for (int e = 0; e < HP; ++e) o[e] = fmaf(o[e], al[h0 + e], ov[e]);
+      for (int hf = 0; hf < OH; ++hf)
+#pragma unroll
+        for (int e = 0; e < HP; ++e) o[hf][e] = fmaf(o[hf][e], al[h0 + e], ov[hf][e]);
     };
 
     uint32_t n = 0;
@@ -790,11 +858,11 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       // one token: threads 0 .. d_v/8 - 1 of warpgroup 0 carry the new V
       // row (one 16-byte chunk each) to the unit's last tile
       const bool append_v = !MULTI && v_new != nullptr && seg.lt1 == seg.ti;
-      const int vch = 1 << shv;
+      const int vch = cpv;
       uint4 vnew = make_uint4(0u, 0u, 0u, 0u);
       long long vrow_w = -1;  // cache row written by the append
       if (append_v && wg == 0 && row < vch) {
-        vnew = __ldg(v_new + ((static_cast<size_t>(seg.i) * g + seg.j) << shv) + row);
+        vnew = __ldg(v_new + (static_cast<size_t>(seg.i) * g + seg.j) * cpv + row);
         if (!PAGED) {
           vrow_w = (static_cast<long long>(seg.i) * g + seg.j) * cap + seg.L - 1;
         } else {
@@ -934,9 +1002,12 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         // tokens: the O-issuing warp patches the new rows) ----
         const bool patch_v = append_v && lt == seg.ti - 1;
         if (wg == 0 && (valid < TT || patch_v)) {
-          const bool vok =
-              mbar_wait(BAR(B_FULL_V + st), (n / kStages) & 1, abort_flag, status, budget);
-          const uint32_t vbase = s_base + st * C::KV_BYTES + 2 * kBoxBytes;
+          // (DEEP: the V chunk 2n + 1 has a slot of its own)
+          const int vst = DEEP ? (2 * n + 1) % kStages : st;
+          const bool vok = mbar_wait(DEEP ? BAR(B_FULL_K + vst) : BAR(B_FULL_V + st),
+                                     DEEP ? ((2 * n + 1) / kStages) & 1 : (n / kStages) & 1,
+                                     abort_flag, status, budget);
+          const uint32_t vbase = s_base + vst * C::KV_BYTES + (DEEP ? 0 : 2 * kBoxBytes);
           if (vok && patch_v && row < vch) {
             // (WIDE: rows 0-255 run on through the second box)
             const int rho = valid - 1;
@@ -945,7 +1016,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(vnew.x),
                          "r"(vnew.y), "r"(vnew.z), "r"(vnew.w)
                          : "memory");
-            if (vrow_w >= 0) v_cache_w[(vrow_w << shv) + row] = vnew;
+            if (vrow_w >= 0) v_cache_w[vrow_w * cpv + row] = vnew;
           }
 #pragma unroll
           for (int hf = 0; hf < NH; ++hf) {
@@ -953,7 +1024,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (vok && pos >= valid) {
               const uint32_t vrow = vbase + pos * 128;
 #pragma unroll
-              for (int hb = 0; hb < (WIDE ? 1 : 2); ++hb)
+              for (int hb = 0; hb < (WIDE ? 1 : (DEEP ? 4 : 2)); ++hb)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
@@ -989,15 +1060,12 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         named_bar_sync(bar_id, 128);
         const bool whole = (seg.lt0 == 0 && seg.lt1 == seg.ti);
         // output row of column c: (i * n + s) * h + j * r + t; thread `row`
-        // holds output column `row` (none past d_v)
-        const bool has_col = row < dv;
+        // holds output column `row` (none past d_v; DEEP: also row + 128)
+        auto has_col = [&](int hf) { return row + 128 * hf < dv; };
         T16* obase = out + (static_cast<size_t>(seg.i) * nq * h + seg.j * r) * dv + row;
         const int u = seg.i * g + seg.j;
         const size_t slot = static_cast<size_t>(u) + blockIdx.x;
-        // l[e] becomes the CTA-wide softmax denominator of head h0 + e;
-        // the shared values this thread needs are loaded before any store
-        float mf[HP];
-        int co[HP];
+        // l[e] becomes the CTA-wide softmax denominator of head h0 + e
 #pragma unroll
         for (int e4 = 0; e4 < HP; e4 += 4) {
           const float4 a = *reinterpret_cast<const float4*>(lred + e4);
@@ -1008,44 +1076,61 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           l[e4 + 1] = a.y + b2.y + c2.y + d2.y;
           l[e4 + 2] = a.z + b2.z + c2.z + d2.z;
           l[e4 + 3] = a.w + b2.w + c2.w + d2.w;
-          const float4 mv = *reinterpret_cast<const float4*>(mfin + e4);
-          mf[e4] = mv.x;
-          mf[e4 + 1] = mv.y;
-          mf[e4 + 2] = mv.z;
-          mf[e4 + 3] = mv.w;
-          const int4 cv = *reinterpret_cast<const int4*>(col_off + h0 + e4);
-          co[e4] = cv.x;
-          co[e4 + 1] = cv.y;
-          co[e4 + 2] = cv.z;
-          co[e4 + 3] = cv.w;
         }
+        // the final maxima and output row offsets of four heads at a time
+        // (shared memory, loaded ahead of the stores that use them)
+        auto mf4 = [&](int e4) { return *reinterpret_cast<const float4*>(mfin + e4); };
+        auto co4 = [&](int e4) { return *reinterpret_cast<const int4*>(col_off + h0 + e4); };
+        auto pick = [](const float4& v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; };
+        auto pick_i = [](const int4& v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; };
         if (cl_merge) {
           // this CTA's partial, for the merge across the cluster
 #pragma unroll
-          for (int e = 0; e < HP; ++e) {
-            if (h0 + e < nr) {
-              if (has_col) cl_o[(h0 + e) * dv + row] = o[e];
-              if (row == 0) {
-                cl_ml[2 * (h0 + e)] = l[e] > 0.f ? mf[e] : -INFINITY;
-                cl_ml[2 * (h0 + e) + 1] = l[e];
+          for (int e4 = 0; e4 < HP; e4 += 4) {
+            const float4 mv = mf4(e4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int e = e4 + k;
+              if (h0 + e < nr) {
+#pragma unroll
+                for (int hf = 0; hf < OH; ++hf)
+                  if (has_col(hf)) cl_o[(h0 + e) * dv + row + 128 * hf] = o[hf][e];
+                if (row == 0) {
+                  cl_ml[2 * (h0 + e)] = l[e] > 0.f ? pick(mv, k) : -INFINITY;
+                  cl_ml[2 * (h0 + e) + 1] = l[e];
+                }
               }
             }
           }
         } else if (whole) {
 #pragma unroll
-          for (int e = 0; e < HP; ++e)
-            if (h0 + e < nr && has_col)
-              obase[co[e]] = Half16<T16>::from(o[e] / l[e]);
+          for (int e4 = 0; e4 < HP; e4 += 4) {
+            const int4 cv = co4(e4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int hf = 0; hf < OH; ++hf)
+                if (h0 + e4 + k < nr && has_col(hf))
+                  obase[pick_i(cv, k) + 128 * hf] =
+                      Half16<T16>::from(o[hf][e4 + k] / l[e4 + k]);
+          }
         } else {
 #pragma unroll
-          for (int e = 0; e < HP; ++e) {
-            if (h0 + e < nr) {
-              const size_t sl = slot * nr + h0 + e;
-              if (has_col) part_o[sl * dv + row] = o[e];
-              if (row == 0) {
-                // a token that saw none of this CTA's positions: empty partial
-                part_ml[sl * 2 + 0] = l[e] > 0.f ? mf[e] : -INFINITY;
-                part_ml[sl * 2 + 1] = l[e];
+          for (int e4 = 0; e4 < HP; e4 += 4) {
+            const float4 mv = mf4(e4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int e = e4 + k;
+              if (h0 + e < nr) {
+                const size_t sl = slot * nr + h0 + e;
+#pragma unroll
+                for (int hf = 0; hf < OH; ++hf)
+                  if (has_col(hf)) part_o[sl * dv + row + 128 * hf] = o[hf][e];
+                if (row == 0) {
+                  // a token that saw none of this CTA's positions: empty partial
+                  part_ml[sl * 2 + 0] = l[e] > 0.f ? pick(mv, k) : -INFINITY;
+                  part_ml[sl * 2 + 1] = l[e];
+                }
               }
             }
           }
@@ -1081,9 +1166,10 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             float m[HP];
 #pragma unroll
             for (int e = 0; e < HP; ++e) {
-              m[e] = (own_first && l[e] > 0.f) ? mf[e] : -INFINITY;
+              m[e] = (own_first && l[e] > 0.f) ? mfin[e] : -INFINITY;
               if (!own_first) {
-                o[e] = 0.f;
+#pragma unroll
+                for (int hf = 0; hf < OH; ++hf) o[hf][e] = 0.f;
                 l[e] = 0.f;
               }
             }
@@ -1093,7 +1179,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
               // eight heads at a time: their loads go out together
 #pragma unroll
               for (int e0 = 0; e0 < HP; e0 += 8) {
-                float mc[8], lc[8], oc[8];
+                float mc[8], lc[8], oc[OH][8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                   if (h0 + e0 + k < nr) {
@@ -1101,7 +1187,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                     mc[k] = __ldcg(part_ml + sl * 2);
                     lc[k] = __ldcg(part_ml + sl * 2 + 1);
                     // (threads past d_v read a valid column and drop it)
-                    oc[k] = __ldcg(part_o + sl * dv + (row & (dv - 1)));
+                    oc[0][k] = __ldcg(part_o + sl * dv + min(row, dv - 1));
+                    if (OH == 2)
+                      oc[OH - 1][k] = __ldcg(part_o + sl * dv + min(row + 128, dv - 1));
                   }
                 }
 #pragma unroll
@@ -1111,7 +1199,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                     const float mn = fmaxf(m[e], mc[k]);
                     const float mr = (mn == -INFINITY) ? 0.f : mn;  // both pieces empty
                     const float sa = ex2(m[e] - mr), sb = ex2(mc[k] - mr);
-                    o[e] = o[e] * sa + oc[k] * sb;
+#pragma unroll
+                    for (int hf = 0; hf < OH; ++hf) o[hf][e] = o[hf][e] * sa + oc[hf][k] * sb;
                     l[e] = l[e] * sa + lc[k] * sb;
                     m[e] = mn;
                   }
@@ -1119,16 +1208,24 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
               }
             }
 #pragma unroll
-            for (int e = 0; e < HP; ++e)
-              if (h0 + e < nr && has_col)
-                obase[co[e]] = Half16<T16>::from(o[e] / l[e]);
+            for (int e4 = 0; e4 < HP; e4 += 4) {
+              const int4 cv = co4(e4);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int hf = 0; hf < OH; ++hf)
+                  if (h0 + e4 + k < nr && has_col(hf))
+                    obase[pick_i(cv, k) + 128 * hf] =
+                        Half16<T16>::from(o[hf][e4 + k] / l[e4 + k]);
+            }
           }
         }
         m_own = -INFINITY;
 #pragma unroll
         for (int e = 0; e < HP; ++e) {
           l[e] = 0.f;
-          o[e] = 0.f;
+#pragma unroll
+          for (int hf = 0; hf < OH; ++hf) o[hf][e] = 0.f;
         }
       }
     }
@@ -1137,7 +1234,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
 #pragma unroll
       for (int e = 0; e < HP; ++e) {
         if (h0 + e < nr) {
-          if (row < dv) cl_o[(h0 + e) * dv + row] = 0.f;
+#pragma unroll
+          for (int hf = 0; hf < OH; ++hf)
+            if (row + 128 * hf < dv) cl_o[(h0 + e) * dv + row + 128 * hf] = 0.f;
           if (row == 0) {
             cl_ml[2 * (h0 + e)] = -INFINITY;
             cl_ml[2 * (h0 + e) + 1] = 0.f;
@@ -1401,10 +1500,10 @@ cudaError_t configure_kernel(K kern, int smem, std::atomic<unsigned long long>& 
   return cudaSuccess;
 }
 
-template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE, bool DEEP = false>
 cudaError_t launch_np(const DecodeLaunch& a) {
   constexpr bool kBf16 = Half16<T16>::kBf16;
-  using C = TcCfg<NP, NWG, MULTI, PAGED, kBf16, WIDE>;
+  using C = TcCfg<NP, NWG, MULTI, PAGED, kBf16, WIDE, DEEP>;
   CUtensorMap mq, mk, mv;
   // contiguous caches: [b * g * cap rows x 128]; pools: [num_blocks * g * block_size rows]
   const uint64_t kv_rows = PAGED ? static_cast<uint64_t>(a.num_blocks) * a.g * a.block_size
@@ -1414,7 +1513,7 @@ cudaError_t launch_np(const DecodeLaunch& a) {
       !make_map(&mk, a.k_cache, a.d, kv_rows, box_rows, kBf16) ||
       !make_map(&mv, a.v_cache, a.dv, kv_rows, box_rows, kBf16))
     return cudaErrorInvalidValue;
-  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16, WIDE>;
+  auto kern = decode_tc_kernel<NP, NWG, MULTI, PAGED, T16, WIDE, DEEP>;
   static std::atomic<unsigned long long> configured{0};  // devices done, this variant
   if (cudaError_t e = configure_kernel(kern, C::SMEM, configured)) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1447,6 +1546,9 @@ template <typename T16, bool WIDE>
 cudaError_t launch_type(const DecodeLaunch& a) {
   const int cols = a.nq * (a.h / a.g);
   const bool one = a.nq == 1;
+  if (deep_dims(a.d, a.dv))  // (contiguous caches, 16 query rows at most)
+    return one ? launch_np<16, 1, false, false, T16, false, true>(a)
+               : launch_np<16, 1, true, false, T16, false, true>(a);
   if (a.block_table != nullptr) {
     if (one)
       return cols <= 16 ? launch_np<16, 1, false, true, T16, WIDE>(a)
@@ -1461,14 +1563,12 @@ cudaError_t launch_type(const DecodeLaunch& a) {
                     : launch_np<32, 2, true, false, T16, WIDE>(a);
 }
 
-// d_k = d_v = 64 takes tiles of 256 positions
-bool wide_tiles(int d_k, int d_v) { return d_k == 64 && d_v == 64; }
-
 }  // namespace
 
-bool tc_supported(int dtype, int d_k, int d_v, int cols) {
-  return (dtype == GQA_BF16 || dtype == GQA_F16) && (d_k == 64 || d_k == 128) &&
-         (d_v == 64 || d_v == 128) && cols >= 1 && cols <= 32;
+bool tc_supported(int dtype, int d_k, int d_v, int cols, bool paged) {
+  if (dtype != GQA_BF16 && dtype != GQA_F16) return false;
+  if (deep_dims(d_k, d_v)) return !paged && cols >= 1 && cols <= 16;
+  return (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128) && cols >= 1 && cols <= 32;
 }
 
 int tc_tile(int d_k, int d_v) { return wide_tiles(d_k, d_v) ? 2 * kT : kT; }
@@ -1483,7 +1583,7 @@ int tc_max_clusters(int csize) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (init[dev][csize].load()) return cache[dev][csize].load();
   using C = TcCfg<32, 2, false, false, true, false>;
-  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16, false>;
+  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16, false, false>;
   static std::atomic<unsigned long long> configured{0};
   if (configure_kernel(kern, C::SMEM, configured) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};

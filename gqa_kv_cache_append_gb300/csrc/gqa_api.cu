@@ -168,18 +168,26 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
       const long long sl = (u + c) * nr + t;
       mc[k] = use ? __ldg(part_ml + sl * 2) : -INFINITY;
       lc[k] = use ? __ldg(part_ml + sl * 2 + 1) : 0.f;
-      if constexpr (CPL == 4) {
-        const float4 v = use ? __ldg(reinterpret_cast<const float4*>(part_o + sl * d) + lane)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        oc[k][0] = v.x;
-        oc[k][1] = v.y;
-        oc[k][2] = v.z;
-        oc[k][3] = v.w;
-      } else {
-        const float2 v = use ? __ldg(reinterpret_cast<const float2*>(part_o + sl * d) + lane)
-                             : make_float2(0.f, 0.f);
-        oc[k][0] = v.x;
-        oc[k][1] = v.y;
+      if constexpr (CPL % 4 == 0) {  // CPL / 4 float4 loads a lane
+#pragma unroll
+        for (int q4 = 0; q4 < CPL / 4; ++q4) {
+          const float4 v =
+              use ? __ldg(reinterpret_cast<const float4*>(part_o + sl * d) + lane * (CPL / 4) + q4)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          oc[k][4 * q4] = v.x;
+          oc[k][4 * q4 + 1] = v.y;
+          oc[k][4 * q4 + 2] = v.z;
+          oc[k][4 * q4 + 3] = v.w;
+        }
+      } else {  // CPL / 2 float2 loads
+#pragma unroll
+        for (int q2 = 0; q2 < CPL / 2; ++q2) {
+          const float2 v =
+              use ? __ldg(reinterpret_cast<const float2*>(part_o + sl * d) + lane * (CPL / 2) + q2)
+                  : make_float2(0.f, 0.f);
+          oc[k][2 * q2] = v.x;
+          oc[k][2 * q2 + 1] = v.y;
+        }
       }
     }
     float mb = M;
@@ -368,11 +376,36 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // combine kernel; fewer splits are merged inside the decode kernel.
 bool use_combine_kernel(long long nc, int b, int g) { return nc > 2ll * b * g; }
 
+// The combine kernel for the call's V head dim (d_v / 32 output columns a
+// lane).
+template <typename DT>
+cudaError_t launch_combine(cudaLaunchConfig_t& cfg, const DecodeLaunch& a, int tile,
+                           const float* po, const float* pml) {
+  DT* o = static_cast<DT*>(a.out);
+  switch (a.dv) {
+    case 64:
+      return cudaLaunchKernelEx(&cfg, combine_kernel<DT, 2>, a.seq_lens, a.b, a.h, a.g, a.cap,
+                                tile, a.nc, a.nq, po, pml, o);
+    case 128:
+      return cudaLaunchKernelEx(&cfg, combine_kernel<DT, 4>, a.seq_lens, a.b, a.h, a.g, a.cap,
+                                tile, a.nc, a.nq, po, pml, o);
+    case 192:
+      return cudaLaunchKernelEx(&cfg, combine_kernel<DT, 6>, a.seq_lens, a.b, a.h, a.g, a.cap,
+                                tile, a.nc, a.nq, po, pml, o);
+    case 256:
+      return cudaLaunchKernelEx(&cfg, combine_kernel<DT, 8>, a.seq_lens, a.b, a.h, a.g, a.cap,
+                                tile, a.nc, a.nq, po, pml, o);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
 int launch_all(DecodeLaunch& a, int tile) {
   // (a cluster launch merges its split units itself)
   const bool separate = a.cluster <= 1 && use_combine_kernel(a.nc, a.b, a.g);
   if (separate) a.counters = nullptr;
-  const bool tc = !a.cuda_cores && tc_supported(a.dtype, a.d, a.dv, a.nq * (a.h / a.g));
+  const bool tc = !a.cuda_cores && tc_supported(a.dtype, a.d, a.dv, a.nq * (a.h / a.g),
+                                                a.block_table != nullptr);
   cudaError_t e = tc ? launch_decode_tc(a) : launch_decode_simt(a);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   if (separate) {
@@ -388,25 +421,12 @@ int launch_all(DecodeLaunch& a, int tile) {
     cfg.numAttrs = 1;
     const float* po = static_cast<const float*>(a.part_o);
     const float* pml = static_cast<const float*>(a.part_ml);
-    if (a.dtype == GQA_BF16) {
-      auto* o = static_cast<__nv_bfloat16*>(a.out);
-      e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 4>, a.seq_lens,
-                                           a.b, a.h, a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
-                      : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 2>, a.seq_lens,
-                                           a.b, a.h, a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
-    } else if (a.dtype == GQA_F16) {
-      auto* o = static_cast<__half*>(a.out);
-      e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__half, 4>, a.seq_lens, a.b, a.h,
-                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
-                      : cudaLaunchKernelEx(&cfg, combine_kernel<__half, 2>, a.seq_lens, a.b, a.h,
-                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
-    } else {
-      auto* o = static_cast<float*>(a.out);
-      e = a.dv == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 4>, a.seq_lens, a.b, a.h,
-                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o)
-                      : cudaLaunchKernelEx(&cfg, combine_kernel<float, 2>, a.seq_lens, a.b, a.h,
-                                           a.g, a.cap, tile, a.nc, a.nq, po, pml, o);
-    }
+    if (a.dtype == GQA_BF16)
+      e = launch_combine<__nv_bfloat16>(cfg, a, tile, po, pml);
+    else if (a.dtype == GQA_F16)
+      e = launch_combine<__half>(cfg, a, tile, po, pml);
+    else
+      e = launch_combine<float>(cfg, a, tile, po, pml);
   }
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -589,7 +609,8 @@ struct DecodePlan {
 // The tensor-core kernel wherever it takes the shape, unless the caller asks
 // for the CUDA-core kernel.
 bool use_tensor_cores(const DecodeArgs& x, int cols) {
-  return !(x.flags & GQA_STEP_CUDA_CORES) && tc_supported(x.dtype, x.d_k, x.d_v, cols);
+  return !(x.flags & GQA_STEP_CUDA_CORES) &&
+         tc_supported(x.dtype, x.d_k, x.d_v, cols, x.block_table != nullptr);
 }
 
 int decode_check(const DecodeArgs& x) {

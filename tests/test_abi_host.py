@@ -79,6 +79,9 @@ def _app(lib_, **kw):
     (dict(dk=128, dv=32), -5), (dict(dk=96, dv=96), -5), (dict(h=64, g=1), -5),
     (dict(dk=128, dv=64, h=66, g=2), -5),       # 33 query rows per KV head
     (dict(dtype=0, h=34, g=1), -5), (dict(dtype=0, dk=64, dv=128, h=17, g=1), -5),
+    # head dims above 128: 16-bit data, at most 16 query rows per KV head
+    (dict(dk=256, dv=256, h=34, g=2), -5), (dict(dtype=0, dk=256, dv=256), -5),
+    (dict(dk=192, dv=64), -5), (dict(dk=64, dv=256), -5), (dict(dk=320, dv=128), -5),
 ])
 def test_decode_attn_host_checks(kw, code):
     assert _attn(_lib(), **kw) == code
@@ -227,6 +230,7 @@ def test_paged_host_checks():
     assert call(f, args, i16=4) == -3
     assert call(f, args, i6=0) == -2                  # n < 1
     assert call(f, args, i6=9) == -5                  # 9 tokens x 4 heads > 32 rows
+    assert call(f, args, i9=256, i10=256) == -5       # head dims above 128: contiguous only
     st = b.lib.gqa_decode_step_paged
     sargs = [A, A, A, A, A, A, A, 2, 1, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, 0, None]
     assert call(st, sargs, i1=0) == -1
@@ -261,6 +265,11 @@ def test_decode_plan_query():
     assert b.gqa_decode_plan(32, 1, 64, 8, 64, 64, 8192, "bf16", num_sms=152)["tile"] == 256
     assert b.gqa_decode_plan(32, 1, 64, 8, 64, 64, 8192, "f16", num_sms=152)["tile"] == 256
     assert b.gqa_decode_plan(32, 1, 64, 8, 64, 128, 8192, "bf16", num_sms=152)["tile"] == 128
+    # head dims above 128 (up to 16 query rows): the tensor-core kernel, 128 positions
+    for dk, dv in [(256, 256), (192, 128), (128, 256), (256, 128), (192, 192)]:
+        p2 = b.gqa_decode_plan(32, 1, 64, 8, dk, dv, 8192, "bf16", num_sms=152)
+        assert p2["tensor_core"] and p2["tile"] == 128
+        assert p2["workspace_bytes"] == (32 * 8 + 152) * 8 * (dv + 2) * 4 + 2 * 32 * 8 * 4
     assert p["workspace_bytes"] == (32 * 8 + 152) * 8 * 130 * 4 + 2 * 32 * 8 * 4
     # long-context MQA: 8 units of 1024 tiles; the best cluster plan (two
     # clusters of 9 per unit, 144 CTAs) would give up ~3.8 us of streaming:

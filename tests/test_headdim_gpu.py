@@ -1,6 +1,7 @@
 """Head dims 64 and 128 on the tensor-core kernel, d_k and d_v independently
-(the pages' einsums take separate k and v widths), through the C ABI
-against the float64 oracle on the same 16-bit inputs.
+(the pages' einsums take separate k and v widths), and head dims above 128
+(192 and 256, up to 16 query rows per KV head), through the C ABI against
+the float64 oracle on the same 16-bit inputs.
 
 Cases: bf16 and fp16; (d_k, d_v) = (64, 64), (64, 128), (128, 64); 1, 8,
 16 and 32 query rows per KV head (one and two softmax warpgroups); ragged
@@ -300,3 +301,95 @@ def test_wide_tiles_paged(bs, n):
     assert to_np(kp_d)[0].tobytes() == kp2.tobytes()
     assert to_np(vp_d)[0].tobytes() == vp2.tobytes()
     assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", f"wide paged bs{bs} n{n}")
+
+
+# ---- head dims above 128 (d_k, d_v in {128, 192, 256}, not both 128): the
+# tensor-core kernel's variant with separate K and V chunks in the ring and
+# two O products for d_v > 128; up to 16 query rows per KV head ----
+DEEP_DIMS = [(256, 256), (192, 128), (128, 256), (256, 128), (192, 192)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dk,dv", DEEP_DIMS)
+@pytest.mark.parametrize("b,h,g,cap,lens", [
+    (3, 8, 1, 400, [400, 129, 1]),            # r = 8
+    (4, 16, 16, 256, [1, 127, 128, 256]),     # r = 1 (MHA)
+    (2, 32, 2, 520, [520, 3]),                # r = 16
+    (1, 8, 1, 16384, [99 * 128 + 2]),         # one unit over many CTAs
+    (96, 8, 2, 384, [258] * 96),              # split units merged in the decode kernel
+    (16, 32, 4, 1024, [1024] * 16),           # every unit in two pieces: clusters of two
+])
+def test_tc_deep_head_dims(dtype, dk, dv, b, h, g, cap, lens):
+    from gqa_kv_cache_append_gb300 import binding as B
+    p = B.gqa_decode_plan(b, 1, h, g, dk, dv, cap, dtype)
+    assert p["tensor_core"] and p["tile"] == 128
+    run_one(dtype, b, h, g, dk, dv, cap, lens, seed=dk + 3 * dv + b + h)
+
+
+@pytest.mark.parametrize("dk,dv", DEEP_DIMS)
+def test_tc_deep_head_dims_two_calls(dk, dv):
+    run_one("bf16", 3, 16, 2, dk, dv, 640, [640, 300, 17], fused=False, seed=dk + dv)
+
+
+@pytest.mark.parametrize("dk,dv", [(256, 256), (192, 128)])
+def test_tc_deep_head_dims_nan_padding(dk, dv):
+    """Rows past L_i hold NaN: masked logits and zeroed V rows keep them out
+    (with d_v = 128 the second half of a V slot is never read)."""
+    B = _b()
+    b, h, g, cap, lens = 2, 16, 2, 300, [131, 250]
+    x, _ = _case("bf16", b, 0, h, g, dk, dv, cap, lens, seed=19)
+    for t in (x["k_cache"], x["v_cache"]):
+        for i, L in enumerate(lens):
+            t[i, :, L:] = float("nan")
+    d = {k: v.cuda() for k, v in x.items()}
+    out = torch.empty((b, h, dv), dtype=torch.bfloat16, device="cuda")
+    B.gqa_decode_attn(d["q"], d["k_cache"], d["v_cache"], d["seq_lens"], b, h, g, dk, dv, 0.1,
+                      out)
+    assert B.gqa_device_status() == 0
+    kc, vc = (torch.nan_to_num(x[k], nan=0.0) for k in ("k_cache", "v_cache"))
+    ref = oracle.grouped_decode_attention(_np(x, "q"), to_np(kc)[0], to_np(vc)[0],
+                                          np.asarray(lens), g, 0.1, dtype="bf16")
+    assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", "deep nan padding")
+
+
+@pytest.mark.parametrize("dk,dv", [(256, 256), (192, 128), (128, 256)])
+@pytest.mark.parametrize("n,h,g", [(2, 16, 2), (4, 8, 2), (16, 4, 4)])
+def test_tc_deep_head_dims_multi_token(dk, dv, n, h, g):
+    """n new tokens, n * h / g = 16 (or 4) query rows per KV head, causal
+    mask; new rows straddle a tile edge for one sequence."""
+    B = _b()
+    b, cap = 3, 512
+    lens = [n, 130, 512]
+    x, _ = _case("bf16", b, n, h, g, dk, dv, cap, lens, seed=dk + dv + n)
+    d = {k: v.cuda() for k, v in x.items()}
+    out = torch.full((b, n, h, dv), 3.0, dtype=torch.bfloat16, device="cuda")
+    scale = 1 / math.sqrt(dk)
+    B.gqa_decode_step_multi(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                            d["seq_lens"], b, n, h, g, dk, dv, scale, out)
+    assert B.gqa_device_status() == 0
+    ref, kc, vc = oracle.decode_step_multi(*(_np(x, k) for k in ("q", "k_cache", "v_cache",
+                                                                   "k_new", "v_new")),
+                                           np.asarray(lens), g, scale, dtype="bf16")
+    assert to_np(d["k_cache"])[0].tobytes() == kc.tobytes()
+    assert to_np(d["v_cache"])[0].tobytes() == vc.tobytes()
+    assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", f"deep n={n} dk{dk} dv{dv}")
+
+
+def test_tc_deep_head_dims_deterministic_and_noalloc():
+    """The same bits on every run, and through the allocation-free call."""
+    B = _b()
+    b, h, g, dk, dv, cap, lens = 4, 16, 2, 256, 256, 3000, [3000, 1, 1500, 2999]
+    x, _ = _case("bf16", b, 0, h, g, dk, dv, cap, lens, seed=5)
+    d = {k: v.cuda() for k, v in x.items()}
+    outs = []
+    for call in ("attn", "attn", "noalloc"):
+        out = torch.empty((b, h, dv), dtype=torch.bfloat16, device="cuda")
+        fn = B.gqa_decode_attn if call == "attn" else B.gqa_decode_attn_noalloc
+        fn(d["q"], d["k_cache"], d["v_cache"], d["seq_lens"], b, h, g, dk, dv, 0.1, out)
+        outs.append(out)
+    assert B.gqa_device_status() == 0
+    assert np.array_equal(bits(outs[0]), bits(outs[1]))
+    assert np.array_equal(bits(outs[0]), bits(outs[2]))
+    ref = oracle.grouped_decode_attention(_np(x, "q"), _np(x, "k_cache"), _np(x, "v_cache"),
+                                          np.asarray(lens), g, 0.1, dtype="bf16")
+    assert_close(oracle.widen(to_np(outs[0])[0], "bf16"), ref, "bf16", "deep determinism")
