@@ -122,7 +122,11 @@ bool deep_dims(int d_k, int d_v) {
 // boxes, each in its own ring slot (chunk 2n: K of tile n, chunk 2n + 1: its
 // V; slot = chunk % 3), so a slot is freed by the product that read it; S
 // runs over d_k / 16 steps, and O is two M = 128 products (output columns
-// 0-127 and 128-255) with d_v > 128.
+// 0-127 and 128-255) with d_v > 128.  A slot holds K and V chunks by turns,
+// so it has a full barrier for each (B_FULL_K / B_FULL_V of the slot), each
+// waited on by one consumer, phase c / 6 for chunk c: a barrier shared by
+// the two consumers would let one of them, waiting for the phase after the
+// other's, take the older completed phase of the same parity.
 template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true, bool WIDE = false,
           bool DEEP = false>
 struct TcCfg {
@@ -482,9 +486,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (!mbar_wait(BAR(B_EMPTY + sv), ((cv / kStages) & 1) ^ 1, abort_flag, status,
                            budget))
               continue;
-            mbar_arrive_expect_tx(BAR(B_FULL_K + sv), vh * kBoxBytes);
+            mbar_arrive_expect_tx(BAR(B_FULL_V + sv), vh * kBoxBytes);
             for (int bx = 0; bx < vh; ++bx)
-              tma_load_2d(s_base + sv * C::KV_BYTES + bx * kBoxBytes, &tm_v, BAR(B_FULL_K + sv),
+              tma_load_2d(s_base + sv * C::KV_BYTES + bx * kBoxBytes, &tm_v, BAR(B_FULL_V + sv),
                           64 * bx, row, pol_stream);
             last_n[sv] = static_cast<int>(cv);
             continue;
@@ -536,8 +540,13 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (idx < 0) continue;
             b0 = BAR(B_FULL_K + s);
             b1 = BAR(B_FULL_V + s);
-            two = !DEEP;  // (DEEP: one barrier a slot)
-            idx /= kStages;
+            two = !DEEP;
+            if (DEEP) {  // the slot's last chunk: K (even) or V (odd), phase c / 6
+              if (idx & 1) b0 = BAR(B_FULL_V + s);
+              idx /= 2 * kStages;
+            } else {
+              idx /= kStages;
+            }
           } else {
             idx = last_q[s - kStages];
             if (idx < 0) continue;
@@ -572,11 +581,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     // (DEEP: tile m's V is chunk 2m + 1, in slot (2m + 1) % 3 from its
     // first box)
     auto v_slot = [&](uint32_t m) -> int { return DEEP ? (2 * m + 1) % kStages : m % kStages; };
-    auto v_full = [&](uint32_t m) -> uint32_t {
-      return DEEP ? BAR(B_FULL_K + v_slot(m)) : BAR(B_FULL_V + v_slot(m));
-    };
+    auto v_full = [&](uint32_t m) -> uint32_t { return BAR(B_FULL_V + v_slot(m)); };
     auto v_phase = [&](uint32_t m) -> uint32_t {
-      return DEEP ? ((2 * m + 1) / kStages) & 1 : (m / kStages) & 1;
+      return DEEP ? ((2 * m + 1) / (2 * kStages)) & 1 : (m / kStages) & 1;
     };
     auto v_base = [&](uint32_t m) -> uint32_t {
       return s_base + v_slot(m) * C::KV_BYTES + (DEEP ? 0 : 2 * kBoxBytes);
@@ -734,7 +741,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         // (DEEP: tile n's K is chunk 2n)
         const int st = DEEP ? (2 * n) % kStages : n % kStages;
-        const uint32_t kph = DEEP ? ((2 * n) / kStages) & 1 : (n / kStages) & 1;
+        const uint32_t kph = DEEP ? ((2 * n) / (2 * kStages)) & 1 : (n / kStages) & 1;
         const uint32_t nb = n & 1;
         bool ok = qok && mbar_wait(BAR(B_FULL_K + st), kph, abort_flag, status, budget);
         ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
@@ -1004,8 +1011,8 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         if (wg == 0 && (valid < TT || patch_v)) {
           // (DEEP: the V chunk 2n + 1 has a slot of its own)
           const int vst = DEEP ? (2 * n + 1) % kStages : st;
-          const bool vok = mbar_wait(DEEP ? BAR(B_FULL_K + vst) : BAR(B_FULL_V + st),
-                                     DEEP ? ((2 * n + 1) / kStages) & 1 : (n / kStages) & 1,
+          const bool vok = mbar_wait(BAR(B_FULL_V + vst),
+                                     DEEP ? ((2 * n + 1) / (2 * kStages)) & 1 : (n / kStages) & 1,
                                      abort_flag, status, budget);
           const uint32_t vbase = s_base + vst * C::KV_BYTES + (DEEP ? 0 : 2 * kBoxBytes);
           if (vok && patch_v && row < vch) {

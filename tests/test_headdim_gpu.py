@@ -393,3 +393,30 @@ def test_tc_deep_head_dims_deterministic_and_noalloc():
     ref = oracle.grouped_decode_attention(_np(x, "q"), _np(x, "k_cache"), _np(x, "v_cache"),
                                           np.asarray(lens), g, 0.1, dtype="bf16")
     assert_close(oracle.widen(to_np(outs[0])[0], "bf16"), ref, "bf16", "deep determinism")
+
+
+@pytest.mark.parametrize("dk,dv", [(256, 256), (192, 128), (128, 256), (128, 128), (64, 64)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_tc_long_segments(monkeypatch, dk, dv, flags):
+    """Two CTAs for four units of 32 tiles: every CTA streams whole units,
+    so its ring slots cycle through many fills (with wide heads a slot holds
+    K and V chunks by turns).  flags = 1: the early-streaming step."""
+    monkeypatch.setenv("GQA_CTAS", "2")
+    B = _b()
+    b, h, g, cap = 2, 16, 2, 4096
+    lens = [4096, 4096 - 77]
+    x, _ = _case("bf16", b, 0, h, g, dk, dv, cap, lens, seed=dk * 7 + dv + flags)
+    d = {k: v.cuda() for k, v in x.items()}
+    assert B.gqa_decode_plan(b, 1, h, g, dk, dv, cap, "bf16")["ctas"] == 2
+    out = torch.empty((b, h, dv), dtype=torch.bfloat16, device="cuda")
+    scale = 1 / math.sqrt(dk)
+    B.gqa_decode_step(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                      d["seq_lens"], b, h, g, dk, dv, scale, out,
+                      flags=B.GQA_STEP_EARLY_STREAM if flags else 0)
+    assert B.gqa_device_status() == 0
+    ref, kc, vc = oracle.decode_step(*(_np(x, k) for k in ("q", "k_cache", "v_cache", "k_new",
+                                                             "v_new")),
+                                     np.asarray(lens), g, scale, dtype="bf16")
+    assert to_np(d["k_cache"])[0].tobytes() == kc.tobytes()
+    assert to_np(d["v_cache"])[0].tobytes() == vc.tobytes()
+    assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", f"long segments {dk}/{dv}")
