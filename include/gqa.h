@@ -130,9 +130,11 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache,
  *
  * Rows p >= L_i of the caches are never used in the result, whatever they
  * hold.  fp32 accumulation; bf16 output is rounded to nearest even.
- * Supported: d_k, d_v in {64, 128} (they may differ); bf16 / fp16 with
+ * Supported: d_k, d_v in {64, 128} (they may differ): bf16 / fp16 with
  * h / g <= 32 (tensor-core kernel), fp32 with h / g <= 16 (CUDA-core
- * kernel).  b <= 65535.
+ * kernel); d_k, d_v in {128, 192, 256}, not both 128 (they may differ):
+ * bf16 / fp16 with h / g <= 16 (tensor-core kernel; contiguous caches
+ * only).  b <= 65535.
  * Returns GQA_OK or an error code (nothing is launched on error).
  */
 int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -200,9 +202,10 @@ int gqa_decode_step(const void* q, const void* k_new, const void* v_new, void* k
  *   q   [b, n, h, d_k]   (read)
  *   out [b, n, h, d_v]   (written)
  * The n * r query rows of one KV head share each K/V tile read (one pass
- * over the cache for all n tokens).  Supported: d_k, d_v in {64, 128};
+ * over the cache for all n tokens).  Supported: d_k, d_v in {64, 128}:
  * n * (h / g) <= 32 with bf16 / fp16 (tensor-core kernel), n * (h / g) <= 16
- * with fp32 (CUDA-core kernel); otherwise GQA_ERR_UNSUPPORTED.  Other
+ * with fp32 (CUDA-core kernel); d_k, d_v in {128, 192, 256}, not both 128:
+ * n * (h / g) <= 16 with bf16 / fp16; otherwise GQA_ERR_UNSUPPORTED.  Other
  * limits, errors and the workspace are those of gqa_decode_attn (the
  * partials grow by the factor n).
  *
@@ -243,7 +246,8 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new,
  * access leaves the pools).  block_size: a power of two in [16, 65536]
  * (GQA_ERR_UNSUPPORTED otherwise).  n new tokens per sequence (n = 1: one
  * token; n > 1: the causal n-token step of gqa_decode_*_multi, with q / out
- * [b, n, h, d] and k_new / v_new [b, n, g, d]).  Kernels and limits
+ * [b, n, h, d] and k_new / v_new [b, n, g, d]).  Head dims d_k, d_v in
+ * {64, 128} (larger ones: GQA_ERR_UNSUPPORTED).  Kernels and limits
  * otherwise as for the contiguous calls; with GQA_STEP_EARLY_STREAM the
  * kernels ahead must not write the block table either.
  *
