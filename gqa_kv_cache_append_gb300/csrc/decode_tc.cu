@@ -63,7 +63,7 @@ namespace gqa {
 namespace {
 
 constexpr int kT = 128;       // positions per tile (MMA M of the S product)
-constexpr int kStages = 3;    // K/V ring depth
+constexpr int kStages = 3;    // K/V ring depth (DEEP: ring slots, three or four)
 constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 // early streaming: tiles past the ring that L2 is asked for before the wait
 // (launches whose merge runs in a separate combine kernel skip it: there the
@@ -122,13 +122,16 @@ bool deep_dims(int d_k, int d_v) {
 // boxes, each in its own ring slot (chunk 2n: K of tile n, chunk 2n + 1: its
 // V; slot = chunk % 3), so a slot is freed by the product that read it; S
 // runs over d_k / 16 steps, and O is two M = 128 products (output columns
-// 0-127 and 128-255) with d_v > 128.  A slot holds K and V chunks by turns,
-// so it has a full barrier for each (B_FULL_K / B_FULL_V of the slot), each
-// waited on by one consumer, phase c / 6 for chunk c: a barrier shared by
-// the two consumers would let one of them, waiting for the phase after the
-// other's, take the older completed phase of the same parity.
+// 0-127 and 128-255) with d_v > 128.  In three 64 KiB slots a slot holds K
+// and V chunks by turns, so it has a full barrier for each (B_FULL_K /
+// B_FULL_V of the slot), each waited on by one consumer, phase c / 6 for
+// chunk c: a barrier shared by the two consumers would let one of them,
+// waiting for the phase after the other's, take the older completed phase
+// of the same parity.  When a K chunk is at most three boxes and a V chunk
+// two (d_k = 192, d_v = 128) the ring is four 48 KiB slots instead: K
+// chunks in slots 0 and 2, V chunks in 1 and 3, phase c / 4.
 template <int NP, int NWG, bool MULTI, bool PAGED = false, bool BF16 = true, bool WIDE = false,
-          bool DEEP = false>
+          int DEEP = 0>
 struct TcCfg {
   static constexpr int THREADS = 96 + 128 * NWG;  // producer, 2 MMA issuers, NWG softmax warpgroups
   static constexpr int TT = WIDE ? 2 * kT : kT;   // positions per tile
@@ -137,7 +140,8 @@ struct TcCfg {
   static constexpr int KV_BYTES = 4 * kBoxBytes;
   static constexpr int QB = DEEP ? 4 : 2;          // [NP x 64] boxes of q
   static constexpr int Q_BYTES = NP * 128 * QB;
-  static constexpr int OH = DEEP ? 2 : 1;          // O accumulators of 128 output columns
+  // O accumulators of 128 output columns (the four-slot ring has d_v <= 128)
+  static constexpr int OH = DEEP == 3 ? 2 : 1;
   static constexpr int P_BYTES = WIDE ? 0 : kT * NP * 2;  // [T rows x NP] bf16 (WIDE: in the stage)
   static constexpr int OFF_Q = kStages * KV_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
@@ -150,7 +154,8 @@ struct TcCfg {
   static constexpr int OFF_ALPHA = OFF_MAX + 2 * NP * 4;     // float [2][NP] rescale factors
   static constexpr int OFF_COL = OFF_ALPHA + 2 * NP * 4;     // int [NP] token, int [NP] out row
   static constexpr int OFF_BAR = OFF_COL + 2 * NP * 4;
-  static constexpr int NBAR = 3 * kStages + 2 * 7 + 1;
+  static constexpr int RS = DEEP == 4 ? 4 : kStages;  // ring slots
+  static constexpr int NBAR = 3 * RS + 2 * 7 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // The dynamic shared-memory base is 1024-byte aligned (the swizzled
   // layouts need it; the kernel checks), so no slack is requested: leaving
@@ -178,22 +183,17 @@ struct TcCfg {
   static_assert(NP % NWG == 0 && (NP / NWG) % 16 == 0, "16 heads or more per warpgroup");
 };
 
-// barrier slots
-enum {
-  B_FULL_K = 0,
-  B_FULL_V = kStages,
-  B_EMPTY = 2 * kStages,
-  B_Q_FULL = 3 * kStages,
-  B_Q_EMPTY = B_Q_FULL + 2,
-  B_S_FULL = B_Q_EMPTY + 2,
-  B_S_FREE = B_S_FULL + 2,
-  B_P_READY = B_S_FREE + 2,
-  B_O_FULL = B_P_READY + 2,
-  B_O_FREE = B_O_FULL + 2,
-  B_DRAIN = B_O_FREE + 2,
+// barrier slots, for a ring of RS slots: full (K and V kinds) and empty per
+// slot, then the q, S, P and O double buffers and the drain barrier
+template <int RS>
+struct Bars {
+  static constexpr int FULL_K = 0, FULL_V = RS, EMPTY = 2 * RS, Q_FULL = 3 * RS,
+                       Q_EMPTY = Q_FULL + 2, S_FULL = Q_EMPTY + 2, S_FREE = S_FULL + 2,
+                       P_READY = S_FREE + 2, O_FULL = P_READY + 2, O_FREE = O_FULL + 2,
+                       DRAIN = O_FREE + 2;
 };
 
-template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE, bool DEEP>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE, int DEEP>
 // (register cap: 11 warps put 3 on a sub-partition, 3 x 32 x 168 of its
 // 16384 registers; 7 warps put 2, so 200 fit)
 __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
@@ -210,6 +210,11 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                      int kh, int vh, int cl_size, int cl_k) {
   using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16, WIDE, DEEP>;
   static_assert(!(DEEP && PAGED), "DEEP: contiguous caches");
+  using Bs = Bars<C::RS>;
+  constexpr int B_FULL_K = Bs::FULL_K, B_FULL_V = Bs::FULL_V, B_EMPTY = Bs::EMPTY,
+                B_Q_FULL = Bs::Q_FULL, B_Q_EMPTY = Bs::Q_EMPTY, B_S_FULL = Bs::S_FULL,
+                B_S_FREE = Bs::S_FREE, B_P_READY = Bs::P_READY, B_O_FULL = Bs::O_FULL,
+                B_O_FREE = Bs::O_FREE, B_DRAIN = Bs::DRAIN;
   constexpr int TT = C::TT;  // positions per tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -237,6 +242,11 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
   // (and q) and of V (1 or 2; DEEP: 2 to 4); a new row is cpk / cpv chunks
   // of 16 bytes
   const int cpk = kh * 8, cpv = vh * 8;
+  // DEEP ring: ns slots of sb bytes, chunk c in slot c % ns, its full
+  // barrier's phase c / pd (pd = lcm(ns, 2))
+  constexpr int ns = C::RS;
+  constexpr uint32_t sb = DEEP == 4 ? 3u * kBoxBytes : static_cast<uint32_t>(C::KV_BYTES);
+  constexpr uint32_t pd = (ns % 2 == 0) ? ns : 2 * ns;
   const int dv = vh * 64;
   // column c = s * r + t is head t of new token s; padded columns never see
   // a position
@@ -419,7 +429,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
       uint32_t n = 0, k = 0;
-      int last_n[kStages] = {-1, -1, -1};
+      int last_n[ns];
+#pragma unroll
+      for (int s2 = 0; s2 < ns; ++s2) last_n[s2] = -1;
       int last_q[2] = {-1, -1};
       auto load_q = [&](uint32_t kk, const Segment& sg) {
         const uint32_t qs = kk & 1;
@@ -464,32 +476,36 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           }
           if constexpr (DEEP) {
             // K chunk 2n, then V chunk 2n + 1, each into the slot its chunk
-            // number gives.  Chunk 3 (tile 1's V) needs slot 0 back, i.e.
-            // tile 0's S product, i.e. q: early streaming stops after tile
-            // 1's K.
+            // number gives.  Chunk ns needs slot 0 back, i.e. tile 0's S
+            // product, i.e. q: early streaming stops before it.
             const int row = unit_row + lt * TT;
             const uint32_t ck = 2 * n, cv = 2 * n + 1;
-            const int sk = ck % kStages, sv = cv % kStages;
-            if (!mbar_wait(BAR(B_EMPTY + sk), ((ck / kStages) & 1) ^ 1, abort_flag, status,
-                           budget))
-              continue;
-            mbar_arrive_expect_tx(BAR(B_FULL_K + sk), kh * kBoxBytes);
-            for (int bx = 0; bx < kh; ++bx)
-              tma_load_2d(s_base + sk * C::KV_BYTES + bx * kBoxBytes, &tm_k, BAR(B_FULL_K + sk),
-                          64 * bx, row, pol_stream);
-            last_n[sk] = static_cast<int>(ck);  // (DEEP: chunk numbers)
-            if (!waited && lt - seg.lt0 == 1) {
+            const int sk = ck % ns, sv = cv % ns;
+            // (four slots: chunk 4 is tile 2's K; three slots: chunk 3 is
+            // tile 1's V)
+            if (DEEP == 4 && !waited && lt - seg.lt0 == 2) {
               pdl_wait_then_release();
               waited = true;
               load_q(k, seg);
             }
-            if (!mbar_wait(BAR(B_EMPTY + sv), ((cv / kStages) & 1) ^ 1, abort_flag, status,
-                           budget))
+            if (!mbar_wait(BAR(B_EMPTY + sk), ((ck / ns) & 1) ^ 1, abort_flag, status, budget))
+              continue;
+            mbar_arrive_expect_tx(BAR(B_FULL_K + sk), kh * kBoxBytes);
+            for (int bx = 0; bx < kh; ++bx)
+              tma_load_2d(s_base + sk * sb + bx * kBoxBytes, &tm_k, BAR(B_FULL_K + sk), 64 * bx,
+                          row, pol_stream);
+            last_n[sk] = static_cast<int>(ck);  // (DEEP: chunk numbers)
+            if (DEEP == 3 && !waited && lt - seg.lt0 == 1) {
+              pdl_wait_then_release();
+              waited = true;
+              load_q(k, seg);
+            }
+            if (!mbar_wait(BAR(B_EMPTY + sv), ((cv / ns) & 1) ^ 1, abort_flag, status, budget))
               continue;
             mbar_arrive_expect_tx(BAR(B_FULL_V + sv), vh * kBoxBytes);
             for (int bx = 0; bx < vh; ++bx)
-              tma_load_2d(s_base + sv * C::KV_BYTES + bx * kBoxBytes, &tm_v, BAR(B_FULL_V + sv),
-                          64 * bx, row, pol_stream);
+              tma_load_2d(s_base + sv * sb + bx * kBoxBytes, &tm_v, BAR(B_FULL_V + sv), 64 * bx,
+                          row, pol_stream);
             last_n[sv] = static_cast<int>(cv);
             continue;
           }
@@ -531,26 +547,26 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       }
       if (!waited) pdl_wait_then_release();  // a CTA with no tiles
       if (*abort_flag) {  // copies in flight must land before the CTA exits
-        for (int s = 0; s < kStages + 2; ++s) {
+        for (int s = 0; s < ns + 2; ++s) {
           int idx;
           uint32_t b0, b1 = 0;
           bool two = false;
-          if (s < kStages) {
+          if (s < ns) {
             idx = last_n[s];
             if (idx < 0) continue;
             b0 = BAR(B_FULL_K + s);
             b1 = BAR(B_FULL_V + s);
             two = !DEEP;
-            if (DEEP) {  // the slot's last chunk: K (even) or V (odd), phase c / 6
+            if (DEEP) {  // the slot's last chunk: K (even) or V (odd), phase c / pd
               if (idx & 1) b0 = BAR(B_FULL_V + s);
-              idx /= 2 * kStages;
+              idx /= static_cast<int>(pd);
             } else {
               idx /= kStages;
             }
           } else {
-            idx = last_q[s - kStages];
+            idx = last_q[s - ns];
             if (idx < 0) continue;
-            b0 = BAR(B_Q_FULL + s - kStages);
+            b0 = BAR(B_Q_FULL + s - ns);
             idx >>= 1;
           }
           const long long t0 = clock64();
@@ -580,13 +596,13 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     // start-address field (16-byte units, no carry out of it)
     // (DEEP: tile m's V is chunk 2m + 1, in slot (2m + 1) % 3 from its
     // first box)
-    auto v_slot = [&](uint32_t m) -> int { return DEEP ? (2 * m + 1) % kStages : m % kStages; };
+    auto v_slot = [&](uint32_t m) -> int { return DEEP ? (2 * m + 1) % ns : m % kStages; };
     auto v_full = [&](uint32_t m) -> uint32_t { return BAR(B_FULL_V + v_slot(m)); };
     auto v_phase = [&](uint32_t m) -> uint32_t {
-      return DEEP ? ((2 * m + 1) / (2 * kStages)) & 1 : (m / kStages) & 1;
+      return DEEP ? ((2 * m + 1) / pd) & 1 : (m / kStages) & 1;
     };
     auto v_base = [&](uint32_t m) -> uint32_t {
-      return s_base + v_slot(m) * C::KV_BYTES + (DEEP ? 0 : 2 * kBoxBytes);
+      return s_base + v_slot(m) * (DEEP ? sb : C::KV_BYTES) + (DEEP ? 0 : 2 * kBoxBytes);
     };
     auto issue_o = [&](uint32_t m) {
       const int st = v_slot(m);
@@ -740,13 +756,13 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           0xffffffffu, mbar_wait(BAR(B_Q_FULL + qs), (k >> 1) & 1, abort_flag, status, budget));
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
         // (DEEP: tile n's K is chunk 2n)
-        const int st = DEEP ? (2 * n) % kStages : n % kStages;
-        const uint32_t kph = DEEP ? ((2 * n) / (2 * kStages)) & 1 : (n / kStages) & 1;
+        const int st = DEEP ? (2 * n) % ns : n % kStages;
+        const uint32_t kph = DEEP ? ((2 * n) / pd) & 1 : (n / kStages) & 1;
         const uint32_t nb = n & 1;
         bool ok = qok && mbar_wait(BAR(B_FULL_K + st), kph, abort_flag, status, budget);
         ok = ok && mbar_wait(BAR(B_S_FREE + nb), ((n >> 1) & 1) ^ 1, abort_flag, status, budget);
         ok = __all_sync(0xffffffffu, ok);
-        const uint32_t kbase = s_base + st * C::KV_BYTES;
+        const uint32_t kbase = s_base + st * (DEEP ? sb : C::KV_BYTES);
         const bool new_rows = nrows > 0 && (lt + 1) * TT > first_new;
         if (new_rows) {
           // rows L_i - n .. L_i - 1 of this tile are the new tokens: use
@@ -762,8 +778,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             for (int hf = 0; hf < NH; ++hf) {
               // (WIDE: half hf = positions 128 hf .. 128 hf + 127, the
               // stage's box hf, into its own accumulator)
-              const uint64_t a0 =
-                  smem_desc(s_base + st * C::KV_BYTES + hf * kBoxBytes, 16, 1024, SWZ_128B);
+              const uint64_t a0 = smem_desc(kbase + hf * kBoxBytes, 16, 1024, SWZ_128B);
 #pragma unroll
               for (int kk = 0; kk < (DEEP ? 16 : 8); ++kk) {
                 // A = K tile, K-major: 128 rows, 16 head-dim columns (32
@@ -1010,11 +1025,12 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         const bool patch_v = append_v && lt == seg.ti - 1;
         if (wg == 0 && (valid < TT || patch_v)) {
           // (DEEP: the V chunk 2n + 1 has a slot of its own)
-          const int vst = DEEP ? (2 * n + 1) % kStages : st;
+          const int vst = DEEP ? (2 * n + 1) % ns : st;
           const bool vok = mbar_wait(BAR(B_FULL_V + vst),
-                                     DEEP ? ((2 * n + 1) / (2 * kStages)) & 1 : (n / kStages) & 1,
+                                     DEEP ? ((2 * n + 1) / pd) & 1 : (n / kStages) & 1,
                                      abort_flag, status, budget);
-          const uint32_t vbase = s_base + vst * C::KV_BYTES + (DEEP ? 0 : 2 * kBoxBytes);
+          const uint32_t vbase =
+              s_base + vst * (DEEP ? sb : C::KV_BYTES) + (DEEP ? 0 : 2 * kBoxBytes);
           if (vok && patch_v && row < vch) {
             // (WIDE: rows 0-255 run on through the second box)
             const int rho = valid - 1;
@@ -1031,7 +1047,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (vok && pos >= valid) {
               const uint32_t vrow = vbase + pos * 128;
 #pragma unroll
-              for (int hb = 0; hb < (WIDE ? 1 : (DEEP ? 4 : 2)); ++hb)
+              // (the boxes the O product reads: DEEP with three slots all
+              // four, with four slots the two of d_v <= 128)
+              for (int hb = 0; hb < (WIDE ? 1 : (DEEP == 3 ? 4 : 2)); ++hb)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
@@ -1507,7 +1525,7 @@ cudaError_t configure_kernel(K kern, int smem, std::atomic<unsigned long long>& 
   return cudaSuccess;
 }
 
-template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE, bool DEEP = false>
+template <int NP, int NWG, bool MULTI, bool PAGED, typename T16, bool WIDE, int DEEP = 0>
 cudaError_t launch_np(const DecodeLaunch& a) {
   constexpr bool kBf16 = Half16<T16>::kBf16;
   using C = TcCfg<NP, NWG, MULTI, PAGED, kBf16, WIDE, DEEP>;
@@ -1553,9 +1571,14 @@ template <typename T16, bool WIDE>
 cudaError_t launch_type(const DecodeLaunch& a) {
   const int cols = a.nq * (a.h / a.g);
   const bool one = a.nq == 1;
-  if (deep_dims(a.d, a.dv))  // (contiguous caches, 16 query rows at most)
-    return one ? launch_np<16, 1, false, false, T16, false, true>(a)
-               : launch_np<16, 1, true, false, T16, false, true>(a);
+  if (deep_dims(a.d, a.dv)) {  // (contiguous caches, 16 query rows at most)
+    // four 48 KiB ring slots when a K chunk fits three boxes and V two
+    if (a.d <= 192 && a.dv <= 128)
+      return one ? launch_np<16, 1, false, false, T16, false, 4>(a)
+                 : launch_np<16, 1, true, false, T16, false, 4>(a);
+    return one ? launch_np<16, 1, false, false, T16, false, 3>(a)
+               : launch_np<16, 1, true, false, T16, false, 3>(a);
+  }
   if (a.block_table != nullptr) {
     if (one)
       return cols <= 16 ? launch_np<16, 1, false, true, T16, WIDE>(a)
@@ -1590,7 +1613,7 @@ int tc_max_clusters(int csize) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (init[dev][csize].load()) return cache[dev][csize].load();
   using C = TcCfg<32, 2, false, false, true, false>;
-  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16, false, false>;
+  auto kern = decode_tc_kernel<32, 2, false, false, __nv_bfloat16, false, 0>;
   static std::atomic<unsigned long long> configured{0};
   if (configure_kernel(kern, C::SMEM, configured) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
