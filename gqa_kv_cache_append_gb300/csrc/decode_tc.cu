@@ -65,9 +65,16 @@ namespace {
 constexpr int kT = 128;       // positions per tile (MMA M of the S product)
 constexpr int kStages = 3;    // K/V ring depth (DEEP: ring slots, three or four)
 constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
-// early streaming: tiles past the ring that L2 is asked for before the wait
-// (launches whose merge runs in a separate combine kernel skip it: there the
-// prefetch competes with the combine's reads of the partials in L2)
+// early streaming: a CTA copies kEarlyTiles tiles into its ring before the
+// dependency wait and asks L2 for the next kPrefetchTiles.  Fewer copies in
+// flight let the q copy after the wait land sooner, and the tiles that
+// follow come from L2.  Measured against three copied tiles (and L2 asked
+// for three more only on launches that merge in place): long-context MQA
+// 85.6 -> 83.4-83.7 us per call, the b = 16 sweep at g = 4 27.0 -> 25.5-26.0,
+// g = 8 43.5 -> 42.6-43.5, g = 1 15.4 -> 15.1-15.3; the Llama-3-70B shape
+// the same (153.0), the Qwen-shaped batch 343 -> 344.  (Two copied tiles, no
+// copied tile, or five asked of L2 were slower on the small calls.)
+constexpr int kEarlyTiles = 1;
 constexpr int kPrefetchTiles = 3;
 // steady state with d_k = d_v = 64 (half-size tiles, the ring holds half
 // the bytes): when tile t's copies are issued, L2 is asked for tile
@@ -448,7 +455,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
       bool waited = !early;  // has this thread passed the dependency wait?
       while (w.next(seg)) {
         // q comes from the previous kernel: load it only after the wait
-        // (early mode: after the first ring's worth of K/V tiles).  Before
+        // (early mode: after the first kEarlyTiles K/V tiles).  Before
         // the wait L2 is asked for it, ahead of the K/V copies: that moves
         // no data into this CTA, and a write by the kernel ahead lands in
         // L2 all the same, where the load after the wait finds it.
@@ -460,10 +467,10 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
         }
         const int unit_row = (seg.i * g + seg.j) * cap;
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
-          if (!waited && (lt - seg.lt0 == kStages)) {
-            // the ring is full: have L2 fetch the next tiles too, so HBM stays
-            // busy until the kernel ahead completes
-            for (int lp = lt; lp < seg.lt1 && lp < lt + (counters ? kPrefetchTiles : 0); ++lp) {
+          if (!waited && (lt - seg.lt0 == (DEEP ? kStages : kEarlyTiles))) {
+            // have L2 fetch the next tiles, so HBM stays busy until the kernel
+            // ahead completes (DEEP waits inside its branch below)
+            for (int lp = lt; lp < seg.lt1 && lp < lt + (DEEP ? 0 : kPrefetchTiles); ++lp) {
               const int rp = unit_row + lp * TT;
               for (int bx = 0; bx < kh; ++bx) tma_prefetch_l2_2d(&tm_k, 64 * bx, rp);
               if (WIDE) tma_prefetch_l2_2d(&tm_k, 0, rp + kT);
@@ -538,7 +545,7 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
             if (vh == 2) tma_prefetch_l2_2d(&tm_v, 64, rp);
           }
         }
-        if (!waited) {  // a first segment shorter than the ring
+        if (!waited) {  // a first segment of kEarlyTiles tiles or fewer
           pdl_wait_then_release();
           waited = true;
           load_q(k, seg);
