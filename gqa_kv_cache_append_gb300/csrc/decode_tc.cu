@@ -216,7 +216,6 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
                      const int* __restrict__ table, int bsz, int max_blocks, int num_blocks,
                      int kh, int vh, int cl_size, int cl_k) {
   using C = TcCfg<NP, NWG, MULTI, PAGED, Half16<T16>::kBf16, WIDE, DEEP>;
-  static_assert(!(DEEP && PAGED), "DEEP: contiguous caches");
   using Bs = Bars<C::RS>;
   constexpr int B_FULL_K = Bs::FULL_K, B_FULL_V = Bs::FULL_V, B_EMPTY = Bs::EMPTY,
                 B_Q_FULL = Bs::Q_FULL, B_Q_EMPTY = Bs::Q_EMPTY, B_S_FULL = Bs::S_FULL,
@@ -328,7 +327,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     const int box_rows = bsz < kT ? bsz : kT;
     const int sub = TT / box_rows;  // boxes per tile and 64-column half
     uint32_t n = 0, k = 0;
-    int last_n[kStages] = {-1, -1, -1};
+    int last_n[ns];
+#pragma unroll
+    for (int s2 = 0; s2 < ns; ++s2) last_n[s2] = -1;
     int last_q[2] = {-1, -1};
     auto load_q = [&](uint32_t kk, const Segment& sg) {
       const uint32_t qs = kk & 1;
@@ -358,6 +359,58 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           pdl_wait_then_release();
           waited = true;
           load_q(k, seg);
+        }
+        if constexpr (DEEP) {
+          // as in the contiguous producer: K chunk 2n, then V chunk 2n + 1,
+          // each into its slot; lane mm < sub copies the rows of box mm of
+          // every 64-column box of the chunk
+          const uint32_t ck = 2 * n, cv = 2 * n + 1;
+          const int sk = ck % ns, sv = cv % ns;
+          const int p_first = lt * TT;
+          const int blk_l = pc.get_lanes(p_first / bsz);
+          const int blk = (box_rows == bsz) ? blk_l : __shfl_sync(0xffffffffu, blk_l, 0);
+          const int pm = p_first + lane * box_rows;
+          bool bad = false;
+          int row = oob_row;
+          if (lane < sub && pm < seg.L) {
+            if (blk >= 0 && blk < num_blocks)
+              row = (blk * g + seg.j) * bsz + pm % bsz;
+            else
+              bad = true;
+          }
+          const uint32_t o = lane * box_rows * 128;
+          if (DEEP == 4 && !waited && lt - seg.lt0 == 2) {
+            pdl_wait_then_release();
+            waited = true;
+            load_q(k, seg);
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_EMPTY + sk), ((ck / ns) & 1) ^ 1,
+                                                 abort_flag, status, budget)))
+            continue;
+          if (lane == 0) mbar_arrive_expect_tx(BAR(B_FULL_K + sk), kh * kBoxBytes);
+          __syncwarp();
+          if (lane < sub)
+            for (int bx = 0; bx < kh; ++bx)
+              tma_load_2d(s_base + sk * sb + bx * kBoxBytes + o, &tm_k, BAR(B_FULL_K + sk),
+                          64 * bx, row, pol_stream);
+          last_n[sk] = static_cast<int>(ck);  // (DEEP: chunk numbers)
+          if (DEEP == 3 && !waited && lt - seg.lt0 == 1) {
+            pdl_wait_then_release();
+            waited = true;
+            load_q(k, seg);
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_EMPTY + sv), ((cv / ns) & 1) ^ 1,
+                                                 abort_flag, status, budget)))
+            continue;
+          if (lane == 0) mbar_arrive_expect_tx(BAR(B_FULL_V + sv), vh * kBoxBytes);
+          __syncwarp();
+          if (lane < sub)
+            for (int bx = 0; bx < vh; ++bx)
+              tma_load_2d(s_base + sv * sb + bx * kBoxBytes + o, &tm_v, BAR(B_FULL_V + sv),
+                          64 * bx, row, pol_stream);
+          last_n[sv] = static_cast<int>(cv);
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, GQA_DEV_BAD_BLOCK);
+          continue;
         }
         const int st = n % kStages;
         const bool ok = __all_sync(0xffffffffu,
@@ -405,21 +458,26 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
     }
     if (!waited) pdl_wait_then_release();
     if (*abort_flag && lane == 0) {
-      for (int s = 0; s < kStages + 2; ++s) {
+      for (int s = 0; s < ns + 2; ++s) {
         int idx;
         uint32_t b0, b1 = 0;
         bool two = false;
-        if (s < kStages) {
+        if (s < ns) {
           idx = last_n[s];
           if (idx < 0) continue;
           b0 = BAR(B_FULL_K + s);
           b1 = BAR(B_FULL_V + s);
-          two = true;
-          idx /= kStages;
+          two = !DEEP;
+          if (DEEP) {  // the slot's last chunk: K (even) or V (odd), phase c / pd
+            if (idx & 1) b0 = BAR(B_FULL_V + s);
+            idx /= static_cast<int>(pd);
+          } else {
+            idx /= kStages;
+          }
         } else {
-          idx = last_q[s - kStages];
+          idx = last_q[s - ns];
           if (idx < 0) continue;
-          b0 = BAR(B_Q_FULL + s - kStages);
+          b0 = BAR(B_Q_FULL + s - ns);
           idx >>= 1;
         }
         const long long t0 = clock64();
@@ -1578,9 +1636,17 @@ template <typename T16, bool WIDE>
 cudaError_t launch_type(const DecodeLaunch& a) {
   const int cols = a.nq * (a.h / a.g);
   const bool one = a.nq == 1;
-  if (deep_dims(a.d, a.dv)) {  // (contiguous caches, 16 query rows at most)
+  if (deep_dims(a.d, a.dv)) {  // (16 query rows at most)
     // four 48 KiB ring slots when a K chunk fits three boxes and V two
-    if (a.d <= 192 && a.dv <= 128)
+    const bool four = a.d <= 192 && a.dv <= 128;
+    if (a.block_table != nullptr) {
+      if (four)
+        return one ? launch_np<16, 1, false, true, T16, false, 4>(a)
+                   : launch_np<16, 1, true, true, T16, false, 4>(a);
+      return one ? launch_np<16, 1, false, true, T16, false, 3>(a)
+                 : launch_np<16, 1, true, true, T16, false, 3>(a);
+    }
+    if (four)
       return one ? launch_np<16, 1, false, false, T16, false, 4>(a)
                  : launch_np<16, 1, true, false, T16, false, 4>(a);
     return one ? launch_np<16, 1, false, false, T16, false, 3>(a)
@@ -1602,9 +1668,9 @@ cudaError_t launch_type(const DecodeLaunch& a) {
 
 }  // namespace
 
-bool tc_supported(int dtype, int d_k, int d_v, int cols, bool paged) {
+bool tc_supported(int dtype, int d_k, int d_v, int cols, bool) {
   if (dtype != GQA_BF16 && dtype != GQA_F16) return false;
-  if (deep_dims(d_k, d_v)) return !paged && cols >= 1 && cols <= 16;
+  if (deep_dims(d_k, d_v)) return cols >= 1 && cols <= 16;
   return (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128) && cols >= 1 && cols <= 32;
 }
 

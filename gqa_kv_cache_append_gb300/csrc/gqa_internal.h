@@ -58,8 +58,8 @@ int simt_ctas_per_sm(int dtype, int d, int r);
 cudaError_t launch_decode_simt(const DecodeLaunch& a);
 
 // tcgen05 tensor-core kernel (bf16 and fp16, d_k and d_v in {64, 128}, up to
-// 32 query rows per KV head; on contiguous caches also d_k, d_v in {128,
-// 192, 256}, up to 16 rows)
+// 32 query rows per KV head; also d_k, d_v in {128, 192, 256}, up to 16
+// rows)
 bool tc_supported(int dtype, int d_k, int d_v, int cols, bool paged);
 int tc_tile(int d_k, int d_v);  // positions per tile (256 for d_k = d_v = 64, else 128)
 // clusters of csize CTAs of the tensor-core kernel that fit on the device

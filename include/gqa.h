@@ -133,8 +133,7 @@ int gqa_kv_append(const void* k_new, const void* v_new, void* k_cache,
  * Supported: d_k, d_v in {64, 128} (they may differ): bf16 / fp16 with
  * h / g <= 32 (tensor-core kernel), fp32 with h / g <= 16 (CUDA-core
  * kernel); d_k, d_v in {128, 192, 256}, not both 128 (they may differ):
- * bf16 / fp16 with h / g <= 16 (tensor-core kernel; contiguous caches
- * only).  b <= 65535.
+ * bf16 / fp16 with h / g <= 16 (tensor-core kernel).  b <= 65535.
  * Returns GQA_OK or an error code (nothing is launched on error).
  */
 int gqa_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -246,9 +245,8 @@ int gqa_decode_step_multi(const void* q, const void* k_new, const void* v_new,
  * access leaves the pools).  block_size: a power of two in [16, 65536]
  * (GQA_ERR_UNSUPPORTED otherwise).  n new tokens per sequence (n = 1: one
  * token; n > 1: the causal n-token step of gqa_decode_*_multi, with q / out
- * [b, n, h, d] and k_new / v_new [b, n, g, d]).  Head dims d_k, d_v in
- * {64, 128} (larger ones: GQA_ERR_UNSUPPORTED).  Kernels and limits
- * otherwise as for the contiguous calls; with GQA_STEP_EARLY_STREAM the
+ * [b, n, h, d] and k_new / v_new [b, n, g, d]).  Kernels and limits as for
+ * the contiguous calls; with GQA_STEP_EARLY_STREAM the
  * kernels ahead must not write the block table either.
  *
  * gqa_kv_append_paged   - the append of gqa_kv_append(_multi) into the pools.

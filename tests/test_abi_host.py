@@ -230,7 +230,7 @@ def test_paged_host_checks():
     assert call(f, args, i16=4) == -3
     assert call(f, args, i6=0) == -2                  # n < 1
     assert call(f, args, i6=9) == -5                  # 9 tokens x 4 heads > 32 rows
-    assert call(f, args, i9=256, i10=256) == -5       # head dims above 128: contiguous only
+    assert call(f, args, i7=64, i9=256, i10=256) == -5  # head dims above 128: 16 rows at most
     st = b.lib.gqa_decode_step_paged
     sargs = [A, A, A, A, A, A, A, 2, 1, 8, 2, 128, 128, 0.1, A, 64, 4, 16, 1, 0, None]
     assert call(st, sargs, i1=0) == -1

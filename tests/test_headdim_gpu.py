@@ -143,7 +143,10 @@ def test_tc_head_dims_multi_token(dtype, dk, dv, fused):
 
 
 @pytest.mark.parametrize("dk,dv,bs,n", [(64, 64, 16, 1), (64, 128, 128, 1), (128, 64, 64, 1),
-                                        (64, 64, 32, 3), (128, 64, 256, 3)])
+                                        (64, 64, 32, 3), (128, 64, 256, 3),
+                                        # head dims above 128
+                                        (256, 256, 16, 1), (192, 128, 64, 1), (128, 256, 256, 3),
+                                        (256, 128, 32, 3), (192, 192, 16, 1), (192, 128, 16, 3)])
 def test_tc_head_dims_paged(dk, dv, bs, n):
     from gqa_kv_cache_append_gb300.inputs import to_paged
     B = _b()
@@ -420,3 +423,31 @@ def test_tc_long_segments(monkeypatch, dk, dv, flags):
     assert to_np(d["k_cache"])[0].tobytes() == kc.tobytes()
     assert to_np(d["v_cache"])[0].tobytes() == vc.tobytes()
     assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", f"long segments {dk}/{dv}")
+
+
+@pytest.mark.parametrize("dk,dv", [(256, 256), (192, 128), (128, 128)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_tc_long_segments_paged(monkeypatch, dk, dv, flags):
+    """The long-segment case through a shuffled table of 16-row blocks."""
+    from gqa_kv_cache_append_gb300.inputs import to_paged
+    monkeypatch.setenv("GQA_CTAS", "2")
+    B = _b()
+    b, h, g, cap, bs = 2, 16, 2, 4096, 16
+    lens = [4096, 4096 - 77]
+    x, _ = _case("bf16", b, 0, h, g, dk, dv, cap, lens, seed=dk + dv + 11 * flags)
+    kp, _, table = to_paged(x["k_cache"], x["k_cache"], bs, seed=5, fill=float("nan"))
+    _, vp, _ = to_paged(x["v_cache"], x["v_cache"], bs, seed=5, fill=float("nan"))
+    d = {k: v.cuda() for k, v in x.items()}
+    kp_d, vp_d = kp.cuda(), vp.cuda()
+    out = torch.empty((b, h, dv), dtype=torch.bfloat16, device="cuda")
+    scale = 1 / math.sqrt(dk)
+    B.gqa_decode_step_paged(d["q"], d["k_new"], d["v_new"], kp_d, vp_d, table.cuda(),
+                            d["seq_lens"], b, h, g, dk, dv, scale, out,
+                            flags=B.GQA_STEP_EARLY_STREAM if flags else 0)
+    assert B.gqa_device_status() == 0
+    ref, kp2, vp2 = oracle.decode_step_paged(_np(x, "q"), to_np(kp)[0], to_np(vp)[0],
+                                             _np(x, "k_new"), _np(x, "v_new"), table.numpy(),
+                                             np.asarray(lens), g, scale, bs, dtype="bf16")
+    assert to_np(kp_d)[0].tobytes() == kp2.tobytes()
+    assert to_np(vp_d)[0].tobytes() == vp2.tobytes()
+    assert_close(oracle.widen(to_np(out)[0], "bf16"), ref, "bf16", f"paged long {dk}/{dv}")
