@@ -2,7 +2,9 @@
 float64 oracle: sequences, query and KV heads (r = 1..32), ragged lengths
 (including 1 and tile edges), one or n new tokens, head dims 64 / 128 for
 K and V independently, bf16 / fp16 / fp32, contiguous or paged caches,
-fused step or the two calls.  Each case draws its own shape from a fixed
+fused step or the two calls; and a second sweep over the head dims above
+128 (128 / 192 / 256 for K and V, not both 128; bf16 / fp16, at most 16
+query rows per KV head).  Each case draws its own shape from a fixed
 generator, so the set is the same every run; the appended rows are
 compared bit for bit, the outputs within the dtype's bound."""
 import math
@@ -18,18 +20,25 @@ pytestmark = pytest.mark.gpu
 
 DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 N_CASES = 40
+N_WIDE = 24
 
 
-def _shape(case):
-    rng = np.random.default_rng(9000 + case)
-    dtype = ["bf16", "f16", "f32"][case % 3]
+def _shape(case, wide=False):
+    rng = np.random.default_rng((9500 if wide else 9000) + case)
+    dtype = (["bf16", "f16"][case % 2]) if wide else ["bf16", "f16", "f32"][case % 3]
     g = int(rng.choice([1, 2, 4, 8]))
     n = int(rng.choice([1, 1, 1, 2, 4]))
-    rmax = (16 if dtype == "f32" else 32) // n
+    rmax = (16 if (dtype == "f32" or wide) else 32) // n
     r = int(rng.choice([x for x in (1, 2, 4, 7, 8, 16, 32) if x <= rmax]))
     b = int(rng.integers(1, 9))
-    dk = int(rng.choice([64, 128]))
-    dv = int(rng.choice([64, 128]))
+    if wide:
+        dk, dv = 128, 128
+        while dk == 128 and dv == 128:
+            dk = int(rng.choice([128, 192, 256]))
+            dv = int(rng.choice([128, 192, 256]))
+    else:
+        dk = int(rng.choice([64, 128]))
+        dv = int(rng.choice([64, 128]))
     cap = int(rng.choice([128, 256, 640, 1500, 4096]))
     lens = rng.integers(n, cap + 1, size=b)
     edge = [n, 127, 128, 129, cap]
@@ -44,9 +53,18 @@ def _shape(case):
 
 @pytest.mark.parametrize("case", range(N_CASES))
 def test_random_shape(case):
+    _run(_shape(case))
+
+
+@pytest.mark.parametrize("case", range(N_WIDE))
+def test_random_wide_shape(case):
+    _run(_shape(case, wide=True))
+
+
+def _run(s):
     from gqa_kv_cache_append_gb300 import binding as B
     from gqa_kv_cache_append_gb300.inputs import to_paged
-    s = _shape(case)
+    case = s["seed"]
     dt, b, n, h, g, dk, dv, cap = (s[k] for k in ("dtype", "b", "n", "h", "g", "dk", "dv", "cap"))
     gen = torch.Generator().manual_seed(77 + case)
     rnd = lambda *sh: torch.randn(sh, generator=gen).to(DT[dt])
