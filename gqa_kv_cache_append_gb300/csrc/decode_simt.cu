@@ -3,7 +3,8 @@
 //
 // One persistent CTA per SM streams its share of the (sequence, KV head)
 // tiles (see Walker).  Warp 0 copies each K/V tile of T positions from HBM
-// into a five-stage shared-memory ring with one bulk copy per tensor (the
+// into a shared-memory ring (three 64 KiB stages for fp32, five of 32 KiB
+// for 16-bit data) with one bulk copy per tensor (the
 // rows of a tile are contiguous in the cache), completing on an mbarrier;
 // only the rows below L_i are copied.  Warps 1-7 serve all r = h/g query
 // heads of the KV head from each tile:
@@ -82,7 +83,10 @@ struct Elt<__half> {
 // Seven compute warps: eight warps in all, two per SM sub-partition, so a
 // thread may hold up to 255 registers (measured: fifteen compute warps of
 // 128 registers were slower on the fp32 Llama-3-70B shape, 2.0 against 2.6
-// TB/s, their share of the weighted sum taking twice as long).
+// TB/s, their share of the weighted sum taking twice as long).  fp32 tiles
+// hold 64 KiB of K + V in a three-stage ring (half the barriers and softmax
+// passes a position of 32 KiB tiles: the fp32 Llama-3-70B shape 848 -> 722
+// us per call), 16-bit ones 32 KiB in five stages.
 template <typename DT, int DK, int DV, int RMAX>
 struct SimtCfg {
   static constexpr int NCW = 7;
@@ -94,15 +98,16 @@ struct SimtCfg {
   static constexpr int EPC = 16 / ELT;         // elements per chunk
   static constexpr int PPW = 32 / CHK;         // K rows per warp step
   static constexpr int DM = DK > DV ? DK : DV;
-  static constexpr int T = 16384 / (DM * ELT); // positions per tile (up to 32 KiB K+V)
+  static constexpr int T = (ELT == 4 ? 32768 : 16384) / (DM * ELT);  // positions per tile
   static constexpr int PPL = T / 16;           // positions per lane in softmax
   static constexpr int NPG = NCT / CHV;        // position groups in the V pass
-  static constexpr int STAGES = 5;
+  static constexpr int STAGES = ELT == 4 ? 3 : 5;
+  static constexpr int NSLOT = ELT == 4 ? 2 : 4;  // segment-end reduction slots
   static constexpr int K_BYTES = T * DK * ELT;
   static constexpr int STAGE_BYTES = T * (DK + DV) * ELT;
   static constexpr int OFF_P = STAGES * STAGE_BYTES;          // float [RMAX][T]
-  static constexpr int OFF_RED = OFF_P + RMAX * T * 4;        // float [4][RMAX][DV]
-  static constexpr int OFF_ML = OFF_RED + 4 * RMAX * DV * 4;  // float m,l,alpha [RMAX]
+  static constexpr int OFF_RED = OFF_P + RMAX * T * 4;            // float [NSLOT][RMAX][DV]
+  static constexpr int OFF_ML = OFF_RED + NSLOT * RMAX * DV * 4;  // float m,l,alpha [RMAX]
   static constexpr int OFF_BAR = OFF_ML + 3 * RMAX * 4;
   static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 128;
@@ -490,21 +495,29 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
           acc[t][e] = v;
         }
       }
-      // (warps 4k .. 4k + 3 add into slots 0-3 in pass k)
+      // (warps NSLOT k .. NSLOT k + NSLOT - 1 add into the slots in pass k)
+      constexpr int NS = C::NSLOT;
 #pragma unroll
-      for (int pass = 0; pass * 4 < kWarps; ++pass) {
-        if (cw / 4 == pass && lane < C::CHV) {
+      for (int pass = 0; pass * NS < kWarps; ++pass) {
+        if (cw / NS == pass && lane < C::CHV) {
 #pragma unroll
           for (int t = 0; t < RMAX; ++t)
             if (t < nr)
 #pragma unroll
               for (int e = 0; e < C::EPC; ++e) {
-                float* dst = sRed + ((cw % 4) * RMAX + t) * DV + chv * C::EPC + e;
+                float* dst = sRed + ((cw % NS) * RMAX + t) * DV + chv * C::EPC + e;
                 *dst = pass == 0 ? acc[t][e] : *dst + acc[t][e];
               }
         }
-        if (pass * 4 + 4 < kWarps) named_bar_sync(1, kCompute);
+        if (pass * NS + NS < kWarps) named_bar_sync(1, kCompute);
       }
+      // the slots' sum for row t, column dd
+      auto red_sum = [&](int t, int dd) {
+        float o = sRed[t * DV + dd];
+#pragma unroll
+        for (int sl = 1; sl < NS; ++sl) o += sRed[(sl * RMAX + t) * DV + dd];
+        return o;
+      };
 #pragma unroll
       for (int t = 0; t < RMAX; ++t)
 #pragma unroll
@@ -519,8 +532,7 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
       };
       for (int idx = ct; idx < nr * DV; idx += kCompute) {
         const int t = idx / DV, dd = idx % DV;
-        const float o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
-                        sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
+        const float o = red_sum(t, dd);
         if (whole) {
           Elt<DT>::store(out + out_row(t) * DV + dd, o / sL[t]);
         } else {
@@ -550,8 +562,7 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
             const int t = idx / DV, dd = idx % DV;
             float o = 0.f, M = -INFINITY, den = 0.f;
             if (own_first) {
-              o = sRed[(0 * RMAX + t) * DV + dd] + sRed[(1 * RMAX + t) * DV + dd] +
-                  sRed[(2 * RMAX + t) * DV + dd] + sRed[(3 * RMAX + t) * DV + dd];
+              o = red_sum(t, dd);
               M = sM[t];
               den = sL[t];
             }
@@ -627,7 +638,9 @@ bool simt_supported(int dtype, int d_k, int d_v, int cols) {
 }
 
 int simt_tile(int dtype, int d_k, int d_v) {
-  return 16384 / ((d_k > d_v ? d_k : d_v) * (dtype == GQA_F32 ? 4 : 2));
+  // (the kernel's SimtCfg::T: K + V of a tile take 64 KiB in fp32, 32 KiB otherwise)
+  const int elt = dtype == GQA_F32 ? 4 : 2;
+  return (dtype == GQA_F32 ? 32768 : 16384) / ((d_k > d_v ? d_k : d_v) * elt);
 }
 
 int simt_ctas_per_sm(int, int, int) { return 1; }

@@ -261,7 +261,7 @@ def test_decode_plan_query():
     p = b.gqa_decode_plan(32, 1, 64, 8, 128, 128, 8192, "bf16", num_sms=152)
     assert p["tensor_core"] and p["tile"] == 128 and p["ctas"] == 152 and p["kernels"] == 1
     assert p["cluster"] == 0
-    # 64-wide heads: tiles of 256 positions (fp32: the CUDA-core kernel's 64)
+    # 64-wide heads: tiles of 256 positions (fp32: the CUDA-core kernel's 128)
     assert b.gqa_decode_plan(32, 1, 64, 8, 64, 64, 8192, "bf16", num_sms=152)["tile"] == 256
     assert b.gqa_decode_plan(32, 1, 64, 8, 64, 64, 8192, "f16", num_sms=152)["tile"] == 256
     assert b.gqa_decode_plan(32, 1, 64, 8, 64, 128, 8192, "bf16", num_sms=152)["tile"] == 128
