@@ -74,8 +74,14 @@ constexpr int kBoxBytes = kT * 64 * 2;  // one [128 rows x 64 cols] bf16 box
 // g = 8 43.5 -> 42.6-43.5, g = 1 15.4 -> 15.1-15.3; the Llama-3-70B shape
 // the same (153.0), the Qwen-shaped batch 343 -> 344.  (Two copied tiles, no
 // copied tile, or five asked of L2 were slower on the small calls.)
+// Launches that merge in place, on segments of 32 tiles or more, ask L2 for
+// kPrefetchLong instead (same box, twice: Llama-3-70B shape 151.7 -> 150.3
+// us per call, Qwen-shaped batch 340.6 -> 338.8, g = 8 sweep point 42.4 ->
+// 41.6; long-context MQA, merged by the combine kernel, and the 16-tile
+// segments of the g = 4 point were slower with it).
 constexpr int kEarlyTiles = 1;
 constexpr int kPrefetchTiles = 3;
+constexpr int kPrefetchLong = 5;
 // steady state with d_k = d_v = 64 (half-size tiles, the ring holds half
 // the bytes): when tile t's copies are issued, L2 is asked for tile
 // t + kL2Ahead of the same segment, so a copy that a freed stage starts
@@ -528,7 +534,9 @@ __global__ void __maxnreg__(NWG == 2 ? 168 : 200)
           if (!waited && (lt - seg.lt0 == (DEEP ? kStages : kEarlyTiles))) {
             // have L2 fetch the next tiles, so HBM stays busy until the kernel
             // ahead completes (DEEP waits inside its branch below)
-            for (int lp = lt; lp < seg.lt1 && lp < lt + (DEEP ? 0 : kPrefetchTiles); ++lp) {
+            const int npf =
+                (counters != nullptr && seg.lt1 - seg.lt0 >= 32) ? kPrefetchLong : kPrefetchTiles;
+            for (int lp = lt; lp < seg.lt1 && lp < lt + (DEEP ? 0 : npf); ++lp) {
               const int rp = unit_row + lp * TT;
               for (int bx = 0; bx < kh; ++bx) tma_prefetch_l2_2d(&tm_k, 64 * bx, rp);
               if (WIDE) tma_prefetch_l2_2d(&tm_k, 0, rp + kT);
