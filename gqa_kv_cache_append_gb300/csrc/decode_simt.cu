@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
                        const uint4* __restrict__ v_new, uint4* __restrict__ k_cache_w,
                        uint4* __restrict__ v_cache_w, unsigned int* status, long long budget,
                        int nq, const int* __restrict__ table, int bsz, int max_blocks,
-                       int num_blocks) {
+                       int num_blocks, int early) {
   using C = SimtCfg<DT, DK, DV, RMAX>;
   constexpr int kCompute = C::NCT, kWarps = C::NCW;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -190,15 +190,20 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  pdl_wait_then_release();  // inputs and the split workspace are read only after this
   if (threadIdx.x >= 32 && threadIdx.x < 32 + RMAX) {
     const int t = threadIdx.x - 32;
     sM[t] = -INFINITY;
     sL[t] = 0.f;
     sA[t] = 0.f;
   }
+  __syncthreads();  // barrier inits and the softmax state (this CTA's own)
+  // Inputs and the split workspace are read only after the dependency wait.
+  // With `early` set the caller guarantees that no kernel still running
+  // writes seq_lens, the block table or the cache rows below L_i - n (e.g.
+  // it is another layer's step), so the producer warp plans its tiles and
+  // copies the first ring's worth before it waits.
+  if (!early || warp != 0) pdl_wait_then_release();
   if (warp == 1 && blockIdx.x == 0) report_bad_lengths(lens, b, nq, cap, status);
-  __syncthreads();
 
   Walker w;
   w.init(lens, b, g, nq, cap, C::T, blockIdx.x, gridDim.x);
@@ -216,10 +221,15 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
       for (int s = 0; s < C::STAGES; ++s) last_n[s] = -1;
       const int piece = bsz < C::T ? bsz : C::T;
       PageCursor pc;
+      bool waited = !early;
       while (w.next(seg)) {
         pc.start(table + static_cast<size_t>(seg.i) * max_blocks, (seg.L + bsz - 1) / bsz,
                  (seg.lt0 * C::T) / bsz);
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          if (!waited && n == static_cast<uint32_t>(C::STAGES)) {  // the ring is full
+            pdl_wait_then_release();
+            waited = true;
+          }
           const int st = n % C::STAGES;
           const bool ok = __all_sync(0xffffffffu,
                                      mbar_wait(empty0 + 8 * st, ((n / C::STAGES) & 1) ^ 1,
@@ -249,6 +259,7 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
           last_n[st] = static_cast<int>(n);
         }
       }
+      if (!waited) pdl_wait_then_release();
       if (*abort_flag && lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
           if (last_n[s] < 0) continue;
@@ -263,9 +274,14 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
       int last_n[C::STAGES];
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) last_n[s] = -1;
+      bool waited = !early;
       while (w.next(seg)) {
         const size_t unit_row = (static_cast<size_t>(seg.i) * g + seg.j) * cap;
         for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
+          if (!waited && n == static_cast<uint32_t>(C::STAGES)) {  // the ring is full
+            pdl_wait_then_release();
+            waited = true;
+          }
           const int st = n % C::STAGES;
           const bool ok = mbar_wait(empty0 + 8 * st, ((n / C::STAGES) & 1) ^ 1, abort_flag,
                                     status, budget);
@@ -281,6 +297,7 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
           last_n[st] = static_cast<int>(n);
         }
       }
+      if (!waited) pdl_wait_then_release();
       if (*abort_flag) {  // let copies in flight land before the CTA exits
         for (int s = 0; s < C::STAGES; ++s) {
           if (last_n[s] < 0) continue;
@@ -625,7 +642,7 @@ cudaError_t launch_t(const DecodeLaunch& a) {
       static_cast<DT*>(a.out), a.part_o, a.part_ml, a.counters,
       static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
       static_cast<uint4*>(a.k_cache_w), static_cast<uint4*>(a.v_cache_w), a.status, a.budget,
-      a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks);
+      a.nq, a.block_table, a.block_size, a.max_blocks, a.num_blocks, a.early ? 1 : 0);
 }
 
 }  // namespace

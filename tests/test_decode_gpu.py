@@ -127,27 +127,31 @@ def test_fused_step_matches_two_calls_bitwise():
     assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
 
 
-@pytest.mark.parametrize("b,h,g,cap,lens", [
-    (8, 64, 8, 2000, None),                  # units split in-kernel
-    (2, 32, 1, 9000, [9000, 4500]),          # few long units: combine kernel
+@pytest.mark.parametrize("dtype,b,h,g,d,cap,lens", [
+    ("bf16", 8, 64, 8, 128, 2000, None),          # units split in-kernel
+    ("bf16", 2, 32, 1, 128, 9000, [9000, 4500]),  # few long units: combine kernel
+    ("f32", 8, 64, 8, 128, 2000, None),           # the CUDA-core kernel
+    ("f32", 1, 8, 1, 64, 256, [256]),             # the fp32 MQA step's shape
+    ("f32", 2, 16, 1, 128, 9000, [9000, 4500]),   # CUDA-core kernel + combine kernel
 ])
-def test_early_stream_matches_ordered_calls(b, h, g, cap, lens):
+def test_early_stream_matches_ordered_calls(dtype, b, h, g, d, cap, lens):
     """Six layers back to back with GQA_STEP_EARLY_STREAM give the same
-    outputs and caches, bit for bit, as the default ordered calls."""
+    outputs and caches, bit for bit, as the default ordered calls (on the
+    tensor-core and the CUDA-core kernel)."""
     B = _b()
-    cfg = cfg_of("bf16", b, h, g, 128, cap, seed=b + g)
+    cfg = cfg_of(dtype, b, h, g, d, cap, seed=b + g)
     lens = np.asarray(lens if lens is not None else [cap - 37 * i for i in range(b)], np.int32)
     layers = [make_layer(cfg, l, "cuda", lens=lens) for l in range(6)]
     results = []
     for flags in (0, B.GQA_STEP_EARLY_STREAM):
         kcs = [x["k_cache"].clone() for x in layers]
         vcs = [x["v_cache"].clone() for x in layers]
-        outs = [torch.empty((b, h, 128), dtype=torch.bfloat16, device="cuda") for _ in layers]
+        outs = [torch.empty((b, h, d), dtype=cfg.torch_dtype, device="cuda") for _ in layers]
         torch.cuda.synchronize()
         for rep in range(3):
             for l, x in enumerate(layers):
                 B.gqa_decode_step(x["q"], x["k_new"], x["v_new"], kcs[l], vcs[l], x["seq_lens"],
-                                  b, h, g, 128, 128, cfg.scale, outs[l], flags=flags)
+                                  b, h, g, d, d, cfg.scale, outs[l], flags=flags)
         torch.cuda.synchronize()
         results.append((outs, kcs, vcs))
     assert B.gqa_device_status() == 0
@@ -158,8 +162,9 @@ def test_early_stream_matches_ordered_calls(b, h, g, cap, lens):
     # and the ordered result is right
     x = layers[0]
     args = [to_np(x[k])[0] for k in ("q", "k_cache", "v_cache", "k_new", "v_new")]
-    ref, _, _ = oracle.decode_step(*args, lens, g, cfg.scale, dtype="bf16")
-    assert_close(oracle.widen(to_np(results[1][0][0])[0], "bf16"), ref, "bf16")
+    tag = to_np(x["q"])[1]
+    ref, _, _ = oracle.decode_step(*args, lens, g, cfg.scale, dtype=tag)
+    assert_close(oracle.widen(to_np(results[1][0][0])[0], tag), ref, tag)
 
 
 @pytest.mark.parametrize("b,h,g,cap", [(4, 64, 8, 1500), (2, 32, 1, 6000)])
