@@ -863,8 +863,10 @@ def run_ours(args, rank, local_rank, world):
     # pinned host memory, runs the layers, and copies all outputs back.  The
     # copies run on a second stream beside the layers: the first layer's
     # inputs, then the next three layers', then the rest, each group waited
-    # for by the first layer that reads it; the outputs go back in groups of
-    # eight layers as each group's last layer ends, the last layer alone.
+    # for by the first layer that reads it; the outputs go back in about ten
+    # groups (at least eight layers each) as each group's last layer ends,
+    # the last layer alone (an event between two launches costs host time,
+    # which a step of short launches feels).
     # The step ends when its last copy has.  The serial form (all inputs,
     # the layers, all outputs, one stream) is timed beside it. ----
     host_in = {k: v.cpu().pin_memory() for k, v in packed.items()}
@@ -874,7 +876,9 @@ def run_ours(args, rank, local_rank, world):
     nl = cfg.layers
     in_cuts = sorted({0, min(1, nl), min(4, nl), nl})
     in_groups = list(zip(in_cuts[:-1], in_cuts[1:]))
-    out_ends = sorted({e for e in range(7, nl - 1, 8)} | {e for e in (nl - 2, nl - 1) if e >= 0})
+    og = max(8, -(-nl // 10))
+    out_ends = sorted({e for e in range(og - 1, nl - 1, og)} |
+                      {e for e in (nl - 2, nl - 1) if e >= 0})
     out_groups = list(zip([0] + [e + 1 for e in out_ends[:-1]], [e + 1 for e in out_ends]))
     side = torch.cuda.Stream(dev)
     ev_start = torch.cuda.Event()
