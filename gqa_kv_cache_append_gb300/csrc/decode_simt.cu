@@ -8,16 +8,17 @@
 // rows of a tile are contiguous in the cache), completing on an mbarrier;
 // only the rows below L_i are copied.  Warps 1-7 serve all r = h/g query
 // heads of the KV head from each tile:
-//   A  logits: 16-byte vector loads of K, fp32 dot products against q held
-//      in registers, summed across the lanes that share a row by a
-//      reduce-scatter of xor shuffles (each round trades half of the heads'
-//      partial sums with the partner lane: r - 1 + log2(lanes / r)
-//      shuffles a row instead of r log2(lanes)) (the "bhk,bhmk->bhm"
+//   A  logits: 16-byte vector loads of K (each lane one or two chunks of a
+//      row: as many as keep q within 64 registers), fp32 dot products
+//      against q held in registers, summed across the lanes that share a
+//      row by a reduce-scatter of xor shuffles (each round trades half of
+//      the heads' partial sums with the partner lane: r - 1 + log2(lanes /
+//      r) shuffles a row instead of r log2(lanes)) (the "bhk,bhmk->bhm"
 //      contraction of the MQA review §2.4);
 //   B  online softmax per head in base 2: warp max, rescale factor, exp2,
 //      warp sum;
-//   C  weighted sum of V rows into fp32 register accumulators ("bhm,bhmv->
-//      bhv"), rescaled by each tile's factor.
+//   C  weighted sum of V rows (two positions a step) into fp32 register
+//      accumulators ("bhm,bhmv->bhv"), rescaled by each tile's factor.
 // A segment's end writes the normalised output; a unit split across CTAs
 // writes a partial instead, and the CTA that finishes the unit last merges
 // the partials (log-sum-exp).  With n new tokens per sequence the "heads"
@@ -96,7 +97,13 @@ struct SimtCfg {
   static constexpr int CHK = DK * ELT / 16;    // 16-byte chunks per K row
   static constexpr int CHV = DV * ELT / 16;    // ... per V row
   static constexpr int EPC = 16 / ELT;         // elements per chunk
-  static constexpr int PPW = 32 / CHK;         // K rows per warp step
+  // logits pass: each lane holds CPL chunks of q per query row (at most 64
+  // registers of q, and at least one head per lane after the reduction),
+  // so LPR lanes share a K row and a warp step covers PPW rows
+  static constexpr int CPL0 = 64 / (RMAX * EPC) < 1 ? 1 : 64 / (RMAX * EPC);
+  static constexpr int CPL = CPL0 < CHK / RMAX ? CPL0 : (CHK / RMAX < 1 ? 1 : CHK / RMAX);
+  static constexpr int LPR = CHK / CPL;
+  static constexpr int PPW = 32 / LPR;         // K rows per warp step
   static constexpr int DM = DK > DV ? DK : DV;
   static constexpr int T = (ELT == 4 ? 32768 : 16384) / (DM * ELT);  // positions per tile
   static constexpr int PPL = T / 16;           // positions per lane in softmax
@@ -115,7 +122,8 @@ struct SimtCfg {
                 "rows must split evenly over lanes");
   static_assert(T % 32 == 0, "tile shape");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(RMAX <= CHK, "a row's lanes hold at least one head each after the reduction");
+  static_assert(RMAX <= LPR, "a row's lanes hold at least one head each after the reduction");
+  static_assert(CHK % CPL == 0 && T % PPW == 0, "logits mapping");
   static_assert(K_BYTES % 16 == 0, "16-byte aligned V tile");
 };
 
@@ -313,9 +321,10 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
     // ---------------- compute (NCT threads) ----------------
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
-    const int sub = lane / C::CHK, ch = lane % C::CHK;  // logits mapping
-    const int pg = ct / C::CHV, chv = lane % C::CHV;     // V-pass mapping
-    float qreg[RMAX][C::EPC];
+    // logits mapping: lane ch of a row's LPR lanes holds chunks ch, ch + LPR, ...
+    const int sub = lane / C::LPR, ch = lane % C::LPR;
+    const int pg = ct / C::CHV, chv = lane % C::CHV;  // V-pass mapping
+    float qreg[RMAX][C::CPL * C::EPC];
     float acc[RMAX][C::EPC];
 #pragma unroll
     for (int t = 0; t < RMAX; ++t)
@@ -350,12 +359,16 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
       for (int t = 0; t < RMAX; ++t) {
         if (t < nr) {
           const int s_ = t / r;
-          const uint4 u = *reinterpret_cast<const uint4*>(
-              q + (obase + s_ * h + (t - s_ * r)) * DK + ch * C::EPC);
-          Elt<DT>::unpack(u, qreg[t]);
+          const DT* qrow = q + (obase + s_ * h + (t - s_ * r)) * DK;
+#pragma unroll
+          for (int c = 0; c < C::CPL; ++c) {
+            const uint4 u =
+                *reinterpret_cast<const uint4*>(qrow + (ch + c * C::LPR) * C::EPC);
+            Elt<DT>::unpack(u, &qreg[t][c * C::EPC]);
+          }
         } else {
 #pragma unroll
-          for (int e = 0; e < C::EPC; ++e) qreg[t][e] = 0.f;
+          for (int e = 0; e < C::CPL * C::EPC; ++e) qreg[t][e] = 0.f;
         }
       }
       for (int lt = seg.lt0; lt < seg.lt1; ++lt, ++n) {
@@ -396,26 +409,30 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
           named_bar_sync(1, kCompute);
         }
         // A: logits (query rows past nr have q = 0 and are not stored)
-        using RR = RowReduce<C::CHK, RMAX>;
+        using RR = RowReduce<C::LPR, RMAX>;
         const int hd = RR::head(lane);
         const bool wr = RR::writer(lane) && hd < nr;
 #pragma unroll
         for (int pb = cw * C::PPW; pb < C::T; pb += kWarps * C::PPW) {
           const int p = pb + sub;
-          float kf[C::EPC];
+          float kf[C::CPL * C::EPC];
           if (ok && p < valid) {
-            const uint4 u = *reinterpret_cast<const uint4*>(sK + p * DK + ch * C::EPC);
-            Elt<DT>::unpack(u, kf);
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) {
+              const uint4 u =
+                  *reinterpret_cast<const uint4*>(sK + p * DK + (ch + c * C::LPR) * C::EPC);
+              Elt<DT>::unpack(u, &kf[c * C::EPC]);
+            }
           } else {
 #pragma unroll
-            for (int e = 0; e < C::EPC; ++e) kf[e] = 0.f;
+            for (int e = 0; e < C::CPL * C::EPC; ++e) kf[e] = 0.f;
           }
           float part[RMAX];
 #pragma unroll
           for (int t = 0; t < RMAX; ++t) {
             part[t] = 0.f;
 #pragma unroll
-            for (int e = 0; e < C::EPC; ++e) part[t] = fmaf(qreg[t][e], kf[e], part[t]);
+            for (int e = 0; e < C::CPL * C::EPC; ++e) part[t] = fmaf(qreg[t][e], kf[e], part[t]);
           }
           RR::run(part, lane);
           if (wr && p < valid) sP[hd * C::T + p] = part[0] * scale_log2;
@@ -480,17 +497,29 @@ __global__ void __launch_bounds__(SimtCfg<DT, DK, DV, RMAX>::THREADS, 1)
               for (int e = 0; e < C::EPC; ++e) acc[t][e] *= al[t];
           }
         }
+        // positions in pairs (one 8-byte load of a row's two weights); the
+        // weight of a position past the valid rows is 0 (phase B), and its V
+        // row is taken as 0 rather than read
         if (ok) {
-          for (int p = pg; p < valid; p += C::NPG) {
-            float vf[C::EPC];
-            const uint4 u = *reinterpret_cast<const uint4*>(sV + p * DV + chv * C::EPC);
-            Elt<DT>::unpack(u, vf);
+          for (int p = 2 * pg; p < valid; p += 2 * C::NPG) {
+            float v0[C::EPC], v1[C::EPC];
+            Elt<DT>::unpack(*reinterpret_cast<const uint4*>(sV + p * DV + chv * C::EPC), v0);
+            if (p + 1 < valid) {
+              Elt<DT>::unpack(
+                  *reinterpret_cast<const uint4*>(sV + (p + 1) * DV + chv * C::EPC), v1);
+            } else {
+#pragma unroll
+              for (int e = 0; e < C::EPC; ++e) v1[e] = 0.f;
+            }
 #pragma unroll
             for (int t = 0; t < RMAX; ++t) {
               if (t < nr) {
-                const float wgt = sP[t * C::T + p];
+                const float2 wgt = *reinterpret_cast<const float2*>(sP + t * C::T + p);
 #pragma unroll
-                for (int e = 0; e < C::EPC; ++e) acc[t][e] = fmaf(wgt, vf[e], acc[t][e]);
+                for (int e = 0; e < C::EPC; ++e) {
+                  acc[t][e] = fmaf(wgt.x, v0[e], acc[t][e]);
+                  acc[t][e] = fmaf(wgt.y, v1[e], acc[t][e]);
+                }
               }
             }
           }
