@@ -84,13 +84,17 @@ struct Elt<__half> {
 // Seven compute warps: eight warps in all, two per SM sub-partition, so a
 // thread may hold up to 255 registers (measured: fifteen compute warps of
 // 128 registers were slower on the fp32 Llama-3-70B shape, 2.0 against 2.6
-// TB/s, their share of the weighted sum taking twice as long).  fp32 tiles
+// TB/s, their share of the weighted sum taking twice as long).  fp32 with
+// both head dims 128 and r <= 8 runs eight (two on each sub-partition
+// besides the copy warp; 224 registers a thread, no spills): a tile's 32
+// position pairs then take four steps of every warp instead of five of
+// the busiest.  fp32 tiles
 // hold 64 KiB of K + V in a three-stage ring (half the barriers and softmax
 // passes a position of 32 KiB tiles: the fp32 Llama-3-70B shape 848 -> 722
 // us per call), 16-bit ones 32 KiB in five stages.
 template <typename DT, int DK, int DV, int RMAX>
 struct SimtCfg {
-  static constexpr int NCW = 7;
+  static constexpr int NCW = (sizeof(DT) == 4 && RMAX <= 8 && DK == 128 && DV == 128) ? 8 : 7;
   static constexpr int NCT = 32 * NCW;          // compute threads
   static constexpr int THREADS = 32 + NCT;      // warp 0 copies
   static constexpr int ELT = Elt<DT>::size;
