@@ -53,18 +53,39 @@ def cfg_of(dtype, b, h, g, d, cap, seed=0, kind="plain"):
                         1.0 / math.sqrt(d), 100 + seed, kind=kind)
 
 
-# ---- CUDA-core kernel: fp32 (tile 64 at d=64, 32 at d=128); 16-bit data on
+# ---- CUDA-core kernel: fp32 (tile 128 at d=64, 64 at d=128); 16-bit data on
 # request (tile 128 at d=64)
 @pytest.mark.parametrize("b,h,g,d,cap,lens", [
     (1, 8, 1, 64, 256, [256]),                  # the fp32 MQA workload shape
     (2, 8, 2, 64, 200, [1, 200]),
     (3, 6, 3, 64, 130, [63, 64, 65]),
     (2, 16, 1, 64, 300, [129, 300]),            # r = 16
-    (2, 12, 4, 128, 100, [31, 33]),             # fp32 d=128, tile 32
+    (2, 12, 4, 128, 100, [31, 33]),             # fp32 d=128, one partial tile
     (4, 5, 5, 128, 97, [97, 1, 50, 32]),        # MHA
 ])
 def test_simt_fp32(b, h, g, d, cap, lens):
     run_step(cfg_of("f32", b, h, g, d, cap, seed=b + h), lens)
+
+
+# fp32 with d_k = d_v = 128 and at most 8 query rows per KV head: the launch
+# with eight compute warps (two chunks of a K row per lane, 16 lanes a row)
+@pytest.mark.parametrize("b,h,g,cap,lens", [
+    (3, 16, 2, 640, [640, 63, 129]),         # r = 8, tile edges (tile 64)
+    (2, 4, 4, 200, [200, 1]),                # r = 1
+    (1, 8, 1, 12000, [11999]),               # one unit over many CTAs: combine kernel
+    (24, 16, 4, 700, None),                  # units split across CTAs, merged in the kernel
+    (4, 64, 8, 4096, [4096, 3000, 17, 2049]),  # Llama-shaped heads, ragged
+])
+def test_simt_fp32_eight_warps(b, h, g, cap, lens):
+    if lens is None:
+        lens = np.random.default_rng(b + cap).integers(1, cap + 1, b).astype(np.int32)
+    run_step(cfg_of("f32", b, h, g, 128, cap, seed=b * 3 + g), lens)
+    run_step(cfg_of("f32", b, h, g, 128, cap, seed=b * 3 + g), lens, fused=True)
+
+
+def test_simt_fp32_eight_warps_nan_padding():
+    lens = [1, 63, 64, 65, 300]
+    run_step(cfg_of("f32", 5, 16, 2, 128, 320, seed=6), lens, pad_fill=float("nan"))
 
 
 @pytest.mark.parametrize("b,h,g,cap,lens", [

@@ -99,12 +99,14 @@ def test_tc_multi_nan_padding():
               pad_fill=float("nan"))
 
 
-# ---- CUDA-core kernel: fp32 (tile 64 at d = 64, 32 at d = 128); bf16 d = 64
+# ---- CUDA-core kernel: fp32 (tile 128 at d = 64, 64 at d = 128); bf16 d = 64
 # (tensor-core kernel)
 @pytest.mark.parametrize("dtype,b,n,h,g,d,cap,lens", [
-    ("f32", 3, 4, 8, 4, 64, 200, [4, 66, 200]),    # rows 62..65 straddle tiles
-    ("f32", 2, 3, 5, 1, 128, 100, [3, 34]),        # 15 rows, tile 32
-    ("f32", 1, 8, 2, 1, 64, 8192, [99 * 64 + 2]),  # combine kernel, unseen tile
+    ("f32", 3, 4, 8, 4, 64, 200, [4, 130, 200]),   # rows 126..129 straddle tiles
+    ("f32", 2, 2, 16, 4, 128, 300, [300, 65]),     # 8 rows, d = 128: eight compute warps
+    ("f32", 2, 4, 4, 2, 128, 200, [66, 130]),      # 8 rows; rows 62..65 straddle tiles
+    ("f32", 2, 3, 5, 1, 128, 100, [3, 34]),        # 15 rows: the 16-row launch
+    ("f32", 1, 8, 2, 1, 64, 12800, [99 * 128 + 2]),  # combine kernel, unseen tile
     ("f32", 96, 4, 2, 1, 64, 192, [130] * 96),     # in-kernel merge, unseen tiles
     ("bf16", 2, 4, 4, 2, 64, 300, [129, 300]),     # 8 rows
 ])

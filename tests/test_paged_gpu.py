@@ -86,7 +86,7 @@ def test_tc_paged_two_calls():
     run_paged(cfg_of("bf16", 3, 16, 4, 128, 640, seed=5), [640, 300, 17], 64, fused=False)
 
 
-# ---- CUDA-core kernel: fp32 (tile 64 at d = 64, 32 at d = 128); bf16 d = 64 on
+# ---- CUDA-core kernel: fp32 (tile 128 at d = 64, 64 at d = 128); bf16 d = 64 on
 # the tensor-core kernel
 @pytest.mark.parametrize("dtype,d,bs", [("f32", 64, 16), ("f32", 64, 64), ("f32", 64, 256),
                                         ("f32", 128, 16), ("bf16", 64, 32), ("bf16", 64, 128)])
