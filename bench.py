@@ -188,6 +188,21 @@ def profiled_traffic(kernel_src: str, workload: str, n: int = 1):
     return int(m_bytes.group(1))
 
 
+def copy_groups(nl: int):
+    """The end-to-end step's copy schedule over `nl` layers, as half-open
+    layer ranges: the inputs in three groups (the first layer, the next
+    three, the rest), the outputs in groups of max(8, ceil(nl / 10)) layers
+    with the last layer alone.  Each list covers 0..nl in order, without
+    gaps or overlaps."""
+    in_cuts = sorted({0, min(1, nl), min(4, nl), nl})
+    in_groups = list(zip(in_cuts[:-1], in_cuts[1:]))
+    og = max(8, -(-nl // 10))
+    out_ends = sorted({e for e in range(og - 1, nl - 1, og)} |
+                      {e for e in (nl - 2, nl - 1) if e >= 0})
+    out_groups = list(zip([0] + [e + 1 for e in out_ends[:-1]], [e + 1 for e in out_ends]))
+    return in_groups, out_groups
+
+
 def kernel_source_hash(kernel_src: str) -> str:
     """sha256 of the kernel's source followed by the device header it
     includes (gqa_device.cuh, next to it: the tile walker, the merge
@@ -873,13 +888,7 @@ def run_ours(args, rank, local_rank, world):
     host_out = torch.empty_like(out_all, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
-    nl = cfg.layers
-    in_cuts = sorted({0, min(1, nl), min(4, nl), nl})
-    in_groups = list(zip(in_cuts[:-1], in_cuts[1:]))
-    og = max(8, -(-nl // 10))
-    out_ends = sorted({e for e in range(og - 1, nl - 1, og)} |
-                      {e for e in (nl - 2, nl - 1) if e >= 0})
-    out_groups = list(zip([0] + [e + 1 for e in out_ends[:-1]], [e + 1 for e in out_ends]))
+    in_groups, out_groups = copy_groups(cfg.layers)
     side = torch.cuda.Stream(dev)
     ev_start = torch.cuda.Event()
     ev_in = [torch.cuda.Event() for _ in in_groups]

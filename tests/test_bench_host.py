@@ -110,3 +110,20 @@ def test_oracle_sample_uses_every_core():
     # every worker ran whole units: bytes are a multiple of one unit's bytes
     one = (256 * cfg.g + cfg.h) * (cfg.d + cfg.dv) * cfg.elt
     assert nbytes % one == 0 and nbytes // one == units // cfg.g
+
+
+@pytest.mark.parametrize("nl", [1, 2, 3, 4, 5, 8, 9, 28, 80, 81, 4011])
+def test_copy_groups_cover_every_layer(nl):
+    """The end-to-end copy schedule: both lists tile 0..nl in order; the
+    inputs take at most three groups, the first layer's alone; the outputs
+    at most about ten plus the last layer alone."""
+    ins, outs = bench.copy_groups(nl)
+    for groups in (ins, outs):
+        assert groups[0][0] == 0 and groups[-1][1] == nl
+        assert all(a < z for a, z in groups)
+        assert all(groups[i][1] == groups[i + 1][0] for i in range(len(groups) - 1))
+    assert ins[0] == (0, 1) and len(ins) <= 3
+    assert outs[-1] == (nl - 1, nl) and len(outs) <= 12
+    if nl == 80:
+        assert ins == [(0, 1), (1, 4), (4, 80)]
+        assert len(outs) == 11 and outs[0] == (0, 8) and outs[-2] == (72, 79)
