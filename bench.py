@@ -1166,7 +1166,7 @@ def main(argv=None):
     ap.add_argument("--ncu-summary", choices=sorted(NCU_KERNELS), default=None,
                     help="profile one launch of this kernel on a small case of the workload "
                          "(ncu, clocks untouched) and write its summary and launch list")
-    ap.add_argument("--ncu-out", default="gpurun_out",
+    ap.add_argument("--ncu-out", default="ncu_reports",
                     help="--ncu-summary: folder for the raw reports and the summaries")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip timing the other workloads after the headline one")
