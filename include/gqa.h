@@ -69,7 +69,7 @@ extern "C" {
                                    sizes whose index range exceeds int32 */
 #define GQA_ERR_DTYPE       -3  /* dtype is not GQA_F32, GQA_BF16 or GQA_F16 */
 #define GQA_ERR_ALIGN       -4  /* a tensor pointer is not 16-byte aligned */
-#define GQA_ERR_UNSUPPORTED -5  /* a shape this build has no kernel for
+#define GQA_ERR_UNSUPPORTED -5  /* a shape the library has no kernel for
                                    (a head dim outside the supported set, too
                                    many query heads per KV head, b > 65535) */
 #define GQA_ERR_CUDA        -6  /* a CUDA runtime call failed */
